@@ -1,0 +1,219 @@
+/*
+ * f64 CPU checker for the affine group-wise quantized matmul.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  The CUDA library never
+ * links it, includes it or calls it, and it shares no source with it.
+ *
+ * What it computes (mlxcel issue #1536, Baseline section: "affine 4-bit /
+ * group 64" weights; PR #1562, What changed: "gather_mm against an f64 dense
+ * per-expert reference"; issue #1538, 4-bit vs 8-bit section: dequantise,
+ * then accumulate in float at every width):
+ *
+ *   q[n,k]   = code of weight (n, k), unpacked from the uint32 words
+ *   w^[n,k]  = s[n, k/G] * q[n,k] + b[n, k/G]                (in f64)
+ *   y[m,n]   = sum_k x[m,k] * w^[n,k]                        (in f64)
+ *   bnd[m,n] = sum_k |x[m,k] * w^[n,k]|
+ *
+ * Packing: 4-bit codes eight per little-endian uint32, the lowest k in the
+ * lowest nibble; 8-bit codes ("unsigned char weights", issue #1538, 4-bit vs
+ * 8-bit section) four per uint32, the lowest k in the lowest byte.
+ *
+ * The sorted-MoE variant (PR #1562, Summary: rows sorted by expert, B =
+ * tokens * top_k) uses for sorted row r the expert e(r) and activation row
+ * src(r).
+ *
+ * Plain loops, no blocking or reordering beyond the definition: a reader can
+ * check each line against the formulas above.  Every function is pinned by
+ * the CPU tests (hand-packed words, closed forms, exact brute force, the
+ * constant-per-expert case).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* bf16 -> double: the bf16 pattern is the upper half of an IEEE binary32. */
+static double bf16_to_f64(uint16_t h) {
+    uint32_t u = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Code of weight (n, k): row n has K*bits/32 words. */
+static unsigned code_at(const uint32_t* w, long long words_per_row, int n, int k, int bits) {
+    int per_word = 32 / bits;
+    uint32_t word = w[(long long)n * words_per_row + k / per_word];
+    int slot = k % per_word;
+    uint32_t mask = (bits == 32) ? 0xFFFFFFFFu : ((1u << bits) - 1u);
+    return (unsigned)((word >> (slot * bits)) & mask);
+}
+
+int oracle_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* Unpack every code of an [N, K] matrix into q (uint8 [N, K]). */
+void oracle_unpack(const uint32_t* w, int N, int K, int bits, uint8_t* q) {
+    long long wpr = (long long)K * bits / 32;
+    for (int n = 0; n < N; ++n)
+        for (int k = 0; k < K; ++k)
+            q[(long long)n * K + k] = (uint8_t)code_at(w, wpr, n, k, bits);
+}
+
+/* Dense f64 dequantised weights w^[N, K]. */
+void oracle_dequant(const uint32_t* w, const uint16_t* scales, const uint16_t* biases,
+                    int N, int K, int bits, int group, double* what) {
+    long long wpr = (long long)K * bits / 32;
+    int ng = K / group;
+    for (int n = 0; n < N; ++n)
+        for (int k = 0; k < K; ++k) {
+            double s = bf16_to_f64(scales[(long long)n * ng + k / group]);
+            double b = bf16_to_f64(biases[(long long)n * ng + k / group]);
+            what[(long long)n * K + k] = s * (double)code_at(w, wpr, n, k, bits) + b;
+        }
+}
+
+/* One output row n for the activation rows listed: dequantise row n of one
+ * expert's matrix into a scratch row, then take the f64 dot products. */
+static void row_dot(const uint16_t* x, const uint32_t* w, const uint16_t* scales,
+                    const uint16_t* biases, int K, int bits, int group, int n,
+                    const int* xrows, int nrows, double* wrow,
+                    double* y_out, double* bnd_out, long long ystride) {
+    long long wpr = (long long)K * bits / 32;
+    int ng = K / group;
+    for (int k = 0; k < K; ++k) {
+        double s = bf16_to_f64(scales[(long long)n * ng + k / group]);
+        double b = bf16_to_f64(biases[(long long)n * ng + k / group]);
+        wrow[k] = s * (double)code_at(w, wpr, n, k, bits) + b;
+    }
+    for (int i = 0; i < nrows; ++i) {
+        const uint16_t* xr = x + (long long)xrows[i] * K;
+        double acc = 0.0, bnd = 0.0;
+        for (int k = 0; k < K; ++k) {
+            double t = bf16_to_f64(xr[k]) * wrow[k];
+            acc += t;
+            bnd += fabs(t);
+        }
+        y_out[(long long)i * ystride] = acc;
+        if (bnd_out) bnd_out[(long long)i * ystride] = bnd;
+    }
+}
+
+/* y[M, N] = x[M, K] . w^[N, K]^T in f64; bound likewise (may be NULL). */
+int oracle_qmm(const uint16_t* x, const uint32_t* w, const uint16_t* scales,
+               const uint16_t* biases, int M, int K, int N, int bits, int group,
+               double* y, double* bound) {
+    int* rows = (int*)malloc(sizeof(int) * (M > 0 ? M : 1));
+    if (!rows) return 1;
+    for (int m = 0; m < M; ++m) rows[m] = m;
+    int fail = 0;
+#pragma omp parallel
+    {
+        double* wrow = (double*)malloc(sizeof(double) * (K > 0 ? K : 1));
+        if (!wrow) {
+#pragma omp atomic write
+            fail = 1;
+        } else {
+#pragma omp for schedule(dynamic, 4)
+            for (int n = 0; n < N; ++n)
+                row_dot(x, w, scales, biases, K, bits, group, n, rows, M, wrow,
+                        y + n, bound ? bound + n : NULL, N);
+            free(wrow);
+        }
+    }
+    free(rows);
+    return fail;
+}
+
+/* qmv is qmm with one activation row. */
+int oracle_qmv(const uint16_t* x, const uint32_t* w, const uint16_t* scales,
+               const uint16_t* biases, int K, int N, int bits, int group,
+               double* y, double* bound) {
+    return oracle_qmm(x, w, scales, biases, 1, K, N, bits, group, y, bound);
+}
+
+/* Sorted-MoE variant: y[B, N]; row r uses expert expert_ids[r] and activation
+ * row row_src[r] (row_src NULL means row r).  w is [E, N, K*bits/32],
+ * scales/biases [E, N, K/G].  Rows whose expert id is out of [0, E) get 0. */
+int oracle_gather_qmm(const uint16_t* x, const uint32_t* w, const uint16_t* scales,
+                      const uint16_t* biases, const int32_t* expert_ids,
+                      const int32_t* row_src, int T, int B, int E, int K, int N,
+                      int bits, int group, double* y, double* bound) {
+    (void)T;
+    long long wmat = (long long)N * K * bits / 32;
+    long long smat = (long long)N * (K / group);
+    int fail = 0;
+#pragma omp parallel
+    {
+        double* wrow = (double*)malloc(sizeof(double) * (K > 0 ? K : 1));
+        if (!wrow) {
+#pragma omp atomic write
+            fail = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int r = 0; r < B; ++r) {
+                int e = expert_ids[r];
+                int src = row_src ? row_src[r] : r;
+                for (int n = 0; n < N; ++n) {
+                    if (e < 0 || e >= E) {
+                        y[(long long)r * N + n] = 0.0;
+                        if (bound) bound[(long long)r * N + n] = 0.0;
+                        continue;
+                    }
+                    row_dot(x, w + e * wmat, scales + e * smat, biases + e * smat, K, bits,
+                            group, n, &src, 1, wrow, y + (long long)r * N + n,
+                            bound ? bound + (long long)r * N + n : NULL, 1);
+                }
+            }
+            free(wrow);
+        }
+    }
+    return fail;
+}
+
+/* Selected outputs of the sorted-MoE variant (or of qmm with E = 1 and
+ * expert_ids NULL): for each i, output (rows[i], cols[i]).  Used to check
+ * full-size launches element by element on a sample. */
+int oracle_points(const uint16_t* x, const uint32_t* w, const uint16_t* scales,
+                  const uint16_t* biases, const int32_t* expert_ids,
+                  const int32_t* row_src, int E, int K, int N, int bits, int group,
+                  const int64_t* rows, const int64_t* cols, long long count,
+                  double* y, double* bound) {
+    long long wmat = (long long)N * K * bits / 32;
+    long long smat = (long long)N * (K / group);
+    int fail = 0;
+#pragma omp parallel
+    {
+        double* wrow = (double*)malloc(sizeof(double) * (K > 0 ? K : 1));
+        if (!wrow) {
+#pragma omp atomic write
+            fail = 1;
+        } else {
+#pragma omp for schedule(dynamic, 8)
+            for (long long i = 0; i < count; ++i) {
+                int r = (int)rows[i];
+                int n = (int)cols[i];
+                int e = expert_ids ? expert_ids[r] : 0;
+                int src = row_src ? row_src[r] : r;
+                if (e < 0 || e >= E) {
+                    y[i] = 0.0;
+                    if (bound) bound[i] = 0.0;
+                    continue;
+                }
+                row_dot(x, w + e * wmat, scales + e * smat, biases + e * smat, K, bits,
+                        group, n, &src, 1, wrow, y + i, bound ? bound + i : NULL, 1);
+            }
+            free(wrow);
+        }
+    }
+    return fail;
+}
