@@ -1,0 +1,267 @@
+"""affine_bit_matmul_gb300 — affine group-wise quantized matmul on GB300.
+
+A thin Python binding over the C ABI of ``libmxq.so`` (declared in
+``include/mxq.h``).  Every step of the computation runs in the library's
+sm_103a kernels; this module only checks tensors, passes their device
+pointers and the current CUDA stream, and turns status codes into
+exceptions.  There is no fallback: if the library is missing or the device
+is not sm_103a, the calls raise.
+
+Storage conventions (mlxcel issue #1536, Baseline section: "affine 4-bit /
+group 64"):
+
+* ``x``: bf16 ``[M, K]`` (``[K]`` for ``qmv``);
+* ``w``: int32 or uint32 ``[N, K*bits/32]`` packed codes, 4-bit codes eight per
+  little-endian word (lowest k in the lowest nibble), 8-bit codes four per word;
+* ``scales``, ``biases``: bf16 ``[N, K/64]``;
+* result ``y``: bf16 ``[M, N]``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "lib",
+    "qmv",
+    "qmm",
+    "gather_qmm",
+    "qmm_workspace_bytes",
+    "gather_workspace_bytes",
+    "MxqError",
+    "DEV_BAD_EXPERT_ID",
+    "DEV_UNSORTED_IDS",
+    "DEV_BAD_ROW_SRC",
+    "DEV_TIMEOUT",
+    "EXPORTED_SYMBOLS",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmxq.so")
+
+MXQ_OK = 0
+STATUS_NAMES = {
+    0: "MXQ_OK",
+    1: "MXQ_ERR_INVALID_ARG",
+    2: "MXQ_ERR_MISALIGNED",
+    3: "MXQ_ERR_UNSUPPORTED",
+    4: "MXQ_ERR_ARCH",
+    5: "MXQ_ERR_CUDA",
+    6: "MXQ_ERR_WORKSPACE",
+}
+DEV_BAD_EXPERT_ID = 0x1
+DEV_UNSORTED_IDS = 0x2
+DEV_BAD_ROW_SRC = 0x4
+DEV_TIMEOUT = 0x8
+
+EXPORTED_SYMBOLS = (
+    "mxq_qmv",
+    "mxq_qmm",
+    "mxq_qmm_workspace_bytes",
+    "mxq_gather_qmm",
+    "mxq_gather_workspace_bytes",
+    "mxq_status_string",
+    "mxq_version",
+)
+
+
+class MxqError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__("%s: %s (%s)" % (what, STATUS_NAMES.get(status, status),
+                                           _status_string(status)))
+
+
+_lib_handle = None
+
+
+def lib():
+    """The loaded ``libmxq.so`` with argument types set (raises if absent)."""
+    global _lib_handle
+    if _lib_handle is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                "libmxq.so is not built; run affine_bit_matmul_gb300.build.build() "
+                "(needs nvcc) before using the library")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        L.mxq_qmv.argtypes = [P, P, P, P, P, I, I, I, I, P]
+        L.mxq_qmv.restype = I
+        L.mxq_qmm.argtypes = [P, P, P, P, P, I, I, I, I, I, P, Z, P, P]
+        L.mxq_qmm.restype = I
+        L.mxq_qmm_workspace_bytes.argtypes = [I, I, I, I]
+        L.mxq_qmm_workspace_bytes.restype = Z
+        L.mxq_gather_qmm.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, Z, P, P]
+        L.mxq_gather_qmm.restype = I
+        L.mxq_gather_workspace_bytes.argtypes = [I, I, I]
+        L.mxq_gather_workspace_bytes.restype = Z
+        L.mxq_status_string.argtypes = [I]
+        L.mxq_status_string.restype = ctypes.c_char_p
+        L.mxq_version.restype = I
+        _lib_handle = L
+    return _lib_handle
+
+
+def _status_string(status: int) -> str:
+    try:
+        return lib().mxq_status_string(status).decode()
+    except Exception:  # library not loadable: name only
+        return STATUS_NAMES.get(status, "unknown")
+
+
+def _check(status: int, what: str):
+    if status != MXQ_OK:
+        raise MxqError(status, what)
+
+
+# ---------------------------------------------------------------- torch level
+
+def _torch():
+    import torch
+
+    return torch
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _stream(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _require(t, name, dtypes, device=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype not in dtypes:
+        raise TypeError("%s has dtype %s, expected one of %s" % (name, t.dtype, dtypes))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if device is not None and t.device != device:
+        raise ValueError("%s is on %s, expected %s" % (name, t.device, device))
+
+
+def _code_dtypes():
+    torch = _torch()
+    out = [torch.int32]
+    if hasattr(torch, "uint32"):
+        out.append(torch.uint32)
+    return tuple(out)
+
+
+def _check_weights(w, scales, biases, N, K, bits, device, lead=()):
+    torch = _torch()
+    _require(w, "w", _code_dtypes(), device)
+    _require(scales, "scales", (torch.bfloat16,), device)
+    _require(biases, "biases", (torch.bfloat16,), device)
+    if tuple(w.shape) != tuple(lead) + (N, K * bits // 32):
+        raise ValueError("w has shape %s, expected %s" % (tuple(w.shape), tuple(lead) + (N, K * bits // 32)))
+    for t, name in ((scales, "scales"), (biases, "biases")):
+        if tuple(t.shape) != tuple(lead) + (N, K // 64):
+            raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(lead) + (N, K // 64)))
+
+
+def qmv(x, w, scales, biases, bits: int, out=None, stream=None):
+    """Decode GEMV: ``y[N] = sum_k x[k] * (s*q + b)[n, k]`` (``x`` bf16 [K])."""
+    torch = _torch()
+    _require(x, "x", (torch.bfloat16,))
+    if x.dim() != 1:
+        raise ValueError("x must be 1-D [K]")
+    K = x.shape[0]
+    N = w.shape[0]
+    _check_weights(w, scales, biases, N, K, bits, x.device)
+    if out is None:
+        out = torch.empty((N,), dtype=torch.bfloat16, device=x.device)
+    _require(out, "out", (torch.bfloat16,), x.device)
+    _check(lib().mxq_qmv(_ptr(x), _ptr(w), _ptr(scales), _ptr(biases), _ptr(out), K, N, bits, 64,
+                         _stream(stream)), "mxq_qmv")
+    return out
+
+
+def qmm_workspace_bytes(M: int, K: int, N: int, bits: int) -> int:
+    return int(lib().mxq_qmm_workspace_bytes(M, K, N, bits))
+
+
+def qmm(x, w, scales, biases, bits: int, out=None, workspace=None, dev_status=None,
+        stream=None):
+    """Prefill GEMM on the tensor cores: ``y[M, N] = x[M, K] . w^[N, K]^T``.
+
+    ``workspace`` (a CUDA uint8 tensor) lets the call split K across CTAs
+    when M and N give few tiles; ``"auto"`` allocates one of the size the
+    library asks for.  ``dev_status`` (CUDA int32 [1]) receives DEV_TIMEOUT
+    if a pipeline wait gave up.
+    """
+    torch = _torch()
+    _require(x, "x", (torch.bfloat16,))
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D [M, K]")
+    M, K = x.shape
+    N = w.shape[0]
+    _check_weights(w, scales, biases, N, K, bits, x.device)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _require(out, "out", (torch.bfloat16,), x.device)
+    if isinstance(workspace, str) and workspace == "auto":
+        nbytes = qmm_workspace_bytes(M, K, N, bits)
+        workspace = torch.empty((max(nbytes, 1),), dtype=torch.uint8, device=x.device)
+    ws_bytes = 0
+    if workspace is not None:
+        _require(workspace, "workspace", (torch.uint8,), x.device)
+        ws_bytes = workspace.numel()
+    if dev_status is not None:
+        _require(dev_status, "dev_status", (torch.int32,), x.device)
+    _check(lib().mxq_qmm(_ptr(x), _ptr(w), _ptr(scales), _ptr(biases), _ptr(out), M, K, N, bits,
+                         64, _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream)),
+           "mxq_qmm")
+    return out
+
+
+def gather_workspace_bytes(B: int, E: int, N: int) -> int:
+    return int(lib().mxq_gather_workspace_bytes(B, E, N))
+
+
+def gather_qmm(x, w, scales, biases, expert_ids, row_src, bits: int, out=None, workspace=None,
+               dev_status=None, stream=None):
+    """Sorted mixture-of-experts GEMM: sorted row r multiplies expert
+    ``expert_ids[r]``'s dequantised matrix by ``x[row_src[r]]``.
+
+    ``w`` is [E, N, K*bits/32], ``scales``/``biases`` [E, N, K/64],
+    ``expert_ids`` int32 [B] non-decreasing, ``row_src`` int32 [B] or None
+    (identity).  Returns y bf16 [B, N] in sorted row order.
+    """
+    torch = _torch()
+    _require(x, "x", (torch.bfloat16,))
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D [T, K]")
+    T, K = x.shape
+    if w.dim() != 3:
+        raise ValueError("w must be 3-D [E, N, K*bits/32]")
+    E, N = w.shape[0], w.shape[1]
+    _check_weights(w, scales, biases, N, K, bits, x.device, lead=(E,))
+    _require(expert_ids, "expert_ids", (torch.int32,), x.device)
+    B = expert_ids.numel()
+    if row_src is not None:
+        _require(row_src, "row_src", (torch.int32,), x.device)
+        if row_src.numel() != B:
+            raise ValueError("row_src must have B entries")
+    if out is None:
+        out = torch.empty((B, N), dtype=torch.bfloat16, device=x.device)
+    _require(out, "out", (torch.bfloat16,), x.device)
+    if workspace is None:
+        workspace = torch.empty((gather_workspace_bytes(B, E, N),), dtype=torch.uint8,
+                                device=x.device)
+    _require(workspace, "workspace", (torch.uint8,), x.device)
+    if dev_status is not None:
+        _require(dev_status, "dev_status", (torch.int32,), x.device)
+    _check(lib().mxq_gather_qmm(_ptr(x), _ptr(w), _ptr(scales), _ptr(biases), _ptr(expert_ids),
+                                _ptr(row_src), _ptr(out), T, B, E, K, N, bits, 64,
+                                _ptr(workspace), workspace.numel(), _ptr(dev_status),
+                                _stream(stream)), "mxq_gather_qmm")
+    return out

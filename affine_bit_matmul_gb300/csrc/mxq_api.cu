@@ -1,0 +1,237 @@
+// C ABI of the library: argument checks, tile and split planning, launches.
+#include <cstdint>
+#include <cstring>
+#include <cuda_runtime.h>
+
+#include "../../include/mxq.h"
+#include "mxq_internal.h"
+
+namespace {
+
+constexpr int kTileN = 128;           // rows of w per CTA in the tensor-core kernel
+constexpr int kMaxRowsPerTile = 256;  // MMA N limit
+constexpr int kGatherRowsPerTile = 128;
+constexpr int kMinKBlocksPerSplit = 8;
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    int checked;  // 0 = not yet, 1 = ok, -1 = wrong arch
+    int sms;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+mxq_status check_device(int* sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MXQ_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return MXQ_ERR_UNSUPPORTED;
+    DeviceInfo& d = g_dev[dev];
+    if (d.checked == 0) {
+        int major = 0, minor = 0, count = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return MXQ_ERR_CUDA;
+        d.sms = count;
+        d.checked = (major == 10 && minor == 3) ? 1 : -1;
+    }
+    if (d.checked < 0) return MXQ_ERR_ARCH;
+    if (sms) *sms = d.sms;
+    return MXQ_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+mxq_status check_common(int K, int N, int bits, int group_size) {
+    if (bits != 4 && bits != 8) return MXQ_ERR_INVALID_ARG;
+    if (group_size != 64) return MXQ_ERR_INVALID_ARG;
+    if (K <= 0 || N <= 0 || K % 64 != 0) return MXQ_ERR_INVALID_ARG;
+    return MXQ_OK;
+}
+
+// Dense GEMM plan: M tiles of equal size (multiple of 16, at most 256) and,
+// when M and N give fewer tiles than SMs, a split of K.
+struct DensePlan {
+    int m_tiles, m_tile, tmem_cols, splits, kb_per_split;
+    size_t partial_bytes, counter_bytes;
+};
+
+DensePlan plan_dense(int M, int K, int N, int sms) {
+    DensePlan pl;
+    const int want_tiles = (M + kMaxRowsPerTile - 1) / kMaxRowsPerTile;
+    const int per = (M + want_tiles - 1) / want_tiles;
+    pl.m_tile = (per + 15) & ~15;                      // <= 256
+    pl.m_tiles = (M + pl.m_tile - 1) / pl.m_tile;      // every tile has >= 1 row
+    int cols = 32;
+    while (cols < pl.m_tile) cols <<= 1;
+    pl.tmem_cols = cols;
+    const int n_tiles = (N + kTileN - 1) / kTileN;
+    const int tiles = n_tiles * pl.m_tiles;
+    const int KB = K / 64;
+    int splits = 1;
+    if (tiles < sms) {
+        splits = sms / tiles;
+        const int max_by_k = KB / kMinKBlocksPerSplit;
+        if (splits > max_by_k) splits = max_by_k;
+        if (splits < 1) splits = 1;
+    }
+    pl.kb_per_split = (KB + splits - 1) / splits;
+    pl.splits = (KB + pl.kb_per_split - 1) / pl.kb_per_split;  // every split gets >= 1 block
+    pl.partial_bytes = pl.splits > 1 ? (size_t)tiles * pl.splits * pl.m_tile * kTileN * 4 : 0;
+    pl.counter_bytes = pl.splits > 1 ? align_up((size_t)tiles * 4, 256) : 0;
+    return pl;
+}
+
+size_t gather_max_tiles(int B, int E) { return (size_t)B / kGatherRowsPerTile + (size_t)E + 1; }
+
+}  // namespace
+
+extern "C" {
+
+const char* mxq_status_string(mxq_status s) {
+    switch (s) {
+        case MXQ_OK: return "ok";
+        case MXQ_ERR_INVALID_ARG: return "invalid argument";
+        case MXQ_ERR_MISALIGNED: return "misaligned pointer";
+        case MXQ_ERR_UNSUPPORTED: return "unsupported";
+        case MXQ_ERR_ARCH: return "device is not compute capability 10.3 (sm_103a)";
+        case MXQ_ERR_CUDA: return "CUDA error";
+        case MXQ_ERR_WORKSPACE: return "workspace missing or too small";
+    }
+    return "unknown status";
+}
+
+int mxq_version(void) { return 100; }
+
+mxq_status mxq_qmv(const void* x, const uint32_t* w, const void* scales, const void* biases,
+                   void* y, int K, int N, int bits, int group_size, void* stream) {
+    mxq_status st = check_common(K, N, bits, group_size);
+    if (st != MXQ_OK) return st;
+    if (!x || !w || !scales || !biases || !y) return MXQ_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 16) || !aligned(scales, 2) ||
+        !aligned(biases, 2))
+        return MXQ_ERR_MISALIGNED;
+    st = check_device(nullptr);
+    if (st != MXQ_OK) return st;
+    cudaError_t err = mxq::launch_qmv(x, w, scales, biases, y, K, N, bits,
+                                      static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA;
+}
+
+size_t mxq_qmm_workspace_bytes(int M, int K, int N, int bits) {
+    if (check_common(K, N, bits, 64) != MXQ_OK || M <= 0) return 0;
+    int sms = 0;
+    if (check_device(&sms) != MXQ_OK) return 0;
+    const DensePlan pl = plan_dense(M, K, N, sms);
+    return pl.partial_bytes + pl.counter_bytes;
+}
+
+mxq_status mxq_qmm(const void* x, const uint32_t* w, const void* scales, const void* biases,
+                   void* y, int M, int K, int N, int bits, int group_size, void* workspace,
+                   size_t workspace_bytes, int32_t* dev_status, void* stream) {
+    mxq_status st = check_common(K, N, bits, group_size);
+    if (st != MXQ_OK) return st;
+    if (M <= 0) return MXQ_ERR_INVALID_ARG;
+    if (!x || !w || !scales || !biases || !y) return MXQ_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 16) || !aligned(scales, 2) ||
+        !aligned(biases, 2) || !aligned(dev_status, 4) || !aligned(workspace, 256))
+        return MXQ_ERR_MISALIGNED;
+    int sms = 0;
+    st = check_device(&sms);
+    if (st != MXQ_OK) return st;
+    DensePlan pl = plan_dense(M, K, N, sms);
+    if (pl.m_tiles > 65535) return MXQ_ERR_UNSUPPORTED;  // grid.y limit
+    const size_t need = pl.partial_bytes + pl.counter_bytes;
+    if (pl.splits > 1 && (!workspace || workspace_bytes < need)) {
+        pl.splits = 1;  // no room to split K: one CTA per tile
+        pl.kb_per_split = K / 64;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dev_status && cudaMemsetAsync(dev_status, 0, sizeof(int32_t), s) != cudaSuccess)
+        return MXQ_ERR_CUDA;
+    mxq::QmmParams p;
+    std::memset(&p, 0, sizeof p);
+    p.x = x;
+    p.w = w;
+    p.scales = static_cast<const uint16_t*>(scales);
+    p.biases = static_cast<const uint16_t*>(biases);
+    p.y = y;
+    p.status = dev_status;
+    p.M = M;
+    p.T = M;
+    p.K = K;
+    p.N = N;
+    p.m_tile = pl.m_tile;
+    p.tmem_cols = pl.tmem_cols;
+    p.splits = pl.splits;
+    p.kb_per_split = pl.kb_per_split;
+    if (pl.splits > 1) {
+        p.partial = static_cast<float*>(workspace);
+        p.counters = reinterpret_cast<int*>(static_cast<char*>(workspace) + pl.partial_bytes);
+        if (cudaMemsetAsync(p.counters, 0, pl.counter_bytes, s) != cudaSuccess) return MXQ_ERR_CUDA;
+    }
+    cudaError_t err = mxq::launch_qmm_tc(p, bits, pl.m_tiles, pl.m_tile, s);
+    return err == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA;
+}
+
+size_t mxq_gather_workspace_bytes(int B, int E, int N) {
+    (void)N;
+    if (B <= 0 || E <= 0) return 0;
+    return align_up(gather_max_tiles(B, E) * sizeof(mxq::MTile), 256) + 256;
+}
+
+mxq_status mxq_gather_qmm(const void* x, const uint32_t* w, const void* scales,
+                          const void* biases, const int32_t* expert_ids, const int32_t* row_src,
+                          void* y, int T, int B, int E, int K, int N, int bits, int group_size,
+                          void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                          void* stream) {
+    mxq_status st = check_common(K, N, bits, group_size);
+    if (st != MXQ_OK) return st;
+    if (T <= 0 || B <= 0 || E <= 0) return MXQ_ERR_INVALID_ARG;
+    if (!row_src && T != B) return MXQ_ERR_INVALID_ARG;
+    if (!x || !w || !scales || !biases || !expert_ids || !y) return MXQ_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 16) || !aligned(scales, 2) ||
+        !aligned(biases, 2) || !aligned(expert_ids, 4) || !aligned(row_src, 4) ||
+        !aligned(dev_status, 4) || !aligned(workspace, 256))
+        return MXQ_ERR_MISALIGNED;
+    if (!workspace || workspace_bytes < mxq_gather_workspace_bytes(B, E, N))
+        return MXQ_ERR_WORKSPACE;
+    const size_t max_tiles = gather_max_tiles(B, E);
+    if (max_tiles > 65535) return MXQ_ERR_UNSUPPORTED;  // grid.y limit
+    st = check_device(nullptr);
+    if (st != MXQ_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    auto* tiles = static_cast<mxq::MTile*>(workspace);
+    int* tile_count = reinterpret_cast<int*>(static_cast<char*>(workspace) +
+                                             align_up(max_tiles * sizeof(mxq::MTile), 256));
+    cudaError_t err = mxq::launch_gather_prepass(expert_ids, row_src, T, B, E, N,
+                                                 kGatherRowsPerTile, tiles, tile_count, y,
+                                                 dev_status, s);
+    if (err != cudaSuccess) return MXQ_ERR_CUDA;
+    mxq::QmmParams p;
+    std::memset(&p, 0, sizeof p);
+    p.x = x;
+    p.w = w;
+    p.scales = static_cast<const uint16_t*>(scales);
+    p.biases = static_cast<const uint16_t*>(biases);
+    p.y = y;
+    p.row_src = row_src;
+    p.tiles = tiles;
+    p.tile_count = tile_count;
+    p.status = dev_status;
+    p.M = B;
+    p.T = T;
+    p.K = K;
+    p.N = N;
+    p.m_tile = kGatherRowsPerTile;
+    p.tmem_cols = kGatherRowsPerTile;
+    p.splits = 1;
+    p.kb_per_split = K / 64;
+    p.w_expert_stride = (long long)N * K * bits / 32;
+    p.sb_expert_stride = (long long)N * (K / 64);
+    err = mxq::launch_qmm_tc(p, bits, (int)max_tiles, kGatherRowsPerTile, s);
+    return err == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,58 @@
+// Host-side declarations shared by the translation units of the library.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mxq {
+
+// One tile of output rows of the grouped (sorted mixture-of-experts) GEMM:
+// rows [row_start, row_start + rows) of the sorted order, all of expert e.
+struct MTile {
+    int e;
+    int row_start;
+    int rows;
+    int pad;
+};
+
+// Arguments of the tcgen05 GEMM kernel (dense and grouped forms).
+struct QmmParams {
+    const void* x;           // bf16 [T or M, K]
+    const uint32_t* w;       // uint32 [E, N, K*bits/32]
+    const uint16_t* scales;  // bf16 [E, N, K/64]
+    const uint16_t* biases;  // bf16 [E, N, K/64]
+    void* y;                 // bf16 [rows, N]
+    const int32_t* row_src;  // grouped form: x row of each sorted row, or null
+    const MTile* tiles;      // grouped form: tile list, or null (dense form)
+    const int* tile_count;   // grouped form: number of valid tiles
+    int32_t* status;         // MXQ_DEV_* bits, or null
+    float* partial;          // split-K partial sums, or null
+    int* counters;           // split-K arrival counters, or null
+    int M;                   // dense form: rows of x and y
+    int T;                   // grouped form: rows of x
+    int K, N;
+    int m_tile;              // dense form: rows per M tile (multiple of 16)
+    int tmem_cols;           // tensor-memory columns allocated per CTA
+    int splits;              // K splits (1 = none)
+    int kb_per_split;        // 64-wide K blocks per split
+    long long w_expert_stride;   // words between experts
+    long long sb_expert_stride;  // scale/bias entries between experts
+};
+
+cudaError_t launch_qmv(const void* x, const uint32_t* w, const void* scales, const void* biases,
+                       void* y, int K, int N, int bits, cudaStream_t stream);
+
+// Dense or grouped tcgen05 GEMM; grid.y = number of M tiles (dense) or an
+// upper bound on the number of tiles (grouped).
+cudaError_t launch_qmm_tc(const QmmParams& p, int bits, int grid_m, int max_rows_per_tile,
+                          cudaStream_t stream);
+
+// Grouped form, step 1: validate ids, find each expert's rows, build the
+// tile list, zero the y rows that no tile covers.
+cudaError_t launch_gather_prepass(const int32_t* expert_ids, const int32_t* row_src, int T,
+                                  int B, int E, int N, int rows_per_tile, MTile* tiles,
+                                  int* tile_count, void* y, int32_t* status,
+                                  cudaStream_t stream);
+
+}  // namespace mxq

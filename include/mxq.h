@@ -1,0 +1,127 @@
+/*
+ * mxq — affine group-wise quantized matrix multiply for sm_103a (GB300).
+ *
+ * The operation (mlxcel issue #1536, Baseline section: weights stored as
+ * "affine 4-bit / group 64", activations bf16; issue #1538, 4-bit vs 8-bit
+ * section: 8-bit codes are unsigned bytes, and the product accumulates in
+ * float at every width):
+ *
+ *   w^[n, k] = s[n, k/64] * q[n, k] + b[n, k/64]
+ *   y[m, n]  = sum_k x[m, k] * w^[n, k]          (fp32 accumulation)
+ *
+ * Storage, all row-major and contiguous:
+ *   x       bf16   [M, K]            activations
+ *   w       uint32 [N, K*bits/32]    packed codes.  4-bit: eight codes per
+ *                                    little-endian word, lowest k in the
+ *                                    lowest nibble (integer_subbyte<4>, the
+ *                                    qmm_naive kernel name in issue #1536's
+ *                                    profile table).  8-bit: four codes per
+ *                                    word, lowest k in the lowest byte.
+ *   scales  bf16   [N, K/64]         s per (output row, group of 64 k)
+ *   biases  bf16   [N, K/64]         b per (output row, group of 64 k)
+ *   y       bf16   [M, N]            output, rounded once from fp32 (RNE)
+ *
+ * All pointers except `stream` are DEVICE pointers owned by the caller; the
+ * library allocates nothing and keeps no pointer after a call returns.  All
+ * calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy default
+ * stream) and return after the launch.  Arguments are checked on the host
+ * before anything is launched; a call that returns an error has launched
+ * nothing and written nothing.  Inputs must be finite.
+ *
+ * Device requirement: compute capability 10.3 (sm_103a).
+ */
+#ifndef MXQ_H
+#define MXQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MXQ_OK = 0,
+    MXQ_ERR_INVALID_ARG = 1, /* bad size, bits, group size or null pointer   */
+    MXQ_ERR_MISALIGNED = 2,  /* x, w or y not 16-byte aligned; or a scale /
+                                bias / id pointer not aligned to its type     */
+    MXQ_ERR_UNSUPPORTED = 3, /* a valid request this build does not implement */
+    MXQ_ERR_ARCH = 4,        /* current device is not compute capability 10.3 */
+    MXQ_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed          */
+    MXQ_ERR_WORKSPACE = 6    /* workspace missing or smaller than required    */
+} mxq_status;
+
+/* Bits set in *dev_status (device memory, written by the kernels when the
+ * caller passes a non-null pointer; the call first stores 0 there).        */
+#define MXQ_DEV_BAD_EXPERT_ID   0x1 /* an expert id outside [0, E)             */
+#define MXQ_DEV_UNSORTED_IDS    0x2 /* expert ids decrease somewhere           */
+#define MXQ_DEV_BAD_ROW_SRC     0x4 /* a row_src entry outside [0, T)          */
+#define MXQ_DEV_TIMEOUT         0x8 /* an on-chip pipeline wait gave up; the
+                                       output is incomplete                   */
+
+/* Decode GEMV, M = 1 (mlxcel issue #1536, Diagnosis item 3: the qmv kernel;
+ * fp32 accumulation at every width is the fix that item names).
+ *   x: bf16 [K]; y: bf16 [N]; w, scales, biases as above.
+ * Requirements: bits in {4, 8}; group_size == 64; K > 0 and K % 64 == 0;
+ * N > 0; x, w, y 16-byte aligned; scales, biases 2-byte aligned.            */
+mxq_status mxq_qmv(const void* x, const uint32_t* w, const void* scales, const void* biases,
+                   void* y, int K, int N, int bits, int group_size, void* stream);
+
+/* Prefill GEMM, y[M, N] = x[M, K] . w^[N, K]^T (mlxcel issue #1536, Baseline
+ * profile table and Diagnosis item 4: the qmm_naive kernel).  Runs on the
+ * tcgen05 tensor cores: codes are dequantised to bf16 in shared memory and
+ * accumulated in fp32 in tensor memory.
+ * Requirements as for mxq_qmv plus M > 0.
+ * `workspace` (device, may be NULL) lets the call split K across CTAs when M
+ * and N alone give too few tiles for the GPU; pass at least
+ * mxq_qmm_workspace_bytes(M, K, N, bits) bytes, 256-byte aligned, or NULL /
+ * 0 to run without splitting (same result, bit for bit).  The call writes
+ * the workspace before it reads it; concurrent calls need distinct
+ * workspaces.  `dev_status` (device int32, may be NULL) receives 0 or
+ * MXQ_DEV_TIMEOUT.                                                         */
+mxq_status mxq_qmm(const void* x, const uint32_t* w, const void* scales, const void* biases,
+                   void* y, int M, int K, int N, int bits, int group_size,
+                   void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/* Workspace bytes that let mxq_qmm split K for this shape (0 = never splits). */
+size_t mxq_qmm_workspace_bytes(int M, int K, int N, int bits);
+
+/* Sorted mixture-of-experts grouped variant (mlxcel PR #1562, Summary: the
+ * sorted-MoE prefill path that routes a quantized GatherQMM into a grouped
+ * GEMM, B = tokens * top_k rows sorted by expert).
+ *   x:          bf16 [T, K]  activation rows
+ *   w:          uint32 [E, N, K*bits/32]; scales, biases: bf16 [E, N, K/64]
+ *   expert_ids: int32 [B], non-decreasing: expert of sorted row r
+ *   row_src:    int32 [B], row of x that feeds sorted row r; NULL means r
+ *               (then T must equal B)
+ *   y:          bf16 [B, N], in sorted row order
+ *   workspace:  device scratch of mxq_gather_workspace_bytes(B, E, N) bytes,
+ *               256-byte aligned; overwritten by the call.
+ *   dev_status: device int32 or NULL; receives the MXQ_DEV_* bits.
+ * Rows whose expert id lies outside [0, E), or whose row_src lies outside
+ * [0, T), are skipped and their y rows set to zero.  If the ids are not
+ * non-decreasing, nothing is computed, all of y is set to zero and
+ * MXQ_DEV_UNSORTED_IDS is reported.  No invalid input makes the kernels
+ * read or write out of bounds.
+ * Requirements: B, E, T, N > 0; K > 0, K % 64 == 0; bits in {4, 8};
+ * group_size == 64; x, w, y 16-byte aligned; the rest aligned to type.       */
+mxq_status mxq_gather_qmm(const void* x, const uint32_t* w, const void* scales,
+                          const void* biases, const int32_t* expert_ids,
+                          const int32_t* row_src, void* y, int T, int B, int E, int K, int N,
+                          int bits, int group_size, void* workspace, size_t workspace_bytes,
+                          int32_t* dev_status, void* stream);
+
+/* Workspace bytes mxq_gather_qmm needs for B rows over E experts. */
+size_t mxq_gather_workspace_bytes(int B, int E, int N);
+
+/* Static description of a status code. */
+const char* mxq_status_string(mxq_status status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int mxq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXQ_H */

@@ -1,0 +1,115 @@
+"""Host-side tests of the C ABI (no GPU needed): the library builds, loads and
+exports every function ``include/mxq.h`` declares, and argument checks
+return the documented status codes before anything touches a device."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mxq.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from affine_bit_matmul_gb300 import build
+
+    build.build()
+    import affine_bit_matmul_gb300 as mxq
+
+    return mxq.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mxq_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("mxq_qmv", "mxq_qmm", "mxq_gather_qmm", "mxq_gather_workspace_bytes",
+              "mxq_qmm_workspace_bytes", "mxq_status_string", "mxq_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    import affine_bit_matmul_gb300 as mxq
+
+    for name in declared_functions():
+        assert hasattr(L, name), name
+        assert name in mxq.EXPORTED_SYMBOLS or name.startswith("mxq_")
+
+
+def test_status_strings(L):
+    for code in range(0, 7):
+        s = L.mxq_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert L.mxq_status_string(99).decode() == "unknown status"
+    assert L.mxq_version() >= 100
+
+
+FAKE = ctypes.c_void_p(0x10000)       # 16-byte aligned, never dereferenced
+FAKE_ODD = ctypes.c_void_p(0x10008)   # 8-byte aligned only
+
+
+def qmv(L, x=FAKE, w=FAKE, s=FAKE, b=FAKE, y=FAKE, K=128, N=64, bits=4, group=64):
+    return L.mxq_qmv(x, w, s, b, y, K, N, bits, group, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(bits=3), 1), (dict(bits=16), 1), (dict(bits=2), 1), (dict(group=32), 1),
+    (dict(group=128), 1), (dict(K=100), 1), (dict(K=0), 1), (dict(K=-64), 1), (dict(N=0), 1),
+    (dict(x=None), 1), (dict(w=None), 1), (dict(s=None), 1), (dict(b=None), 1), (dict(y=None), 1),
+    (dict(x=FAKE_ODD), 2), (dict(w=FAKE_ODD), 2), (dict(y=FAKE_ODD), 2),
+    (dict(s=ctypes.c_void_p(0x10001)), 2),
+])
+def test_qmv_argument_checks(L, kw, code):
+    assert qmv(L, **kw) == code
+
+
+def qmm(L, M=16, K=128, N=64, bits=4, group=64, ws=None, wsb=0, status=None, x=FAKE, y=FAKE):
+    return L.mxq_qmm(x, FAKE, FAKE, FAKE, y, M, K, N, bits, group, ws, wsb, status, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(M=0), 1), (dict(M=-1), 1), (dict(bits=5), 1), (dict(group=16), 1), (dict(K=96), 1),
+    (dict(x=None), 1), (dict(x=FAKE_ODD), 2), (dict(y=FAKE_ODD), 2),
+    (dict(ws=ctypes.c_void_p(0x10010), wsb=64), 2), (dict(status=ctypes.c_void_p(0x10002)), 2),
+])
+def test_qmm_argument_checks(L, kw, code):
+    assert qmm(L, **kw) == code
+
+
+def gather(L, T=8, B=8, E=2, K=128, N=64, bits=4, group=64, ids=FAKE, src=FAKE, ws=FAKE,
+           wsb=1 << 20):
+    return L.mxq_gather_qmm(FAKE, FAKE, FAKE, FAKE, ids, src, FAKE, T, B, E, K, N, bits, group,
+                            ws, wsb, None, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(T=0), 1), (dict(B=0), 1), (dict(E=0), 1), (dict(bits=6), 1), (dict(K=65), 1),
+    (dict(ids=None), 1), (dict(src=None, T=5, B=8), 1),
+    (dict(ids=ctypes.c_void_p(0x10002)), 2), (dict(ws=ctypes.c_void_p(0x10080)), 2),
+    (dict(ws=None), 6), (dict(wsb=16), 6),
+])
+def test_gather_argument_checks(L, kw, code):
+    assert gather(L, **kw) == code
+
+
+def test_workspace_sizes(L):
+    n = L.mxq_gather_workspace_bytes(4584, 128, 704)
+    # one 16-byte tile record per possible tile plus the count
+    assert n >= (4584 // 128 + 128) * 16
+    assert L.mxq_gather_workspace_bytes(0, 4, 4) == 0
+
+
+def test_valid_call_without_sm103_device_reports_device_error(L):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; covered by the GPU tests")
+    # arguments pass the host checks; the device check must then refuse
+    assert qmv(L) in (4, 5)

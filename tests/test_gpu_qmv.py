@@ -1,0 +1,80 @@
+"""GPU parity of mxq_qmv (decode GEMV) against the f64 checker, element by
+element, through the C ABI.  Shapes: the tiny and decode workloads (K=512
+N=256; K=5120 N=17408; K=17408 N=5120) plus ragged edges."""
+
+import numpy as np
+import pytest
+
+import oracle
+from tests.gpu_util import DenseCase, assert_close, bf16_dev, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(case, out=None):
+    import affine_bit_matmul_gb300 as mxq
+
+    return mxq.qmv(case.x_d[0], case.w_d, case.s_d, case.b_d, case.bits, out=out)
+
+
+def _ref(case):
+    return oracle.qmv(case.x[0], case.qw.w, case.qw.scales, case.qw.biases, case.K, case.N,
+                      case.bits)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("K,N", [(512, 256), (64, 1), (64, 7), (128, 17), (704, 33), (1088, 100),
+                                 (1024, 16), (2048, 31), (5120, 513), (6144, 129)])
+def test_qmv_small(bits, K, N):
+    case = DenseCase(1, K, N, bits, seed=K + N, x_seed=K)
+    y = _run(case)
+    yr, bnd = _ref(case)
+    assert_close(to_f64(y), yr, bnd, "qmv K=%d N=%d bits=%d" % (K, N, bits))
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("K,N", [(5120, 17408), (17408, 5120)])
+def test_qmv_decode_full(bits, K, N):
+    case = DenseCase(1, K, N, bits, seed=0, x_seed=1)
+    y = _run(case)
+    yr, bnd = _ref(case)
+    assert_close(to_f64(y), yr, bnd, "qmv decode K=%d N=%d bits=%d" % (K, N, bits))
+    # bitwise run-to-run determinism
+    import torch
+
+    y2 = _run(case)
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+
+
+def test_qmv_guard_bands_untouched():
+    import torch
+
+    case = DenseCase(1, 1024, 300, 4, seed=3)
+    guard = 4096
+    buf = torch.full((guard + 300 + guard,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    out = buf[guard:guard + 300]
+    _run(case, out=out)
+    torch.cuda.synchronize()
+    assert torch.isnan(buf[:guard]).all() and torch.isnan(buf[guard + 300:]).all()
+    yr, bnd = _ref(case)
+    assert_close(to_f64(out), yr, bnd, "qmv guarded")
+
+
+def test_qmv_closed_form_zero_scale():
+    # s = 0, b = c: y = c * sum_k x_k (all values small integers: exact)
+    import synth
+    import affine_bit_matmul_gb300 as mxq
+    from tests.gpu_util import codes_dev
+
+    K, N = 1024, 64
+    rng = np.random.default_rng(9)
+    x = rng.integers(-4, 5, size=(1, K)).astype(np.float32)
+    xb = synth.f32_to_bf16_bits(x)
+    c = (np.arange(N) % 8 + 1) / 8.0
+    s = np.zeros((N, K // 64), np.uint16)
+    b = np.repeat(synth.f32_to_bf16_bits(c.astype(np.float32))[:, None], K // 64, axis=1)
+    w = rng.integers(0, 2 ** 32, size=(N, K // 8), dtype=np.uint64).astype(np.uint32)
+    y = mxq.qmv(bf16_dev(xb)[0], codes_dev(w), bf16_dev(s), bf16_dev(b), 4)
+    exact = (c * x.sum()).astype(np.float32)  # exact in fp32
+    want = synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(exact)).astype(np.float64)
+    assert np.array_equal(to_f64(y), want)
