@@ -1,0 +1,513 @@
+"""Benchmark of the affine group-wise quantized matmul library on GB300.
+
+One step is the decode GEMV (qmv) over the decode workload: K=5120 N=17408
+and K=17408 N=5120, each with 4-bit and 8-bit codes (group 64, bf16 scales
+and biases, W ~ N(0, 0.02) quantized with scale=(max-min)/(2^bits-1),
+bias=min, x ~ N(0, 1)).  ``value`` is the whole-job achieved HBM bandwidth
+over algorithmic bytes (codes + scales + biases + x + y) in GB/s.  Each
+case keeps two copies of its inputs and alternates between them, so the
+working set of a step pass (580 MB) is larger than the 129 MB L2.
+
+The same JSON line carries, measured after the main timed region and with
+their own rotation: the prefill GEMM (M=600, K=5120, N=17408), the M sweep
+at K=N=5120, the sorted-MoE gather (E=128, top_k=8, 573 tokens; K=2816
+N=704 and K=704 N=2816) and the 4-bit vs 8-bit controlled pair, each with
+its binding roofline.
+
+``--impl reference`` times the f64 CPU checker on the same metric (the
+slow reference program, not a target).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "qmv HBM GB/s and qmm/gather_qmm TFLOPS on 1 GB300, % of roofline"
+DECODE_CASES = [(5120, 17408, 4), (5120, 17408, 8), (17408, 5120, 4), (17408, 5120, 8)]
+WORKLOAD = ("qmv decode M=1: K=5120 N=17408 and K=17408 N=5120, 4-bit and 8-bit, group 64, "
+            "bf16 scales/biases")
+
+
+def qmv_bytes(K, N, bits):
+    return N * K * bits // 8 + N * (K // 64) * 4 + K * 2 + N * 2
+
+
+def qmm_bytes(M, K, N, bits):
+    return N * K * bits // 8 + N * (K // 64) * 4 + M * K * 2 + M * N * 2
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(
+            p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ------------------------------------------------------------------ helpers
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile(mode="w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [l.strip().split(",") for l in self.file.read().splitlines() if l.strip()]
+        os.unlink(self.file.name)
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sms.append(float(r[1]))
+                maxes.append(float(r[2]))
+                for name, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(name)
+            except (ValueError, IndexError):
+                continue
+        if not sms:
+            return None
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes),
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(value, world):
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ device inputs
+
+
+def dev_bf16(a, dev):
+    import torch
+
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16).copy()).view(
+        torch.bfloat16).to(dev)
+
+
+def dev_codes(a, dev):
+    import torch
+
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int32).copy()).to(dev)
+
+
+class DenseInputs:
+    def __init__(self, W, M, K, N, bits, dev, copies, x_seed=1):
+        import torch
+
+        qw = synth.quantize(W, bits)
+        self.M, self.K, self.N, self.bits = M, K, N, bits
+        self.host = (qw.w, qw.scales, qw.biases)
+        self.x_host = synth.activations(M, K, seed=x_seed)
+        w, s, b = dev_codes(qw.w, dev), dev_bf16(qw.scales, dev), dev_bf16(qw.biases, dev)
+        self.copies = [(w, s, b)] + [(w.clone(), s.clone(), b.clone()) for _ in range(copies - 1)]
+        self.x = dev_bf16(self.x_host, dev)
+        self.y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+
+
+def time_launches(fn, iters, stream):
+    """Average device time of fn() over iters launches (CUDA events on the
+    launching stream, each launch bracketed)."""
+    import torch
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(iters)]
+    for i in range(iters):
+        evs[i][0].record(stream)
+        fn(i)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    ts = [a.elapsed_time(b) for a, b in evs]
+    return statistics.median(ts) * 1e-3, ts
+
+
+# ------------------------------------------------------------------ our arm
+
+
+def run_mxq(args):
+    import torch
+
+    import affine_bit_matmul_gb300 as mxq
+    from affine_bit_matmul_gb300 import build as _build
+
+    world, rank, local = dist_setup(args.gpus)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    _build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    hbm, bf16_peak, bf16_sus, peak_src = load_peaks()
+
+    # ---- decode workload: 4 cases, two input copies each
+    Ws = {}
+    cases = []
+    for K, N, bits in DECODE_CASES:
+        if (K, N) not in Ws:
+            Ws[(K, N)] = synth.dense_weights(N, K, seed=0)
+        cases.append(DenseInputs(Ws[(K, N)], 1, K, N, bits, dev, copies=2))
+    step_bytes = sum(qmv_bytes(c.K, c.N, c.bits) for c in cases)
+
+    def step(i, record=None):
+        for ci, c in enumerate(cases):
+            w, s, b = c.copies[i % 2]
+            if record is not None:
+                record[ci][0].record(stream)
+            mxq.qmv(c.x[0], w, s, b, c.bits, out=c.y[0])
+            if record is not None:
+                record[ci][1].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    clocks = Clocks(local)
+    ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+           for _ in cases] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    t0.record(stream)
+    for i in range(args.steps):
+        step(i, ev[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    elapsed = max_over_ranks(t0.elapsed_time(t1) * 1e-3, world)
+    value = step_bytes * args.steps * world / elapsed / 1e9
+    per_case = []
+    qmv_time = 0.0
+    for ci, c in enumerate(cases):
+        ts = [ev[i][ci][0].elapsed_time(ev[i][ci][1]) * 1e-3 for i in range(args.steps)]
+        avg = sum(ts) / len(ts)
+        qmv_time += sum(ts)
+        per_case.append({"K": c.K, "N": c.N, "bits": c.bits, "us": avg * 1e6,
+                         "GB_s": qmv_bytes(c.K, c.N, c.bits) / avg / 1e9,
+                         "frac_hbm": qmv_bytes(c.K, c.N, c.bits) / avg / 1e9 / hbm})
+    achieved = step_bytes * args.steps / qmv_time / 1e9
+
+    # ---- end to end through the public API with host buffers
+    pinned = []
+    for c in cases:
+        w, s, b = c.host
+        pinned.append({
+            "w": torch.from_numpy(w.view(np.int32).copy()).pin_memory(),
+            "s": torch.from_numpy(s.view(np.int16).copy()).view(torch.bfloat16).pin_memory(),
+            "b": torch.from_numpy(b.view(np.int16).copy()).view(torch.bfloat16).pin_memory(),
+            "x": torch.from_numpy(c.x_host.view(np.int16).copy()).view(torch.bfloat16).pin_memory(),
+            "y": torch.empty((c.N,), dtype=torch.bfloat16).pin_memory(),
+        })
+    h2d = sum(sum(p[k].numel() * p[k].element_size() for k in ("w", "s", "b", "x")) for p in pinned)
+    d2h = sum(p["y"].numel() * 2 for p in pinned)
+
+    def e2e_step():
+        for c, p in zip(cases, pinned):
+            w, s, b = c.copies[0]
+            w.copy_(p["w"], non_blocking=True)
+            s.copy_(p["s"], non_blocking=True)
+            b.copy_(p["b"], non_blocking=True)
+            c.x[0].copy_(p["x"][0], non_blocking=True)
+            mxq.qmv(c.x[0], w, s, b, c.bits, out=c.y[0])
+            p["y"].copy_(c.y[0], non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    a, bq = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    bq.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_elapsed = max_over_ranks(a.elapsed_time(bq) * 1e-3, world)
+    e2e_value = step_bytes * e2e_steps * world / e2e_elapsed / 1e9
+
+    secondary = []
+    if not args.no_secondary:
+        secondary = secondary_measurements(mxq, dev, stream, hbm, bf16_peak, Ws)
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": elapsed / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "u4/u8 codes, bf16 x, fp32 accumulate",
+        "data": "synthetic (seeded W~N(0,0.02) quantized per the workload recipe, x~N(0,1))",
+        "config": {"workload": WORKLOAD, "M": 1, "group_size": 64,
+                   "l2": "inputs larger than L2: each case alternates two input copies "
+                         "(580 MB working set vs 129 MB L2)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "kernel": "qmv_kernel (4- and 8-bit)",
+                     "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": None,
+                     "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs copy bandwidth)"},
+        "per_case": per_case,
+        "gpu_launches": len(cases) * args.steps,
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "note": "public API qmv with inputs copied from pinned host memory every step"},
+        "clocks": clk,
+        "secondary": secondary,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def secondary_measurements(mxq, dev, stream, hbm, bf16_peak, Ws):
+    """Prefill GEMM, M sweep, sorted-MoE gather and the 4/8-bit pair."""
+    import torch
+
+    out = []
+    iters = 40
+
+    def dense_entry(name, M, K, N, bits, W, copies):
+        d = DenseInputs(W, M, K, N, bits, dev, copies=copies)
+        ws = torch.empty((max(1, mxq.qmm_workspace_bytes(M, K, N, bits)),), dtype=torch.uint8,
+                         device=dev)
+        if M == 1:
+            fn = lambda i: mxq.qmv(d.x[0], *d.copies[i % copies], bits, out=d.y[0])  # noqa: E731
+            kern = "qmv_kernel"
+        else:
+            fn = lambda i: mxq.qmm(d.x, *d.copies[i % copies], bits, out=d.y, workspace=ws)  # noqa: E731
+            kern = "qmm_tc_kernel"
+        for i in range(5):
+            fn(i)
+        t, _ = time_launches(fn, iters, stream)
+        flops = 2.0 * M * K * N
+        nbytes = qmm_bytes(M, K, N, bits)
+        t_star = max(nbytes / (hbm * 1e9), flops / (bf16_peak * 1e12))
+        bound = "hbm" if nbytes / (hbm * 1e9) >= flops / (bf16_peak * 1e12) else "tensor"
+        del d
+        return {"name": name, "kernel": kern, "M": M, "K": K, "N": N, "bits": bits,
+                "us": t * 1e6, "TFLOPS": flops / t / 1e12, "GB_s": nbytes / t / 1e9,
+                "frac_tensor": flops / t / 1e12 / bf16_peak, "frac_hbm": nbytes / t / 1e9 / hbm,
+                "bound": bound, "frac_roofline": t_star / t, "tokens_per_s": M / t}
+
+    W_big = Ws.get((5120, 17408)) if Ws.get((5120, 17408)) is not None else synth.dense_weights(
+        17408, 5120, seed=0)
+    out.append(dense_entry("qmm prefill", 600, 5120, 17408, 4, W_big, copies=3))
+    W_sq = synth.dense_weights(5120, 5120, seed=0)
+    for M in (1, 8, 32, 128, 600):
+        out.append(dense_entry("qmm sweep", M, 5120, 5120, 4, W_sq, copies=6))
+    # controlled pair: same W, 8-bit (4-bit rows are in the sweep above)
+    out.append(dense_entry("pair qmv 8-bit", 1, 5120, 5120, 8, W_sq, copies=6))
+    out.append(dense_entry("pair qmv 4-bit", 1, 5120, 5120, 4, W_sq, copies=6))
+    out.append(dense_entry("pair qmm 8-bit", 128, 5120, 5120, 8, W_sq, copies=6))
+
+    # sorted MoE gather, both expert shapes
+    for K, N, ident in ((2816, 704, False), (704, 2816, True)):
+        E, T, top_k, bits = 128, 573, 8, 4
+        ids, src = synth.routing(T, E, top_k, seed=2)
+        B = ids.shape[0]
+        wl, sl, bl = [], [], []
+        for e in range(E):
+            q = synth.quantize(synth.dense_weights(N, K, seed=e), bits)
+            wl.append(q.w)
+            sl.append(q.scales)
+            bl.append(q.biases)
+        w = dev_codes(np.stack(wl), dev)
+        s = dev_bf16(np.stack(sl), dev)
+        b = dev_bf16(np.stack(bl), dev)
+        copies = [(w, s, b), (w.clone(), s.clone(), b.clone())]
+        Tx = B if ident else T
+        x = dev_bf16(synth.activations(Tx, K, seed=1), dev)
+        ids_d = torch.from_numpy(ids).to(dev)
+        src_d = None if ident else torch.from_numpy(src).to(dev)
+        y = torch.empty((B, N), dtype=torch.bfloat16, device=dev)
+        wsz = torch.empty((mxq.gather_workspace_bytes(B, E, N),), dtype=torch.uint8, device=dev)
+        fn = lambda i: mxq.gather_qmm(x, *copies[i % 2], ids_d, src_d, bits, out=y,  # noqa: E731
+                                      workspace=wsz)
+        for i in range(5):
+            fn(i)
+        t, _ = time_launches(fn, iters, stream)
+        flops = 2.0 * B * K * N
+        nbytes = E * (N * K * bits // 8 + N * (K // 64) * 4) + Tx * K * 2 + B * N * 2
+        t_star = max(nbytes / (hbm * 1e9), flops / (bf16_peak * 1e12))
+        out.append({"name": "gather_qmm", "kernel": "gather_prepass + qmm_tc_kernel",
+                    "E": E, "top_k": top_k, "tokens": T, "B": B, "K": K, "N": N, "bits": bits,
+                    "us": t * 1e6, "TFLOPS": flops / t / 1e12, "GB_s": nbytes / t / 1e9,
+                    "frac_tensor": flops / t / 1e12 / bf16_peak, "frac_hbm": nbytes / t / 1e9 / hbm,
+                    "bound": "hbm", "frac_roofline": t_star / t, "tokens_per_s": T / t})
+        del w, s, b, copies, x, y
+        torch.cuda.empty_cache()
+    return out
+
+
+# ------------------------------------------------------------------ CPU side
+
+
+def cpu_baseline(seconds):
+    """The f64 checker on the host cores: qmv K=5120 N=17408 4-bit, whole
+    output, repeated for about ``seconds``."""
+    import oracle
+
+    K, N, bits = 5120, 17408, 4
+    qw = synth.quantize(synth.dense_weights(N, K, seed=0), bits)
+    x = synth.activations(1, K, seed=1)
+    oracle.qmv(x[0], qw.w, qw.scales, qw.biases, K, N, bits)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.qmv(x[0], qw.w, qw.scales, qw.biases, K, N, bits)
+        reps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = (time.perf_counter() - t0) / reps
+    return {"value": round(qmv_bytes(K, N, bits) / dt / 1e9, 3), "unit": "GB/s",
+            "cores": oracle.threads(), "kind": "oracle",
+            "sample": "f64 qmv K=5120 N=17408 4-bit, whole output, %d repetitions" % reps}
+
+
+def run_reference(args):
+    """The f64 checker as the reference arm: the same decode step (all four
+    cases, whole outputs) on the host cores."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+
+    cases = []
+    Ws = {}
+    for K, N, bits in DECODE_CASES:
+        if (K, N) not in Ws:
+            Ws[(K, N)] = synth.dense_weights(N, K, seed=0)
+        qw = synth.quantize(Ws[(K, N)], bits)
+        cases.append((K, N, bits, qw, synth.activations(1, K, seed=1)))
+    step_bytes = sum(qmv_bytes(K, N, bits) for K, N, bits, _, _ in cases)
+
+    def step():
+        for K, N, bits, qw, x in cases:
+            oracle.qmv(x[0], qw.w, qw.scales, qw.biases, K, N, bits)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = step_bytes * args.steps / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": 1, "group_size": 64},
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": oracle.threads(),
+                         "kind": "oracle",
+                         "sample": "f64 checker, all four decode cases per step, whole outputs"},
+        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["mxq", "reference"], default="mxq")
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_mxq(args)
+
+
+if __name__ == "__main__":
+    main()

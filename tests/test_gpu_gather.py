@@ -20,15 +20,18 @@ def _mxq():
     return mxq
 
 
-def _run(c, out=None, status=None, ids_d=None, src_d="same"):
+_SAME = object()
+
+
+def _run(c, out=None, status=None, ids_d=None, src_d=_SAME):
     return _mxq().gather_qmm(c.x_d, c.w_d, c.s_d, c.b_d, c.ids_d if ids_d is None else ids_d,
-                             c.src_d if src_d == "same" else src_d, c.bits, out=out,
+                             c.src_d if src_d is _SAME else src_d, c.bits, out=out,
                              dev_status=status)
 
 
-def _ref(c, ids=None, src="same"):
+def _ref(c, ids=None, src=_SAME):
     return oracle.gather_qmm(c.x, c.w, c.s, c.b, c.ids if ids is None else ids,
-                             c.src if src == "same" else src, c.T, c.B, c.E, c.K, c.N, c.bits)
+                             c.src if src is _SAME else src, c.T, c.B, c.E, c.K, c.N, c.bits)
 
 
 @pytest.mark.parametrize("bits", [4, 8])
