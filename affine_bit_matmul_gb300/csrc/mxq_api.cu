@@ -160,6 +160,7 @@ mxq_status mxq_qmm(const void* x, const uint32_t* w, const void* scales, const v
     p.status = dev_status;
     p.M = M;
     p.T = M;
+    p.E = 1;
     p.K = K;
     p.N = N;
     p.m_tile = pl.m_tile;
@@ -222,6 +223,7 @@ mxq_status mxq_gather_qmm(const void* x, const uint32_t* w, const void* scales,
     p.status = dev_status;
     p.M = B;
     p.T = T;
+    p.E = E;
     p.K = K;
     p.N = N;
     p.m_tile = kGatherRowsPerTile;

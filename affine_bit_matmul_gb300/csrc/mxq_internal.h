@@ -31,6 +31,7 @@ struct QmmParams {
     int* counters;           // split-K arrival counters, or null
     int M;                   // dense form: rows of x and y
     int T;                   // grouped form: rows of x
+    int E;                   // grouped form: experts
     int K, N;
     int m_tile;              // dense form: rows per M tile (multiple of 16)
     int tmem_cols;           // tensor-memory columns allocated per CTA

@@ -9,20 +9,24 @@
 //  * swap-AB: the MMA's M side is 128 rows of w (output columns n), its N side
 //    is a tile of up to 256 activation rows, so a 36-row expert segment or a
 //    single decode row still fills the 128-row tensor-core tile;
-//  * per 64-wide K block (one quantisation group), producer warps copy the
-//    packed codes and the activation rows (gathered through row_src in the
-//    grouped form) into a shared-memory ring with cp.async; four dequant warps
-//    turn codes into bf16 w^ = s*q + b (one bf16 rounding) written directly in
-//    the 128-byte-swizzled K-major layout the tensor core reads; one thread
-//    issues four 128xNx16 tcgen05.mma per block into fp32 tensor memory;
-//  * the dequant warps then read the accumulators back with tcgen05.ld and
-//    store bf16 (or, with K split across CTAs, fp32 partials that the last
-//    CTA of the tile sums in a fixed order: results do not depend on timing).
+//  * per 64-wide K block (one quantisation group) a TMA copy brings the
+//    packed codes of the 128 w rows into a deep ring of small stages; the
+//    activation tile comes by TMA with 128-byte swizzle (dense form) or is
+//    gathered row by row through row_src with cp.async (grouped form);
+//  * eight dequant warps (two threads per w row) turn codes into bf16
+//    w^ = s*q + b (one rounding) and write it straight into the
+//    128-byte-swizzled K-major layout the tensor core reads;
+//  * one thread issues four 128xNx16 tcgen05.mma per block into fp32 tensor
+//    memory; the dequant warps then read the accumulators back with
+//    tcgen05.ld and store bf16 (or, with K split across CTAs, fp32 partials
+//    that the last CTA of the tile sums in a fixed order: the result does not
+//    depend on timing).
 //
 // Every wait on an mbarrier is bounded; on expiry the kernel sets
-// MXQ_DEV_TIMEOUT, stops issuing work, drains what it issued and frees its
+// MXQ_DEV_TIMEOUT, stops issuing work, lets issued work finish and frees its
 // tensor memory before returning.
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -33,42 +37,43 @@
 namespace mxq {
 namespace {
 
-constexpr int kThreads = 256;       // 8 warps
-constexpr int kDequantWarps = 4;    // warps 0-3: dequant + epilogue (thread t <-> w row t)
-constexpr int kProducerFirst = 4;   // warps 4-6: cp.async producers
-constexpr int kProducerThreads = 96;
-constexpr int kMmaWarp = 7;         // warp 7: TMEM owner, lane 0 issues MMAs
-constexpr int kTileN = 128;         // rows of w per CTA (MMA M)
-constexpr int kBK = 64;             // K per pipeline stage (= one group)
-constexpr int kMaxStages = 8;
-constexpr int kLag = 2;             // stages a producer keeps in flight before signalling
-constexpr int kMaxRows = 256;       // activation rows per tile (MMA N <= 256)
-constexpr int kSmemBudget = 200 * 1024;
-
-__host__ __device__ constexpr int code_bytes_per_stage(int bits) { return kTileN * kBK * bits / 8; }
+constexpr int kDequantWarps = 8;     // warps 0-7: dequant + epilogue
+constexpr int kDequantThreads = kDequantWarps * 32;
+constexpr int kTmaWarp = 8;          // lane 0: codes TMA; lane 1: activation TMA (dense)
+constexpr int kMmaWarp = 9;          // TMEM owner, lane 0 issues MMAs
+constexpr int kGatherWarp0 = 10;     // warps 10-11: activation rows by cp.async (grouped)
+constexpr int kGatherThreads = 64;
+constexpr int kThreads = 12 * 32;
+constexpr int kTileN = 128;          // rows of w per CTA (MMA M)
+constexpr int kBK = 64;              // K per stage (= one group)
+constexpr int kMaxRows = 256;        // activation rows per tile (MMA N <= 256)
+constexpr int kCodeStages = 8;
+constexpr int kMaxAxStages = 6;
+constexpr int kSmemBudget = 210 * 1024;
 
 struct SmemLayout {
-    int stages;
-    int a_bytes, x_bytes, c_bytes, stage_bytes;
-    int bar_offset;  // after all stages
-    int src_offset;  // activation row of each tile row (-1 = zero row)
-    int total;
+    int c_bytes, c_stages;    // packed-code ring
+    int a_bytes, x_bytes, ax_bytes, ax_stages;  // dequantised w + activation ring
+    int c_offset;             // code ring after the ax ring
+    int bar_offset, src_offset, total;
 };
 
 __host__ __device__ inline SmemLayout make_layout(int bits, int max_rows) {
     SmemLayout L;
-    const int rows16 = (max_rows + 15) & ~15;          // n_mma never exceeds this
-    L.a_bytes = kTileN * kBK * 2;                      // 16 KB bf16
-    L.x_bytes = (rows16 / 8) * 1024;                   // rows x 128 B, 8-row atoms
-    L.c_bytes = code_bytes_per_stage(bits);            // 4 KB or 8 KB
-    L.stage_bytes = L.a_bytes + L.x_bytes + L.c_bytes; // multiple of 1024
-    int s = kSmemBudget / L.stage_bytes;
-    // the producers signal a stage kLag stages late, so the ring needs more
-    L.stages = s > kMaxStages ? kMaxStages : (s < kLag + 1 ? kLag + 1 : s);
-    L.bar_offset = L.stages * L.stage_bytes;
-    // full, afull, empty per stage, accf, tmem base, flag, then source rows
-    L.src_offset = L.bar_offset + (3 * kMaxStages + 1) * 8 + 16;
-    L.total = L.src_offset + kMaxRows * 4 + 1024 /* alignment slack */;
+    const int rows16 = (max_rows + 15) & ~15;
+    L.c_bytes = kTileN * kBK * bits / 8;              // 4 KB or 8 KB
+    L.c_stages = kCodeStages;
+    L.a_bytes = kTileN * kBK * 2;                     // 16 KB
+    L.x_bytes = (rows16 / 8) * 1024;                  // 128 B per row, 8-row atoms
+    L.ax_bytes = L.a_bytes + L.x_bytes;               // multiple of 1024
+    int s = (kSmemBudget - L.c_stages * L.c_bytes) / L.ax_bytes;
+    L.ax_stages = s > kMaxAxStages ? kMaxAxStages : (s < 2 ? 2 : s);
+    L.c_offset = L.ax_stages * L.ax_bytes;
+    L.bar_offset = L.c_offset + L.c_stages * L.c_bytes;
+    // cfull, cempty per code stage; xfull, afull, axempty per ax stage; accf;
+    // tmem base; flag
+    L.src_offset = L.bar_offset + (2 * kCodeStages + 3 * kMaxAxStages + 1) * 8 + 16;
+    L.total = L.src_offset + kMaxRows * 4 + 1024;     // + alignment slack
     return L;
 }
 
@@ -113,8 +118,8 @@ __device__ __forceinline__ void dequant_word4(uint32_t wd, uint32_t s2, uint32_t
 }
 
 // Four 8-bit codes (lowest k in the lowest byte) -> two bf16x2 words.  The
-// code is exact in fp32 (2^23 + q, minus 2^23), s*q + b is formed by one fp32
-// FMA (s*q is exact) and rounded to bf16.
+// code is exact in fp32 (2^23 + q, minus 2^23), s*q + b is one fp32 FMA
+// (s*q is exact), then rounded to bf16.
 __device__ __forceinline__ void dequant_word8(uint32_t wd, float s, float b, uint32_t (&out)[2]) {
     const float m = 8388608.f;
     const float q0 = __uint_as_float(prmt(wd, 0x4B000000u, 0x7440u)) - m;
@@ -146,31 +151,63 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int c) {
     return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile(
+        "{\n\t.reg .b64 st;\n\t"
+        "mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+            smem_u32(bar)),
+        "r"(bytes)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void flag_status(int32_t* status, int bits) {
     if (status) atomicOr(status, bits);
 }
 
-template <int BITS>
-__global__ void __launch_bounds__(kThreads, 1) qmm_tc_kernel(const QmmParams p, int max_rows) {
+template <int BITS, bool GATHER>
+__global__ void __launch_bounds__(kThreads, 1)
+    qmm_tc_kernel(const QmmParams p, int max_rows, const __grid_constant__ CUtensorMap code_map,
+                  const __grid_constant__ CUtensorMap x_map) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const SmemLayout L = make_layout(BITS, max_rows);
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_offset);
-    uint64_t* afull = full + kMaxStages;
-    uint64_t* empty = afull + kMaxStages;
-    uint64_t* accf = empty + kMaxStages;
+    uint64_t* cfull = reinterpret_cast<uint64_t*>(smem + L.bar_offset);
+    uint64_t* cempty = cfull + kCodeStages;
+    uint64_t* xfull = cempty + kCodeStages;
+    uint64_t* afull = xfull + kMaxAxStages;
+    uint64_t* axempty = afull + kMaxAxStages;
+    uint64_t* accf = axempty + kMaxAxStages;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
     int* last_flag = reinterpret_cast<int*>(tmem_slot + 1);
     int* src_rows = reinterpret_cast<int*>(smem + L.src_offset);
     const uint32_t smem_base = smem_u32(smem);
+    const uint32_t c_base0 = smem_base + L.c_offset;
 
     const int warp = threadIdx.x >> 5;
     const int lane = lane_id();
 
     // ---- which tile this CTA computes
     int e = 0, row_start, rows;
-    if (p.tiles) {
+    if (GATHER) {
         if ((int)blockIdx.y >= *p.tile_count) return;  // whole CTA, before any sync
         const MTile t = p.tiles[blockIdx.y];
         e = t.e;
@@ -184,34 +221,35 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_tc_kernel(const QmmParams p, 
     const int n0 = blockIdx.x * kTileN;
     const int KB = p.K / kBK;
     const int kb_begin = blockIdx.z * p.kb_per_split;
-    const int kb_end = min(KB, kb_begin + p.kb_per_split);
-    const int nkb = kb_end - kb_begin;
+    const int nkb = min(KB, kb_begin + p.kb_per_split) - kb_begin;
     const int groups = p.K / 64;
-    const long long wpr = (long long)p.K * BITS / 32;  // words per w row
-    const uint32_t* wexp = p.w + (long long)e * p.w_expert_stride;
-    const uint16_t* sexp = p.scales + (long long)e * p.sb_expert_stride;
-    const uint16_t* bexp = p.biases + (long long)e * p.sb_expert_stride;
-    const int S = L.stages;
+    const int SC = L.c_stages;
+    const int SAX = L.ax_stages;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < S; ++i) {
-            mbar_init(&full[i], kProducerThreads);
-            mbar_init(&afull[i], kDequantWarps * 32);
-            mbar_init(&empty[i], 1);
+        for (int i = 0; i < SC; ++i) {
+            mbar_init(&cfull[i], 1);
+            mbar_init(&cempty[i], kDequantThreads);
+        }
+        for (int i = 0; i < SAX; ++i) {
+            mbar_init(&xfull[i], GATHER ? kGatherThreads : 1);
+            mbar_init(&afull[i], kDequantThreads);
+            mbar_init(&axempty[i], 1);
         }
         mbar_init(accf, 1);
         *last_flag = 0;
         mbar_init_fence();
     }
-    for (int r = threadIdx.x; r < n_mma; r += kThreads) {
-        int src = -1;
-        if (r < rows) {
-            const int sr = row_start + r;
-            src = p.row_src ? p.row_src[sr] : sr;
-            const int limit = p.tiles ? p.T : p.M;
-            if (src < 0 || src >= limit) src = -1;  // reported by the prepass; row reads as zero
+    if (GATHER) {
+        for (int r = threadIdx.x; r < n_mma; r += kThreads) {
+            int src = -1;
+            if (r < rows) {
+                const int sr = row_start + r;
+                src = p.row_src ? p.row_src[sr] : sr;
+                if (src < 0 || src >= p.T) src = -1;  // reported by the prepass; reads as zero
+            }
+            src_rows[r] = src;
         }
-        src_rows[r] = src;
     }
     if (warp == kMmaWarp) {
         tmem_alloc(tmem_slot, (uint32_t)p.tmem_cols);
@@ -223,127 +261,138 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_tc_kernel(const QmmParams p, 
     const uint32_t tmem = *tmem_slot;
     bool ok = true;
 
-    if (warp >= kProducerFirst && warp < kProducerFirst + 3) {
-        // ---------------------------------------------------------------- producers
-        const int pt = threadIdx.x - kProducerFirst * 32;
-        constexpr int kCodeChunksPerRow = kBK * BITS / 8 / 16;  // 2 or 4
-        const int code_chunks = kTileN * kCodeChunksPerRow;
-        const int x_chunks = n_mma * 8;
-        const int total = code_chunks + x_chunks;
+    if (warp == kTmaWarp) {
+        // ---------------------------------------------------------------- TMA issue
+        if (lane == 0) {
+            // packed codes: [128 rows x (64*BITS/32) words] per stage
+            constexpr int kWordsPerBlock = kBK * BITS / 32;
+            for (int i = 0; i < nkb; ++i) {
+                const int slot = i % SC;
+                if (i >= SC && !mbar_wait(&cempty[slot], ((i / SC) + 1) & 1)) { ok = false; break; }
+                mbar_expect_tx(&cfull[slot], (uint32_t)L.c_bytes);
+                const int c0 = (kb_begin + i) * kWordsPerBlock;
+                if (GATHER)
+                    tma_load_3d(c_base0 + slot * L.c_bytes, &code_map, c0, n0, e, &cfull[slot]);
+                else
+                    tma_load_2d(c_base0 + slot * L.c_bytes, &code_map, c0, n0, &cfull[slot]);
+            }
+        } else if (lane == 1 && !GATHER) {
+            // activation tile: [m_tile rows x 64] bf16, 128-byte swizzle
+            const uint32_t x_box_bytes = (uint32_t)(((p.m_tile + 15) & ~15) * 128);
+            for (int i = 0; i < nkb; ++i) {
+                const int slot = i % SAX;
+                if (i >= SAX && !mbar_wait(&axempty[slot], ((i / SAX) + 1) & 1)) { ok = false; break; }
+                mbar_expect_tx(&xfull[slot], x_box_bytes);
+                tma_load_2d(smem_base + slot * L.ax_bytes + L.a_bytes, &x_map, (kb_begin + i) * kBK,
+                            row_start, &xfull[slot]);
+            }
+        }
+        __syncwarp();
+    } else if (GATHER && warp >= kGatherWarp0) {
+        // ---------------------------------------------------------------- gathered rows
+        const int pt = threadIdx.x - kGatherWarp0 * 32;
+        const int chunks = n_mma * 8;
+        const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(p.x);
         for (int i = 0; i < nkb; ++i) {
-            const int slot = i % S;
-            if (i >= S && !mbar_wait(&empty[slot], ((i / S) + 1) & 1)) { ok = false; break; }
+            const int slot = i % SAX;
+            if (i >= SAX && !mbar_wait(&axempty[slot], ((i / SAX) + 1) & 1)) { ok = false; break; }
+            const uint32_t x_base = smem_base + slot * L.ax_bytes + L.a_bytes;
             const int kb = kb_begin + i;
-            const uint32_t a_base = smem_base + slot * L.stage_bytes;
-            const uint32_t x_base = a_base + L.a_bytes;
-            const uint32_t c_base = x_base + L.x_bytes;
-            for (int c = pt; c < total; c += kProducerThreads) {
-                if (c < code_chunks) {
-                    const int r = c / kCodeChunksPerRow;
-                    const int ch = c % kCodeChunksPerRow;
-                    const int n = n0 + r;
-                    const bool valid = n < p.N;
-                    const uint32_t* src =
-                        wexp + (valid ? (long long)n * wpr + (long long)kb * (kBK * BITS / 32) + ch * 4
-                                      : 0);
-                    cp_async_16(c_base + r * (kCodeChunksPerRow * 16) + ch * 16, src, valid ? 16u : 0u);
-                } else {
-                    const int xc = c - code_chunks;
-                    const int r = xc >> 3;
-                    const int ch = xc & 7;
-                    const int src_row = src_rows[r];
-                    const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(p.x);
-                    const void* src = xb + (src_row >= 0 ? (long long)src_row * p.K + kb * kBK + ch * 8 : 0);
-                    cp_async_16(x_base + sw128_offset(r, ch), src, src_row >= 0 ? 16u : 0u);
-                }
+            for (int c = pt; c < chunks; c += kGatherThreads) {
+                const int r = c >> 3;
+                const int ch = c & 7;
+                const int src = src_rows[r];
+                const void* g = xb + (src >= 0 ? (long long)src * p.K + kb * kBK + ch * 8 : 0);
+                cp_async_16(x_base + sw128_offset(r, ch), g, src >= 0 ? 16u : 0u);
             }
             cp_async_commit();
-            if (i >= kLag) {
-                cp_async_wait<kLag>();
+            if (i >= 1) {
+                cp_async_wait<1>();  // the previous stage has landed
                 fence_proxy_async_smem();
-                mbar_arrive(&full[(i - kLag) % S]);
+                mbar_arrive(&xfull[(i - 1) % SAX]);
             }
         }
         cp_async_wait<0>();
-        if (ok) {
+        if (ok && nkb > 0) {
             fence_proxy_async_smem();
-            for (int i = (nkb > kLag ? nkb - kLag : 0); i < nkb; ++i) mbar_arrive(&full[i % S]);
+            mbar_arrive(&xfull[(nkb - 1) % SAX]);
         }
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issue
         if (lane == 0) {
             const uint32_t idesc = umma_idesc_bf16(kTileN, (uint32_t)n_mma);
             for (int i = 0; i < nkb; ++i) {
-                const int slot = i % S;
-                const uint32_t par = (i / S) & 1;
-                if (!mbar_wait(&full[slot], par) || !mbar_wait(&afull[slot], par)) {
+                const int slot = i % SAX;
+                const uint32_t par = (i / SAX) & 1;
+                if (!mbar_wait(&xfull[slot], par) || !mbar_wait(&afull[slot], par)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t a_base = smem_base + slot * L.stage_bytes;
-                const uint32_t x_base = a_base + L.a_bytes;
+                const uint32_t a_base = smem_base + slot * L.ax_bytes;
                 const uint64_t ad = umma_desc_sw128(a_base);
-                const uint64_t bd = umma_desc_sw128(x_base);
+                const uint64_t bd = umma_desc_sw128(a_base + L.a_bytes);
 #pragma unroll
                 for (int j = 0; j < kBK / 16; ++j)
                     umma_bf16(tmem, ad + 2 * j, bd + 2 * j, idesc, (i > 0 || j > 0) ? 1u : 0u);
-                umma_commit(&empty[slot]);
+                umma_commit(&axempty[slot]);
             }
             umma_commit(accf);  // also after an abort: fires once issued MMAs finish
         }
         __syncwarp();
-    } else {
+    } else if (warp < kDequantWarps) {
         // ---------------------------------------------------------------- dequant
-        const int t = threadIdx.x;  // row of the w tile, lane of tensor memory
-        const int n = n0 + t;
+        const int t = threadIdx.x;
+        const int r = t & (kTileN - 1);   // row of the w tile
+        const int h = t >> 7;             // which 32 of the 64 k values
+        const int n = n0 + r;
         const bool row_ok = n < p.N;
-        const uint16_t* srow = sexp + (long long)n * groups;
-        const uint16_t* brow = bexp + (long long)n * groups;
+        const uint16_t* srow = p.scales + (long long)e * p.sb_expert_stride + (long long)n * groups;
+        const uint16_t* brow = p.biases + (long long)e * p.sb_expert_stride + (long long)n * groups;
         // scale/bias of the block two ahead are loaded while this one is used
         uint32_t sA = 0, bA = 0, sB = 0, bB = 0;
         if (row_ok && nkb > 0) { sA = __ldg(srow + kb_begin); bA = __ldg(brow + kb_begin); }
         if (row_ok && nkb > 1) { sB = __ldg(srow + kb_begin + 1); bB = __ldg(brow + kb_begin + 1); }
         auto stage = [&](int i, uint32_t sbits, uint32_t bbits) -> bool {
-            const int slot = i % S;
-            if (!mbar_wait(&full[slot], (i / S) & 1)) return false;
-            const uint32_t a_base = smem_base + slot * L.stage_bytes;
-            const uint32_t c_base = a_base + L.a_bytes + L.x_bytes;
-            const uint32_t a_row = a_base + (t >> 3) * 1024 + (t & 7) * 128;
+            const int cs = i % SC;
+            if (!mbar_wait(&cfull[cs], (i / SC) & 1)) return false;
+            const uint32_t c_row = c_base0 + cs * L.c_bytes + r * (kBK * BITS / 8);
+            uint4 cw[BITS / 4];
+#pragma unroll
+            for (int j = 0; j < BITS / 4; ++j) cw[j] = ld_shared_v4(c_row + (h * BITS / 4 + j) * 16);
+            mbar_arrive(&cempty[cs]);
+            const int as = i % SAX;
+            if (i >= SAX && !mbar_wait(&axempty[as], ((i / SAX) + 1) & 1)) return false;
+            const uint32_t a_row = smem_base + as * L.ax_bytes + (r >> 3) * 1024 + (r & 7) * 128;
             if (BITS == 4) {
                 const uint32_t s2 = sbits | (sbits << 16);
                 const uint32_t b2 = bbits | (bbits << 16);
+                const uint32_t wd[4] = {cw[0].x, cw[0].y, cw[0].z, cw[0].w};
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint4 cw = ld_shared_v4(c_base + t * 32 + h * 16);
-                    const uint32_t wd[4] = {cw.x, cw.y, cw.z, cw.w};
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        uint32_t o[4];
-                        dequant_word4(wd[j], s2, b2, o);
-                        const int chunk = h * 4 + j;  // 8 k per word = one 16-byte chunk
-                        st_shared_v4(a_row + ((chunk ^ (t & 7)) << 4), o[0], o[1], o[2], o[3]);
-                    }
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t o[4];
+                    dequant_word4(wd[j], s2, b2, o);
+                    const int chunk = h * 4 + j;  // 8 k per word = one 16-byte chunk
+                    st_shared_v4(a_row + ((chunk ^ (r & 7)) << 4), o[0], o[1], o[2], o[3]);
                 }
             } else {
                 const float s = bf16_bits_to_float(sbits);
                 const float b = bf16_bits_to_float(bbits);
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const uint4 cw = ld_shared_v4(c_base + t * 64 + h * 16);
-                    const uint32_t wd[4] = {cw.x, cw.y, cw.z, cw.w};
+                for (int q = 0; q < 2; ++q) {
+                    const uint32_t wd[4] = {cw[q].x, cw[q].y, cw[q].z, cw[q].w};
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
                         uint32_t o0[2], o1[2];
                         dequant_word8(wd[2 * j], s, b, o0);
                         dequant_word8(wd[2 * j + 1], s, b, o1);
-                        const int chunk = h * 2 + j;
-                        st_shared_v4(a_row + ((chunk ^ (t & 7)) << 4), o0[0], o0[1], o1[0], o1[1]);
+                        const int chunk = h * 4 + q * 2 + j;
+                        st_shared_v4(a_row + ((chunk ^ (r & 7)) << 4), o0[0], o0[1], o1[0], o1[1]);
                     }
                 }
             }
             fence_proxy_async_smem();
-            mbar_arrive(&afull[slot]);
+            mbar_arrive(&afull[as]);
             return true;
         };
         for (int i = 0; i < nkb && ok; i += 2) {
@@ -357,57 +406,64 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_tc_kernel(const QmmParams p, 
         // ---------------------------------------------------------------- epilogue
         if (ok && !mbar_wait(accf, 0)) ok = false;
         tc_fence_after();
-        const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
+        const int quarter = warp & 3;     // tensor-memory lanes 32*quarter ...
+        const int colhalf = warp >> 2;    // 16-column chunks of this parity
+        const int lane_row = quarter * 32 + lane;
+        const int ny = n0 + lane_row;
+        const bool y_ok = ny < p.N;
+        const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
         __nv_bfloat16* y = static_cast<__nv_bfloat16*>(p.y);
         if (p.splits == 1) {
-            for (int c0 = 0; c0 < n_mma; c0 += 16) {
-                uint32_t r[16];
-                tmem_ld16(taddr + c0, r);
+            for (int c0 = colhalf * 16; c0 < n_mma; c0 += 32) {
+                uint32_t v[16];
+                tmem_ld16(taddr + c0, v);
                 tmem_ld_wait();
-                if (ok && row_ok) {
+                if (ok && y_ok) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int m = c0 + j;
                         if (m < rows)
-                            y[(long long)(row_start + m) * p.N + n] =
-                                __float2bfloat16_rn(__uint_as_float(r[j]));
+                            y[(long long)(row_start + m) * p.N + ny] =
+                                __float2bfloat16_rn(__uint_as_float(v[j]));
                     }
                 }
             }
         } else {
-            // fp32 partial [m][128] of this split, then the last split to
-            // arrive sums all of them in split order
+            // fp32 partial [m][128] of this split; the last split to arrive
+            // sums all of them in split order
             const long long tile_id = blockIdx.x + (long long)gridDim.x * blockIdx.y;
             const long long tile_elems = (long long)p.m_tile * kTileN;
             float* mine = p.partial + (tile_id * p.splits + blockIdx.z) * tile_elems;
-            for (int c0 = 0; c0 < n_mma; c0 += 16) {
-                uint32_t r[16];
-                tmem_ld16(taddr + c0, r);
+            for (int c0 = colhalf * 16; c0 < n_mma; c0 += 32) {
+                uint32_t v[16];
+                tmem_ld16(taddr + c0, v);
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int m = c0 + j;
-                    if (m < rows) mine[(long long)m * kTileN + t] = __uint_as_float(r[j]);
+                    if (m < rows) mine[(long long)m * kTileN + lane_row] = __uint_as_float(v[j]);
                 }
             }
             __threadfence();
-            asm volatile("bar.sync 1, %0;" ::"n"(kDequantWarps * 32) : "memory");
-            if (t == 0) {
+            asm volatile("bar.sync 1, %0;" ::"n"(kDequantThreads) : "memory");
+            if (threadIdx.x == 0) {
                 const int prev = atomicAdd(p.counters + tile_id, 1);
                 *last_flag = (prev == p.splits - 1) ? 1 : 0;
             }
-            asm volatile("bar.sync 1, %0;" ::"n"(kDequantWarps * 32) : "memory");
+            asm volatile("bar.sync 1, %0;" ::"n"(kDequantThreads) : "memory");
             if (*last_flag) {
                 __threadfence();
                 const float* base = p.partial + tile_id * p.splits * tile_elems;
-                for (int m = 0; m < rows; ++m) {
+                const int col = threadIdx.x & (kTileN - 1);
+                const int n_out = n0 + col;
+                for (int m = threadIdx.x >> 7; m < rows; m += kDequantThreads / kTileN) {
                     float acc = 0.f;
                     for (int z = 0; z < p.splits; ++z)
-                        acc += __ldcg(base + z * tile_elems + (long long)m * kTileN + t);
-                    if (ok && row_ok)
-                        y[(long long)(row_start + m) * p.N + n] = __float2bfloat16_rn(acc);
+                        acc += __ldcg(base + z * tile_elems + (long long)m * kTileN + col);
+                    if (ok && n_out < p.N)
+                        y[(long long)(row_start + m) * p.N + n_out] = __float2bfloat16_rn(acc);
                 }
-                if (t == 0) p.counters[tile_id] = 0;  // ready for the next call
+                if (threadIdx.x == 0) p.counters[tile_id] = 0;  // ready for the next call
             }
         }
     }
@@ -418,31 +474,95 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_tc_kernel(const QmmParams p, 
     if (warp == kMmaWarp) {
         tc_fence_after();
         // make sure no MMA is still writing tensor memory (bounded wait)
-        if (!ok) (void)mbar_wait(accf, 0);
+        if (lane == 0 && !ok) (void)mbar_wait(accf, 0);
+        __syncwarp();
         tmem_dealloc(tmem, (uint32_t)p.tmem_cols);
     }
+}
+
+// ------------------------------------------------------------------ host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+template <int BITS, bool GATHER>
+cudaError_t launch_variant(const QmmParams& p, int grid_m, int max_rows, const CUtensorMap& cm,
+                           const CUtensorMap& xm, cudaStream_t stream) {
+    const SmemLayout L = make_layout(BITS, max_rows);
+    // the shared-memory opt-in is per device; do it once each
+    static bool attr_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        cudaError_t err = cudaFuncSetAttribute(qmm_tc_kernel<BITS, GATHER>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               232448);
+        if (err != cudaSuccess) return err;
+        attr_set[dev] = true;
+    }
+    const dim3 grid((p.N + kTileN - 1) / kTileN, grid_m, p.splits);
+    qmm_tc_kernel<BITS, GATHER><<<grid, kThreads, L.total, stream>>>(p, max_rows, cm, xm);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_qmm_tc(const QmmParams& p, int bits, int grid_m, int max_rows_per_tile,
                           cudaStream_t stream) {
-    const SmemLayout L = make_layout(bits, max_rows_per_tile);
-    const dim3 grid((p.N + kTileN - 1) / kTileN, grid_m, p.splits);
-    const dim3 block(kThreads);
-    cudaError_t err;
-    if (bits == 4) {
-        err = cudaFuncSetAttribute(qmm_tc_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   L.total);
-        if (err != cudaSuccess) return err;
-        qmm_tc_kernel<4><<<grid, block, L.total, stream>>>(p, max_rows_per_tile);
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const bool gather = p.tiles != nullptr;
+    // packed codes: words along K, rows n, experts
+    CUtensorMap cm, xm;
+    const cuuint64_t words = (cuuint64_t)p.K * bits / 32;
+    const cuuint32_t box_words = 64 * bits / 32;
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (gather) {
+        const cuuint64_t dims[3] = {words, (cuuint64_t)p.N, (cuuint64_t)p.E};
+        const cuuint64_t strides[2] = {words * 4, words * 4 * (cuuint64_t)p.N};
+        const cuuint32_t box[3] = {box_words, (cuuint32_t)kTileN, 1};
+        if (enc(&cm, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint32_t*>(p.w), dims, strides,
+                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        xm = cm;  // unused in the grouped form
     } else {
-        err = cudaFuncSetAttribute(qmm_tc_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   L.total);
-        if (err != cudaSuccess) return err;
-        qmm_tc_kernel<8><<<grid, block, L.total, stream>>>(p, max_rows_per_tile);
+        const cuuint64_t dims[2] = {words, (cuuint64_t)p.N};
+        const cuuint64_t strides[1] = {words * 4};
+        const cuuint32_t box[2] = {box_words, (cuuint32_t)kTileN};
+        if (enc(&cm, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(p.w), dims, strides,
+                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        const cuuint64_t xdims[2] = {(cuuint64_t)p.K, (cuuint64_t)p.M};
+        const cuuint64_t xstrides[1] = {(cuuint64_t)p.K * 2};
+        const cuuint32_t xbox[2] = {64, (cuuint32_t)((p.m_tile + 15) & ~15)};
+        if (enc(&xm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p.x), xdims, xstrides,
+                xbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
+    if (bits == 4)
+        return gather ? launch_variant<4, true>(p, grid_m, max_rows_per_tile, cm, xm, stream)
+                      : launch_variant<4, false>(p, grid_m, max_rows_per_tile, cm, xm, stream);
+    return gather ? launch_variant<8, true>(p, grid_m, max_rows_per_tile, cm, xm, stream)
+                  : launch_variant<8, false>(p, grid_m, max_rows_per_tile, cm, xm, stream);
 }
 
 }  // namespace mxq

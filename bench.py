@@ -179,20 +179,43 @@ class DenseInputs:
         self.y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
 
 
-def time_launches(fn, iters, stream):
-    """Average device time of fn() over iters launches (CUDA events on the
-    launching stream, each launch bracketed)."""
+def capture(fn, count):
+    """A CUDA graph of fn(0), ..., fn(count - 1) (launch overhead out of the
+    timed work; inputs alternate between copies by the index)."""
     import torch
 
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(iters)]
-    for i in range(iters):
-        evs[i][0].record(stream)
-        fn(i)
-        evs[i][1].record(stream)
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for i in range(count):  # warm the code path on the capture stream
+            fn(i)
+    torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
-    ts = [a.elapsed_time(b) for a, b in evs]
-    return statistics.median(ts) * 1e-3, ts
+    with torch.cuda.graph(g):
+        for i in range(count):
+            fn(i)
+    torch.cuda.synchronize()
+    return g
+
+
+def time_launches(fn, iters, stream, reps=5):
+    """Median per-launch device time of fn over graphs of ``iters`` launches
+    (CUDA events on the launching stream around each graph replay)."""
+    import torch
+
+    g = capture(fn, iters)
+    g.replay()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b) * 1e-3 / iters)
+    return statistics.median(ts), ts
 
 
 # ------------------------------------------------------------------ our arm
@@ -222,44 +245,43 @@ def run_mxq(args):
         cases.append(DenseInputs(Ws[(K, N)], 1, K, N, bits, dev, copies=2))
     step_bytes = sum(qmv_bytes(c.K, c.N, c.bits) for c in cases)
 
-    def step(i, record=None):
-        for ci, c in enumerate(cases):
-            w, s, b = c.copies[i % 2]
-            if record is not None:
-                record[ci][0].record(stream)
-            mxq.qmv(c.x[0], w, s, b, c.bits, out=c.y[0])
-            if record is not None:
-                record[ci][1].record(stream)
+    def step(i):
+        for c in cases:
+            w, s_, b = c.copies[i % 2]
+            mxq.qmv(c.x[0], w, s_, b, c.bits, out=c.y[0])
 
+    # one graph per step parity: the four launches of a step, back to back
+    graphs = [capture(lambda j, par=par: step(par), 1) for par in (0, 1)]
     for i in range(args.warmup):
-        step(i)
+        graphs[i % 2].replay()
     torch.cuda.synchronize()
     clocks = Clocks(local)
-    ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
-           for _ in cases] for _ in range(args.steps)]
+    clocks.start()
+    time.sleep(0.3)  # let the sampler start before the timed region
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
-    clocks.start()
     t0.record(stream)
     for i in range(args.steps):
-        step(i, ev[i])
+        graphs[i % 2].replay()
     t1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
     elapsed = max_over_ranks(t0.elapsed_time(t1) * 1e-3, world)
     value = step_bytes * args.steps * world / elapsed / 1e9
+
+    # per-kernel device time: each case alone, graphs of 20 launches
     per_case = []
     qmv_time = 0.0
-    for ci, c in enumerate(cases):
-        ts = [ev[i][ci][0].elapsed_time(ev[i][ci][1]) * 1e-3 for i in range(args.steps)]
-        avg = sum(ts) / len(ts)
-        qmv_time += sum(ts)
-        per_case.append({"K": c.K, "N": c.N, "bits": c.bits, "us": avg * 1e6,
-                         "GB_s": qmv_bytes(c.K, c.N, c.bits) / avg / 1e9,
-                         "frac_hbm": qmv_bytes(c.K, c.N, c.bits) / avg / 1e9 / hbm})
-    achieved = step_bytes * args.steps / qmv_time / 1e9
+    for c in cases:
+        t, _ = time_launches(
+            lambda i, c=c: mxq.qmv(c.x[0], *c.copies[i % 2], c.bits, out=c.y[0]), 20, stream)
+        qmv_time += t
+        nb = qmv_bytes(c.K, c.N, c.bits)
+        per_case.append({"K": c.K, "N": c.N, "bits": c.bits, "us": t * 1e6, "GB_s": nb / t / 1e9,
+                         "frac_hbm": nb / t / 1e9 / hbm})
+    achieved = step_bytes / qmv_time / 1e9
 
     # ---- end to end through the public API with host buffers
     pinned = []
@@ -491,10 +513,60 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_profile(args):
+    """A few plain launches of one workload, for ncu (no graphs, no timing)."""
+    import torch
+
+    import affine_bit_matmul_gb300 as mxq
+    from affine_bit_matmul_gb300 import build as _build
+
+    _build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    name = args.profile
+    launches = args.profile_launches
+    if name.startswith("qmv"):
+        K, N, bits = {"qmv4": (5120, 17408, 4), "qmv8": (5120, 17408, 8),
+                      "qmv4t": (17408, 5120, 4), "qmv8t": (17408, 5120, 8)}[name]
+        d = DenseInputs(synth.dense_weights(N, K, seed=0), 1, K, N, bits, dev, copies=2)
+        for i in range(launches):
+            mxq.qmv(d.x[0], *d.copies[i % 2], bits, out=d.y[0])
+    elif name.startswith("qmm"):
+        M, K, N, bits = {"qmm": (600, 5120, 17408, 4), "qmm128": (128, 5120, 5120, 4),
+                         "qmm8": (8, 5120, 5120, 4), "qmm32": (32, 5120, 5120, 4)}[name]
+        d = DenseInputs(synth.dense_weights(N, K, seed=0), M, K, N, bits, dev, copies=2)
+        ws = torch.empty((max(1, mxq.qmm_workspace_bytes(M, K, N, bits)),), dtype=torch.uint8,
+                         device=dev)
+        for i in range(launches):
+            mxq.qmm(d.x, *d.copies[i % 2], bits, out=d.y, workspace=ws)
+    else:
+        K, N, ident = {"gather_up": (2816, 704, False), "gather_down": (704, 2816, True)}[name]
+        E, T, top_k, bits = 128, 573, 8, 4
+        ids, src = synth.routing(T, E, top_k, seed=2)
+        B = ids.shape[0]
+        rng = np.random.default_rng(0)
+        # timing-only inputs: random codes, small scales
+        w = torch.from_numpy(rng.integers(0, 2 ** 31, size=(E, N, K // 8), dtype=np.int32)).to(dev)
+        s = torch.full((E, N, K // 64), 0.001, dtype=torch.bfloat16, device=dev)
+        b = torch.full((E, N, K // 64), -0.01, dtype=torch.bfloat16, device=dev)
+        Tx = B if ident else T
+        x = dev_bf16(synth.activations(Tx, K, seed=1), dev)
+        ids_d = torch.from_numpy(ids).to(dev)
+        src_d = None if ident else torch.from_numpy(src).to(dev)
+        for i in range(launches):
+            mxq.gather_qmm(x, w, s, b, ids_d, src_d, bits)
+    torch.cuda.synchronize()
+    print("profile run done: %s x%d" % (name, launches))
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--profile", default=None,
+                    help="plain launches of one workload for ncu: qmv4 qmv8 qmv4t qmv8t qmm "
+                         "qmm128 qmm8 qmm32 gather_up gather_down")
+    ap.add_argument("--profile-launches", type=int, default=4)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["mxq", "reference"], default="mxq")
     ap.add_argument("--no-secondary", action="store_true")
@@ -503,7 +575,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.profile:
+        run_profile(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_mxq(args)
