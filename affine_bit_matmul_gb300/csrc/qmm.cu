@@ -360,7 +360,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint4 cw[BITS / 4];
 #pragma unroll
             for (int j = 0; j < BITS / 4; ++j) cw[j] = ld_shared_v4(c_row + (h * BITS / 4 + j) * 16);
-            mbar_arrive(&cempty[cs]);
             const int as = i % SAX;
             if (i >= SAX && !mbar_wait(&axempty[as], ((i / SAX) + 1) & 1)) return false;
             const uint32_t a_row = smem_base + as * L.ax_bytes + (r >> 3) * 1024 + (r & 7) * 128;
@@ -391,6 +390,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            // release the code slot only now that the loaded words have been
+            // consumed: an arrive placed right after the shared loads let the
+            // next TMA overwrite the slot before the loads had returned
+            mbar_arrive(&cempty[cs]);
             fence_proxy_async_smem();
             mbar_arrive(&afull[as]);
             return true;
