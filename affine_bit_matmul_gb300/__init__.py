@@ -86,7 +86,7 @@ def lib():
                 "(needs nvcc) before using the library")
         L = ctypes.CDLL(LIB_PATH)
         P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
-        L.mxq_qmv.argtypes = [P, P, P, P, P, I, I, I, I, P]
+        L.mxq_qmv.argtypes = [P, P, P, P, P, I, I, I, I, P, P]
         L.mxq_qmv.restype = I
         L.mxq_qmm.argtypes = [P, P, P, P, P, I, I, I, I, I, P, Z, P, P]
         L.mxq_qmm.restype = I
@@ -168,8 +168,9 @@ def _check_weights(w, scales, biases, N, K, bits, device, lead=()):
             raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(lead) + (N, K // 64)))
 
 
-def qmv(x, w, scales, biases, bits: int, out=None, stream=None):
-    """Decode GEMV: ``y[N] = sum_k x[k] * (s*q + b)[n, k]`` (``x`` bf16 [K])."""
+def qmv(x, w, scales, biases, bits: int, out=None, dev_status=None, stream=None):
+    """Decode GEMV: ``y[N] = sum_k x[k] * (s*q + b)[n, k]`` (``x`` bf16 [K]).
+    ``dev_status`` (CUDA int32 [1]) receives DEV_TIMEOUT if a wait gave up."""
     torch = _torch()
     _require(x, "x", (torch.bfloat16,))
     if x.dim() != 1:
@@ -180,8 +181,10 @@ def qmv(x, w, scales, biases, bits: int, out=None, stream=None):
     if out is None:
         out = torch.empty((N,), dtype=torch.bfloat16, device=x.device)
     _require(out, "out", (torch.bfloat16,), x.device)
+    if dev_status is not None:
+        _require(dev_status, "dev_status", (torch.int32,), x.device)
     _check(lib().mxq_qmv(_ptr(x), _ptr(w), _ptr(scales), _ptr(biases), _ptr(out), K, N, bits, 64,
-                         _stream(stream)), "mxq_qmv")
+                         _ptr(dev_status), _stream(stream)), "mxq_qmv")
     return out
 
 

@@ -105,17 +105,21 @@ const char* mxq_status_string(mxq_status s) {
 int mxq_version(void) { return 100; }
 
 mxq_status mxq_qmv(const void* x, const uint32_t* w, const void* scales, const void* biases,
-                   void* y, int K, int N, int bits, int group_size, void* stream) {
+                   void* y, int K, int N, int bits, int group_size, int32_t* dev_status,
+                   void* stream) {
     mxq_status st = check_common(K, N, bits, group_size);
     if (st != MXQ_OK) return st;
     if (!x || !w || !scales || !biases || !y) return MXQ_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 16) || !aligned(scales, 2) ||
-        !aligned(biases, 2))
+        !aligned(biases, 2) || !aligned(dev_status, 4))
         return MXQ_ERR_MISALIGNED;
-    st = check_device(nullptr);
+    int sms = 0;
+    st = check_device(&sms);
     if (st != MXQ_OK) return st;
-    cudaError_t err = mxq::launch_qmv(x, w, scales, biases, y, K, N, bits,
-                                      static_cast<cudaStream_t>(stream));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dev_status && cudaMemsetAsync(dev_status, 0, sizeof(int32_t), s) != cudaSuccess)
+        return MXQ_ERR_CUDA;
+    cudaError_t err = mxq::launch_qmv(x, w, scales, biases, y, K, N, bits, sms, dev_status, s);
     return err == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA;
 }
 

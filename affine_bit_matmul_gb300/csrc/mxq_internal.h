@@ -42,7 +42,8 @@ struct QmmParams {
 };
 
 cudaError_t launch_qmv(const void* x, const uint32_t* w, const void* scales, const void* biases,
-                       void* y, int K, int N, int bits, cudaStream_t stream);
+                       void* y, int K, int N, int bits, int sms, int32_t* status,
+                       cudaStream_t stream);
 
 // Dense or grouped tcgen05 GEMM; grid.y = number of M tiles (dense) or an
 // upper bound on the number of tiles (grouped).

@@ -39,9 +39,10 @@ namespace {
 
 constexpr int kDequantWarps = 8;     // warps 0-7: dequant + epilogue
 constexpr int kDequantThreads = kDequantWarps * 32;
-constexpr int kTmaWarp = 8;          // lane 0: codes TMA; lane 1: activation TMA (dense)
+constexpr int kTmaWarp = 8;          // lane 0: codes TMA
 constexpr int kMmaWarp = 9;          // TMEM owner, lane 0 issues MMAs
-constexpr int kGatherWarp0 = 10;     // warps 10-11: activation rows by cp.async (grouped)
+constexpr int kGatherWarp0 = 10;     // dense: warp 10 lane 0 issues the activation TMA;
+                                     // grouped: warps 10-11 gather rows by cp.async
 constexpr int kGatherThreads = 64;
 constexpr int kThreads = 12 * 32;
 constexpr int kTileN = 128;          // rows of w per CTA (MMA M)
@@ -229,11 +230,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < SC; ++i) {
             mbar_init(&cfull[i], 1);
-            mbar_init(&cempty[i], kDequantThreads);
+            mbar_init(&cempty[i], kDequantThreads / 2);  // one group per block
         }
         for (int i = 0; i < SAX; ++i) {
             mbar_init(&xfull[i], GATHER ? kGatherThreads : 1);
-            mbar_init(&afull[i], kDequantThreads);
+            mbar_init(&afull[i], kDequantThreads / 2);
             mbar_init(&axempty[i], 1);
         }
         mbar_init(accf, 1);
@@ -276,8 +277,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else
                     tma_load_2d(c_base0 + slot * L.c_bytes, &code_map, c0, n0, &cfull[slot]);
             }
-        } else if (lane == 1 && !GATHER) {
-            // activation tile: [m_tile rows x 64] bf16, 128-byte swizzle
+        }
+        __syncwarp();
+    } else if (!GATHER && warp == kGatherWarp0) {
+        // ---------------------------------------------------------------- activation TMA
+        if (lane == 0) {
+            // [m_tile rows x 64] bf16 per block, 128-byte swizzle
             const uint32_t x_box_bytes = (uint32_t)(((p.m_tile + 15) & ~15) * 128);
             for (int i = 0; i < nkb; ++i) {
                 const int slot = i % SAX;
@@ -342,50 +347,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp < kDequantWarps) {
         // ---------------------------------------------------------------- dequant
-        const int t = threadIdx.x;
-        const int r = t & (kTileN - 1);   // row of the w tile
-        const int h = t >> 7;             // which 32 of the 64 k values
+        // two groups of four warps take alternate K blocks, so two blocks are
+        // dequantised at once; a thread handles all 64 k of one w row
+        const int r = threadIdx.x & (kTileN - 1);  // row of the w tile = TMEM lane
+        const int grp = warp >> 2;                  // K blocks with i % 2 == grp
         const int n = n0 + r;
         const bool row_ok = n < p.N;
         const uint16_t* srow = p.scales + (long long)e * p.sb_expert_stride + (long long)n * groups;
         const uint16_t* brow = p.biases + (long long)e * p.sb_expert_stride + (long long)n * groups;
-        // scale/bias of the block two ahead are loaded while this one is used
-        uint32_t sA = 0, bA = 0, sB = 0, bB = 0;
-        if (row_ok && nkb > 0) { sA = __ldg(srow + kb_begin); bA = __ldg(brow + kb_begin); }
-        if (row_ok && nkb > 1) { sB = __ldg(srow + kb_begin + 1); bB = __ldg(brow + kb_begin + 1); }
         auto stage = [&](int i, uint32_t sbits, uint32_t bbits) -> bool {
             const int cs = i % SC;
             if (!mbar_wait(&cfull[cs], (i / SC) & 1)) return false;
             const uint32_t c_row = c_base0 + cs * L.c_bytes + r * (kBK * BITS / 8);
-            uint4 cw[BITS / 4];
+            uint4 cw[BITS / 2];
 #pragma unroll
-            for (int j = 0; j < BITS / 4; ++j) cw[j] = ld_shared_v4(c_row + (h * BITS / 4 + j) * 16);
+            for (int j = 0; j < BITS / 2; ++j) cw[j] = ld_shared_v4(c_row + j * 16);
             const int as = i % SAX;
             if (i >= SAX && !mbar_wait(&axempty[as], ((i / SAX) + 1) & 1)) return false;
             const uint32_t a_row = smem_base + as * L.ax_bytes + (r >> 3) * 1024 + (r & 7) * 128;
             if (BITS == 4) {
                 const uint32_t s2 = sbits | (sbits << 16);
                 const uint32_t b2 = bbits | (bbits << 16);
-                const uint32_t wd[4] = {cw[0].x, cw[0].y, cw[0].z, cw[0].w};
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint32_t o[4];
-                    dequant_word4(wd[j], s2, b2, o);
-                    const int chunk = h * 4 + j;  // 8 k per word = one 16-byte chunk
-                    st_shared_v4(a_row + ((chunk ^ (r & 7)) << 4), o[0], o[1], o[2], o[3]);
+                for (int q = 0; q < 2; ++q) {
+                    const uint32_t wd[4] = {cw[q].x, cw[q].y, cw[q].z, cw[q].w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t o[4];
+                        dequant_word4(wd[j], s2, b2, o);
+                        const int chunk = q * 4 + j;  // 8 k per word = one 16-byte chunk
+                        st_shared_v4(a_row + ((chunk ^ (r & 7)) << 4), o[0], o[1], o[2], o[3]);
+                    }
                 }
             } else {
                 const float s = bf16_bits_to_float(sbits);
                 const float b = bf16_bits_to_float(bbits);
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
+                for (int q = 0; q < 4; ++q) {
                     const uint32_t wd[4] = {cw[q].x, cw[q].y, cw[q].z, cw[q].w};
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
                         uint32_t o0[2], o1[2];
                         dequant_word8(wd[2 * j], s, b, o0);
                         dequant_word8(wd[2 * j + 1], s, b, o1);
-                        const int chunk = h * 4 + q * 2 + j;
+                        const int chunk = q * 2 + j;
                         st_shared_v4(a_row + ((chunk ^ (r & 7)) << 4), o0[0], o0[1], o1[0], o1[1]);
                     }
                 }
@@ -398,12 +403,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&afull[as]);
             return true;
         };
-        for (int i = 0; i < nkb && ok; i += 2) {
+        // scale/bias of this group's blocks, loaded two blocks ahead
+        uint32_t sA = 0, bA = 0, sB = 0, bB = 0;
+        if (row_ok && grp < nkb) { sA = __ldg(srow + kb_begin + grp); bA = __ldg(brow + kb_begin + grp); }
+        if (row_ok && grp + 2 < nkb) { sB = __ldg(srow + kb_begin + grp + 2); bB = __ldg(brow + kb_begin + grp + 2); }
+        for (int i = grp; i < nkb && ok; i += 4) {
             ok = stage(i, sA, bA);
-            if (row_ok && i + 2 < nkb) { sA = __ldg(srow + kb_begin + i + 2); bA = __ldg(brow + kb_begin + i + 2); }
-            if (!ok || i + 1 >= nkb) break;
-            ok = stage(i + 1, sB, bB);
-            if (row_ok && i + 3 < nkb) { sB = __ldg(srow + kb_begin + i + 3); bB = __ldg(brow + kb_begin + i + 3); }
+            if (row_ok && i + 4 < nkb) { sA = __ldg(srow + kb_begin + i + 4); bA = __ldg(brow + kb_begin + i + 4); }
+            if (!ok || i + 2 >= nkb) break;
+            ok = stage(i + 2, sB, bB);
+            if (row_ok && i + 6 < nkb) { sB = __ldg(srow + kb_begin + i + 6); bB = __ldg(brow + kb_begin + i + 6); }
         }
 
         // ---------------------------------------------------------------- epilogue

@@ -4,7 +4,21 @@
 // float at every bit width; it is the HBM-bound half of decoding (Baseline
 // section: the qmv share of a decode step moves ~15 GB of codes).
 //
-// Layout of the work:
+// Two kernels share the arithmetic below.
+//
+// qmv_stream_kernel (K a multiple of 512, K <= 24576, 16-byte aligned
+// scales/biases): persistent CTAs, one per SM.  A producer thread streams
+// chunks of R consecutive rows (their codes, scales and biases are each one
+// contiguous block) into a ring of shared-memory stages with bulk async
+// copies (cp.async.bulk + mbarrier transaction counts), so ~100 KB per SM
+// stay in flight without any thread waiting on HBM.  Compute warps own one
+// 1024-wide K segment each (several warps per segment take alternate rows);
+// every lane keeps its 32 activations in registers for the whole kernel.
+//
+// qmv_generic_kernel (any other shape): direct 16-byte loads, one CTA per 16
+// rows.
+//
+// Layout of the work in both:
 //  * a lane owns 16 bytes of codes per row (32 four-bit or 16 eight-bit
 //    codes, always inside one group of 64), so a warp covers a K segment of
 //    1024 (4-bit) or 512 (8-bit) values with one coalesced 512-byte load per
@@ -98,7 +112,7 @@ __device__ __forceinline__ float dot_chunk8(const uint4 c, const float2 (&x2)[16
 }
 
 template <int BITS>
-__global__ void __launch_bounds__(kMaxWarps * 32) qmv_kernel(const __nv_bfloat16* __restrict__ x,
+__global__ void __launch_bounds__(kMaxWarps * 32) qmv_generic_kernel(const __nv_bfloat16* __restrict__ x,
                                                    const uint32_t* __restrict__ w,
                                                    const uint16_t* __restrict__ scales,
                                                    const uint16_t* __restrict__ biases,
@@ -191,25 +205,288 @@ __global__ void __launch_bounds__(kMaxWarps * 32) qmv_kernel(const __nv_bfloat16
     }
 }
 
+
+// ---------------------------------------------------------------- streaming form
+
+constexpr int kStreamStages = 6;
+constexpr int kChunkBytes = 24 * 1024;   // codes per stage, about
+constexpr int kTargetWarps = 20;
+constexpr int kMaxStreamWarps = 24;
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile(
+        "{\n\t.reg .b64 st;\n\t"
+        "mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+            smem_u32(bar)),
+        "r"(bytes)
+        : "memory");
+}
+
+// Waits unless another role already gave up; on its own timeout it raises
+// the shared abort flag so that every role winds down without waiting.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort_flag) return false;
+        if (clock64() - t0 > kWaitBudgetCycles) {
+            *abort_flag = 1;
+            return false;
+        }
+    }
+    return true;
+}
+
+struct StreamShape {
+    int nseg;        // 1024-wide K segments
+    int phases;      // warps per segment (they take alternate rows)
+    int warps;       // compute warps = nseg * phases
+    int rows;        // rows per chunk = phases * RPW
+    int row_bytes;   // codes bytes per row
+    int sb_bytes;    // scale (or bias) bytes per row
+    int stage_bytes; // codes + scales + biases, 16-byte aligned pieces
+    int nchunks;
+};
+
+// Dot of one lane's 32 codes with its 32 activations, v_k = 1 + q_k 2^-p.
+template <int BITS>
+__device__ __forceinline__ float lane_dot(uint32_t codes_addr, const float2 (&x2)[16]) {
+    if (BITS == 4) {
+        uint4 c;
+        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(c.x), "=r"(c.y), "=r"(c.z), "=r"(c.w)
+                     : "r"(codes_addr));
+        return dot_chunk4(c, x2);
+    } else {
+        uint4 c0, c1;
+        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(c0.x), "=r"(c0.y), "=r"(c0.z), "=r"(c0.w)
+                     : "r"(codes_addr));
+        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(c1.x), "=r"(c1.y), "=r"(c1.z), "=r"(c1.w)
+                     : "r"(codes_addr + 16));
+        float2 hi[16];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) hi[j] = x2[8 + j];
+        return dot_chunk8(c0, x2) + dot_chunk8(c1, hi);
+    }
+}
+
+template <int BITS, int RPW>
+__global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
+    qmv_stream_kernel(const __nv_bfloat16* __restrict__ x, const uint32_t* __restrict__ w,
+                      const uint16_t* __restrict__ scales, const uint16_t* __restrict__ biases,
+                      __nv_bfloat16* __restrict__ y, int K, int N, const StreamShape sh,
+                      int32_t* status) {
+    constexpr float kUnscale = BITS == 4 ? 128.f : 32768.f;
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ uint64_t full[kStreamStages], empty[kStreamStages];
+    __shared__ float red[2][kMaxStreamWarps * 8];
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = lane_id();
+    const uint32_t base = smem_u32(smem);
+    const int groups = K / 64;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStreamStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], sh.warps);
+        }
+        abort_flag = 0;
+        mbar_init_fence();
+    }
+    __syncthreads();
+
+    if (warp == sh.warps) {
+        // ---------------------------------------------------------------- producer
+        if (lane == 0) {
+            const char* wb = reinterpret_cast<const char*>(w);
+            const char* sbp = reinterpret_cast<const char*>(scales);
+            const char* bbp = reinterpret_cast<const char*>(biases);
+            for (int j = 0;; ++j) {
+                const int chunk = blockIdx.x + j * gridDim.x;
+                if (chunk >= sh.nchunks) break;
+                const int st = j % kStreamStages;
+                if (j >= kStreamStages &&
+                    !wait_or_abort(&empty[st], ((j / kStreamStages) + 1) & 1, &abort_flag))
+                    break;
+                const int r0 = chunk * sh.rows;
+                const int rows = min(sh.rows, N - r0);
+                const uint32_t cb = (uint32_t)(rows * sh.row_bytes);
+                const uint32_t sbb = (uint32_t)(rows * sh.sb_bytes);
+                const uint32_t dst = base + st * sh.stage_bytes;
+                expect_tx(&full[st], cb + 2 * sbb);
+                bulk_g2s(dst, wb + (long long)r0 * sh.row_bytes, cb, &full[st]);
+                bulk_g2s(dst + sh.rows * sh.row_bytes, sbp + (long long)r0 * sh.sb_bytes, sbb,
+                         &full[st]);
+                bulk_g2s(dst + sh.rows * (sh.row_bytes + sh.sb_bytes),
+                         bbp + (long long)r0 * sh.sb_bytes, sbb, &full[st]);
+            }
+        }
+        return;  // the producer takes no part in the compute warps' barrier
+    }
+
+    // -------------------------------------------------------------------- compute
+    const int seg = warp % sh.nseg;
+    const int phase = warp / sh.nseg;
+    const int k0 = seg * 1024 + lane * 32;   // this lane's 32 values
+    const bool active = k0 < K;
+    float2 x2[16];
+    float X = 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) x2[j] = make_float2(0.f, 0.f);
+    if (active) {
+        const uint4* xp = reinterpret_cast<const uint4*>(x + k0);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint4 v = __ldg(xp + c);
+            const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                x2[c * 4 + j].x = __uint_as_float(u[j] << 16);
+                x2[c * 4 + j].y = __uint_as_float(u[j] & 0xFFFF0000u);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) X += x2[j].x + x2[j].y;
+    }
+    const int g = k0 / 64;
+    const uint32_t lane_code_off = (uint32_t)(seg * 1024 + lane * 32) * BITS / 8;
+    const int compute_threads = sh.warps * 32;
+
+    for (int j = 0;; ++j) {
+        const int chunk = blockIdx.x + j * gridDim.x;
+        if (chunk >= sh.nchunks) break;
+        const int st = j % kStreamStages;
+        const bool have = wait_or_abort(&full[st], (j / kStreamStages) & 1, &abort_flag);
+        const uint32_t sbase = base + st * sh.stage_bytes;
+        const uint32_t s_off = sbase + sh.rows * sh.row_bytes;
+        const uint32_t b_off = s_off + sh.rows * sh.sb_bytes;
+        const int r0 = chunk * sh.rows;
+        const int rows = min(sh.rows, N - r0);
+        float part[RPW];
+#pragma unroll
+        for (int q = 0; q < RPW; ++q) {
+            const int r = phase + q * sh.phases;   // row within the chunk
+            part[q] = 0.f;
+            if (have && active && r < rows) {
+                const float A = lane_dot<BITS>(sbase + r * sh.row_bytes + lane_code_off, x2);
+                uint16_t sv, bv;
+                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(sv) : "r"(s_off + (r * groups + g) * 2));
+                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(bv) : "r"(b_off + (r * groups + g) * 2));
+                const float s = bf16_bits_to_float(sv), b = bf16_bits_to_float(bv);
+                part[q] = fmaf(s * kUnscale, A - X, b * X);
+            }
+        }
+        // all shared reads of this stage are consumed: hand it back
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+        // reduce-scatter over lanes: row q ends on lanes q * (32 / RPW) ...
+#pragma unroll
+        for (int half = RPW / 2, off = 16; half >= 1; half >>= 1, off >>= 1) {
+            const bool upper = (lane & off) != 0;
+#pragma unroll
+            for (int i = 0; i < half; ++i) {
+                const float send = upper ? part[i] : part[i + half];
+                const float keep = upper ? part[i + half] : part[i];
+                part[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, off);
+            }
+        }
+#pragma unroll
+        for (int off = 16 / RPW; off >= 1; off >>= 1)
+            part[0] += __shfl_xor_sync(0xFFFFFFFFu, part[0], off);
+        const int span = 32 / RPW;
+        if ((lane & (span - 1)) == 0) {
+            const int q = lane / span;
+            const int r = phase + q * sh.phases;
+            red[j & 1][r * sh.nseg + seg] = part[0];
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(compute_threads) : "memory");
+        if (threadIdx.x < rows) {
+            float acc = 0.f;
+            for (int sgi = 0; sgi < sh.nseg; ++sgi) acc += red[j & 1][threadIdx.x * sh.nseg + sgi];
+            y[r0 + threadIdx.x] = __float2bfloat16_rn(acc);
+        }
+    }
+    if (threadIdx.x == 0 && abort_flag && status) atomicOr(status, 0x8 /* MXQ_DEV_TIMEOUT */);
+}
+
+template <int BITS>
+cudaError_t launch_stream(const __nv_bfloat16* x, const uint32_t* w, const uint16_t* s,
+                          const uint16_t* b, __nv_bfloat16* y, int K, int N, int rpw,
+                          const StreamShape& sh, int grid, int32_t* status, cudaStream_t stream) {
+    const int smem = kStreamStages * sh.stage_bytes;
+    const dim3 block((sh.warps + 1) * 32);
+#define MXQ_STREAM_CASE(R)                                                                      \
+    case R: {                                                                                   \
+        cudaError_t e = cudaFuncSetAttribute(qmv_stream_kernel<BITS, R>,                        \
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem); \
+        if (e != cudaSuccess) return e;                                                         \
+        qmv_stream_kernel<BITS, R><<<grid, block, smem, stream>>>(x, w, s, b, y, K, N, sh, status); \
+        break;                                                                                  \
+    }
+    switch (rpw) {
+        MXQ_STREAM_CASE(1)
+        MXQ_STREAM_CASE(2)
+        MXQ_STREAM_CASE(4)
+        MXQ_STREAM_CASE(8)
+        default: return cudaErrorInvalidValue;
+    }
+#undef MXQ_STREAM_CASE
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_qmv(const void* x, const uint32_t* w, const void* scales, const void* biases,
-                       void* y, int K, int N, int bits, cudaStream_t stream) {
-    const int seg_k = bits == 4 ? 1024 : 512;
-    const int nseg = (K + seg_k - 1) / seg_k;
-    // as few passes over the segments as the warp limit allows, spread evenly
-    const int passes = (nseg + kMaxWarps - 1) / kMaxWarps;
-    const int warps = (nseg + passes - 1) / passes;
-    const dim3 grid((N + kRows - 1) / kRows);
-    const dim3 block(32 * warps);
+                       void* y, int K, int N, int bits, int sms, int32_t* status,
+                       cudaStream_t stream) {
     const auto* xb = static_cast<const __nv_bfloat16*>(x);
     const auto* sb = static_cast<const uint16_t*>(scales);
     const auto* bb = static_cast<const uint16_t*>(biases);
     auto* yb = static_cast<__nv_bfloat16*>(y);
+    const bool sb_aligned = (reinterpret_cast<uintptr_t>(scales) % 16 == 0) &&
+                            (reinterpret_cast<uintptr_t>(biases) % 16 == 0);
+    const int nseg = (K + 1023) / 1024;
+    if (K % 512 == 0 && nseg <= kMaxStreamWarps && sb_aligned) {
+        StreamShape sh;
+        sh.nseg = nseg;
+        sh.phases = kTargetWarps / nseg > 1 ? kTargetWarps / nseg : 1;
+        if (sh.phases * nseg > kMaxStreamWarps) sh.phases = kMaxStreamWarps / nseg;
+        sh.warps = sh.phases * nseg;
+        sh.row_bytes = K * bits / 8;
+        sh.sb_bytes = (K / 64) * 2;
+        int rpw = kChunkBytes / (sh.row_bytes * sh.phases);
+        rpw = rpw >= 8 ? 8 : rpw >= 4 ? 4 : rpw >= 2 ? 2 : 1;
+        sh.rows = sh.phases * rpw;
+        sh.stage_bytes = sh.rows * (sh.row_bytes + 2 * sh.sb_bytes);  // pieces are 16-byte multiples
+        sh.nchunks = (N + sh.rows - 1) / sh.rows;
+        const int grid = sh.nchunks < sms ? sh.nchunks : sms;
+        return bits == 4 ? launch_stream<4>(xb, w, sb, bb, yb, K, N, rpw, sh, grid, status, stream)
+                         : launch_stream<8>(xb, w, sb, bb, yb, K, N, rpw, sh, grid, status, stream);
+    }
+    const int seg_k = bits == 4 ? 1024 : 512;
+    const int nseg_g = (K + seg_k - 1) / seg_k;
+    // as few passes over the segments as the warp limit allows, spread evenly
+    const int passes = (nseg_g + kMaxWarps - 1) / kMaxWarps;
+    const int warps = (nseg_g + passes - 1) / passes;
+    const dim3 grid((N + kRows - 1) / kRows);
+    const dim3 block(32 * warps);
     if (bits == 4)
-        qmv_kernel<4><<<grid, block, 0, stream>>>(xb, w, sb, bb, yb, K, N);
+        qmv_generic_kernel<4><<<grid, block, 0, stream>>>(xb, w, sb, bb, yb, K, N);
     else
-        qmv_kernel<8><<<grid, block, 0, stream>>>(xb, w, sb, bb, yb, K, N);
+        qmv_generic_kernel<8><<<grid, block, 0, stream>>>(xb, w, sb, bb, yb, K, N);
     return cudaGetLastError();
 }
 

@@ -62,10 +62,15 @@ typedef enum {
 /* Decode GEMV, M = 1 (mlxcel issue #1536, Diagnosis item 3: the qmv kernel;
  * fp32 accumulation at every width is the fix that item names).
  *   x: bf16 [K]; y: bf16 [N]; w, scales, biases as above.
+ *   dev_status: device int32 or NULL; receives 0 or MXQ_DEV_TIMEOUT.
  * Requirements: bits in {4, 8}; group_size == 64; K > 0 and K % 64 == 0;
- * N > 0; x, w, y 16-byte aligned; scales, biases 2-byte aligned.            */
+ * N > 0; x, w, y 16-byte aligned; scales, biases 2-byte aligned.  The
+ * streaming kernel is used when K % 512 == 0, K <= 24576 and scales/biases
+ * are 16-byte aligned; other shapes take a direct-load kernel (same result
+ * rule, different summation order).                                        */
 mxq_status mxq_qmv(const void* x, const uint32_t* w, const void* scales, const void* biases,
-                   void* y, int K, int N, int bits, int group_size, void* stream);
+                   void* y, int K, int N, int bits, int group_size, int32_t* dev_status,
+                   void* stream);
 
 /* Prefill GEMM, y[M, N] = x[M, K] . w^[N, K]^T (mlxcel issue #1536, Baseline
  * profile table and Diagnosis item 4: the qmm_naive kernel).  Runs on the
@@ -75,7 +80,8 @@ mxq_status mxq_qmv(const void* x, const uint32_t* w, const void* scales, const v
  * `workspace` (device, may be NULL) lets the call split K across CTAs when M
  * and N alone give too few tiles for the GPU; pass at least
  * mxq_qmm_workspace_bytes(M, K, N, bits) bytes, 256-byte aligned, or NULL /
- * 0 to run without splitting (same result, bit for bit).  The call writes
+ * 0 to run without splitting (same result rule; the fp32 partial sums are
+ * added in a fixed order, so each configuration is deterministic).  The call writes
  * the workspace before it reads it; concurrent calls need distinct
  * workspaces.  `dev_status` (device int32, may be NULL) receives 0 or
  * MXQ_DEV_TIMEOUT.                                                         */

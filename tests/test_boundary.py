@@ -55,8 +55,8 @@ FAKE = ctypes.c_void_p(0x10000)       # 16-byte aligned, never dereferenced
 FAKE_ODD = ctypes.c_void_p(0x10008)   # 8-byte aligned only
 
 
-def qmv(L, x=FAKE, w=FAKE, s=FAKE, b=FAKE, y=FAKE, K=128, N=64, bits=4, group=64):
-    return L.mxq_qmv(x, w, s, b, y, K, N, bits, group, None)
+def qmv(L, x=FAKE, w=FAKE, s=FAKE, b=FAKE, y=FAKE, K=128, N=64, bits=4, group=64, status=None):
+    return L.mxq_qmv(x, w, s, b, y, K, N, bits, group, status, None)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -64,7 +64,7 @@ def qmv(L, x=FAKE, w=FAKE, s=FAKE, b=FAKE, y=FAKE, K=128, N=64, bits=4, group=64
     (dict(group=128), 1), (dict(K=100), 1), (dict(K=0), 1), (dict(K=-64), 1), (dict(N=0), 1),
     (dict(x=None), 1), (dict(w=None), 1), (dict(s=None), 1), (dict(b=None), 1), (dict(y=None), 1),
     (dict(x=FAKE_ODD), 2), (dict(w=FAKE_ODD), 2), (dict(y=FAKE_ODD), 2),
-    (dict(s=ctypes.c_void_p(0x10001)), 2),
+    (dict(s=ctypes.c_void_p(0x10001)), 2), (dict(status=ctypes.c_void_p(0x10002)), 2),
 ])
 def test_qmv_argument_checks(L, kw, code):
     assert qmv(L, **kw) == code

@@ -78,3 +78,39 @@ def test_qmv_closed_form_zero_scale():
     exact = (c * x.sum()).astype(np.float32)  # exact in fp32
     want = synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(exact)).astype(np.float64)
     assert np.array_equal(to_f64(y), want)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_qmv_direct_load_path(bits):
+    # scales/biases that are only 2-byte aligned, and K beyond the streaming
+    # kernel's range, take the direct-load kernel: same acceptance rule
+    import torch
+
+    case = DenseCase(1, 1536, 300, bits, seed=12, x_seed=13)
+    import affine_bit_matmul_gb300 as mxq
+
+    s_off = torch.empty(case.s_d.numel() + 1, dtype=torch.bfloat16, device="cuda")[1:]
+    b_off = torch.empty(case.b_d.numel() + 1, dtype=torch.bfloat16, device="cuda")[1:]
+    s_off.copy_(case.s_d.view(-1))
+    b_off.copy_(case.b_d.view(-1))
+    y = mxq.qmv(case.x_d[0], case.w_d, s_off.view_as(case.s_d), b_off.view_as(case.b_d), bits)
+    yr, bnd = _ref(case)
+    assert_close(to_f64(y), yr, bnd, "qmv unaligned scales bits=%d" % bits)
+    big = DenseCase(1, 32768, 96, bits, seed=14, x_seed=15)
+    y = _run(big)
+    yr, bnd = _ref(big)
+    assert_close(to_f64(y), yr, bnd, "qmv K=32768 bits=%d" % bits)
+    del torch
+
+
+def test_qmv_status_word_clear():
+    import torch
+
+    case = DenseCase(1, 5120, 1000, 4, seed=16)
+    import affine_bit_matmul_gb300 as mxq
+
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    y = mxq.qmv(case.x_d[0], case.w_d, case.s_d, case.b_d, 4, dev_status=status)
+    assert int(status.item()) == 0
+    yr, bnd = _ref(case)
+    assert_close(to_f64(y), yr, bnd, "qmv with status")
