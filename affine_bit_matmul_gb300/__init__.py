@@ -27,7 +27,6 @@ __all__ = [
     "qmv",
     "qmm",
     "gather_qmm",
-    "qmm_workspace_bytes",
     "gather_workspace_bytes",
     "MxqError",
     "DEV_BAD_EXPERT_ID",
@@ -58,7 +57,6 @@ DEV_TIMEOUT = 0x8
 EXPORTED_SYMBOLS = (
     "mxq_qmv",
     "mxq_qmm",
-    "mxq_qmm_workspace_bytes",
     "mxq_gather_qmm",
     "mxq_gather_workspace_bytes",
     "mxq_status_string",
@@ -88,10 +86,8 @@ def lib():
         P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
         L.mxq_qmv.argtypes = [P, P, P, P, P, I, I, I, I, P, P]
         L.mxq_qmv.restype = I
-        L.mxq_qmm.argtypes = [P, P, P, P, P, I, I, I, I, I, P, Z, P, P]
+        L.mxq_qmm.argtypes = [P, P, P, P, P, I, I, I, I, I, P, P]
         L.mxq_qmm.restype = I
-        L.mxq_qmm_workspace_bytes.argtypes = [I, I, I, I]
-        L.mxq_qmm_workspace_bytes.restype = Z
         L.mxq_gather_qmm.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, Z, P, P]
         L.mxq_gather_qmm.restype = I
         L.mxq_gather_workspace_bytes.argtypes = [I, I, I]
@@ -188,18 +184,11 @@ def qmv(x, w, scales, biases, bits: int, out=None, dev_status=None, stream=None)
     return out
 
 
-def qmm_workspace_bytes(M: int, K: int, N: int, bits: int) -> int:
-    return int(lib().mxq_qmm_workspace_bytes(M, K, N, bits))
-
-
-def qmm(x, w, scales, biases, bits: int, out=None, workspace=None, dev_status=None,
-        stream=None):
+def qmm(x, w, scales, biases, bits: int, out=None, dev_status=None, stream=None):
     """Prefill GEMM on the tensor cores: ``y[M, N] = x[M, K] . w^[N, K]^T``.
 
-    ``workspace`` (a CUDA uint8 tensor) lets the call split K across CTAs
-    when M and N give few tiles; ``"auto"`` allocates one of the size the
-    library asks for.  ``dev_status`` (CUDA int32 [1]) receives DEV_TIMEOUT
-    if a pipeline wait gave up.
+    ``dev_status`` (CUDA int32 [1]) receives DEV_TIMEOUT if a pipeline wait
+    gave up.
     """
     torch = _torch()
     _require(x, "x", (torch.bfloat16,))
@@ -211,18 +200,10 @@ def qmm(x, w, scales, biases, bits: int, out=None, workspace=None, dev_status=No
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     _require(out, "out", (torch.bfloat16,), x.device)
-    if isinstance(workspace, str) and workspace == "auto":
-        nbytes = qmm_workspace_bytes(M, K, N, bits)
-        workspace = torch.empty((max(nbytes, 1),), dtype=torch.uint8, device=x.device)
-    ws_bytes = 0
-    if workspace is not None:
-        _require(workspace, "workspace", (torch.uint8,), x.device)
-        ws_bytes = workspace.numel()
     if dev_status is not None:
         _require(dev_status, "dev_status", (torch.int32,), x.device)
     _check(lib().mxq_qmm(_ptr(x), _ptr(w), _ptr(scales), _ptr(biases), _ptr(out), M, K, N, bits,
-                         64, _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream)),
-           "mxq_qmm")
+                         64, _ptr(dev_status), _stream(stream)), "mxq_qmm")
     return out
 
 

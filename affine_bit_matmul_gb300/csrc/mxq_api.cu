@@ -12,6 +12,7 @@ constexpr int kTileN = 128;           // rows of w per CTA in the tensor-core ke
 constexpr int kMaxRowsPerTile = 256;  // MMA N limit
 constexpr int kGatherRowsPerTile = 128;
 constexpr int kMinKBlocksPerSplit = 8;
+constexpr int kMaxSplits = 8;             // portable cluster size
 constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
@@ -51,10 +52,10 @@ mxq_status check_common(int K, int N, int bits, int group_size) {
 }
 
 // Dense GEMM plan: M tiles of equal size (multiple of 16, at most 256) and,
-// when M and N give fewer tiles than SMs, a split of K.
+// when M and N give fewer tiles than SMs, a split of K over the CTAs of a
+// cluster (at most 8, each with at least kMinKBlocksPerSplit 64-wide blocks).
 struct DensePlan {
     int m_tiles, m_tile, tmem_cols, splits, kb_per_split;
-    size_t partial_bytes, counter_bytes;
 };
 
 DensePlan plan_dense(int M, int K, int N, int sms) {
@@ -74,12 +75,11 @@ DensePlan plan_dense(int M, int K, int N, int sms) {
         splits = sms / tiles;
         const int max_by_k = KB / kMinKBlocksPerSplit;
         if (splits > max_by_k) splits = max_by_k;
+        if (splits > kMaxSplits) splits = kMaxSplits;
         if (splits < 1) splits = 1;
     }
     pl.kb_per_split = (KB + splits - 1) / splits;
     pl.splits = (KB + pl.kb_per_split - 1) / pl.kb_per_split;  // every split gets >= 1 block
-    pl.partial_bytes = pl.splits > 1 ? (size_t)tiles * pl.splits * pl.m_tile * kTileN * 4 : 0;
-    pl.counter_bytes = pl.splits > 1 ? align_up((size_t)tiles * 4, 256) : 0;
     return pl;
 }
 
@@ -123,34 +123,21 @@ mxq_status mxq_qmv(const void* x, const uint32_t* w, const void* scales, const v
     return err == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA;
 }
 
-size_t mxq_qmm_workspace_bytes(int M, int K, int N, int bits) {
-    if (check_common(K, N, bits, 64) != MXQ_OK || M <= 0) return 0;
-    int sms = 0;
-    if (check_device(&sms) != MXQ_OK) return 0;
-    const DensePlan pl = plan_dense(M, K, N, sms);
-    return pl.partial_bytes + pl.counter_bytes;
-}
-
 mxq_status mxq_qmm(const void* x, const uint32_t* w, const void* scales, const void* biases,
-                   void* y, int M, int K, int N, int bits, int group_size, void* workspace,
-                   size_t workspace_bytes, int32_t* dev_status, void* stream) {
+                   void* y, int M, int K, int N, int bits, int group_size, int32_t* dev_status,
+                   void* stream) {
     mxq_status st = check_common(K, N, bits, group_size);
     if (st != MXQ_OK) return st;
     if (M <= 0) return MXQ_ERR_INVALID_ARG;
     if (!x || !w || !scales || !biases || !y) return MXQ_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 16) || !aligned(scales, 2) ||
-        !aligned(biases, 2) || !aligned(dev_status, 4) || !aligned(workspace, 256))
+        !aligned(biases, 2) || !aligned(dev_status, 4))
         return MXQ_ERR_MISALIGNED;
     int sms = 0;
     st = check_device(&sms);
     if (st != MXQ_OK) return st;
-    DensePlan pl = plan_dense(M, K, N, sms);
+    const DensePlan pl = plan_dense(M, K, N, sms);
     if (pl.m_tiles > 65535) return MXQ_ERR_UNSUPPORTED;  // grid.y limit
-    const size_t need = pl.partial_bytes + pl.counter_bytes;
-    if (pl.splits > 1 && (!workspace || workspace_bytes < need)) {
-        pl.splits = 1;  // no room to split K: one CTA per tile
-        pl.kb_per_split = K / 64;
-    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (dev_status && cudaMemsetAsync(dev_status, 0, sizeof(int32_t), s) != cudaSuccess)
         return MXQ_ERR_CUDA;
@@ -171,11 +158,6 @@ mxq_status mxq_qmm(const void* x, const uint32_t* w, const void* scales, const v
     p.tmem_cols = pl.tmem_cols;
     p.splits = pl.splits;
     p.kb_per_split = pl.kb_per_split;
-    if (pl.splits > 1) {
-        p.partial = static_cast<float*>(workspace);
-        p.counters = reinterpret_cast<int*>(static_cast<char*>(workspace) + pl.partial_bytes);
-        if (cudaMemsetAsync(p.counters, 0, pl.counter_bytes, s) != cudaSuccess) return MXQ_ERR_CUDA;
-    }
     cudaError_t err = mxq::launch_qmm_tc(p, bits, pl.m_tiles, pl.m_tile, s);
     return err == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA;
 }

@@ -27,15 +27,13 @@ struct QmmParams {
     const MTile* tiles;      // grouped form: tile list, or null (dense form)
     const int* tile_count;   // grouped form: number of valid tiles
     int32_t* status;         // MXQ_DEV_* bits, or null
-    float* partial;          // split-K partial sums, or null
-    int* counters;           // split-K arrival counters, or null
     int M;                   // dense form: rows of x and y
     int T;                   // grouped form: rows of x
     int E;                   // grouped form: experts
     int K, N;
     int m_tile;              // dense form: rows per M tile (multiple of 16)
     int tmem_cols;           // tensor-memory columns allocated per CTA
-    int splits;              // K splits (1 = none)
+    int splits;              // K splits = cluster size along z (1 = none)
     int kb_per_split;        // 64-wide K blocks per split
     long long w_expert_stride;   // words between experts
     long long sb_expert_stride;  // scale/bias entries between experts

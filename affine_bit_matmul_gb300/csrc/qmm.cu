@@ -48,32 +48,43 @@ constexpr int kThreads = 12 * 32;
 constexpr int kTileN = 128;          // rows of w per CTA (MMA M)
 constexpr int kBK = 64;              // K per stage (= one group)
 constexpr int kMaxRows = 256;        // activation rows per tile (MMA N <= 256)
-constexpr int kCodeStages = 8;
-constexpr int kMaxAxStages = 6;
+constexpr int kMaxSplits = 8;        // K splits per tile = cluster size (portable limit)
+constexpr int kMaxCodeStages = 8;
+constexpr int kMaxAStages = 3;
+constexpr int kMaxXStages = 16;
 constexpr int kSmemBudget = 210 * 1024;
 
 struct SmemLayout {
     int c_bytes, c_stages;    // packed-code ring
-    int a_bytes, x_bytes, ax_bytes, ax_stages;  // dequantised w + activation ring
-    int c_offset;             // code ring after the ax ring
+    int a_bytes, a_stages;    // dequantised w ring (MMA A operand)
+    int x_bytes, x_stages;    // activation ring (MMA B operand)
+    int x_offset, c_offset;   // rings: A at 0, then x, then codes
     int bar_offset, src_offset, total;
 };
 
+// The three rings are sized separately: the activation tile arrives with the
+// longest latency (it is re-read by every w tile), so it gets the deepest
+// ring the shared-memory budget allows.
 __host__ __device__ inline SmemLayout make_layout(int bits, int max_rows) {
     SmemLayout L;
     const int rows16 = (max_rows + 15) & ~15;
     L.c_bytes = kTileN * kBK * bits / 8;              // 4 KB or 8 KB
-    L.c_stages = kCodeStages;
+    L.c_stages = bits == 4 ? 8 : 6;
     L.a_bytes = kTileN * kBK * 2;                     // 16 KB
+    L.a_stages = kMaxAStages;
     L.x_bytes = (rows16 / 8) * 1024;                  // 128 B per row, 8-row atoms
-    L.ax_bytes = L.a_bytes + L.x_bytes;               // multiple of 1024
-    int s = (kSmemBudget - L.c_stages * L.c_bytes) / L.ax_bytes;
-    L.ax_stages = s > kMaxAxStages ? kMaxAxStages : (s < 2 ? 2 : s);
-    L.c_offset = L.ax_stages * L.ax_bytes;
+    int s = (kSmemBudget - L.c_stages * L.c_bytes - L.a_stages * L.a_bytes) / L.x_bytes;
+    if (s < 3) {                                      // large tiles: fewer A stages
+        L.a_stages = 2;
+        s = (kSmemBudget - L.c_stages * L.c_bytes - L.a_stages * L.a_bytes) / L.x_bytes;
+    }
+    L.x_stages = s > kMaxXStages ? kMaxXStages : (s < 2 ? 2 : s);
+    L.x_offset = L.a_stages * L.a_bytes;
+    L.c_offset = L.x_offset + L.x_stages * L.x_bytes;
     L.bar_offset = L.c_offset + L.c_stages * L.c_bytes;
-    // cfull, cempty per code stage; xfull, afull, axempty per ax stage; accf;
-    // tmem base; flag
-    L.src_offset = L.bar_offset + (2 * kCodeStages + 3 * kMaxAxStages + 1) * 8 + 16;
+    // cfull, cempty; afull, aempty; xfull, xempty; accf; tmem base; flag
+    L.src_offset = L.bar_offset +
+                   (2 * kMaxCodeStages + 2 * kMaxAStages + 2 * kMaxXStages + 1) * 8 + 16;
     L.total = L.src_offset + kMaxRows * 4 + 1024;     // + alignment slack
     return L;
 }
@@ -179,6 +190,33 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Address of the same shared-memory offset in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t map_cluster(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void flag_status(int32_t* status, int bits) {
     if (status) atomicOr(status, bits);
 }
@@ -192,13 +230,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     uint64_t* cfull = reinterpret_cast<uint64_t*>(smem + L.bar_offset);
-    uint64_t* cempty = cfull + kCodeStages;
-    uint64_t* xfull = cempty + kCodeStages;
-    uint64_t* afull = xfull + kMaxAxStages;
-    uint64_t* axempty = afull + kMaxAxStages;
-    uint64_t* accf = axempty + kMaxAxStages;
+    uint64_t* cempty = cfull + kMaxCodeStages;
+    uint64_t* afull = cempty + kMaxCodeStages;
+    uint64_t* aempty = afull + kMaxAStages;
+    uint64_t* xfull = aempty + kMaxAStages;
+    uint64_t* xempty = xfull + kMaxXStages;
+    uint64_t* accf = xempty + kMaxXStages;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
-    int* last_flag = reinterpret_cast<int*>(tmem_slot + 1);
     int* src_rows = reinterpret_cast<int*>(smem + L.src_offset);
     const uint32_t smem_base = smem_u32(smem);
     const uint32_t c_base0 = smem_base + L.c_offset;
@@ -225,20 +263,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nkb = min(KB, kb_begin + p.kb_per_split) - kb_begin;
     const int groups = p.K / 64;
     const int SC = L.c_stages;
-    const int SAX = L.ax_stages;
+    const int SA = L.a_stages;
+    const int SX = L.x_stages;
+    const uint32_t x_base0 = smem_base + L.x_offset;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < SC; ++i) {
             mbar_init(&cfull[i], 1);
             mbar_init(&cempty[i], kDequantThreads / 2);  // one group per block
         }
-        for (int i = 0; i < SAX; ++i) {
+        for (int i = 0; i < SA; ++i) {
+            mbar_init(&afull[i], kDequantThreads / 2);  // one group per block
+            mbar_init(&aempty[i], 1);
+        }
+        for (int i = 0; i < SX; ++i) {
             mbar_init(&xfull[i], GATHER ? kGatherThreads : 1);
-            mbar_init(&afull[i], kDequantThreads / 2);
-            mbar_init(&axempty[i], 1);
+            mbar_init(&xempty[i], 1);
         }
         mbar_init(accf, 1);
-        *last_flag = 0;
         mbar_init_fence();
     }
     if (GATHER) {
@@ -285,11 +327,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // [m_tile rows x 64] bf16 per block, 128-byte swizzle
             const uint32_t x_box_bytes = (uint32_t)(((p.m_tile + 15) & ~15) * 128);
             for (int i = 0; i < nkb; ++i) {
-                const int slot = i % SAX;
-                if (i >= SAX && !mbar_wait(&axempty[slot], ((i / SAX) + 1) & 1)) { ok = false; break; }
+                const int slot = i % SX;
+                if (i >= SX && !mbar_wait(&xempty[slot], ((i / SX) + 1) & 1)) { ok = false; break; }
                 mbar_expect_tx(&xfull[slot], x_box_bytes);
-                tma_load_2d(smem_base + slot * L.ax_bytes + L.a_bytes, &x_map, (kb_begin + i) * kBK,
-                            row_start, &xfull[slot]);
+                tma_load_2d(x_base0 + slot * L.x_bytes, &x_map, (kb_begin + i) * kBK, row_start,
+                            &xfull[slot]);
             }
         }
         __syncwarp();
@@ -299,9 +341,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int chunks = n_mma * 8;
         const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(p.x);
         for (int i = 0; i < nkb; ++i) {
-            const int slot = i % SAX;
-            if (i >= SAX && !mbar_wait(&axempty[slot], ((i / SAX) + 1) & 1)) { ok = false; break; }
-            const uint32_t x_base = smem_base + slot * L.ax_bytes + L.a_bytes;
+            const int slot = i % SX;
+            if (i >= SX && !mbar_wait(&xempty[slot], ((i / SX) + 1) & 1)) { ok = false; break; }
+            const uint32_t x_base = x_base0 + slot * L.x_bytes;
             const int kb = kb_begin + i;
             for (int c = pt; c < chunks; c += kGatherThreads) {
                 const int r = c >> 3;
@@ -314,33 +356,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (i >= 1) {
                 cp_async_wait<1>();  // the previous stage has landed
                 fence_proxy_async_smem();
-                mbar_arrive(&xfull[(i - 1) % SAX]);
+                mbar_arrive(&xfull[(i - 1) % SX]);
             }
         }
         cp_async_wait<0>();
         if (ok && nkb > 0) {
             fence_proxy_async_smem();
-            mbar_arrive(&xfull[(nkb - 1) % SAX]);
+            mbar_arrive(&xfull[(nkb - 1) % SX]);
         }
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issue
         if (lane == 0) {
             const uint32_t idesc = umma_idesc_bf16(kTileN, (uint32_t)n_mma);
             for (int i = 0; i < nkb; ++i) {
-                const int slot = i % SAX;
-                const uint32_t par = (i / SAX) & 1;
-                if (!mbar_wait(&xfull[slot], par) || !mbar_wait(&afull[slot], par)) {
+                const int xs = i % SX;
+                const int as = i % SA;
+                if (!mbar_wait(&xfull[xs], (i / SX) & 1) || !mbar_wait(&afull[as], (i / SA) & 1)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t a_base = smem_base + slot * L.ax_bytes;
-                const uint64_t ad = umma_desc_sw128(a_base);
-                const uint64_t bd = umma_desc_sw128(a_base + L.a_bytes);
+                const uint64_t ad = umma_desc_sw128(smem_base + as * L.a_bytes);
+                const uint64_t bd = umma_desc_sw128(x_base0 + xs * L.x_bytes);
 #pragma unroll
                 for (int j = 0; j < kBK / 16; ++j)
                     umma_bf16(tmem, ad + 2 * j, bd + 2 * j, idesc, (i > 0 || j > 0) ? 1u : 0u);
-                umma_commit(&axempty[slot]);
+                umma_commit(&aempty[as]);
+                umma_commit(&xempty[xs]);
             }
             umma_commit(accf);  // also after an abort: fires once issued MMAs finish
         }
@@ -362,9 +404,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint4 cw[BITS / 2];
 #pragma unroll
             for (int j = 0; j < BITS / 2; ++j) cw[j] = ld_shared_v4(c_row + j * 16);
-            const int as = i % SAX;
-            if (i >= SAX && !mbar_wait(&axempty[as], ((i / SAX) + 1) & 1)) return false;
-            const uint32_t a_row = smem_base + as * L.ax_bytes + (r >> 3) * 1024 + (r & 7) * 128;
+            const int as = i % SA;
+            if (i >= SA && !mbar_wait(&aempty[as], ((i / SA) + 1) & 1)) return false;
+            const uint32_t a_row = smem_base + as * L.a_bytes + (r >> 3) * 1024 + (r & 7) * 128;
             if (BITS == 4) {
                 const uint32_t s2 = sbits | (sbits << 16);
                 const uint32_t b2 = bbits | (bbits << 16);
@@ -441,43 +483,78 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         } else {
-            // fp32 partial [m][128] of this split; the last split to arrive
-            // sums all of them in split order
-            const long long tile_id = blockIdx.x + (long long)gridDim.x * blockIdx.y;
-            const long long tile_elems = (long long)p.m_tile * kTileN;
-            float* mine = p.partial + (tile_id * p.splits + blockIdx.z) * tile_elems;
+            // K split over the CTAs of a cluster: each writes its fp32 partial
+            // tile [m][128] into its own shared memory (the rings are idle now:
+            // every stage has been consumed by the MMAs)
+            const uint32_t part = smem_base;
             for (int c0 = colhalf * 16; c0 < n_mma; c0 += 32) {
                 uint32_t v[16];
                 tmem_ld16(taddr + c0, v);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int m = c0 + j;
-                    if (m < rows) mine[(long long)m * kTileN + lane_row] = __uint_as_float(v[j]);
-                }
-            }
-            __threadfence();
-            asm volatile("bar.sync 1, %0;" ::"n"(kDequantThreads) : "memory");
-            if (threadIdx.x == 0) {
-                const int prev = atomicAdd(p.counters + tile_id, 1);
-                *last_flag = (prev == p.splits - 1) ? 1 : 0;
-            }
-            asm volatile("bar.sync 1, %0;" ::"n"(kDequantThreads) : "memory");
-            if (*last_flag) {
-                __threadfence();
-                const float* base = p.partial + tile_id * p.splits * tile_elems;
-                const int col = threadIdx.x & (kTileN - 1);
-                const int n_out = n0 + col;
-                for (int m = threadIdx.x >> 7; m < rows; m += kDequantThreads / kTileN) {
-                    float acc = 0.f;
-                    for (int z = 0; z < p.splits; ++z)
-                        acc += __ldcg(base + z * tile_elems + (long long)m * kTileN + col);
-                    if (ok && n_out < p.N)
-                        y[(long long)(row_start + m) * p.N + n_out] = __float2bfloat16_rn(acc);
-                }
-                if (threadIdx.x == 0) p.counters[tile_id] = 0;  // ready for the next call
+                for (int j = 0; j < 16; ++j)
+                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(part + ((c0 + j) * kTileN + lane_row) * 4),
+                                 "r"(v[j])
+                                 : "memory");
             }
         }
+    }
+
+    if (p.splits > 1) {
+        // every thread of every CTA of the cluster takes part in both barriers
+        cluster_sync();
+        if (warp < kDequantWarps) {
+            // rank z sums rows m = z, z + S, ... over all ranks in rank order;
+            // a thread takes 4 consecutive columns of 4 rows at a time and
+            // issues all of their remote loads before adding
+            const int rank = (int)cluster_rank();
+            const int S = p.splits;
+            const int c4 = (threadIdx.x & 31) * 4;
+            const int ph = threadIdx.x >> 5;
+            const int n_out = n0 + c4;
+            __nv_bfloat16* y = static_cast<__nv_bfloat16*>(p.y);
+            const bool vec_ok = (p.N % 4 == 0) && (n_out + 3 < p.N);
+            for (int m0 = rank + S * ph; m0 < rows; m0 += S * kDequantWarps * 4) {
+                float4 acc[4];
+                float4 v[4][kMaxSplits];
+#pragma unroll
+                for (int z = 0; z < kMaxSplits; ++z) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int m = m0 + u * S * kDequantWarps;
+                        if (z < S && m < rows)
+                            v[u][z] = ld_cluster_f32x4(
+                                map_cluster(smem_base + (m * kTileN + c4) * 4, (uint32_t)z));
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int z = 0; z < kMaxSplits; ++z)
+                        if (z < S) {
+                            acc[u].x += v[u][z].x;
+                            acc[u].y += v[u][z].y;
+                            acc[u].z += v[u][z].z;
+                            acc[u].w += v[u][z].w;
+                        }
+                    const int m = m0 + u * S * kDequantWarps;
+                    if (!ok || m >= rows) continue;
+                    __nv_bfloat16* yr = y + (long long)(row_start + m) * p.N;
+                    if (vec_ok) {
+                        uint2 pk;
+                        pk.x = cvt_bf16x2(acc[u].x, acc[u].y);
+                        pk.y = cvt_bf16x2(acc[u].z, acc[u].w);
+                        *reinterpret_cast<uint2*>(yr + n_out) = pk;
+                    } else {
+                        const float a4[4] = {acc[u].x, acc[u].y, acc[u].z, acc[u].w};
+                        for (int j = 0; j < 4; ++j)
+                            if (n_out + j < p.N) yr[n_out + j] = __float2bfloat16_rn(a4[j]);
+                    }
+                }
+            }
+        }
+        cluster_sync();  // partials stay readable until every rank is done
     }
 
     if (!ok) flag_status(p.status, MXQ_DEV_TIMEOUT);
@@ -529,7 +606,20 @@ cudaError_t launch_variant(const QmmParams& p, int grid_m, int max_rows, const C
         attr_set[dev] = true;
     }
     const dim3 grid((p.N + kTileN - 1) / kTileN, grid_m, p.splits);
-    qmm_tc_kernel<BITS, GATHER><<<grid, kThreads, L.total, stream>>>(p, max_rows, cm, xm);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = L.total;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = p.splits;  // the K splits of one tile form a cluster
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t err = cudaLaunchKernelEx(&cfg, qmm_tc_kernel<BITS, GATHER>, p, max_rows, cm, xm);
+    if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
 

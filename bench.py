@@ -374,13 +374,11 @@ def secondary_measurements(mxq, dev, stream, hbm, bf16_peak, Ws):
 
     def dense_entry(name, M, K, N, bits, W, copies):
         d = DenseInputs(W, M, K, N, bits, dev, copies=copies)
-        ws = torch.empty((max(1, mxq.qmm_workspace_bytes(M, K, N, bits)),), dtype=torch.uint8,
-                         device=dev)
         if M == 1:
             fn = lambda i: mxq.qmv(d.x[0], *d.copies[i % copies], bits, out=d.y[0])  # noqa: E731
             kern = "qmv_kernel"
         else:
-            fn = lambda i: mxq.qmm(d.x, *d.copies[i % copies], bits, out=d.y, workspace=ws)  # noqa: E731
+            fn = lambda i: mxq.qmm(d.x, *d.copies[i % copies], bits, out=d.y)  # noqa: E731
             kern = "qmm_tc_kernel"
         for i in range(5):
             fn(i)
@@ -535,10 +533,8 @@ def run_profile(args):
         M, K, N, bits = {"qmm": (600, 5120, 17408, 4), "qmm128": (128, 5120, 5120, 4),
                          "qmm8": (8, 5120, 5120, 4), "qmm32": (32, 5120, 5120, 4)}[name]
         d = DenseInputs(synth.dense_weights(N, K, seed=0), M, K, N, bits, dev, copies=2)
-        ws = torch.empty((max(1, mxq.qmm_workspace_bytes(M, K, N, bits)),), dtype=torch.uint8,
-                         device=dev)
         for i in range(launches):
-            mxq.qmm(d.x, *d.copies[i % 2], bits, out=d.y, workspace=ws)
+            mxq.qmm(d.x, *d.copies[i % 2], bits, out=d.y)
     else:
         K, N, ident = {"gather_up": (2816, 704, False), "gather_down": (704, 2816, True)}[name]
         E, T, top_k, bits = 128, 573, 8, 4

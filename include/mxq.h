@@ -75,22 +75,15 @@ mxq_status mxq_qmv(const void* x, const uint32_t* w, const void* scales, const v
 /* Prefill GEMM, y[M, N] = x[M, K] . w^[N, K]^T (mlxcel issue #1536, Baseline
  * profile table and Diagnosis item 4: the qmm_naive kernel).  Runs on the
  * tcgen05 tensor cores: codes are dequantised to bf16 in shared memory and
- * accumulated in fp32 in tensor memory.
- * Requirements as for mxq_qmv plus M > 0.
- * `workspace` (device, may be NULL) lets the call split K across CTAs when M
- * and N alone give too few tiles for the GPU; pass at least
- * mxq_qmm_workspace_bytes(M, K, N, bits) bytes, 256-byte aligned, or NULL /
- * 0 to run without splitting (same result rule; the fp32 partial sums are
- * added in a fixed order, so each configuration is deterministic).  The call writes
- * the workspace before it reads it; concurrent calls need distinct
- * workspaces.  `dev_status` (device int32, may be NULL) receives 0 or
- * MXQ_DEV_TIMEOUT.                                                         */
+ * accumulated in fp32 in tensor memory.  When M and N give fewer tiles than
+ * the GPU has SMs, K is split over up to 8 CTAs of a thread-block cluster and
+ * the fp32 partials are added through distributed shared memory in a fixed
+ * order (deterministic for a given shape).
+ * Requirements as for mxq_qmv plus M > 0.  `dev_status` (device int32, may
+ * be NULL) receives 0 or MXQ_DEV_TIMEOUT.                                   */
 mxq_status mxq_qmm(const void* x, const uint32_t* w, const void* scales, const void* biases,
-                   void* y, int M, int K, int N, int bits, int group_size,
-                   void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream);
-
-/* Workspace bytes that let mxq_qmm split K for this shape (0 = never splits). */
-size_t mxq_qmm_workspace_bytes(int M, int K, int N, int bits);
+                   void* y, int M, int K, int N, int bits, int group_size, int32_t* dev_status,
+                   void* stream);
 
 /* Sorted mixture-of-experts grouped variant (mlxcel PR #1562, Summary: the
  * sorted-MoE prefill path that routes a quantized GatherQMM into a grouped

@@ -31,7 +31,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("mxq_qmv", "mxq_qmm", "mxq_gather_qmm", "mxq_gather_workspace_bytes",
-              "mxq_qmm_workspace_bytes", "mxq_status_string", "mxq_version"):
+              "mxq_status_string", "mxq_version"):
         assert n in names
 
 
@@ -70,14 +70,14 @@ def test_qmv_argument_checks(L, kw, code):
     assert qmv(L, **kw) == code
 
 
-def qmm(L, M=16, K=128, N=64, bits=4, group=64, ws=None, wsb=0, status=None, x=FAKE, y=FAKE):
-    return L.mxq_qmm(x, FAKE, FAKE, FAKE, y, M, K, N, bits, group, ws, wsb, status, None)
+def qmm(L, M=16, K=128, N=64, bits=4, group=64, status=None, x=FAKE, y=FAKE):
+    return L.mxq_qmm(x, FAKE, FAKE, FAKE, y, M, K, N, bits, group, status, None)
 
 
 @pytest.mark.parametrize("kw,code", [
     (dict(M=0), 1), (dict(M=-1), 1), (dict(bits=5), 1), (dict(group=16), 1), (dict(K=96), 1),
     (dict(x=None), 1), (dict(x=FAKE_ODD), 2), (dict(y=FAKE_ODD), 2),
-    (dict(ws=ctypes.c_void_p(0x10010), wsb=64), 2), (dict(status=ctypes.c_void_p(0x10002)), 2),
+    (dict(status=ctypes.c_void_p(0x10002)), 2),
 ])
 def test_qmm_argument_checks(L, kw, code):
     assert qmm(L, **kw) == code
