@@ -39,50 +39,54 @@ namespace {
 
 constexpr int kDequantWarps = 8;     // warps 0-7: dequant + epilogue
 constexpr int kDequantThreads = kDequantWarps * 32;
-constexpr int kTmaWarp = 8;          // lane 0: codes TMA
-constexpr int kMmaWarp = 9;          // TMEM owner, lane 0 issues MMAs
-constexpr int kGatherWarp0 = 10;     // dense: warp 10 lane 0 issues the activation TMA;
+constexpr int kCodeWarp = 8;         // codes TMA
+constexpr int kMmaWarp = 9;          // TMEM owner, MMA issue
+constexpr int kXWarp0 = 10;          // dense: activation TMA (warp 10);
                                      // grouped: warps 10-11 gather rows by cp.async
 constexpr int kGatherThreads = 64;
 constexpr int kThreads = 12 * 32;
 constexpr int kTileN = 128;          // rows of w per CTA (MMA M)
-constexpr int kBK = 64;              // K per stage (= one group)
+constexpr int kBK = 128;             // K per dequant/MMA stage: two 64-wide groups
+constexpr int kHalfK = 64;           // K per activation slot (one 128-byte swizzle atom)
 constexpr int kMaxRows = 256;        // activation rows per tile (MMA N <= 256)
 constexpr int kMaxSplits = 8;        // K splits per tile = cluster size (portable limit)
-constexpr int kMaxCodeStages = 8;
-constexpr int kMaxAStages = 3;
+constexpr int kMaxCodeStages = 4;
+constexpr int kMaxAStages = 4;
 constexpr int kMaxXStages = 16;
 constexpr int kSmemBudget = 210 * 1024;
 
 struct SmemLayout {
-    int c_bytes, c_stages;    // packed-code ring
-    int a_bytes, a_stages;    // dequantised w ring (MMA A operand)
-    int x_bytes, x_stages;    // activation ring (MMA B operand)
+    int c_bytes, c_stages;    // packed-code ring, one 128-wide K stage per slot
+    int a_bytes, a_stages;    // dequantised w ring (MMA A operand), 2 atoms per slot
+    int x_bytes, x_stages;    // activation ring (MMA B operand), one 64-wide atom per slot
     int x_offset, c_offset;   // rings: A at 0, then x, then codes
     int bar_offset, src_offset, total;
 };
 
-// The three rings are sized separately: the activation tile arrives with the
-// longest latency (it is re-read by every w tile), so it gets the deepest
-// ring the shared-memory budget allows.
+// The activation tile arrives with the longest latency (it is re-read by
+// every w tile), so after a minimal A and code ring it gets the deepest ring
+// the shared-memory budget allows; leftover room deepens the A ring.
 __host__ __device__ inline SmemLayout make_layout(int bits, int max_rows) {
     SmemLayout L;
     const int rows16 = (max_rows + 15) & ~15;
-    L.c_bytes = kTileN * kBK * bits / 8;              // 4 KB or 8 KB
-    L.c_stages = bits == 4 ? 8 : 6;
-    L.a_bytes = kTileN * kBK * 2;                     // 16 KB
-    L.a_stages = kMaxAStages;
+    L.c_bytes = kTileN * kBK * bits / 8;              // 8 KB or 16 KB
+    L.c_stages = bits == 4 ? 4 : 3;
+    L.a_bytes = kTileN * kBK * 2;                     // 32 KB
+    L.a_stages = 2;
     L.x_bytes = (rows16 / 8) * 1024;                  // 128 B per row, 8-row atoms
-    int s = (kSmemBudget - L.c_stages * L.c_bytes - L.a_stages * L.a_bytes) / L.x_bytes;
-    if (s < 3) {                                      // large tiles: fewer A stages
-        L.a_stages = 2;
-        s = (kSmemBudget - L.c_stages * L.c_bytes - L.a_stages * L.a_bytes) / L.x_bytes;
+    int room = kSmemBudget - L.c_stages * L.c_bytes - L.a_stages * L.a_bytes;
+    int sx = room / L.x_bytes;
+    sx = sx > kMaxXStages ? kMaxXStages : (sx < 2 ? 2 : sx);
+    room -= sx * L.x_bytes;
+    while (L.a_stages < kMaxAStages && room >= L.a_bytes) {
+        ++L.a_stages;
+        room -= L.a_bytes;
     }
-    L.x_stages = s > kMaxXStages ? kMaxXStages : (s < 2 ? 2 : s);
+    L.x_stages = sx;
     L.x_offset = L.a_stages * L.a_bytes;
     L.c_offset = L.x_offset + L.x_stages * L.x_bytes;
     L.bar_offset = L.c_offset + L.c_stages * L.c_bytes;
-    // cfull, cempty; afull, aempty; xfull, xempty; accf; tmem base; flag
+    // cfull, cempty; afull, aempty; xfull, xempty; accf; tmem base
     L.src_offset = L.bar_offset +
                    (2 * kMaxCodeStages + 2 * kMaxAStages + 2 * kMaxXStages + 1) * 8 + 16;
     L.total = L.src_offset + kMaxRows * 4 + 1024;     // + alignment slack
@@ -217,6 +221,59 @@ __device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t addr) {
     return v;
 }
 
+// One lane of the (converged) warp returns true.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b32 r;\n\t"
+        "elect.sync r|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
+// Tests up to three barrier phases with one round trip.
+__device__ __forceinline__ bool mbar_try_wait3(uint64_t* a, uint32_t pa, uint64_t* b, uint32_t pb,
+                                               uint64_t* c, uint32_t pc) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p, q, r;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 q, [%3], %4;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 r, [%5], %6;\n\t"
+        "and.pred p, p, q;\n\t"
+        "and.pred p, p, r;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(a)), "r"(pa), "r"(smem_u32(b)), "r"(pb), "r"(smem_u32(c)), "r"(pc)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait3(uint64_t* a, uint32_t pa, uint64_t* b, uint32_t pb,
+                                           uint64_t* c, uint32_t pc) {
+    if (mbar_try_wait3(a, pa, b, pb, c, pc)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait3(a, pa, b, pb, c, pc)) {
+        if (clock64() - t0 > kWaitBudgetCycles) return false;
+    }
+    return true;
+}
+
+// Whole-warp waits: every lane polls with its own bounded budget, then the
+// warp agrees on the outcome, so the warp stays converged for elect.sync even
+// when a wait gives up.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
+    const bool ok = mbar_wait(bar, parity);
+    return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ bool warp_wait3(uint64_t* a, uint32_t pa, uint64_t* b, uint32_t pb,
+                                           uint64_t* c, uint32_t pc) {
+    const bool ok = mbar_wait3(a, pa, b, pb, c, pc);
+    return __all_sync(0xffffffffu, ok);
+}
+
 __device__ __forceinline__ void flag_status(int32_t* status, int bits) {
     if (status) atomicOr(status, bits);
 }
@@ -239,6 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
     int* src_rows = reinterpret_cast<int*>(smem + L.src_offset);
     const uint32_t smem_base = smem_u32(smem);
+    const uint32_t x_base0 = smem_base + L.x_offset;
     const uint32_t c_base0 = smem_base + L.c_offset;
 
     const int warp = threadIdx.x >> 5;
@@ -258,22 +316,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int n_mma = (rows + 15) & ~15;
     const int n0 = blockIdx.x * kTileN;
-    const int KB = p.K / kBK;
-    const int kb_begin = blockIdx.z * p.kb_per_split;
+    const int KB = p.K / kHalfK;                       // 64-wide blocks (= groups)
+    const int kb_begin = blockIdx.z * p.kb_per_split;  // in 64-wide blocks
     const int nkb = min(KB, kb_begin + p.kb_per_split) - kb_begin;
+    const int nst = (nkb + 1) / 2;                     // 128-wide stages
     const int groups = p.K / 64;
     const int SC = L.c_stages;
     const int SA = L.a_stages;
     const int SX = L.x_stages;
-    const uint32_t x_base0 = smem_base + L.x_offset;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < SC; ++i) {
             mbar_init(&cfull[i], 1);
-            mbar_init(&cempty[i], kDequantThreads / 2);  // one group per block
+            mbar_init(&cempty[i], kDequantThreads);
         }
         for (int i = 0; i < SA; ++i) {
-            mbar_init(&afull[i], kDequantThreads / 2);  // one group per block
+            mbar_init(&afull[i], kDequantThreads);
             mbar_init(&aempty[i], 1);
         }
         for (int i = 0; i < SX; ++i) {
@@ -304,59 +362,61 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
     bool ok = true;
 
-    if (warp == kTmaWarp) {
-        // ---------------------------------------------------------------- TMA issue
-        if (lane == 0) {
-            // packed codes: [128 rows x (64*BITS/32) words] per stage
-            constexpr int kWordsPerBlock = kBK * BITS / 32;
-            for (int i = 0; i < nkb; ++i) {
-                const int slot = i % SC;
-                if (i >= SC && !mbar_wait(&cempty[slot], ((i / SC) + 1) & 1)) { ok = false; break; }
+    if (warp == kCodeWarp) {
+        // ---------------------------------------------------------------- codes TMA
+        // [128 rows x 128 k] packed codes per stage; a box that runs past K
+        // is zero-filled, a second half that belongs to the next K split is
+        // loaded but never dequantised
+        constexpr int kWordsPerStage = kBK * BITS / 32;
+        for (int s = 0; s < nst; ++s) {
+            const int slot = s % SC;
+            if (s >= SC && !warp_wait(&cempty[slot], ((s / SC) + 1) & 1)) { ok = false; break; }
+            if (elect_one()) {
                 mbar_expect_tx(&cfull[slot], (uint32_t)L.c_bytes);
-                const int c0 = (kb_begin + i) * kWordsPerBlock;
+                const int c0 = kb_begin * (kHalfK * BITS / 32) + s * kWordsPerStage;
                 if (GATHER)
                     tma_load_3d(c_base0 + slot * L.c_bytes, &code_map, c0, n0, e, &cfull[slot]);
                 else
                     tma_load_2d(c_base0 + slot * L.c_bytes, &code_map, c0, n0, &cfull[slot]);
             }
+            __syncwarp();
         }
-        __syncwarp();
-    } else if (!GATHER && warp == kGatherWarp0) {
+    } else if (!GATHER && warp == kXWarp0) {
         // ---------------------------------------------------------------- activation TMA
-        if (lane == 0) {
-            // [m_tile rows x 64] bf16 per block, 128-byte swizzle
-            const uint32_t x_box_bytes = (uint32_t)(((p.m_tile + 15) & ~15) * 128);
-            for (int i = 0; i < nkb; ++i) {
-                const int slot = i % SX;
-                if (i >= SX && !mbar_wait(&xempty[slot], ((i / SX) + 1) & 1)) { ok = false; break; }
+        // one [m_tile rows x 64] bf16 box (128-byte swizzle) per 64-wide block
+        const uint32_t x_box_bytes = (uint32_t)(((p.m_tile + 15) & ~15) * 128);
+        for (int q = 0; q < nkb; ++q) {
+            const int slot = q % SX;
+            if (q >= SX && !warp_wait(&xempty[slot], ((q / SX) + 1) & 1)) { ok = false; break; }
+            if (elect_one()) {
                 mbar_expect_tx(&xfull[slot], x_box_bytes);
-                tma_load_2d(x_base0 + slot * L.x_bytes, &x_map, (kb_begin + i) * kBK, row_start,
+                tma_load_2d(x_base0 + slot * L.x_bytes, &x_map, (kb_begin + q) * kHalfK, row_start,
                             &xfull[slot]);
             }
+            __syncwarp();
         }
-        __syncwarp();
-    } else if (GATHER && warp >= kGatherWarp0) {
+    } else if (GATHER && warp >= kXWarp0) {
         // ---------------------------------------------------------------- gathered rows
-        const int pt = threadIdx.x - kGatherWarp0 * 32;
+        const int pt = threadIdx.x - kXWarp0 * 32;
         const int chunks = n_mma * 8;
         const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(p.x);
-        for (int i = 0; i < nkb; ++i) {
-            const int slot = i % SX;
-            if (i >= SX && !mbar_wait(&xempty[slot], ((i / SX) + 1) & 1)) { ok = false; break; }
+        for (int q = 0; q < nkb; ++q) {
+            const int slot = q % SX;
+            if (q >= SX && !mbar_wait(&xempty[slot], ((q / SX) + 1) & 1)) { ok = false; break; }
             const uint32_t x_base = x_base0 + slot * L.x_bytes;
-            const int kb = kb_begin + i;
+            const int kb = kb_begin + q;
             for (int c = pt; c < chunks; c += kGatherThreads) {
                 const int r = c >> 3;
                 const int ch = c & 7;
                 const int src = src_rows[r];
-                const void* g = xb + (src >= 0 ? (long long)src * p.K + kb * kBK + ch * 8 : 0);
+                const void* g = xb + (src >= 0 ? (long long)src * p.K + kb * kHalfK + ch * 8 : 0);
                 cp_async_16(x_base + sw128_offset(r, ch), g, src >= 0 ? 16u : 0u);
             }
             cp_async_commit();
-            if (i >= 1) {
-                cp_async_wait<1>();  // the previous stage has landed
+            if (q >= 1) {
+                cp_async_wait<1>();  // the previous block has landed
                 fence_proxy_async_smem();
-                mbar_arrive(&xfull[(i - 1) % SX]);
+                mbar_arrive(&xfull[(q - 1) % SX]);
             }
         }
         cp_async_wait<0>();
@@ -366,74 +426,92 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issue
-        if (lane == 0) {
-            const uint32_t idesc = umma_idesc_bf16(kTileN, (uint32_t)n_mma);
-            for (int i = 0; i < nkb; ++i) {
-                const int xs = i % SX;
-                const int as = i % SA;
-                if (!mbar_wait(&xfull[xs], (i / SX) & 1) || !mbar_wait(&afull[as], (i / SA) & 1)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint64_t ad = umma_desc_sw128(smem_base + as * L.a_bytes);
-                const uint64_t bd = umma_desc_sw128(x_base0 + xs * L.x_bytes);
-#pragma unroll
-                for (int j = 0; j < kBK / 16; ++j)
-                    umma_bf16(tmem, ad + 2 * j, bd + 2 * j, idesc, (i > 0 || j > 0) ? 1u : 0u);
-                umma_commit(&aempty[as]);
-                umma_commit(&xempty[xs]);
+        // the whole warp waits (three barriers per stage in one round trip);
+        // one elected lane issues the MMAs and the commits
+        const uint32_t idesc = umma_idesc_bf16(kTileN, (uint32_t)n_mma);
+        for (int s = 0; s < nst; ++s) {
+            const int as = s % SA;
+            const int q0 = 2 * s, q1 = 2 * s + 1;
+            const bool two = q1 < nkb;
+            const int x0 = q0 % SX, x1 = two ? q1 % SX : x0;
+            const uint32_t p1 = two ? (uint32_t)((q1 / SX) & 1) : (uint32_t)((q0 / SX) & 1);
+            if (!warp_wait3(&afull[as], (s / SA) & 1, &xfull[x0], (q0 / SX) & 1, &xfull[x1], p1)) {
+                ok = false;
+                break;
             }
-            umma_commit(accf);  // also after an abort: fires once issued MMAs finish
+            tc_fence_after();
+            if (elect_one()) {
+                const uint32_t a_base = smem_base + as * L.a_bytes;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    if (h == 1 && !two) break;
+                    const uint64_t ad = umma_desc_sw128(a_base + h * (L.a_bytes / 2));
+                    const uint64_t bd = umma_desc_sw128(x_base0 + (h ? x1 : x0) * L.x_bytes);
+#pragma unroll
+                    for (int j = 0; j < kHalfK / 16; ++j)
+                        umma_bf16(tmem, ad + 2 * j, bd + 2 * j, idesc,
+                                  (s > 0 || h > 0 || j > 0) ? 1u : 0u);
+                }
+                umma_commit(&aempty[as]);
+                umma_commit(&xempty[x0]);
+                if (two) umma_commit(&xempty[x1]);
+            }
+            __syncwarp();
         }
+        if (elect_one()) umma_commit(accf);  // also after an abort: fires once issued MMAs finish
         __syncwarp();
     } else if (warp < kDequantWarps) {
         // ---------------------------------------------------------------- dequant
-        // two groups of four warps take alternate K blocks, so two blocks are
-        // dequantised at once; a thread handles all 64 k of one w row
-        const int r = threadIdx.x & (kTileN - 1);  // row of the w tile = TMEM lane
-        const int grp = warp >> 2;                  // K blocks with i % 2 == grp
+        // thread (r, h): w row r of the tile, 64-wide half h of every stage
+        const int r = threadIdx.x & (kTileN - 1);   // = TMEM lane of the row
+        const int h = warp >> 2;
         const int n = n0 + r;
         const bool row_ok = n < p.N;
         const uint16_t* srow = p.scales + (long long)e * p.sb_expert_stride + (long long)n * groups;
         const uint16_t* brow = p.biases + (long long)e * p.sb_expert_stride + (long long)n * groups;
-        auto stage = [&](int i, uint32_t sbits, uint32_t bbits) -> bool {
-            const int cs = i % SC;
-            if (!mbar_wait(&cfull[cs], (i / SC) & 1)) return false;
-            const uint32_t c_row = c_base0 + cs * L.c_bytes + r * (kBK * BITS / 8);
+        auto stage = [&](int s, uint32_t sbits, uint32_t bbits) -> bool {
+            const bool valid = 2 * s + h < nkb;
+            const int cs = s % SC;
+            if (!mbar_wait(&cfull[cs], (s / SC) & 1)) return false;
+            constexpr int kRowBytes = kBK * BITS / 8;        // codes of one row per stage
+            const uint32_t c_row = c_base0 + cs * L.c_bytes + r * kRowBytes + h * (kRowBytes / 2);
             uint4 cw[BITS / 2];
 #pragma unroll
             for (int j = 0; j < BITS / 2; ++j) cw[j] = ld_shared_v4(c_row + j * 16);
-            const int as = i % SA;
-            if (i >= SA && !mbar_wait(&aempty[as], ((i / SA) + 1) & 1)) return false;
-            const uint32_t a_row = smem_base + as * L.a_bytes + (r >> 3) * 1024 + (r & 7) * 128;
-            if (BITS == 4) {
-                const uint32_t s2 = sbits | (sbits << 16);
-                const uint32_t b2 = bbits | (bbits << 16);
+            const int as = s % SA;
+            if (s >= SA && !mbar_wait(&aempty[as], ((s / SA) + 1) & 1)) return false;
+            const uint32_t a_row = smem_base + as * L.a_bytes + h * (L.a_bytes / 2) +
+                                   (r >> 3) * 1024 + (r & 7) * 128;
+            if (valid) {
+                if (BITS == 4) {
+                    const uint32_t s2 = sbits | (sbits << 16);
+                    const uint32_t b2 = bbits | (bbits << 16);
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const uint32_t wd[4] = {cw[q].x, cw[q].y, cw[q].z, cw[q].w};
+                    for (int q = 0; q < 2; ++q) {
+                        const uint32_t wd[4] = {cw[q].x, cw[q].y, cw[q].z, cw[q].w};
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        uint32_t o[4];
-                        dequant_word4(wd[j], s2, b2, o);
-                        const int chunk = q * 4 + j;  // 8 k per word = one 16-byte chunk
-                        st_shared_v4(a_row + ((chunk ^ (r & 7)) << 4), o[0], o[1], o[2], o[3]);
+                        for (int j = 0; j < 4; ++j) {
+                            uint32_t o[4];
+                            dequant_word4(wd[j], s2, b2, o);
+                            const int chunk = q * 4 + j;  // 8 k per word = one 16-byte chunk
+                            st_shared_v4(a_row + ((chunk ^ (r & 7)) << 4), o[0], o[1], o[2], o[3]);
+                        }
                     }
-                }
-            } else {
-                const float s = bf16_bits_to_float(sbits);
-                const float b = bf16_bits_to_float(bbits);
+                } else {
+                    const float sf = bf16_bits_to_float(sbits);
+                    const float bf = bf16_bits_to_float(bbits);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint32_t wd[4] = {cw[q].x, cw[q].y, cw[q].z, cw[q].w};
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t wd[4] = {cw[q].x, cw[q].y, cw[q].z, cw[q].w};
 #pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        uint32_t o0[2], o1[2];
-                        dequant_word8(wd[2 * j], s, b, o0);
-                        dequant_word8(wd[2 * j + 1], s, b, o1);
-                        const int chunk = q * 2 + j;
-                        st_shared_v4(a_row + ((chunk ^ (r & 7)) << 4), o0[0], o0[1], o1[0], o1[1]);
+                        for (int j = 0; j < 2; ++j) {
+                            uint32_t o0[2], o1[2];
+                            dequant_word8(wd[2 * j], sf, bf, o0);
+                            dequant_word8(wd[2 * j + 1], sf, bf, o1);
+                            const int chunk = q * 2 + j;
+                            st_shared_v4(a_row + ((chunk ^ (r & 7)) << 4), o0[0], o0[1], o1[0],
+                                         o1[1]);
+                        }
                     }
                 }
             }
@@ -445,16 +523,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&afull[as]);
             return true;
         };
-        // scale/bias of this group's blocks, loaded two blocks ahead
+        // scale/bias of this thread's block, two stages ahead
+        auto sb_load = [&](int s, uint32_t& sv, uint32_t& bv) {
+            const int b = 2 * s + h;
+            if (row_ok && s < nst && b < nkb) {
+                sv = __ldg(srow + kb_begin + b);
+                bv = __ldg(brow + kb_begin + b);
+            }
+        };
         uint32_t sA = 0, bA = 0, sB = 0, bB = 0;
-        if (row_ok && grp < nkb) { sA = __ldg(srow + kb_begin + grp); bA = __ldg(brow + kb_begin + grp); }
-        if (row_ok && grp + 2 < nkb) { sB = __ldg(srow + kb_begin + grp + 2); bB = __ldg(brow + kb_begin + grp + 2); }
-        for (int i = grp; i < nkb && ok; i += 4) {
-            ok = stage(i, sA, bA);
-            if (row_ok && i + 4 < nkb) { sA = __ldg(srow + kb_begin + i + 4); bA = __ldg(brow + kb_begin + i + 4); }
-            if (!ok || i + 2 >= nkb) break;
-            ok = stage(i + 2, sB, bB);
-            if (row_ok && i + 6 < nkb) { sB = __ldg(srow + kb_begin + i + 6); bB = __ldg(brow + kb_begin + i + 6); }
+        sb_load(0, sA, bA);
+        sb_load(1, sB, bB);
+        for (int s = 0; s < nst && ok; s += 2) {
+            ok = stage(s, sA, bA);
+            sb_load(s + 2, sA, bA);
+            if (!ok || s + 1 >= nst) break;
+            ok = stage(s + 1, sB, bB);
+            sb_load(s + 3, sB, bB);
         }
 
         // ---------------------------------------------------------------- epilogue
@@ -633,7 +718,7 @@ cudaError_t launch_qmm_tc(const QmmParams& p, int bits, int grid_m, int max_rows
     // packed codes: words along K, rows n, experts
     CUtensorMap cm, xm;
     const cuuint64_t words = (cuuint64_t)p.K * bits / 32;
-    const cuuint32_t box_words = 64 * bits / 32;
+    const cuuint32_t box_words = kBK * bits / 32;   // 128 k per stage
     const cuuint32_t estr[3] = {1, 1, 1};
     if (gather) {
         const cuuint64_t dims[3] = {words, (cuuint64_t)p.N, (cuuint64_t)p.E};
@@ -654,7 +739,7 @@ cudaError_t launch_qmm_tc(const QmmParams& p, int bits, int grid_m, int max_rows
             return cudaErrorInvalidValue;
         const cuuint64_t xdims[2] = {(cuuint64_t)p.K, (cuuint64_t)p.M};
         const cuuint64_t xstrides[1] = {(cuuint64_t)p.K * 2};
-        const cuuint32_t xbox[2] = {64, (cuuint32_t)((p.m_tile + 15) & ~15)};
+        const cuuint32_t xbox[2] = {(cuuint32_t)kHalfK, (cuuint32_t)((p.m_tile + 15) & ~15)};
         if (enc(&xm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p.x), xdims, xstrides,
                 xbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
