@@ -274,6 +274,20 @@ __device__ __forceinline__ bool warp_wait3(uint64_t* a, uint32_t pa, uint64_t* b
     return __all_sync(0xffffffffu, ok);
 }
 
+// cp.async.wait_group with a run-time count (0..7).
+__device__ __forceinline__ void cp_async_wait_n(int n) {
+    switch (n) {
+        case 0: cp_async_wait<0>(); break;
+        case 1: cp_async_wait<1>(); break;
+        case 2: cp_async_wait<2>(); break;
+        case 3: cp_async_wait<3>(); break;
+        case 4: cp_async_wait<4>(); break;
+        case 5: cp_async_wait<5>(); break;
+        case 6: cp_async_wait<6>(); break;
+        default: cp_async_wait<7>(); break;
+    }
+}
+
 __device__ __forceinline__ void flag_status(int32_t* status, int bits) {
     if (status) atomicOr(status, bits);
 }
@@ -399,6 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------------- gathered rows
         const int pt = threadIdx.x - kXWarp0 * 32;
         const int chunks = n_mma * 8;
+        const int lag = SX - 1 < 7 ? SX - 1 : 7;  // the ring must hold lag + 1 blocks
         const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(p.x);
         for (int q = 0; q < nkb; ++q) {
             const int slot = q % SX;
@@ -413,16 +428,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 cp_async_16(x_base + sw128_offset(r, ch), g, src >= 0 ? 16u : 0u);
             }
             cp_async_commit();
-            if (q >= 1) {
-                cp_async_wait<1>();  // the previous block has landed
+            // keep up to `lag` blocks in flight; signal the oldest once landed
+            if (q >= lag) {
+                cp_async_wait_n(lag);
                 fence_proxy_async_smem();
-                mbar_arrive(&xfull[(q - 1) % SX]);
+                mbar_arrive(&xfull[(q - lag) % SX]);
             }
         }
         cp_async_wait<0>();
-        if (ok && nkb > 0) {
+        if (ok) {
             fence_proxy_async_smem();
-            mbar_arrive(&xfull[(nkb - 1) % SX]);
+            for (int q = (nkb > lag ? nkb - lag : 0); q < nkb; ++q) mbar_arrive(&xfull[q % SX]);
         }
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issue
