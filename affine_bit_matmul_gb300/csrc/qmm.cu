@@ -413,7 +413,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------------- gathered rows
         const int pt = threadIdx.x - kXWarp0 * 32;
         const int chunks = n_mma * 8;
-        const int lag = SX - 1 < 7 ? SX - 1 : 7;  // the ring must hold lag + 1 blocks
+        // blocks kept in flight before signalling: the MMA consumes blocks in
+        // pairs, so block q - SX + 1 must be signalled before block q waits
+        // for its slot; hence lag <= SX - 2
+        const int lag = SX - 2 < 0 ? 0 : (SX - 2 < 7 ? SX - 2 : 7);
         const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(p.x);
         for (int q = 0; q < nkb; ++q) {
             const int slot = q % SX;
