@@ -90,7 +90,7 @@ def lib():
         L.mxq_qmm.restype = I
         L.mxq_gather_qmm.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, Z, P, P]
         L.mxq_gather_qmm.restype = I
-        L.mxq_gather_workspace_bytes.argtypes = [I, I, I]
+        L.mxq_gather_workspace_bytes.argtypes = [I, I, I, I]
         L.mxq_gather_workspace_bytes.restype = Z
         L.mxq_status_string.argtypes = [I]
         L.mxq_status_string.restype = ctypes.c_char_p
@@ -207,8 +207,9 @@ def qmm(x, w, scales, biases, bits: int, out=None, dev_status=None, stream=None)
     return out
 
 
-def gather_workspace_bytes(B: int, E: int, N: int) -> int:
-    return int(lib().mxq_gather_workspace_bytes(B, E, N))
+def gather_workspace_bytes(B: int, E: int, K: int, N: int) -> int:
+    """Workspace bytes for gather_qmm; pass K = 0 when row_src is None."""
+    return int(lib().mxq_gather_workspace_bytes(B, E, K, N))
 
 
 def gather_qmm(x, w, scales, biases, expert_ids, row_src, bits: int, out=None, workspace=None,
@@ -239,8 +240,8 @@ def gather_qmm(x, w, scales, biases, expert_ids, row_src, bits: int, out=None, w
         out = torch.empty((B, N), dtype=torch.bfloat16, device=x.device)
     _require(out, "out", (torch.bfloat16,), x.device)
     if workspace is None:
-        workspace = torch.empty((gather_workspace_bytes(B, E, N),), dtype=torch.uint8,
-                                device=x.device)
+        workspace = torch.empty((gather_workspace_bytes(B, E, K if row_src is not None else 0, N),),
+                                dtype=torch.uint8, device=x.device)
     _require(workspace, "workspace", (torch.uint8,), x.device)
     if dev_status is not None:
         _require(dev_status, "dev_status", (torch.int32,), x.device)

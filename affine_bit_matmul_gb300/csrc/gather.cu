@@ -10,6 +10,10 @@
 //      size, and writes the tile list with a block-wide exclusive scan;
 //   4. zeroes the y rows no tile covers (ids outside [0, E)).
 // Unsorted ids make the call produce an all-zero y and no tiles.
+//
+// When the activation rows are routed through row_src, a second kernel
+// copies them into sorted order (x_sorted[r] = x[row_src[r]], zero for an
+// invalid source) so that the GEMM reads every activation tile with TMA.
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -113,7 +117,32 @@ __global__ void __launch_bounds__(kPrepThreads) gather_prepass_kernel(
     zero_rows(y, seg_last, B, N);
 }
 
+// One warp per sorted row, 16-byte copies.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x,
+                                                          const int32_t* __restrict__ row_src,
+                                                          int T, int B, int K,
+                                                          uint4* __restrict__ x_sorted) {
+    const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (r >= B) return;
+    const int chunks = K / 8;  // 16-byte chunks per row (K % 64 == 0)
+    const int src = row_src[r];
+    uint4* dst = x_sorted + (long long)r * chunks;
+    if (src < 0 || src >= T) {
+        for (int c = threadIdx.x & 31; c < chunks; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
+        return;
+    }
+    const uint4* s = x + (long long)src * chunks;
+    for (int c = threadIdx.x & 31; c < chunks; c += 32) dst[c] = __ldg(s + c);
+}
+
 }  // namespace
+
+cudaError_t launch_gather_rows(const void* x, const int32_t* row_src, int T, int B, int K,
+                               void* x_sorted, cudaStream_t stream) {
+    gather_rows_kernel<<<(B + 7) / 8, 256, 0, stream>>>(static_cast<const uint4*>(x), row_src, T,
+                                                        B, K, static_cast<uint4*>(x_sorted));
+    return cudaGetLastError();
+}
 
 cudaError_t launch_gather_prepass(const int32_t* expert_ids, const int32_t* row_src, int T,
                                   int B, int E, int N, int rows_per_tile, MTile* tiles,

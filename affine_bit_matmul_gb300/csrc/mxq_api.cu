@@ -85,6 +85,11 @@ DensePlan plan_dense(int M, int K, int N, int sms) {
 
 size_t gather_max_tiles(int B, int E) { return (size_t)B / kGatherRowsPerTile + (size_t)E + 1; }
 
+// Tile records plus the tile count, 256-byte aligned.
+size_t gather_table_bytes(int B, int E) {
+    return align_up(gather_max_tiles(B, E) * sizeof(mxq::MTile), 256) + 256;
+}
+
 }  // namespace
 
 extern "C" {
@@ -154,6 +159,8 @@ mxq_status mxq_qmm(const void* x, const uint32_t* w, const void* scales, const v
     p.E = 1;
     p.K = K;
     p.N = N;
+    p.x_rows = M;
+    p.x_box_rows = pl.m_tile;
     p.m_tile = pl.m_tile;
     p.tmem_cols = pl.tmem_cols;
     p.splits = pl.splits;
@@ -162,10 +169,11 @@ mxq_status mxq_qmm(const void* x, const uint32_t* w, const void* scales, const v
     return err == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA;
 }
 
-size_t mxq_gather_workspace_bytes(int B, int E, int N) {
+size_t mxq_gather_workspace_bytes(int B, int E, int K, int N) {
     (void)N;
-    if (B <= 0 || E <= 0) return 0;
-    return align_up(gather_max_tiles(B, E) * sizeof(mxq::MTile), 256) + 256;
+    if (B <= 0 || E <= 0 || K < 0) return 0;
+    // tile table + count, then room for the activation rows in sorted order
+    return gather_table_bytes(B, E) + align_up((size_t)B * K * 2, 256);
 }
 
 mxq_status mxq_gather_qmm(const void* x, const uint32_t* w, const void* scales,
@@ -182,8 +190,8 @@ mxq_status mxq_gather_qmm(const void* x, const uint32_t* w, const void* scales,
         !aligned(biases, 2) || !aligned(expert_ids, 4) || !aligned(row_src, 4) ||
         !aligned(dev_status, 4) || !aligned(workspace, 256))
         return MXQ_ERR_MISALIGNED;
-    if (!workspace || workspace_bytes < mxq_gather_workspace_bytes(B, E, N))
-        return MXQ_ERR_WORKSPACE;
+    const size_t need = row_src ? mxq_gather_workspace_bytes(B, E, K, N) : gather_table_bytes(B, E);
+    if (!workspace || workspace_bytes < need) return MXQ_ERR_WORKSPACE;
     const size_t max_tiles = gather_max_tiles(B, E);
     if (max_tiles > 65535) return MXQ_ERR_UNSUPPORTED;  // grid.y limit
     st = check_device(nullptr);
@@ -196,17 +204,25 @@ mxq_status mxq_gather_qmm(const void* x, const uint32_t* w, const void* scales,
                                                  kGatherRowsPerTile, tiles, tile_count, y,
                                                  dev_status, s);
     if (err != cudaSuccess) return MXQ_ERR_CUDA;
+    const void* xa = x;
+    if (row_src) {
+        void* x_sorted = static_cast<char*>(workspace) + gather_table_bytes(B, E);
+        err = mxq::launch_gather_rows(x, row_src, T, B, K, x_sorted, s);
+        if (err != cudaSuccess) return MXQ_ERR_CUDA;
+        xa = x_sorted;
+    }
     mxq::QmmParams p;
     std::memset(&p, 0, sizeof p);
-    p.x = x;
+    p.x = xa;
     p.w = w;
     p.scales = static_cast<const uint16_t*>(scales);
     p.biases = static_cast<const uint16_t*>(biases);
     p.y = y;
-    p.row_src = row_src;
     p.tiles = tiles;
     p.tile_count = tile_count;
     p.status = dev_status;
+    p.x_rows = B;
+    p.x_box_rows = 16;
     p.M = B;
     p.T = T;
     p.E = E;

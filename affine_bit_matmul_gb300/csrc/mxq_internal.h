@@ -23,10 +23,11 @@ struct QmmParams {
     const uint16_t* scales;  // bf16 [E, N, K/64]
     const uint16_t* biases;  // bf16 [E, N, K/64]
     void* y;                 // bf16 [rows, N]
-    const int32_t* row_src;  // grouped form: x row of each sorted row, or null
     const MTile* tiles;      // grouped form: tile list, or null (dense form)
     const int* tile_count;   // grouped form: number of valid tiles
     int32_t* status;         // MXQ_DEV_* bits, or null
+    int x_rows;              // rows of the activation matrix the TMA reads
+    int x_box_rows;          // rows per activation TMA box (multiple of 8, <= 256)
     int M;                   // dense form: rows of x and y
     int T;                   // grouped form: rows of x
     int E;                   // grouped form: experts
@@ -50,9 +51,13 @@ cudaError_t launch_qmm_tc(const QmmParams& p, int bits, int grid_m, int max_rows
 
 // Grouped form, step 1: validate ids, find each expert's rows, build the
 // tile list, zero the y rows that no tile covers.
+// Step 2 (when row_src is given): copy the activation rows into sorted order.
 cudaError_t launch_gather_prepass(const int32_t* expert_ids, const int32_t* row_src, int T,
                                   int B, int E, int N, int rows_per_tile, MTile* tiles,
                                   int* tile_count, void* y, int32_t* status,
                                   cudaStream_t stream);
+
+cudaError_t launch_gather_rows(const void* x, const int32_t* row_src, int T, int B, int K,
+                               void* x_sorted, cudaStream_t stream);
 
 }  // namespace mxq

@@ -9,18 +9,19 @@
 //  * swap-AB: the MMA's M side is 128 rows of w (output columns n), its N side
 //    is a tile of up to 256 activation rows, so a 36-row expert segment or a
 //    single decode row still fills the 128-row tensor-core tile;
-//  * per 64-wide K block (one quantisation group) a TMA copy brings the
-//    packed codes of the 128 w rows into a deep ring of small stages; the
-//    activation tile comes by TMA with 128-byte swizzle (dense form) or is
-//    gathered row by row through row_src with cp.async (grouped form);
-//  * eight dequant warps (two threads per w row) turn codes into bf16
-//    w^ = s*q + b (one rounding) and write it straight into the
-//    128-byte-swizzled K-major layout the tensor core reads;
-//  * one thread issues four 128xNx16 tcgen05.mma per block into fp32 tensor
-//    memory; the dequant warps then read the accumulators back with
-//    tcgen05.ld and store bf16 (or, with K split across CTAs, fp32 partials
-//    that the last CTA of the tile sums in a fixed order: the result does not
-//    depend on timing).
+//  * per 128-wide K stage (two quantisation groups) a TMA copy brings the
+//    packed codes of the 128 w rows into a deep ring (the codes stream from
+//    HBM with the longest latency); per 64-wide block the activation tile
+//    comes by TMA with 128-byte swizzle into its own ring (in the grouped
+//    form from a copy of the activation rows in sorted order);
+//  * eight dequant warps (two threads per w row, one 64-wide half each) turn
+//    codes into bf16 w^ = s*q + b (one rounding) and write it straight into
+//    the 128-byte-swizzled K-major layout the tensor core reads;
+//  * one elected lane issues eight 128xNx16 tcgen05.mma per stage into fp32
+//    tensor memory; the dequant warps then read the accumulators back with
+//    tcgen05.ld and store bf16.  With K split across the CTAs of a cluster,
+//    the fp32 partials are added through distributed shared memory in rank
+//    order, so the result does not depend on timing.
 //
 // Every wait on an mbarrier is bounded; on expiry the kernel sets
 // MXQ_DEV_TIMEOUT, stops issuing work, lets issued work finish and frees its
@@ -41,19 +42,17 @@ constexpr int kDequantWarps = 8;     // warps 0-7: dequant + epilogue
 constexpr int kDequantThreads = kDequantWarps * 32;
 constexpr int kCodeWarp = 8;         // codes TMA
 constexpr int kMmaWarp = 9;          // TMEM owner, MMA issue
-constexpr int kXWarp0 = 10;          // dense: activation TMA (warp 10);
-                                     // grouped: warps 10-11 gather rows by cp.async
-constexpr int kGatherThreads = 64;
-constexpr int kThreads = 12 * 32;
+constexpr int kXWarp0 = 10;          // activation TMA
+constexpr int kThreads = 11 * 32;
 constexpr int kTileN = 128;          // rows of w per CTA (MMA M)
 constexpr int kBK = 128;             // K per dequant/MMA stage: two 64-wide groups
 constexpr int kHalfK = 64;           // K per activation slot (one 128-byte swizzle atom)
 constexpr int kMaxRows = 256;        // activation rows per tile (MMA N <= 256)
 constexpr int kMaxSplits = 8;        // K splits per tile = cluster size (portable limit)
-constexpr int kMaxCodeStages = 4;
+constexpr int kMaxCodeStages = 16;
 constexpr int kMaxAStages = 4;
 constexpr int kMaxXStages = 16;
-constexpr int kSmemBudget = 210 * 1024;
+constexpr int kSmemBudget = 224 * 1024;
 
 struct SmemLayout {
     int c_bytes, c_stages;    // packed-code ring, one 128-wide K stage per slot
@@ -63,33 +62,40 @@ struct SmemLayout {
     int bar_offset, src_offset, total;
 };
 
-// The activation tile arrives with the longest latency (it is re-read by
-// every w tile), so after a minimal A and code ring it gets the deepest ring
-// the shared-memory budget allows; leftover room deepens the A ring.
+// Ring depths.  The packed codes stream from HBM with the longest latency
+// under load (about 2 us), the activation tile comes from L2 (it is re-read
+// by every w tile), and the dequantised tile only has to stay one stage
+// ahead of the MMAs.  So: 2 A stages, at least 4 activation slots, then as
+// many code stages as fit (up to 16), then more activation slots, then more
+// A stages.
 __host__ __device__ inline SmemLayout make_layout(int bits, int max_rows) {
     SmemLayout L;
     const int rows16 = (max_rows + 15) & ~15;
     L.c_bytes = kTileN * kBK * bits / 8;              // 8 KB or 16 KB
-    L.c_stages = bits == 4 ? 4 : 3;
     L.a_bytes = kTileN * kBK * 2;                     // 32 KB
-    L.a_stages = 2;
     L.x_bytes = (rows16 / 8) * 1024;                  // 128 B per row, 8-row atoms
-    int room = kSmemBudget - L.c_stages * L.c_bytes - L.a_stages * L.a_bytes;
-    int sx = room / L.x_bytes;
-    sx = sx > kMaxXStages ? kMaxXStages : (sx < 2 ? 2 : sx);
-    room -= sx * L.x_bytes;
+    L.a_stages = 2;
+    L.x_stages = 4;
+    int room = kSmemBudget - L.a_stages * L.a_bytes - L.x_stages * L.x_bytes;
+    L.c_stages = room / L.c_bytes;
+    if (L.c_stages > kMaxCodeStages) L.c_stages = kMaxCodeStages;
+    if (L.c_stages < 2) L.c_stages = 2;
+    room -= L.c_stages * L.c_bytes;
+    while (L.x_stages < kMaxXStages && room >= L.x_bytes) {
+        ++L.x_stages;
+        room -= L.x_bytes;
+    }
     while (L.a_stages < kMaxAStages && room >= L.a_bytes) {
         ++L.a_stages;
         room -= L.a_bytes;
     }
-    L.x_stages = sx;
     L.x_offset = L.a_stages * L.a_bytes;
     L.c_offset = L.x_offset + L.x_stages * L.x_bytes;
     L.bar_offset = L.c_offset + L.c_stages * L.c_bytes;
     // cfull, cempty; afull, aempty; xfull, xempty; accf; tmem base
     L.src_offset = L.bar_offset +
                    (2 * kMaxCodeStages + 2 * kMaxAStages + 2 * kMaxXStages + 1) * 8 + 16;
-    L.total = L.src_offset + kMaxRows * 4 + 1024;     // + alignment slack
+    L.total = L.src_offset + 1024;                    // + alignment slack
     return L;
 }
 
@@ -308,7 +314,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* xempty = xfull + kMaxXStages;
     uint64_t* accf = xempty + kMaxXStages;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
-    int* src_rows = reinterpret_cast<int*>(smem + L.src_offset);
     const uint32_t smem_base = smem_u32(smem);
     const uint32_t x_base0 = smem_base + L.x_offset;
     const uint32_t c_base0 = smem_base + L.c_offset;
@@ -349,22 +354,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&aempty[i], 1);
         }
         for (int i = 0; i < SX; ++i) {
-            mbar_init(&xfull[i], GATHER ? kGatherThreads : 1);
+            mbar_init(&xfull[i], 1);
             mbar_init(&xempty[i], 1);
         }
         mbar_init(accf, 1);
         mbar_init_fence();
-    }
-    if (GATHER) {
-        for (int r = threadIdx.x; r < n_mma; r += kThreads) {
-            int src = -1;
-            if (r < rows) {
-                const int sr = row_start + r;
-                src = p.row_src ? p.row_src[sr] : sr;
-                if (src < 0 || src >= p.T) src = -1;  // reported by the prepass; reads as zero
-            }
-            src_rows[r] = src;
-        }
     }
     if (warp == kMmaWarp) {
         tmem_alloc(tmem_slot, (uint32_t)p.tmem_cols);
@@ -395,53 +389,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
         }
-    } else if (!GATHER && warp == kXWarp0) {
+    } else if (warp == kXWarp0) {
         // ---------------------------------------------------------------- activation TMA
-        // one [m_tile rows x 64] bf16 box (128-byte swizzle) per 64-wide block
-        const uint32_t x_box_bytes = (uint32_t)(((p.m_tile + 15) & ~15) * 128);
+        // per 64-wide block, boxes of [x_box_rows x 64] bf16 (128-byte
+        // swizzle) stacked to cover the tile's n_mma rows; rows past the end
+        // of x read as zero, rows past the tile are never stored
+        const int boxes = (n_mma + p.x_box_rows - 1) / p.x_box_rows;
+        const uint32_t x_bytes_in = (uint32_t)(boxes * p.x_box_rows * 128);
         for (int q = 0; q < nkb; ++q) {
             const int slot = q % SX;
             if (q >= SX && !warp_wait(&xempty[slot], ((q / SX) + 1) & 1)) { ok = false; break; }
             if (elect_one()) {
-                mbar_expect_tx(&xfull[slot], x_box_bytes);
-                tma_load_2d(x_base0 + slot * L.x_bytes, &x_map, (kb_begin + q) * kHalfK, row_start,
-                            &xfull[slot]);
+                mbar_expect_tx(&xfull[slot], x_bytes_in);
+                for (int b = 0; b < boxes; ++b)
+                    tma_load_2d(x_base0 + slot * L.x_bytes + b * p.x_box_rows * 128, &x_map,
+                                (kb_begin + q) * kHalfK, row_start + b * p.x_box_rows, &xfull[slot]);
             }
             __syncwarp();
-        }
-    } else if (GATHER && warp >= kXWarp0) {
-        // ---------------------------------------------------------------- gathered rows
-        const int pt = threadIdx.x - kXWarp0 * 32;
-        const int chunks = n_mma * 8;
-        // blocks kept in flight before signalling: the MMA consumes blocks in
-        // pairs, so block q - SX + 1 must be signalled before block q waits
-        // for its slot; hence lag <= SX - 2
-        const int lag = SX - 2 < 0 ? 0 : (SX - 2 < 7 ? SX - 2 : 7);
-        const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(p.x);
-        for (int q = 0; q < nkb; ++q) {
-            const int slot = q % SX;
-            if (q >= SX && !mbar_wait(&xempty[slot], ((q / SX) + 1) & 1)) { ok = false; break; }
-            const uint32_t x_base = x_base0 + slot * L.x_bytes;
-            const int kb = kb_begin + q;
-            for (int c = pt; c < chunks; c += kGatherThreads) {
-                const int r = c >> 3;
-                const int ch = c & 7;
-                const int src = src_rows[r];
-                const void* g = xb + (src >= 0 ? (long long)src * p.K + kb * kHalfK + ch * 8 : 0);
-                cp_async_16(x_base + sw128_offset(r, ch), g, src >= 0 ? 16u : 0u);
-            }
-            cp_async_commit();
-            // keep up to `lag` blocks in flight; signal the oldest once landed
-            if (q >= lag) {
-                cp_async_wait_n(lag);
-                fence_proxy_async_smem();
-                mbar_arrive(&xfull[(q - lag) % SX]);
-            }
-        }
-        cp_async_wait<0>();
-        if (ok) {
-            fence_proxy_async_smem();
-            for (int q = (nkb > lag ? nkb - lag : 0); q < nkb; ++q) mbar_arrive(&xfull[q % SX]);
         }
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issue
@@ -747,7 +711,6 @@ cudaError_t launch_qmm_tc(const QmmParams& p, int bits, int grid_m, int max_rows
                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
-        xm = cm;  // unused in the grouped form
     } else {
         const cuuint64_t dims[2] = {words, (cuuint64_t)p.N};
         const cuuint64_t strides[1] = {words * 4};
@@ -756,14 +719,15 @@ cudaError_t launch_qmm_tc(const QmmParams& p, int bits, int grid_m, int max_rows
                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
-        const cuuint64_t xdims[2] = {(cuuint64_t)p.K, (cuuint64_t)p.M};
-        const cuuint64_t xstrides[1] = {(cuuint64_t)p.K * 2};
-        const cuuint32_t xbox[2] = {(cuuint32_t)kHalfK, (cuuint32_t)((p.m_tile + 15) & ~15)};
-        if (enc(&xm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p.x), xdims, xstrides,
-                xbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
     }
+    // activation rows: [x_rows, K] bf16 (the sorted copy in the grouped form)
+    const cuuint64_t xdims[2] = {(cuuint64_t)p.K, (cuuint64_t)p.x_rows};
+    const cuuint64_t xstrides[1] = {(cuuint64_t)p.K * 2};
+    const cuuint32_t xbox[2] = {(cuuint32_t)kHalfK, (cuuint32_t)p.x_box_rows};
+    if (enc(&xm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p.x), xdims, xstrides, xbox,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
     if (bits == 4)
         return gather ? launch_variant<4, true>(p, grid_m, max_rows_per_tile, cm, xm, stream)
                       : launch_variant<4, false>(p, grid_m, max_rows_per_tile, cm, xm, stream);

@@ -424,7 +424,7 @@ def secondary_measurements(mxq, dev, stream, hbm, bf16_peak, Ws):
         ids_d = torch.from_numpy(ids).to(dev)
         src_d = None if ident else torch.from_numpy(src).to(dev)
         y = torch.empty((B, N), dtype=torch.bfloat16, device=dev)
-        wsz = torch.empty((mxq.gather_workspace_bytes(B, E, N),), dtype=torch.uint8, device=dev)
+        wsz = torch.empty((mxq.gather_workspace_bytes(B, E, K if src_d is not None else 0, N),), dtype=torch.uint8, device=dev)
         fn = lambda i: mxq.gather_qmm(x, *copies[i % 2], ids_d, src_d, bits, out=y,  # noqa: E731
                                       workspace=wsz)
         for i in range(5):

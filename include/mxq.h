@@ -94,8 +94,11 @@ mxq_status mxq_qmm(const void* x, const uint32_t* w, const void* scales, const v
  *   row_src:    int32 [B], row of x that feeds sorted row r; NULL means r
  *               (then T must equal B)
  *   y:          bf16 [B, N], in sorted row order
- *   workspace:  device scratch of mxq_gather_workspace_bytes(B, E, N) bytes,
- *               256-byte aligned; overwritten by the call.
+ *   workspace:  device scratch, 256-byte aligned, overwritten by the call:
+ *               mxq_gather_workspace_bytes(B, E, K, N) bytes when row_src
+ *               is given (it also holds the activation rows in sorted
+ *               order), otherwise the smaller mxq_gather_workspace_bytes(B,
+ *               E, 0, N) suffices.
  *   dev_status: device int32 or NULL; receives the MXQ_DEV_* bits.
  * Rows whose expert id lies outside [0, E), or whose row_src lies outside
  * [0, T), are skipped and their y rows set to zero.  If the ids are not
@@ -110,8 +113,9 @@ mxq_status mxq_gather_qmm(const void* x, const uint32_t* w, const void* scales,
                           int bits, int group_size, void* workspace, size_t workspace_bytes,
                           int32_t* dev_status, void* stream);
 
-/* Workspace bytes mxq_gather_qmm needs for B rows over E experts. */
-size_t mxq_gather_workspace_bytes(int B, int E, int N);
+/* Workspace bytes mxq_gather_qmm needs for B rows over E experts with
+ * K-wide activation rows routed through row_src (K = 0: no row_src). */
+size_t mxq_gather_workspace_bytes(int B, int E, int K, int N);
 
 /* Static description of a status code. */
 const char* mxq_status_string(mxq_status status);

@@ -84,7 +84,7 @@ def test_qmm_argument_checks(L, kw, code):
 
 
 def gather(L, T=8, B=8, E=2, K=128, N=64, bits=4, group=64, ids=FAKE, src=FAKE, ws=FAKE,
-           wsb=1 << 20):
+           wsb=1 << 24):
     return L.mxq_gather_qmm(FAKE, FAKE, FAKE, FAKE, ids, src, FAKE, T, B, E, K, N, bits, group,
                             ws, wsb, None, None)
 
@@ -100,10 +100,13 @@ def test_gather_argument_checks(L, kw, code):
 
 
 def test_workspace_sizes(L):
-    n = L.mxq_gather_workspace_bytes(4584, 128, 704)
+    n0 = L.mxq_gather_workspace_bytes(4584, 128, 0, 704)
     # one 16-byte tile record per possible tile plus the count
-    assert n >= (4584 // 128 + 128) * 16
-    assert L.mxq_gather_workspace_bytes(0, 4, 4) == 0
+    assert n0 >= (4584 // 128 + 128) * 16
+    # with routed rows it also holds the sorted activation copy
+    n1 = L.mxq_gather_workspace_bytes(4584, 128, 2816, 704)
+    assert n1 >= n0 + 4584 * 2816 * 2
+    assert L.mxq_gather_workspace_bytes(0, 4, 64, 4) == 0
 
 
 def test_valid_call_without_sm103_device_reports_device_error(L):
