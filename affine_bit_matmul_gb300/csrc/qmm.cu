@@ -347,10 +347,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < SC; ++i) {
             mbar_init(&cfull[i], 1);
-            mbar_init(&cempty[i], kDequantThreads);
+            mbar_init(&cempty[i], kDequantThreads / 2);  // one group per stage
         }
         for (int i = 0; i < SA; ++i) {
-            mbar_init(&afull[i], kDequantThreads);
+            mbar_init(&afull[i], kDequantThreads / 2);
             mbar_init(&aempty[i], 1);
         }
         for (int i = 0; i < SX; ++i) {
@@ -445,33 +445,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp < kDequantWarps) {
         // ---------------------------------------------------------------- dequant
-        // thread (r, h): w row r of the tile, 64-wide half h of every stage
-        const int r = threadIdx.x & (kTileN - 1);   // = TMEM lane of the row
-        const int h = warp >> 2;
+        // two groups of four warps take alternate 128-wide stages, so two
+        // stages are dequantised at once; thread r handles w row r (its TMEM
+        // lane) over the whole stage: two 64-wide groups
+        const int r = threadIdx.x & (kTileN - 1);
+        const int grp = warp >> 2;
         const int n = n0 + r;
         const bool row_ok = n < p.N;
         const uint16_t* srow = p.scales + (long long)e * p.sb_expert_stride + (long long)n * groups;
         const uint16_t* brow = p.biases + (long long)e * p.sb_expert_stride + (long long)n * groups;
-        auto stage = [&](int s, uint32_t sbits, uint32_t bbits) -> bool {
-            const bool valid = 2 * s + h < nkb;
+        constexpr int kRowBytes = kBK * BITS / 8;  // codes of one row per stage
+        auto stage = [&](int s, const uint32_t (&sb)[4]) -> bool {
             const int cs = s % SC;
             if (!mbar_wait(&cfull[cs], (s / SC) & 1)) return false;
-            constexpr int kRowBytes = kBK * BITS / 8;        // codes of one row per stage
-            const uint32_t c_row = c_base0 + cs * L.c_bytes + r * kRowBytes + h * (kRowBytes / 2);
-            uint4 cw[BITS / 2];
+            const uint32_t c_row = c_base0 + cs * L.c_bytes + r * kRowBytes;
+            uint4 cw[BITS];
 #pragma unroll
-            for (int j = 0; j < BITS / 2; ++j) cw[j] = ld_shared_v4(c_row + j * 16);
+            for (int j = 0; j < BITS; ++j) cw[j] = ld_shared_v4(c_row + j * 16);
             const int as = s % SA;
             if (s >= SA && !mbar_wait(&aempty[as], ((s / SA) + 1) & 1)) return false;
-            const uint32_t a_row = smem_base + as * L.a_bytes + h * (L.a_bytes / 2) +
-                                   (r >> 3) * 1024 + (r & 7) * 128;
-            if (valid) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                if (2 * s + h >= nkb) break;  // the second half past this split's K
+                const uint32_t a_row = smem_base + as * L.a_bytes + h * (L.a_bytes / 2) +
+                                       (r >> 3) * 1024 + (r & 7) * 128;
+                const uint32_t sbits = sb[h], bbits = sb[2 + h];
                 if (BITS == 4) {
                     const uint32_t s2 = sbits | (sbits << 16);
                     const uint32_t b2 = bbits | (bbits << 16);
 #pragma unroll
                     for (int q = 0; q < 2; ++q) {
-                        const uint32_t wd[4] = {cw[q].x, cw[q].y, cw[q].z, cw[q].w};
+                        const uint4 c = cw[h * 2 + q];
+                        const uint32_t wd[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             uint32_t o[4];
@@ -485,7 +490,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float bf = bf16_bits_to_float(bbits);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        const uint32_t wd[4] = {cw[q].x, cw[q].y, cw[q].z, cw[q].w};
+                        const uint4 c = cw[h * 4 + q];
+                        const uint32_t wd[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
                         for (int j = 0; j < 2; ++j) {
                             uint32_t o0[2], o1[2];
@@ -506,23 +512,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&afull[as]);
             return true;
         };
-        // scale/bias of this thread's block, two stages ahead
-        auto sb_load = [&](int s, uint32_t& sv, uint32_t& bv) {
-            const int b = 2 * s + h;
-            if (row_ok && s < nst && b < nkb) {
-                sv = __ldg(srow + kb_begin + b);
-                bv = __ldg(brow + kb_begin + b);
+        // scales and biases of a stage's two groups: {s0, s1, b0, b1}
+        auto sb_load = [&](int s, uint32_t (&sb)[4]) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int b = 2 * s + h;
+                if (row_ok && s < nst && b < nkb) {
+                    sb[h] = __ldg(srow + kb_begin + b);
+                    sb[2 + h] = __ldg(brow + kb_begin + b);
+                }
             }
         };
-        uint32_t sA = 0, bA = 0, sB = 0, bB = 0;
-        sb_load(0, sA, bA);
-        sb_load(1, sB, bB);
-        for (int s = 0; s < nst && ok; s += 2) {
-            ok = stage(s, sA, bA);
-            sb_load(s + 2, sA, bA);
-            if (!ok || s + 1 >= nst) break;
-            ok = stage(s + 1, sB, bB);
-            sb_load(s + 3, sB, bB);
+        // this group's stages grp, grp + 2, ...; scales loaded a stage ahead
+        uint32_t sbA[4] = {0, 0, 0, 0}, sbB[4] = {0, 0, 0, 0};
+        sb_load(grp, sbA);
+        sb_load(grp + 2, sbB);
+        for (int s = grp; s < nst && ok; s += 4) {
+            ok = stage(s, sbA);
+            sb_load(s + 4, sbA);
+            if (!ok || s + 2 >= nst) break;
+            ok = stage(s + 2, sbB);
+            sb_load(s + 6, sbB);
         }
 
         // ---------------------------------------------------------------- epilogue
@@ -584,28 +594,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool vec_ok = (p.N % 4 == 0) && (n_out + 3 < p.N);
             for (int m0 = rank + S * ph; m0 < rows; m0 += S * kDequantWarps * 4) {
                 float4 acc[4];
-                float4 v[4][kMaxSplits];
 #pragma unroll
-                for (int z = 0; z < kMaxSplits; ++z) {
+                for (int u = 0; u < 4; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int z0 = 0; z0 < S; z0 += 2) {
+                    float4 v[4][2];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         const int m = m0 + u * S * kDequantWarps;
-                        if (z < S && m < rows)
-                            v[u][z] = ld_cluster_f32x4(
-                                map_cluster(smem_base + (m * kTileN + c4) * 4, (uint32_t)z));
+#pragma unroll
+                        for (int dz = 0; dz < 2; ++dz) {
+                            v[u][dz] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            if (z0 + dz < S && m < rows)
+                                v[u][dz] = ld_cluster_f32x4(
+                                    map_cluster(smem_base + (m * kTileN + c4) * 4, (uint32_t)(z0 + dz)));
+                        }
                     }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+#pragma unroll
+                        for (int dz = 0; dz < 2; ++dz) {  // rank order: z0, then z0 + 1
+                            acc[u].x += v[u][dz].x;
+                            acc[u].y += v[u][dz].y;
+                            acc[u].z += v[u][dz].z;
+                            acc[u].w += v[u][dz].w;
+                        }
                 }
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                    for (int z = 0; z < kMaxSplits; ++z)
-                        if (z < S) {
-                            acc[u].x += v[u][z].x;
-                            acc[u].y += v[u][z].y;
-                            acc[u].z += v[u][z].z;
-                            acc[u].w += v[u][z].w;
-                        }
                     const int m = m0 + u * S * kDequantWarps;
                     if (!ok || m >= rows) continue;
                     __nv_bfloat16* yr = y + (long long)(row_start + m) * p.N;
