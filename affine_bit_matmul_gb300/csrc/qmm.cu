@@ -50,33 +50,31 @@ constexpr int kHalfK = 64;           // K per activation slot (one 128-byte swiz
 constexpr int kMaxRows = 256;        // activation rows per tile (MMA N <= 256)
 constexpr int kMaxSplits = 8;        // K splits per tile = cluster size (portable limit)
 constexpr int kMaxCodeStages = 16;
-constexpr int kMaxAStages = 4;
+constexpr int kMaxAStages = 6;       // dequantised stages held in tensor memory
 constexpr int kMaxXStages = 16;
 constexpr int kSmemBudget = 224 * 1024;
+constexpr int kTmemCols = 512;       // accumulator + dequantised A stages
+constexpr int kAStageCols = kBK / 2; // one bf16 pair per 32-bit column
 
 struct SmemLayout {
     int c_bytes, c_stages;    // packed-code ring, one 128-wide K stage per slot
-    int a_bytes, a_stages;    // dequantised w ring (MMA A operand), 2 atoms per slot
     int x_bytes, x_stages;    // activation ring (MMA B operand), one 64-wide atom per slot
-    int x_offset, c_offset;   // rings: A at 0, then x, then codes
-    int bar_offset, src_offset, total;
+    int c_offset;             // rings: x at 0, then codes
+    int bar_offset, total;
 };
 
-// Ring depths.  The packed codes stream from HBM with the longest latency
-// under load (about 2 us), the activation tile comes from L2 (it is re-read
-// by every w tile), and the dequantised tile only has to stay one stage
-// ahead of the MMAs.  So: 2 A stages, at least 4 activation slots, then as
-// many code stages as fit (up to 16), then more activation slots, then more
-// A stages.
+// Ring depths in shared memory (the dequantised A operand lives in tensor
+// memory).  The activation tile comes from L2 with about a microsecond of
+// latency and the packed codes stream from HBM with up to two: at least six
+// activation slots, then as many code stages as fit (up to 16), then more
+// activation slots.
 __host__ __device__ inline SmemLayout make_layout(int bits, int max_rows) {
     SmemLayout L;
     const int rows16 = (max_rows + 15) & ~15;
     L.c_bytes = kTileN * kBK * bits / 8;              // 8 KB or 16 KB
-    L.a_bytes = kTileN * kBK * 2;                     // 32 KB
     L.x_bytes = (rows16 / 8) * 1024;                  // 128 B per row, 8-row atoms
-    L.a_stages = 2;
-    L.x_stages = 4;
-    int room = kSmemBudget - L.a_stages * L.a_bytes - L.x_stages * L.x_bytes;
+    L.x_stages = 6;
+    int room = kSmemBudget - L.x_stages * L.x_bytes;
     L.c_stages = room / L.c_bytes;
     if (L.c_stages > kMaxCodeStages) L.c_stages = kMaxCodeStages;
     if (L.c_stages < 2) L.c_stages = 2;
@@ -85,17 +83,11 @@ __host__ __device__ inline SmemLayout make_layout(int bits, int max_rows) {
         ++L.x_stages;
         room -= L.x_bytes;
     }
-    while (L.a_stages < kMaxAStages && room >= L.a_bytes) {
-        ++L.a_stages;
-        room -= L.a_bytes;
-    }
-    L.x_offset = L.a_stages * L.a_bytes;
-    L.c_offset = L.x_offset + L.x_stages * L.x_bytes;
+    L.c_offset = L.x_stages * L.x_bytes;
     L.bar_offset = L.c_offset + L.c_stages * L.c_bytes;
     // cfull, cempty; afull, aempty; xfull, xempty; accf; tmem base
-    L.src_offset = L.bar_offset +
-                   (2 * kMaxCodeStages + 2 * kMaxAStages + 2 * kMaxXStages + 1) * 8 + 16;
-    L.total = L.src_offset + 1024;                    // + alignment slack
+    L.total = L.bar_offset + (2 * kMaxCodeStages + 2 * kMaxAStages + 2 * kMaxXStages + 1) * 8 +
+              16 + 1024;                              // + alignment slack
     return L;
 }
 
@@ -315,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* accf = xempty + kMaxXStages;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
     const uint32_t smem_base = smem_u32(smem);
-    const uint32_t x_base0 = smem_base + L.x_offset;
+    const uint32_t x_base0 = smem_base;
     const uint32_t c_base0 = smem_base + L.c_offset;
 
     const int warp = threadIdx.x >> 5;
@@ -341,8 +333,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nst = (nkb + 1) / 2;                     // 128-wide stages
     const int groups = p.K / 64;
     const int SC = L.c_stages;
-    const int SA = L.a_stages;
     const int SX = L.x_stages;
+    // tensor memory: accumulator in columns [0, n_mma), dequantised stages
+    // of 64 columns from a0 on
+    const int a0 = (n_mma + kAStageCols - 1) / kAStageCols * kAStageCols;
+    const int SA = min(kMaxAStages, (kTmemCols - a0) / kAStageCols);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < SC; ++i) {
@@ -361,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init_fence();
     }
     if (warp == kMmaWarp) {
-        tmem_alloc(tmem_slot, (uint32_t)p.tmem_cols);
+        tmem_alloc(tmem_slot, (uint32_t)kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -424,16 +419,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             if (elect_one()) {
-                const uint32_t a_base = smem_base + as * L.a_bytes;
+                const uint32_t a_col = tmem + (uint32_t)(a0 + as * kAStageCols);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     if (h == 1 && !two) break;
-                    const uint64_t ad = umma_desc_sw128(a_base + h * (L.a_bytes / 2));
                     const uint64_t bd = umma_desc_sw128(x_base0 + (h ? x1 : x0) * L.x_bytes);
 #pragma unroll
                     for (int j = 0; j < kHalfK / 16; ++j)
-                        umma_bf16(tmem, ad + 2 * j, bd + 2 * j, idesc,
-                                  (s > 0 || h > 0 || j > 0) ? 1u : 0u);
+                        umma_bf16_tmem_a(tmem, a_col + h * (kAStageCols / 2) + j * 8, bd + 2 * j,
+                                         idesc, (s > 0 || h > 0 || j > 0) ? 1u : 0u);
                 }
                 umma_commit(&aempty[as]);
                 umma_commit(&xempty[x0]);
@@ -455,60 +449,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint16_t* srow = p.scales + (long long)e * p.sb_expert_stride + (long long)n * groups;
         const uint16_t* brow = p.biases + (long long)e * p.sb_expert_stride + (long long)n * groups;
         constexpr int kRowBytes = kBK * BITS / 8;  // codes of one row per stage
+        // this warp's 32 TMEM lanes
+        const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         auto stage = [&](int s, const uint32_t (&sb)[4]) -> bool {
             const int cs = s % SC;
-            if (!mbar_wait(&cfull[cs], (s / SC) & 1)) return false;
+            if (!warp_wait(&cfull[cs], (s / SC) & 1)) return false;
             const uint32_t c_row = c_base0 + cs * L.c_bytes + r * kRowBytes;
             uint4 cw[BITS];
 #pragma unroll
             for (int j = 0; j < BITS; ++j) cw[j] = ld_shared_v4(c_row + j * 16);
             const int as = s % SA;
-            if (s >= SA && !mbar_wait(&aempty[as], ((s / SA) + 1) & 1)) return false;
+            if (s >= SA && !warp_wait(&aempty[as], ((s / SA) + 1) & 1)) return false;
+            tc_fence_after();
+            const uint32_t a_col = t_lane + (uint32_t)(a0 + as * kAStageCols);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 if (2 * s + h >= nkb) break;  // the second half past this split's K
-                const uint32_t a_row = smem_base + as * L.a_bytes + h * (L.a_bytes / 2) +
-                                       (r >> 3) * 1024 + (r & 7) * 128;
                 const uint32_t sbits = sb[h], bbits = sb[2 + h];
-                if (BITS == 4) {
-                    const uint32_t s2 = sbits | (sbits << 16);
-                    const uint32_t b2 = bbits | (bbits << 16);
 #pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        const uint4 c = cw[h * 2 + q];
-                        const uint32_t wd[4] = {c.x, c.y, c.z, c.w};
+                for (int c = 0; c < 2; ++c) {  // 32 k = 16 columns per store
+                    uint32_t o[16];
+                    if (BITS == 4) {
+                        const uint32_t s2 = sbits | (sbits << 16);
+                        const uint32_t b2 = bbits | (bbits << 16);
+                        const uint4 cv = cw[h * 2 + c];
+                        const uint32_t wd[4] = {cv.x, cv.y, cv.z, cv.w};
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            uint32_t o[4];
-                            dequant_word4(wd[j], s2, b2, o);
-                            const int chunk = q * 4 + j;  // 8 k per word = one 16-byte chunk
-                            st_shared_v4(a_row + ((chunk ^ (r & 7)) << 4), o[0], o[1], o[2], o[3]);
+                            uint32_t q4[4];
+                            dequant_word4(wd[j], s2, b2, q4);
+#pragma unroll
+                            for (int t = 0; t < 4; ++t) o[j * 4 + t] = q4[t];
+                        }
+                    } else {
+                        const float sf = bf16_bits_to_float(sbits);
+                        const float bf = bf16_bits_to_float(bbits);
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) {
+                            const uint4 cv = cw[h * 4 + c * 2 + q];
+                            const uint32_t wd[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                uint32_t q2[2];
+                                dequant_word8(wd[j], sf, bf, q2);
+                                o[q * 8 + j * 2] = q2[0];
+                                o[q * 8 + j * 2 + 1] = q2[1];
+                            }
                         }
                     }
-                } else {
-                    const float sf = bf16_bits_to_float(sbits);
-                    const float bf = bf16_bits_to_float(bbits);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const uint4 c = cw[h * 4 + q];
-                        const uint32_t wd[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-                        for (int j = 0; j < 2; ++j) {
-                            uint32_t o0[2], o1[2];
-                            dequant_word8(wd[2 * j], sf, bf, o0);
-                            dequant_word8(wd[2 * j + 1], sf, bf, o1);
-                            const int chunk = q * 2 + j;
-                            st_shared_v4(a_row + ((chunk ^ (r & 7)) << 4), o0[0], o0[1], o1[0],
-                                         o1[1]);
-                        }
-                    }
+                    tmem_st16(a_col + h * (kAStageCols / 2) + c * 16, o);
                 }
             }
+            tmem_st_wait();
             // release the code slot only now that the loaded words have been
             // consumed: an arrive placed right after the shared loads let the
             // next TMA overwrite the slot before the loads had returned
             mbar_arrive(&cempty[cs]);
-            fence_proxy_async_smem();
+            tc_fence_before();
             mbar_arrive(&afull[as]);
             return true;
         };
@@ -648,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // make sure no MMA is still writing tensor memory (bounded wait)
         if (lane == 0 && !ok) (void)mbar_wait(accf, 0);
         __syncwarp();
-        tmem_dealloc(tmem, (uint32_t)p.tmem_cols);
+        tmem_dealloc(tmem, (uint32_t)kTmemCols);
     }
 }
 

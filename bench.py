@@ -530,8 +530,9 @@ def run_profile(args):
         for i in range(launches):
             mxq.qmv(d.x[0], *d.copies[i % 2], bits, out=d.y[0])
     elif name.startswith("qmm"):
-        M, K, N, bits = {"qmm": (600, 5120, 17408, 4), "qmm128": (128, 5120, 5120, 4),
-                         "qmm8": (8, 5120, 5120, 4), "qmm32": (32, 5120, 5120, 4)}[name]
+        M, K, N, bits = {"qmm": (600, 5120, 17408, 4), "qmm600": (600, 5120, 5120, 4),
+                         "qmm128": (128, 5120, 5120, 4), "qmm8": (8, 5120, 5120, 4),
+                         "qmm32": (32, 5120, 5120, 4)}[name]
         d = DenseInputs(synth.dense_weights(N, K, seed=0), M, K, N, bits, dev, copies=2)
         for i in range(launches):
             mxq.qmm(d.x, *d.copies[i % 2], bits, out=d.y)
@@ -559,7 +560,7 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--profile", default=None,
                     help="plain launches of one workload for ncu: qmv4 qmv8 qmv4t qmv8t qmm "
-                         "qmm128 qmm8 qmm32 gather_up gather_down")
+                         "qmm600 qmm128 qmm8 qmm32 gather_up gather_down")
     ap.add_argument("--profile-launches", type=int, default=4)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20000)
