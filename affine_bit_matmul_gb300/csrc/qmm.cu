@@ -258,6 +258,20 @@ __device__ __forceinline__ bool mbar_wait3(uint64_t* a, uint32_t pa, uint64_t* b
     return true;
 }
 
+// Position in a ring of n slots: the slot of the current item and the parity
+// of its round (round = item / n), advanced without divisions.
+struct Ring {
+    int n, slot;
+    uint32_t parity;
+    __device__ explicit Ring(int n_) : n(n_), slot(0), parity(0) {}
+    __device__ void next() {
+        if (++slot == n) {
+            slot = 0;
+            parity ^= 1u;
+        }
+    }
+};
+
 // Whole-warp waits: every lane polls with its own bounded budget, then the
 // warp agrees on the outcome, so the warp stays converged for elect.sync even
 // when a wait gives up.
@@ -371,16 +385,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // is zero-filled, a second half that belongs to the next K split is
         // loaded but never dequantised
         constexpr int kWordsPerStage = kBK * BITS / 32;
-        for (int s = 0; s < nst; ++s) {
-            const int slot = s % SC;
-            if (s >= SC && !warp_wait(&cempty[slot], ((s / SC) + 1) & 1)) { ok = false; break; }
+        Ring ring(SC);
+        for (int s = 0; s < nst; ++s, ring.next()) {
+            if (s >= SC && !warp_wait(&cempty[ring.slot], ring.parity ^ 1)) { ok = false; break; }
             if (elect_one()) {
-                mbar_expect_tx(&cfull[slot], (uint32_t)L.c_bytes);
+                mbar_expect_tx(&cfull[ring.slot], (uint32_t)L.c_bytes);
                 const int c0 = kb_begin * (kHalfK * BITS / 32) + s * kWordsPerStage;
+                const uint32_t dst = c_base0 + ring.slot * L.c_bytes;
                 if (GATHER)
-                    tma_load_3d(c_base0 + slot * L.c_bytes, &code_map, c0, n0, e, &cfull[slot]);
+                    tma_load_3d(dst, &code_map, c0, n0, e, &cfull[ring.slot]);
                 else
-                    tma_load_2d(c_base0 + slot * L.c_bytes, &code_map, c0, n0, &cfull[slot]);
+                    tma_load_2d(dst, &code_map, c0, n0, &cfull[ring.slot]);
             }
             __syncwarp();
         }
@@ -391,14 +406,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // of x read as zero, rows past the tile are never stored
         const int boxes = (n_mma + p.x_box_rows - 1) / p.x_box_rows;
         const uint32_t x_bytes_in = (uint32_t)(boxes * p.x_box_rows * 128);
-        for (int q = 0; q < nkb; ++q) {
-            const int slot = q % SX;
-            if (q >= SX && !warp_wait(&xempty[slot], ((q / SX) + 1) & 1)) { ok = false; break; }
+        Ring ring(SX);
+        for (int q = 0; q < nkb; ++q, ring.next()) {
+            if (q >= SX && !warp_wait(&xempty[ring.slot], ring.parity ^ 1)) { ok = false; break; }
             if (elect_one()) {
-                mbar_expect_tx(&xfull[slot], x_bytes_in);
+                mbar_expect_tx(&xfull[ring.slot], x_bytes_in);
                 for (int b = 0; b < boxes; ++b)
-                    tma_load_2d(x_base0 + slot * L.x_bytes + b * p.x_box_rows * 128, &x_map,
-                                (kb_begin + q) * kHalfK, row_start + b * p.x_box_rows, &xfull[slot]);
+                    tma_load_2d(x_base0 + ring.slot * L.x_bytes + b * p.x_box_rows * 128, &x_map,
+                                (kb_begin + q) * kHalfK, row_start + b * p.x_box_rows,
+                                &xfull[ring.slot]);
             }
             __syncwarp();
         }
@@ -407,19 +423,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the whole warp waits (three barriers per stage in one round trip);
         // one elected lane issues the MMAs and the commits
         const uint32_t idesc = umma_idesc_bf16(kTileN, (uint32_t)n_mma);
-        for (int s = 0; s < nst; ++s) {
-            const int as = s % SA;
-            const int q0 = 2 * s, q1 = 2 * s + 1;
-            const bool two = q1 < nkb;
-            const int x0 = q0 % SX, x1 = two ? q1 % SX : x0;
-            const uint32_t p1 = two ? (uint32_t)((q1 / SX) & 1) : (uint32_t)((q0 / SX) & 1);
-            if (!warp_wait3(&afull[as], (s / SA) & 1, &xfull[x0], (q0 / SX) & 1, &xfull[x1], p1)) {
+        Ring ar(SA), xr(SX);
+        for (int s = 0; s < nst; ++s, ar.next()) {
+            const bool two = 2 * s + 1 < nkb;
+            const int x0 = xr.slot;
+            const uint32_t p0 = xr.parity;
+            xr.next();
+            const int x1 = two ? xr.slot : x0;
+            const uint32_t p1 = two ? xr.parity : p0;
+            if (two) xr.next();
+            if (!warp_wait3(&afull[ar.slot], ar.parity, &xfull[x0], p0, &xfull[x1], p1)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             if (elect_one()) {
-                const uint32_t a_col = tmem + (uint32_t)(a0 + as * kAStageCols);
+                const uint32_t a_col = tmem + (uint32_t)(a0 + ar.slot * kAStageCols);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     if (h == 1 && !two) break;
@@ -429,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         umma_bf16_tmem_a(tmem, a_col + h * (kAStageCols / 2) + j * 8, bd + 2 * j,
                                          idesc, (s > 0 || h > 0 || j > 0) ? 1u : 0u);
                 }
-                umma_commit(&aempty[as]);
+                umma_commit(&aempty[ar.slot]);
                 umma_commit(&xempty[x0]);
                 if (two) umma_commit(&xempty[x1]);
             }
@@ -451,15 +470,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr int kRowBytes = kBK * BITS / 8;  // codes of one row per stage
         // this warp's 32 TMEM lanes
         const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        // slot and phase of stage s in the code and A rings, advanced by two
+        // stages per step (this group's stages), without divisions
+        Ring cr(SC), ar(SA);
+        if (grp) {
+            cr.next();
+            ar.next();
+        }
         auto stage = [&](int s, const uint32_t (&sb)[4]) -> bool {
-            const int cs = s % SC;
-            if (!warp_wait(&cfull[cs], (s / SC) & 1)) return false;
+            const int cs = cr.slot;
+            if (!warp_wait(&cfull[cs], cr.parity)) return false;
             const uint32_t c_row = c_base0 + cs * L.c_bytes + r * kRowBytes;
             uint4 cw[BITS];
 #pragma unroll
             for (int j = 0; j < BITS; ++j) cw[j] = ld_shared_v4(c_row + j * 16);
-            const int as = s % SA;
-            if (s >= SA && !warp_wait(&aempty[as], ((s / SA) + 1) & 1)) return false;
+            const int as = ar.slot;
+            if (s >= SA && !warp_wait(&aempty[as], ar.parity ^ 1)) return false;
             tc_fence_after();
             const uint32_t a_col = t_lane + (uint32_t)(a0 + as * kAStageCols);
 #pragma unroll
@@ -507,6 +533,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&cempty[cs]);
             tc_fence_before();
             mbar_arrive(&afull[as]);
+            cr.next();  // on to stage s + 2
+            cr.next();
+            ar.next();
+            ar.next();
             return true;
         };
         // scales and biases of a stage's two groups: {s0, s1, b0, b1}
