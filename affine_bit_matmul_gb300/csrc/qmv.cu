@@ -93,6 +93,53 @@ __device__ __forceinline__ float dot_chunk4(const uint4 c, const float2 (&x2)[16
     return acc.x + acc.y;
 }
 
+// One word of 4-bit codes against 8 activations held as four fp32 pairs
+// (x_{2j}, x_{2j+1}): v_k = 1 + q_k/128 built by byte permutes straight into
+// register pairs, accumulated with packed fp32 FMAs (acc holds two partial
+// sums).  Written as one block so the pairs need no register moves.
+__device__ __forceinline__ void word4_f32x2(uint32_t wd, const unsigned long long (&xq)[4],
+                                            unsigned long long& acc) {
+    asm("{\n\t"
+        ".reg .b32 lo, hi, v0, v1;\n\t"
+        ".reg .b64 p;\n\t"
+        "lop3.b32 lo, %1, 0x0F0F0F0F, 0x80808080, 0xEA;\n\t"   // (w & m) | c
+        "shr.u32 hi, %1, 4;\n\t"
+        "lop3.b32 hi, hi, 0x0F0F0F0F, 0x80808080, 0xEA;\n\t"
+        "prmt.b32 v0, lo, 0x3F000000, 0x7044;\n\t"
+        "prmt.b32 v1, hi, 0x3F000000, 0x7044;\n\t"
+        "mov.b64 p, {v0, v1};\n\t"
+        "fma.rn.f32x2 %0, p, %2, %0;\n\t"
+        "prmt.b32 v0, lo, 0x3F000000, 0x7144;\n\t"
+        "prmt.b32 v1, hi, 0x3F000000, 0x7144;\n\t"
+        "mov.b64 p, {v0, v1};\n\t"
+        "fma.rn.f32x2 %0, p, %3, %0;\n\t"
+        "prmt.b32 v0, lo, 0x3F000000, 0x7244;\n\t"
+        "prmt.b32 v1, hi, 0x3F000000, 0x7244;\n\t"
+        "mov.b64 p, {v0, v1};\n\t"
+        "fma.rn.f32x2 %0, p, %4, %0;\n\t"
+        "prmt.b32 v0, lo, 0x3F000000, 0x7344;\n\t"
+        "prmt.b32 v1, hi, 0x3F000000, 0x7344;\n\t"
+        "mov.b64 p, {v0, v1};\n\t"
+        "fma.rn.f32x2 %0, p, %5, %0;\n\t"
+        "}"
+        : "+l"(acc)
+        : "r"(wd), "l"(xq[0]), "l"(xq[1]), "l"(xq[2]), "l"(xq[3]));
+}
+
+// Sum over the lane's 32 four-bit codes of x_k * (1 + q_k/128), from fp32
+// activation pairs xq[j] = (x_{2j}, x_{2j+1}).
+__device__ __forceinline__ float dot_chunk4_f32x2(const uint4 c,
+                                                  const unsigned long long (&xq)[16]) {
+    const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+    unsigned long long acc = 0ull;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        const unsigned long long q4[4] = {xq[4 * w], xq[4 * w + 1], xq[4 * w + 2], xq[4 * w + 3]};
+        word4_f32x2(words[w], q4, acc);
+    }
+    return __uint_as_float((uint32_t)acc) + __uint_as_float((uint32_t)(acc >> 32));
+}
+
 // Same for 16 eight-bit codes: v_k = 1 + q_k * 2^-15.  x2 holds 8 pairs.
 __device__ __forceinline__ float dot_chunk8(const uint4 c, const float2 (&x2)[16]) {
     const uint32_t words[4] = {c.x, c.y, c.z, c.w};
@@ -259,13 +306,14 @@ struct StreamShape {
 
 // Dot of one lane's 32 codes with its 32 activations, v_k = 1 + q_k 2^-p.
 template <int BITS>
-__device__ __forceinline__ float lane_dot(uint32_t codes_addr, const float2 (&x2)[16]) {
+__device__ __forceinline__ float lane_dot(uint32_t codes_addr, const float2 (&x2)[16],
+                                          const unsigned long long (&xq)[16]) {
     if (BITS == 4) {
         uint4 c;
         asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
                      : "=r"(c.x), "=r"(c.y), "=r"(c.z), "=r"(c.w)
                      : "r"(codes_addr));
-        return dot_chunk4(c, x2);
+        return dot_chunk4_f32x2(c, xq);
     } else {
         uint4 c0, c1;
         asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
@@ -287,7 +335,9 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
                       const uint16_t* __restrict__ scales, const uint16_t* __restrict__ biases,
                       __nv_bfloat16* __restrict__ y, int K, int N, const StreamShape sh,
                       int32_t* status) {
+    // A = sum x v with v = 1 + q 2^-7 (4-bit) or 1 + q 2^-15 (8-bit)
     constexpr float kUnscale = BITS == 4 ? 128.f : 32768.f;
+    constexpr float kOffset = 1.f;
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ uint64_t full[kStreamStages], empty[kStreamStages];
     __shared__ float red[2][kMaxStreamWarps * 8];
@@ -342,20 +392,25 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
     const int phase = warp / sh.nseg;
     const int k0 = seg * 1024 + lane * 32;   // this lane's 32 values
     const bool active = k0 < K;
-    float2 x2[16];
+    float2 x2[16];              // (x_{2j}, x_{2j+1}) as floats
+    unsigned long long xq[16];  // the same pairs packed for fma.rn.f32x2
     float X = 0.f;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) x2[j] = make_float2(0.f, 0.f);
+    for (int j = 0; j < 16; ++j) {
+        x2[j] = make_float2(0.f, 0.f);
+        xq[j] = 0ull;
+    }
     if (active) {
-        const uint4* xp = reinterpret_cast<const uint4*>(x + k0);
+        const uint4* xg = reinterpret_cast<const uint4*>(x + k0);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            const uint4 v = __ldg(xp + c);
+            const uint4 v = __ldg(xg + c);
             const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 x2[c * 4 + j].x = __uint_as_float(u[j] << 16);
                 x2[c * 4 + j].y = __uint_as_float(u[j] & 0xFFFF0000u);
+                xq[c * 4 + j] = ((unsigned long long)(u[j] & 0xFFFF0000u) << 32) | (u[j] << 16);
             }
         }
 #pragma unroll
@@ -381,12 +436,12 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
             const int r = phase + q * sh.phases;   // row within the chunk
             part[q] = 0.f;
             if (have && active && r < rows) {
-                const float A = lane_dot<BITS>(sbase + r * sh.row_bytes + lane_code_off, x2);
+                const float A = lane_dot<BITS>(sbase + r * sh.row_bytes + lane_code_off, x2, xq);
                 uint16_t sv, bv;
                 asm volatile("ld.shared.u16 %0, [%1];" : "=h"(sv) : "r"(s_off + (r * groups + g) * 2));
                 asm volatile("ld.shared.u16 %0, [%1];" : "=h"(bv) : "r"(b_off + (r * groups + g) * 2));
                 const float s = bf16_bits_to_float(sv), b = bf16_bits_to_float(bv);
-                part[q] = fmaf(s * kUnscale, A - X, b * X);
+                part[q] = fmaf(s * kUnscale, fmaf(-kOffset, X, A), b * X);
             }
         }
         // all shared reads of this stage are consumed: hand it back
