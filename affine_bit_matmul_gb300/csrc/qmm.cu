@@ -49,7 +49,10 @@ constexpr int kBK = 128;             // K per dequant/MMA stage: two 64-wide gro
 constexpr int kHalfK = 64;           // K per activation slot (one 128-byte swizzle atom)
 constexpr int kMaxRows = 256;        // activation rows per tile (MMA N <= 256)
 constexpr int kMaxSplits = 8;        // K splits per tile = cluster size (portable limit)
-constexpr int kMaxCodeStages = 16;
+constexpr int kMaxCodeStages = 8;    // code slots
+// One code TMA box covers 256 bytes of each of the 128 w rows: the TMA engine
+// handles long row segments far faster than 64-byte ones.
+constexpr int kCodeSlotRowBytes = 256;
 constexpr int kMaxAStages = 6;       // dequantised stages held in tensor memory
 constexpr int kMaxXStages = 16;
 constexpr int kSmemBudget = 224 * 1024;
@@ -57,7 +60,7 @@ constexpr int kTmemCols = 512;       // accumulator + dequantised A stages
 constexpr int kAStageCols = kBK / 2; // one bf16 pair per 32-bit column
 
 struct SmemLayout {
-    int c_bytes, c_stages;    // packed-code ring, one 128-wide K stage per slot
+    int c_bytes, c_stages;    // packed-code ring: slots of kCodeSlotRowBytes per w row
     int x_bytes, x_stages;    // activation ring (MMA B operand), one 64-wide atom per slot
     int c_offset;             // rings: x at 0, then codes
     int bar_offset, total;
@@ -71,7 +74,7 @@ struct SmemLayout {
 __host__ __device__ inline SmemLayout make_layout(int bits, int max_rows) {
     SmemLayout L;
     const int rows16 = (max_rows + 15) & ~15;
-    L.c_bytes = kTileN * kBK * bits / 8;              // 8 KB or 16 KB
+    L.c_bytes = kTileN * kCodeSlotRowBytes;           // 32 KB: 4 (4-bit) or 2 (8-bit) stages
     L.x_bytes = (rows16 / 8) * 1024;                  // 128 B per row, 8-row atoms
     L.x_stages = 6;
     int room = kSmemBudget - L.x_stages * L.x_bytes;
@@ -85,7 +88,7 @@ __host__ __device__ inline SmemLayout make_layout(int bits, int max_rows) {
     }
     L.c_offset = L.x_stages * L.x_bytes;
     L.bar_offset = L.c_offset + L.c_stages * L.c_bytes;
-    // cfull, cempty; afull, aempty; xfull, xempty; accf; tmem base
+    // cfull, cempty (per code slot); afull, aempty; xfull, xempty; accf; tmem base
     L.total = L.bar_offset + (2 * kMaxCodeStages + 2 * kMaxAStages + 2 * kMaxXStages + 1) * 8 +
               16 + 1024;                              // + alignment slack
     return L;
@@ -347,6 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nst = (nkb + 1) / 2;                     // 128-wide stages
     const int groups = p.K / 64;
     const int SC = L.c_stages;
+    constexpr int kStagesPerSlot = kCodeSlotRowBytes / (kBK * BITS / 8);
     const int SX = L.x_stages;
     // tensor memory: accumulator in columns [0, n_mma), dequantised stages
     // of 64 columns from a0 on
@@ -356,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < SC; ++i) {
             mbar_init(&cfull[i], 1);
-            mbar_init(&cempty[i], kDequantThreads / 2);  // one group per stage
+            mbar_init(&cempty[i], kDequantThreads / 2 * kStagesPerSlot);  // 128 per stage
         }
         for (int i = 0; i < SA; ++i) {
             mbar_init(&afull[i], kDequantThreads / 2);
@@ -384,13 +388,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // [128 rows x 128 k] packed codes per stage; a box that runs past K
         // is zero-filled, a second half that belongs to the next K split is
         // loaded but never dequantised
-        constexpr int kWordsPerStage = kBK * BITS / 32;
+        constexpr int kWordsPerSlot = kCodeSlotRowBytes / 4;
+        const int nslots = (nst + kStagesPerSlot - 1) / kStagesPerSlot;
         Ring ring(SC);
-        for (int s = 0; s < nst; ++s, ring.next()) {
-            if (s >= SC && !warp_wait(&cempty[ring.slot], ring.parity ^ 1)) { ok = false; break; }
+        for (int i = 0; i < nslots; ++i, ring.next()) {
+            if (i >= SC && !warp_wait(&cempty[ring.slot], ring.parity ^ 1)) { ok = false; break; }
             if (elect_one()) {
                 mbar_expect_tx(&cfull[ring.slot], (uint32_t)L.c_bytes);
-                const int c0 = kb_begin * (kHalfK * BITS / 32) + s * kWordsPerStage;
+                const int c0 = kb_begin * (kHalfK * BITS / 32) + i * kWordsPerSlot;
                 const uint32_t dst = c_base0 + ring.slot * L.c_bytes;
                 if (GATHER)
                     tma_load_3d(dst, &code_map, c0, n0, e, &cfull[ring.slot]);
@@ -473,14 +478,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // slot and phase of stage s in the code and A rings, advanced by two
         // stages per step (this group's stages), without divisions
         Ring cr(SC), ar(SA);
-        if (grp) {
-            cr.next();
-            ar.next();
-        }
+        int csub = grp;  // stage within the code slot (kStagesPerSlot >= 2)
+        if (grp) ar.next();
         auto stage = [&](int s, const uint32_t (&sb)[4]) -> bool {
             const int cs = cr.slot;
             if (!warp_wait(&cfull[cs], cr.parity)) return false;
-            const uint32_t c_row = c_base0 + cs * L.c_bytes + r * kRowBytes;
+            const uint32_t c_row = c_base0 + cs * L.c_bytes + r * kCodeSlotRowBytes + csub * kRowBytes;
             uint4 cw[BITS];
 #pragma unroll
             for (int j = 0; j < BITS; ++j) cw[j] = ld_shared_v4(c_row + j * 16);
@@ -533,8 +536,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&cempty[cs]);
             tc_fence_before();
             mbar_arrive(&afull[as]);
-            cr.next();  // on to stage s + 2
-            cr.next();
+            csub += 2;  // on to stage s + 2
+            if (csub >= kStagesPerSlot) {
+                csub -= kStagesPerSlot;
+                cr.next();
+            }
             ar.next();
             ar.next();
             return true;
@@ -743,7 +749,7 @@ cudaError_t launch_qmm_tc(const QmmParams& p, int bits, int grid_m, int max_rows
     // packed codes: words along K, rows n, experts
     CUtensorMap cm, xm;
     const cuuint64_t words = (cuuint64_t)p.K * bits / 32;
-    const cuuint32_t box_words = kBK * bits / 32;   // 128 k per stage
+    const cuuint32_t box_words = kCodeSlotRowBytes / 4;   // 256 bytes of each row
     const cuuint32_t estr[3] = {1, 1, 1};
     if (gather) {
         const cuuint64_t dims[3] = {words, (cuuint64_t)p.N, (cuuint64_t)p.E};

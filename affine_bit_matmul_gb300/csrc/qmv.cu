@@ -255,8 +255,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32) qmv_generic_kernel(const __nv_
 
 // ---------------------------------------------------------------- streaming form
 
-constexpr int kStreamStages = 6;
-constexpr int kChunkBytes = 24 * 1024;   // codes per stage, about
+constexpr int kStreamStages = 4;
+constexpr int kChunkBytes = 48 * 1024;   // codes per stage, about
 constexpr int kTargetWarps = 20;
 constexpr int kMaxStreamWarps = 24;
 
