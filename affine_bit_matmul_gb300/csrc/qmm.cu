@@ -76,12 +76,18 @@ __host__ __device__ inline SmemLayout make_layout(int bits, int max_rows) {
     const int rows16 = (max_rows + 15) & ~15;
     L.c_bytes = kTileN * kCodeSlotRowBytes;           // 32 KB: 4 (4-bit) or 2 (8-bit) stages
     L.x_bytes = (rows16 / 8) * 1024;                  // 128 B per row, 8-row atoms
-    L.x_stages = 6;
-    int room = kSmemBudget - L.x_stages * L.x_bytes;
-    L.c_stages = room / L.c_bytes;
-    if (L.c_stages > kMaxCodeStages) L.c_stages = kMaxCodeStages;
-    if (L.c_stages < 2) L.c_stages = 2;
-    room -= L.c_stages * L.c_bytes;
+    // two code slots, up to six activation slots, then more code slots (up
+    // to kMaxCodeStages), then more activation slots (up to kMaxXStages)
+    L.c_stages = 2;
+    int room = kSmemBudget - L.c_stages * L.c_bytes;
+    L.x_stages = room / L.x_bytes;
+    if (L.x_stages > 6) L.x_stages = 6;
+    if (L.x_stages < 2) L.x_stages = 2;
+    room -= L.x_stages * L.x_bytes;
+    while (L.c_stages < kMaxCodeStages && room >= L.c_bytes) {
+        ++L.c_stages;
+        room -= L.c_bytes;
+    }
     while (L.x_stages < kMaxXStages && room >= L.x_bytes) {
         ++L.x_stages;
         room -= L.x_bytes;
@@ -721,6 +727,7 @@ cudaError_t launch_variant(const QmmParams& p, int grid_m, int max_rows, const C
         if (err != cudaSuccess) return err;
         attr_set[dev] = true;
     }
+    if (L.total > 232448) return cudaErrorInvalidConfiguration;  // cannot happen for rows <= 256
     const dim3 grid((p.N + kTileN - 1) / kTileN, grid_m, p.splits);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
