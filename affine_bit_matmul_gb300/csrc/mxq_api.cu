@@ -10,7 +10,7 @@ namespace {
 
 constexpr int kTileN = 128;           // rows of w per CTA in the tensor-core kernel
 constexpr int kMaxRowsPerTile = 256;  // MMA N limit
-constexpr int kGatherRowsPerTile = 128;
+constexpr int kGatherRowsPerTile = 64;  // expert segments average ~36 rows
 constexpr int kMinKBlocksPerSplit = 8;
 constexpr int kMaxSplits = 8;             // portable cluster size
 constexpr int kMaxDevices = 64;
@@ -58,7 +58,7 @@ struct DensePlan {
     int m_tiles, m_tile, tmem_cols, splits, kb_per_split;
 };
 
-DensePlan plan_dense(int M, int K, int N, int sms) {
+DensePlan plan_dense(int M, int K, int N, int bits, int sms) {
     DensePlan pl;
     const int want_tiles = (M + kMaxRowsPerTile - 1) / kMaxRowsPerTile;
     const int per = (M + want_tiles - 1) / want_tiles;
@@ -70,9 +70,11 @@ DensePlan plan_dense(int M, int K, int N, int sms) {
     const int n_tiles = (N + kTileN - 1) / kTileN;
     const int tiles = n_tiles * pl.m_tiles;
     const int KB = K / 64;
+    // tiles of <= 64 rows with 4-bit codes run two CTAs per SM
+    const int slots = (bits == 4 && pl.m_tile <= 64) ? 2 * sms : sms;
     int splits = 1;
-    if (tiles < sms) {
-        splits = sms / tiles;
+    if (tiles < slots) {
+        splits = slots / tiles;
         const int max_by_k = KB / kMinKBlocksPerSplit;
         if (splits > max_by_k) splits = max_by_k;
         if (splits > kMaxSplits) splits = kMaxSplits;
@@ -141,7 +143,7 @@ mxq_status mxq_qmm(const void* x, const uint32_t* w, const void* scales, const v
     int sms = 0;
     st = check_device(&sms);
     if (st != MXQ_OK) return st;
-    const DensePlan pl = plan_dense(M, K, N, sms);
+    const DensePlan pl = plan_dense(M, K, N, bits, sms);
     if (pl.m_tiles > 65535) return MXQ_ERR_UNSUPPORTED;  // grid.y limit
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (dev_status && cudaMemsetAsync(dev_status, 0, sizeof(int32_t), s) != cudaSuccess)

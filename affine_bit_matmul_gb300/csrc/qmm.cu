@@ -57,6 +57,16 @@ constexpr int kMaxAStages = 6;       // dequantised stages held in tensor memory
 constexpr int kMaxXStages = 16;
 constexpr int kSmemBudget = 224 * 1024;
 constexpr int kTmemCols = 512;       // accumulator + dequantised A stages
+// Compact mode (tiles of at most 64 activation rows, 4-bit codes): half the
+// shared and tensor memory, so two CTAs share an SM and two pipelines hide
+// each other's latency.
+constexpr int kCompactRows = 64;
+constexpr int kCompactSmemBudget = 108 * 1024;
+constexpr int kCompactTmemCols = 256;
+
+__host__ __device__ constexpr bool compact_mode(int bits, int max_rows) {
+    return bits == 4 && max_rows <= kCompactRows;
+}
 constexpr int kAStageCols = kBK / 2; // one bf16 pair per 32-bit column
 
 struct SmemLayout {
@@ -73,13 +83,14 @@ struct SmemLayout {
 // activation slots.
 __host__ __device__ inline SmemLayout make_layout(int bits, int max_rows) {
     SmemLayout L;
+    const int budget = compact_mode(bits, max_rows) ? kCompactSmemBudget : kSmemBudget;
     const int rows16 = (max_rows + 15) & ~15;
     L.c_bytes = kTileN * kCodeSlotRowBytes;           // 32 KB: 4 (4-bit) or 2 (8-bit) stages
     L.x_bytes = (rows16 / 8) * 1024;                  // 128 B per row, 8-row atoms
     // two code slots, up to six activation slots, then more code slots (up
     // to kMaxCodeStages), then more activation slots (up to kMaxXStages)
     L.c_stages = 2;
-    int room = kSmemBudget - L.c_stages * L.c_bytes;
+    int room = budget - L.c_stages * L.c_bytes;
     L.x_stages = room / L.x_bytes;
     if (L.x_stages > 6) L.x_stages = 6;
     if (L.x_stages < 2) L.x_stages = 2;
@@ -181,6 +192,11 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
             smem_u32(bar)),
         "r"(bytes)
         : "memory");
+}
+
+// Bring a tensor map into the descriptor cache ahead of its first use.
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
@@ -313,8 +329,8 @@ __device__ __forceinline__ void flag_status(int32_t* status, int bits) {
     if (status) atomicOr(status, bits);
 }
 
-template <int BITS, bool GATHER>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int BITS, bool GATHER, bool COMPACT>
+__global__ void __launch_bounds__(kThreads, COMPACT ? 2 : 1)
     qmm_tc_kernel(const QmmParams p, int max_rows, const __grid_constant__ CUtensorMap code_map,
                   const __grid_constant__ CUtensorMap x_map) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -361,8 +377,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tensor memory: accumulator in columns [0, n_mma), dequantised stages
     // of 64 columns from a0 on
     const int a0 = (n_mma + kAStageCols - 1) / kAStageCols * kAStageCols;
-    const int SA = min(kMaxAStages, (kTmemCols - a0) / kAStageCols);
+    constexpr int kCols = COMPACT ? kCompactTmemCols : kTmemCols;
+    const int SA = min(kMaxAStages, (kCols - a0) / kAStageCols);
 
+    if (warp == kCodeWarp && lane == 0) prefetch_tmap(&code_map);
+    if (warp == kXWarp0 && lane == 0) prefetch_tmap(&x_map);
     if (threadIdx.x == 0) {
         for (int i = 0; i < SC; ++i) {
             mbar_init(&cfull[i], 1);
@@ -380,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init_fence();
     }
     if (warp == kMmaWarp) {
-        tmem_alloc(tmem_slot, (uint32_t)kTmemCols);
+        tmem_alloc(tmem_slot, (uint32_t)kCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -687,7 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // make sure no MMA is still writing tensor memory (bounded wait)
         if (lane == 0 && !ok) (void)mbar_wait(accf, 0);
         __syncwarp();
-        tmem_dealloc(tmem, (uint32_t)kTmemCols);
+        tmem_dealloc(tmem, (uint32_t)kCols);
     }
 }
 
@@ -711,7 +730,7 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-template <int BITS, bool GATHER>
+template <int BITS, bool GATHER, bool COMPACT>
 cudaError_t launch_variant(const QmmParams& p, int grid_m, int max_rows, const CUtensorMap& cm,
                            const CUtensorMap& xm, cudaStream_t stream) {
     const SmemLayout L = make_layout(BITS, max_rows);
@@ -721,7 +740,7 @@ cudaError_t launch_variant(const QmmParams& p, int grid_m, int max_rows, const C
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-        cudaError_t err = cudaFuncSetAttribute(qmm_tc_kernel<BITS, GATHER>,
+        cudaError_t err = cudaFuncSetAttribute(qmm_tc_kernel<BITS, GATHER, COMPACT>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                232448);
         if (err != cudaSuccess) return err;
@@ -741,7 +760,7 @@ cudaError_t launch_variant(const QmmParams& p, int grid_m, int max_rows, const C
     attr[0].val.clusterDim.z = p.splits;  // the K splits of one tile form a cluster
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t err = cudaLaunchKernelEx(&cfg, qmm_tc_kernel<BITS, GATHER>, p, max_rows, cm, xm);
+    cudaError_t err = cudaLaunchKernelEx(&cfg, qmm_tc_kernel<BITS, GATHER, COMPACT>, p, max_rows, cm, xm);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
@@ -784,10 +803,15 @@ cudaError_t launch_qmm_tc(const QmmParams& p, int bits, int grid_m, int max_rows
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     if (bits == 4)
-        return gather ? launch_variant<4, true>(p, grid_m, max_rows_per_tile, cm, xm, stream)
-                      : launch_variant<4, false>(p, grid_m, max_rows_per_tile, cm, xm, stream);
-    return gather ? launch_variant<8, true>(p, grid_m, max_rows_per_tile, cm, xm, stream)
-                  : launch_variant<8, false>(p, grid_m, max_rows_per_tile, cm, xm, stream);
+    {
+        if (compact_mode(4, max_rows_per_tile))
+            return gather ? launch_variant<4, true, true>(p, grid_m, max_rows_per_tile, cm, xm, stream)
+                          : launch_variant<4, false, true>(p, grid_m, max_rows_per_tile, cm, xm, stream);
+        return gather ? launch_variant<4, true, false>(p, grid_m, max_rows_per_tile, cm, xm, stream)
+                      : launch_variant<4, false, false>(p, grid_m, max_rows_per_tile, cm, xm, stream);
+    }
+    return gather ? launch_variant<8, true, false>(p, grid_m, max_rows_per_tile, cm, xm, stream)
+                  : launch_variant<8, false, false>(p, grid_m, max_rows_per_tile, cm, xm, stream);
 }
 
 }  // namespace mxq
