@@ -70,8 +70,8 @@ DensePlan plan_dense(int M, int K, int N, int bits, int sms) {
     const int n_tiles = (N + kTileN - 1) / kTileN;
     const int tiles = n_tiles * pl.m_tiles;
     const int KB = K / 64;
-    // tiles of <= 64 rows with 4-bit codes run two CTAs per SM
-    const int slots = (bits == 4 && pl.m_tile <= 64) ? 2 * sms : sms;
+    const int slots = sms;
+    (void)bits;
     int splits = 1;
     if (tiles < slots) {
         splits = slots / tiles;

@@ -64,8 +64,8 @@ constexpr int kCompactRows = 64;
 constexpr int kCompactSmemBudget = 108 * 1024;
 constexpr int kCompactTmemCols = 256;
 
-__host__ __device__ constexpr bool compact_mode(int bits, int max_rows) {
-    return bits == 4 && max_rows <= kCompactRows;
+__host__ __device__ constexpr bool compact_mode(int bits, int max_rows, bool gather) {
+    return gather && bits == 4 && max_rows <= kCompactRows;
 }
 constexpr int kAStageCols = kBK / 2; // one bf16 pair per 32-bit column
 
@@ -81,9 +81,9 @@ struct SmemLayout {
 // latency and the packed codes stream from HBM with up to two: at least six
 // activation slots, then as many code stages as fit (up to 16), then more
 // activation slots.
-__host__ __device__ inline SmemLayout make_layout(int bits, int max_rows) {
+__host__ __device__ inline SmemLayout make_layout(int bits, int max_rows, bool compact) {
     SmemLayout L;
-    const int budget = compact_mode(bits, max_rows) ? kCompactSmemBudget : kSmemBudget;
+    const int budget = compact ? kCompactSmemBudget : kSmemBudget;
     const int rows16 = (max_rows + 15) & ~15;
     L.c_bytes = kTileN * kCodeSlotRowBytes;           // 32 KB: 4 (4-bit) or 2 (8-bit) stages
     L.x_bytes = (rows16 / 8) * 1024;                  // 128 B per row, 8-row atoms
@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, COMPACT ? 2 : 1)
     qmm_tc_kernel(const QmmParams p, int max_rows, const __grid_constant__ CUtensorMap code_map,
                   const __grid_constant__ CUtensorMap x_map) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    const SmemLayout L = make_layout(BITS, max_rows);
+    const SmemLayout L = make_layout(BITS, max_rows, COMPACT);
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     uint64_t* cfull = reinterpret_cast<uint64_t*>(smem + L.bar_offset);
@@ -733,7 +733,7 @@ EncodeTiledFn encode_fn() {
 template <int BITS, bool GATHER, bool COMPACT>
 cudaError_t launch_variant(const QmmParams& p, int grid_m, int max_rows, const CUtensorMap& cm,
                            const CUtensorMap& xm, cudaStream_t stream) {
-    const SmemLayout L = make_layout(BITS, max_rows);
+    const SmemLayout L = make_layout(BITS, max_rows, COMPACT);
     // the shared-memory opt-in is per device; do it once each
     static bool attr_set[64] = {};
     int dev = 0;
@@ -804,7 +804,8 @@ cudaError_t launch_qmm_tc(const QmmParams& p, int bits, int grid_m, int max_rows
         return cudaErrorInvalidValue;
     if (bits == 4)
     {
-        if (compact_mode(4, max_rows_per_tile))
+        // dense small-M launches split K instead (more CTAs, one per SM)
+        if (compact_mode(4, max_rows_per_tile, gather))
             return gather ? launch_variant<4, true, true>(p, grid_m, max_rows_per_tile, cm, xm, stream)
                           : launch_variant<4, false, true>(p, grid_m, max_rows_per_tile, cm, xm, stream);
         return gather ? launch_variant<4, true, false>(p, grid_m, max_rows_per_tile, cm, xm, stream)
