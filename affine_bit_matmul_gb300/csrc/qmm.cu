@@ -50,9 +50,15 @@ constexpr int kHalfK = 64;           // K per activation slot (one 128-byte swiz
 constexpr int kMaxRows = 256;        // activation rows per tile (MMA N <= 256)
 constexpr int kMaxSplits = 8;        // K splits per tile = cluster size (portable limit)
 constexpr int kMaxCodeStages = 8;    // code slots
-// One code TMA box covers 256 bytes of each of the 128 w rows: the TMA engine
-// handles long row segments far faster than 64-byte ones.
+// A code slot holds 256 bytes of each of the 128 w rows (the TMA engine
+// handles long row segments far faster than 64-byte ones), as two boxes of
+// 128 bytes per row stored with the 128-byte swizzle: 16-byte chunk c of row
+// r sits at chunk c ^ (r % 8) of its 128-byte line, so the eight threads of
+// a quarter warp, reading the same chunk of eight consecutive rows, hit
+// eight different bank groups.
 constexpr int kCodeSlotRowBytes = 256;
+constexpr int kCodeBoxRowBytes = 128;
+constexpr int kCodeBoxBytes = kTileN * kCodeBoxRowBytes;
 constexpr int kMaxAStages = 6;       // dequantised stages held in tensor memory
 constexpr int kMaxXStages = 16;
 constexpr int kSmemBudget = 224 * 1024;
@@ -414,18 +420,27 @@ __global__ void __launch_bounds__(kThreads, COMPACT ? 2 : 1)
         // is zero-filled, a second half that belongs to the next K split is
         // loaded but never dequantised
         constexpr int kWordsPerSlot = kCodeSlotRowBytes / 4;
+        constexpr int kWordsPerBox = kCodeBoxRowBytes / 4;
+        const int words = p.K * BITS / 32;
         const int nslots = (nst + kStagesPerSlot - 1) / kStagesPerSlot;
         Ring ring(SC);
         for (int i = 0; i < nslots; ++i, ring.next()) {
             if (i >= SC && !warp_wait(&cempty[ring.slot], ring.parity ^ 1)) { ok = false; break; }
             if (elect_one()) {
-                mbar_expect_tx(&cfull[ring.slot], (uint32_t)L.c_bytes);
                 const int c0 = kb_begin * (kHalfK * BITS / 32) + i * kWordsPerSlot;
+                // a box that starts past the end of the row is not loaded
+                // (its stages are never dequantised)
+                const int nbox = c0 + kWordsPerBox < words ? 2 : 1;
+                mbar_expect_tx(&cfull[ring.slot], (uint32_t)(nbox * kCodeBoxBytes));
                 const uint32_t dst = c_base0 + ring.slot * L.c_bytes;
-                if (GATHER)
-                    tma_load_3d(dst, &code_map, c0, n0, e, &cfull[ring.slot]);
-                else
-                    tma_load_2d(dst, &code_map, c0, n0, &cfull[ring.slot]);
+                for (int b = 0; b < nbox; ++b) {
+                    if (GATHER)
+                        tma_load_3d(dst + b * kCodeBoxBytes, &code_map, c0 + b * kWordsPerBox, n0,
+                                    e, &cfull[ring.slot]);
+                    else
+                        tma_load_2d(dst + b * kCodeBoxBytes, &code_map, c0 + b * kWordsPerBox, n0,
+                                    &cfull[ring.slot]);
+                }
             }
             __syncwarp();
         }
@@ -508,10 +523,16 @@ __global__ void __launch_bounds__(kThreads, COMPACT ? 2 : 1)
         auto stage = [&](int s, const uint32_t (&sb)[4]) -> bool {
             const int cs = cr.slot;
             if (!warp_wait(&cfull[cs], cr.parity)) return false;
-            const uint32_t c_row = c_base0 + cs * L.c_bytes + r * kCodeSlotRowBytes + csub * kRowBytes;
+            // this stage's kRowBytes of row r: box (off / 128), chunks from
+            // (off % 128) / 16 on, each at its swizzled place in the line
+            const int off = csub * kRowBytes;
+            const uint32_t c_line = c_base0 + cs * L.c_bytes + (off / kCodeBoxRowBytes) * kCodeBoxBytes +
+                                    r * kCodeBoxRowBytes;
+            const int chunk0 = (off % kCodeBoxRowBytes) / 16;
             uint4 cw[BITS];
 #pragma unroll
-            for (int j = 0; j < BITS; ++j) cw[j] = ld_shared_v4(c_row + j * 16);
+            for (int j = 0; j < BITS; ++j)
+                cw[j] = ld_shared_v4(c_line + (uint32_t)(((chunk0 + j) ^ (r & 7)) << 4));
             const int as = ar.slot;
             if (s >= SA && !warp_wait(&aempty[as], ar.parity ^ 1)) return false;
             tc_fence_after();
@@ -775,14 +796,14 @@ cudaError_t launch_qmm_tc(const QmmParams& p, int bits, int grid_m, int max_rows
     // packed codes: words along K, rows n, experts
     CUtensorMap cm, xm;
     const cuuint64_t words = (cuuint64_t)p.K * bits / 32;
-    const cuuint32_t box_words = kCodeSlotRowBytes / 4;   // 256 bytes of each row
+    const cuuint32_t box_words = kCodeBoxRowBytes / 4;    // 128 bytes of each row
     const cuuint32_t estr[3] = {1, 1, 1};
     if (gather) {
         const cuuint64_t dims[3] = {words, (cuuint64_t)p.N, (cuuint64_t)p.E};
         const cuuint64_t strides[2] = {words * 4, words * 4 * (cuuint64_t)p.N};
         const cuuint32_t box[3] = {box_words, (cuuint32_t)kTileN, 1};
         if (enc(&cm, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint32_t*>(p.w), dims, strides,
-                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     } else {
@@ -790,7 +811,7 @@ cudaError_t launch_qmm_tc(const QmmParams& p, int bits, int grid_m, int max_rows
         const cuuint64_t strides[1] = {words * 4};
         const cuuint32_t box[2] = {box_words, (cuuint32_t)kTileN};
         if (enc(&cm, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(p.w), dims, strides,
-                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }

@@ -37,6 +37,8 @@ if ROOT not in sys.path:
 
 import synth  # noqa: E402
 
+STEPS_PER_GRAPH = 20
+
 METRIC = "qmv HBM GB/s and qmm/gather_qmm TFLOPS on 1 GB300, % of roofline"
 DECODE_CASES = [(5120, 17408, 4), (5120, 17408, 8), (17408, 5120, 4), (17408, 5120, 8)]
 WORKLOAD = ("qmv decode M=1: K=5120 N=17408 and K=17408 N=5120, 4-bit and 8-bit, group 64, "
@@ -63,6 +65,39 @@ def load_peaks():
 
 
 # ------------------------------------------------------------------ helpers
+
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "qmv_stream_decode_traffic.txt")
+QMV_SOURCES = [os.path.join(ROOT, "affine_bit_matmul_gb300", "csrc", f)
+               for f in ("qmv.cu", "mxq_device.cuh")]
+
+
+def qmv_source_hash():
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in QMV_SOURCES:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_per_launch():
+    """DRAM bytes (read + write) per qmv launch, mean over the four decode
+    cases, from the committed ncu capture; None when the kernel sources have
+    changed since that capture (or there is none)."""
+    try:
+        fields = {}
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields[k.strip()] = v.strip()
+        if fields.get("source_hash") != qmv_source_hash():
+            return None
+        return int(fields["mean_dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
 
 
 class Clocks:
@@ -179,10 +214,30 @@ class DenseInputs:
         self.y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
 
 
+# --no-graphs issues every launch directly on the stream (same kernels, same
+# arguments); ncu's launch list is taken that way because it does not follow
+# launches made during stream capture.
+USE_GRAPHS = True
+
+
+class _Direct:
+    """Stands in for a CUDA graph: replay() issues the launches directly."""
+
+    def __init__(self, fn, count):
+        self.fn, self.count = fn, count
+
+    def replay(self):
+        for i in range(self.count):
+            self.fn(i)
+
+
 def capture(fn, count):
     """A CUDA graph of fn(0), ..., fn(count - 1) (launch overhead out of the
     timed work; inputs alternate between copies by the index)."""
     import torch
+
+    if not USE_GRAPHS:
+        return _Direct(fn, count)
 
     g = torch.cuda.CUDAGraph()
     side = torch.cuda.Stream()
@@ -250,7 +305,10 @@ def run_mxq(args):
             w, s_, b = c.copies[i % 2]
             mxq.qmv(c.x[0], w, s_, b, c.bits, out=c.y[0])
 
-    # one graph per step parity: the four launches of a step, back to back
+    # graphs of STEPS_PER_GRAPH steps (inputs alternate by step parity) plus
+    # one-step graphs per parity for a remainder: exactly args.steps steps run
+    # in the timed region
+    big = capture(lambda j: step(j), STEPS_PER_GRAPH)
     graphs = [capture(lambda j, par=par: step(par), 1) for par in (0, 1)]
     for i in range(args.warmup):
         graphs[i % 2].replay()
@@ -262,26 +320,32 @@ def run_mxq(args):
     barrier(world)
     torch.cuda.synchronize()
     t0.record(stream)
-    for i in range(args.steps):
+    full = args.steps // STEPS_PER_GRAPH
+    for _ in range(full):
+        big.replay()
+    for i in range(full * STEPS_PER_GRAPH, args.steps):
         graphs[i % 2].replay()
     t1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
-    elapsed = max_over_ranks(t0.elapsed_time(t1) * 1e-3, world)
+    local_elapsed = t0.elapsed_time(t1) * 1e-3
+    elapsed = max_over_ranks(local_elapsed, world)
     value = step_bytes * args.steps * world / elapsed / 1e9
+    # the timed region holds nothing but qmv launches (four per step): the
+    # kernel's algorithmic bytes per launch over its mean launch duration
+    # there is this rank's step bytes over its time per step
+    achieved = step_bytes * args.steps / local_elapsed / 1e9
 
-    # per-kernel device time: each case alone, graphs of 20 launches
+    # per-case device time, each case alone (graphs of 20 launches): the
+    # breakdown of the step, not the roofline figure
     per_case = []
-    qmv_time = 0.0
     for c in cases:
         t, _ = time_launches(
             lambda i, c=c: mxq.qmv(c.x[0], *c.copies[i % 2], c.bits, out=c.y[0]), 20, stream)
-        qmv_time += t
         nb = qmv_bytes(c.K, c.N, c.bits)
         per_case.append({"K": c.K, "N": c.N, "bits": c.bits, "us": t * 1e6, "GB_s": nb / t / 1e9,
                          "frac_hbm": nb / t / 1e9 / hbm})
-    achieved = step_bytes / qmv_time / 1e9
 
     # ---- end to end through the public API with host buffers
     pinned = []
@@ -343,9 +407,10 @@ def run_mxq(args):
                    "l2": "inputs larger than L2: each case alternates two input copies "
                          "(580 MB working set vs 129 MB L2)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": {"bound": "hbm", "kernel": "qmv_kernel (4- and 8-bit)",
+        "roofline": {"bound": "hbm", "kernel": "qmv_stream_kernel (4- and 8-bit)",
                      "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(achieved / hbm, 4), "traffic": None,
+                     "frac": round(achieved / hbm, 4), "traffic": traffic_per_launch(),
+                     "algorithmic_bytes_per_launch": step_bytes // len(cases),
                      "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs copy bandwidth)"},
         "per_case": per_case,
         "gpu_launches": len(cases) * args.steps,
@@ -523,7 +588,14 @@ def run_profile(args):
     torch.cuda.set_device(dev)
     name = args.profile
     launches = args.profile_launches
-    if name.startswith("qmv"):
+    if name == "decode":
+        for K, N, bits in DECODE_CASES:
+            d = DenseInputs(synth.dense_weights(N, K, seed=0), 1, K, N, bits, dev, copies=2)
+            for i in range(launches):
+                mxq.qmv(d.x[0], *d.copies[i % 2], bits, out=d.y[0])
+            torch.cuda.synchronize()
+            del d
+    elif name.startswith("qmv"):
         K, N, bits = {"qmv4": (5120, 17408, 4), "qmv8": (5120, 17408, 8),
                       "qmv4t": (17408, 5120, 4), "qmv8t": (17408, 5120, 8)}[name]
         d = DenseInputs(synth.dense_weights(N, K, seed=0), 1, K, N, bits, dev, copies=2)
@@ -559,7 +631,7 @@ def run_profile(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--profile", default=None,
-                    help="plain launches of one workload for ncu: qmv4 qmv8 qmv4t qmv8t qmm "
+                    help="plain launches of one workload for ncu: decode qmv4 qmv8 qmv4t qmv8t qmm "
                          "qmm600 qmm128 qmm8 qmm32 gather_up gather_down")
     ap.add_argument("--profile-launches", type=int, default=4)
     ap.add_argument("--gpus", type=int, default=1)
@@ -569,7 +641,12 @@ def main():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-graphs", action="store_true",
+                    help="issue every launch directly instead of through CUDA graphs")
     args = ap.parse_args()
+    if args.no_graphs:
+        global USE_GRAPHS
+        USE_GRAPHS = False
     if args.warmup < 3:
         args.warmup = 3
     if args.profile:
