@@ -6,7 +6,7 @@
 //
 // Two kernels share the arithmetic below.
 //
-// qmv_stream_kernel (K a multiple of 512, K <= 24576, 16-byte aligned
+// qmv_stream_kernel (K a multiple of 512, K <= 20480, 16-byte aligned
 // scales/biases): persistent CTAs, one per SM.  A producer thread streams
 // chunks of R consecutive rows (their codes, scales and biases are each one
 // contiguous block) into a ring of shared-memory stages with bulk async
@@ -25,12 +25,15 @@
 //    row;
 //  * a CTA has one warp per K segment and owns a block of ROWS output rows;
 //    each lane keeps its 32/16 activations in registers for all the rows;
-//  * the codes are turned into floats 1 + q*2^-7 (4-bit) or 1 + q*2^-15
-//    (8-bit) by placing them in the mantissa of a constant with one byte
-//    permute each; the lane's products are summed in fp32 and the affine
-//    terms are applied once per lane and row:
-//        sum_k x_k (s q_k + b) = s * 2^p * (sum_k x_k v_k - X) + b * X,
-//    with X = sum_k x_k over the lane's values, p = 7 or 15;
+//  * the affine terms are applied once per lane and row:
+//        sum_k x_k (s q_k + b) = s * (sum_k x_k q_k) + b * X,
+//    with X = sum_k x_k over the lane's values (fp32);
+//  * the streaming kernel forms sum_k x_k q_k exactly with integer 4-way
+//    dot products over byte planes of the activations (see lane_dot_int);
+//    the direct-load kernel turns the codes into floats 1 + q*2^-7 (4-bit)
+//    or 1 + q*2^-15 (8-bit) by placing them in the mantissa of a constant
+//    with one byte permute each, sums x_k v_k in fp32 and uses
+//    sum_k x_k q_k = 2^p * (sum_k x_k v_k - X), p = 7 or 15;
 //  * per-row partials are reduced across lanes with a reduce-scatter
 //    butterfly, then across warps through shared memory in a fixed order,
 //    so results are identical from run to run.
@@ -91,53 +94,6 @@ __device__ __forceinline__ float dot_chunk4(const uint4 c, const float2 (&x2)[16
         }
     }
     return acc.x + acc.y;
-}
-
-// One word of 4-bit codes against 8 activations held as four fp32 pairs
-// (x_{2j}, x_{2j+1}): v_k = 1 + q_k/128 built by byte permutes straight into
-// register pairs, accumulated with packed fp32 FMAs (acc holds two partial
-// sums).  Written as one block so the pairs need no register moves.
-__device__ __forceinline__ void word4_f32x2(uint32_t wd, const unsigned long long (&xq)[4],
-                                            unsigned long long& acc) {
-    asm("{\n\t"
-        ".reg .b32 lo, hi, v0, v1;\n\t"
-        ".reg .b64 p;\n\t"
-        "lop3.b32 lo, %1, 0x0F0F0F0F, 0x80808080, 0xEA;\n\t"   // (w & m) | c
-        "shr.u32 hi, %1, 4;\n\t"
-        "lop3.b32 hi, hi, 0x0F0F0F0F, 0x80808080, 0xEA;\n\t"
-        "prmt.b32 v0, lo, 0x3F000000, 0x7044;\n\t"
-        "prmt.b32 v1, hi, 0x3F000000, 0x7044;\n\t"
-        "mov.b64 p, {v0, v1};\n\t"
-        "fma.rn.f32x2 %0, p, %2, %0;\n\t"
-        "prmt.b32 v0, lo, 0x3F000000, 0x7144;\n\t"
-        "prmt.b32 v1, hi, 0x3F000000, 0x7144;\n\t"
-        "mov.b64 p, {v0, v1};\n\t"
-        "fma.rn.f32x2 %0, p, %3, %0;\n\t"
-        "prmt.b32 v0, lo, 0x3F000000, 0x7244;\n\t"
-        "prmt.b32 v1, hi, 0x3F000000, 0x7244;\n\t"
-        "mov.b64 p, {v0, v1};\n\t"
-        "fma.rn.f32x2 %0, p, %4, %0;\n\t"
-        "prmt.b32 v0, lo, 0x3F000000, 0x7344;\n\t"
-        "prmt.b32 v1, hi, 0x3F000000, 0x7344;\n\t"
-        "mov.b64 p, {v0, v1};\n\t"
-        "fma.rn.f32x2 %0, p, %5, %0;\n\t"
-        "}"
-        : "+l"(acc)
-        : "r"(wd), "l"(xq[0]), "l"(xq[1]), "l"(xq[2]), "l"(xq[3]));
-}
-
-// Sum over the lane's 32 four-bit codes of x_k * (1 + q_k/128), from fp32
-// activation pairs xq[j] = (x_{2j}, x_{2j+1}).
-__device__ __forceinline__ float dot_chunk4_f32x2(const uint4 c,
-                                                  const unsigned long long (&xq)[16]) {
-    const uint32_t words[4] = {c.x, c.y, c.z, c.w};
-    unsigned long long acc = 0ull;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-        const unsigned long long q4[4] = {xq[4 * w], xq[4 * w + 1], xq[4 * w + 2], xq[4 * w + 3]};
-        word4_f32x2(words[w], q4, acc);
-    }
-    return __uint_as_float((uint32_t)acc) + __uint_as_float((uint32_t)(acc >> 32));
 }
 
 // Same for 16 eight-bit codes: v_k = 1 + q_k * 2^-15.  x2 holds 8 pairs.
@@ -258,7 +214,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) qmv_generic_kernel(const __nv_
 constexpr int kStreamStages = 4;
 constexpr int kChunkBytes = 48 * 1024;   // codes per stage, about
 constexpr int kTargetWarps = 20;
-constexpr int kMaxStreamWarps = 24;
+constexpr int kMaxStreamWarps = 20;  // K <= 20480; the activation planes need ~80 registers
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
                                          uint64_t* bar) {
@@ -304,29 +260,118 @@ struct StreamShape {
     int nchunks;
 };
 
-// Dot of one lane's 32 codes with its 32 activations, v_k = 1 + q_k 2^-p.
+// ---- exact integer dot products (streaming form)
+//
+// A lane's 32 activations are written as integers on a common scale:
+// x_k = X_k * 2^(emax - 149), emax the largest biased exponent among them,
+// so X_k = (bf16 significand) * 2^(e_k - emax + 15) is an integer below
+// 2^23 in magnitude (exact unless x_k lies more than 2^15 below the lane's
+// largest value; then it is rounded to the nearest integer, an error under
+// 2^-23 of the largest).  X_k is split into byte planes
+// X_k = a_k 2^16 + b_k 2^8 + c_k (a_k signed, b_k and c_k unsigned), and the
+// code sums sum_k q_k a_k, sum_k q_k b_k, sum_k q_k c_k are exact 4-way
+// integer dot products (dp4a).  The lane's sum_k x_k q_k is then
+// ((A * 256 + B) * 256 + C) * 2^(emax - 149) with one fp32 rounding, so the
+// fp32 accumulation of the method is kept and the codes need no conversion
+// to floating point at all.
+
+__device__ __forceinline__ int dp4a_su(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t dp4a_uu(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+__device__ __forceinline__ int bf16_exp_eff(uint32_t h) {
+    const int e = (int)((h >> 7) & 0xFFu);
+    return e > 0 ? e : 1;  // subnormals and zero share exponent 1
+}
+
+// X_k of one bf16 value on the scale 2^(emax - 149).
+__device__ __forceinline__ int bf16_fixed24(uint32_t h, int emax) {
+    const int e = (int)((h >> 7) & 0xFFu);
+    const int mag = (e ? 128 : 0) | (int)(h & 0x7Fu);
+    const int sh = (e > 0 ? e : 1) - emax + 15;  // <= 15
+    int v;
+    if (sh >= 0)
+        v = mag << sh;
+    else if (sh >= -9)
+        v = (mag + (1 << (-sh - 1))) >> -sh;   // round half up; 0 below -9
+    else
+        v = 0;
+    return (h & 0x8000u) ? -v : v;
+}
+
+// Byte planes of a lane's 32 activations, arranged like its codes: for
+// 4-bit codes register 2w holds k = 8w, 8w+2, 8w+4, 8w+6 (the even nibbles
+// of word w) and register 2w+1 the odd ones; for 8-bit codes register w
+// holds k = 4w .. 4w+3.
+struct XPlanes {
+    uint32_t a[8], b[8], c[8];
+};
+
+// u holds the 32 activations as bf16 pairs (k = 2j in the low half of u[j]).
 template <int BITS>
-__device__ __forceinline__ float lane_dot(uint32_t codes_addr, const float2 (&x2)[16],
-                                          const unsigned long long (&xq)[16]) {
-    if (BITS == 4) {
-        uint4 c;
-        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                     : "=r"(c.x), "=r"(c.y), "=r"(c.z), "=r"(c.w)
-                     : "r"(codes_addr));
-        return dot_chunk4_f32x2(c, xq);
-    } else {
-        uint4 c0, c1;
+__device__ __forceinline__ void make_planes(const uint32_t (&u)[16], int emax, XPlanes& P) {
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        uint32_t a = 0, b = 0, c = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int k = BITS == 4 ? (r >> 1) * 8 + 2 * i + (r & 1) : r * 4 + i;
+            const uint32_t h = (u[k >> 1] >> (16 * (k & 1))) & 0xFFFFu;
+            const uint32_t X = (uint32_t)bf16_fixed24(h, emax);
+            a |= ((X >> 16) & 0xFFu) << (8 * i);
+            b |= ((X >> 8) & 0xFFu) << (8 * i);
+            c |= (X & 0xFFu) << (8 * i);
+        }
+        P.a[r] = a;
+        P.b[r] = b;
+        P.c[r] = c;
+    }
+}
+
+// sum_k X_k q_k over the lane's 32 codes (exact up to the final rounding).
+template <int BITS>
+__device__ __forceinline__ float lane_dot_int(uint32_t codes_addr, const XPlanes& P) {
+    uint32_t wd[8];
+    {
+        uint4 c0;
         asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
                      : "=r"(c0.x), "=r"(c0.y), "=r"(c0.z), "=r"(c0.w)
                      : "r"(codes_addr));
-        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                     : "=r"(c1.x), "=r"(c1.y), "=r"(c1.z), "=r"(c1.w)
-                     : "r"(codes_addr + 16));
-        float2 hi[16];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) hi[j] = x2[8 + j];
-        return dot_chunk8(c0, x2) + dot_chunk8(c1, hi);
+        wd[0] = c0.x; wd[1] = c0.y; wd[2] = c0.z; wd[3] = c0.w;
+        if (BITS == 8) {
+            uint4 c1;
+            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(c1.x), "=r"(c1.y), "=r"(c1.z), "=r"(c1.w)
+                         : "r"(codes_addr + 16));
+            wd[4] = c1.x; wd[5] = c1.y; wd[6] = c1.z; wd[7] = c1.w;
+        }
     }
+    int A = 0;
+    uint32_t B = 0, C = 0;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        uint32_t q;
+        if (BITS == 4)
+            q = (r & 1) ? (wd[r >> 1] >> 4) & 0x0F0F0F0Fu : wd[r >> 1] & 0x0F0F0F0Fu;
+        else
+            q = wd[r];
+        A = dp4a_su(P.a[r], q, A);
+        B = dp4a_uu(P.b[r], q, B);
+        C = dp4a_uu(P.c[r], q, C);
+    }
+    // |A| <= 32*15*128 and B < 32*15*256 (4-bit), or 32*255*128 and
+    // 32*255*256 (8-bit): A*256 + B stays below 2^31 and converts exactly
+    // when below 2^24 (always for 4-bit)
+    const int AB = A * 256 + (int)B;
+    return fmaf((float)AB, 256.f, (float)C);
 }
 
 template <int BITS, int RPW>
@@ -335,9 +380,6 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
                       const uint16_t* __restrict__ scales, const uint16_t* __restrict__ biases,
                       __nv_bfloat16* __restrict__ y, int K, int N, const StreamShape sh,
                       int32_t* status) {
-    // A = sum x v with v = 1 + q 2^-7 (4-bit) or 1 + q 2^-15 (8-bit)
-    constexpr float kUnscale = BITS == 4 ? 128.f : 32768.f;
-    constexpr float kOffset = 1.f;
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ uint64_t full[kStreamStages], empty[kStreamStages];
     __shared__ float red[2][kMaxStreamWarps * 8];
@@ -392,29 +434,33 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
     const int phase = warp / sh.nseg;
     const int k0 = seg * 1024 + lane * 32;   // this lane's 32 values
     const bool active = k0 < K;
-    float2 x2[16];              // (x_{2j}, x_{2j+1}) as floats
-    unsigned long long xq[16];  // the same pairs packed for fma.rn.f32x2
-    float X = 0.f;
+    XPlanes P;
+    float X = 0.f;          // sum of the lane's activations (bias term)
+    float xscale = 0.f;     // 2^(emax - 149)
+    {
+        uint32_t u[16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        x2[j] = make_float2(0.f, 0.f);
-        xq[j] = 0ull;
-    }
-    if (active) {
-        const uint4* xg = reinterpret_cast<const uint4*>(x + k0);
+        for (int j = 0; j < 16; ++j) u[j] = 0;
+        if (active) {
+            const uint4* xg = reinterpret_cast<const uint4*>(x + k0);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const uint4 v = __ldg(xg + c);
-            const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                x2[c * 4 + j].x = __uint_as_float(u[j] << 16);
-                x2[c * 4 + j].y = __uint_as_float(u[j] & 0xFFFF0000u);
-                xq[c * 4 + j] = ((unsigned long long)(u[j] & 0xFFFF0000u) << 32) | (u[j] << 16);
+            for (int c = 0; c < 4; ++c) {
+                const uint4 v = __ldg(xg + c);
+                u[4 * c] = v.x;
+                u[4 * c + 1] = v.y;
+                u[4 * c + 2] = v.z;
+                u[4 * c + 3] = v.w;
             }
         }
+        int emax = 1;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) X += x2[j].x + x2[j].y;
+        for (int j = 0; j < 16; ++j) {
+            emax = max(emax, max(bf16_exp_eff(u[j] & 0xFFFFu), bf16_exp_eff(u[j] >> 16)));
+            X += bf16_bits_to_float(u[j] & 0xFFFFu) + bf16_bits_to_float(u[j] >> 16);
+        }
+        make_planes<BITS>(u, emax, P);
+        // 2^(emax - 149): a normal float from emax = 23 on, else subnormal
+        xscale = __int_as_float(emax >= 23 ? (emax - 22) << 23 : 1 << emax);
     }
     const int g = k0 / 64;
     const uint32_t lane_code_off = (uint32_t)(seg * 1024 + lane * 32) * BITS / 8;
@@ -436,12 +482,12 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
             const int r = phase + q * sh.phases;   // row within the chunk
             part[q] = 0.f;
             if (have && active && r < rows) {
-                const float A = lane_dot<BITS>(sbase + r * sh.row_bytes + lane_code_off, x2, xq);
+                const float A = lane_dot_int<BITS>(sbase + r * sh.row_bytes + lane_code_off, P);
                 uint16_t sv, bv;
                 asm volatile("ld.shared.u16 %0, [%1];" : "=h"(sv) : "r"(s_off + (r * groups + g) * 2));
                 asm volatile("ld.shared.u16 %0, [%1];" : "=h"(bv) : "r"(b_off + (r * groups + g) * 2));
                 const float s = bf16_bits_to_float(sv), b = bf16_bits_to_float(bv);
-                part[q] = fmaf(s * kUnscale, fmaf(-kOffset, X, A), b * X);
+                part[q] = fmaf(s, A * xscale, b * X);
             }
         }
         // all shared reads of this stage are consumed: hand it back

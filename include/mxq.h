@@ -65,7 +65,7 @@ typedef enum {
  *   dev_status: device int32 or NULL; receives 0 or MXQ_DEV_TIMEOUT.
  * Requirements: bits in {4, 8}; group_size == 64; K > 0 and K % 64 == 0;
  * N > 0; x, w, y 16-byte aligned; scales, biases 2-byte aligned.  The
- * streaming kernel is used when K % 512 == 0, K <= 24576 and scales/biases
+ * streaming kernel is used when K % 512 == 0, K <= 20480 and scales/biases
  * are 16-byte aligned; other shapes take a direct-load kernel (same result
  * rule, different summation order).                                        */
 mxq_status mxq_qmv(const void* x, const uint32_t* w, const void* scales, const void* biases,

@@ -114,3 +114,70 @@ def test_qmv_status_word_clear():
     assert int(status.item()) == 0
     yr, bnd = _ref(case)
     assert_close(to_f64(y), yr, bnd, "qmv with status")
+
+
+def _qmv_bits(case, xbits):
+    import affine_bit_matmul_gb300 as mxq
+
+    return mxq.qmv(bf16_dev(xbits.reshape(1, -1))[0], case.w_d, case.s_d, case.b_d, case.bits)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("K,N", [(5120, 256), (2048, 100), (32768, 64)])
+def test_qmv_power_of_two_scale_equivariance(bits, K, N):
+    # Scaling x by 2^-100 scales every exact product and every fp32 partial
+    # by 2^-100 with no rounding (all values stay normal), so the result is
+    # the unscaled result times 2^-100 bit for bit.  This pins the exponent
+    # handling of both kernels (the streaming kernel re-bases activations
+    # on their largest exponent; the direct-load kernel works in fp32).
+    import synth
+
+    case = DenseCase(1, K, N, bits, seed=21, x_seed=22)
+    xf = synth.bf16_bits_to_f32(case.x[0])
+    xs = synth.f32_to_bf16_bits((xf * np.float32(2.0 ** -100)).astype(np.float32))
+    assert np.array_equal(synth.bf16_bits_to_f32(xs).astype(np.float64),
+                          xf.astype(np.float64) * 2.0 ** -100)
+    y1 = to_f64(_qmv_bits(case, case.x[0]))
+    y2 = to_f64(_qmv_bits(case, xs))
+    assert np.array_equal(y2, y1 * 2.0 ** -100)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_qmv_wide_range_activations(bits):
+    # activations spanning 2^-60 .. 2^20 inside every 32-value lane block,
+    # with zeros, subnormal bf16 values and both signs: the streaming
+    # kernel's fixed-point activations round only values more than 2^15
+    # below the block's largest, far inside the acceptance rule
+    import synth
+
+    K, N = 2048, 128
+    case = DenseCase(1, K, N, bits, seed=23, x_seed=24)
+    rng = np.random.default_rng(25)
+    mag = (1.0 + rng.random(K)) * 2.0 ** rng.integers(-60, 21, size=K)
+    x = np.where(rng.random(K) < 0.5, -mag, mag)
+    x[rng.random(K) < 0.1] = 0.0
+    x[::97] = 2.0 ** -130  # subnormal in bf16
+    xb = synth.f32_to_bf16_bits(x.astype(np.float32))
+    y = to_f64(_qmv_bits(case, xb))
+    yr, bnd = oracle.qmv(xb, case.qw.w, case.qw.scales, case.qw.biases, K, N, bits)
+    assert_close(y, yr, bnd, "qmv wide-range x bits=%d" % bits)
+    # relative check without the absolute term
+    assert np.all(np.abs(y - yr) <= 8e-3 * bnd + 1e-30)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_qmv_tiny_activations(bits):
+    # every activation near 2^-110: the common scale of a lane block is a
+    # subnormal float, the products and the result are still normal
+    import synth
+
+    K, N = 1024, 64
+    case = DenseCase(1, K, N, bits, seed=26, x_seed=27)
+    rng = np.random.default_rng(28)
+    x = (rng.standard_normal(K) * 2.0 ** -110).astype(np.float32)
+    x[np.abs(x) < 2.0 ** -118] = 2.0 ** -118
+    xb = synth.f32_to_bf16_bits(x)
+    y = to_f64(_qmv_bits(case, xb))
+    yr, bnd = oracle.qmv(xb, case.qw.w, case.qw.scales, case.qw.biases, K, N, bits)
+    assert np.all(np.isfinite(y))
+    assert np.all(np.abs(y - yr) <= 8e-3 * bnd + 2.0 ** -140)
