@@ -15,6 +15,11 @@
 // 1024-wide K segment each (several warps per segment take alternate rows);
 // every lane keeps its 32 activations in registers for the whole kernel.
 //
+// The chunks are equal in size (within one row) and as many as a multiple
+// of the grid, so every CTA streams the same share.  The kernel is a
+// programmatic dependent launch: its CTAs start as the previous kernel's
+// finish and wait for that kernel to complete before reading anything.
+//
 // qmv_generic_kernel (any other shape): direct 16-byte loads, one CTA per 16
 // rows.
 //
@@ -234,6 +239,14 @@ __device__ __forceinline__ void expect_tx(uint64_t* bar, uint32_t bytes) {
         : "memory");
 }
 
+// Programmatic dependent launch: the kernel launched after this one on the
+// stream may start its CTAs as ours finish; it waits in grid_dep_wait()
+// until this grid has completed and its writes are visible.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Waits unless another role already gave up; on its own timeout it raises
 // the shared abort flag so that every role winds down without waiting.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
@@ -257,7 +270,19 @@ struct StreamShape {
     int row_bytes;   // codes bytes per row
     int sb_bytes;    // scale (or bias) bytes per row
     int stage_bytes; // codes + scales + biases, 16-byte aligned pieces
-    int nchunks;
+    int nchunks;     // chunks over all of N: at most `rows` rows each, a multiple of the grid
+};
+
+// The first `rem` chunks of the launch have q + 1 rows, the others q rows
+// (q = N / nchunks): nchunks is a multiple of the grid, so every CTA streams
+// the same number of chunks of (within one row) the same size.  CTA b takes
+// chunks b, b + grid, ...:
+// at any time the CTAs stream one contiguous window of the weights, which
+// keeps all DRAM channels evenly loaded (a contiguous share per CTA instead
+// spreads 152 streams at a fixed stride and runs markedly slower).
+struct ChunkRows {
+    int q, rem;
+    __device__ int begin(int chunk) const { return chunk * q + min(chunk, rem); }
 };
 
 // ---- exact integer dot products (streaming form)
@@ -397,6 +422,7 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
         }
         abort_flag = 0;
         mbar_init_fence();
+        grid_dep_launch_dependents();
     }
     __syncthreads();
 
@@ -406,6 +432,10 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
             const char* wb = reinterpret_cast<const char*>(w);
             const char* sbp = reinterpret_cast<const char*>(scales);
             const char* bbp = reinterpret_cast<const char*>(biases);
+            const ChunkRows cr{N / sh.nchunks, N % sh.nchunks};
+            // every read into shared memory, and every read of x or write
+            // of y, comes after the previous kernel on the stream completed
+            grid_dep_wait();
             for (int j = 0;; ++j) {
                 const int chunk = blockIdx.x + j * gridDim.x;
                 if (chunk >= sh.nchunks) break;
@@ -413,8 +443,8 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
                 if (j >= kStreamStages &&
                     !wait_or_abort(&empty[st], ((j / kStreamStages) + 1) & 1, &abort_flag))
                     break;
-                const int r0 = chunk * sh.rows;
-                const int rows = min(sh.rows, N - r0);
+                const int r0 = cr.begin(chunk);
+                const int rows = cr.begin(chunk + 1) - r0;
                 const uint32_t cb = (uint32_t)(rows * sh.row_bytes);
                 const uint32_t sbb = (uint32_t)(rows * sh.sb_bytes);
                 const uint32_t dst = base + st * sh.stage_bytes;
@@ -430,6 +460,7 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
     }
 
     // -------------------------------------------------------------------- compute
+    grid_dep_wait();  // x may come from the previous kernel, y may be read by it
     const int seg = warp % sh.nseg;
     const int phase = warp / sh.nseg;
     const int k0 = seg * 1024 + lane * 32;   // this lane's 32 values
@@ -466,6 +497,7 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
     const uint32_t lane_code_off = (uint32_t)(seg * 1024 + lane * 32) * BITS / 8;
     const int compute_threads = sh.warps * 32;
 
+    const ChunkRows cr{N / sh.nchunks, N % sh.nchunks};
     for (int j = 0;; ++j) {
         const int chunk = blockIdx.x + j * gridDim.x;
         if (chunk >= sh.nchunks) break;
@@ -474,8 +506,8 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
         const uint32_t sbase = base + st * sh.stage_bytes;
         const uint32_t s_off = sbase + sh.rows * sh.row_bytes;
         const uint32_t b_off = s_off + sh.rows * sh.sb_bytes;
-        const int r0 = chunk * sh.rows;
-        const int rows = min(sh.rows, N - r0);
+        const int r0 = cr.begin(chunk);
+        const int rows = cr.begin(chunk + 1) - r0;
         float part[RPW];
 #pragma unroll
         for (int q = 0; q < RPW; ++q) {
@@ -528,13 +560,23 @@ cudaError_t launch_stream(const __nv_bfloat16* x, const uint32_t* w, const uint1
                           const uint16_t* b, __nv_bfloat16* y, int K, int N, int rpw,
                           const StreamShape& sh, int grid, int32_t* status, cudaStream_t stream) {
     const int smem = kStreamStages * sh.stage_bytes;
-    const dim3 block((sh.warps + 1) * 32);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3((sh.warps + 1) * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
 #define MXQ_STREAM_CASE(R)                                                                      \
     case R: {                                                                                   \
         cudaError_t e = cudaFuncSetAttribute(qmv_stream_kernel<BITS, R>,                        \
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem); \
         if (e != cudaSuccess) return e;                                                         \
-        qmv_stream_kernel<BITS, R><<<grid, block, smem, stream>>>(x, w, s, b, y, K, N, sh, status); \
+        e = cudaLaunchKernelEx(&cfg, qmv_stream_kernel<BITS, R>, x, w, s, b, y, K, N, sh, status); \
+        if (e != cudaSuccess) return e;                                                         \
         break;                                                                                  \
     }
     switch (rpw) {
@@ -572,8 +614,11 @@ cudaError_t launch_qmv(const void* x, const uint32_t* w, const void* scales, con
         rpw = rpw >= 8 ? 8 : rpw >= 4 ? 4 : rpw >= 2 ? 2 : 1;
         sh.rows = sh.phases * rpw;
         sh.stage_bytes = sh.rows * (sh.row_bytes + 2 * sh.sb_bytes);  // pieces are 16-byte multiples
+        // chunks of at most sh.rows rows, as many as a multiple of the grid
         sh.nchunks = (N + sh.rows - 1) / sh.rows;
         const int grid = sh.nchunks < sms ? sh.nchunks : sms;
+        sh.nchunks = (sh.nchunks + grid - 1) / grid * grid;
+        if (sh.nchunks > N) sh.nchunks = N;
         return bits == 4 ? launch_stream<4>(xb, w, sb, bb, yb, K, N, rpw, sh, grid, status, stream)
                          : launch_stream<8>(xb, w, sb, bb, yb, K, N, rpw, sh, grid, status, stream);
     }

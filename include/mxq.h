@@ -67,7 +67,10 @@ typedef enum {
  * N > 0; x, w, y 16-byte aligned; scales, biases 2-byte aligned.  The
  * streaming kernel is used when K % 512 == 0, K <= 20480 and scales/biases
  * are 16-byte aligned; other shapes take a direct-load kernel (same result
- * rule, different summation order).                                        */
+ * rule, different summation order).  The streaming kernel is launched as a
+ * programmatic dependent launch: its CTAs may be placed on SMs while the
+ * kernel before it on the stream finishes, but they read and write nothing
+ * until that kernel has completed, so stream order is kept.                 */
 mxq_status mxq_qmv(const void* x, const uint32_t* w, const void* scales, const void* biases,
                    void* y, int K, int N, int bits, int group_size, int32_t* dev_status,
                    void* stream);
