@@ -28,6 +28,8 @@ __all__ = [
     "qmm",
     "gather_qmm",
     "gather_workspace_bytes",
+    "gather_qmm_noalloc",
+    "NOALLOC_SCRATCH_BYTES",
     "MxqError",
     "DEV_BAD_EXPERT_ID",
     "DEV_UNSORTED_IDS",
@@ -48,17 +50,20 @@ STATUS_NAMES = {
     4: "MXQ_ERR_ARCH",
     5: "MXQ_ERR_CUDA",
     6: "MXQ_ERR_WORKSPACE",
+    7: "MXQ_ERR_SCRATCH_LIMIT",
 }
 DEV_BAD_EXPERT_ID = 0x1
 DEV_UNSORTED_IDS = 0x2
 DEV_BAD_ROW_SRC = 0x4
 DEV_TIMEOUT = 0x8
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024  # MXQ_NOALLOC_SCRATCH_BYTES
 
 EXPORTED_SYMBOLS = (
     "mxq_qmv",
     "mxq_qmm",
     "mxq_gather_qmm",
     "mxq_gather_workspace_bytes",
+    "mxq_gather_qmm_noalloc",
     "mxq_status_string",
     "mxq_version",
 )
@@ -90,6 +95,8 @@ def lib():
         L.mxq_qmm.restype = I
         L.mxq_gather_qmm.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, Z, P, P]
         L.mxq_gather_qmm.restype = I
+        L.mxq_gather_qmm_noalloc.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P]
+        L.mxq_gather_qmm_noalloc.restype = I
         L.mxq_gather_workspace_bytes.argtypes = [I, I, I, I]
         L.mxq_gather_workspace_bytes.restype = Z
         L.mxq_status_string.argtypes = [I]
@@ -210,6 +217,38 @@ def qmm(x, w, scales, biases, bits: int, out=None, dev_status=None, stream=None)
 def gather_workspace_bytes(B: int, E: int, K: int, N: int) -> int:
     """Workspace bytes for gather_qmm; pass K = 0 when row_src is None."""
     return int(lib().mxq_gather_workspace_bytes(B, E, K, N))
+
+
+def gather_qmm_noalloc(x, w, scales, biases, expert_ids, row_src, bits: int, out,
+                       dev_status=None, stream=None):
+    """gather_qmm without any allocation: ``out`` must be given, and the
+    scratch is the library's fixed MXQ_NOALLOC_SCRATCH_BYTES array (calls on
+    one device must not overlap in time; see include/mxq.h)."""
+    torch = _torch()
+    _require(x, "x", (torch.bfloat16,))
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D [T, K]")
+    T, K = x.shape
+    if w.dim() != 3:
+        raise ValueError("w must be 3-D [E, N, K*bits/32]")
+    E, N = w.shape[0], w.shape[1]
+    _check_weights(w, scales, biases, N, K, bits, x.device, lead=(E,))
+    _require(expert_ids, "expert_ids", (torch.int32,), x.device)
+    B = expert_ids.numel()
+    if row_src is not None:
+        _require(row_src, "row_src", (torch.int32,), x.device)
+        if row_src.numel() != B:
+            raise ValueError("row_src must have B entries")
+    _require(out, "out", (torch.bfloat16,), x.device)
+    if tuple(out.shape) != (B, N):
+        raise ValueError("out has shape %s, expected %s" % (tuple(out.shape), (B, N)))
+    if dev_status is not None:
+        _require(dev_status, "dev_status", (torch.int32,), x.device)
+    _check(lib().mxq_gather_qmm_noalloc(_ptr(x), _ptr(w), _ptr(scales), _ptr(biases),
+                                        _ptr(expert_ids), _ptr(row_src), _ptr(out), T, B, E, K,
+                                        N, bits, 64, _ptr(dev_status), _stream(stream)),
+           "mxq_gather_qmm_noalloc")
+    return out
 
 
 def gather_qmm(x, w, scales, biases, expert_ids, row_src, bits: int, out=None, workspace=None,

@@ -105,6 +105,7 @@ const char* mxq_status_string(mxq_status s) {
         case MXQ_ERR_ARCH: return "device is not compute capability 10.3 (sm_103a)";
         case MXQ_ERR_CUDA: return "CUDA error";
         case MXQ_ERR_WORKSPACE: return "workspace missing or too small";
+        case MXQ_ERR_SCRATCH_LIMIT: return "request exceeds the fixed scratch of the no-allocation entry point";
     }
     return "unknown status";
 }

@@ -48,7 +48,9 @@ typedef enum {
     MXQ_ERR_UNSUPPORTED = 3, /* a valid request this build does not implement */
     MXQ_ERR_ARCH = 4,        /* current device is not compute capability 10.3 */
     MXQ_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed          */
-    MXQ_ERR_WORKSPACE = 6    /* workspace missing or smaller than required    */
+    MXQ_ERR_WORKSPACE = 6,   /* workspace missing or smaller than required    */
+    MXQ_ERR_SCRATCH_LIMIT = 7 /* mxq_gather_qmm_noalloc: the request needs more
+                                 than MXQ_NOALLOC_SCRATCH_BYTES of scratch      */
 } mxq_status;
 
 /* Bits set in *dev_status (device memory, written by the kernels when the
@@ -119,6 +121,42 @@ mxq_status mxq_gather_qmm(const void* x, const uint32_t* w, const void* scales,
 /* Workspace bytes mxq_gather_qmm needs for B rows over E experts with
  * K-wide activation rows routed through row_src (K = 0: no row_src). */
 size_t mxq_gather_workspace_bytes(int B, int E, int K, int N);
+
+/* Sorted mixture-of-experts GEMM without any allocation: the same operation,
+ * arguments, results and checks as mxq_gather_qmm, but the scratch memory
+ * comes from one fixed array inside the library instead of a caller-provided
+ * workspace.  (The pages that define the operation have no counterpart to
+ * this call; it exists for callers that cannot provide device memory.)
+ *
+ * Who needs it: callers that have no device allocator of their own (plain C
+ * hosts), runtimes whose device memory is fully reserved before serving
+ * starts, and loops that must not allocate between steps.  Nothing is
+ * allocated at call time, by the caller or by the library: the scratch is
+ * MXQ_NOALLOC_SCRATCH_BYTES of device memory reserved on each device when
+ * the library's device code is loaded there.
+ *
+ * Limit: a request whose scratch, mxq_gather_workspace_bytes(B, E, K, N)
+ * with row_src (or mxq_gather_workspace_bytes(B, E, 0, N) without), exceeds
+ * MXQ_NOALLOC_SCRATCH_BYTES returns MXQ_ERR_SCRATCH_LIMIT before anything
+ * touches the device.  32 MiB holds, for example, the tile table and the
+ * sorted rows of 4584 routed rows of K = 2816.
+ *
+ * Set-up: the first call on each device looks up the scratch's device
+ * address with that device current (this may load the library's device
+ * code); make that first call before capturing a stream into a graph.
+ * Nothing in the scratch has to start at zero: every call writes all the
+ * scratch it reads.
+ *
+ * Concurrency: all calls on one device share the scratch.  Two calls whose
+ * execution overlaps (different streams, or different threads without
+ * ordering between them) race on it and produce wrong results; order them,
+ * for example by issuing every call on the same stream.                    */
+#define MXQ_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+mxq_status mxq_gather_qmm_noalloc(const void* x, const uint32_t* w, const void* scales,
+                                  const void* biases, const int32_t* expert_ids,
+                                  const int32_t* row_src, void* y, int T, int B, int E, int K,
+                                  int N, int bits, int group_size, int32_t* dev_status,
+                                  void* stream);
 
 /* Static description of a status code. */
 const char* mxq_status_string(mxq_status status);

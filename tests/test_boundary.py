@@ -31,7 +31,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("mxq_qmv", "mxq_qmm", "mxq_gather_qmm", "mxq_gather_workspace_bytes",
-              "mxq_status_string", "mxq_version"):
+              "mxq_gather_qmm_noalloc", "mxq_status_string", "mxq_version"):
         assert n in names
 
 
@@ -44,7 +44,7 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_status_strings(L):
-    for code in range(0, 7):
+    for code in range(0, 8):
         s = L.mxq_status_string(code).decode()
         assert s and s != "unknown status"
     assert L.mxq_status_string(99).decode() == "unknown status"
@@ -116,3 +116,22 @@ def test_valid_call_without_sm103_device_reports_device_error(L):
         pytest.skip("a GPU is present; covered by the GPU tests")
     # arguments pass the host checks; the device check must then refuse
     assert qmv(L) in (4, 5)
+
+
+def test_noalloc_scratch_limit_refused_before_device(L):
+    import affine_bit_matmul_gb300 as mxq
+
+    text = open(HEADER).read()
+    m = re.search(r"#define MXQ_NOALLOC_SCRATCH_BYTES \((\d+)u \* 1024u \* 1024u\)", text)
+    assert m and int(m.group(1)) * 2 ** 20 == mxq.NOALLOC_SCRATCH_BYTES
+    # 100000 routed rows of K = 8192 need 1.6 GB of scratch: refused with
+    # MXQ_ERR_SCRATCH_LIMIT before any device is touched (this runs on hosts
+    # without a GPU too)
+    rc = L.mxq_gather_qmm_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 100000, 100000, 8,
+                                  8192, 64, 4, 64, None, None)
+    assert rc == 7
+    # without row_src only the tile table is needed: the same B fits
+    need = L.mxq_gather_workspace_bytes(100000, 8, 0, 64)
+    assert 0 < need <= mxq.NOALLOC_SCRATCH_BYTES
+    # the routed up projection of the sorted-MoE workload fits
+    assert L.mxq_gather_workspace_bytes(4584, 128, 2816, 704) <= mxq.NOALLOC_SCRATCH_BYTES
