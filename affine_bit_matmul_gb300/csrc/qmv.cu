@@ -217,6 +217,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32) qmv_generic_kernel(const __nv_
 // ---------------------------------------------------------------- streaming form
 
 constexpr int kStreamStages = 4;
+constexpr int kRedBufs = 4;        // partial-sum buffers between compute warps and reducer
+constexpr int kStreamSmemMax = 227 * 1024 - 2048;  // dynamic shared memory (static part aside)
 constexpr int kChunkBytes = 48 * 1024;   // codes per stage, about
 constexpr int kTargetWarps = 20;
 constexpr int kMaxStreamWarps = 20;  // K <= 20480; the activation planes need ~80 registers
@@ -270,6 +272,7 @@ struct StreamShape {
     int row_bytes;   // codes bytes per row
     int sb_bytes;    // scale (or bias) bytes per row
     int stage_bytes; // codes + scales + biases, 16-byte aligned pieces
+    int x_offset;    // shared-memory offset of the activation copy (after the ring)
     int nchunks;     // chunks over all of N: at most `rows` rows each, a multiple of the grid
 };
 
@@ -400,14 +403,17 @@ __device__ __forceinline__ float lane_dot_int(uint32_t codes_addr, const XPlanes
 }
 
 template <int BITS, int RPW>
-__global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
+__global__ void __launch_bounds__((kMaxStreamWarps + 2) * 32, 1)
     qmv_stream_kernel(const __nv_bfloat16* __restrict__ x, const uint32_t* __restrict__ w,
                       const uint16_t* __restrict__ scales, const uint16_t* __restrict__ biases,
                       __nv_bfloat16* __restrict__ y, int K, int N, const StreamShape sh,
                       int32_t* status) {
     extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ uint64_t full[kStreamStages], empty[kStreamStages];
-    __shared__ float red[2][kMaxStreamWarps * 8];
+    __shared__ uint64_t full[kStreamStages], empty[kStreamStages], xfull;
+    // per-chunk partial sums of each (row, K segment), handed to the reducer
+    // warp through a ring of kRedBufs buffers
+    __shared__ float red[kRedBufs][kMaxStreamWarps * 8];
+    __shared__ uint64_t redfull[kRedBufs], redempty[kRedBufs];
     __shared__ int abort_flag;
 
     const int warp = threadIdx.x >> 5;
@@ -419,6 +425,11 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
         for (int i = 0; i < kStreamStages; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], sh.warps);
+        }
+        mbar_init(&xfull, 1);
+        for (int i = 0; i < kRedBufs; ++i) {
+            mbar_init(&redfull[i], sh.warps);
+            mbar_init(&redempty[i], 1);
         }
         abort_flag = 0;
         mbar_init_fence();
@@ -436,6 +447,11 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
             // every read into shared memory, and every read of x or write
             // of y, comes after the previous kernel on the stream completed
             grid_dep_wait();
+            // the activations first: copies issued by one SM are served in
+            // order, so x arrives ahead of the weight stream instead of
+            // queueing behind tens of megabytes of it
+            expect_tx(&xfull, (uint32_t)(K * 2));
+            bulk_g2s(base + sh.x_offset, x, (uint32_t)(K * 2), &xfull);
             for (int j = 0;; ++j) {
                 const int chunk = blockIdx.x + j * gridDim.x;
                 if (chunk >= sh.nchunks) break;
@@ -456,7 +472,30 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
                          bbp + (long long)r0 * sh.sb_bytes, sbb, &full[st]);
             }
         }
-        return;  // the producer takes no part in the compute warps' barrier
+        return;
+    }
+    if (warp == sh.warps + 1) {
+        // ---------------------------------------------------------------- reducer
+        // sums each row's K-segment partials in a fixed order and stores y,
+        // so the compute warps go on to the next chunk without waiting for
+        // one another
+        const ChunkRows cr{N / sh.nchunks, N % sh.nchunks};
+        for (int j = 0;; ++j) {
+            const int chunk = blockIdx.x + j * gridDim.x;
+            if (chunk >= sh.nchunks) break;
+            const int buf = j % kRedBufs;
+            if (!wait_or_abort(&redfull[buf], (j / kRedBufs) & 1, &abort_flag)) break;
+            const int r0 = cr.begin(chunk);
+            const int rows = cr.begin(chunk + 1) - r0;
+            for (int r = lane; r < rows; r += 32) {
+                float acc = 0.f;
+                for (int sgi = 0; sgi < sh.nseg; ++sgi) acc += red[buf][r * sh.nseg + sgi];
+                y[r0 + r] = __float2bfloat16_rn(acc);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&redempty[buf]);
+        }
+        return;
     }
 
     // -------------------------------------------------------------------- compute
@@ -472,16 +511,14 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
         uint32_t u[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) u[j] = 0;
-        if (active) {
-            const uint4* xg = reinterpret_cast<const uint4*>(x + k0);
+        if (wait_or_abort(&xfull, 0, &abort_flag) && active) {
+            const uint32_t xs = base + sh.x_offset + (uint32_t)k0 * 2;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const uint4 v = __ldg(xg + c);
-                u[4 * c] = v.x;
-                u[4 * c + 1] = v.y;
-                u[4 * c + 2] = v.z;
-                u[4 * c + 3] = v.w;
-            }
+            for (int c = 0; c < 4; ++c)
+                asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                             : "=r"(u[4 * c]), "=r"(u[4 * c + 1]), "=r"(u[4 * c + 2]),
+                               "=r"(u[4 * c + 3])
+                             : "r"(xs + c * 16));
         }
         int emax = 1;
 #pragma unroll
@@ -495,7 +532,6 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
     }
     const int g = k0 / 64;
     const uint32_t lane_code_off = (uint32_t)(seg * 1024 + lane * 32) * BITS / 8;
-    const int compute_threads = sh.warps * 32;
 
     const ChunkRows cr{N / sh.nchunks, N % sh.nchunks};
     for (int j = 0;; ++j) {
@@ -540,17 +576,17 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
         for (int off = 16 / RPW; off >= 1; off >>= 1)
             part[0] += __shfl_xor_sync(0xFFFFFFFFu, part[0], off);
         const int span = 32 / RPW;
-        if ((lane & (span - 1)) == 0) {
+        const int buf = j % kRedBufs;
+        // the reducer must be done with this buffer's previous chunk
+        const bool free_buf =
+            j < kRedBufs || wait_or_abort(&redempty[buf], ((j / kRedBufs) + 1) & 1, &abort_flag);
+        if (free_buf && (lane & (span - 1)) == 0) {
             const int q = lane / span;
             const int r = phase + q * sh.phases;
-            red[j & 1][r * sh.nseg + seg] = part[0];
+            red[buf][r * sh.nseg + seg] = part[0];
         }
-        asm volatile("bar.sync 1, %0;" ::"r"(compute_threads) : "memory");
-        if (threadIdx.x < rows) {
-            float acc = 0.f;
-            for (int sgi = 0; sgi < sh.nseg; ++sgi) acc += red[j & 1][threadIdx.x * sh.nseg + sgi];
-            y[r0 + threadIdx.x] = __float2bfloat16_rn(acc);
-        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&redfull[buf]);
     }
     if (threadIdx.x == 0 && abort_flag && status) atomicOr(status, 0x8 /* MXQ_DEV_TIMEOUT */);
 }
@@ -559,10 +595,10 @@ template <int BITS>
 cudaError_t launch_stream(const __nv_bfloat16* x, const uint32_t* w, const uint16_t* s,
                           const uint16_t* b, __nv_bfloat16* y, int K, int N, int rpw,
                           const StreamShape& sh, int grid, int32_t* status, cudaStream_t stream) {
-    const int smem = kStreamStages * sh.stage_bytes;
+    const int smem = sh.x_offset + K * 2;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3((sh.warps + 1) * 32);
+    cfg.blockDim = dim3((sh.warps + 2) * 32);  // compute warps, producer, reducer
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -613,7 +649,13 @@ cudaError_t launch_qmv(const void* x, const uint32_t* w, const void* scales, con
         int rpw = kChunkBytes / (sh.row_bytes * sh.phases);
         rpw = rpw >= 8 ? 8 : rpw >= 4 ? 4 : rpw >= 2 ? 2 : 1;
         sh.rows = sh.phases * rpw;
+        // the ring and the activation copy share the 227 KB of shared memory
+        while (rpw > 1 && kStreamStages * sh.phases * rpw * (sh.row_bytes + 2 * sh.sb_bytes) +
+                                  K * 2 > kStreamSmemMax)
+            rpw /= 2;
+        sh.rows = sh.phases * rpw;
         sh.stage_bytes = sh.rows * (sh.row_bytes + 2 * sh.sb_bytes);  // pieces are 16-byte multiples
+        sh.x_offset = kStreamStages * sh.stage_bytes;
         // chunks of at most sh.rows rows, as many as a multiple of the grid
         sh.nchunks = (N + sh.rows - 1) / sh.rows;
         const int grid = sh.nchunks < sms ? sh.nchunks : sms;
