@@ -315,26 +315,6 @@ __device__ __forceinline__ uint32_t dp4a_uu(uint32_t a, uint32_t b, uint32_t c) 
     return d;
 }
 
-__device__ __forceinline__ int bf16_exp_eff(uint32_t h) {
-    const int e = (int)((h >> 7) & 0xFFu);
-    return e > 0 ? e : 1;  // subnormals and zero share exponent 1
-}
-
-// X_k of one bf16 value on the scale 2^(emax - 149).
-__device__ __forceinline__ int bf16_fixed24(uint32_t h, int emax) {
-    const int e = (int)((h >> 7) & 0xFFu);
-    const int mag = (e ? 128 : 0) | (int)(h & 0x7Fu);
-    const int sh = (e > 0 ? e : 1) - emax + 15;  // <= 15
-    int v;
-    if (sh >= 0)
-        v = mag << sh;
-    else if (sh >= -9)
-        v = (mag + (1 << (-sh - 1))) >> -sh;   // round half up; 0 below -9
-    else
-        v = 0;
-    return (h & 0x8000u) ? -v : v;
-}
-
 // Byte planes of a lane's 32 activations, arranged like its codes: for
 // 4-bit codes register 2w holds k = 8w, 8w+2, 8w+4, 8w+6 (the even nibbles
 // of word w) and register 2w+1 the odd ones; for 8-bit codes register w
@@ -343,25 +323,45 @@ struct XPlanes {
     uint32_t a[8], b[8], c[8];
 };
 
-// u holds the 32 activations as bf16 pairs (k = 2j in the low half of u[j]).
+__device__ __forceinline__ uint32_t prmt_b32(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// Planes of the lane's activations xf (fp32 copies of the bf16 values) on
+// the scale 2^(emax - 149).  X_k = rint(x_k * 2^(149 - emax)): the scaling
+// is by a power of two, done as two exact multiplications (each factor a
+// normal float), and the one rounding only touches values more than 2^15
+// below the largest.  Returns emax.
 template <int BITS>
-__device__ __forceinline__ void make_planes(const uint32_t (&u)[16], int emax, XPlanes& P) {
+__device__ __forceinline__ int make_planes(const float (&xf)[32], XPlanes& P) {
+    float m = 0.f;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) m = fmaxf(m, fabsf(xf[k]));
+    const int emax = max(1, (int)(__float_as_uint(m) >> 23));  // biased exponent of the largest
+    const int p = 149 - emax;                                    // -105 .. 148
+    const int p1 = min(p, 127);
+    const float s1 = __int_as_float((p1 + 127) << 23);
+    const float s2 = __int_as_float((p - p1 + 127) << 23);
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
-        uint32_t a = 0, b = 0, c = 0;
+        int X[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int k = BITS == 4 ? (r >> 1) * 8 + 2 * i + (r & 1) : r * 4 + i;
-            const uint32_t h = (u[k >> 1] >> (16 * (k & 1))) & 0xFFFFu;
-            const uint32_t X = (uint32_t)bf16_fixed24(h, emax);
-            a |= ((X >> 16) & 0xFFu) << (8 * i);
-            b |= ((X >> 8) & 0xFFu) << (8 * i);
-            c |= (X & 0xFFu) << (8 * i);
+            X[i] = __float2int_rn((xf[k] * s1) * s2);
         }
-        P.a[r] = a;
-        P.b[r] = b;
-        P.c[r] = c;
+        // bytes 0 and 1 of X0..X3, then byte 2 (signed: |X| < 2^23)
+        const uint32_t t01 = prmt_b32((uint32_t)X[0], (uint32_t)X[1], 0x5140u);
+        const uint32_t t23 = prmt_b32((uint32_t)X[2], (uint32_t)X[3], 0x5140u);
+        const uint32_t v01 = prmt_b32((uint32_t)X[0], (uint32_t)X[1], 0x7362u);
+        const uint32_t v23 = prmt_b32((uint32_t)X[2], (uint32_t)X[3], 0x7362u);
+        P.c[r] = prmt_b32(t01, t23, 0x5410u);
+        P.b[r] = prmt_b32(t01, t23, 0x7632u);
+        P.a[r] = prmt_b32(v01, v23, 0x5410u);
     }
+    return emax;
 }
 
 // sum_k X_k q_k over the lane's 32 codes (exact up to the final rounding).
@@ -520,13 +520,14 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 2) * 32, 1)
                                "=r"(u[4 * c + 3])
                              : "r"(xs + c * 16));
         }
-        int emax = 1;
+        float xf[32];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-            emax = max(emax, max(bf16_exp_eff(u[j] & 0xFFFFu), bf16_exp_eff(u[j] >> 16)));
-            X += bf16_bits_to_float(u[j] & 0xFFFFu) + bf16_bits_to_float(u[j] >> 16);
+            xf[2 * j] = __uint_as_float(u[j] << 16);
+            xf[2 * j + 1] = __uint_as_float(u[j] & 0xFFFF0000u);
+            X += xf[2 * j] + xf[2 * j + 1];
         }
-        make_planes<BITS>(u, emax, P);
+        const int emax = make_planes<BITS>(xf, P);
         // 2^(emax - 149): a normal float from emax = 23 on, else subnormal
         xscale = __int_as_float(emax >= 23 ? (emax - 22) << 23 : 1 << emax);
     }
