@@ -144,6 +144,13 @@ mxq_status mxq_qmm(const void* x, const uint32_t* w, const void* scales, const v
     int sms = 0;
     st = check_device(&sms);
     if (st != MXQ_OK) return st;
+    // enough tiles of at most 256 rows to fill every SM: the persistent
+    // kernel (no K split; the next tile's loads overlap this tile's MMAs and
+    // epilogue); otherwise the K split over thread-block clusters
+    const int n_tiles = (N + 127) / 128;
+    const int pm_tiles = (M + 255) / 256;
+    const int pm_tile = (((M + pm_tiles - 1) / pm_tiles) + 15) & ~15;
+    const bool persistent = (long long)n_tiles * pm_tiles >= sms;
     const DensePlan pl = plan_dense(M, K, N, bits, sms);
     if (pl.m_tiles > 65535) return MXQ_ERR_UNSUPPORTED;  // grid.y limit
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -168,6 +175,18 @@ mxq_status mxq_qmm(const void* x, const uint32_t* w, const void* scales, const v
     p.tmem_cols = pl.tmem_cols;
     p.splits = pl.splits;
     p.kb_per_split = pl.kb_per_split;
+    if (persistent) {
+        p.persistent = 1;
+        p.m_tile = pm_tile;
+        p.x_box_rows = pm_tile;
+        p.m_tiles = pm_tiles;
+        p.splits = 1;
+        p.kb_per_split = K / 64;
+        const long long tiles = (long long)n_tiles * pm_tiles;
+        p.grid_ctas = (int)(tiles < sms ? tiles : sms);
+        cudaError_t err = mxq::launch_qmm_tc(p, bits, pm_tiles, pm_tile, s);
+        return err == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA;
+    }
     cudaError_t err = mxq::launch_qmm_tc(p, bits, pl.m_tiles, pl.m_tile, s);
     return err == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA;
 }
@@ -197,7 +216,8 @@ mxq_status mxq_gather_qmm(const void* x, const uint32_t* w, const void* scales,
     if (!workspace || workspace_bytes < need) return MXQ_ERR_WORKSPACE;
     const size_t max_tiles = gather_max_tiles(B, E);
     if (max_tiles > 65535) return MXQ_ERR_UNSUPPORTED;  // grid.y limit
-    st = check_device(nullptr);
+    int sms = 0;
+    st = check_device(&sms);
     if (st != MXQ_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     auto* tiles = static_cast<mxq::MTile*>(workspace);
@@ -237,6 +257,10 @@ mxq_status mxq_gather_qmm(const void* x, const uint32_t* w, const void* scales,
     p.kb_per_split = K / 64;
     p.w_expert_stride = (long long)N * K * bits / 32;
     p.sb_expert_stride = (long long)N * (K / 64);
+    // one CTA per (tile, n tile), two per SM for 4-bit codes: the short
+    // expert tiles are bound by the dequantisation, which two independent
+    // pipelines per SM run twice as fast as one persistent pipeline
+    (void)sms;
     err = mxq::launch_qmm_tc(p, bits, (int)max_tiles, kGatherRowsPerTile, s);
     return err == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA;
 }

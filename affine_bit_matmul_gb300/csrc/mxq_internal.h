@@ -38,6 +38,9 @@ struct QmmParams {
     int kb_per_split;        // 64-wide K blocks per split
     long long w_expert_stride;   // words between experts
     long long sb_expert_stride;  // scale/bias entries between experts
+    int persistent;          // 1: one CTA per SM walks the tiles (no K split)
+    int m_tiles;             // dense persistent form: M tiles
+    int grid_ctas;           // persistent form: CTAs launched
 };
 
 cudaError_t launch_qmv(const void* x, const uint32_t* w, const void* scales, const void* biases,

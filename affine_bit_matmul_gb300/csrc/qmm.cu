@@ -731,6 +731,524 @@ __global__ void __launch_bounds__(kThreads, COMPACT ? 2 : 1)
     }
 }
 
+// ================================================================== persistent form
+//
+// One CTA per SM walks a fixed sequence of output tiles (tile t = blockIdx.x,
+// blockIdx.x + gridDim.x, ...).  Every ring (packed codes, activations,
+// dequantised A stages in tensor memory) runs on across tile boundaries, so
+// the loads of the next tile start while the current one is still being
+// multiplied, and the pipeline fills once per CTA instead of once per tile.
+// Four epilogue warps drain the fp32 accumulator of a finished tile while
+// the MMAs of the next tile run: with tiles of at most 128 activation rows
+// the accumulator is double-buffered in tensor memory.
+//
+// Warps: 0-7 dequantise (two groups of four take alternate 128-wide stages
+// of the global stage sequence), 8 issues the code copies, 9 owns tensor
+// memory and issues the MMAs, 10 issues the activation copies, 11-14 are the
+// epilogue (warp w reads tensor-memory lanes 32 * (w % 4) ...).
+constexpr int kPEpiWarp0 = 11;
+constexpr int kPThreads = 15 * 32;
+constexpr int kPEpiThreads = 128;
+constexpr int kPBarBytes = 64;  // accfull[2], accempty[2], done, tmem slot, abort flag
+
+struct PTile {
+    int e, row_start, rows, n0, n_mma;
+};
+
+template <bool GATHER>
+__device__ __forceinline__ PTile ptile(const QmmParams& p, int t, int m_tiles, int n_tiles) {
+    PTile r;
+    int nt;
+    if (GATHER) {
+        const int lt = t / n_tiles;  // tile of rows (one expert); its n tiles run side by side
+        nt = t - lt * n_tiles;
+        const MTile mt = p.tiles[lt];
+        r.e = mt.e;
+        r.row_start = mt.row_start;
+        r.rows = mt.rows;
+    } else {
+        nt = t / m_tiles;  // the M tiles of one n tile run side by side: its codes come from
+        const int mt = t - nt * m_tiles;  // HBM once and from L2 for the others
+        r.e = 0;
+        r.row_start = mt * p.m_tile;
+        r.rows = min(p.m_tile, p.M - r.row_start);
+    }
+    r.n0 = nt * kTileN;
+    r.n_mma = (r.rows + 15) & ~15;
+    return r;
+}
+
+// try_wait that lets the thread sleep in hardware until the phase completes
+// (or the hint, in ns, runs out), so waiting warps take no issue slots from
+// the warps doing the work.
+constexpr uint32_t kSuspendNs = 20000;
+
+__device__ __forceinline__ bool mbar_try_wait_s(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait that also gives up as soon as another role has given up.
+__device__ __forceinline__ bool wait_ab(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait_s(bar, parity)) {
+        if (*abort_flag) return false;
+        if (clock64() - t0 > kWaitBudgetCycles) {
+            *abort_flag = 1;
+            return false;
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ bool warp_wait_ab(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    const bool ok = wait_ab(bar, parity, abort_flag);
+    return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ bool warp_wait3_ab(uint64_t* a, uint32_t pa, uint64_t* b, uint32_t pb,
+                                              uint64_t* c, uint32_t pc, volatile int* abort_flag) {
+    const bool ok = wait_ab(a, pa, abort_flag) && wait_ab(b, pb, abort_flag) && wait_ab(c, pc, abort_flag);
+    return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// Arrive with a count (the arrivals of stages a partly used code slot never
+// holds are made by the threads of the tile's last stage).
+__device__ __forceinline__ void mbar_arrive_n(uint64_t* bar, uint32_t count) {
+    asm volatile(
+        "{\n\t.reg .b64 st;\n\t"
+        "mbarrier.arrive.release.cta.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+        "r"(count)
+        : "memory");
+}
+
+// After giving up: wait a short, bounded while for the copies a producer
+// issued into the last `n` slots of its ring, so none lands after exit.
+__device__ __forceinline__ void drain_copies(uint64_t* full, int slots, long long issued, int n) {
+    for (long long g = issued - 1; g >= 0 && g >= issued - n; --g) {
+        const int slot = (int)(g % slots);
+        const uint32_t parity = (uint32_t)((g / slots) & 1);
+        const long long t0 = clock64();
+        while (!mbar_try_wait(&full[slot], parity))
+            if (clock64() - t0 > kWaitBudgetCycles / 16) break;
+    }
+}
+
+template <int BITS, bool GATHER>
+__global__ void __launch_bounds__(kPThreads, 1)
+    qmm_persistent_kernel(const QmmParams p, int max_rows, int m_tiles, int n_tiles,
+                          const __grid_constant__ CUtensorMap code_map,
+                          const __grid_constant__ CUtensorMap x_map) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const SmemLayout L = make_layout(BITS, max_rows, false);
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    uint64_t* cfull = reinterpret_cast<uint64_t*>(smem + L.bar_offset);
+    uint64_t* cempty = cfull + kMaxCodeStages;
+    uint64_t* afull = cempty + kMaxCodeStages;
+    uint64_t* aempty = afull + kMaxAStages;
+    uint64_t* xfull = aempty + kMaxAStages;
+    uint64_t* xempty = xfull + kMaxXStages;
+    uint64_t* accfull = xempty + kMaxXStages;   // [2]
+    uint64_t* accempty = accfull + 2;           // [2]
+    uint64_t* done = accempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const uint32_t smem_base = smem_u32(smem);
+    const uint32_t x_base0 = smem_base;
+    const uint32_t c_base0 = smem_base + L.c_offset;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = lane_id();
+    const int total = GATHER ? (*p.tile_count) * n_tiles : m_tiles * n_tiles;
+    const int KB = p.K / kHalfK;              // 64-wide blocks (= groups)
+    const int nst = (KB + 1) / 2;             // 128-wide stages per tile
+    constexpr int kSPS = kCodeSlotRowBytes / (kBK * BITS / 8);  // stages per code slot
+    const int nslots = (nst + kSPS - 1) / kSPS;
+    const int groups = p.K / 64;
+    const int SC = L.c_stages;
+    const int SX = L.x_stages;
+    // tensor memory: one or two accumulators, then the dequantised A stages
+    const int rows16 = (max_rows + 15) & ~15;
+    const int acc_cols = (rows16 + kAStageCols - 1) / kAStageCols * kAStageCols;
+    const int acc_bufs = acc_cols <= 128 ? 2 : 1;
+    const int a0 = acc_bufs * acc_cols;
+    const int SA = min(kMaxAStages, (kTmemCols - a0) / kAStageCols);
+
+    if (warp == kCodeWarp && lane == 0) prefetch_tmap(&code_map);
+    if (warp == kXWarp0 && lane == 0) prefetch_tmap(&x_map);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < SC; ++i) {
+            mbar_init(&cfull[i], 1);
+            mbar_init(&cempty[i], kDequantThreads / 2 * kSPS);  // 128 per stage
+        }
+        for (int i = 0; i < SA; ++i) {
+            mbar_init(&afull[i], kDequantThreads / 2);
+            mbar_init(&aempty[i], 1);
+        }
+        for (int i = 0; i < SX; ++i) {
+            mbar_init(&xfull[i], 1);
+            mbar_init(&xempty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&accfull[i], 1);
+            mbar_init(&accempty[i], kPEpiThreads);
+        }
+        mbar_init(done, 1);
+        *abort_flag = 0;
+        mbar_init_fence();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(tmem_slot, (uint32_t)kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    bool ok = true;
+
+    if (warp == kCodeWarp) {
+        // ---------------------------------------------------------------- codes TMA
+        constexpr int kWordsPerSlot = kCodeSlotRowBytes / 4;
+        constexpr int kWordsPerBox = kCodeBoxRowBytes / 4;
+        const int words = p.K * BITS / 32;
+        Ring ring(SC);
+        long long issued = 0;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const PTile ti = ptile<GATHER>(p, t, m_tiles, n_tiles);
+            for (int j = 0; j < nslots; ++j, ring.next(), ++issued) {
+                if (issued >= SC && !warp_wait_ab(&cempty[ring.slot], ring.parity ^ 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (elect_one()) {
+                    const int c0 = j * kWordsPerSlot;
+                    const int nbox = c0 + kWordsPerBox < words ? 2 : 1;
+                    mbar_expect_tx(&cfull[ring.slot], (uint32_t)(nbox * kCodeBoxBytes));
+                    const uint32_t dst = c_base0 + ring.slot * L.c_bytes;
+                    for (int b = 0; b < nbox; ++b) {
+                        if (GATHER)
+                            tma_load_3d(dst + b * kCodeBoxBytes, &code_map, c0 + b * kWordsPerBox,
+                                        ti.n0, ti.e, &cfull[ring.slot]);
+                        else
+                            tma_load_2d(dst + b * kCodeBoxBytes, &code_map, c0 + b * kWordsPerBox,
+                                        ti.n0, &cfull[ring.slot]);
+                    }
+                }
+                __syncwarp();
+            }
+        }
+        if (!ok && lane == 0) drain_copies(cfull, SC, issued, SC);
+    } else if (warp == kXWarp0) {
+        // ---------------------------------------------------------------- activation TMA
+        Ring ring(SX);
+        long long issued = 0;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const PTile ti = ptile<GATHER>(p, t, m_tiles, n_tiles);
+            const int boxes = (ti.n_mma + p.x_box_rows - 1) / p.x_box_rows;
+            const uint32_t x_bytes_in = (uint32_t)(boxes * p.x_box_rows * 128);
+            for (int q = 0; q < KB; ++q, ring.next(), ++issued) {
+                if (issued >= SX && !warp_wait_ab(&xempty[ring.slot], ring.parity ^ 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (elect_one()) {
+                    mbar_expect_tx(&xfull[ring.slot], x_bytes_in);
+                    for (int b = 0; b < boxes; ++b)
+                        tma_load_2d(x_base0 + ring.slot * L.x_bytes + b * p.x_box_rows * 128, &x_map,
+                                    q * kHalfK, ti.row_start + b * p.x_box_rows, &xfull[ring.slot]);
+                }
+                __syncwarp();
+            }
+        }
+        if (!ok && lane == 0) drain_copies(xfull, SX, issued, SX);
+    } else if (warp == kMmaWarp) {
+        // ---------------------------------------------------------------- MMA issue
+        Ring ar(SA), xr(SX);
+        int i = 0;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++i) {
+            const PTile ti = ptile<GATHER>(p, t, m_tiles, n_tiles);
+            const int buf = acc_bufs == 2 ? (i & 1) : 0;
+            const int use = acc_bufs == 2 ? (i >> 1) : i;  // earlier tiles on this buffer
+            if (use > 0 && !warp_wait_ab(&accempty[buf], (uint32_t)((use - 1) & 1), abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t idesc = umma_idesc_bf16(kTileN, (uint32_t)ti.n_mma);
+            const uint32_t d_tmem = tmem + (uint32_t)(buf * acc_cols);
+            for (int s = 0; s < nst; ++s, ar.next()) {
+                const bool two = 2 * s + 1 < KB;
+                const int x0 = xr.slot;
+                const uint32_t p0 = xr.parity;
+                xr.next();
+                const int x1 = two ? xr.slot : x0;
+                const uint32_t p1 = two ? xr.parity : p0;
+                if (two) xr.next();
+                if (!warp_wait3_ab(&afull[ar.slot], ar.parity, &xfull[x0], p0, &xfull[x1], p1,
+                                   abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (elect_one()) {
+                    const uint32_t a_col = tmem + (uint32_t)(a0 + ar.slot * kAStageCols);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        if (h == 1 && !two) break;
+                        const uint64_t bd = umma_desc_sw128(x_base0 + (h ? x1 : x0) * L.x_bytes);
+#pragma unroll
+                        for (int j = 0; j < kHalfK / 16; ++j)
+                            umma_bf16_tmem_a(d_tmem, a_col + h * (kAStageCols / 2) + j * 8, bd + 2 * j,
+                                             idesc, (s > 0 || h > 0 || j > 0) ? 1u : 0u);
+                    }
+                    umma_commit(&aempty[ar.slot]);
+                    umma_commit(&xempty[x0]);
+                    if (two) umma_commit(&xempty[x1]);
+                    if (s == nst - 1) umma_commit(&accfull[buf]);
+                }
+                __syncwarp();
+            }
+        }
+        // every MMA issued so far has finished before tensor memory is freed
+        if (elect_one()) {
+            umma_commit(done);
+            const long long t0 = clock64();
+            while (!mbar_try_wait(done, 0))
+                if (clock64() - t0 > kWaitBudgetCycles) break;
+        }
+        __syncwarp();
+    } else if (warp >= kPEpiWarp0) {
+        // ---------------------------------------------------------------- epilogue
+        const int quarter = warp & 3;  // tensor-memory lanes 32 * quarter ...
+        const int lane_row = quarter * 32 + lane;
+        const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
+        __nv_bfloat16* y = static_cast<__nv_bfloat16*>(p.y);
+        int i = 0;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++i) {
+            const PTile ti = ptile<GATHER>(p, t, m_tiles, n_tiles);
+            const int buf = acc_bufs == 2 ? (i & 1) : 0;
+            const int use = acc_bufs == 2 ? (i >> 1) : i;
+            if (!warp_wait_ab(&accfull[buf], (uint32_t)(use & 1), abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int ny = ti.n0 + lane_row;
+            const bool y_ok = ny < p.N;
+            const uint32_t acc = t_lane + (uint32_t)(buf * acc_cols);
+            for (int c0 = 0; c0 < ti.n_mma; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld16(acc + c0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                if (c0 + 16 < ti.n_mma) tmem_ld16(acc + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+                tmem_ld_wait();
+                if (y_ok) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int m = c0 + j;
+                        if (m < ti.rows)
+                            y[(long long)(ti.row_start + m) * p.N + ny] =
+                                __float2bfloat16_rn(__uint_as_float(v[j]));
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&accempty[buf]);
+        }
+    } else if (warp < kDequantWarps) {
+        // ---------------------------------------------------------------- dequant
+        // group g takes the stages whose global index (over all tiles of this
+        // CTA) is congruent to g mod 2; thread r handles w row r (its TMEM
+        // lane) over the whole stage: two 64-wide groups
+        const int r = threadIdx.x & (kTileN - 1);
+        const int grp = warp >> 2;
+        constexpr int kRowBytes = kBK * BITS / 8;  // codes of one row per stage
+        const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        // last code slot of a tile: stages it never holds, whose arrivals the
+        // threads of the tile's last stage make
+        const int missing = nslots * kSPS - nst;
+        Ring cr(SC), ar(SA);
+        if (grp) ar.next();
+        long long cpos = 0;   // global index of the code slot cr points at
+        long long g0 = 0;     // global index of the tile's first stage
+        long long tile_i = 0;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tile_i, g0 += nst) {
+            const PTile ti = ptile<GATHER>(p, t, m_tiles, n_tiles);
+            const int n = ti.n0 + r;
+            const bool row_ok = n < p.N;
+            const uint16_t* srow = p.scales + (long long)ti.e * p.sb_expert_stride + (long long)n * groups;
+            const uint16_t* brow = p.biases + (long long)ti.e * p.sb_expert_stride + (long long)n * groups;
+            // bring the next tile's scales and biases of this row into L2
+            // now (a new tile's are otherwise cold, and its first stages
+            // would wait for HBM)
+            if (grp == 0 && t + (int)gridDim.x < total) {
+                const PTile tn = ptile<GATHER>(p, t + gridDim.x, m_tiles, n_tiles);
+                const int nn = tn.n0 + r;
+                if (nn < p.N) {
+                    const long long off = (long long)tn.e * p.sb_expert_stride + (long long)nn * groups;
+                    const char* sp = reinterpret_cast<const char*>(p.scales + off);
+                    const char* bp = reinterpret_cast<const char*>(p.biases + off);
+                    const uintptr_t s_lo = reinterpret_cast<uintptr_t>(sp) & ~uintptr_t(127);
+                    const uintptr_t b_lo = reinterpret_cast<uintptr_t>(bp) & ~uintptr_t(127);
+                    for (uintptr_t a = s_lo; a < reinterpret_cast<uintptr_t>(sp + groups * 2); a += 128)
+                        prefetch_l2(reinterpret_cast<const void*>(a));
+                    for (uintptr_t a = b_lo; a < reinterpret_cast<uintptr_t>(bp + groups * 2); a += 128)
+                        prefetch_l2(reinterpret_cast<const void*>(a));
+                }
+            }
+            const int s0 = (int)((grp + g0) & 1);
+            int csub = s0;  // stage within the code slot (kSPS >= 2, so s0 < kSPS)
+            // scales and biases of a stage's two groups: {s0, s1, b0, b1}
+            auto sb_load = [&](int s, uint32_t (&sb)[4]) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int b = 2 * s + h;
+                    sb[h] = 0;
+                    sb[2 + h] = 0;
+                    if (row_ok && s < nst && b < KB) {
+                        sb[h] = __ldg(srow + b);
+                        sb[2 + h] = __ldg(brow + b);
+                    }
+                }
+            };
+            auto stage = [&](int s, const uint32_t (&sb)[4]) -> bool {
+                const int cs = cr.slot;
+                if (!warp_wait_ab(&cfull[cs], cr.parity, abort_flag)) return false;
+                const int off = csub * kRowBytes;
+                const uint32_t c_line = c_base0 + cs * L.c_bytes + (off / kCodeBoxRowBytes) * kCodeBoxBytes +
+                                        r * kCodeBoxRowBytes;
+                const int chunk0 = (off % kCodeBoxRowBytes) / 16;
+                uint4 cw[BITS];
+#pragma unroll
+                for (int j = 0; j < BITS; ++j)
+                    cw[j] = ld_shared_v4(c_line + (uint32_t)(((chunk0 + j) ^ (r & 7)) << 4));
+                const int as = ar.slot;
+                if (g0 + s >= SA && !warp_wait_ab(&aempty[as], ar.parity ^ 1, abort_flag)) return false;
+                tc_fence_after();
+                const uint32_t a_col = t_lane + (uint32_t)(a0 + as * kAStageCols);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    if (2 * s + h >= KB) break;  // a last half-stage when K / 64 is odd
+                    const uint32_t sbits = sb[h], bbits = sb[2 + h];
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {  // 32 k = 16 columns per store
+                        uint32_t o[16];
+                        if (BITS == 4) {
+                            const uint32_t s2 = sbits | (sbits << 16);
+                            const uint32_t b2 = bbits | (bbits << 16);
+                            const uint4 cv = cw[h * 2 + c];
+                            const uint32_t wd[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                uint32_t q4[4];
+                                dequant_word4(wd[j], s2, b2, q4);
+#pragma unroll
+                                for (int u = 0; u < 4; ++u) o[j * 4 + u] = q4[u];
+                            }
+                        } else {
+                            const float sf = bf16_bits_to_float(sbits);
+                            const float bf = bf16_bits_to_float(bbits);
+#pragma unroll
+                            for (int q = 0; q < 2; ++q) {
+                                const uint4 cv = cw[h * 4 + c * 2 + q];
+                                const uint32_t wd[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) {
+                                    uint32_t q2[2];
+                                    dequant_word8(wd[j], sf, bf, q2);
+                                    o[q * 8 + j * 2] = q2[0];
+                                    o[q * 8 + j * 2 + 1] = q2[1];
+                                }
+                            }
+                        }
+                        tmem_st16(a_col + h * (kAStageCols / 2) + c * 16, o);
+                    }
+                }
+                tmem_st_wait();
+                // release the code slot once its words are consumed; the last
+                // stage of the tile also makes the arrivals of the stages its
+                // slot never holds
+                mbar_arrive_n(&cempty[cs], s == nst - 1 ? 1u + (uint32_t)missing : 1u);
+                tc_fence_before();
+                mbar_arrive(&afull[as]);
+                csub += 2;
+                if (csub >= kSPS) {
+                    csub -= kSPS;
+                    cr.next();
+                    ++cpos;
+                }
+                ar.next();
+                ar.next();
+                return true;
+            };
+            // this group's stages s0, s0 + 2, ...: two scale/bias buffers,
+            // each reloaded (two of this group's stages ahead) right after
+            // its use, so no register copy ever waits on a pending load
+            uint32_t sbA[4], sbB[4];
+            sb_load(s0, sbA);
+            sb_load(s0 + 2, sbB);
+            for (int s = s0; s < nst && ok; s += 4) {
+                ok = stage(s, sbA);
+                sb_load(s + 4, sbA);
+                if (!ok || s + 2 >= nst) break;
+                ok = stage(s + 2, sbB);
+                sb_load(s + 6, sbB);
+            }
+            // on to the next tile's first code slot
+            while (ok && cpos < (tile_i + 1) * nslots) {
+                cr.next();
+                ++cpos;
+            }
+        }
+    }
+
+    if (!ok || *abort_flag) {
+        if (threadIdx.x == 0) flag_status(p.status, MXQ_DEV_TIMEOUT);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, (uint32_t)kTmemCols);
+    }
+}
+
+template <int BITS, bool GATHER>
+cudaError_t launch_persistent(const QmmParams& p, int max_rows, int m_tiles, int n_tiles,
+                              int grid, const CUtensorMap& cm, const CUtensorMap& xm,
+                              cudaStream_t stream) {
+    const SmemLayout L = make_layout(BITS, max_rows, false);
+    const int smem = L.total + kPBarBytes;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        cudaError_t err = cudaFuncSetAttribute(qmm_persistent_kernel<BITS, GATHER>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               232448);
+        if (err != cudaSuccess) return err;
+        attr_set[dev] = true;
+    }
+    if (smem > 232448) return cudaErrorInvalidConfiguration;
+    qmm_persistent_kernel<BITS, GATHER><<<grid, kPThreads, smem, stream>>>(p, max_rows, m_tiles,
+                                                                          n_tiles, cm, xm);
+    return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ host side
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -823,6 +1341,16 @@ cudaError_t launch_qmm_tc(const QmmParams& p, int bits, int grid_m, int max_rows
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
+    if (p.persistent) {
+        // dense only: the short expert tiles of the grouped form run faster
+        // as two independent CTAs per SM (below)
+        if (gather) return cudaErrorNotSupported;
+        const int n_tiles = (p.N + kTileN - 1) / kTileN;
+        return bits == 4 ? launch_persistent<4, false>(p, max_rows_per_tile, p.m_tiles, n_tiles,
+                                                       p.grid_ctas, cm, xm, stream)
+                         : launch_persistent<8, false>(p, max_rows_per_tile, p.m_tiles, n_tiles,
+                                                       p.grid_ctas, cm, xm, stream);
+    }
     if (bits == 4)
     {
         // dense small-M launches split K instead (more CTAs, one per SM)

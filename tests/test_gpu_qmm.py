@@ -38,6 +38,19 @@ def _sample(case, y, count=3000, seed=0):
 
 @pytest.mark.parametrize("bits", [4, 8])
 @pytest.mark.parametrize("M,K,N", [
+    # enough tiles of <= 256 rows to fill the GPU: the persistent kernel, with
+    # ragged K (a partly used last code slot; an odd number of 64-blocks),
+    # ragged M and N, one or two accumulator buffers (tiles above / up to
+    # 128 rows) and tiles per CTA that differ
+    (300, 640, 19456), (333, 192, 19500), (129, 320, 19456), (1000, 64, 9800),
+    (100, 704, 19456),
+])
+def test_qmm_persistent_shapes(bits, M, K, N):
+    test_qmm_small(bits, M, K, N)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("M,K,N", [
     (1, 64, 128), (7, 128, 128), (9, 704, 200), (16, 512, 256), (33, 1024, 130),
     (127, 704, 384), (129, 640, 257), (256, 256, 128), (257, 320, 100), (600, 704, 136),
 ])
