@@ -87,9 +87,10 @@ DensePlan plan_dense(int M, int K, int N, int bits, int sms) {
 
 size_t gather_max_tiles(int B, int E) { return (size_t)B / kGatherRowsPerTile + (size_t)E + 1; }
 
-// Tile records plus the tile count, 256-byte aligned.
+// Tile records, the tile count, each expert's first row; 256-byte aligned.
 size_t gather_table_bytes(int B, int E) {
-    return align_up(gather_max_tiles(B, E) * sizeof(mxq::MTile), 256) + 256;
+    return align_up(gather_max_tiles(B, E) * sizeof(mxq::MTile), 256) + 256 +
+           align_up(((size_t)E + 1) * sizeof(int), 256);
 }
 
 }  // namespace
@@ -223,9 +224,10 @@ mxq_status mxq_gather_qmm(const void* x, const uint32_t* w, const void* scales,
     auto* tiles = static_cast<mxq::MTile*>(workspace);
     int* tile_count = reinterpret_cast<int*>(static_cast<char*>(workspace) +
                                              align_up(max_tiles * sizeof(mxq::MTile), 256));
+    int* seg_start = tile_count + 256 / sizeof(int);
     cudaError_t err = mxq::launch_gather_prepass(expert_ids, row_src, T, B, E, N,
-                                                 kGatherRowsPerTile, tiles, tile_count, y,
-                                                 dev_status, s);
+                                                 kGatherRowsPerTile, tiles, tile_count, seg_start,
+                                                 y, dev_status, s);
     if (err != cudaSuccess) return MXQ_ERR_CUDA;
     const void* xa = x;
     if (row_src) {

@@ -55,9 +55,10 @@ cudaError_t launch_qmm_tc(const QmmParams& p, int bits, int grid_m, int max_rows
 // Grouped form, step 1: validate ids, find each expert's rows, build the
 // tile list, zero the y rows that no tile covers.
 // Step 2 (when row_src is given): copy the activation rows into sorted order.
+// seg_start: device scratch of E + 1 ints (each expert's first sorted row).
 cudaError_t launch_gather_prepass(const int32_t* expert_ids, const int32_t* row_src, int T,
                                   int B, int E, int N, int rows_per_tile, MTile* tiles,
-                                  int* tile_count, void* y, int32_t* status,
+                                  int* tile_count, int* seg_start, void* y, int32_t* status,
                                   cudaStream_t stream);
 
 cudaError_t launch_gather_rows(const void* x, const int32_t* row_src, int T, int B, int K,
