@@ -259,10 +259,16 @@ mxq_status mxq_gather_qmm(const void* x, const uint32_t* w, const void* scales,
     p.kb_per_split = K / 64;
     p.w_expert_stride = (long long)N * K * bits / 32;
     p.sb_expert_stride = (long long)N * (K / 64);
-    // one CTA per (tile, n tile), two per SM for 4-bit codes: the short
-    // expert tiles are bound by the dequantisation, which two independent
-    // pipelines per SM run twice as fast as one persistent pipeline
-    (void)sms;
+    // short tiles (K <= 2048: at most 16 stages each), 4-bit: two persistent
+    // CTAs per SM walk (tile list) x (n tiles), so the pipeline fills once
+    // per CTA instead of once per tile; long tiles: one CTA per tile, which
+    // the hardware hands out as SMs free up (better balance when a tile is
+    // long); 8-bit: one CTA per tile
+    if (bits == 4 && K <= 2048) {
+        const long long bound = (long long)max_tiles * ((N + 127) / 128);
+        p.persistent = 1;
+        p.grid_ctas = (int)(bound < 2LL * sms ? bound : 2LL * sms);
+    }
     err = mxq::launch_qmm_tc(p, bits, (int)max_tiles, kGatherRowsPerTile, s);
     return err == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA;
 }

@@ -846,13 +846,14 @@ __device__ __forceinline__ void drain_copies(uint64_t* full, int slots, long lon
     }
 }
 
-template <int BITS, bool GATHER>
-__global__ void __launch_bounds__(kPThreads, 1)
+template <int BITS, bool GATHER, bool COMPACT>
+__global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 1)
     qmm_persistent_kernel(const QmmParams p, int max_rows, int m_tiles, int n_tiles,
                           const __grid_constant__ CUtensorMap code_map,
                           const __grid_constant__ CUtensorMap x_map) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    const SmemLayout L = make_layout(BITS, max_rows, false);
+    const SmemLayout L = make_layout(BITS, max_rows, COMPACT);
+    constexpr int kCols = COMPACT ? kCompactTmemCols : kTmemCols;
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     uint64_t* cfull = reinterpret_cast<uint64_t*>(smem + L.bar_offset);
@@ -883,9 +884,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // tensor memory: one or two accumulators, then the dequantised A stages
     const int rows16 = (max_rows + 15) & ~15;
     const int acc_cols = (rows16 + kAStageCols - 1) / kAStageCols * kAStageCols;
-    const int acc_bufs = acc_cols <= 128 ? 2 : 1;
+    // the compact form (two CTAs per SM) has one accumulator: its epilogue is
+    // done by the dequant warps, and the SM's other CTA keeps the tensor
+    // cores busy meanwhile
+    const int acc_bufs = (!COMPACT && acc_cols <= 128) ? 2 : 1;
     const int a0 = acc_bufs * acc_cols;
-    const int SA = min(kMaxAStages, (kTmemCols - a0) / kAStageCols);
+    const int SA = min(kMaxAStages, (kCols - a0) / kAStageCols);
 
     if (warp == kCodeWarp && lane == 0) prefetch_tmap(&code_map);
     if (warp == kXWarp0 && lane == 0) prefetch_tmap(&x_map);
@@ -904,14 +908,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&accfull[i], 1);
-            mbar_init(&accempty[i], kPEpiThreads);
+            mbar_init(&accempty[i], COMPACT ? kDequantThreads : kPEpiThreads);
         }
         mbar_init(done, 1);
         *abort_flag = 0;
         mbar_init_fence();
     }
     if (warp == kMmaWarp) {
-        tmem_alloc(tmem_slot, (uint32_t)kTmemCols);
+        tmem_alloc(tmem_slot, (uint32_t)kCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -1031,7 +1035,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 if (clock64() - t0 > kWaitBudgetCycles) break;
         }
         __syncwarp();
-    } else if (warp >= kPEpiWarp0) {
+    } else if (!COMPACT && warp >= kPEpiWarp0) {
         // ---------------------------------------------------------------- epilogue
         const int quarter = warp & 3;  // tensor-memory lanes 32 * quarter ...
         const int lane_row = quarter * 32 + lane;
@@ -1212,6 +1216,37 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 cr.next();
                 ++cpos;
             }
+            if (COMPACT && ok) {
+                // epilogue of this tile: warp w reads tensor-memory lanes
+                // 32 * (w % 4) ... and every other 16-column chunk
+                if (!warp_wait_ab(&accfull[0], (uint32_t)(tile_i & 1), abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int quarter = warp & 3;
+                const int colhalf = warp >> 2;
+                const int ny = ti.n0 + quarter * 32 + lane;
+                const bool y_ok = ny < p.N;
+                const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
+                __nv_bfloat16* y = static_cast<__nv_bfloat16*>(p.y);
+                for (int c0 = colhalf * 16; c0 < ti.n_mma; c0 += 32) {
+                    uint32_t v[16];
+                    tmem_ld16(taddr + c0, v);
+                    tmem_ld_wait();
+                    if (y_ok) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int m = c0 + j;
+                            if (m < ti.rows)
+                                y[(long long)(ti.row_start + m) * p.N + ny] =
+                                    __float2bfloat16_rn(__uint_as_float(v[j]));
+                        }
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&accempty[0]);
+            }
         }
     }
 
@@ -1222,30 +1257,31 @@ __global__ void __launch_bounds__(kPThreads, 1)
     __syncthreads();
     if (warp == kMmaWarp) {
         tc_fence_after();
-        tmem_dealloc(tmem, (uint32_t)kTmemCols);
+        tmem_dealloc(tmem, (uint32_t)kCols);
     }
 }
 
-template <int BITS, bool GATHER>
+template <int BITS, bool GATHER, bool COMPACT>
 cudaError_t launch_persistent(const QmmParams& p, int max_rows, int m_tiles, int n_tiles,
                               int grid, const CUtensorMap& cm, const CUtensorMap& xm,
                               cudaStream_t stream) {
-    const SmemLayout L = make_layout(BITS, max_rows, false);
+    const SmemLayout L = make_layout(BITS, max_rows, COMPACT);
     const int smem = L.total + kPBarBytes;
     static bool attr_set[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-        cudaError_t err = cudaFuncSetAttribute(qmm_persistent_kernel<BITS, GATHER>,
+        cudaError_t err = cudaFuncSetAttribute(qmm_persistent_kernel<BITS, GATHER, COMPACT>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                232448);
         if (err != cudaSuccess) return err;
         attr_set[dev] = true;
     }
     if (smem > 232448) return cudaErrorInvalidConfiguration;
-    qmm_persistent_kernel<BITS, GATHER><<<grid, kPThreads, smem, stream>>>(p, max_rows, m_tiles,
-                                                                          n_tiles, cm, xm);
+    qmm_persistent_kernel<BITS, GATHER, COMPACT>
+        <<<grid, COMPACT ? kThreads : kPThreads, smem, stream>>>(p, max_rows, m_tiles, n_tiles, cm,
+                                                                 xm);
     return cudaGetLastError();
 }
 
@@ -1342,14 +1378,17 @@ cudaError_t launch_qmm_tc(const QmmParams& p, int bits, int grid_m, int max_rows
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     if (p.persistent) {
-        // dense only: the short expert tiles of the grouped form run faster
-        // as two independent CTAs per SM (below)
-        if (gather) return cudaErrorNotSupported;
         const int n_tiles = (p.N + kTileN - 1) / kTileN;
-        return bits == 4 ? launch_persistent<4, false>(p, max_rows_per_tile, p.m_tiles, n_tiles,
-                                                       p.grid_ctas, cm, xm, stream)
-                         : launch_persistent<8, false>(p, max_rows_per_tile, p.m_tiles, n_tiles,
-                                                       p.grid_ctas, cm, xm, stream);
+        if (gather) {
+            // grouped, 4-bit, short tiles: two persistent CTAs per SM
+            if (bits != 4 || !compact_mode(4, max_rows_per_tile, true)) return cudaErrorNotSupported;
+            return launch_persistent<4, true, true>(p, max_rows_per_tile, 0, n_tiles, p.grid_ctas,
+                                                    cm, xm, stream);
+        }
+        return bits == 4 ? launch_persistent<4, false, false>(p, max_rows_per_tile, p.m_tiles,
+                                                              n_tiles, p.grid_ctas, cm, xm, stream)
+                         : launch_persistent<8, false, false>(p, max_rows_per_tile, p.m_tiles,
+                                                              n_tiles, p.grid_ctas, cm, xm, stream);
     }
     if (bits == 4)
     {
