@@ -73,7 +73,10 @@ __global__ void __launch_bounds__(kPrepThreads) gather_prepass_kernel(
     // the sorted copy of the activation rows (the next launch) does not read
     // anything this kernel writes: let it start now and run alongside
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (threadIdx.x == 0) flags = 0;
+    if (threadIdx.x == 0) {
+        flags = 0;
+        tile_count[1] = 0;  // the grouped GEMM's next-unclaimed-tile counter
+    }
     __syncthreads();
 
     // 1. validate (eight rows per thread per round, all loads issued first)

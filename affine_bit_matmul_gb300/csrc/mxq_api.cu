@@ -259,15 +259,14 @@ mxq_status mxq_gather_qmm(const void* x, const uint32_t* w, const void* scales,
     p.kb_per_split = K / 64;
     p.w_expert_stride = (long long)N * K * bits / 32;
     p.sb_expert_stride = (long long)N * (K / 64);
-    // short tiles (K <= 2048: at most 16 stages each), 4-bit: two persistent
-    // CTAs per SM walk (tile list) x (n tiles), so the pipeline fills once
-    // per CTA instead of once per tile; long tiles: one CTA per tile, which
-    // the hardware hands out as SMs free up (better balance when a tile is
-    // long); 8-bit: one CTA per tile
-    if (bits == 4 && K <= 2048) {
+    // 4-bit: two persistent CTAs per SM take tiles of (tile list) x (n tiles)
+    // from a counter as they finish the previous one, so the pipeline fills
+    // once per CTA and long and short tiles balance; 8-bit: one CTA per tile
+    if (bits == 4) {
         const long long bound = (long long)max_tiles * ((N + 127) / 128);
         p.persistent = 1;
         p.grid_ctas = (int)(bound < 2LL * sms ? bound : 2LL * sms);
+        p.tile_counter = tile_count + 1;  // tiles handed out as CTAs free up
     }
     err = mxq::launch_qmm_tc(p, bits, (int)max_tiles, kGatherRowsPerTile, s);
     return err == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA;

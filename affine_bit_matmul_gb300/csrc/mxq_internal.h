@@ -41,6 +41,8 @@ struct QmmParams {
     int persistent;          // 1: one CTA per SM walks the tiles (no K split)
     int m_tiles;             // dense persistent form: M tiles
     int grid_ctas;           // persistent form: CTAs launched
+    int* tile_counter;       // persistent form: next unclaimed tile (zeroed before the
+                             // launch), or null for a fixed gridDim.x stride
 };
 
 cudaError_t launch_qmv(const void* x, const uint32_t* w, const void* scales, const void* biases,
@@ -53,7 +55,8 @@ cudaError_t launch_qmm_tc(const QmmParams& p, int bits, int grid_m, int max_rows
                           cudaStream_t stream);
 
 // Grouped form, step 1: validate ids, find each expert's rows, build the
-// tile list, zero the y rows that no tile covers.
+// tile list (count in tile_count[0]), zero tile_count[1] (the GEMM's tile
+// counter) and the y rows that no tile covers.
 // Step 2 (when row_src is given): copy the activation rows into sorted order.
 // seg_start: device scratch of E + 1 ints (each expert's first sorted row).
 cudaError_t launch_gather_prepass(const int32_t* expert_ids, const int32_t* row_src, int T,

@@ -749,7 +749,9 @@ __global__ void __launch_bounds__(kThreads, COMPACT ? 2 : 1)
 constexpr int kPEpiWarp0 = 11;
 constexpr int kPThreads = 15 * 32;
 constexpr int kPEpiThreads = 128;
-constexpr int kPBarBytes = 64;  // accfull[2], accempty[2], done, tmem slot, abort flag
+constexpr int kTQ = 4;          // tile-id queue between the code-copy warp and the others
+constexpr int kPBarBytes = 64 + kTQ * 20;  // accfull[2], accempty[2], done, tmem slot, abort flag,
+                                           // tile queue (ids, full and empty barriers)
 
 struct PTile {
     int e, row_start, rows, n0, n_mma;
@@ -820,9 +822,6 @@ __device__ __forceinline__ bool warp_wait3_ab(uint64_t* a, uint32_t pa, uint64_t
     return __all_sync(0xffffffffu, ok);
 }
 
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
 
 // Arrive with a count (the arrivals of stages a partly used code slot never
 // holds are made by the threads of the tile's last stage).
@@ -865,8 +864,11 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
     uint64_t* accfull = xempty + kMaxXStages;   // [2]
     uint64_t* accempty = accfull + 2;           // [2]
     uint64_t* done = accempty + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    uint64_t* tqfull = done + 1;                // [kTQ]
+    uint64_t* tqempty = tqfull + kTQ;           // [kTQ]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tqempty + kTQ);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* tq = reinterpret_cast<volatile int*>(tmem_slot + 2);  // [kTQ] tile ids
     const uint32_t smem_base = smem_u32(smem);
     const uint32_t x_base0 = smem_base;
     const uint32_t c_base0 = smem_base + L.c_offset;
@@ -911,6 +913,12 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
             mbar_init(&accempty[i], COMPACT ? kDequantThreads : kPEpiThreads);
         }
         mbar_init(done, 1);
+        // tile queue: filled by the code-copy warp, read by the activation
+        // copy warp, the MMA warp, each dequant warp and each epilogue warp
+        for (int i = 0; i < kTQ; ++i) {
+            mbar_init(&tqfull[i], 1);
+            mbar_init(&tqempty[i], 2 + kDequantWarps + (COMPACT ? 0 : 4));
+        }
         *abort_flag = 0;
         mbar_init_fence();
     }
@@ -924,6 +932,31 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
     const uint32_t tmem = *tmem_slot;
     bool ok = true;
 
+    // The tile sequence.  The code-copy warp takes tile i: blockIdx.x first,
+    // then (with a tile counter, zeroed by the prepass) the next unclaimed
+    // tile, so CTAs that finish early take more; without one, every
+    // gridDim.x-th tile.  It passes the id through a kTQ-deep queue; a tile
+    // id >= total tells every role to stop.
+    auto tq_push = [&](int i, int t) -> bool {
+        const int slot = i % kTQ;
+        if (i >= kTQ && !warp_wait_ab(&tqempty[slot], (uint32_t)(((i / kTQ) - 1) & 1), abort_flag))
+            return false;
+        if (lane == 0) {
+            tq[slot] = t;
+            mbar_arrive(&tqfull[slot]);
+        }
+        __syncwarp();
+        return true;
+    };
+    auto tq_pop = [&](int i, int* t) -> bool {
+        const int slot = i % kTQ;
+        if (!warp_wait_ab(&tqfull[slot], (uint32_t)((i / kTQ) & 1), abort_flag)) return false;
+        *t = tq[slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tqempty[slot]);
+        return true;
+    };
+
     if (warp == kCodeWarp) {
         // ---------------------------------------------------------------- codes TMA
         constexpr int kWordsPerSlot = kCodeSlotRowBytes / 4;
@@ -931,7 +964,19 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
         const int words = p.K * BITS / 32;
         Ring ring(SC);
         long long issued = 0;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        for (int i = 0; ok; ++i) {
+            int t = blockIdx.x + i * gridDim.x;
+            if (i > 0 && p.tile_counter) {
+                int c = 0;
+                if (lane == 0) c = atomicAdd(p.tile_counter, 1);
+                t = gridDim.x + __shfl_sync(0xffffffffu, c, 0);
+            }
+            if (t > total) t = total;
+            if (!tq_push(i, t)) {
+                ok = false;
+                break;
+            }
+            if (t >= total) break;
             const PTile ti = ptile<GATHER>(p, t, m_tiles, n_tiles);
             for (int j = 0; j < nslots; ++j, ring.next(), ++issued) {
                 if (issued >= SC && !warp_wait_ab(&cempty[ring.slot], ring.parity ^ 1, abort_flag)) {
@@ -960,7 +1005,13 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
         // ---------------------------------------------------------------- activation TMA
         Ring ring(SX);
         long long issued = 0;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        for (int i = 0; ok; ++i) {
+            int t;
+            if (!tq_pop(i, &t)) {
+                ok = false;
+                break;
+            }
+            if (t >= total) break;
             const PTile ti = ptile<GATHER>(p, t, m_tiles, n_tiles);
             const int boxes = (ti.n_mma + p.x_box_rows - 1) / p.x_box_rows;
             const uint32_t x_bytes_in = (uint32_t)(boxes * p.x_box_rows * 128);
@@ -982,8 +1033,13 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issue
         Ring ar(SA), xr(SX);
-        int i = 0;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++i) {
+        for (int i = 0; ok; ++i) {
+            int t;
+            if (!tq_pop(i, &t)) {
+                ok = false;
+                break;
+            }
+            if (t >= total) break;
             const PTile ti = ptile<GATHER>(p, t, m_tiles, n_tiles);
             const int buf = acc_bufs == 2 ? (i & 1) : 0;
             const int use = acc_bufs == 2 ? (i >> 1) : i;  // earlier tiles on this buffer
@@ -1041,8 +1097,13 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
         const int lane_row = quarter * 32 + lane;
         const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
         __nv_bfloat16* y = static_cast<__nv_bfloat16*>(p.y);
-        int i = 0;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++i) {
+        for (int i = 0; ok; ++i) {
+            int t;
+            if (!tq_pop(i, &t)) {
+                ok = false;
+                break;
+            }
+            if (t >= total) break;
             const PTile ti = ptile<GATHER>(p, t, m_tiles, n_tiles);
             const int buf = acc_bufs == 2 ? (i & 1) : 0;
             const int use = acc_bufs == 2 ? (i >> 1) : i;
@@ -1089,30 +1150,18 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
         long long cpos = 0;   // global index of the code slot cr points at
         long long g0 = 0;     // global index of the tile's first stage
         long long tile_i = 0;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tile_i, g0 += nst) {
+        for (int qi = 0; ok; ++qi, ++tile_i, g0 += nst) {
+            int t;
+            if (!tq_pop(qi, &t)) {
+                ok = false;
+                break;
+            }
+            if (t >= total) break;
             const PTile ti = ptile<GATHER>(p, t, m_tiles, n_tiles);
             const int n = ti.n0 + r;
             const bool row_ok = n < p.N;
             const uint16_t* srow = p.scales + (long long)ti.e * p.sb_expert_stride + (long long)n * groups;
             const uint16_t* brow = p.biases + (long long)ti.e * p.sb_expert_stride + (long long)n * groups;
-            // bring the next tile's scales and biases of this row into L2
-            // now (a new tile's are otherwise cold, and its first stages
-            // would wait for HBM)
-            if (grp == 0 && t + (int)gridDim.x < total) {
-                const PTile tn = ptile<GATHER>(p, t + gridDim.x, m_tiles, n_tiles);
-                const int nn = tn.n0 + r;
-                if (nn < p.N) {
-                    const long long off = (long long)tn.e * p.sb_expert_stride + (long long)nn * groups;
-                    const char* sp = reinterpret_cast<const char*>(p.scales + off);
-                    const char* bp = reinterpret_cast<const char*>(p.biases + off);
-                    const uintptr_t s_lo = reinterpret_cast<uintptr_t>(sp) & ~uintptr_t(127);
-                    const uintptr_t b_lo = reinterpret_cast<uintptr_t>(bp) & ~uintptr_t(127);
-                    for (uintptr_t a = s_lo; a < reinterpret_cast<uintptr_t>(sp + groups * 2); a += 128)
-                        prefetch_l2(reinterpret_cast<const void*>(a));
-                    for (uintptr_t a = b_lo; a < reinterpret_cast<uintptr_t>(bp + groups * 2); a += 128)
-                        prefetch_l2(reinterpret_cast<const void*>(a));
-                }
-            }
             const int s0 = (int)((grp + g0) & 1);
             int csub = s0;  // stage within the code slot (kSPS >= 2, so s0 < kSPS)
             // scales and biases of a stage's two groups: {s0, s1, b0, b1}
