@@ -12,6 +12,9 @@ constexpr int kTileN = 128;           // rows of w per CTA in the tensor-core ke
 constexpr int kMaxRowsPerTile = 256;  // MMA N limit
 constexpr int kGatherRowsPerTile = 64;  // expert segments average ~36 rows
 constexpr int kMinKBlocksPerSplit = 8;
+// Grouped calls with at most this many rows (a decode step: a few tokens x
+// top_k) run one HBM-bound GEMV per row instead of the tensor-core GEMM.
+constexpr int kGatherDecodeRows = 32;
 constexpr int kMaxSplits = 8;             // portable cluster size
 constexpr int kMaxDevices = 64;
 
@@ -221,6 +224,13 @@ mxq_status mxq_gather_qmm(const void* x, const uint32_t* w, const void* scales,
     st = check_device(&sms);
     if (st != MXQ_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (B <= kGatherDecodeRows) {
+        if (dev_status && cudaMemsetAsync(dev_status, 0, sizeof(int32_t), s) != cudaSuccess)
+            return MXQ_ERR_CUDA;
+        cudaError_t err = mxq::launch_gather_qmv(x, w, scales, biases, expert_ids, row_src, y, T,
+                                                 B, E, K, N, bits, dev_status, s);
+        return err == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA;
+    }
     auto* tiles = static_cast<mxq::MTile*>(workspace);
     int* tile_count = reinterpret_cast<int*>(static_cast<char*>(workspace) +
                                              align_up(max_tiles * sizeof(mxq::MTile), 256));

@@ -64,6 +64,13 @@ cudaError_t launch_gather_prepass(const int32_t* expert_ids, const int32_t* row_
                                   int* tile_count, int* seg_start, void* y, int32_t* status,
                                   cudaStream_t stream);
 
+// Grouped form with few rows (decode): one GEMV per sorted row against its
+// expert's matrix, validating the ids itself (no tile table, no row copy).
+cudaError_t launch_gather_qmv(const void* x, const uint32_t* w, const void* scales,
+                              const void* biases, const int32_t* expert_ids,
+                              const int32_t* row_src, void* y, int T, int B, int E, int K, int N,
+                              int bits, int32_t* status, cudaStream_t stream);
+
 cudaError_t launch_gather_rows(const void* x, const int32_t* row_src, int T, int B, int K,
                                void* x_sorted, cudaStream_t stream);
 

@@ -9,19 +9,28 @@
 //  * swap-AB: the MMA's M side is 128 rows of w (output columns n), its N side
 //    is a tile of up to 256 activation rows, so a 36-row expert segment or a
 //    single decode row still fills the 128-row tensor-core tile;
-//  * per 128-wide K stage (two quantisation groups) a TMA copy brings the
-//    packed codes of the 128 w rows into a deep ring (the codes stream from
-//    HBM with the longest latency); per 64-wide block the activation tile
-//    comes by TMA with 128-byte swizzle into its own ring (in the grouped
-//    form from a copy of the activation rows in sorted order);
-//  * eight dequant warps (two threads per w row, one 64-wide half each) turn
-//    codes into bf16 w^ = s*q + b (one rounding) and write it straight into
-//    the 128-byte-swizzled K-major layout the tensor core reads;
+//  * a TMA copy brings the packed codes of the 128 w rows into a ring of
+//    slots of 256 bytes per row (two 128-byte-swizzled boxes); per 64-wide
+//    block the activation tile comes by TMA with 128-byte swizzle into its
+//    own ring (in the grouped form from a copy of the activation rows in
+//    sorted order);
+//  * eight dequant warps (two groups of four take alternate 128-wide stages;
+//    thread r owns w row r, its tensor-memory lane) turn codes into bf16
+//    w^ = s*q + b (one rounding) and store them in tensor memory, where the
+//    MMA reads its A operand;
 //  * one elected lane issues eight 128xNx16 tcgen05.mma per stage into fp32
-//    tensor memory; the dequant warps then read the accumulators back with
-//    tcgen05.ld and store bf16.  With K split across the CTAs of a cluster,
-//    the fp32 partials are added through distributed shared memory in rank
-//    order, so the result does not depend on timing.
+//    tensor memory; the epilogue reads the accumulators with tcgen05.ld and
+//    stores bf16.
+//
+// Three launch forms:
+//  * qmm_tc_kernel: one CTA per output tile.  With few tiles (small M), K is
+//    split over the CTAs of a cluster and the fp32 partials are added through
+//    distributed shared memory in rank order, so the result does not depend
+//    on timing;
+//  * qmm_persistent_kernel, dense: one CTA per SM walks the tiles with its
+//    rings running across tile boundaries and four epilogue warps;
+//  * qmm_persistent_kernel, compact (grouped, 4-bit): two CTAs per SM, tiles
+//    handed out by a counter, the dequant warps run the epilogue.
 //
 // Every wait on an mbarrier is bounded; on expiry the kernel sets
 // MXQ_DEV_TIMEOUT, stops issuing work, lets issued work finish and frees its
@@ -47,8 +56,6 @@ constexpr int kThreads = 11 * 32;
 constexpr int kTileN = 128;          // rows of w per CTA (MMA M)
 constexpr int kBK = 128;             // K per dequant/MMA stage: two 64-wide groups
 constexpr int kHalfK = 64;           // K per activation slot (one 128-byte swizzle atom)
-constexpr int kMaxRows = 256;        // activation rows per tile (MMA N <= 256)
-constexpr int kMaxSplits = 8;        // K splits per tile = cluster size (portable limit)
 constexpr int kMaxCodeStages = 8;    // code slots
 // A code slot holds 256 bytes of each of the 128 w rows (the TMA engine
 // handles long row segments far faster than 64-byte ones), as two boxes of
@@ -63,8 +70,9 @@ constexpr int kMaxAStages = 6;       // dequantised stages held in tensor memory
 constexpr int kMaxXStages = 16;
 constexpr int kSmemBudget = 224 * 1024;
 constexpr int kTmemCols = 512;       // accumulator + dequantised A stages
-// Compact mode (tiles of at most 64 activation rows, 4-bit codes): half the
-// shared and tensor memory, so two CTAs share an SM and two pipelines hide
+// Compact layout (grouped form, tiles of at most 64 activation rows, 4-bit
+// codes): half the shared and tensor memory, so two persistent CTAs share an
+// SM and their two pipelines hide
 // each other's latency.
 constexpr int kCompactRows = 64;
 constexpr int kCompactSmemBudget = 108 * 1024;
@@ -170,12 +178,6 @@ __device__ __forceinline__ void dequant_word8(uint32_t wd, float s, float b, uin
     out[1] = cvt_bf16x2(fmaf(s, q2, b), fmaf(s, q3, b));
 }
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-                 "r"(d)
-                 : "memory");
-}
 
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
     uint4 v;
@@ -186,10 +188,6 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
     return v;
 }
 
-// Offset of 16-byte chunk c of row r in a 128-byte-swizzled K-major tile.
-__device__ __forceinline__ uint32_t sw128_offset(int r, int c) {
-    return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
-}
 
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile(
@@ -317,30 +315,17 @@ __device__ __forceinline__ bool warp_wait3(uint64_t* a, uint32_t pa, uint64_t* b
     return __all_sync(0xffffffffu, ok);
 }
 
-// cp.async.wait_group with a run-time count (0..7).
-__device__ __forceinline__ void cp_async_wait_n(int n) {
-    switch (n) {
-        case 0: cp_async_wait<0>(); break;
-        case 1: cp_async_wait<1>(); break;
-        case 2: cp_async_wait<2>(); break;
-        case 3: cp_async_wait<3>(); break;
-        case 4: cp_async_wait<4>(); break;
-        case 5: cp_async_wait<5>(); break;
-        case 6: cp_async_wait<6>(); break;
-        default: cp_async_wait<7>(); break;
-    }
-}
 
 __device__ __forceinline__ void flag_status(int32_t* status, int bits) {
     if (status) atomicOr(status, bits);
 }
 
-template <int BITS, bool GATHER, bool COMPACT>
-__global__ void __launch_bounds__(kThreads, COMPACT ? 2 : 1)
+template <int BITS, bool GATHER>
+__global__ void __launch_bounds__(kThreads, 1)
     qmm_tc_kernel(const QmmParams p, int max_rows, const __grid_constant__ CUtensorMap code_map,
                   const __grid_constant__ CUtensorMap x_map) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    const SmemLayout L = make_layout(BITS, max_rows, COMPACT);
+    const SmemLayout L = make_layout(BITS, max_rows, false);
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     uint64_t* cfull = reinterpret_cast<uint64_t*>(smem + L.bar_offset);
@@ -383,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, COMPACT ? 2 : 1)
     // tensor memory: accumulator in columns [0, n_mma), dequantised stages
     // of 64 columns from a0 on
     const int a0 = (n_mma + kAStageCols - 1) / kAStageCols * kAStageCols;
-    constexpr int kCols = COMPACT ? kCompactTmemCols : kTmemCols;
+    constexpr int kCols = kTmemCols;
     const int SA = min(kMaxAStages, (kCols - a0) / kAStageCols);
 
     if (warp == kCodeWarp && lane == 0) prefetch_tmap(&code_map);
@@ -1354,17 +1339,17 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-template <int BITS, bool GATHER, bool COMPACT>
+template <int BITS, bool GATHER>
 cudaError_t launch_variant(const QmmParams& p, int grid_m, int max_rows, const CUtensorMap& cm,
                            const CUtensorMap& xm, cudaStream_t stream) {
-    const SmemLayout L = make_layout(BITS, max_rows, COMPACT);
+    const SmemLayout L = make_layout(BITS, max_rows, false);
     // the shared-memory opt-in is per device; do it once each
     static bool attr_set[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-        cudaError_t err = cudaFuncSetAttribute(qmm_tc_kernel<BITS, GATHER, COMPACT>,
+        cudaError_t err = cudaFuncSetAttribute(qmm_tc_kernel<BITS, GATHER>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                232448);
         if (err != cudaSuccess) return err;
@@ -1384,7 +1369,7 @@ cudaError_t launch_variant(const QmmParams& p, int grid_m, int max_rows, const C
     attr[0].val.clusterDim.z = p.splits;  // the K splits of one tile form a cluster
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t err = cudaLaunchKernelEx(&cfg, qmm_tc_kernel<BITS, GATHER, COMPACT>, p, max_rows, cm, xm);
+    cudaError_t err = cudaLaunchKernelEx(&cfg, qmm_tc_kernel<BITS, GATHER>, p, max_rows, cm, xm);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
@@ -1439,17 +1424,12 @@ cudaError_t launch_qmm_tc(const QmmParams& p, int bits, int grid_m, int max_rows
                          : launch_persistent<8, false, false>(p, max_rows_per_tile, p.m_tiles,
                                                               n_tiles, p.grid_ctas, cm, xm, stream);
     }
-    if (bits == 4)
-    {
-        // dense small-M launches split K instead (more CTAs, one per SM)
-        if (compact_mode(4, max_rows_per_tile, gather))
-            return gather ? launch_variant<4, true, true>(p, grid_m, max_rows_per_tile, cm, xm, stream)
-                          : launch_variant<4, false, true>(p, grid_m, max_rows_per_tile, cm, xm, stream);
-        return gather ? launch_variant<4, true, false>(p, grid_m, max_rows_per_tile, cm, xm, stream)
-                      : launch_variant<4, false, false>(p, grid_m, max_rows_per_tile, cm, xm, stream);
+    if (bits == 4) {
+        if (gather) return cudaErrorNotSupported;  // 4-bit grouped calls are persistent (above)
+        return launch_variant<4, false>(p, grid_m, max_rows_per_tile, cm, xm, stream);
     }
-    return gather ? launch_variant<8, true, false>(p, grid_m, max_rows_per_tile, cm, xm, stream)
-                  : launch_variant<8, false, false>(p, grid_m, max_rows_per_tile, cm, xm, stream);
+    return gather ? launch_variant<8, true>(p, grid_m, max_rows_per_tile, cm, xm, stream)
+                  : launch_variant<8, false>(p, grid_m, max_rows_per_tile, cm, xm, stream);
 }
 
 }  // namespace mxq

@@ -119,12 +119,16 @@ __device__ __forceinline__ float dot_chunk8(const uint4 c, const float2 (&x2)[16
     return acc.x + acc.y;
 }
 
+// The direct-load GEMV for output rows [row0, row0 + kRows) of one matrix:
+// y[n] = sum_k x[k] * w^[n, k].  Warps split K into segments; a CTA's warps
+// then add their partials in a fixed order.
 template <int BITS>
-__global__ void __launch_bounds__(kMaxWarps * 32) qmv_generic_kernel(const __nv_bfloat16* __restrict__ x,
-                                                   const uint32_t* __restrict__ w,
-                                                   const uint16_t* __restrict__ scales,
-                                                   const uint16_t* __restrict__ biases,
-                                                   __nv_bfloat16* __restrict__ y, int K, int N) {
+__device__ __forceinline__ void qmv_rows_direct(const __nv_bfloat16* __restrict__ x,
+                                                const uint32_t* __restrict__ w,
+                                                const uint16_t* __restrict__ scales,
+                                                const uint16_t* __restrict__ biases,
+                                                __nv_bfloat16* __restrict__ y, int K, int N,
+                                                int row0) {
     constexpr int kCodesPerLane = 128 / BITS;          // 32 or 16
     constexpr int kSegK = 32 * kCodesPerLane;          // 1024 or 512
     constexpr float kUnscale = BITS == 4 ? 128.f : 32768.f;
@@ -133,7 +137,6 @@ __global__ void __launch_bounds__(kMaxWarps * 32) qmv_generic_kernel(const __nv_
     const int lane = lane_id();
     const int warp = threadIdx.x >> 5;
     const int nwarps = blockDim.x >> 5;
-    const int row0 = blockIdx.x * kRows;
     const int nseg = (K + kSegK - 1) / kSegK;
     const long long words_per_row = (long long)K * BITS / 32;
     const int groups = K / 64;
@@ -211,6 +214,60 @@ __global__ void __launch_bounds__(kMaxWarps * 32) qmv_generic_kernel(const __nv_
         for (int wi = 0; wi < nwarps; ++wi) acc += red[wi][threadIdx.x];
         if (n < N) y[n] = __float2bfloat16_rn(acc);
     }
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(kMaxWarps * 32) qmv_generic_kernel(const __nv_bfloat16* __restrict__ x,
+                                                   const uint32_t* __restrict__ w,
+                                                   const uint16_t* __restrict__ scales,
+                                                   const uint16_t* __restrict__ biases,
+                                                   __nv_bfloat16* __restrict__ y, int K, int N) {
+    qmv_rows_direct<BITS>(x, w, scales, biases, y, K, N, blockIdx.x * kRows);
+}
+
+// Grouped form with few rows (decode): sorted row r = blockIdx.y is the GEMV
+// of expert ids[r]'s matrix with activation row row_src[r].  Every CTA checks
+// all the (few) ids itself, so no separate pass is needed: an id outside
+// [0, E) or a source row outside [0, T) makes the row zero; ids that
+// decrease anywhere make every row zero; the first CTA reports the bits.
+template <int BITS>
+__global__ void __launch_bounds__(kMaxWarps * 32) gather_qmv_kernel(
+    const __nv_bfloat16* __restrict__ x, const uint32_t* __restrict__ w,
+    const uint16_t* __restrict__ scales, const uint16_t* __restrict__ biases,
+    const int32_t* __restrict__ ids, const int32_t* __restrict__ row_src,
+    __nv_bfloat16* __restrict__ y, int T, int B, int E, int K, int N, long long w_expert_stride,
+    long long sb_expert_stride, int32_t* status) {
+    __shared__ int flags;
+    if (threadIdx.x == 0) flags = 0;
+    __syncthreads();
+    int f = 0;
+    for (int i = threadIdx.x; i < B; i += blockDim.x) {
+        const int e = ids[i];
+        if (e < 0 || e >= E) f |= 0x1;               // MXQ_DEV_BAD_EXPERT_ID
+        if (i > 0 && ids[i - 1] > e) f |= 0x2;       // MXQ_DEV_UNSORTED_IDS
+        if (row_src) {
+            const int sr = row_src[i];
+            if (sr < 0 || sr >= T) f |= 0x4;         // MXQ_DEV_BAD_ROW_SRC
+        }
+    }
+    if (f) atomicOr(&flags, f);
+    __syncthreads();
+    const int all = flags;
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && all && status)
+        atomicOr(status, all);
+    const int r = blockIdx.y;
+    const int row0 = blockIdx.x * kRows;
+    const int e = ids[r];
+    const int src = row_src ? row_src[r] : r;
+    if ((all & 0x2) || e < 0 || e >= E || src < 0 || src >= T) {
+        if (threadIdx.x < kRows && row0 + (int)threadIdx.x < N)
+            y[(long long)r * N + row0 + threadIdx.x] = __float2bfloat16_rn(0.f);
+        return;  // the whole CTA: no barrier follows
+    }
+    qmv_rows_direct<BITS>(x + (long long)src * K, w + (long long)e * w_expert_stride,
+                          scales + (long long)e * sb_expert_stride,
+                          biases + (long long)e * sb_expert_stride, y + (long long)r * N, K, N,
+                          row0);
 }
 
 
@@ -628,6 +685,31 @@ cudaError_t launch_stream(const __nv_bfloat16* x, const uint32_t* w, const uint1
 }
 
 }  // namespace
+
+cudaError_t launch_gather_qmv(const void* x, const uint32_t* w, const void* scales,
+                              const void* biases, const int32_t* expert_ids,
+                              const int32_t* row_src, void* y, int T, int B, int E, int K, int N,
+                              int bits, int32_t* status, cudaStream_t stream) {
+    const int seg_k = bits == 4 ? 1024 : 512;
+    const int nseg_g = (K + seg_k - 1) / seg_k;
+    const int passes = (nseg_g + kMaxWarps - 1) / kMaxWarps;
+    const int warps = (nseg_g + passes - 1) / passes;
+    const dim3 grid((N + kRows - 1) / kRows, B);
+    const dim3 block(32 * warps);
+    const auto* xb = static_cast<const __nv_bfloat16*>(x);
+    const auto* sb = static_cast<const uint16_t*>(scales);
+    const auto* bb = static_cast<const uint16_t*>(biases);
+    auto* yb = static_cast<__nv_bfloat16*>(y);
+    const long long wst = (long long)N * K * bits / 32;
+    const long long sbst = (long long)N * (K / 64);
+    if (bits == 4)
+        gather_qmv_kernel<4><<<grid, block, 0, stream>>>(xb, w, sb, bb, expert_ids, row_src, yb, T,
+                                                        B, E, K, N, wst, sbst, status);
+    else
+        gather_qmv_kernel<8><<<grid, block, 0, stream>>>(xb, w, sb, bb, expert_ids, row_src, yb, T,
+                                                        B, E, K, N, wst, sbst, status);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_qmv(const void* x, const uint32_t* w, const void* scales, const void* biases,
                        void* y, int K, int N, int bits, int sms, int32_t* status,

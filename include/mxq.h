@@ -110,6 +110,9 @@ mxq_status mxq_qmm(const void* x, const uint32_t* w, const void* scales, const v
  * non-decreasing, nothing is computed, all of y is set to zero and
  * MXQ_DEV_UNSORTED_IDS is reported.  No invalid input makes the kernels
  * read or write out of bounds.
+ * Calls with at most 32 rows (a decode step) run one GEMV per row against
+ * its expert's matrix (the same result rule, another summation order) and
+ * use no workspace memory, though the size check still applies.
  * Requirements: B, E, T, N > 0; K > 0, K % 64 == 0; bits in {4, 8};
  * group_size == 64; x, w, y 16-byte aligned; the rest aligned to type.       */
 mxq_status mxq_gather_qmm(const void* x, const uint32_t* w, const void* scales,

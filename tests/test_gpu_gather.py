@@ -185,3 +185,67 @@ def test_gather_bad_row_src_row_is_zero():
     good[[5, 11]] = False
     yr, bnd = _ref(c, src=np.where(good, src, 0))
     assert_close(y[good], yr[good], bnd[good], "gather with bad row_src")
+
+
+# ---- decode-sized calls (at most 32 sorted rows): one GEMV per row
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("T,K,N,ident", [(1, 2816, 704, False), (4, 704, 2816, True),
+                                         (3, 2816, 704, False)])
+def test_gather_decode_rows(bits, T, K, N, ident):
+    # one to four tokens routed to 8 of 128 experts: whole outputs, and
+    # bitwise determinism
+    import torch
+
+    c = MoECase(T, 128, 8, K, N, bits, seed=11 + T, identity_src=ident, routing_seed=5 + T)
+    assert c.B <= 32
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    y = _run(c, status=status)
+    yr, bnd = _ref(c)
+    assert_close(to_f64(y), yr, bnd, "gather decode T=%d K=%d N=%d bits=%d" % (T, K, N, bits))
+    assert int(status.item()) == 0
+    y2 = _run(c)
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+
+
+def test_gather_decode_constant_per_expert_exact():
+    T, E, top_k, K, N = 4, 12, 8, 256, 136
+    ids, src = synth.routing(T, E, top_k, seed=7)
+    rng = np.random.default_rng(8)
+    x = rng.integers(-4, 5, size=(T, K)).astype(np.float32)
+    cvals = np.array([[(e + 1) + (n % 16) / 16.0 for n in range(N)] for e in range(E)],
+                     np.float32)
+    cb = synth.f32_to_bf16_bits(cvals)
+    s = np.zeros((E, N, K // 64), np.uint16)
+    b = np.repeat(cb[:, :, None], K // 64, axis=2)
+    w = rng.integers(0, 2 ** 32, size=(E, N, K // 8), dtype=np.uint64).astype(np.uint32)
+    y = _mxq().gather_qmm(bf16_dev(synth.f32_to_bf16_bits(x)), codes_dev(w), bf16_dev(s),
+                          bf16_dev(b), i32_dev(ids), i32_dev(src), 4)
+    exact = cvals.astype(np.float64)[ids] * x.sum(axis=1, dtype=np.float64)[src][:, None]
+    want = synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(exact.astype(np.float32)))
+    assert np.array_equal(to_f64(y), want.astype(np.float64))
+
+
+def test_gather_decode_invalid_ids_and_sources():
+    import torch
+
+    T, E, K, N = 12, 4, 128, 128
+    c = MoECase(T, E, 2, K, N, 4, seed=21)
+    ids = np.sort(c.ids).copy()
+    ids[0] = -1
+    ids[-1] = E            # out of range at both ends
+    src = c.src.copy()
+    src[5] = T + 1
+    c.ids = ids.astype(np.int32)
+    c.ids_d = i32_dev(c.ids)
+    status = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    out = torch.full((c.B, N), 7.0, dtype=torch.bfloat16, device="cuda")
+    _run(c, out=out, status=status, src_d=i32_dev(src))
+    st = int(status.item())
+    assert st & _mxq().DEV_BAD_EXPERT_ID and st & _mxq().DEV_BAD_ROW_SRC
+    y = to_f64(out)
+    assert np.all(y[0] == 0) and np.all(y[-1] == 0) and np.all(y[5] == 0)
+    good = np.ones(c.B, bool)
+    good[[0, 5, c.B - 1]] = False
+    yr, bnd = _ref(c, ids=np.clip(ids, 0, E - 1), src=np.where(good, src, 0))
+    assert_close(y[good], yr[good], bnd[good], "gather decode with invalid rows")
