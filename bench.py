@@ -503,6 +503,25 @@ def secondary_measurements(mxq, dev, stream, hbm, bf16_peak, Ws):
                     "us": t * 1e6, "TFLOPS": flops / t / 1e12, "GB_s": nbytes / t / 1e9,
                     "frac_tensor": flops / t / 1e12 / bf16_peak, "frac_hbm": nbytes / t / 1e9 / hbm,
                     "bound": "hbm", "frac_roofline": t_star / t, "tokens_per_s": T / t})
+        # decode-sized call on the same experts: 4 tokens x top 8 = 32 rows
+        ids4, src4 = synth.routing(4, E, top_k, seed=3)
+        B4 = ids4.shape[0]
+        x4 = dev_bf16(synth.activations(B4 if ident else 4, K, seed=1), dev)
+        ids4_d = torch.from_numpy(ids4).to(dev)
+        src4_d = None if ident else torch.from_numpy(src4).to(dev)
+        y4 = torch.empty((B4, N), dtype=torch.bfloat16, device=dev)
+        fn4 = lambda i: mxq.gather_qmm(x4, *copies[i % 2], ids4_d, src4_d, bits, out=y4,  # noqa: E731
+                                       workspace=wsz)
+        for i in range(5):
+            fn4(i)
+        t4, _ = time_launches(fn4, iters, stream)
+        used = len(set(ids4.tolist()))
+        nb4 = used * (N * K * bits // 8 + N * (K // 64) * 4) + x4.numel() * 2 + B4 * N * 2
+        out.append({"name": "gather_qmm decode", "kernel": "gather_qmv_kernel",
+                    "E": E, "top_k": top_k, "tokens": 4, "B": B4, "experts_used": used, "K": K,
+                    "N": N, "bits": bits, "us": t4 * 1e6, "TFLOPS": 2.0 * B4 * K * N / t4 / 1e12,
+                    "GB_s": nb4 / t4 / 1e9, "frac_hbm": nb4 / t4 / 1e9 / hbm, "bound": "hbm",
+                    "frac_roofline": nb4 / t4 / 1e9 / hbm, "tokens_per_s": 4 / t4})
         del w, s, b, copies, x, y
         torch.cuda.empty_cache()
     return out
