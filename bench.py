@@ -441,10 +441,10 @@ def secondary_measurements(mxq, dev, stream, hbm, bf16_peak, Ws):
         d = DenseInputs(W, M, K, N, bits, dev, copies=copies)
         if M == 1:
             fn = lambda i: mxq.qmv(d.x[0], *d.copies[i % copies], bits, out=d.y[0])  # noqa: E731
-            kern = "qmv_kernel"
+            kern = "qmv_stream_kernel"
         else:
             fn = lambda i: mxq.qmm(d.x, *d.copies[i % copies], bits, out=d.y)  # noqa: E731
-            kern = "qmm_tc_kernel"
+            kern = "qmm_tc_kernel or qmm_persistent_kernel"
         for i in range(5):
             fn(i)
         t, _ = time_launches(fn, iters, stream)
@@ -498,7 +498,7 @@ def secondary_measurements(mxq, dev, stream, hbm, bf16_peak, Ws):
         flops = 2.0 * B * K * N
         nbytes = E * (N * K * bits // 8 + N * (K // 64) * 4) + Tx * K * 2 + B * N * 2
         t_star = max(nbytes / (hbm * 1e9), flops / (bf16_peak * 1e12))
-        out.append({"name": "gather_qmm", "kernel": "gather_prepass + qmm_tc_kernel",
+        out.append({"name": "gather_qmm", "kernel": "gather_prepass + gather_rows + qmm_persistent_kernel",
                     "E": E, "top_k": top_k, "tokens": T, "B": B, "K": K, "N": N, "bits": bits,
                     "us": t * 1e6, "TFLOPS": flops / t / 1e12, "GB_s": nbytes / t / 1e9,
                     "frac_tensor": flops / t / 1e12 / bf16_peak, "frac_hbm": nbytes / t / 1e9 / hbm,

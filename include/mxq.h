@@ -79,11 +79,13 @@ mxq_status mxq_qmv(const void* x, const uint32_t* w, const void* scales, const v
 
 /* Prefill GEMM, y[M, N] = x[M, K] . w^[N, K]^T (mlxcel issue #1536, Baseline
  * profile table and Diagnosis item 4: the qmm_naive kernel).  Runs on the
- * tcgen05 tensor cores: codes are dequantised to bf16 in shared memory and
- * accumulated in fp32 in tensor memory.  When M and N give fewer tiles than
- * the GPU has SMs, K is split over up to 8 CTAs of a thread-block cluster and
- * the fp32 partials are added through distributed shared memory in a fixed
- * order (deterministic for a given shape).
+ * tcgen05 tensor cores: codes are dequantised to bf16 into tensor memory
+ * (the MMA's A operand) and the products accumulate in fp32 in tensor
+ * memory.  When M and N give fewer 128 x 256 tiles than the GPU has SMs, K is
+ * split over up to 8 CTAs of a thread-block cluster and the fp32 partials are
+ * added through distributed shared memory in a fixed order; with enough
+ * tiles, one persistent CTA per SM walks them.  Either way the result is
+ * deterministic for a given shape.
  * Requirements as for mxq_qmv plus M > 0.  `dev_status` (device int32, may
  * be NULL) receives 0 or MXQ_DEV_TIMEOUT.                                   */
 mxq_status mxq_qmm(const void* x, const uint32_t* w, const void* scales, const void* biases,
