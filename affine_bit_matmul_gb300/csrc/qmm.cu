@@ -92,10 +92,11 @@ struct SmemLayout {
 
 // Ring depths in shared memory (the dequantised A operand lives in tensor
 // memory).  The activation tile comes from L2 with about a microsecond of
-// latency and the packed codes stream from HBM with up to two: at least six
-// activation slots, then as many code stages as fit (up to 16), then more
-// activation slots.
-__host__ __device__ inline SmemLayout make_layout(int bits, int max_rows, bool compact) {
+// latency and the packed codes stream from HBM with up to two: two code
+// slots, up to six activation slots, then more code slots (up to 8), then
+// more activation slots (up to 16).  A code slot is the same 32 KB for both
+// widths (4 stages of 4-bit codes or 2 of 8-bit).
+__host__ __device__ inline SmemLayout make_layout(int max_rows, bool compact) {
     SmemLayout L;
     const int budget = compact ? kCompactSmemBudget : kSmemBudget;
     const int rows16 = (max_rows + 15) & ~15;
@@ -325,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     qmm_tc_kernel(const QmmParams p, int max_rows, const __grid_constant__ CUtensorMap code_map,
                   const __grid_constant__ CUtensorMap x_map) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    const SmemLayout L = make_layout(BITS, max_rows, false);
+    const SmemLayout L = make_layout(max_rows, false);
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     uint64_t* cfull = reinterpret_cast<uint64_t*>(smem + L.bar_offset);
@@ -836,7 +837,7 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
                           const __grid_constant__ CUtensorMap code_map,
                           const __grid_constant__ CUtensorMap x_map) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    const SmemLayout L = make_layout(BITS, max_rows, COMPACT);
+    const SmemLayout L = make_layout(max_rows, COMPACT);
     constexpr int kCols = COMPACT ? kCompactTmemCols : kTmemCols;
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -1299,7 +1300,7 @@ template <int BITS, bool GATHER, bool COMPACT>
 cudaError_t launch_persistent(const QmmParams& p, int max_rows, int m_tiles, int n_tiles,
                               int grid, const CUtensorMap& cm, const CUtensorMap& xm,
                               cudaStream_t stream) {
-    const SmemLayout L = make_layout(BITS, max_rows, COMPACT);
+    const SmemLayout L = make_layout(max_rows, COMPACT);
     const int smem = L.total + kPBarBytes;
     static bool attr_set[64] = {};
     int dev = 0;
@@ -1342,7 +1343,7 @@ EncodeTiledFn encode_fn() {
 template <int BITS, bool GATHER>
 cudaError_t launch_variant(const QmmParams& p, int grid_m, int max_rows, const CUtensorMap& cm,
                            const CUtensorMap& xm, cudaStream_t stream) {
-    const SmemLayout L = make_layout(BITS, max_rows, false);
+    const SmemLayout L = make_layout(max_rows, false);
     // the shared-memory opt-in is per device; do it once each
     static bool attr_set[64] = {};
     int dev = 0;
