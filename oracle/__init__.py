@@ -58,6 +58,7 @@ def _load():
             lib.oracle_points.argtypes = [P, P, P, P, P, P, I, I, I, I, I,
                                           P, P, ctypes.c_longlong, P, P]
             lib.oracle_points.restype = I
+            lib.oracle_quantize.argtypes = [P, I, I, I, I, P, P, P]
             _lib = lib
     return _lib
 
@@ -163,6 +164,20 @@ def points(x, w, scales, biases, rows, cols, K: int, N: int, bits: int, group: i
     if rc:
         raise MemoryError("oracle_points failed")
     return y, bnd
+
+
+def quantize(W, bits: int, group: int = 64):
+    """The affine min/max encoder, binary32 decisions: (codes uint32
+    [N, K*bits/32], scales and biases as bf16 bits uint16 [N, K/group])."""
+    W, pw = _c(W, np.float32)
+    N, K = W.shape
+    codes = np.zeros((N, K * bits // 32), np.uint32)
+    scales = np.zeros((N, K // group), np.uint16)
+    biases = np.zeros((N, K // group), np.uint16)
+    _load().oracle_quantize(pw, N, K, bits, group, codes.ctypes.data_as(ctypes.c_void_p),
+                            scales.ctypes.data_as(ctypes.c_void_p),
+                            biases.ctypes.data_as(ctypes.c_void_p))
+    return codes, scales, biases
 
 
 def within_tolerance(y_gpu, y_ref, bound, rel: float = 8e-3, abs_: float = 1e-3):

@@ -217,3 +217,74 @@ int oracle_points(const uint16_t* x, const uint32_t* w, const uint16_t* scales,
     }
     return fail;
 }
+
+/* ------------------------------------------------------------------ encoder
+ *
+ * The affine min/max encoder that produces the stored format (mlxcel issue
+ * #1536, Baseline section: "affine 4-bit / group 64"; the affine map is read
+ * in its plainest form: per (row, group) the bias is the group minimum and
+ * the scale spreads the group's range over the 2^bits - 1 code steps).  Every
+ * decision is taken in binary32, the precision the GPU encoder uses, so both
+ * sides reach the same codes bit for bit:
+ *
+ *   mn, mx = min, max of the group's values (-0 read as +0)
+ *   s      = bf16(RN(RN(mx - mn) / (2^bits - 1)))     bf16 rounding: RNE
+ *   b      = bf16(mn)
+ *   q      = 0 when s == 0, else clamp(rint(RN(RN(w - b) / s)), 0, 2^bits - 1)
+ *
+ * with s and b used as their stored bf16 values, rint rounding half to even.
+ */
+static uint16_t f32_to_bf16_rne(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+static float bf16_to_f32(uint16_t h) {
+    uint32_t u = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+void oracle_quantize(const float* W, int N, int K, int bits, int group, uint32_t* codes,
+                     uint16_t* scales, uint16_t* biases) {
+    const int levels = (1 << bits) - 1;
+    const int per_word = 32 / bits;
+    const int groups = K / group;
+    const long long words_per_row = (long long)K / per_word;
+#pragma omp parallel for schedule(static)
+    for (int n = 0; n < N; ++n) {
+        for (long long i = 0; i < words_per_row; ++i) codes[(long long)n * words_per_row + i] = 0;
+        for (int g = 0; g < groups; ++g) {
+            const float* v = W + (long long)n * K + (long long)g * group;
+            float mn = v[0] + 0.0f, mx = v[0] + 0.0f;
+            for (int j = 1; j < group; ++j) {
+                const float t = v[j] + 0.0f;
+                if (t < mn) mn = t;
+                if (t > mx) mx = t;
+            }
+            const volatile float range = mx - mn;
+            const volatile float step = range / (float)levels;
+            const uint16_t sb = f32_to_bf16_rne(step);
+            const uint16_t bb = f32_to_bf16_rne(mn);
+            scales[(long long)n * groups + g] = sb;
+            biases[(long long)n * groups + g] = bb;
+            const float s = bf16_to_f32(sb), b = bf16_to_f32(bb);
+            for (int j = 0; j < group; ++j) {
+                unsigned q = 0;
+                if (s != 0.0f) {
+                    const volatile float d = v[j] - b;
+                    const volatile float t = d / s;
+                    float r = rintf(t);
+                    if (r < 0.0f) r = 0.0f;
+                    if (r > (float)levels) r = (float)levels;
+                    q = (unsigned)r;
+                }
+                const int k = g * group + j;
+                codes[(long long)n * words_per_row + k / per_word] |= (uint32_t)q << ((k % per_word) * bits);
+            }
+        }
+    }
+}

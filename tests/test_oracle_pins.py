@@ -392,3 +392,68 @@ def test_routing_recipe():
     assert np.all(np.bincount(src, minlength=573) == 8)
     pairs = set(zip(src.tolist(), ids.tolist()))
     assert len(pairs) == 4584
+
+
+# ---- the affine encoder (binary32 decisions)
+
+def test_quantize_hand_example_exact_grid():
+    # values -1 + 0.25 * (j % 16): min -1, max 2.75, range/15 = 0.25 exactly,
+    # so every code is j % 16 and the stored scale/bias are 0.25 and -1
+    j = np.arange(64)
+    W = (-1.0 + 0.25 * (j % 16)).astype(np.float32)[None, :]
+    for bits in (4, 8):
+        codes, s, b = oracle.quantize(W, bits)
+        step = 0.25 if bits == 4 else 3.75 / 255
+        assert s[0, 0] == synth.f32_to_bf16_bits(np.float32(step))
+        assert b[0, 0] == 0xBF80  # -1.0
+        q = oracle.unpack(codes, 1, 64, bits)[0]
+        if bits == 4:
+            assert np.array_equal(q, j % 16)
+        else:
+            s_f = float(np.asarray(synth.bf16_bits_to_f32(s)).reshape(-1)[0])
+            assert np.array_equal(q, np.clip(np.rint((W[0] + 1.0) / s_f), 0, 255))
+
+
+def test_quantize_flat_group_and_signed_zero():
+    W = np.zeros((2, 128), np.float32)
+    W[0, :64] = 0.3
+    W[0, 64:] = -0.0          # a group of negative zeros
+    W[1, :64] = -0.0
+    W[1, 64:] = np.where(np.arange(64) % 2 == 0, 0.0, -0.0).astype(np.float32)
+    codes, s, b = oracle.quantize(W, 4)
+    assert np.all(s == 0) and np.all(codes == 0)
+    assert b[0, 0] == synth.f32_to_bf16_bits(np.float32(0.3))
+    assert b[0, 1] == 0 and b[1, 0] == 0 and b[1, 1] == 0   # -0 is read as +0
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_quantize_round_trip_bound(bits):
+    rng = np.random.default_rng(31 + bits)
+    W = (rng.standard_normal((48, 1024)) * 0.02).astype(np.float32)
+    codes, s, b = oracle.quantize(W, bits)
+    w_hat = oracle.dequant(codes, s, b, 48, 1024, bits)
+    s_f = np.repeat(synth.bf16_bits_to_f32(s).astype(np.float64), 64, axis=1)
+    Wg = W.reshape(48, 16, 64).astype(np.float64)
+    mag = np.repeat(np.abs(Wg).max(axis=2), 64, axis=1)
+    # half a step; the stored scale is the exact step rounded to bf16 (relative
+    # error <= 2^-9), so the top of the range can sit up to levels * 2^-9
+    # steps past the last code; plus the bf16 rounding of the bias (the group
+    # minimum)
+    levels = (1 << bits) - 1
+    assert np.all(np.abs(W - w_hat) <= (0.5 + levels * 2.0 ** -9) * s_f + 2.0 ** -8 * mag + 1e-12)
+    # and within plain half a step away from the clamped ends
+    inner = (W > np.repeat(Wg.min(axis=2), 64, axis=1) + 2 * s_f) & \
+            (W < np.repeat(Wg.max(axis=2), 64, axis=1) - 2 * s_f)
+    assert np.all(np.abs(W - w_hat)[inner] <= 0.5 * s_f[inner] * (1 + 1e-6) + 1e-12)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_quantize_agrees_with_float64_encoder(bits):
+    # synth.quantize takes the same decisions in float64 (numpy): away from
+    # exact ties the two encoders must agree on every code, scale and bias
+    rng = np.random.default_rng(41 + bits)
+    W = (rng.standard_normal((96, 2048)) * 0.02).astype(np.float32)
+    codes, s, b = oracle.quantize(W, bits)
+    qw = synth.quantize(W, bits)
+    assert np.array_equal(s, qw.scales) and np.array_equal(b, qw.biases)
+    assert np.array_equal(codes, qw.w)
