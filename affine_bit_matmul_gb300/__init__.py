@@ -29,6 +29,7 @@ __all__ = [
     "gather_qmm",
     "gather_workspace_bytes",
     "gather_qmm_noalloc",
+    "quantize",
     "NOALLOC_SCRATCH_BYTES",
     "MxqError",
     "DEV_BAD_EXPERT_ID",
@@ -64,6 +65,7 @@ EXPORTED_SYMBOLS = (
     "mxq_gather_qmm",
     "mxq_gather_workspace_bytes",
     "mxq_gather_qmm_noalloc",
+    "mxq_quantize",
     "mxq_status_string",
     "mxq_version",
 )
@@ -97,6 +99,8 @@ def lib():
         L.mxq_gather_qmm.restype = I
         L.mxq_gather_qmm_noalloc.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P]
         L.mxq_gather_qmm_noalloc.restype = I
+        L.mxq_quantize.argtypes = [P, P, P, P, I, I, I, I, P]
+        L.mxq_quantize.restype = I
         L.mxq_gather_workspace_bytes.argtypes = [I, I, I, I]
         L.mxq_gather_workspace_bytes.restype = Z
         L.mxq_status_string.argtypes = [I]
@@ -212,6 +216,27 @@ def qmm(x, w, scales, biases, bits: int, out=None, dev_status=None, stream=None)
     _check(lib().mxq_qmm(_ptr(x), _ptr(w), _ptr(scales), _ptr(biases), _ptr(out), M, K, N, bits,
                          64, _ptr(dev_status), _stream(stream)), "mxq_qmm")
     return out
+
+
+def quantize(w, bits: int, codes=None, scales=None, biases=None, stream=None):
+    """Affine group-64 encoder on the GPU: float32 ``w`` [N, K] -> (codes
+    int32 [N, K*bits/32], scales bf16 [N, K/64], biases bf16 [N, K/64])."""
+    torch = _torch()
+    _require(w, "w", (torch.float32,))
+    if w.dim() != 2:
+        raise ValueError("w must be 2-D [N, K]")
+    N, K = w.shape
+    dev = w.device
+    if codes is None:
+        codes = torch.empty((N, K * bits // 32), dtype=torch.int32, device=dev)
+    if scales is None:
+        scales = torch.empty((N, K // 64), dtype=torch.bfloat16, device=dev)
+    if biases is None:
+        biases = torch.empty((N, K // 64), dtype=torch.bfloat16, device=dev)
+    _check_weights(codes, scales, biases, N, K, bits, dev)
+    _check(lib().mxq_quantize(_ptr(w), _ptr(codes), _ptr(scales), _ptr(biases), N, K, bits, 64,
+                              _stream(stream)), "mxq_quantize")
+    return codes, scales, biases
 
 
 def gather_workspace_bytes(B: int, E: int, K: int, N: int) -> int:

@@ -195,6 +195,20 @@ mxq_status mxq_qmm(const void* x, const uint32_t* w, const void* scales, const v
     return err == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA;
 }
 
+mxq_status mxq_quantize(const float* w, uint32_t* codes, void* scales, void* biases, int N,
+                        int K, int bits, int group_size, void* stream) {
+    mxq_status st = check_common(K, N, bits, group_size);
+    if (st != MXQ_OK) return st;
+    if (!w || !codes || !scales || !biases) return MXQ_ERR_INVALID_ARG;
+    if (!aligned(w, 16) || !aligned(codes, 16) || !aligned(scales, 2) || !aligned(biases, 2))
+        return MXQ_ERR_MISALIGNED;
+    st = check_device(nullptr);
+    if (st != MXQ_OK) return st;
+    cudaError_t err = mxq::launch_quantize(w, codes, scales, biases, N, K, bits,
+                                           static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA;
+}
+
 size_t mxq_gather_workspace_bytes(int B, int E, int K, int N) {
     (void)N;
     if (B <= 0 || E <= 0 || K < 0) return 0;

@@ -71,6 +71,11 @@ cudaError_t launch_gather_qmv(const void* x, const uint32_t* w, const void* scal
                               const int32_t* row_src, void* y, int T, int B, int E, int K, int N,
                               int bits, int32_t* status, cudaStream_t stream);
 
+// Affine group-wise encoder (group 64): float [N, K] -> codes, bf16 scales
+// and biases.
+cudaError_t launch_quantize(const float* W, uint32_t* codes, void* scales, void* biases, int N,
+                            int K, int bits, cudaStream_t stream);
+
 cudaError_t launch_gather_rows(const void* x, const int32_t* row_src, int T, int B, int K,
                                void* x_sorted, cudaStream_t stream);
 

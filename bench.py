@@ -469,6 +469,24 @@ def secondary_measurements(mxq, dev, stream, hbm, bf16_peak, Ws):
     out.append(dense_entry("pair qmv 4-bit", 1, 5120, 5120, 4, W_sq, copies=6))
     out.append(dense_entry("pair qmm 8-bit", 128, 5120, 5120, 8, W_sq, copies=6))
 
+    # the encoder on the prefill weight shape (float32 in, 4-bit codes out)
+    N_q, K_q = 17408, 5120
+    Wq = [torch.randn((N_q, K_q), device=dev) * 0.02 for _ in range(2)]
+    cq = torch.empty((N_q, K_q // 8), dtype=torch.int32, device=dev)
+    sq = torch.empty((N_q, K_q // 64), dtype=torch.bfloat16, device=dev)
+    bq = torch.empty((N_q, K_q // 64), dtype=torch.bfloat16, device=dev)
+    fnq = lambda i: mxq.quantize(Wq[i % 2], 4, codes=cq, scales=sq, biases=bq)  # noqa: E731
+    for i in range(3):
+        fnq(i)
+    tq, _ = time_launches(fnq, iters, stream)
+    nbq = N_q * K_q * 4 + N_q * K_q // 2 + N_q * (K_q // 64) * 4
+    out.append({"name": "quantize", "kernel": "quantize_kernel", "K": K_q, "N": N_q, "bits": 4,
+                "us": tq * 1e6, "TFLOPS": 0.0, "GB_s": nbq / tq / 1e9,
+                "frac_hbm": nbq / tq / 1e9 / hbm, "bound": "hbm",
+                "frac_roofline": nbq / tq / 1e9 / hbm, "tokens_per_s": 0.0})
+    del Wq, cq, sq, bq
+    torch.cuda.empty_cache()
+
     # sorted MoE gather, both expert shapes
     for K, N, ident in ((2816, 704, False), (704, 2816, True)):
         E, T, top_k, bits = 128, 573, 8, 4

@@ -163,6 +163,21 @@ mxq_status mxq_gather_qmm_noalloc(const void* x, const uint32_t* w, const void* 
                                   int N, int bits, int group_size, int32_t* dev_status,
                                   void* stream);
 
+/* Affine group-wise encoder: the stored format from float weights (the
+ * format of mlxcel issue #1536, Baseline section; the affine map read as
+ * bias = group minimum, scale = group range / (2^bits - 1)).
+ *   w:      float [N, K] row-major (finite), 16-byte aligned
+ *   codes:  uint32 [N, K*bits/32], 16-byte aligned (output)
+ *   scales, biases: bf16 [N, K/64] (output)
+ * Per (row, group of 64): mn, mx = min, max (-0 read as +0);
+ * s = bf16(RN(RN(mx - mn) / (2^bits - 1))), b = bf16(mn), rounded to nearest
+ * even; q = clamp(rint(RN(RN(w - b) / s)), 0, 2^bits - 1) with the stored
+ * bf16 s and b, q = 0 when s == 0.  All decisions in binary32, so the codes
+ * are reproducible bit for bit.  Requirements: bits in {4, 8};
+ * group_size == 64; K > 0, K % 64 == 0; N > 0.                              */
+mxq_status mxq_quantize(const float* w, uint32_t* codes, void* scales, void* biases, int N,
+                        int K, int bits, int group_size, void* stream);
+
 /* Static description of a status code. */
 const char* mxq_status_string(mxq_status status);
 

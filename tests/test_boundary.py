@@ -135,3 +135,16 @@ def test_noalloc_scratch_limit_refused_before_device(L):
     assert 0 < need <= mxq.NOALLOC_SCRATCH_BYTES
     # the routed up projection of the sorted-MoE workload fits
     assert L.mxq_gather_workspace_bytes(4584, 128, 2816, 704) <= mxq.NOALLOC_SCRATCH_BYTES
+
+
+def quantize(L, w=FAKE, codes=FAKE, s=FAKE, b=FAKE, N=16, K=128, bits=4, group=64):
+    return L.mxq_quantize(w, codes, s, b, N, K, bits, group, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(bits=3), 1), (dict(group=32), 1), (dict(K=100), 1), (dict(N=0), 1), (dict(w=None), 1),
+    (dict(codes=None), 1), (dict(w=FAKE_ODD), 2), (dict(codes=FAKE_ODD), 2),
+    (dict(s=ctypes.c_void_p(0x10001)), 2),
+])
+def test_quantize_argument_checks(L, kw, code):
+    assert quantize(L, **kw) == code
