@@ -13,7 +13,8 @@ group 64"):
 * ``x``: bf16 ``[M, K]`` (``[K]`` for ``qmv``);
 * ``w``: int32 or uint32 ``[N, K*bits/32]`` packed codes, 4-bit codes eight per
   little-endian word (lowest k in the lowest nibble), 8-bit codes four per word;
-* ``scales``, ``biases``: bf16 ``[N, K/64]``;
+* ``scales``, ``biases``: bf16 ``[N, K/group_size]``, one pair per group of
+  ``group_size`` consecutive k (32, 64 or 128; every call defaults to 64);
 * result ``y``: bf16 ``[M, N]``.
 """
 
@@ -163,19 +164,23 @@ def _code_dtypes():
     return tuple(out)
 
 
-def _check_weights(w, scales, biases, N, K, bits, device, lead=()):
+def _check_weights(w, scales, biases, N, K, bits, device, lead=(), group_size=64):
     torch = _torch()
     _require(w, "w", _code_dtypes(), device)
     _require(scales, "scales", (torch.bfloat16,), device)
     _require(biases, "biases", (torch.bfloat16,), device)
     if tuple(w.shape) != tuple(lead) + (N, K * bits // 32):
         raise ValueError("w has shape %s, expected %s" % (tuple(w.shape), tuple(lead) + (N, K * bits // 32)))
+    if group_size <= 0:
+        raise ValueError("group_size must be positive")
     for t, name in ((scales, "scales"), (biases, "biases")):
-        if tuple(t.shape) != tuple(lead) + (N, K // 64):
-            raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(lead) + (N, K // 64)))
+        if tuple(t.shape) != tuple(lead) + (N, K // group_size):
+            raise ValueError("%s has shape %s, expected %s" % (
+                name, tuple(t.shape), tuple(lead) + (N, K // group_size)))
 
 
-def qmv(x, w, scales, biases, bits: int, out=None, dev_status=None, stream=None):
+def qmv(x, w, scales, biases, bits: int, out=None, dev_status=None, stream=None,
+        group_size: int = 64):
     """Decode GEMV: ``y[N] = sum_k x[k] * (s*q + b)[n, k]`` (``x`` bf16 [K]).
     ``dev_status`` (CUDA int32 [1]) receives DEV_TIMEOUT if a wait gave up."""
     torch = _torch()
@@ -184,18 +189,19 @@ def qmv(x, w, scales, biases, bits: int, out=None, dev_status=None, stream=None)
         raise ValueError("x must be 1-D [K]")
     K = x.shape[0]
     N = w.shape[0]
-    _check_weights(w, scales, biases, N, K, bits, x.device)
+    _check_weights(w, scales, biases, N, K, bits, x.device, group_size=group_size)
     if out is None:
         out = torch.empty((N,), dtype=torch.bfloat16, device=x.device)
     _require(out, "out", (torch.bfloat16,), x.device)
     if dev_status is not None:
         _require(dev_status, "dev_status", (torch.int32,), x.device)
-    _check(lib().mxq_qmv(_ptr(x), _ptr(w), _ptr(scales), _ptr(biases), _ptr(out), K, N, bits, 64,
-                         _ptr(dev_status), _stream(stream)), "mxq_qmv")
+    _check(lib().mxq_qmv(_ptr(x), _ptr(w), _ptr(scales), _ptr(biases), _ptr(out), K, N, bits,
+                         group_size, _ptr(dev_status), _stream(stream)), "mxq_qmv")
     return out
 
 
-def qmm(x, w, scales, biases, bits: int, out=None, dev_status=None, stream=None):
+def qmm(x, w, scales, biases, bits: int, out=None, dev_status=None, stream=None,
+        group_size: int = 64):
     """Prefill GEMM on the tensor cores: ``y[M, N] = x[M, K] . w^[N, K]^T``.
 
     ``dev_status`` (CUDA int32 [1]) receives DEV_TIMEOUT if a pipeline wait
@@ -207,20 +213,22 @@ def qmm(x, w, scales, biases, bits: int, out=None, dev_status=None, stream=None)
         raise ValueError("x must be 2-D [M, K]")
     M, K = x.shape
     N = w.shape[0]
-    _check_weights(w, scales, biases, N, K, bits, x.device)
+    _check_weights(w, scales, biases, N, K, bits, x.device, group_size=group_size)
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     _require(out, "out", (torch.bfloat16,), x.device)
     if dev_status is not None:
         _require(dev_status, "dev_status", (torch.int32,), x.device)
     _check(lib().mxq_qmm(_ptr(x), _ptr(w), _ptr(scales), _ptr(biases), _ptr(out), M, K, N, bits,
-                         64, _ptr(dev_status), _stream(stream)), "mxq_qmm")
+                         group_size, _ptr(dev_status), _stream(stream)), "mxq_qmm")
     return out
 
 
-def quantize(w, bits: int, codes=None, scales=None, biases=None, stream=None):
-    """Affine group-64 encoder on the GPU: float32 ``w`` [N, K] -> (codes
-    int32 [N, K*bits/32], scales bf16 [N, K/64], biases bf16 [N, K/64])."""
+def quantize(w, bits: int, codes=None, scales=None, biases=None, stream=None,
+             group_size: int = 64):
+    """Affine group-wise encoder on the GPU: float32 ``w`` [N, K] -> (codes
+    int32 [N, K*bits/32], scales bf16 [N, K/G], biases bf16 [N, K/G]),
+    G = ``group_size``."""
     torch = _torch()
     _require(w, "w", (torch.float32,))
     if w.dim() != 2:
@@ -229,13 +237,15 @@ def quantize(w, bits: int, codes=None, scales=None, biases=None, stream=None):
     dev = w.device
     if codes is None:
         codes = torch.empty((N, K * bits // 32), dtype=torch.int32, device=dev)
+    if group_size <= 0:
+        raise ValueError("group_size must be positive")
     if scales is None:
-        scales = torch.empty((N, K // 64), dtype=torch.bfloat16, device=dev)
+        scales = torch.empty((N, K // group_size), dtype=torch.bfloat16, device=dev)
     if biases is None:
-        biases = torch.empty((N, K // 64), dtype=torch.bfloat16, device=dev)
-    _check_weights(codes, scales, biases, N, K, bits, dev)
-    _check(lib().mxq_quantize(_ptr(w), _ptr(codes), _ptr(scales), _ptr(biases), N, K, bits, 64,
-                              _stream(stream)), "mxq_quantize")
+        biases = torch.empty((N, K // group_size), dtype=torch.bfloat16, device=dev)
+    _check_weights(codes, scales, biases, N, K, bits, dev, group_size=group_size)
+    _check(lib().mxq_quantize(_ptr(w), _ptr(codes), _ptr(scales), _ptr(biases), N, K, bits,
+                              group_size, _stream(stream)), "mxq_quantize")
     return codes, scales, biases
 
 
@@ -245,7 +255,7 @@ def gather_workspace_bytes(B: int, E: int, K: int, N: int) -> int:
 
 
 def gather_qmm_noalloc(x, w, scales, biases, expert_ids, row_src, bits: int, out,
-                       dev_status=None, stream=None):
+                       dev_status=None, stream=None, group_size: int = 64):
     """gather_qmm without any allocation: ``out`` must be given, and the
     scratch is the library's fixed MXQ_NOALLOC_SCRATCH_BYTES array (calls on
     one device must not overlap in time; see include/mxq.h)."""
@@ -257,7 +267,7 @@ def gather_qmm_noalloc(x, w, scales, biases, expert_ids, row_src, bits: int, out
     if w.dim() != 3:
         raise ValueError("w must be 3-D [E, N, K*bits/32]")
     E, N = w.shape[0], w.shape[1]
-    _check_weights(w, scales, biases, N, K, bits, x.device, lead=(E,))
+    _check_weights(w, scales, biases, N, K, bits, x.device, lead=(E,), group_size=group_size)
     _require(expert_ids, "expert_ids", (torch.int32,), x.device)
     B = expert_ids.numel()
     if row_src is not None:
@@ -271,17 +281,17 @@ def gather_qmm_noalloc(x, w, scales, biases, expert_ids, row_src, bits: int, out
         _require(dev_status, "dev_status", (torch.int32,), x.device)
     _check(lib().mxq_gather_qmm_noalloc(_ptr(x), _ptr(w), _ptr(scales), _ptr(biases),
                                         _ptr(expert_ids), _ptr(row_src), _ptr(out), T, B, E, K,
-                                        N, bits, 64, _ptr(dev_status), _stream(stream)),
+                                        N, bits, group_size, _ptr(dev_status), _stream(stream)),
            "mxq_gather_qmm_noalloc")
     return out
 
 
 def gather_qmm(x, w, scales, biases, expert_ids, row_src, bits: int, out=None, workspace=None,
-               dev_status=None, stream=None):
+               dev_status=None, stream=None, group_size: int = 64):
     """Sorted mixture-of-experts GEMM: sorted row r multiplies expert
     ``expert_ids[r]``'s dequantised matrix by ``x[row_src[r]]``.
 
-    ``w`` is [E, N, K*bits/32], ``scales``/``biases`` [E, N, K/64],
+    ``w`` is [E, N, K*bits/32], ``scales``/``biases`` [E, N, K/group_size],
     ``expert_ids`` int32 [B] non-decreasing, ``row_src`` int32 [B] or None
     (identity).  Returns y bf16 [B, N] in sorted row order.
     """
@@ -293,7 +303,7 @@ def gather_qmm(x, w, scales, biases, expert_ids, row_src, bits: int, out=None, w
     if w.dim() != 3:
         raise ValueError("w must be 3-D [E, N, K*bits/32]")
     E, N = w.shape[0], w.shape[1]
-    _check_weights(w, scales, biases, N, K, bits, x.device, lead=(E,))
+    _check_weights(w, scales, biases, N, K, bits, x.device, lead=(E,), group_size=group_size)
     _require(expert_ids, "expert_ids", (torch.int32,), x.device)
     B = expert_ids.numel()
     if row_src is not None:
@@ -310,7 +320,7 @@ def gather_qmm(x, w, scales, biases, expert_ids, row_src, bits: int, out=None, w
     if dev_status is not None:
         _require(dev_status, "dev_status", (torch.int32,), x.device)
     _check(lib().mxq_gather_qmm(_ptr(x), _ptr(w), _ptr(scales), _ptr(biases), _ptr(expert_ids),
-                                _ptr(row_src), _ptr(out), T, B, E, K, N, bits, 64,
+                                _ptr(row_src), _ptr(out), T, B, E, K, N, bits, group_size,
                                 _ptr(workspace), workspace.numel(), _ptr(dev_status),
                                 _stream(stream)), "mxq_gather_qmm")
     return out

@@ -49,8 +49,8 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 mxq_status check_common(int K, int N, int bits, int group_size) {
     if (bits != 4 && bits != 8) return MXQ_ERR_INVALID_ARG;
-    if (group_size != 64) return MXQ_ERR_INVALID_ARG;
-    if (K <= 0 || N <= 0 || K % 64 != 0) return MXQ_ERR_INVALID_ARG;
+    if (group_size != 32 && group_size != 64 && group_size != 128) return MXQ_ERR_INVALID_ARG;
+    if (K <= 0 || N <= 0 || K % 64 != 0 || K % group_size != 0) return MXQ_ERR_INVALID_ARG;
     return MXQ_OK;
 }
 
@@ -131,7 +131,8 @@ mxq_status mxq_qmv(const void* x, const uint32_t* w, const void* scales, const v
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (dev_status && cudaMemsetAsync(dev_status, 0, sizeof(int32_t), s) != cudaSuccess)
         return MXQ_ERR_CUDA;
-    cudaError_t err = mxq::launch_qmv(x, w, scales, biases, y, K, N, bits, sms, dev_status, s);
+    cudaError_t err =
+        mxq::launch_qmv(x, w, scales, biases, y, K, N, bits, group_size, sms, dev_status, s);
     return err == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA;
 }
 
@@ -173,6 +174,7 @@ mxq_status mxq_qmm(const void* x, const uint32_t* w, const void* scales, const v
     p.E = 1;
     p.K = K;
     p.N = N;
+    p.group = group_size;
     p.x_rows = M;
     p.x_box_rows = pl.m_tile;
     p.m_tile = pl.m_tile;
@@ -204,7 +206,7 @@ mxq_status mxq_quantize(const float* w, uint32_t* codes, void* scales, void* bia
         return MXQ_ERR_MISALIGNED;
     st = check_device(nullptr);
     if (st != MXQ_OK) return st;
-    cudaError_t err = mxq::launch_quantize(w, codes, scales, biases, N, K, bits,
+    cudaError_t err = mxq::launch_quantize(w, codes, scales, biases, N, K, bits, group_size,
                                            static_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA;
 }
@@ -242,7 +244,7 @@ mxq_status mxq_gather_qmm(const void* x, const uint32_t* w, const void* scales,
         if (dev_status && cudaMemsetAsync(dev_status, 0, sizeof(int32_t), s) != cudaSuccess)
             return MXQ_ERR_CUDA;
         cudaError_t err = mxq::launch_gather_qmv(x, w, scales, biases, expert_ids, row_src, y, T,
-                                                 B, E, K, N, bits, dev_status, s);
+                                                 B, E, K, N, bits, group_size, dev_status, s);
         return err == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA;
     }
     auto* tiles = static_cast<mxq::MTile*>(workspace);
@@ -277,12 +279,13 @@ mxq_status mxq_gather_qmm(const void* x, const uint32_t* w, const void* scales,
     p.E = E;
     p.K = K;
     p.N = N;
+    p.group = group_size;
     p.m_tile = kGatherRowsPerTile;
     p.tmem_cols = kGatherRowsPerTile;
     p.splits = 1;
     p.kb_per_split = K / 64;
     p.w_expert_stride = (long long)N * K * bits / 32;
-    p.sb_expert_stride = (long long)N * (K / 64);
+    p.sb_expert_stride = (long long)N * (K / group_size);
     // 4-bit: two persistent CTAs per SM take tiles of (tile list) x (n tiles)
     // from a counter as they finish the previous one, so the pipeline fills
     // once per CTA and long and short tiles balance; 8-bit: one CTA per tile

@@ -20,8 +20,8 @@ struct MTile {
 struct QmmParams {
     const void* x;           // bf16 [T or M, K]
     const uint32_t* w;       // uint32 [E, N, K*bits/32]
-    const uint16_t* scales;  // bf16 [E, N, K/64]
-    const uint16_t* biases;  // bf16 [E, N, K/64]
+    const uint16_t* scales;  // bf16 [E, N, K/group]
+    const uint16_t* biases;  // bf16 [E, N, K/group]
     void* y;                 // bf16 [rows, N]
     const MTile* tiles;      // grouped form: tile list, or null (dense form)
     const int* tile_count;   // grouped form: number of valid tiles
@@ -32,6 +32,7 @@ struct QmmParams {
     int T;                   // grouped form: rows of x
     int E;                   // grouped form: experts
     int K, N;
+    int group;               // k values per scale/bias pair: 32, 64 or 128
     int m_tile;              // dense form: rows per M tile (multiple of 16)
     int tmem_cols;           // tensor-memory columns allocated per CTA
     int splits;              // K splits = cluster size along z (1 = none)
@@ -45,8 +46,9 @@ struct QmmParams {
                              // launch), or null for a fixed gridDim.x stride
 };
 
+// Decode GEMV; group = k values per scale/bias pair (32, 64 or 128).
 cudaError_t launch_qmv(const void* x, const uint32_t* w, const void* scales, const void* biases,
-                       void* y, int K, int N, int bits, int sms, int32_t* status,
+                       void* y, int K, int N, int bits, int group, int sms, int32_t* status,
                        cudaStream_t stream);
 
 // Dense or grouped tcgen05 GEMM; grid.y = number of M tiles (dense) or an
@@ -69,12 +71,12 @@ cudaError_t launch_gather_prepass(const int32_t* expert_ids, const int32_t* row_
 cudaError_t launch_gather_qmv(const void* x, const uint32_t* w, const void* scales,
                               const void* biases, const int32_t* expert_ids,
                               const int32_t* row_src, void* y, int T, int B, int E, int K, int N,
-                              int bits, int32_t* status, cudaStream_t stream);
+                              int bits, int group, int32_t* status, cudaStream_t stream);
 
-// Affine group-wise encoder (group 64): float [N, K] -> codes, bf16 scales
-// and biases.
+// Affine group-wise encoder (groups of 32, 64 or 128): float [N, K] ->
+// codes, bf16 scales and biases.
 cudaError_t launch_quantize(const float* W, uint32_t* codes, void* scales, void* biases, int N,
-                            int K, int bits, cudaStream_t stream);
+                            int K, int bits, int group, cudaStream_t stream);
 
 cudaError_t launch_gather_rows(const void* x, const int32_t* row_src, int T, int B, int K,
                                void* x_sorted, cudaStream_t stream);

@@ -1,5 +1,6 @@
 // Quantized GEMM on the sm_103a tensor cores: y = x . w^T with w dequantised
-// on the fly (w^ = s*q + b per 64-wide group), dense and sorted-MoE forms.
+// on the fly (w^ = s*q + b per group of 32, 64 or 128 consecutive k), dense
+// and sorted-MoE forms.
 //
 // Prior art: the qmm_naive and grouped-GEMM kernels profiled in mlxcel issue
 // #1536 (Baseline profile table; Diagnosis items 1, 4 and 5) and PR #1562
@@ -77,6 +78,23 @@ constexpr int kTmemCols = 512;       // accumulator + dequantised A stages
 constexpr int kCompactRows = 64;
 constexpr int kCompactSmemBudget = 108 * 1024;
 constexpr int kCompactTmemCols = 256;
+
+// Scale/bias pairs of one 128-wide stage.  Groups of 64 or 128 give one
+// pair per 64-wide half (two halves of one 128-group load the same pair);
+// groups of 32 give one pair per 32-wide quarter.  Pair i of a stage whose
+// first 64-wide block is kb (counted from k = 0) belongs to group
+// group_of(kb, i); the dequantiser's half h, 32-wide chunk c uses pair
+// pair_of(h, c).
+template <int GROUP>
+struct StageGroups {
+    static_assert(GROUP == 32 || GROUP == 64 || GROUP == 128, "group of 32, 64 or 128");
+    static constexpr int kPairs = GROUP == 32 ? 4 : 2;
+    __device__ static constexpr int half_of(int i) { return GROUP == 32 ? i >> 1 : i; }
+    __device__ static constexpr int pair_of(int h, int c) { return GROUP == 32 ? h * 2 + c : h; }
+    __device__ static int group_of(int kb, int i) {
+        return GROUP == 32 ? kb * 2 + i : (kb + i) / (GROUP / 64);
+    }
+};
 
 __host__ __device__ constexpr bool compact_mode(int bits, int max_rows, bool gather) {
     return gather && bits == 4 && max_rows <= kCompactRows;
@@ -321,7 +339,7 @@ __device__ __forceinline__ void flag_status(int32_t* status, int bits) {
     if (status) atomicOr(status, bits);
 }
 
-template <int BITS, bool GATHER>
+template <int BITS, bool GATHER, int GROUP>
 __global__ void __launch_bounds__(kThreads, 1)
     qmm_tc_kernel(const QmmParams p, int max_rows, const __grid_constant__ CUtensorMap code_map,
                   const __grid_constant__ CUtensorMap x_map) {
@@ -358,11 +376,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int n_mma = (rows + 15) & ~15;
     const int n0 = blockIdx.x * kTileN;
-    const int KB = p.K / kHalfK;                       // 64-wide blocks (= groups)
+    const int KB = p.K / kHalfK;                       // 64-wide blocks
     const int kb_begin = blockIdx.z * p.kb_per_split;  // in 64-wide blocks
     const int nkb = min(KB, kb_begin + p.kb_per_split) - kb_begin;
     const int nst = (nkb + 1) / 2;                     // 128-wide stages
-    const int groups = p.K / 64;
+    const int groups = p.K / GROUP;
+    using SG = StageGroups<GROUP>;
+    constexpr int kP = SG::kPairs;
     const int SC = L.c_stages;
     constexpr int kStagesPerSlot = kCodeSlotRowBytes / (kBK * BITS / 8);
     const int SX = L.x_stages;
@@ -491,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------------- dequant
         // two groups of four warps take alternate 128-wide stages, so two
         // stages are dequantised at once; thread r handles w row r (its TMEM
-        // lane) over the whole stage: two 64-wide groups
+        // lane) over the whole stage
         const int r = threadIdx.x & (kTileN - 1);
         const int grp = warp >> 2;
         const int n = n0 + r;
@@ -506,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         Ring cr(SC), ar(SA);
         int csub = grp;  // stage within the code slot (kStagesPerSlot >= 2)
         if (grp) ar.next();
-        auto stage = [&](int s, const uint32_t (&sb)[4]) -> bool {
+        auto stage = [&](int s, const uint32_t (&sb)[2 * kP]) -> bool {
             const int cs = cr.slot;
             if (!warp_wait(&cfull[cs], cr.parity)) return false;
             // this stage's kRowBytes of row r: box (off / 128), chunks from
@@ -526,9 +546,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 if (2 * s + h >= nkb) break;  // the second half past this split's K
-                const uint32_t sbits = sb[h], bbits = sb[2 + h];
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {  // 32 k = 16 columns per store
+                    const uint32_t sbits = sb[SG::pair_of(h, c)];
+                    const uint32_t bbits = sb[kP + SG::pair_of(h, c)];
                     uint32_t o[16];
                     if (BITS == 4) {
                         const uint32_t s2 = sbits | (sbits << 16);
@@ -577,19 +598,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             ar.next();
             return true;
         };
-        // scales and biases of a stage's two groups: {s0, s1, b0, b1}
-        auto sb_load = [&](int s, uint32_t (&sb)[4]) {
+        // scales then biases of a stage's pairs: {s_0 .. s_kP-1, b_0 .. b_kP-1}
+        auto sb_load = [&](int s, uint32_t (&sb)[2 * kP]) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int b = 2 * s + h;
+            for (int i = 0; i < kP; ++i) {
+                const int b = 2 * s + SG::half_of(i);
                 if (row_ok && s < nst && b < nkb) {
-                    sb[h] = __ldg(srow + kb_begin + b);
-                    sb[2 + h] = __ldg(brow + kb_begin + b);
+                    const int g = SG::group_of(kb_begin + 2 * s, i);
+                    sb[i] = __ldg(srow + g);
+                    sb[kP + i] = __ldg(brow + g);
                 }
             }
         };
         // this group's stages grp, grp + 2, ...; scales loaded a stage ahead
-        uint32_t sbA[4] = {0, 0, 0, 0}, sbB[4] = {0, 0, 0, 0};
+        uint32_t sbA[2 * kP] = {}, sbB[2 * kP] = {};
         sb_load(grp, sbA);
         sb_load(grp + 2, sbB);
         for (int s = grp; s < nst && ok; s += 4) {
@@ -831,7 +853,7 @@ __device__ __forceinline__ void drain_copies(uint64_t* full, int slots, long lon
     }
 }
 
-template <int BITS, bool GATHER, bool COMPACT>
+template <int BITS, bool GATHER, bool COMPACT, int GROUP>
 __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 1)
     qmm_persistent_kernel(const QmmParams p, int max_rows, int m_tiles, int n_tiles,
                           const __grid_constant__ CUtensorMap code_map,
@@ -862,11 +884,13 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
     const int warp = threadIdx.x >> 5;
     const int lane = lane_id();
     const int total = GATHER ? (*p.tile_count) * n_tiles : m_tiles * n_tiles;
-    const int KB = p.K / kHalfK;              // 64-wide blocks (= groups)
+    const int KB = p.K / kHalfK;              // 64-wide blocks
     const int nst = (KB + 1) / 2;             // 128-wide stages per tile
     constexpr int kSPS = kCodeSlotRowBytes / (kBK * BITS / 8);  // stages per code slot
     const int nslots = (nst + kSPS - 1) / kSPS;
-    const int groups = p.K / 64;
+    const int groups = p.K / GROUP;
+    using SG = StageGroups<GROUP>;
+    constexpr int kP = SG::kPairs;
     const int SC = L.c_stages;
     const int SX = L.x_stages;
     // tensor memory: one or two accumulators, then the dequantised A stages
@@ -1123,7 +1147,7 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
         // ---------------------------------------------------------------- dequant
         // group g takes the stages whose global index (over all tiles of this
         // CTA) is congruent to g mod 2; thread r handles w row r (its TMEM
-        // lane) over the whole stage: two 64-wide groups
+        // lane) over the whole stage
         const int r = threadIdx.x & (kTileN - 1);
         const int grp = warp >> 2;
         constexpr int kRowBytes = kBK * BITS / 8;  // codes of one row per stage
@@ -1150,20 +1174,21 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
             const uint16_t* brow = p.biases + (long long)ti.e * p.sb_expert_stride + (long long)n * groups;
             const int s0 = (int)((grp + g0) & 1);
             int csub = s0;  // stage within the code slot (kSPS >= 2, so s0 < kSPS)
-            // scales and biases of a stage's two groups: {s0, s1, b0, b1}
-            auto sb_load = [&](int s, uint32_t (&sb)[4]) {
+            // scales then biases of a stage's pairs: {s_0 .. s_kP-1, b_0 .. b_kP-1}
+            auto sb_load = [&](int s, uint32_t (&sb)[2 * kP]) {
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int b = 2 * s + h;
-                    sb[h] = 0;
-                    sb[2 + h] = 0;
+                for (int i = 0; i < kP; ++i) {
+                    const int b = 2 * s + SG::half_of(i);
+                    sb[i] = 0;
+                    sb[kP + i] = 0;
                     if (row_ok && s < nst && b < KB) {
-                        sb[h] = __ldg(srow + b);
-                        sb[2 + h] = __ldg(brow + b);
+                        const int g = SG::group_of(2 * s, i);
+                        sb[i] = __ldg(srow + g);
+                        sb[kP + i] = __ldg(brow + g);
                     }
                 }
             };
-            auto stage = [&](int s, const uint32_t (&sb)[4]) -> bool {
+            auto stage = [&](int s, const uint32_t (&sb)[2 * kP]) -> bool {
                 const int cs = cr.slot;
                 if (!warp_wait_ab(&cfull[cs], cr.parity, abort_flag)) return false;
                 const int off = csub * kRowBytes;
@@ -1181,9 +1206,10 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     if (2 * s + h >= KB) break;  // a last half-stage when K / 64 is odd
-                    const uint32_t sbits = sb[h], bbits = sb[2 + h];
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {  // 32 k = 16 columns per store
+                        const uint32_t sbits = sb[SG::pair_of(h, c)];
+                        const uint32_t bbits = sb[kP + SG::pair_of(h, c)];
                         uint32_t o[16];
                         if (BITS == 4) {
                             const uint32_t s2 = sbits | (sbits << 16);
@@ -1236,7 +1262,7 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
             // this group's stages s0, s0 + 2, ...: two scale/bias buffers,
             // each reloaded (two of this group's stages ahead) right after
             // its use, so no register copy ever waits on a pending load
-            uint32_t sbA[4], sbB[4];
+            uint32_t sbA[2 * kP], sbB[2 * kP];
             sb_load(s0, sbA);
             sb_load(s0 + 2, sbB);
             for (int s = s0; s < nst && ok; s += 4) {
@@ -1296,7 +1322,7 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
     }
 }
 
-template <int BITS, bool GATHER, bool COMPACT>
+template <int BITS, bool GATHER, bool COMPACT, int GROUP>
 cudaError_t launch_persistent(const QmmParams& p, int max_rows, int m_tiles, int n_tiles,
                               int grid, const CUtensorMap& cm, const CUtensorMap& xm,
                               cudaStream_t stream) {
@@ -1307,14 +1333,14 @@ cudaError_t launch_persistent(const QmmParams& p, int max_rows, int m_tiles, int
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-        cudaError_t err = cudaFuncSetAttribute(qmm_persistent_kernel<BITS, GATHER, COMPACT>,
+        cudaError_t err = cudaFuncSetAttribute(qmm_persistent_kernel<BITS, GATHER, COMPACT, GROUP>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                232448);
         if (err != cudaSuccess) return err;
         attr_set[dev] = true;
     }
     if (smem > 232448) return cudaErrorInvalidConfiguration;
-    qmm_persistent_kernel<BITS, GATHER, COMPACT>
+    qmm_persistent_kernel<BITS, GATHER, COMPACT, GROUP>
         <<<grid, COMPACT ? kThreads : kPThreads, smem, stream>>>(p, max_rows, m_tiles, n_tiles, cm,
                                                                  xm);
     return cudaGetLastError();
@@ -1340,7 +1366,7 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-template <int BITS, bool GATHER>
+template <int BITS, bool GATHER, int GROUP>
 cudaError_t launch_variant(const QmmParams& p, int grid_m, int max_rows, const CUtensorMap& cm,
                            const CUtensorMap& xm, cudaStream_t stream) {
     const SmemLayout L = make_layout(max_rows, false);
@@ -1350,7 +1376,7 @@ cudaError_t launch_variant(const QmmParams& p, int grid_m, int max_rows, const C
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-        cudaError_t err = cudaFuncSetAttribute(qmm_tc_kernel<BITS, GATHER>,
+        cudaError_t err = cudaFuncSetAttribute(qmm_tc_kernel<BITS, GATHER, GROUP>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                232448);
         if (err != cudaSuccess) return err;
@@ -1370,9 +1396,36 @@ cudaError_t launch_variant(const QmmParams& p, int grid_m, int max_rows, const C
     attr[0].val.clusterDim.z = p.splits;  // the K splits of one tile form a cluster
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t err = cudaLaunchKernelEx(&cfg, qmm_tc_kernel<BITS, GATHER>, p, max_rows, cm, xm);
+    cudaError_t err = cudaLaunchKernelEx(&cfg, qmm_tc_kernel<BITS, GATHER, GROUP>, p, max_rows, cm, xm);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
+}
+
+// Launch form for one group size: persistent (dense 4/8-bit; grouped 4-bit
+// compact), else one CTA per tile (dense with a K split; grouped 8-bit).
+template <int GROUP>
+cudaError_t launch_group(const QmmParams& p, int bits, bool gather, int grid_m,
+                         int max_rows_per_tile, const CUtensorMap& cm, const CUtensorMap& xm,
+                         cudaStream_t stream) {
+    if (p.persistent) {
+        const int n_tiles = (p.N + kTileN - 1) / kTileN;
+        if (gather) {
+            // grouped, 4-bit, short tiles: two persistent CTAs per SM
+            if (bits != 4 || !compact_mode(4, max_rows_per_tile, true)) return cudaErrorNotSupported;
+            return launch_persistent<4, true, true, GROUP>(p, max_rows_per_tile, 0, n_tiles,
+                                                           p.grid_ctas, cm, xm, stream);
+        }
+        return bits == 4 ? launch_persistent<4, false, false, GROUP>(
+                               p, max_rows_per_tile, p.m_tiles, n_tiles, p.grid_ctas, cm, xm, stream)
+                         : launch_persistent<8, false, false, GROUP>(
+                               p, max_rows_per_tile, p.m_tiles, n_tiles, p.grid_ctas, cm, xm, stream);
+    }
+    if (bits == 4) {
+        if (gather) return cudaErrorNotSupported;  // 4-bit grouped calls are persistent (above)
+        return launch_variant<4, false, GROUP>(p, grid_m, max_rows_per_tile, cm, xm, stream);
+    }
+    return gather ? launch_variant<8, true, GROUP>(p, grid_m, max_rows_per_tile, cm, xm, stream)
+                  : launch_variant<8, false, GROUP>(p, grid_m, max_rows_per_tile, cm, xm, stream);
 }
 
 }  // namespace
@@ -1412,25 +1465,12 @@ cudaError_t launch_qmm_tc(const QmmParams& p, int bits, int grid_m, int max_rows
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    if (p.persistent) {
-        const int n_tiles = (p.N + kTileN - 1) / kTileN;
-        if (gather) {
-            // grouped, 4-bit, short tiles: two persistent CTAs per SM
-            if (bits != 4 || !compact_mode(4, max_rows_per_tile, true)) return cudaErrorNotSupported;
-            return launch_persistent<4, true, true>(p, max_rows_per_tile, 0, n_tiles, p.grid_ctas,
-                                                    cm, xm, stream);
-        }
-        return bits == 4 ? launch_persistent<4, false, false>(p, max_rows_per_tile, p.m_tiles,
-                                                              n_tiles, p.grid_ctas, cm, xm, stream)
-                         : launch_persistent<8, false, false>(p, max_rows_per_tile, p.m_tiles,
-                                                              n_tiles, p.grid_ctas, cm, xm, stream);
+    switch (p.group) {
+        case 32: return launch_group<32>(p, bits, gather, grid_m, max_rows_per_tile, cm, xm, stream);
+        case 64: return launch_group<64>(p, bits, gather, grid_m, max_rows_per_tile, cm, xm, stream);
+        case 128: return launch_group<128>(p, bits, gather, grid_m, max_rows_per_tile, cm, xm, stream);
+        default: return cudaErrorInvalidValue;
     }
-    if (bits == 4) {
-        if (gather) return cudaErrorNotSupported;  // 4-bit grouped calls are persistent (above)
-        return launch_variant<4, false>(p, grid_m, max_rows_per_tile, cm, xm, stream);
-    }
-    return gather ? launch_variant<8, true>(p, grid_m, max_rows_per_tile, cm, xm, stream)
-                  : launch_variant<8, false>(p, grid_m, max_rows_per_tile, cm, xm, stream);
 }
 
 }  // namespace mxq

@@ -7,7 +7,7 @@
 // Two kernels share the arithmetic below.
 //
 // qmv_stream_kernel (K a multiple of 512, K <= 20480, 16-byte aligned
-// scales/biases): persistent CTAs, one per SM.  A producer thread streams
+// scales/biases, a multiple of 8 groups per row): persistent CTAs, one per SM.  A producer thread streams
 // chunks of R consecutive rows (their codes, scales and biases are each one
 // contiguous block) into a ring of shared-memory stages with bulk async
 // copies (cp.async.bulk + mbarrier transaction counts), so ~100 KB per SM
@@ -25,7 +25,8 @@
 //
 // Layout of the work in both:
 //  * a lane owns 16 bytes of codes per row (32 four-bit or 16 eight-bit
-//    codes, always inside one group of 64), so a warp covers a K segment of
+//    codes, always inside one group: groups are 32, 64 or 128 wide and a
+//    lane's first k is a multiple of its code count), so a warp covers a K segment of
 //    1024 (4-bit) or 512 (8-bit) values with one coalesced 512-byte load per
 //    row;
 //  * a CTA has one warp per K segment and owns a block of ROWS output rows;
@@ -128,7 +129,7 @@ __device__ __forceinline__ void qmv_rows_direct(const __nv_bfloat16* __restrict_
                                                 const uint16_t* __restrict__ scales,
                                                 const uint16_t* __restrict__ biases,
                                                 __nv_bfloat16* __restrict__ y, int K, int N,
-                                                int row0) {
+                                                int group, int row0) {
     constexpr int kCodesPerLane = 128 / BITS;          // 32 or 16
     constexpr int kSegK = 32 * kCodesPerLane;          // 1024 or 512
     constexpr float kUnscale = BITS == 4 ? 128.f : 32768.f;
@@ -139,7 +140,7 @@ __device__ __forceinline__ void qmv_rows_direct(const __nv_bfloat16* __restrict_
     const int nwarps = blockDim.x >> 5;
     const int nseg = (K + kSegK - 1) / kSegK;
     const long long words_per_row = (long long)K * BITS / 32;
-    const int groups = K / 64;
+    const int groups = K / group;
 
     float part[kRows];
 #pragma unroll
@@ -166,7 +167,7 @@ __device__ __forceinline__ void qmv_rows_direct(const __nv_bfloat16* __restrict_
 #pragma unroll
             for (int j = 0; j < kCodesPerLane / 2; ++j) X += x2[j].x + x2[j].y;
         }
-        const int g = k0 / 64;
+        const int g = k0 / group;
         const long long wofs = (long long)k0 * BITS / 32;  // word offset in a row
 
 #pragma unroll
@@ -221,8 +222,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32) qmv_generic_kernel(const __nv_
                                                    const uint32_t* __restrict__ w,
                                                    const uint16_t* __restrict__ scales,
                                                    const uint16_t* __restrict__ biases,
-                                                   __nv_bfloat16* __restrict__ y, int K, int N) {
-    qmv_rows_direct<BITS>(x, w, scales, biases, y, K, N, blockIdx.x * kRows);
+                                                   __nv_bfloat16* __restrict__ y, int K, int N,
+                                                   int group) {
+    qmv_rows_direct<BITS>(x, w, scales, biases, y, K, N, group, blockIdx.x * kRows);
 }
 
 // Grouped form with few rows (decode): sorted row r = blockIdx.y is the GEMV
@@ -235,8 +237,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32) gather_qmv_kernel(
     const __nv_bfloat16* __restrict__ x, const uint32_t* __restrict__ w,
     const uint16_t* __restrict__ scales, const uint16_t* __restrict__ biases,
     const int32_t* __restrict__ ids, const int32_t* __restrict__ row_src,
-    __nv_bfloat16* __restrict__ y, int T, int B, int E, int K, int N, long long w_expert_stride,
-    long long sb_expert_stride, int32_t* status) {
+    __nv_bfloat16* __restrict__ y, int T, int B, int E, int K, int N, int group,
+    long long w_expert_stride, long long sb_expert_stride, int32_t* status) {
     __shared__ int flags;
     if (threadIdx.x == 0) flags = 0;
     __syncthreads();
@@ -267,7 +269,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) gather_qmv_kernel(
     qmv_rows_direct<BITS>(x + (long long)src * K, w + (long long)e * w_expert_stride,
                           scales + (long long)e * sb_expert_stride,
                           biases + (long long)e * sb_expert_stride, y + (long long)r * N, K, N,
-                          row0);
+                          group, row0);
 }
 
 
@@ -463,8 +465,8 @@ template <int BITS, int RPW>
 __global__ void __launch_bounds__((kMaxStreamWarps + 2) * 32, 1)
     qmv_stream_kernel(const __nv_bfloat16* __restrict__ x, const uint32_t* __restrict__ w,
                       const uint16_t* __restrict__ scales, const uint16_t* __restrict__ biases,
-                      __nv_bfloat16* __restrict__ y, int K, int N, const StreamShape sh,
-                      int32_t* status) {
+                      __nv_bfloat16* __restrict__ y, int K, int N, int group,
+                      const StreamShape sh, int32_t* status) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ uint64_t full[kStreamStages], empty[kStreamStages], xfull;
     // per-chunk partial sums of each (row, K segment), handed to the reducer
@@ -476,7 +478,7 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 2) * 32, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = lane_id();
     const uint32_t base = smem_u32(smem);
-    const int groups = K / 64;
+    const int groups = K / group;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStreamStages; ++i) {
@@ -588,7 +590,7 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 2) * 32, 1)
         // 2^(emax - 149): a normal float from emax = 23 on, else subnormal
         xscale = __int_as_float(emax >= 23 ? (emax - 22) << 23 : 1 << emax);
     }
-    const int g = k0 / 64;
+    const int g = k0 / group;
     const uint32_t lane_code_off = (uint32_t)(seg * 1024 + lane * 32) * BITS / 8;
 
     const ChunkRows cr{N / sh.nchunks, N % sh.nchunks};
@@ -651,7 +653,7 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 2) * 32, 1)
 
 template <int BITS>
 cudaError_t launch_stream(const __nv_bfloat16* x, const uint32_t* w, const uint16_t* s,
-                          const uint16_t* b, __nv_bfloat16* y, int K, int N, int rpw,
+                          const uint16_t* b, __nv_bfloat16* y, int K, int N, int group, int rpw,
                           const StreamShape& sh, int grid, int32_t* status, cudaStream_t stream) {
     const int smem = sh.x_offset + K * 2;
     cudaLaunchConfig_t cfg = {};
@@ -669,7 +671,8 @@ cudaError_t launch_stream(const __nv_bfloat16* x, const uint32_t* w, const uint1
         cudaError_t e = cudaFuncSetAttribute(qmv_stream_kernel<BITS, R>,                        \
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem); \
         if (e != cudaSuccess) return e;                                                         \
-        e = cudaLaunchKernelEx(&cfg, qmv_stream_kernel<BITS, R>, x, w, s, b, y, K, N, sh, status); \
+        e = cudaLaunchKernelEx(&cfg, qmv_stream_kernel<BITS, R>, x, w, s, b, y, K, N, group, sh, \
+                               status);                                                         \
         if (e != cudaSuccess) return e;                                                         \
         break;                                                                                  \
     }
@@ -689,7 +692,7 @@ cudaError_t launch_stream(const __nv_bfloat16* x, const uint32_t* w, const uint1
 cudaError_t launch_gather_qmv(const void* x, const uint32_t* w, const void* scales,
                               const void* biases, const int32_t* expert_ids,
                               const int32_t* row_src, void* y, int T, int B, int E, int K, int N,
-                              int bits, int32_t* status, cudaStream_t stream) {
+                              int bits, int group, int32_t* status, cudaStream_t stream) {
     const int seg_k = bits == 4 ? 1024 : 512;
     const int nseg_g = (K + seg_k - 1) / seg_k;
     const int passes = (nseg_g + kMaxWarps - 1) / kMaxWarps;
@@ -701,18 +704,18 @@ cudaError_t launch_gather_qmv(const void* x, const uint32_t* w, const void* scal
     const auto* bb = static_cast<const uint16_t*>(biases);
     auto* yb = static_cast<__nv_bfloat16*>(y);
     const long long wst = (long long)N * K * bits / 32;
-    const long long sbst = (long long)N * (K / 64);
+    const long long sbst = (long long)N * (K / group);
     if (bits == 4)
         gather_qmv_kernel<4><<<grid, block, 0, stream>>>(xb, w, sb, bb, expert_ids, row_src, yb, T,
-                                                        B, E, K, N, wst, sbst, status);
+                                                        B, E, K, N, group, wst, sbst, status);
     else
         gather_qmv_kernel<8><<<grid, block, 0, stream>>>(xb, w, sb, bb, expert_ids, row_src, yb, T,
-                                                        B, E, K, N, wst, sbst, status);
+                                                        B, E, K, N, group, wst, sbst, status);
     return cudaGetLastError();
 }
 
 cudaError_t launch_qmv(const void* x, const uint32_t* w, const void* scales, const void* biases,
-                       void* y, int K, int N, int bits, int sms, int32_t* status,
+                       void* y, int K, int N, int bits, int group, int sms, int32_t* status,
                        cudaStream_t stream) {
     const auto* xb = static_cast<const __nv_bfloat16*>(x);
     const auto* sb = static_cast<const uint16_t*>(scales);
@@ -721,14 +724,17 @@ cudaError_t launch_qmv(const void* x, const uint32_t* w, const void* scales, con
     const bool sb_aligned = (reinterpret_cast<uintptr_t>(scales) % 16 == 0) &&
                             (reinterpret_cast<uintptr_t>(biases) % 16 == 0);
     const int nseg = (K + 1023) / 1024;
-    if (K % 512 == 0 && nseg <= kMaxStreamWarps && sb_aligned) {
+    // a chunk's scales (and biases) are one bulk copy: a row's pairs must
+    // fill whole 16-byte units
+    const bool sb_rows16 = (K / group) % 8 == 0;
+    if (K % 512 == 0 && nseg <= kMaxStreamWarps && sb_aligned && sb_rows16) {
         StreamShape sh;
         sh.nseg = nseg;
         sh.phases = kTargetWarps / nseg > 1 ? kTargetWarps / nseg : 1;
         if (sh.phases * nseg > kMaxStreamWarps) sh.phases = kMaxStreamWarps / nseg;
         sh.warps = sh.phases * nseg;
         sh.row_bytes = K * bits / 8;
-        sh.sb_bytes = (K / 64) * 2;
+        sh.sb_bytes = (K / group) * 2;
         int rpw = kChunkBytes / (sh.row_bytes * sh.phases);
         rpw = rpw >= 8 ? 8 : rpw >= 4 ? 4 : rpw >= 2 ? 2 : 1;
         sh.rows = sh.phases * rpw;
@@ -744,8 +750,9 @@ cudaError_t launch_qmv(const void* x, const uint32_t* w, const void* scales, con
         const int grid = sh.nchunks < sms ? sh.nchunks : sms;
         sh.nchunks = (sh.nchunks + grid - 1) / grid * grid;
         if (sh.nchunks > N) sh.nchunks = N;
-        return bits == 4 ? launch_stream<4>(xb, w, sb, bb, yb, K, N, rpw, sh, grid, status, stream)
-                         : launch_stream<8>(xb, w, sb, bb, yb, K, N, rpw, sh, grid, status, stream);
+        return bits == 4
+                   ? launch_stream<4>(xb, w, sb, bb, yb, K, N, group, rpw, sh, grid, status, stream)
+                   : launch_stream<8>(xb, w, sb, bb, yb, K, N, group, rpw, sh, grid, status, stream);
     }
     const int seg_k = bits == 4 ? 1024 : 512;
     const int nseg_g = (K + seg_k - 1) / seg_k;
@@ -755,9 +762,9 @@ cudaError_t launch_qmv(const void* x, const uint32_t* w, const void* scales, con
     const dim3 grid((N + kRows - 1) / kRows);
     const dim3 block(32 * warps);
     if (bits == 4)
-        qmv_generic_kernel<4><<<grid, block, 0, stream>>>(xb, w, sb, bb, yb, K, N);
+        qmv_generic_kernel<4><<<grid, block, 0, stream>>>(xb, w, sb, bb, yb, K, N, group);
     else
-        qmv_generic_kernel<8><<<grid, block, 0, stream>>>(xb, w, sb, bb, yb, K, N);
+        qmv_generic_kernel<8><<<grid, block, 0, stream>>>(xb, w, sb, bb, yb, K, N, group);
     return cudaGetLastError();
 }
 

@@ -1,8 +1,9 @@
 // Affine group-wise encoder: float weights -> packed codes, bf16 scales and
 // biases (the stored format of mlxcel issue #1536, Baseline section: "affine
-// 4-bit / group 64"; 8-bit codes are unsigned bytes).
+// 4-bit / group 64"; 8-bit codes are unsigned bytes; groups of 32 and 128
+// consecutive k use the same rule).
 //
-// Per (row n, group g of 64 consecutive k): mn, mx = the group's minimum and
+// Per (row n, group g of GROUP consecutive k): mn, mx = the group's minimum and
 // maximum (-0 read as +0); s = bf16(RN(RN(mx - mn) / (2^bits - 1))) and
 // b = bf16(mn), both rounded to nearest even; then every code is
 // q = clamp(rint(RN(RN(w - b) / s)), 0, 2^bits - 1) against the stored bf16 s
@@ -11,8 +12,9 @@
 // bit wherever the same rule is evaluated in binary32.
 //
 // One warp per row: each lane holds 8 consecutive values of a 256-wide block
-// (two 16-byte loads), eight lanes make a group, so a group's minimum and
-// maximum take three shuffle steps and each lane packs its own code word(s).
+// (two 16-byte loads), GROUP / 8 lanes make a group (4, 8 or 16), so a
+// group's minimum and maximum take two to four shuffle steps and each lane
+// packs its own code word(s).
 // HBM-bound: 4 bytes read per weight, bits/8 written.
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -25,18 +27,19 @@ namespace {
 
 constexpr int kEncWarps = 8;  // rows per CTA
 
-template <int BITS>
+template <int BITS, int GROUP>
 __global__ void __launch_bounds__(kEncWarps * 32) quantize_kernel(const float* __restrict__ W,
                                                                  uint32_t* __restrict__ codes,
                                                                  uint16_t* __restrict__ scales,
                                                                  uint16_t* __restrict__ biases,
                                                                  int N, int K) {
     constexpr int kLevels = (1 << BITS) - 1;
+    constexpr int kGroupLanes = GROUP / 8;
     const int lane = threadIdx.x & 31;
     const int n = blockIdx.x * kEncWarps + (threadIdx.x >> 5);
     if (n >= N) return;  // the whole warp
     const float* row = W + (long long)n * K;
-    const int groups = K / 64;
+    const int groups = K / GROUP;
     // four 256-wide blocks per round: all their loads are issued before any
     // arithmetic, so each lane keeps 128 bytes in flight
     constexpr int kBlocks = 4;
@@ -57,7 +60,7 @@ __global__ void __launch_bounds__(kEncWarps * 32) quantize_kernel(const float* _
             const int k0 = kb + u * 256;
             if (k0 >= K) break;  // warp-uniform
             const int k = k0 + lane * 8;
-            const bool active = k < K;  // K % 64 == 0: whole 8-lane groups drop out
+            const bool active = k < K;  // K % GROUP == 0: whole groups of lanes drop out
             float mn = __int_as_float(0x7f800000), mx = -__int_as_float(0x7f800000);
             if (active) {
 #pragma unroll
@@ -68,7 +71,7 @@ __global__ void __launch_bounds__(kEncWarps * 32) quantize_kernel(const float* _
                 }
             }
 #pragma unroll
-            for (int off = 1; off < 8; off <<= 1) {
+            for (int off = 1; off < kGroupLanes; off <<= 1) {
                 mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
             }
@@ -96,8 +99,8 @@ __global__ void __launch_bounds__(kEncWarps * 32) quantize_kernel(const float* _
                 words.y = q[4] | (q[5] << 8) | (q[6] << 16) | (q[7] << 24);
                 *reinterpret_cast<uint2*>(codes + (long long)n * (K / 4) + k / 4) = words;
             }
-            if ((lane & 7) == 0) {
-                const long long gi = (long long)n * groups + k / 64;
+            if ((lane & (kGroupLanes - 1)) == 0) {
+                const long long gi = (long long)n * groups + k / GROUP;
                 scales[gi] = __bfloat16_as_ushort(sb);
                 biases[gi] = __bfloat16_as_ushort(bb);
             }
@@ -108,15 +111,25 @@ __global__ void __launch_bounds__(kEncWarps * 32) quantize_kernel(const float* _
 }  // namespace
 
 cudaError_t launch_quantize(const float* W, uint32_t* codes, void* scales, void* biases, int N,
-                            int K, int bits, cudaStream_t stream) {
+                            int K, int bits, int group, cudaStream_t stream) {
     const dim3 grid((N + kEncWarps - 1) / kEncWarps);
     const dim3 block(kEncWarps * 32);
     auto* s = static_cast<uint16_t*>(scales);
     auto* b = static_cast<uint16_t*>(biases);
-    if (bits == 4)
-        quantize_kernel<4><<<grid, block, 0, stream>>>(W, codes, s, b, N, K);
-    else
-        quantize_kernel<8><<<grid, block, 0, stream>>>(W, codes, s, b, N, K);
+#define MXQ_ENC_CASE(G)                                                                \
+    case G:                                                                            \
+        if (bits == 4)                                                                 \
+            quantize_kernel<4, G><<<grid, block, 0, stream>>>(W, codes, s, b, N, K);   \
+        else                                                                           \
+            quantize_kernel<8, G><<<grid, block, 0, stream>>>(W, codes, s, b, N, K);   \
+        break;
+    switch (group) {
+        MXQ_ENC_CASE(32)
+        MXQ_ENC_CASE(64)
+        MXQ_ENC_CASE(128)
+        default: return cudaErrorInvalidValue;
+    }
+#undef MXQ_ENC_CASE
     return cudaGetLastError();
 }
 

@@ -45,12 +45,12 @@ WORKLOAD = ("qmv decode M=1: K=5120 N=17408 and K=17408 N=5120, 4-bit and 8-bit,
             "bf16 scales/biases")
 
 
-def qmv_bytes(K, N, bits):
-    return N * K * bits // 8 + N * (K // 64) * 4 + K * 2 + N * 2
+def qmv_bytes(K, N, bits, group=64):
+    return N * K * bits // 8 + N * (K // group) * 4 + K * 2 + N * 2
 
 
-def qmm_bytes(M, K, N, bits):
-    return N * K * bits // 8 + N * (K // 64) * 4 + M * K * 2 + M * N * 2
+def qmm_bytes(M, K, N, bits, group=64):
+    return N * K * bits // 8 + N * (K // group) * 4 + M * K * 2 + M * N * 2
 
 
 def load_peaks():
@@ -201,11 +201,11 @@ def dev_codes(a, dev):
 
 
 class DenseInputs:
-    def __init__(self, W, M, K, N, bits, dev, copies, x_seed=1):
+    def __init__(self, W, M, K, N, bits, dev, copies, x_seed=1, group=64):
         import torch
 
-        qw = synth.quantize(W, bits)
-        self.M, self.K, self.N, self.bits = M, K, N, bits
+        qw = synth.quantize(W, bits, group)
+        self.M, self.K, self.N, self.bits, self.group = M, K, N, bits, group
         self.host = (qw.w, qw.scales, qw.biases)
         self.x_host = synth.activations(M, K, seed=x_seed)
         w, s, b = dev_codes(qw.w, dev), dev_bf16(qw.scales, dev), dev_bf16(qw.biases, dev)
@@ -437,24 +437,26 @@ def secondary_measurements(mxq, dev, stream, hbm, bf16_peak, Ws):
     out = []
     iters = 40
 
-    def dense_entry(name, M, K, N, bits, W, copies):
-        d = DenseInputs(W, M, K, N, bits, dev, copies=copies)
+    def dense_entry(name, M, K, N, bits, W, copies, group=64):
+        d = DenseInputs(W, M, K, N, bits, dev, copies=copies, group=group)
         if M == 1:
-            fn = lambda i: mxq.qmv(d.x[0], *d.copies[i % copies], bits, out=d.y[0])  # noqa: E731
+            fn = lambda i: mxq.qmv(d.x[0], *d.copies[i % copies], bits, out=d.y[0],  # noqa: E731
+                                   group_size=group)
             kern = "qmv_stream_kernel"
         else:
-            fn = lambda i: mxq.qmm(d.x, *d.copies[i % copies], bits, out=d.y)  # noqa: E731
+            fn = lambda i: mxq.qmm(d.x, *d.copies[i % copies], bits, out=d.y,  # noqa: E731
+                                   group_size=group)
             kern = "qmm_tc_kernel or qmm_persistent_kernel"
         for i in range(5):
             fn(i)
         t, _ = time_launches(fn, iters, stream)
         flops = 2.0 * M * K * N
-        nbytes = qmm_bytes(M, K, N, bits)
+        nbytes = qmm_bytes(M, K, N, bits, group)
         t_star = max(nbytes / (hbm * 1e9), flops / (bf16_peak * 1e12))
         bound = "hbm" if nbytes / (hbm * 1e9) >= flops / (bf16_peak * 1e12) else "tensor"
         del d
         return {"name": name, "kernel": kern, "M": M, "K": K, "N": N, "bits": bits,
-                "us": t * 1e6, "TFLOPS": flops / t / 1e12, "GB_s": nbytes / t / 1e9,
+                "group": group, "us": t * 1e6, "TFLOPS": flops / t / 1e12, "GB_s": nbytes / t / 1e9,
                 "frac_tensor": flops / t / 1e12 / bf16_peak, "frac_hbm": nbytes / t / 1e9 / hbm,
                 "bound": bound, "frac_roofline": t_star / t, "tokens_per_s": M / t}
 
@@ -468,6 +470,11 @@ def secondary_measurements(mxq, dev, stream, hbm, bf16_peak, Ws):
     out.append(dense_entry("pair qmv 8-bit", 1, 5120, 5120, 8, W_sq, copies=6))
     out.append(dense_entry("pair qmv 4-bit", 1, 5120, 5120, 4, W_sq, copies=6))
     out.append(dense_entry("pair qmm 8-bit", 128, 5120, 5120, 8, W_sq, copies=6))
+    # group sizes 32 and 128 on the decode and prefill shapes (same weights)
+    for group in (32, 128):
+        out.append(dense_entry("group qmv", 1, 5120, 17408, 4, W_big, copies=6, group=group))
+        out.append(dense_entry("group qmm prefill", 600, 5120, 17408, 4, W_big, copies=3,
+                               group=group))
 
     # the encoder on the prefill weight shape (float32 in, 4-bit codes out)
     N_q, K_q = 17408, 5120

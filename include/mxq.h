@@ -6,8 +6,13 @@
  * section: 8-bit codes are unsigned bytes, and the product accumulates in
  * float at every width):
  *
- *   w^[n, k] = s[n, k/64] * q[n, k] + b[n, k/64]
+ *   w^[n, k] = s[n, k/G] * q[n, k] + b[n, k/G]
  *   y[m, n]  = sum_k x[m, k] * w^[n, k]          (fp32 accumulation)
+ *
+ * G = group_size, the k values that share one scale/bias pair: 64 (the
+ * stored format named above), 32 or 128 (issue #1536, Diagnosis item 4: the
+ * tile choice there tests group_size <= 64, so the format also comes with
+ * other group sizes; 32 and 128 are the sizes on either side of 64).
  *
  * Storage, all row-major and contiguous:
  *   x       bf16   [M, K]            activations
@@ -17,8 +22,8 @@
  *                                    qmm_naive kernel name in issue #1536's
  *                                    profile table).  8-bit: four codes per
  *                                    word, lowest k in the lowest byte.
- *   scales  bf16   [N, K/64]         s per (output row, group of 64 k)
- *   biases  bf16   [N, K/64]         b per (output row, group of 64 k)
+ *   scales  bf16   [N, K/G]          s per (output row, group of G k)
+ *   biases  bf16   [N, K/G]          b per (output row, group of G k)
  *   y       bf16   [M, N]            output, rounded once from fp32 (RNE)
  *
  * All pointers except `stream` are DEVICE pointers owned by the caller; the
@@ -65,10 +70,11 @@ typedef enum {
  * fp32 accumulation at every width is the fix that item names).
  *   x: bf16 [K]; y: bf16 [N]; w, scales, biases as above.
  *   dev_status: device int32 or NULL; receives 0 or MXQ_DEV_TIMEOUT.
- * Requirements: bits in {4, 8}; group_size == 64; K > 0 and K % 64 == 0;
- * N > 0; x, w, y 16-byte aligned; scales, biases 2-byte aligned.  The
- * streaming kernel is used when K % 512 == 0, K <= 20480 and scales/biases
- * are 16-byte aligned; other shapes take a direct-load kernel (same result
+ * Requirements: bits in {4, 8}; group_size in {32, 64, 128}; K > 0,
+ * K % 64 == 0 and K % group_size == 0; N > 0; x, w, y 16-byte aligned;
+ * scales, biases 2-byte aligned.  The streaming kernel is used when
+ * K % 512 == 0, K <= 20480, K / group_size % 8 == 0 and scales/biases are
+ * 16-byte aligned; other shapes take a direct-load kernel (same result
  * rule, different summation order).  The streaming kernel is launched as a
  * programmatic dependent launch: its CTAs may be placed on SMs while the
  * kernel before it on the stream finishes, but they read and write nothing
@@ -96,7 +102,7 @@ mxq_status mxq_qmm(const void* x, const uint32_t* w, const void* scales, const v
  * sorted-MoE prefill path that routes a quantized GatherQMM into a grouped
  * GEMM, B = tokens * top_k rows sorted by expert).
  *   x:          bf16 [T, K]  activation rows
- *   w:          uint32 [E, N, K*bits/32]; scales, biases: bf16 [E, N, K/64]
+ *   w:          uint32 [E, N, K*bits/32]; scales, biases: bf16 [E, N, K/G]
  *   expert_ids: int32 [B], non-decreasing: expert of sorted row r
  *   row_src:    int32 [B], row of x that feeds sorted row r; NULL means r
  *               (then T must equal B)
@@ -115,8 +121,9 @@ mxq_status mxq_qmm(const void* x, const uint32_t* w, const void* scales, const v
  * Calls with at most 32 rows (a decode step) run one GEMV per row against
  * its expert's matrix (the same result rule, another summation order) and
  * use no workspace memory, though the size check still applies.
- * Requirements: B, E, T, N > 0; K > 0, K % 64 == 0; bits in {4, 8};
- * group_size == 64; x, w, y 16-byte aligned; the rest aligned to type.       */
+ * Requirements: B, E, T, N > 0; K > 0, K % 64 == 0, K % group_size == 0;
+ * bits in {4, 8}; group_size in {32, 64, 128}; x, w, y 16-byte aligned; the
+ * rest aligned to type.                                                      */
 mxq_status mxq_gather_qmm(const void* x, const uint32_t* w, const void* scales,
                           const void* biases, const int32_t* expert_ids,
                           const int32_t* row_src, void* y, int T, int B, int E, int K, int N,
@@ -168,13 +175,14 @@ mxq_status mxq_gather_qmm_noalloc(const void* x, const uint32_t* w, const void* 
  * bias = group minimum, scale = group range / (2^bits - 1)).
  *   w:      float [N, K] row-major (finite), 16-byte aligned
  *   codes:  uint32 [N, K*bits/32], 16-byte aligned (output)
- *   scales, biases: bf16 [N, K/64] (output)
- * Per (row, group of 64): mn, mx = min, max (-0 read as +0);
+ *   scales, biases: bf16 [N, K/G] (output)
+ * Per (row, group of G = group_size): mn, mx = min, max (-0 read as +0);
  * s = bf16(RN(RN(mx - mn) / (2^bits - 1))), b = bf16(mn), rounded to nearest
  * even; q = clamp(rint(RN(RN(w - b) / s)), 0, 2^bits - 1) with the stored
  * bf16 s and b, q = 0 when s == 0.  All decisions in binary32, so the codes
  * are reproducible bit for bit.  Requirements: bits in {4, 8};
- * group_size == 64; K > 0, K % 64 == 0; N > 0.                              */
+ * group_size in {32, 64, 128}; K > 0, K % 64 == 0, K % group_size == 0;
+ * N > 0.                                                                    */
 mxq_status mxq_quantize(const float* w, uint32_t* codes, void* scales, void* biases, int N,
                         int K, int bits, int group_size, void* stream);
 

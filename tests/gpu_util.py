@@ -62,9 +62,9 @@ def assert_close(y_gpu, y_ref, bound, what=""):
 class DenseCase:
     """Quantized dense weight + activations on host and device."""
 
-    def __init__(self, M, K, N, bits, seed=0, x_seed=1):
-        self.M, self.K, self.N, self.bits = M, K, N, bits
-        self.qw = synth.quantize(synth.dense_weights(N, K, seed=seed), bits)
+    def __init__(self, M, K, N, bits, seed=0, x_seed=1, group=64):
+        self.M, self.K, self.N, self.bits, self.group = M, K, N, bits, group
+        self.qw = synth.quantize(synth.dense_weights(N, K, seed=seed), bits, group)
         self.x = synth.activations(M, K, seed=x_seed)
         self.w_d = codes_dev(self.qw.w)
         self.s_d = bf16_dev(self.qw.scales)
@@ -76,8 +76,8 @@ class MoECase:
     """Sorted-MoE routing + per-expert quantized weights."""
 
     def __init__(self, T, E, top_k, K, N, bits, seed=0, identity_src=False, routing_seed=2,
-                 x_seed=1):
-        self.E, self.K, self.N, self.bits = E, K, N, bits
+                 x_seed=1, group=64):
+        self.E, self.K, self.N, self.bits, self.group = E, K, N, bits, group
         ids, src = synth.routing(T, E, top_k, seed=routing_seed)
         self.B = ids.shape[0]
         self.ids = ids
@@ -89,7 +89,7 @@ class MoECase:
             self.T = T
         ws, ss, bs = [], [], []
         for e in range(E):
-            q = synth.quantize(synth.dense_weights(N, K, seed=seed * 100003 + e), bits)
+            q = synth.quantize(synth.dense_weights(N, K, seed=seed * 100003 + e), bits, group)
             ws.append(q.w)
             ss.append(q.scales)
             bs.append(q.biases)

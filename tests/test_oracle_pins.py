@@ -227,14 +227,14 @@ def _bf16_fraction(h):
     return Fraction(struct.unpack("<f", struct.pack("<I", int(h) << 16))[0])
 
 
-def _brute(x, w, s, b, M, K, N, bits):
+def _brute(x, w, s, b, M, K, N, bits, group=64):
     y = [[Fraction(0)] * N for _ in range(M)]
     per = 32 // bits
     for n in range(N):
         codes = []
         for j in range(K // per):
             codes += _hex_unpack(int(w[n, j]), bits)
-        wrow = [_bf16_fraction(s[n, k // 64]) * codes[k] + _bf16_fraction(b[n, k // 64])
+        wrow = [_bf16_fraction(s[n, k // group]) * codes[k] + _bf16_fraction(b[n, k // group])
                 for k in range(K)]
         for m in range(M):
             y[m][n] = sum((_bf16_fraction(x[m, k]) * wrow[k] for k in range(K)), Fraction(0))
@@ -426,15 +426,17 @@ def test_quantize_flat_group_and_signed_zero():
     assert b[0, 1] == 0 and b[1, 0] == 0 and b[1, 1] == 0   # -0 is read as +0
 
 
+@pytest.mark.parametrize("group", [32, 64, 128])
 @pytest.mark.parametrize("bits", [4, 8])
-def test_quantize_round_trip_bound(bits):
+def test_quantize_round_trip_bound(bits, group):
     rng = np.random.default_rng(31 + bits)
     W = (rng.standard_normal((48, 1024)) * 0.02).astype(np.float32)
-    codes, s, b = oracle.quantize(W, bits)
-    w_hat = oracle.dequant(codes, s, b, 48, 1024, bits)
-    s_f = np.repeat(synth.bf16_bits_to_f32(s).astype(np.float64), 64, axis=1)
-    Wg = W.reshape(48, 16, 64).astype(np.float64)
-    mag = np.repeat(np.abs(Wg).max(axis=2), 64, axis=1)
+    codes, s, b = oracle.quantize(W, bits, group)
+    assert s.shape == (48, 1024 // group)
+    w_hat = oracle.dequant(codes, s, b, 48, 1024, bits, group)
+    s_f = np.repeat(synth.bf16_bits_to_f32(s).astype(np.float64), group, axis=1)
+    Wg = W.reshape(48, 1024 // group, group).astype(np.float64)
+    mag = np.repeat(np.abs(Wg).max(axis=2), group, axis=1)
     # half a step; the stored scale is the exact step rounded to bf16 (relative
     # error <= 2^-9), so the top of the range can sit up to levels * 2^-9
     # steps past the last code; plus the bf16 rounding of the bias (the group
@@ -442,18 +444,129 @@ def test_quantize_round_trip_bound(bits):
     levels = (1 << bits) - 1
     assert np.all(np.abs(W - w_hat) <= (0.5 + levels * 2.0 ** -9) * s_f + 2.0 ** -8 * mag + 1e-12)
     # and within plain half a step away from the clamped ends
-    inner = (W > np.repeat(Wg.min(axis=2), 64, axis=1) + 2 * s_f) & \
-            (W < np.repeat(Wg.max(axis=2), 64, axis=1) - 2 * s_f)
+    inner = (W > np.repeat(Wg.min(axis=2), group, axis=1) + 2 * s_f) & \
+            (W < np.repeat(Wg.max(axis=2), group, axis=1) - 2 * s_f)
     assert np.all(np.abs(W - w_hat)[inner] <= 0.5 * s_f[inner] * (1 + 1e-6) + 1e-12)
 
 
+@pytest.mark.parametrize("group", [32, 64, 128])
 @pytest.mark.parametrize("bits", [4, 8])
-def test_quantize_agrees_with_float64_encoder(bits):
+def test_quantize_agrees_with_float64_encoder(bits, group):
     # synth.quantize takes the same decisions in float64 (numpy): away from
     # exact ties the two encoders must agree on every code, scale and bias
     rng = np.random.default_rng(41 + bits)
     W = (rng.standard_normal((96, 2048)) * 0.02).astype(np.float32)
-    codes, s, b = oracle.quantize(W, bits)
-    qw = synth.quantize(W, bits)
+    codes, s, b = oracle.quantize(W, bits, group)
+    qw = synth.quantize(W, bits, group)
     assert np.array_equal(s, qw.scales) and np.array_equal(b, qw.biases)
     assert np.array_equal(codes, qw.w)
+
+
+# ---- group sizes 32 and 128 (issue #1536, Diagnosis item 4: the group size
+# is a parameter of the stored format; 32 and 128 sit on either side of 64)
+
+
+def _group_sb(N, ng):
+    """Exact, pairwise distinct scale and bias per (row, group)."""
+    g = np.arange(ng)[None, :]
+    n = np.arange(N)[:, None]
+    s_vals = (2.0 ** ((n + g) % 7 - 4)).astype(np.float32)
+    b_vals = ((g + 1) * 0.125 * np.where(n % 2 == 0, 1.0, -1.0) + n).astype(np.float32)
+    return s_vals, b_vals
+
+
+@pytest.mark.parametrize("group", [32, 128])
+@pytest.mark.parametrize("bits", [4, 8])
+def test_one_hot_x_selects_weight_group_sizes(bits, group):
+    # x = e_k picks out w^[n, k] = s[n, k/G] q + b[n, k/G]: a k charged to
+    # the neighbouring group reads another (s, b) pair
+    rng = np.random.default_rng(60 + bits + group)
+    N, K = 3, 384
+    ng = K // group
+    q = rng.integers(0, 1 << bits, size=(N, K), dtype=np.uint8)
+    w = synth.pack_codes(q, bits)
+    s_vals, b_vals = _group_sb(N, ng)
+    s, b = _bf16_exact(s_vals), _bf16_exact(b_vals)
+    for k in sorted({0, 1, group - 1, group, group + 1, 2 * group - 1, 2 * group, K - 1}):
+        x = np.zeros((1, K), dtype=np.float32)
+        x[0, k] = 1.0
+        y, _ = oracle.qmm(_bf16_exact(x), w, s, b, 1, K, N, bits, group)
+        g = k // group
+        want = s_vals[:, g].astype(np.float64) * q[:, k] + b_vals[:, g]
+        assert np.array_equal(y[0], want), k
+
+
+@pytest.mark.parametrize("group", [32, 128])
+def test_alternating_group_scales_pin_group_boundary_sizes(group):
+    # Group g has s = 2^g, b = -g; with x = 1 and q = 1 the sum is
+    # G * sum_g (2^g - g); moving one unit of code from k = G-1 to k = G
+    # changes it by s_1 - s_0 = 1, and by a different amount if either k
+    # sits in the wrong group.
+    K, N, bits = 512, 2, 4
+    ng = K // group
+    q = np.ones((N, K), dtype=np.uint8)
+    s = _bf16_exact(np.tile([2.0 ** g for g in range(ng)], (N, 1)))
+    b = _bf16_exact(np.tile([-float(g) for g in range(ng)], (N, 1)))
+    x = _bf16_exact(np.ones((1, K), np.float32))
+    y, _ = oracle.qmm(x, synth.pack_codes(q, bits), s, b, 1, K, N, bits, group)
+    assert np.all(y == group * sum(2.0 ** g - g for g in range(ng)))
+    q2 = q.copy()
+    q2[:, group - 1] = 0
+    q2[:, group] = 2
+    y2, _ = oracle.qmm(x, synth.pack_codes(q2, bits), s, b, 1, K, N, bits, group)
+    assert np.all(y2 - y == 1.0)
+
+
+@pytest.mark.parametrize("group", [32, 128])
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("M,N,K", [(1, 2, 128), (2, 3, 256)])
+def test_brute_force_exact_group_sizes(bits, group, M, N, K):
+    seed = 7 * group + 100 * bits + 10 * M + N + K
+    W = synth.dense_weights(N, K, seed=seed)
+    qw = synth.quantize(W, bits, group)
+    x = synth.activations(M, K, seed=seed + 1)
+    y, bnd = oracle.qmm(x, qw.w, qw.scales, qw.biases, M, K, N, bits, group)
+    exact = _brute(x, qw.w, qw.scales, qw.biases, M, K, N, bits, group)
+    for m in range(M):
+        for n in range(N):
+            assert abs(y[m, n] - float(exact[m][n])) <= 1e-12 * bnd[m, n] + 1e-300, (m, n)
+
+
+@pytest.mark.parametrize("group", [32, 128])
+def test_gather_group_sizes_constant_per_expert(group):
+    # s = 0, b = c_{e,n} per group: y[r, n] = c_{e(r),n} * sum_k x[src(r), k]
+    # exactly, whatever the group size, and the group count per row is K/G
+    E, N, K, T = 3, 4, 256, 5
+    ng = K // group
+    rng = np.random.default_rng(70 + group)
+    x = rng.integers(-4, 5, size=(T, K)).astype(np.float32)
+    c = ((np.arange(E)[:, None] + 1) / 4.0 + np.arange(N)[None, :] / 64.0).astype(np.float32)
+    w = np.zeros((E, N, K // 8), np.uint32)
+    s = _bf16_exact(np.zeros((E, N, ng), np.float32))
+    b = _bf16_exact(np.repeat(c[:, :, None], ng, axis=2))
+    ids = np.array([0, 0, 1, 2, 2, 2], np.int32)
+    src = np.array([4, 1, 0, 3, 2, 0], np.int32)
+    y, _ = oracle.gather_qmm(_bf16_exact(x), w, s, b, ids, src, T, 6, E, K, N, 4, group)
+    want = x.sum(axis=1, dtype=np.float64)[src][:, None] * c[ids].astype(np.float64)
+    assert np.array_equal(y, want)
+
+
+@pytest.mark.parametrize("group", [32, 128])
+def test_quantize_hand_example_group_sizes(group):
+    # the exact grid -1 + 0.25 * (j % 16) repeats inside every group of 32
+    # or 128, so every group stores s = 0.25, b = -1 and codes j % 16
+    K = 256
+    j = np.arange(K)
+    W = (-1.0 + 0.25 * (j % 16)).astype(np.float32)[None, :]
+    codes, s, b = oracle.quantize(W, 4, group)
+    assert s.shape == (1, K // group)
+    assert np.all(s == synth.f32_to_bf16_bits(np.float32(0.25)))
+    assert np.all(b == 0xBF80)
+    assert np.array_equal(oracle.unpack(codes, 1, K, 4)[0], j % 16)
+    # a single group's range change moves only that group's pair
+    W2 = W.copy()
+    W2[0, group + 3] = 5.0
+    _, s2, b2 = oracle.quantize(W2, 4, group)
+    changed = np.nonzero(s2[0] != s[0])[0]
+    assert list(changed) == [1]
+    assert np.array_equal(b2, b)
