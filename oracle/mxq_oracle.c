@@ -17,7 +17,12 @@
  *
  * Packing: 4-bit codes eight per little-endian uint32, the lowest k in the
  * lowest nibble; 8-bit codes ("unsigned char weights", issue #1538, 4-bit vs
- * 8-bit section) four per uint32, the lowest k in the lowest byte.
+ * 8-bit section) four per uint32, the lowest k in the lowest byte.  Both are
+ * one little-endian bit stream per row: code k holds bits [k*b, k*b + b) of
+ * the row, word j bits [32j, 32j + 32).  The other widths (2, 3 and 6 bits;
+ * the bit width is a parameter of the kernels in issue #1536, Diagnosis
+ * item 3) are read with the same rule, so a 3- or 6-bit code may start in
+ * one word and end in the next.
  *
  * The sorted-MoE variant (PR #1562, Summary: rows sorted by expert, B =
  * tokens * top_k) uses for sorted row r the expert e(r) and activation row
@@ -44,13 +49,16 @@ static double bf16_to_f64(uint16_t h) {
     return (double)f;
 }
 
-/* Code of weight (n, k): row n has K*bits/32 words. */
+/* Code of weight (n, k): row n has K*bits/32 words; the code's bits start
+ * at bit k*bits of the row and may continue into the next word. */
 static unsigned code_at(const uint32_t* w, long long words_per_row, int n, int k, int bits) {
-    int per_word = 32 / bits;
-    uint32_t word = w[(long long)n * words_per_row + k / per_word];
-    int slot = k % per_word;
-    uint32_t mask = (bits == 32) ? 0xFFFFFFFFu : ((1u << bits) - 1u);
-    return (unsigned)((word >> (slot * bits)) & mask);
+    const uint32_t* row = w + (long long)n * words_per_row;
+    long long first = (long long)k * bits;       /* bit index of the code's lowest bit */
+    long long j = first / 32;
+    int off = (int)(first % 32);
+    uint64_t v = row[j] >> off;
+    if (off + bits > 32) v |= (uint64_t)row[j + 1] << (32 - off);
+    return (unsigned)(v & ((1u << bits) - 1u));
 }
 
 int oracle_threads(void) {
@@ -251,9 +259,8 @@ static float bf16_to_f32(uint16_t h) {
 void oracle_quantize(const float* W, int N, int K, int bits, int group, uint32_t* codes,
                      uint16_t* scales, uint16_t* biases) {
     const int levels = (1 << bits) - 1;
-    const int per_word = 32 / bits;
     const int groups = K / group;
-    const long long words_per_row = (long long)K / per_word;
+    const long long words_per_row = (long long)K * bits / 32;
 #pragma omp parallel for schedule(static)
     for (int n = 0; n < N; ++n) {
         for (long long i = 0; i < words_per_row; ++i) codes[(long long)n * words_per_row + i] = 0;
@@ -282,8 +289,12 @@ void oracle_quantize(const float* W, int N, int K, int bits, int group, uint32_t
                     if (r > (float)levels) r = (float)levels;
                     q = (unsigned)r;
                 }
-                const int k = g * group + j;
-                codes[(long long)n * words_per_row + k / per_word] |= (uint32_t)q << ((k % per_word) * bits);
+                /* code k occupies bits [k*bits, k*bits + bits) of the row */
+                uint32_t* row = codes + (long long)n * words_per_row;
+                const long long first = (long long)(g * group + j) * bits;
+                const int off = (int)(first % 32);
+                row[first / 32] |= (uint32_t)q << off;
+                if (off + bits > 32) row[first / 32 + 1] |= (uint32_t)q >> (32 - off);
             }
         }
     }

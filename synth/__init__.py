@@ -72,15 +72,16 @@ def activations(M: int, K: int, seed: int, std: float = 1.0) -> np.ndarray:
 
 def pack_codes(q: np.ndarray, bits: int) -> np.ndarray:
     """Pack integer codes ``q[N, K]`` (values < 2^bits) into uint32 words
-    ``[N, K*bits/32]``: lowest k in the lowest bits of each word."""
+    ``[N, K*bits/32]`` as one little-endian bit stream per row: code k holds
+    bits [k*bits, k*bits + bits), word j bits [32j, 32j + 32)."""
     q = np.asarray(q)
     N, K = q.shape
-    per = 32 // bits
-    if K % per:
-        raise ValueError("K must be a multiple of the codes per word")
-    qq = q.astype(np.uint32).reshape(N, K // per, per)
-    shifts = (np.arange(per, dtype=np.uint32) * np.uint32(bits))[None, None, :]
-    return np.bitwise_or.reduce(qq << shifts, axis=2).astype(np.uint32)
+    if (K * bits) % 32:
+        raise ValueError("K * bits must be a multiple of 32")
+    bitplanes = (q.astype(np.uint32)[:, :, None] >> np.arange(bits, dtype=np.uint32)) & 1
+    stream = bitplanes.astype(np.uint8).reshape(N, K * bits)
+    packed = np.packbits(stream, axis=1, bitorder="little")
+    return packed.view("<u4").astype(np.uint32).reshape(N, K * bits // 32)
 
 
 class QuantizedWeight:
