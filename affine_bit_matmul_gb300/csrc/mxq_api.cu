@@ -48,7 +48,7 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 mxq_status check_common(int K, int N, int bits, int group_size) {
-    if (bits != 4 && bits != 8) return MXQ_ERR_INVALID_ARG;
+    if (bits != 2 && bits != 4 && bits != 8) return MXQ_ERR_INVALID_ARG;
     if (group_size != 32 && group_size != 64 && group_size != 128) return MXQ_ERR_INVALID_ARG;
     if (K <= 0 || N <= 0 || K % 64 != 0 || K % group_size != 0) return MXQ_ERR_INVALID_ARG;
     return MXQ_OK;
@@ -286,10 +286,11 @@ mxq_status mxq_gather_qmm(const void* x, const uint32_t* w, const void* scales,
     p.kb_per_split = K / 64;
     p.w_expert_stride = (long long)N * K * bits / 32;
     p.sb_expert_stride = (long long)N * (K / group_size);
-    // 4-bit: two persistent CTAs per SM take tiles of (tile list) x (n tiles)
-    // from a counter as they finish the previous one, so the pipeline fills
-    // once per CTA and long and short tiles balance; 8-bit: one CTA per tile
-    if (bits == 4) {
+    // 2- and 4-bit: two persistent CTAs per SM take tiles of (tile list) x
+    // (n tiles) from a counter as they finish the previous one, so the
+    // pipeline fills once per CTA and long and short tiles balance; 8-bit:
+    // one CTA per tile
+    if (bits <= 4) {
         const long long bound = (long long)max_tiles * ((N + 127) / 128);
         p.persistent = 1;
         p.grid_ctas = (int)(bound < 2LL * sms ? bound : 2LL * sms);

@@ -97,7 +97,7 @@ struct StageGroups {
 };
 
 __host__ __device__ constexpr bool compact_mode(int bits, int max_rows, bool gather) {
-    return gather && bits == 4 && max_rows <= kCompactRows;
+    return gather && bits <= 4 && max_rows <= kCompactRows;
 }
 constexpr int kAStageCols = kBK / 2; // one bf16 pair per 32-bit column
 
@@ -166,6 +166,30 @@ __device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
     uint32_t d;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
     return d;
+}
+
+// Sixteen 2-bit codes (one word, lowest k in the lowest two bits) -> eight
+// bf16x2 words (k pairs 0-1, ..., 14-15) of s*q + b, one rounding each.
+__device__ __forceinline__ void dequant_word2(uint32_t wd, uint32_t s2, uint32_t b2,
+                                              uint32_t (&out)[8]) {
+    // plane j holds codes j, 4 + j, 8 + j, 12 + j in its four bytes
+    const uint32_t p0 = wd & 0x03030303u;
+    const uint32_t p1 = (wd >> 2) & 0x03030303u;
+    const uint32_t p2 = (wd >> 4) & 0x03030303u;
+    const uint32_t p3 = (wd >> 6) & 0x03030303u;
+    const uint32_t a01 = prmt(p0, p1, 0x5140u);    // q0 q1 q4 q5
+    const uint32_t a23 = prmt(p2, p3, 0x5140u);    // q2 q3 q6 q7
+    const uint32_t c01 = prmt(p0, p1, 0x7362u);    // q8 q9 q12 q13
+    const uint32_t c23 = prmt(p2, p3, 0x7362u);    // q10 q11 q14 q15
+    const uint32_t e[4] = {prmt(a01, a23, 0x5410u), prmt(a01, a23, 0x7632u),
+                           prmt(c01, c23, 0x5410u), prmt(c01, c23, 0x7632u)};  // q0-3 ... q12-15
+    // bf16 0x43qq = 128 + q exactly; subtracting 128 is exact
+    const uint32_t k128 = 0x43004300u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        out[2 * i] = hfma2_bf16(hsub2_bf16(prmt(e[i], 0x43u, 0x4140u), k128), s2, b2);
+        out[2 * i + 1] = hfma2_bf16(hsub2_bf16(prmt(e[i], 0x43u, 0x4342u), k128), s2, b2);
+    }
 }
 
 // Eight 4-bit codes (one word, lowest k in the lowest nibble) -> four bf16x2
@@ -551,7 +575,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t sbits = sb[SG::pair_of(h, c)];
                     const uint32_t bbits = sb[kP + SG::pair_of(h, c)];
                     uint32_t o[16];
-                    if (BITS == 4) {
+                    if (BITS == 2) {
+                        const uint32_t s2 = sbits | (sbits << 16);
+                        const uint32_t b2 = bbits | (bbits << 16);
+                        const uint4 cv = cw[h];  // 64 codes: words 0-1 are chunk 0
+                        const uint32_t wd[2] = {c ? cv.z : cv.x, c ? cv.w : cv.y};
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            uint32_t q8[8];
+                            dequant_word2(wd[j], s2, b2, q8);
+#pragma unroll
+                            for (int t = 0; t < 8; ++t) o[j * 8 + t] = q8[t];
+                        }
+                    } else if (BITS == 4) {
                         const uint32_t s2 = sbits | (sbits << 16);
                         const uint32_t b2 = bbits | (bbits << 16);
                         const uint4 cv = cw[h * 2 + c];
@@ -1211,7 +1247,19 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
                         const uint32_t sbits = sb[SG::pair_of(h, c)];
                         const uint32_t bbits = sb[kP + SG::pair_of(h, c)];
                         uint32_t o[16];
-                        if (BITS == 4) {
+                        if (BITS == 2) {
+                            const uint32_t s2 = sbits | (sbits << 16);
+                            const uint32_t b2 = bbits | (bbits << 16);
+                            const uint4 cv = cw[h];  // 64 codes: words 0-1 are chunk 0
+                            const uint32_t wd[2] = {c ? cv.z : cv.x, c ? cv.w : cv.y};
+#pragma unroll
+                            for (int j = 0; j < 2; ++j) {
+                                uint32_t q8[8];
+                                dequant_word2(wd[j], s2, b2, q8);
+#pragma unroll
+                                for (int u = 0; u < 8; ++u) o[j * 8 + u] = q8[u];
+                            }
+                        } else if (BITS == 4) {
                             const uint32_t s2 = sbits | (sbits << 16);
                             const uint32_t b2 = bbits | (bbits << 16);
                             const uint4 cv = cw[h * 2 + c];
@@ -1410,15 +1458,26 @@ cudaError_t launch_group(const QmmParams& p, int bits, bool gather, int grid_m,
     if (p.persistent) {
         const int n_tiles = (p.N + kTileN - 1) / kTileN;
         if (gather) {
-            // grouped, 4-bit, short tiles: two persistent CTAs per SM
-            if (bits != 4 || !compact_mode(4, max_rows_per_tile, true)) return cudaErrorNotSupported;
-            return launch_persistent<4, true, true, GROUP>(p, max_rows_per_tile, 0, n_tiles,
-                                                           p.grid_ctas, cm, xm, stream);
+            // grouped, 2- or 4-bit, short tiles: two persistent CTAs per SM
+            if (bits > 4 || !compact_mode(bits, max_rows_per_tile, true)) return cudaErrorNotSupported;
+            return bits == 2 ? launch_persistent<2, true, true, GROUP>(p, max_rows_per_tile, 0,
+                                                                       n_tiles, p.grid_ctas, cm, xm,
+                                                                       stream)
+                             : launch_persistent<4, true, true, GROUP>(p, max_rows_per_tile, 0,
+                                                                       n_tiles, p.grid_ctas, cm, xm,
+                                                                       stream);
         }
+        if (bits == 2)
+            return launch_persistent<2, false, false, GROUP>(p, max_rows_per_tile, p.m_tiles,
+                                                             n_tiles, p.grid_ctas, cm, xm, stream);
         return bits == 4 ? launch_persistent<4, false, false, GROUP>(
                                p, max_rows_per_tile, p.m_tiles, n_tiles, p.grid_ctas, cm, xm, stream)
                          : launch_persistent<8, false, false, GROUP>(
                                p, max_rows_per_tile, p.m_tiles, n_tiles, p.grid_ctas, cm, xm, stream);
+    }
+    if (bits == 2) {
+        if (gather) return cudaErrorNotSupported;  // 2-bit grouped calls are persistent (above)
+        return launch_variant<2, false, GROUP>(p, grid_m, max_rows_per_tile, cm, xm, stream);
     }
     if (bits == 4) {
         if (gather) return cudaErrorNotSupported;  // 4-bit grouped calls are persistent (above)

@@ -25,10 +25,10 @@
 //
 // Layout of the work in both:
 //  * a lane owns 16 bytes of codes per row (32 four-bit or 16 eight-bit
-//    codes, always inside one group: groups are 32, 64 or 128 wide and a
-//    lane's first k is a multiple of its code count), so a warp covers a K segment of
-//    1024 (4-bit) or 512 (8-bit) values with one coalesced 512-byte load per
-//    row;
+//    codes), or 8 bytes (32 two-bit codes), always inside one group: groups
+//    are 32, 64 or 128 wide and a lane's first k is a multiple of its code
+//    count; a warp covers a K segment of 1024 (2- and 4-bit) or 512 (8-bit)
+//    values with one coalesced load per row;
 //  * a CTA has one warp per K segment and owns a block of ROWS output rows;
 //    each lane keeps its 32/16 activations in registers for all the rows;
 //  * the affine terms are applied once per lane and row:
@@ -36,8 +36,8 @@
 //    with X = sum_k x_k over the lane's values (fp32);
 //  * the streaming kernel forms sum_k x_k q_k exactly with integer 4-way
 //    dot products over byte planes of the activations (see lane_dot_int);
-//    the direct-load kernel turns the codes into floats 1 + q*2^-7 (4-bit)
-//    or 1 + q*2^-15 (8-bit) by placing them in the mantissa of a constant
+//    the direct-load kernel turns the codes into floats 1 + q*2^-7 (2- and
+//    4-bit) or 1 + q*2^-15 (8-bit) by placing them in the mantissa of a constant
 //    with one byte permute each, sums x_k v_k in fp32 and uses
 //    sum_k x_k q_k = 2^p * (sum_k x_k v_k - X), p = 7 or 15;
 //  * per-row partials are reduced across lanes with a reduce-scatter
@@ -77,6 +77,40 @@ __device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(p));
     return v;
+}
+
+__device__ __forceinline__ uint2 ldg_stream2(const uint2* p) {
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+                 : "=r"(v.x), "=r"(v.y)
+                 : "l"(p));
+    return v;
+}
+
+// Sum over the lane's codes of x_k * v_k, v_k = 1 + q_k * 2^-7, for 32
+// two-bit codes in c.x, c.y (lowest k in the lowest two bits of each word).
+// Byte i of plane j = (word >> 2j) & 0x03030303 is code 4i + j of the word,
+// so planes 2t and 2t + 1 give the pairs (x_{4i+2t}, x_{4i+2t+1}).
+__device__ __forceinline__ float dot_chunk2(const uint4 c, const float2 (&x2)[16]) {
+    const uint32_t words[2] = {c.x, c.y};
+    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const uint32_t pe = ((words[w] >> (4 * t)) & 0x03030303u) | 0x80808080u;
+            const uint32_t po = ((words[w] >> (4 * t + 2)) & 0x03030303u) | 0x80808080u;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t sel = 0x7044u | (uint32_t(i) << 8);
+                float2 v;
+                v.x = __uint_as_float(prmt(pe, 0x3F000000u, sel));
+                v.y = __uint_as_float(prmt(po, 0x3F000000u, sel));
+                ffma2(acc, v, x2[w * 8 + i * 2 + t]);
+            }
+        }
+    }
+    return acc.x + acc.y;
 }
 
 // Sum over the lane's codes of x_k * v_k, v_k = 1 + q_k * 2^-7, for one
@@ -130,9 +164,9 @@ __device__ __forceinline__ void qmv_rows_direct(const __nv_bfloat16* __restrict_
                                                 const uint16_t* __restrict__ biases,
                                                 __nv_bfloat16* __restrict__ y, int K, int N,
                                                 int group, int row0) {
-    constexpr int kCodesPerLane = 128 / BITS;          // 32 or 16
+    constexpr int kCodesPerLane = BITS == 8 ? 16 : 32;
     constexpr int kSegK = 32 * kCodesPerLane;          // 1024 or 512
-    constexpr float kUnscale = BITS == 4 ? 128.f : 32768.f;
+    constexpr float kUnscale = BITS == 8 ? 32768.f : 128.f;
     __shared__ float red[kMaxWarps][kRows];
 
     const int lane = lane_id();
@@ -178,7 +212,13 @@ __device__ __forceinline__ void qmv_rows_direct(const __nv_bfloat16* __restrict_
             for (int u = 0; u < kUnroll; ++u) {
                 const int n = row0 + r0 + u;
                 if (n < N) {
-                    c[u] = ldg_stream(reinterpret_cast<const uint4*>(w + n * words_per_row + wofs));
+                    if (BITS == 2) {
+                        const uint2 v =
+                            ldg_stream2(reinterpret_cast<const uint2*>(w + n * words_per_row + wofs));
+                        c[u] = make_uint4(v.x, v.y, 0u, 0u);
+                    } else {
+                        c[u] = ldg_stream(reinterpret_cast<const uint4*>(w + n * words_per_row + wofs));
+                    }
                     s[u] = bf16_bits_to_float(__ldg(scales + (long long)n * groups + g));
                     b[u] = bf16_bits_to_float(__ldg(biases + (long long)n * groups + g));
                 } else {
@@ -189,7 +229,9 @@ __device__ __forceinline__ void qmv_rows_direct(const __nv_bfloat16* __restrict_
             }
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
-                const float A = BITS == 4 ? dot_chunk4(c[u], x2) : dot_chunk8(c[u], x2);
+                const float A = BITS == 2   ? dot_chunk2(c[u], x2)
+                                : BITS == 4 ? dot_chunk4(c[u], x2)
+                                            : dot_chunk8(c[u], x2);
                 part[r0 + u] += fmaf(s[u] * kUnscale, A - X, b[u] * X);
             }
         }
@@ -377,7 +419,8 @@ __device__ __forceinline__ uint32_t dp4a_uu(uint32_t a, uint32_t b, uint32_t c) 
 // Byte planes of a lane's 32 activations, arranged like its codes: for
 // 4-bit codes register 2w holds k = 8w, 8w+2, 8w+4, 8w+6 (the even nibbles
 // of word w) and register 2w+1 the odd ones; for 8-bit codes register w
-// holds k = 4w .. 4w+3.
+// holds k = 4w .. 4w+3; for 2-bit codes register 4w+j holds
+// k = 16w+j, 16w+4+j, 16w+8+j, 16w+12+j (code j of each byte of word w).
 struct XPlanes {
     uint32_t a[8], b[8], c[8];
 };
@@ -408,7 +451,9 @@ __device__ __forceinline__ int make_planes(const float (&xf)[32], XPlanes& P) {
         int X[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const int k = BITS == 4 ? (r >> 1) * 8 + 2 * i + (r & 1) : r * 4 + i;
+            const int k = BITS == 2   ? (r >> 2) * 16 + 4 * i + (r & 3)
+                          : BITS == 4 ? (r >> 1) * 8 + 2 * i + (r & 1)
+                                      : r * 4 + i;
             X[i] = __float2int_rn((xf[k] * s1) * s2);
         }
         // bytes 0 and 1 of X0..X3, then byte 2 (signed: |X| < 2^23)
@@ -427,7 +472,9 @@ __device__ __forceinline__ int make_planes(const float (&xf)[32], XPlanes& P) {
 template <int BITS>
 __device__ __forceinline__ float lane_dot_int(uint32_t codes_addr, const XPlanes& P) {
     uint32_t wd[8];
-    {
+    if (BITS == 2) {
+        asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(wd[0]), "=r"(wd[1]) : "r"(codes_addr));
+    } else {
         uint4 c0;
         asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
                      : "=r"(c0.x), "=r"(c0.y), "=r"(c0.z), "=r"(c0.w)
@@ -446,7 +493,9 @@ __device__ __forceinline__ float lane_dot_int(uint32_t codes_addr, const XPlanes
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
         uint32_t q;
-        if (BITS == 4)
+        if (BITS == 2)
+            q = (wd[r >> 2] >> (2 * (r & 3))) & 0x03030303u;
+        else if (BITS == 4)
             q = (r & 1) ? (wd[r >> 1] >> 4) & 0x0F0F0F0Fu : wd[r >> 1] & 0x0F0F0F0Fu;
         else
             q = wd[r];
@@ -454,9 +503,9 @@ __device__ __forceinline__ float lane_dot_int(uint32_t codes_addr, const XPlanes
         B = dp4a_uu(P.b[r], q, B);
         C = dp4a_uu(P.c[r], q, C);
     }
-    // |A| <= 32*15*128 and B < 32*15*256 (4-bit), or 32*255*128 and
-    // 32*255*256 (8-bit): A*256 + B stays below 2^31 and converts exactly
-    // when below 2^24 (always for 4-bit)
+    // |A| <= 32*15*128 and B < 32*15*256 (4-bit; less for 2-bit), or
+    // 32*255*128 and 32*255*256 (8-bit): A*256 + B stays below 2^31 and
+    // converts exactly when below 2^24 (always for 2- and 4-bit)
     const int AB = A * 256 + (int)B;
     return fmaf((float)AB, 256.f, (float)C);
 }
@@ -693,7 +742,7 @@ cudaError_t launch_gather_qmv(const void* x, const uint32_t* w, const void* scal
                               const void* biases, const int32_t* expert_ids,
                               const int32_t* row_src, void* y, int T, int B, int E, int K, int N,
                               int bits, int group, int32_t* status, cudaStream_t stream) {
-    const int seg_k = bits == 4 ? 1024 : 512;
+    const int seg_k = bits == 8 ? 512 : 1024;
     const int nseg_g = (K + seg_k - 1) / seg_k;
     const int passes = (nseg_g + kMaxWarps - 1) / kMaxWarps;
     const int warps = (nseg_g + passes - 1) / passes;
@@ -705,7 +754,10 @@ cudaError_t launch_gather_qmv(const void* x, const uint32_t* w, const void* scal
     auto* yb = static_cast<__nv_bfloat16*>(y);
     const long long wst = (long long)N * K * bits / 32;
     const long long sbst = (long long)N * (K / group);
-    if (bits == 4)
+    if (bits == 2)
+        gather_qmv_kernel<2><<<grid, block, 0, stream>>>(xb, w, sb, bb, expert_ids, row_src, yb, T,
+                                                        B, E, K, N, group, wst, sbst, status);
+    else if (bits == 4)
         gather_qmv_kernel<4><<<grid, block, 0, stream>>>(xb, w, sb, bb, expert_ids, row_src, yb, T,
                                                         B, E, K, N, group, wst, sbst, status);
     else
@@ -750,18 +802,22 @@ cudaError_t launch_qmv(const void* x, const uint32_t* w, const void* scales, con
         const int grid = sh.nchunks < sms ? sh.nchunks : sms;
         sh.nchunks = (sh.nchunks + grid - 1) / grid * grid;
         if (sh.nchunks > N) sh.nchunks = N;
+        if (bits == 2)
+            return launch_stream<2>(xb, w, sb, bb, yb, K, N, group, rpw, sh, grid, status, stream);
         return bits == 4
                    ? launch_stream<4>(xb, w, sb, bb, yb, K, N, group, rpw, sh, grid, status, stream)
                    : launch_stream<8>(xb, w, sb, bb, yb, K, N, group, rpw, sh, grid, status, stream);
     }
-    const int seg_k = bits == 4 ? 1024 : 512;
+    const int seg_k = bits == 8 ? 512 : 1024;
     const int nseg_g = (K + seg_k - 1) / seg_k;
     // as few passes over the segments as the warp limit allows, spread evenly
     const int passes = (nseg_g + kMaxWarps - 1) / kMaxWarps;
     const int warps = (nseg_g + passes - 1) / passes;
     const dim3 grid((N + kRows - 1) / kRows);
     const dim3 block(32 * warps);
-    if (bits == 4)
+    if (bits == 2)
+        qmv_generic_kernel<2><<<grid, block, 0, stream>>>(xb, w, sb, bb, yb, K, N, group);
+    else if (bits == 4)
         qmv_generic_kernel<4><<<grid, block, 0, stream>>>(xb, w, sb, bb, yb, K, N, group);
     else
         qmv_generic_kernel<8><<<grid, block, 0, stream>>>(xb, w, sb, bb, yb, K, N, group);

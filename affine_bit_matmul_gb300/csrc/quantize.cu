@@ -1,7 +1,8 @@
 // Affine group-wise encoder: float weights -> packed codes, bf16 scales and
 // biases (the stored format of mlxcel issue #1536, Baseline section: "affine
-// 4-bit / group 64"; 8-bit codes are unsigned bytes; groups of 32 and 128
-// consecutive k use the same rule).
+// 4-bit / group 64"; 8-bit codes are unsigned bytes; 2-bit codes are packed
+// sixteen per word like the 4-bit ones; groups of 32 and 128 consecutive k
+// use the same rule).
 //
 // Per (row n, group g of GROUP consecutive k): mn, mx = the group's minimum and
 // maximum (-0 read as +0); s = bf16(RN(RN(mx - mn) / (2^bits - 1))) and
@@ -14,7 +15,7 @@
 // One warp per row: each lane holds 8 consecutive values of a 256-wide block
 // (two 16-byte loads), GROUP / 8 lanes make a group (4, 8 or 16), so a
 // group's minimum and maximum take two to four shuffle steps and each lane
-// packs its own code word(s).
+// packs its own codes (half a word at 2 bits, one word at 4, two at 8).
 // HBM-bound: 4 bytes read per weight, bits/8 written.
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -88,7 +89,13 @@ __global__ void __launch_bounds__(kEncWarps * 32) quantize_kernel(const float* _
                     r = fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(v[u][i], b), s)), 0.f), (float)kLevels);
                 q[i] = (uint32_t)r;
             }
-            if (BITS == 4) {
+            if (BITS == 2) {
+                uint32_t half = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) half |= q[i] << (2 * i);
+                // row n has K / 8 halves of 16 bits; lane's k is a multiple of 8
+                reinterpret_cast<uint16_t*>(codes)[(long long)n * (K / 8) + k / 8] = (uint16_t)half;
+            } else if (BITS == 4) {
                 uint32_t word = 0;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) word |= q[i] << (4 * i);
@@ -118,7 +125,9 @@ cudaError_t launch_quantize(const float* W, uint32_t* codes, void* scales, void*
     auto* b = static_cast<uint16_t*>(biases);
 #define MXQ_ENC_CASE(G)                                                                \
     case G:                                                                            \
-        if (bits == 4)                                                                 \
+        if (bits == 2)                                                                 \
+            quantize_kernel<2, G><<<grid, block, 0, stream>>>(W, codes, s, b, N, K);   \
+        else if (bits == 4)                                                            \
             quantize_kernel<4, G><<<grid, block, 0, stream>>>(W, codes, s, b, N, K);   \
         else                                                                           \
             quantize_kernel<8, G><<<grid, block, 0, stream>>>(W, codes, s, b, N, K);   \

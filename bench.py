@@ -470,7 +470,10 @@ def secondary_measurements(mxq, dev, stream, hbm, bf16_peak, Ws):
     out.append(dense_entry("pair qmv 8-bit", 1, 5120, 5120, 8, W_sq, copies=6))
     out.append(dense_entry("pair qmv 4-bit", 1, 5120, 5120, 4, W_sq, copies=6))
     out.append(dense_entry("pair qmm 8-bit", 128, 5120, 5120, 8, W_sq, copies=6))
-    # group sizes 32 and 128 on the decode and prefill shapes (same weights)
+    # 2-bit codes and group sizes 32 and 128 on the decode and prefill shapes
+    # (same weights)
+    out.append(dense_entry("2-bit qmv", 1, 5120, 17408, 2, W_big, copies=6))
+    out.append(dense_entry("2-bit qmm prefill", 600, 5120, 17408, 2, W_big, copies=3))
     for group in (32, 128):
         out.append(dense_entry("group qmv", 1, 5120, 17408, 4, W_big, copies=6, group=group))
         out.append(dense_entry("group qmm prefill", 600, 5120, 17408, 4, W_big, copies=3,

@@ -22,6 +22,10 @@
  *                                    qmm_naive kernel name in issue #1536's
  *                                    profile table).  8-bit: four codes per
  *                                    word, lowest k in the lowest byte.
+ *                                    2-bit: sixteen codes per word, lowest k
+ *                                    in the lowest two bits (the bit width
+ *                                    is a parameter of the kernels in issue
+ *                                    #1536, Diagnosis item 3).
  *   scales  bf16   [N, K/G]          s per (output row, group of G k)
  *   biases  bf16   [N, K/G]          b per (output row, group of G k)
  *   y       bf16   [M, N]            output, rounded once from fp32 (RNE)
@@ -70,7 +74,7 @@ typedef enum {
  * fp32 accumulation at every width is the fix that item names).
  *   x: bf16 [K]; y: bf16 [N]; w, scales, biases as above.
  *   dev_status: device int32 or NULL; receives 0 or MXQ_DEV_TIMEOUT.
- * Requirements: bits in {4, 8}; group_size in {32, 64, 128}; K > 0,
+ * Requirements: bits in {2, 4, 8}; group_size in {32, 64, 128}; K > 0,
  * K % 64 == 0 and K % group_size == 0; N > 0; x, w, y 16-byte aligned;
  * scales, biases 2-byte aligned.  The streaming kernel is used when
  * K % 512 == 0, K <= 20480, K / group_size % 8 == 0 and scales/biases are
@@ -122,7 +126,7 @@ mxq_status mxq_qmm(const void* x, const uint32_t* w, const void* scales, const v
  * its expert's matrix (the same result rule, another summation order) and
  * use no workspace memory, though the size check still applies.
  * Requirements: B, E, T, N > 0; K > 0, K % 64 == 0, K % group_size == 0;
- * bits in {4, 8}; group_size in {32, 64, 128}; x, w, y 16-byte aligned; the
+ * bits in {2, 4, 8}; group_size in {32, 64, 128}; x, w, y 16-byte aligned; the
  * rest aligned to type.                                                      */
 mxq_status mxq_gather_qmm(const void* x, const uint32_t* w, const void* scales,
                           const void* biases, const int32_t* expert_ids,
@@ -180,7 +184,7 @@ mxq_status mxq_gather_qmm_noalloc(const void* x, const uint32_t* w, const void* 
  * s = bf16(RN(RN(mx - mn) / (2^bits - 1))), b = bf16(mn), rounded to nearest
  * even; q = clamp(rint(RN(RN(w - b) / s)), 0, 2^bits - 1) with the stored
  * bf16 s and b, q = 0 when s == 0.  All decisions in binary32, so the codes
- * are reproducible bit for bit.  Requirements: bits in {4, 8};
+ * are reproducible bit for bit.  Requirements: bits in {2, 4, 8};
  * group_size in {32, 64, 128}; K > 0, K % 64 == 0, K % group_size == 0;
  * N > 0.                                                                    */
 mxq_status mxq_quantize(const float* w, uint32_t* codes, void* scales, void* biases, int N,

@@ -60,7 +60,7 @@ def qmv(L, x=FAKE, w=FAKE, s=FAKE, b=FAKE, y=FAKE, K=128, N=64, bits=4, group=64
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(bits=3), 1), (dict(bits=16), 1), (dict(bits=2), 1), (dict(group=16), 1),
+    (dict(bits=3), 1), (dict(bits=16), 1), (dict(bits=1), 1), (dict(group=16), 1),
     (dict(group=48), 1), (dict(group=256), 1), (dict(group=0), 1), (dict(group=128, K=192), 1),
     (dict(group=32, K=96), 1), (dict(K=100), 1), (dict(K=0), 1), (dict(K=-64), 1), (dict(N=0), 1),
     (dict(x=None), 1), (dict(w=None), 1), (dict(s=None), 1), (dict(b=None), 1), (dict(y=None), 1),
