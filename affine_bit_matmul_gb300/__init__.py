@@ -13,7 +13,9 @@ group 64"):
 * ``x``: bf16 ``[M, K]`` (``[K]`` for ``qmv``);
 * ``w``: int32 or uint32 ``[N, K*bits/32]`` packed codes, 4-bit codes eight per
   little-endian word (lowest k in the lowest nibble), 2-bit codes sixteen per
-  word, 8-bit codes four per word (``bits`` in 2, 4, 8);
+  word, 8-bit codes four per word; 3- and 6-bit codes continue the same
+  little-endian bit stream per row and may straddle words (``bits`` in 2, 3,
+  4, 6, 8);
 * ``scales``, ``biases``: bf16 ``[N, K/group_size]``, one pair per group of
   ``group_size`` consecutive k (32, 64 or 128; every call defaults to 64);
 * result ``y``: bf16 ``[M, N]``.

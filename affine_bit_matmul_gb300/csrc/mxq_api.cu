@@ -48,9 +48,12 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 mxq_status check_common(int K, int N, int bits, int group_size) {
-    if (bits != 2 && bits != 4 && bits != 8) return MXQ_ERR_INVALID_ARG;
+    if (bits != 2 && bits != 3 && bits != 4 && bits != 6 && bits != 8) return MXQ_ERR_INVALID_ARG;
     if (group_size != 32 && group_size != 64 && group_size != 128) return MXQ_ERR_INVALID_ARG;
     if (K <= 0 || N <= 0 || K % 64 != 0 || K % group_size != 0) return MXQ_ERR_INVALID_ARG;
+    // rows of codes are whole 16-byte units (the tensor-core kernels copy
+    // them with TMA): a multiple of 128 codes at 3 bits
+    if (bits == 3 && K % 128 != 0) return MXQ_ERR_INVALID_ARG;
     return MXQ_OK;
 }
 
@@ -74,7 +77,6 @@ DensePlan plan_dense(int M, int K, int N, int bits, int sms) {
     const int tiles = n_tiles * pl.m_tiles;
     const int KB = K / 64;
     const int slots = sms;
-    (void)bits;
     int splits = 1;
     if (tiles < slots) {
         splits = slots / tiles;
@@ -84,6 +86,9 @@ DensePlan plan_dense(int M, int K, int N, int bits, int sms) {
         if (splits < 1) splits = 1;
     }
     pl.kb_per_split = (KB + splits - 1) / splits;
+    // a split starts on a 16-byte boundary of the code rows: 3-bit blocks
+    // of 64 codes are 24 bytes, so splits of 3-bit codes hold an even number
+    if (bits == 3 && (pl.kb_per_split & 1)) ++pl.kb_per_split;
     pl.splits = (KB + pl.kb_per_split - 1) / pl.kb_per_split;  // every split gets >= 1 block
     return pl;
 }
@@ -288,9 +293,9 @@ mxq_status mxq_gather_qmm(const void* x, const uint32_t* w, const void* scales,
     p.sb_expert_stride = (long long)N * (K / group_size);
     // 2- and 4-bit: two persistent CTAs per SM take tiles of (tile list) x
     // (n tiles) from a counter as they finish the previous one, so the
-    // pipeline fills once per CTA and long and short tiles balance; 8-bit:
-    // one CTA per tile
-    if (bits <= 4) {
+    // pipeline fills once per CTA and long and short tiles balance; 3-, 6-
+    // and 8-bit (code slots too large for two CTAs per SM): one CTA per tile
+    if (bits == 2 || bits == 4) {
         const long long bound = (long long)max_tiles * ((N + 127) / 128);
         p.persistent = 1;
         p.grid_ctas = (int)(bound < 2LL * sms ? bound : 2LL * sms);

@@ -66,6 +66,11 @@ constexpr int kMaxCodeStages = 8;    // code slots
 // eight different bank groups.
 constexpr int kCodeSlotRowBytes = 256;
 constexpr int kCodeBoxRowBytes = 128;
+// 3- and 6-bit stages are 48 and 96 bytes per row: their slots hold 384
+// bytes (three boxes, 8 or 4 stages), so a stage may cross a box boundary.
+__host__ __device__ constexpr int slot_row_bytes(int bits) {
+    return (bits == 3 || bits == 6) ? 384 : kCodeSlotRowBytes;
+}
 constexpr int kCodeBoxBytes = kTileN * kCodeBoxRowBytes;
 constexpr int kMaxAStages = 6;       // dequantised stages held in tensor memory
 constexpr int kMaxXStages = 16;
@@ -97,12 +102,12 @@ struct StageGroups {
 };
 
 __host__ __device__ constexpr bool compact_mode(int bits, int max_rows, bool gather) {
-    return gather && bits <= 4 && max_rows <= kCompactRows;
+    return gather && (bits == 2 || bits == 4) && max_rows <= kCompactRows;
 }
 constexpr int kAStageCols = kBK / 2; // one bf16 pair per 32-bit column
 
 struct SmemLayout {
-    int c_bytes, c_stages;    // packed-code ring: slots of kCodeSlotRowBytes per w row
+    int c_bytes, c_stages;    // packed-code ring: slots of slot_row_bytes(bits) per w row
     int x_bytes, x_stages;    // activation ring (MMA B operand), one 64-wide atom per slot
     int c_offset;             // rings: x at 0, then codes
     int bar_offset, total;
@@ -114,11 +119,11 @@ struct SmemLayout {
 // slots, up to six activation slots, then more code slots (up to 8), then
 // more activation slots (up to 16).  A code slot is the same 32 KB for both
 // widths (4 stages of 4-bit codes or 2 of 8-bit).
-__host__ __device__ inline SmemLayout make_layout(int max_rows, bool compact) {
+__host__ __device__ inline SmemLayout make_layout(int max_rows, bool compact, int slot_bytes) {
     SmemLayout L;
     const int budget = compact ? kCompactSmemBudget : kSmemBudget;
     const int rows16 = (max_rows + 15) & ~15;
-    L.c_bytes = kTileN * kCodeSlotRowBytes;           // 32 KB: 4 (4-bit) or 2 (8-bit) stages
+    L.c_bytes = kTileN * slot_bytes;  // 32 KB: 8, 4 or 2 stages of 2-, 4-, 8-bit; 48 KB: 8 or 4 of 3-, 6-bit
     L.x_bytes = (rows16 / 8) * 1024;                  // 128 B per row, 8-row atoms
     // two code slots, up to six activation slots, then more code slots (up
     // to kMaxCodeStages), then more activation slots (up to kMaxXStages)
@@ -189,6 +194,45 @@ __device__ __forceinline__ void dequant_word2(uint32_t wd, uint32_t s2, uint32_t
     for (int i = 0; i < 4; ++i) {
         out[2 * i] = hfma2_bf16(hsub2_bf16(prmt(e[i], 0x43u, 0x4140u), k128), s2, b2);
         out[2 * i + 1] = hfma2_bf16(hsub2_bf16(prmt(e[i], 0x43u, 0x4342u), k128), s2, b2);
+    }
+}
+
+// Word j of a stage's codes (uint4 chunks in order, four words each).
+template <int BITS>
+__device__ __forceinline__ uint32_t stage_word(const uint4 (&cw)[BITS], int j) {
+    const uint4 v = cw[j >> 2];
+    const int e = j & 3;
+    return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+}
+
+// Bits [p, p + BITS) of the little-endian bit stream in the stage's words,
+// placed at bit `at` of the result (0 or 16), all other bits zero.
+template <int BITS>
+__device__ __forceinline__ uint32_t stream_field(const uint4 (&cw)[BITS], int p, int at) {
+    const int j = p >> 5, off = p & 31;
+    uint32_t t;
+    if (off + BITS > 32)
+        t = __funnelshift_r(stage_word<BITS>(cw, j), stage_word<BITS>(cw, j + 1), off - at);
+    else if (off >= at)
+        t = stage_word<BITS>(cw, j) >> (off - at);
+    else
+        t = stage_word<BITS>(cw, j) << (at - off);
+    return t & (((1u << BITS) - 1u) << at);
+}
+
+// 32 codes of 3 or 6 bits starting at word w0 of the stage (32 * BITS bits,
+// word aligned) -> sixteen bf16x2 words of s*q + b, one rounding each.
+template <int BITS>
+__device__ __forceinline__ void dequant_stream32(const uint4 (&cw)[BITS], int w0, uint32_t s2,
+                                                 uint32_t b2, uint32_t (&out)[16]) {
+    const uint32_t k128 = 0x43004300u;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int p = w0 * 32 + 2 * i * BITS;
+        // bf16 0x43qq = 128 + q exactly (q < 64); subtracting 128 is exact
+        const uint32_t e = stream_field<BITS>(cw, p, 0) | stream_field<BITS>(cw, p + BITS, 16) |
+                           0x43004300u;
+        out[i] = hfma2_bf16(hsub2_bf16(e, k128), s2, b2);
     }
 }
 
@@ -368,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     qmm_tc_kernel(const QmmParams p, int max_rows, const __grid_constant__ CUtensorMap code_map,
                   const __grid_constant__ CUtensorMap x_map) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    const SmemLayout L = make_layout(max_rows, false);
+    const SmemLayout L = make_layout(max_rows, false, slot_row_bytes(BITS));
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     uint64_t* cfull = reinterpret_cast<uint64_t*>(smem + L.bar_offset);
@@ -408,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     using SG = StageGroups<GROUP>;
     constexpr int kP = SG::kPairs;
     const int SC = L.c_stages;
-    constexpr int kStagesPerSlot = kCodeSlotRowBytes / (kBK * BITS / 8);
+    constexpr int kStagesPerSlot = slot_row_bytes(BITS) / (kBK * BITS / 8);
     const int SX = L.x_stages;
     // tensor memory: accumulator in columns [0, n_mma), dequantised stages
     // of 64 columns from a0 on
@@ -449,8 +493,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // [128 rows x 128 k] packed codes per stage; a box that runs past K
         // is zero-filled, a second half that belongs to the next K split is
         // loaded but never dequantised
-        constexpr int kWordsPerSlot = kCodeSlotRowBytes / 4;
+        constexpr int kWordsPerSlot = slot_row_bytes(BITS) / 4;
         constexpr int kWordsPerBox = kCodeBoxRowBytes / 4;
+        constexpr int kBoxes = slot_row_bytes(BITS) / kCodeBoxRowBytes;
         const int words = p.K * BITS / 32;
         const int nslots = (nst + kStagesPerSlot - 1) / kStagesPerSlot;
         Ring ring(SC);
@@ -460,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int c0 = kb_begin * (kHalfK * BITS / 32) + i * kWordsPerSlot;
                 // a box that starts past the end of the row is not loaded
                 // (its stages are never dequantised)
-                const int nbox = c0 + kWordsPerBox < words ? 2 : 1;
+                const int nbox = min(kBoxes, (words - c0 + kWordsPerBox - 1) / kWordsPerBox);
                 mbar_expect_tx(&cfull[ring.slot], (uint32_t)(nbox * kCodeBoxBytes));
                 const uint32_t dst = c_base0 + ring.slot * L.c_bytes;
                 for (int b = 0; b < nbox; ++b) {
@@ -556,13 +601,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             // this stage's kRowBytes of row r: box (off / 128), chunks from
             // (off % 128) / 16 on, each at its swizzled place in the line
             const int off = csub * kRowBytes;
-            const uint32_t c_line = c_base0 + cs * L.c_bytes + (off / kCodeBoxRowBytes) * kCodeBoxBytes +
-                                    r * kCodeBoxRowBytes;
-            const int chunk0 = (off % kCodeBoxRowBytes) / 16;
             uint4 cw[BITS];
+            if (BITS == 3 || BITS == 6) {
+                // 48- or 96-byte stages may cross a box: place each 16-byte
+                // chunk by its own box
+                const uint32_t c_slot = c_base0 + cs * L.c_bytes + r * kCodeBoxRowBytes;
 #pragma unroll
-            for (int j = 0; j < BITS; ++j)
-                cw[j] = ld_shared_v4(c_line + (uint32_t)(((chunk0 + j) ^ (r & 7)) << 4));
+                for (int j = 0; j < BITS; ++j) {
+                    const int byte = off + 16 * j;
+                    cw[j] = ld_shared_v4(c_slot + (uint32_t)((byte >> 7) * kCodeBoxBytes) +
+                                         (uint32_t)((((byte >> 4) & 7) ^ (r & 7)) << 4));
+                }
+            } else {
+                const uint32_t c_line = c_base0 + cs * L.c_bytes +
+                                        (off / kCodeBoxRowBytes) * kCodeBoxBytes +
+                                        r * kCodeBoxRowBytes;
+                const int chunk0 = (off % kCodeBoxRowBytes) / 16;
+#pragma unroll
+                for (int j = 0; j < BITS; ++j)
+                    cw[j] = ld_shared_v4(c_line + (uint32_t)(((chunk0 + j) ^ (r & 7)) << 4));
+            }
             const int as = ar.slot;
             if (s >= SA && !warp_wait(&aempty[as], ar.parity ^ 1)) return false;
             tc_fence_after();
@@ -575,7 +633,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t sbits = sb[SG::pair_of(h, c)];
                     const uint32_t bbits = sb[kP + SG::pair_of(h, c)];
                     uint32_t o[16];
-                    if (BITS == 2) {
+                    if (BITS == 3 || BITS == 6) {
+                        const uint32_t s2 = sbits | (sbits << 16);
+                        const uint32_t b2 = bbits | (bbits << 16);
+                        dequant_stream32<BITS>(cw, (2 * h + c) * BITS, s2, b2, o);
+                    } else if (BITS == 2) {
                         const uint32_t s2 = sbits | (sbits << 16);
                         const uint32_t b2 = bbits | (bbits << 16);
                         const uint4 cv = cw[h];  // 64 codes: words 0-1 are chunk 0
@@ -895,7 +957,7 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
                           const __grid_constant__ CUtensorMap code_map,
                           const __grid_constant__ CUtensorMap x_map) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    const SmemLayout L = make_layout(max_rows, COMPACT);
+    const SmemLayout L = make_layout(max_rows, COMPACT, slot_row_bytes(BITS));
     constexpr int kCols = COMPACT ? kCompactTmemCols : kTmemCols;
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -922,7 +984,7 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
     const int total = GATHER ? (*p.tile_count) * n_tiles : m_tiles * n_tiles;
     const int KB = p.K / kHalfK;              // 64-wide blocks
     const int nst = (KB + 1) / 2;             // 128-wide stages per tile
-    constexpr int kSPS = kCodeSlotRowBytes / (kBK * BITS / 8);  // stages per code slot
+    constexpr int kSPS = slot_row_bytes(BITS) / (kBK * BITS / 8);  // stages per code slot
     const int nslots = (nst + kSPS - 1) / kSPS;
     const int groups = p.K / GROUP;
     using SG = StageGroups<GROUP>;
@@ -1005,8 +1067,9 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
 
     if (warp == kCodeWarp) {
         // ---------------------------------------------------------------- codes TMA
-        constexpr int kWordsPerSlot = kCodeSlotRowBytes / 4;
+        constexpr int kWordsPerSlot = slot_row_bytes(BITS) / 4;
         constexpr int kWordsPerBox = kCodeBoxRowBytes / 4;
+        constexpr int kBoxes = slot_row_bytes(BITS) / kCodeBoxRowBytes;
         const int words = p.K * BITS / 32;
         Ring ring(SC);
         long long issued = 0;
@@ -1031,7 +1094,7 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
                 }
                 if (elect_one()) {
                     const int c0 = j * kWordsPerSlot;
-                    const int nbox = c0 + kWordsPerBox < words ? 2 : 1;
+                    const int nbox = min(kBoxes, (words - c0 + kWordsPerBox - 1) / kWordsPerBox);
                     mbar_expect_tx(&cfull[ring.slot], (uint32_t)(nbox * kCodeBoxBytes));
                     const uint32_t dst = c_base0 + ring.slot * L.c_bytes;
                     for (int b = 0; b < nbox; ++b) {
@@ -1228,13 +1291,25 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
                 const int cs = cr.slot;
                 if (!warp_wait_ab(&cfull[cs], cr.parity, abort_flag)) return false;
                 const int off = csub * kRowBytes;
-                const uint32_t c_line = c_base0 + cs * L.c_bytes + (off / kCodeBoxRowBytes) * kCodeBoxBytes +
-                                        r * kCodeBoxRowBytes;
-                const int chunk0 = (off % kCodeBoxRowBytes) / 16;
                 uint4 cw[BITS];
+                if (BITS == 3 || BITS == 6) {
+                    // 48- or 96-byte stages may cross a box
+                    const uint32_t c_slot = c_base0 + cs * L.c_bytes + r * kCodeBoxRowBytes;
 #pragma unroll
-                for (int j = 0; j < BITS; ++j)
-                    cw[j] = ld_shared_v4(c_line + (uint32_t)(((chunk0 + j) ^ (r & 7)) << 4));
+                    for (int j = 0; j < BITS; ++j) {
+                        const int byte = off + 16 * j;
+                        cw[j] = ld_shared_v4(c_slot + (uint32_t)((byte >> 7) * kCodeBoxBytes) +
+                                             (uint32_t)((((byte >> 4) & 7) ^ (r & 7)) << 4));
+                    }
+                } else {
+                    const uint32_t c_line = c_base0 + cs * L.c_bytes +
+                                            (off / kCodeBoxRowBytes) * kCodeBoxBytes +
+                                            r * kCodeBoxRowBytes;
+                    const int chunk0 = (off % kCodeBoxRowBytes) / 16;
+#pragma unroll
+                    for (int j = 0; j < BITS; ++j)
+                        cw[j] = ld_shared_v4(c_line + (uint32_t)(((chunk0 + j) ^ (r & 7)) << 4));
+                }
                 const int as = ar.slot;
                 if (g0 + s >= SA && !warp_wait_ab(&aempty[as], ar.parity ^ 1, abort_flag)) return false;
                 tc_fence_after();
@@ -1247,7 +1322,11 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
                         const uint32_t sbits = sb[SG::pair_of(h, c)];
                         const uint32_t bbits = sb[kP + SG::pair_of(h, c)];
                         uint32_t o[16];
-                        if (BITS == 2) {
+                        if (BITS == 3 || BITS == 6) {
+                            const uint32_t s2 = sbits | (sbits << 16);
+                            const uint32_t b2 = bbits | (bbits << 16);
+                            dequant_stream32<BITS>(cw, (2 * h + c) * BITS, s2, b2, o);
+                        } else if (BITS == 2) {
                             const uint32_t s2 = sbits | (sbits << 16);
                             const uint32_t b2 = bbits | (bbits << 16);
                             const uint4 cv = cw[h];  // 64 codes: words 0-1 are chunk 0
@@ -1374,7 +1453,7 @@ template <int BITS, bool GATHER, bool COMPACT, int GROUP>
 cudaError_t launch_persistent(const QmmParams& p, int max_rows, int m_tiles, int n_tiles,
                               int grid, const CUtensorMap& cm, const CUtensorMap& xm,
                               cudaStream_t stream) {
-    const SmemLayout L = make_layout(max_rows, COMPACT);
+    const SmemLayout L = make_layout(max_rows, COMPACT, slot_row_bytes(BITS));
     const int smem = L.total + kPBarBytes;
     static bool attr_set[64] = {};
     int dev = 0;
@@ -1417,7 +1496,7 @@ EncodeTiledFn encode_fn() {
 template <int BITS, bool GATHER, int GROUP>
 cudaError_t launch_variant(const QmmParams& p, int grid_m, int max_rows, const CUtensorMap& cm,
                            const CUtensorMap& xm, cudaStream_t stream) {
-    const SmemLayout L = make_layout(max_rows, false);
+    const SmemLayout L = make_layout(max_rows, false, slot_row_bytes(BITS));
     // the shared-memory opt-in is per device; do it once each
     static bool attr_set[64] = {};
     int dev = 0;
@@ -1449,8 +1528,9 @@ cudaError_t launch_variant(const QmmParams& p, int grid_m, int max_rows, const C
     return cudaGetLastError();
 }
 
-// Launch form for one group size: persistent (dense 4/8-bit; grouped 4-bit
-// compact), else one CTA per tile (dense with a K split; grouped 8-bit).
+// Launch form for one group size: persistent (dense, every width; grouped 2-
+// and 4-bit compact), else one CTA per tile (dense with a K split; grouped 3-,
+// 6- and 8-bit).
 template <int GROUP>
 cudaError_t launch_group(const QmmParams& p, int bits, bool gather, int grid_m,
                          int max_rows_per_tile, const CUtensorMap& cm, const CUtensorMap& xm,
@@ -1459,7 +1539,7 @@ cudaError_t launch_group(const QmmParams& p, int bits, bool gather, int grid_m,
         const int n_tiles = (p.N + kTileN - 1) / kTileN;
         if (gather) {
             // grouped, 2- or 4-bit, short tiles: two persistent CTAs per SM
-            if (bits > 4 || !compact_mode(bits, max_rows_per_tile, true)) return cudaErrorNotSupported;
+            if (!compact_mode(bits, max_rows_per_tile, true)) return cudaErrorNotSupported;
             return bits == 2 ? launch_persistent<2, true, true, GROUP>(p, max_rows_per_tile, 0,
                                                                        n_tiles, p.grid_ctas, cm, xm,
                                                                        stream)
@@ -1470,6 +1550,12 @@ cudaError_t launch_group(const QmmParams& p, int bits, bool gather, int grid_m,
         if (bits == 2)
             return launch_persistent<2, false, false, GROUP>(p, max_rows_per_tile, p.m_tiles,
                                                              n_tiles, p.grid_ctas, cm, xm, stream);
+        if (bits == 3)
+            return launch_persistent<3, false, false, GROUP>(p, max_rows_per_tile, p.m_tiles,
+                                                             n_tiles, p.grid_ctas, cm, xm, stream);
+        if (bits == 6)
+            return launch_persistent<6, false, false, GROUP>(p, max_rows_per_tile, p.m_tiles,
+                                                             n_tiles, p.grid_ctas, cm, xm, stream);
         return bits == 4 ? launch_persistent<4, false, false, GROUP>(
                                p, max_rows_per_tile, p.m_tiles, n_tiles, p.grid_ctas, cm, xm, stream)
                          : launch_persistent<8, false, false, GROUP>(
@@ -1479,6 +1565,12 @@ cudaError_t launch_group(const QmmParams& p, int bits, bool gather, int grid_m,
         if (gather) return cudaErrorNotSupported;  // 2-bit grouped calls are persistent (above)
         return launch_variant<2, false, GROUP>(p, grid_m, max_rows_per_tile, cm, xm, stream);
     }
+    if (bits == 3)
+        return gather ? launch_variant<3, true, GROUP>(p, grid_m, max_rows_per_tile, cm, xm, stream)
+                      : launch_variant<3, false, GROUP>(p, grid_m, max_rows_per_tile, cm, xm, stream);
+    if (bits == 6)
+        return gather ? launch_variant<6, true, GROUP>(p, grid_m, max_rows_per_tile, cm, xm, stream)
+                      : launch_variant<6, false, GROUP>(p, grid_m, max_rows_per_tile, cm, xm, stream);
     if (bits == 4) {
         if (gather) return cudaErrorNotSupported;  // 4-bit grouped calls are persistent (above)
         return launch_variant<4, false, GROUP>(p, grid_m, max_rows_per_tile, cm, xm, stream);

@@ -25,7 +25,8 @@
 //
 // Layout of the work in both:
 //  * a lane owns 16 bytes of codes per row (32 four-bit or 16 eight-bit
-//    codes), or 8 bytes (32 two-bit codes), always inside one group: groups
+//    codes), or 8, 12 or 24 bytes (32 two-, three- or six-bit codes; the
+//    last two only in the direct-load kernel), always inside one group: groups
 //    are 32, 64 or 128 wide and a lane's first k is a multiple of its code
 //    count; a warp covers a K segment of 1024 (2- and 4-bit) or 512 (8-bit)
 //    values with one coalesced load per row;
@@ -56,6 +57,12 @@ namespace {
 constexpr int kRows = 16;    // output rows per CTA
 constexpr int kUnroll = 4;   // rows whose codes are in flight together
 constexpr int kMaxWarps = 20;  // one warp per K segment up to K = 20480 (4-bit)
+
+// Warps per CTA of the direct-load kernels: 3- and 6-bit codes are cut out
+// of the bit stream one by one and need more registers, so fewer warps.
+__host__ __device__ constexpr int direct_max_warps(int bits) {
+    return (bits == 3 || bits == 6) ? 16 : kMaxWarps;
+}
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t d;
@@ -136,6 +143,37 @@ __device__ __forceinline__ float dot_chunk4(const uint4 c, const float2 (&x2)[16
     return acc.x + acc.y;
 }
 
+// 3- and 6-bit codes: the lane's 32 codes are BITS words of the row's
+// little-endian bit stream (code m holds bits [m*BITS, m*BITS + BITS) of
+// them, possibly across two words).  code_as_float places code m in the
+// mantissa at bit 16: v = 1 + q * 2^-7.
+template <int BITS>
+__device__ __forceinline__ float code_as_float(const uint32_t (&w)[6], int m) {
+    const int p = m * BITS;
+    const int j = p >> 5, off = p & 31;
+    uint32_t t;
+    if (off + BITS > 32)
+        t = __funnelshift_r(w[j], w[j + 1], off - 16);  // off > 26 here
+    else if (off >= 16)
+        t = w[j] >> (off - 16);
+    else
+        t = w[j] << (16 - off);
+    return __uint_as_float((t & (((1u << BITS) - 1u) << 16)) | 0x3F800000u);
+}
+
+template <int BITS>
+__device__ __forceinline__ float dot_chunk_stream(const uint32_t (&w)[6], const float2 (&x2)[16]) {
+    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        float2 v;
+        v.x = code_as_float<BITS>(w, 2 * i);
+        v.y = code_as_float<BITS>(w, 2 * i + 1);
+        ffma2(acc, v, x2[i]);
+    }
+    return acc.x + acc.y;
+}
+
 // Same for 16 eight-bit codes: v_k = 1 + q_k * 2^-15.  x2 holds 8 pairs.
 __device__ __forceinline__ float dot_chunk8(const uint4 c, const float2 (&x2)[16]) {
     const uint32_t words[4] = {c.x, c.y, c.z, c.w};
@@ -166,6 +204,9 @@ __device__ __forceinline__ void qmv_rows_direct(const __nv_bfloat16* __restrict_
                                                 int group, int row0) {
     constexpr int kCodesPerLane = BITS == 8 ? 16 : 32;
     constexpr int kSegK = 32 * kCodesPerLane;          // 1024 or 512
+    // rows whose codes are in flight together (two for 3- and 6-bit rows,
+    // whose codes are cut out of the bit stream one by one)
+    constexpr int kU = (BITS == 3 || BITS == 6) ? 2 : kUnroll;
     constexpr float kUnscale = BITS == 8 ? 32768.f : 128.f;
     __shared__ float red[kMaxWarps][kRows];
 
@@ -205,14 +246,32 @@ __device__ __forceinline__ void qmv_rows_direct(const __nv_bfloat16* __restrict_
         const long long wofs = (long long)k0 * BITS / 32;  // word offset in a row
 
 #pragma unroll
-        for (int r0 = 0; r0 < kRows; r0 += kUnroll) {
-            uint4 c[kUnroll];
-            float s[kUnroll], b[kUnroll];
+        for (int r0 = 0; r0 < kRows; r0 += kU) {
+            uint4 c[kU];
+            uint32_t cs[kU][6];  // 3- and 6-bit codes: BITS words per lane
+            float s[kU], b[kU];
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
+            for (int u = 0; u < kU; ++u) {
                 const int n = row0 + r0 + u;
+#pragma unroll
+                for (int j = 0; j < 6; ++j) cs[u][j] = 0u;
                 if (n < N) {
-                    if (BITS == 2) {
+                    if (BITS == 3) {
+                        const uint32_t* src = w + n * words_per_row + wofs;
+#pragma unroll
+                        for (int j = 0; j < 3; ++j) cs[u][j] = __ldg(src + j);
+                        c[u] = make_uint4(0u, 0u, 0u, 0u);
+                    } else if (BITS == 6) {
+                        // 24 bytes from an 8-byte aligned offset (6 * k0 / 32 words)
+                        const uint2* src = reinterpret_cast<const uint2*>(w + n * words_per_row + wofs);
+#pragma unroll
+                        for (int j = 0; j < 3; ++j) {
+                            const uint2 v = __ldg(src + j);
+                            cs[u][2 * j] = v.x;
+                            cs[u][2 * j + 1] = v.y;
+                        }
+                        c[u] = make_uint4(0u, 0u, 0u, 0u);
+                    } else if (BITS == 2) {
                         const uint2 v =
                             ldg_stream2(reinterpret_cast<const uint2*>(w + n * words_per_row + wofs));
                         c[u] = make_uint4(v.x, v.y, 0u, 0u);
@@ -228,10 +287,11 @@ __device__ __forceinline__ void qmv_rows_direct(const __nv_bfloat16* __restrict_
                 }
             }
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const float A = BITS == 2   ? dot_chunk2(c[u], x2)
-                                : BITS == 4 ? dot_chunk4(c[u], x2)
-                                            : dot_chunk8(c[u], x2);
+            for (int u = 0; u < kU; ++u) {
+                const float A = (BITS == 3 || BITS == 6) ? dot_chunk_stream<BITS>(cs[u], x2)
+                                : BITS == 2                ? dot_chunk2(c[u], x2)
+                                : BITS == 4                ? dot_chunk4(c[u], x2)
+                                                           : dot_chunk8(c[u], x2);
                 part[r0 + u] += fmaf(s[u] * kUnscale, A - X, b[u] * X);
             }
         }
@@ -260,7 +320,7 @@ __device__ __forceinline__ void qmv_rows_direct(const __nv_bfloat16* __restrict_
 }
 
 template <int BITS>
-__global__ void __launch_bounds__(kMaxWarps * 32) qmv_generic_kernel(const __nv_bfloat16* __restrict__ x,
+__global__ void __launch_bounds__(direct_max_warps(BITS) * 32) qmv_generic_kernel(const __nv_bfloat16* __restrict__ x,
                                                    const uint32_t* __restrict__ w,
                                                    const uint16_t* __restrict__ scales,
                                                    const uint16_t* __restrict__ biases,
@@ -275,7 +335,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) qmv_generic_kernel(const __nv_
 // [0, E) or a source row outside [0, T) makes the row zero; ids that
 // decrease anywhere make every row zero; the first CTA reports the bits.
 template <int BITS>
-__global__ void __launch_bounds__(kMaxWarps * 32) gather_qmv_kernel(
+__global__ void __launch_bounds__(direct_max_warps(BITS) * 32) gather_qmv_kernel(
     const __nv_bfloat16* __restrict__ x, const uint32_t* __restrict__ w,
     const uint16_t* __restrict__ scales, const uint16_t* __restrict__ biases,
     const int32_t* __restrict__ ids, const int32_t* __restrict__ row_src,
@@ -744,7 +804,8 @@ cudaError_t launch_gather_qmv(const void* x, const uint32_t* w, const void* scal
                               int bits, int group, int32_t* status, cudaStream_t stream) {
     const int seg_k = bits == 8 ? 512 : 1024;
     const int nseg_g = (K + seg_k - 1) / seg_k;
-    const int passes = (nseg_g + kMaxWarps - 1) / kMaxWarps;
+    const int max_warps = direct_max_warps(bits);
+    const int passes = (nseg_g + max_warps - 1) / max_warps;
     const int warps = (nseg_g + passes - 1) / passes;
     const dim3 grid((N + kRows - 1) / kRows, B);
     const dim3 block(32 * warps);
@@ -756,6 +817,12 @@ cudaError_t launch_gather_qmv(const void* x, const uint32_t* w, const void* scal
     const long long sbst = (long long)N * (K / group);
     if (bits == 2)
         gather_qmv_kernel<2><<<grid, block, 0, stream>>>(xb, w, sb, bb, expert_ids, row_src, yb, T,
+                                                        B, E, K, N, group, wst, sbst, status);
+    else if (bits == 3)
+        gather_qmv_kernel<3><<<grid, block, 0, stream>>>(xb, w, sb, bb, expert_ids, row_src, yb, T,
+                                                        B, E, K, N, group, wst, sbst, status);
+    else if (bits == 6)
+        gather_qmv_kernel<6><<<grid, block, 0, stream>>>(xb, w, sb, bb, expert_ids, row_src, yb, T,
                                                         B, E, K, N, group, wst, sbst, status);
     else if (bits == 4)
         gather_qmv_kernel<4><<<grid, block, 0, stream>>>(xb, w, sb, bb, expert_ids, row_src, yb, T,
@@ -779,7 +846,8 @@ cudaError_t launch_qmv(const void* x, const uint32_t* w, const void* scales, con
     // a chunk's scales (and biases) are one bulk copy: a row's pairs must
     // fill whole 16-byte units
     const bool sb_rows16 = (K / group) % 8 == 0;
-    if (K % 512 == 0 && nseg <= kMaxStreamWarps && sb_aligned && sb_rows16) {
+    const bool stream_bits = bits == 2 || bits == 4 || bits == 8;
+    if (stream_bits && K % 512 == 0 && nseg <= kMaxStreamWarps && sb_aligned && sb_rows16) {
         StreamShape sh;
         sh.nseg = nseg;
         sh.phases = kTargetWarps / nseg > 1 ? kTargetWarps / nseg : 1;
@@ -811,12 +879,17 @@ cudaError_t launch_qmv(const void* x, const uint32_t* w, const void* scales, con
     const int seg_k = bits == 8 ? 512 : 1024;
     const int nseg_g = (K + seg_k - 1) / seg_k;
     // as few passes over the segments as the warp limit allows, spread evenly
-    const int passes = (nseg_g + kMaxWarps - 1) / kMaxWarps;
+    const int max_warps = direct_max_warps(bits);
+    const int passes = (nseg_g + max_warps - 1) / max_warps;
     const int warps = (nseg_g + passes - 1) / passes;
     const dim3 grid((N + kRows - 1) / kRows);
     const dim3 block(32 * warps);
     if (bits == 2)
         qmv_generic_kernel<2><<<grid, block, 0, stream>>>(xb, w, sb, bb, yb, K, N, group);
+    else if (bits == 3)
+        qmv_generic_kernel<3><<<grid, block, 0, stream>>>(xb, w, sb, bb, yb, K, N, group);
+    else if (bits == 6)
+        qmv_generic_kernel<6><<<grid, block, 0, stream>>>(xb, w, sb, bb, yb, K, N, group);
     else if (bits == 4)
         qmv_generic_kernel<4><<<grid, block, 0, stream>>>(xb, w, sb, bb, yb, K, N, group);
     else

@@ -1,8 +1,8 @@
 // Affine group-wise encoder: float weights -> packed codes, bf16 scales and
 // biases (the stored format of mlxcel issue #1536, Baseline section: "affine
-// 4-bit / group 64"; 8-bit codes are unsigned bytes; 2-bit codes are packed
-// sixteen per word like the 4-bit ones; groups of 32 and 128 consecutive k
-// use the same rule).
+// 4-bit / group 64"; 8-bit codes are unsigned bytes; 2-, 3- and 6-bit codes
+// continue the same little-endian bit stream per row, so 3- and 6-bit codes
+// may straddle words; groups of 32 and 128 consecutive k use the same rule).
 //
 // Per (row n, group g of GROUP consecutive k): mn, mx = the group's minimum and
 // maximum (-0 read as +0); s = bf16(RN(RN(mx - mn) / (2^bits - 1))) and
@@ -15,7 +15,7 @@
 // One warp per row: each lane holds 8 consecutive values of a 256-wide block
 // (two 16-byte loads), GROUP / 8 lanes make a group (4, 8 or 16), so a
 // group's minimum and maximum take two to four shuffle steps and each lane
-// packs its own codes (half a word at 2 bits, one word at 4, two at 8).
+// packs its own codes (2, 3, 4, 6 or 8 bytes at 2, 3, 4, 6 or 8 bits).
 // HBM-bound: 4 bytes read per weight, bits/8 written.
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -89,7 +89,17 @@ __global__ void __launch_bounds__(kEncWarps * 32) quantize_kernel(const float* _
                     r = fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(v[u][i], b), s)), 0.f), (float)kLevels);
                 q[i] = (uint32_t)r;
             }
-            if (BITS == 2) {
+            if (BITS == 3 || BITS == 6) {
+                // the lane's 8 codes are 3 or 6 whole bytes of the row's bit
+                // stream, starting at byte k * BITS / 8 (k is a multiple of 8)
+                uint64_t v = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v |= (uint64_t)q[i] << (BITS * i);
+                uint8_t* row = reinterpret_cast<uint8_t*>(codes) + (long long)n * (K / 8) * BITS;
+                uint8_t* dst = row + (long long)(k / 8) * BITS;
+#pragma unroll
+                for (int i = 0; i < BITS; ++i) dst[i] = (uint8_t)(v >> (8 * i));
+            } else if (BITS == 2) {
                 uint32_t half = 0;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) half |= q[i] << (2 * i);
@@ -127,6 +137,10 @@ cudaError_t launch_quantize(const float* W, uint32_t* codes, void* scales, void*
     case G:                                                                            \
         if (bits == 2)                                                                 \
             quantize_kernel<2, G><<<grid, block, 0, stream>>>(W, codes, s, b, N, K);   \
+        else if (bits == 3)                                                            \
+            quantize_kernel<3, G><<<grid, block, 0, stream>>>(W, codes, s, b, N, K);   \
+        else if (bits == 6)                                                            \
+            quantize_kernel<6, G><<<grid, block, 0, stream>>>(W, codes, s, b, N, K);   \
         else if (bits == 4)                                                            \
             quantize_kernel<4, G><<<grid, block, 0, stream>>>(W, codes, s, b, N, K);   \
         else                                                                           \

@@ -442,7 +442,7 @@ def secondary_measurements(mxq, dev, stream, hbm, bf16_peak, Ws):
         if M == 1:
             fn = lambda i: mxq.qmv(d.x[0], *d.copies[i % copies], bits, out=d.y[0],  # noqa: E731
                                    group_size=group)
-            kern = "qmv_stream_kernel"
+            kern = "qmv_stream_kernel" if bits in (2, 4, 8) else "qmv_generic_kernel"
         else:
             fn = lambda i: mxq.qmm(d.x, *d.copies[i % copies], bits, out=d.y,  # noqa: E731
                                    group_size=group)
@@ -470,10 +470,12 @@ def secondary_measurements(mxq, dev, stream, hbm, bf16_peak, Ws):
     out.append(dense_entry("pair qmv 8-bit", 1, 5120, 5120, 8, W_sq, copies=6))
     out.append(dense_entry("pair qmv 4-bit", 1, 5120, 5120, 4, W_sq, copies=6))
     out.append(dense_entry("pair qmm 8-bit", 128, 5120, 5120, 8, W_sq, copies=6))
-    # 2-bit codes and group sizes 32 and 128 on the decode and prefill shapes
-    # (same weights)
-    out.append(dense_entry("2-bit qmv", 1, 5120, 17408, 2, W_big, copies=6))
-    out.append(dense_entry("2-bit qmm prefill", 600, 5120, 17408, 2, W_big, copies=3))
+    # 2-, 3- and 6-bit codes and group sizes 32 and 128 on the decode and
+    # prefill shapes (same weights)
+    for bits in (2, 3, 6):
+        out.append(dense_entry("%d-bit qmv" % bits, 1, 5120, 17408, bits, W_big, copies=6))
+        out.append(dense_entry("%d-bit qmm prefill" % bits, 600, 5120, 17408, bits, W_big,
+                               copies=3))
     for group in (32, 128):
         out.append(dense_entry("group qmv", 1, 5120, 17408, 4, W_big, copies=6, group=group))
         out.append(dense_entry("group qmm prefill", 600, 5120, 17408, 4, W_big, copies=3,

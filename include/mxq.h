@@ -23,9 +23,12 @@
  *                                    profile table).  8-bit: four codes per
  *                                    word, lowest k in the lowest byte.
  *                                    2-bit: sixteen codes per word, lowest k
- *                                    in the lowest two bits (the bit width
- *                                    is a parameter of the kernels in issue
- *                                    #1536, Diagnosis item 3).
+ *                                    in the lowest two bits.  3- and 6-bit:
+ *                                    the same little-endian bit stream per
+ *                                    row, code k in bits [k*b, k*b + b), so
+ *                                    a code may straddle two words (the bit
+ *                                    width is a parameter of the kernels in
+ *                                    issue #1536, Diagnosis item 3).
  *   scales  bf16   [N, K/G]          s per (output row, group of G k)
  *   biases  bf16   [N, K/G]          b per (output row, group of G k)
  *   y       bf16   [M, N]            output, rounded once from fp32 (RNE)
@@ -74,11 +77,12 @@ typedef enum {
  * fp32 accumulation at every width is the fix that item names).
  *   x: bf16 [K]; y: bf16 [N]; w, scales, biases as above.
  *   dev_status: device int32 or NULL; receives 0 or MXQ_DEV_TIMEOUT.
- * Requirements: bits in {2, 4, 8}; group_size in {32, 64, 128}; K > 0,
- * K % 64 == 0 and K % group_size == 0; N > 0; x, w, y 16-byte aligned;
- * scales, biases 2-byte aligned.  The streaming kernel is used when
- * K % 512 == 0, K <= 20480, K / group_size % 8 == 0 and scales/biases are
- * 16-byte aligned; other shapes take a direct-load kernel (same result
+ * Requirements: bits in {2, 3, 4, 6, 8}; group_size in {32, 64, 128}; K > 0,
+ * K % 64 == 0 and K % group_size == 0 (K % 128 == 0 at 3 bits); N > 0;
+ * x, w, y 16-byte aligned; scales, biases 2-byte aligned.  The streaming
+ * kernel is used when bits is 2, 4 or 8, K % 512 == 0, K <= 20480,
+ * K / group_size % 8 == 0 and scales/biases are 16-byte aligned; other
+ * shapes take a direct-load kernel (same result
  * rule, different summation order).  The streaming kernel is launched as a
  * programmatic dependent launch: its CTAs may be placed on SMs while the
  * kernel before it on the stream finishes, but they read and write nothing
@@ -126,7 +130,8 @@ mxq_status mxq_qmm(const void* x, const uint32_t* w, const void* scales, const v
  * its expert's matrix (the same result rule, another summation order) and
  * use no workspace memory, though the size check still applies.
  * Requirements: B, E, T, N > 0; K > 0, K % 64 == 0, K % group_size == 0;
- * bits in {2, 4, 8}; group_size in {32, 64, 128}; x, w, y 16-byte aligned; the
+ * bits in {2, 3, 4, 6, 8} (K % 128 == 0 at 3 bits); group_size in
+ * {32, 64, 128}; x, w, y 16-byte aligned; the
  * rest aligned to type.                                                      */
 mxq_status mxq_gather_qmm(const void* x, const uint32_t* w, const void* scales,
                           const void* biases, const int32_t* expert_ids,
@@ -184,7 +189,8 @@ mxq_status mxq_gather_qmm_noalloc(const void* x, const uint32_t* w, const void* 
  * s = bf16(RN(RN(mx - mn) / (2^bits - 1))), b = bf16(mn), rounded to nearest
  * even; q = clamp(rint(RN(RN(w - b) / s)), 0, 2^bits - 1) with the stored
  * bf16 s and b, q = 0 when s == 0.  All decisions in binary32, so the codes
- * are reproducible bit for bit.  Requirements: bits in {2, 4, 8};
+ * are reproducible bit for bit.  Requirements: bits in {2, 3, 4, 6, 8}
+ * (K % 128 == 0 at 3 bits);
  * group_size in {32, 64, 128}; K > 0, K % 64 == 0, K % group_size == 0;
  * N > 0.                                                                    */
 mxq_status mxq_quantize(const float* w, uint32_t* codes, void* scales, void* biases, int N,

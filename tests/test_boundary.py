@@ -60,7 +60,8 @@ def qmv(L, x=FAKE, w=FAKE, s=FAKE, b=FAKE, y=FAKE, K=128, N=64, bits=4, group=64
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(bits=3), 1), (dict(bits=16), 1), (dict(bits=1), 1), (dict(group=16), 1),
+    (dict(bits=5), 1), (dict(bits=16), 1), (dict(bits=1), 1), (dict(bits=7), 1),
+    (dict(bits=3, K=192), 1), (dict(group=16), 1),
     (dict(group=48), 1), (dict(group=256), 1), (dict(group=0), 1), (dict(group=128, K=192), 1),
     (dict(group=32, K=96), 1), (dict(K=100), 1), (dict(K=0), 1), (dict(K=-64), 1), (dict(N=0), 1),
     (dict(x=None), 1), (dict(w=None), 1), (dict(s=None), 1), (dict(b=None), 1), (dict(y=None), 1),
@@ -92,7 +93,8 @@ def gather(L, T=8, B=8, E=2, K=128, N=64, bits=4, group=64, ids=FAKE, src=FAKE, 
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(T=0), 1), (dict(B=0), 1), (dict(E=0), 1), (dict(bits=6), 1), (dict(K=65), 1),
+    (dict(T=0), 1), (dict(B=0), 1), (dict(E=0), 1), (dict(bits=7), 1), (dict(K=65), 1),
+    (dict(bits=3, K=64), 1),
     (dict(group=64 + 32), 1), (dict(group=128, K=192), 1),
     (dict(ids=None), 1), (dict(src=None, T=5, B=8), 1),
     (dict(ids=ctypes.c_void_p(0x10002)), 2), (dict(ws=ctypes.c_void_p(0x10080)), 2),
@@ -145,7 +147,8 @@ def quantize(L, w=FAKE, codes=FAKE, s=FAKE, b=FAKE, N=16, K=128, bits=4, group=6
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(bits=3), 1), (dict(group=16), 1), (dict(group=256), 1), (dict(group=128, K=192), 1),
+    (dict(bits=5), 1), (dict(bits=3, K=64), 1), (dict(group=16), 1), (dict(group=256), 1),
+    (dict(group=128, K=192), 1),
     (dict(K=100), 1), (dict(N=0), 1), (dict(w=None), 1),
     (dict(codes=None), 1), (dict(w=FAKE_ODD), 2), (dict(codes=FAKE_ODD), 2),
     (dict(s=ctypes.c_void_p(0x10001)), 2),
