@@ -672,7 +672,12 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 2) * 32, 1)
     const int phase = warp / sh.nseg;
     const int k0 = seg * 1024 + lane * 32;   // this lane's 32 values
     const bool active = k0 < K;
+    // 3- and 6-bit codes are cut out of the row's bit stream into floats
+    // 1 + q * 2^-7 (the direct-load kernel's arithmetic), so those widths keep
+    // the activations as fp32 pairs; the others use exact integer planes
+    constexpr bool kFloatCodes = BITS == 3 || BITS == 6;
     XPlanes P;
+    float2 x2[16];
     float X = 0.f;          // sum of the lane's activations (bias term)
     float xscale = 0.f;     // 2^(emax - 149)
     {
@@ -695,9 +700,14 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 2) * 32, 1)
             xf[2 * j + 1] = __uint_as_float(u[j] & 0xFFFF0000u);
             X += xf[2 * j] + xf[2 * j + 1];
         }
-        const int emax = make_planes<BITS>(xf, P);
-        // 2^(emax - 149): a normal float from emax = 23 on, else subnormal
-        xscale = __int_as_float(emax >= 23 ? (emax - 22) << 23 : 1 << emax);
+        if (kFloatCodes) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) x2[j] = make_float2(xf[2 * j], xf[2 * j + 1]);
+        } else {
+            const int emax = make_planes<BITS>(xf, P);
+            // 2^(emax - 149): a normal float from emax = 23 on, else subnormal
+            xscale = __int_as_float(emax >= 23 ? (emax - 22) << 23 : 1 << emax);
+        }
     }
     const int g = k0 / group;
     const uint32_t lane_code_off = (uint32_t)(seg * 1024 + lane * 32) * BITS / 8;
@@ -719,12 +729,32 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 2) * 32, 1)
             const int r = phase + q * sh.phases;   // row within the chunk
             part[q] = 0.f;
             if (have && active && r < rows) {
-                const float A = lane_dot_int<BITS>(sbase + r * sh.row_bytes + lane_code_off, P);
+                const uint32_t caddr = sbase + r * sh.row_bytes + lane_code_off;
+                float xq;  // sum over the lane's codes of x_k * q_k
+                if (kFloatCodes) {
+                    uint32_t wd[6] = {0u, 0u, 0u, 0u, 0u, 0u};
+                    if (BITS == 3) {
+                        // 12 bytes at a 4-byte aligned offset
+#pragma unroll
+                        for (int i = 0; i < 3; ++i)
+                            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(wd[i]) : "r"(caddr + 4 * i));
+                    } else {
+                        // 24 bytes at an 8-byte aligned offset
+#pragma unroll
+                        for (int i = 0; i < 3; ++i)
+                            asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];"
+                                         : "=r"(wd[2 * i]), "=r"(wd[2 * i + 1])
+                                         : "r"(caddr + 8 * i));
+                    }
+                    xq = (dot_chunk_stream<BITS>(wd, x2) - X) * 128.f;
+                } else {
+                    xq = lane_dot_int<BITS>(caddr, P) * xscale;
+                }
                 uint16_t sv, bv;
                 asm volatile("ld.shared.u16 %0, [%1];" : "=h"(sv) : "r"(s_off + (r * groups + g) * 2));
                 asm volatile("ld.shared.u16 %0, [%1];" : "=h"(bv) : "r"(b_off + (r * groups + g) * 2));
                 const float s = bf16_bits_to_float(sv), b = bf16_bits_to_float(bv);
-                part[q] = fmaf(s, A * xscale, b * X);
+                part[q] = fmaf(s, xq, b * X);
             }
         }
         // all shared reads of this stage are consumed: hand it back
@@ -846,7 +876,7 @@ cudaError_t launch_qmv(const void* x, const uint32_t* w, const void* scales, con
     // a chunk's scales (and biases) are one bulk copy: a row's pairs must
     // fill whole 16-byte units
     const bool sb_rows16 = (K / group) % 8 == 0;
-    const bool stream_bits = bits == 2 || bits == 4 || bits == 8;
+    const bool stream_bits = true;  // every width (3 and 6 bits: float code path)
     if (stream_bits && K % 512 == 0 && nseg <= kMaxStreamWarps && sb_aligned && sb_rows16) {
         StreamShape sh;
         sh.nseg = nseg;
@@ -872,6 +902,10 @@ cudaError_t launch_qmv(const void* x, const uint32_t* w, const void* scales, con
         if (sh.nchunks > N) sh.nchunks = N;
         if (bits == 2)
             return launch_stream<2>(xb, w, sb, bb, yb, K, N, group, rpw, sh, grid, status, stream);
+        if (bits == 3)
+            return launch_stream<3>(xb, w, sb, bb, yb, K, N, group, rpw, sh, grid, status, stream);
+        if (bits == 6)
+            return launch_stream<6>(xb, w, sb, bb, yb, K, N, group, rpw, sh, grid, status, stream);
         return bits == 4
                    ? launch_stream<4>(xb, w, sb, bb, yb, K, N, group, rpw, sh, grid, status, stream)
                    : launch_stream<8>(xb, w, sb, bb, yb, K, N, group, rpw, sh, grid, status, stream);

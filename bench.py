@@ -442,7 +442,7 @@ def secondary_measurements(mxq, dev, stream, hbm, bf16_peak, Ws):
         if M == 1:
             fn = lambda i: mxq.qmv(d.x[0], *d.copies[i % copies], bits, out=d.y[0],  # noqa: E731
                                    group_size=group)
-            kern = "qmv_stream_kernel" if bits in (2, 4, 8) else "qmv_generic_kernel"
+            kern = "qmv_stream_kernel"
         else:
             fn = lambda i: mxq.qmm(d.x, *d.copies[i % copies], bits, out=d.y,  # noqa: E731
                                    group_size=group)
