@@ -59,6 +59,8 @@ def _load():
                                           P, P, ctypes.c_longlong, P, P]
             lib.oracle_points.restype = I
             lib.oracle_quantize.argtypes = [P, I, I, I, I, P, P, P]
+            lib.oracle_qmm_kn.argtypes = [P, P, P, P, I, I, I, I, I, P, P]
+            lib.oracle_qmm_kn.restype = I
             _lib = lib
     return _lib
 
@@ -100,6 +102,23 @@ def qmm(x, w, scales, biases, M: int, K: int, N: int, bits: int, group: int = 64
                             y.ctypes.data_as(ctypes.c_void_p), bnd.ctypes.data_as(ctypes.c_void_p))
     if rc:
         raise MemoryError("oracle_qmm failed")
+    return y, bnd
+
+
+def qmm_kn(x, w, scales, biases, M: int, K: int, N: int, bits: int, group: int = 64):
+    """The [K, N] operand layout: w uint32 [K, N*bits/32] (codes along n),
+    scales/biases bf16 bits [K, N/group]; y[M, N] and bound[M, N] in f64."""
+    x, px = _c(x, np.uint16)
+    w, pw = _c(w, np.uint32)
+    s, ps = _c(scales, np.uint16)
+    b, pb = _c(biases, np.uint16)
+    y = np.empty((M, N), dtype=np.float64)
+    bnd = np.empty((M, N), dtype=np.float64)
+    rc = _load().oracle_qmm_kn(px, pw, ps, pb, M, K, N, bits, group,
+                               y.ctypes.data_as(ctypes.c_void_p),
+                               bnd.ctypes.data_as(ctypes.c_void_p))
+    if rc:
+        raise MemoryError("oracle_qmm_kn failed")
     return y, bnd
 
 

@@ -149,6 +149,54 @@ int oracle_qmv(const uint16_t* x, const uint32_t* w, const uint16_t* scales,
     return oracle_qmm(x, w, scales, biases, 1, K, N, bits, group, y, bound);
 }
 
+/* The other operand layout (PR #1562, What changed: the grouped GEMM is
+ * checked for both operand layouts): w is stored [K, N], row k holding the
+ * codes of all N outputs as the same little-endian bit stream (code n of row
+ * k in bits [n*b, n*b + b)), and the groups run along n:
+ *
+ *   w^[k,n] = s[k, n/G] * q[k,n] + b[k, n/G]      scales, biases [K, N/G]
+ *   y[m,n]  = sum_k x[m,k] * w^[k,n]              (in f64, k in order)
+ *
+ * One output column at a time: dequantise column n into a scratch vector,
+ * then the f64 dot products. */
+int oracle_qmm_kn(const uint16_t* x, const uint32_t* w, const uint16_t* scales,
+                  const uint16_t* biases, int M, int K, int N, int bits, int group,
+                  double* y, double* bound) {
+    long long wpr = (long long)N * bits / 32;  /* words per row k */
+    int ng = N / group;
+    int fail = 0;
+#pragma omp parallel
+    {
+        double* wcol = (double*)malloc(sizeof(double) * (K > 0 ? K : 1));
+        if (!wcol) {
+#pragma omp atomic write
+            fail = 1;
+        } else {
+#pragma omp for schedule(dynamic, 4)
+            for (int n = 0; n < N; ++n) {
+                for (int k = 0; k < K; ++k) {
+                    double s = bf16_to_f64(scales[(long long)k * ng + n / group]);
+                    double b = bf16_to_f64(biases[(long long)k * ng + n / group]);
+                    wcol[k] = s * (double)code_at(w, wpr, k, n, bits) + b;
+                }
+                for (int m = 0; m < M; ++m) {
+                    const uint16_t* xr = x + (long long)m * K;
+                    double acc = 0.0, bnd = 0.0;
+                    for (int k = 0; k < K; ++k) {
+                        double t = bf16_to_f64(xr[k]) * wcol[k];
+                        acc += t;
+                        bnd += fabs(t);
+                    }
+                    y[(long long)m * N + n] = acc;
+                    if (bound) bound[(long long)m * N + n] = bnd;
+                }
+            }
+            free(wcol);
+        }
+    }
+    return fail;
+}
+
 /* Sorted-MoE variant: y[B, N]; row r uses expert expert_ids[r] and activation
  * row row_src[r] (row_src NULL means row r).  w is [E, N, K*bits/32],
  * scales/biases [E, N, K/G].  Rows whose expert id is out of [0, E) get 0. */

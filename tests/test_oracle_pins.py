@@ -638,3 +638,89 @@ def test_quantize_hand_example_group_sizes(group):
     changed = np.nonzero(s2[0] != s[0])[0]
     assert list(changed) == [1]
     assert np.array_equal(b2, b)
+
+
+# ---- the [K, N] operand layout (PR #1562, What changed: both operand
+# layouts): row k holds the codes of every output n, groups run along n
+
+
+def _kn_case(K, N, bits, group, seed):
+    rng = np.random.default_rng(seed)
+    q = rng.integers(0, 1 << bits, size=(K, N), dtype=np.uint8)
+    w = synth.pack_codes(q, bits)                      # [K, N*bits/32]
+    g = np.arange(N // group)[None, :]
+    k = np.arange(K)[:, None]
+    s_vals = (2.0 ** ((k + 2 * g) % 6 - 5)).astype(np.float32)
+    b_vals = ((g + 1) * 0.25 - (k % 3) * 0.5).astype(np.float32)
+    return q, w, s_vals, b_vals
+
+
+@pytest.mark.parametrize("group", [32, 64, 128])
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_kn_one_hot_selects_weight(bits, group):
+    # x = e_k picks row k: y[n] = s[k, n/G] q[k, n] + b[k, n/G], so a code
+    # read from the wrong row or column, or a scale from the wrong (row,
+    # group), shows
+    K, N = 7, 384
+    q, w, s_vals, b_vals = _kn_case(K, N, bits, group, 80 + bits + group)
+    s, b = _bf16_exact(s_vals), _bf16_exact(b_vals)
+    for k in range(K):
+        x = np.zeros((1, K), np.float32)
+        x[0, k] = 1.0
+        y, _ = oracle.qmm_kn(_bf16_exact(x), w, s, b, 1, K, N, bits, group)
+        gidx = np.arange(N) // group
+        want = s_vals[k, gidx].astype(np.float64) * q[k] + b_vals[k, gidx]
+        assert np.array_equal(y[0], want), k
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_kn_uniform_scales_equal_transposed_layout(bits):
+    # with one scale and bias everywhere the two layouts hold the same
+    # matrix: the [K, N] result equals the [N, K] result on the transposed
+    # codes
+    rng = np.random.default_rng(90 + bits)
+    M, K, N = 3, 128, 192
+    q = rng.integers(0, 1 << bits, size=(K, N), dtype=np.uint8)
+    x = synth.activations(M, K, seed=91)
+    y_kn, b_kn = oracle.qmm_kn(x, synth.pack_codes(q, bits),
+                               _bf16_exact(np.full((K, N // 64), 0.125, np.float32)),
+                               _bf16_exact(np.full((K, N // 64), -0.5, np.float32)),
+                               M, K, N, bits)
+    y_nk, b_nk = oracle.qmm(x, synth.pack_codes(np.ascontiguousarray(q.T), bits),
+                            _bf16_exact(np.full((N, K // 64), 0.125, np.float32)),
+                            _bf16_exact(np.full((N, K // 64), -0.5, np.float32)),
+                            M, K, N, bits)
+    assert np.array_equal(y_kn, y_nk)
+    assert np.array_equal(b_kn, b_nk)
+
+
+@pytest.mark.parametrize("group", [32, 64])
+def test_kn_zero_scale_closed_form(group):
+    # s = 0: y[m, n] = sum_k x[m, k] b[k, n/G], exact for integer x
+    rng = np.random.default_rng(95)
+    M, K, N = 2, 40, 128
+    x = rng.integers(-4, 5, size=(M, K)).astype(np.float32)
+    bv = (rng.integers(-8, 9, size=(K, N // group)) / 4.0).astype(np.float32)
+    q = rng.integers(0, 16, size=(K, N), dtype=np.uint8)
+    y, _ = oracle.qmm_kn(_bf16_exact(x), synth.pack_codes(q, 4),
+                         _bf16_exact(np.zeros((K, N // group), np.float32)), _bf16_exact(bv),
+                         M, K, N, 4, group)
+    want = x.astype(np.float64) @ np.repeat(bv, group, axis=1).astype(np.float64)
+    assert np.array_equal(y, want)
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("group", [32, 64])
+def test_kn_brute_force_exact(bits, group):
+    M, K, N = 2, 5, 64
+    q, w, s_vals, b_vals = _kn_case(K, N, bits, group, 97 + bits)
+    s, b = _bf16_exact(s_vals), _bf16_exact(b_vals)
+    x = synth.activations(M, K, seed=98)
+    y, bnd = oracle.qmm_kn(x, w, s, b, M, K, N, bits, group)
+    for n in range(N):
+        col = [_row_codes(w[k], N, bits)[n] for k in range(K)]
+        for m in range(M):
+            exact = sum((_bf16_fraction(x[m, k]) *
+                         (_bf16_fraction(s[k, n // group]) * col[k] +
+                          _bf16_fraction(b[k, n // group])) for k in range(K)), Fraction(0))
+            assert abs(y[m, n] - float(exact)) <= 1e-12 * bnd[m, n] + 1e-300, (m, n)
