@@ -30,6 +30,7 @@ __all__ = [
     "lib",
     "qmv",
     "qmm",
+    "qmv_kn",
     "gather_qmm",
     "gather_workspace_bytes",
     "gather_qmm_noalloc",
@@ -66,6 +67,7 @@ NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024  # MXQ_NOALLOC_SCRATCH_BYTES
 EXPORTED_SYMBOLS = (
     "mxq_qmv",
     "mxq_qmm",
+    "mxq_qmv_kn",
     "mxq_gather_qmm",
     "mxq_gather_workspace_bytes",
     "mxq_gather_qmm_noalloc",
@@ -99,6 +101,8 @@ def lib():
         L.mxq_qmv.restype = I
         L.mxq_qmm.argtypes = [P, P, P, P, P, I, I, I, I, I, P, P]
         L.mxq_qmm.restype = I
+        L.mxq_qmv_kn.argtypes = [P, P, P, P, P, I, I, I, I, P, P]
+        L.mxq_qmv_kn.restype = I
         L.mxq_gather_qmm.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, Z, P, P]
         L.mxq_gather_qmm.restype = I
         L.mxq_gather_qmm_noalloc.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P]
@@ -200,6 +204,38 @@ def qmv(x, w, scales, biases, bits: int, out=None, dev_status=None, stream=None,
         _require(dev_status, "dev_status", (torch.int32,), x.device)
     _check(lib().mxq_qmv(_ptr(x), _ptr(w), _ptr(scales), _ptr(biases), _ptr(out), K, N, bits,
                          group_size, _ptr(dev_status), _stream(stream)), "mxq_qmv")
+    return out
+
+
+def qmv_kn(x, w, scales, biases, bits: int, out=None, dev_status=None, stream=None,
+           group_size: int = 64):
+    """Decode GEMV with w stored [K, N] (codes and groups along n):
+    ``y[n] = sum_k x[k] * (s[k, n/G] q[k, n] + b[k, n/G])``; ``w`` int32
+    [K, N*bits/32], ``scales``/``biases`` bf16 [K, N/G], ``x`` bf16 [K]."""
+    torch = _torch()
+    _require(x, "x", (torch.bfloat16,))
+    if x.dim() != 1:
+        raise ValueError("x must be 1-D [K]")
+    K = x.shape[0]
+    _require(w, "w", _code_dtypes(), x.device)
+    _require(scales, "scales", (torch.bfloat16,), x.device)
+    _require(biases, "biases", (torch.bfloat16,), x.device)
+    if w.dim() != 2 or w.shape[0] != K:
+        raise ValueError("w must be [K, N*bits/32]")
+    N = w.shape[1] * 32 // bits
+    if group_size <= 0:
+        raise ValueError("group_size must be positive")
+    for t, name in ((scales, "scales"), (biases, "biases")):
+        if tuple(t.shape) != (K, N // group_size):
+            raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape),
+                                                               (K, N // group_size)))
+    if out is None:
+        out = torch.empty((N,), dtype=torch.bfloat16, device=x.device)
+    _require(out, "out", (torch.bfloat16,), x.device)
+    if dev_status is not None:
+        _require(dev_status, "dev_status", (torch.int32,), x.device)
+    _check(lib().mxq_qmv_kn(_ptr(x), _ptr(w), _ptr(scales), _ptr(biases), _ptr(out), K, N, bits,
+                            group_size, _ptr(dev_status), _stream(stream)), "mxq_qmv_kn")
     return out
 
 

@@ -202,6 +202,27 @@ mxq_status mxq_qmm(const void* x, const uint32_t* w, const void* scales, const v
     return err == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA;
 }
 
+mxq_status mxq_qmv_kn(const void* x, const uint32_t* w, const void* scales, const void* biases,
+                      void* y, int K, int N, int bits, int group_size, int32_t* dev_status,
+                      void* stream) {
+    if (bits == 3 || bits == 6) return MXQ_ERR_UNSUPPORTED;
+    if (bits != 2 && bits != 4 && bits != 8) return MXQ_ERR_INVALID_ARG;
+    if (group_size != 32 && group_size != 64 && group_size != 128) return MXQ_ERR_INVALID_ARG;
+    if (K <= 0 || N <= 0 || N % 64 != 0 || N % group_size != 0) return MXQ_ERR_INVALID_ARG;
+    if (!x || !w || !scales || !biases || !y) return MXQ_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 16) || !aligned(scales, 2) ||
+        !aligned(biases, 2) || !aligned(dev_status, 4))
+        return MXQ_ERR_MISALIGNED;
+    int sms = 0;
+    mxq_status st = check_device(&sms);
+    if (st != MXQ_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dev_status && cudaMemsetAsync(dev_status, 0, sizeof(int32_t), s) != cudaSuccess)
+        return MXQ_ERR_CUDA;
+    cudaError_t err = mxq::launch_qmv_kn(x, w, scales, biases, y, K, N, bits, group_size, sms, s);
+    return err == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA;
+}
+
 mxq_status mxq_quantize(const float* w, uint32_t* codes, void* scales, void* biases, int N,
                         int K, int bits, int group_size, void* stream) {
     mxq_status st = check_common(K, N, bits, group_size);

@@ -78,6 +78,11 @@ cudaError_t launch_gather_qmv(const void* x, const uint32_t* w, const void* scal
 cudaError_t launch_quantize(const float* W, uint32_t* codes, void* scales, void* biases, int N,
                             int K, int bits, int group, cudaStream_t stream);
 
+// Decode GEMV for w stored [K, N] (codes and groups along n), 2/4/8-bit.
+cudaError_t launch_qmv_kn(const void* x, const uint32_t* w, const void* scales, const void* biases,
+                          void* y, int K, int N, int bits, int group, int sms,
+                          cudaStream_t stream);
+
 cudaError_t launch_gather_rows(const void* x, const int32_t* row_src, int T, int B, int K,
                                void* x_sorted, cudaStream_t stream);
 

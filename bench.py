@@ -481,6 +481,27 @@ def secondary_measurements(mxq, dev, stream, hbm, bf16_peak, Ws):
         out.append(dense_entry("group qmm prefill", 600, 5120, 17408, 4, W_big, copies=3,
                                group=group))
 
+    # the decode GEMV for the [K, N] operand layout (codes and groups along n)
+    for (K, N) in ((5120, 17408), (17408, 5120)):
+        Wkn = synth.dense_weights(K, N, seed=0)
+        qkn = synth.quantize(Wkn, 4)
+        kn_copies = [(dev_codes(qkn.w, dev), dev_bf16(qkn.scales, dev), dev_bf16(qkn.biases, dev))]
+        kn_copies += [tuple(t.clone() for t in kn_copies[0]) for _ in range(5)]
+        xkn = dev_bf16(synth.activations(1, K, seed=1), dev)[0]
+        ykn = torch.empty((N,), dtype=torch.bfloat16, device=dev)
+        fnk = lambda i: mxq.qmv_kn(xkn, *kn_copies[i % 6], 4, out=ykn)  # noqa: E731
+        for i in range(5):
+            fnk(i)
+        tk, _ = time_launches(fnk, iters, stream)
+        nbk = qmv_bytes(K, N, 4)
+        out.append({"name": "qmv [K, N] layout", "kernel": "qmv_kn_kernel", "M": 1, "K": K,
+                    "N": N, "bits": 4, "group": 64, "us": tk * 1e6,
+                    "TFLOPS": 2.0 * K * N / tk / 1e12, "GB_s": nbk / tk / 1e9,
+                    "frac_hbm": nbk / tk / 1e9 / hbm, "bound": "hbm",
+                    "frac_roofline": nbk / tk / 1e9 / hbm, "tokens_per_s": 1 / tk})
+        del kn_copies, Wkn, qkn
+    torch.cuda.empty_cache()
+
     # the encoder on the prefill weight shape (float32 in, 4-bit codes out)
     N_q, K_q = 17408, 5120
     Wq = [torch.randn((N_q, K_q), device=dev) * 0.02 for _ in range(2)]

@@ -91,6 +91,24 @@ mxq_status mxq_qmv(const void* x, const uint32_t* w, const void* scales, const v
                    void* y, int K, int N, int bits, int group_size, int32_t* dev_status,
                    void* stream);
 
+/* Decode GEMV for the other operand layout (mlxcel PR #1562, What changed:
+ * the grouped GEMM is checked for both operand layouts): w is stored [K, N],
+ * row k holding the codes of every output n as the same little-endian bit
+ * stream (code n in bits [n*b, n*b + b) of row k), and each group is G
+ * consecutive n of one row:
+ *   w:      uint32 [K, N*bits/32]
+ *   scales, biases: bf16 [K, N/G]
+ *   y[n] = sum_k x[k] * (s[k, n/G] * q[k, n] + b[k, n/G])   (fp32 accumulation)
+ *   x: bf16 [K]; y: bf16 [N].
+ * Requirements: bits in {2, 4, 8} (3 and 6: MXQ_ERR_UNSUPPORTED); group_size
+ * in {32, 64, 128}; K > 0; N > 0, N % 64 == 0 and N % group_size == 0;
+ * x, w, y 16-byte aligned; scales, biases 2-byte aligned.  `dev_status`
+ * (device int32, may be NULL) receives 0.  Up to 8 CTAs of a thread-block
+ * cluster split K and add their partials in rank order: deterministic.     */
+mxq_status mxq_qmv_kn(const void* x, const uint32_t* w, const void* scales, const void* biases,
+                      void* y, int K, int N, int bits, int group_size, int32_t* dev_status,
+                      void* stream);
+
 /* Prefill GEMM, y[M, N] = x[M, K] . w^[N, K]^T (mlxcel issue #1536, Baseline
  * profile table and Diagnosis item 4: the qmm_naive kernel).  Runs on the
  * tcgen05 tensor cores: codes are dequantised to bf16 into tensor memory

@@ -30,8 +30,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("mxq_qmv", "mxq_qmm", "mxq_gather_qmm", "mxq_gather_workspace_bytes",
-              "mxq_gather_qmm_noalloc", "mxq_status_string", "mxq_version"):
+    for n in ("mxq_qmv", "mxq_qmm", "mxq_qmv_kn", "mxq_gather_qmm", "mxq_gather_workspace_bytes",
+              "mxq_gather_qmm_noalloc", "mxq_quantize", "mxq_status_string", "mxq_version"):
         assert n in names
 
 
@@ -70,6 +70,20 @@ def qmv(L, x=FAKE, w=FAKE, s=FAKE, b=FAKE, y=FAKE, K=128, N=64, bits=4, group=64
 ])
 def test_qmv_argument_checks(L, kw, code):
     assert qmv(L, **kw) == code
+
+
+def qmv_kn(L, K=100, N=128, bits=4, group=64, x=FAKE, w=FAKE, y=FAKE, status=None):
+    return L.mxq_qmv_kn(x, w, FAKE, FAKE, y, K, N, bits, group, status, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(bits=3), 3), (dict(bits=6), 3), (dict(bits=5), 1), (dict(group=16), 1),
+    (dict(N=96), 1), (dict(N=0), 1), (dict(K=0), 1), (dict(N=64, group=128), 1),
+    (dict(x=None), 1), (dict(w=None), 1), (dict(y=FAKE_ODD), 2), (dict(w=FAKE_ODD), 2),
+    (dict(status=ctypes.c_void_p(0x10002)), 2),
+])
+def test_qmv_kn_argument_checks(L, kw, code):
+    assert qmv_kn(L, **kw) == code
 
 
 def qmm(L, M=16, K=128, N=64, bits=4, group=64, status=None, x=FAKE, y=FAKE):
