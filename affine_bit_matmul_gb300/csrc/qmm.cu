@@ -55,7 +55,7 @@ constexpr int kMmaWarp = 9;          // TMEM owner, MMA issue
 constexpr int kXWarp0 = 10;          // activation TMA
 constexpr int kThreads = 11 * 32;
 constexpr int kTileN = 128;          // rows of w per CTA (MMA M)
-constexpr int kBK = 128;             // K per dequant/MMA stage: two 64-wide groups
+constexpr int kBK = 128;             // K per dequant/MMA stage: two 64-wide halves
 constexpr int kHalfK = 64;           // K per activation slot (one 128-byte swizzle atom)
 constexpr int kMaxCodeStages = 8;    // code slots
 // A code slot holds 256 bytes of each of the 128 w rows (the TMA engine

@@ -431,7 +431,8 @@ def run_mxq(args):
 
 
 def secondary_measurements(mxq, dev, stream, hbm, bf16_peak, Ws):
-    """Prefill GEMM, M sweep, sorted-MoE gather and the 4/8-bit pair."""
+    """Prefill GEMM, M sweep, the 4/8-bit pair, other bit widths and group sizes,
+    the [K, N] layout GEMV, the encoder and the sorted-MoE gather."""
     import torch
 
     out = []
