@@ -147,10 +147,12 @@ mxq_status mxq_qmm(const void* x, const uint32_t* w, const void* scales, const v
  * Calls with at most 32 rows (a decode step) run one GEMV per row against
  * its expert's matrix (the same result rule, another summation order) and
  * use no workspace memory, though the size check still applies.
+ * Larger calls build a tile table on the GPU and run the tensor-core GEMM:
+ * at 2 and 4 bits two persistent CTAs per SM take tiles from a counter; at
+ * 3, 6 and 8 bits one CTA computes each tile.
  * Requirements: B, E, T, N > 0; K > 0, K % 64 == 0, K % group_size == 0;
  * bits in {2, 3, 4, 6, 8} (K % 128 == 0 at 3 bits); group_size in
- * {32, 64, 128}; x, w, y 16-byte aligned; the
- * rest aligned to type.                                                      */
+ * {32, 64, 128}; x, w, y 16-byte aligned; the rest aligned to type.          */
 mxq_status mxq_gather_qmm(const void* x, const uint32_t* w, const void* scales,
                           const void* biases, const int32_t* expert_ids,
                           const int32_t* row_src, void* y, int T, int B, int E, int K, int N,
