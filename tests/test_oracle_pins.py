@@ -724,3 +724,21 @@ def test_kn_brute_force_exact(bits, group):
                          (_bf16_fraction(s[k, n // group]) * col[k] +
                           _bf16_fraction(b[k, n // group])) for k in range(K)), Fraction(0))
             assert abs(y[m, n] - float(exact)) <= 1e-12 * bnd[m, n] + 1e-300, (m, n)
+
+
+def test_quantize_writes_golden_stream_words():
+    # weights on an exact grid whose codes are known: the encoder's packing of
+    # straddling 3- and 6-bit codes must give the hand-packed words
+    streams = {(b, tuple(c)): w for b, w, c in _golden_streams()}
+    j = np.arange(64)
+    # 3-bit: -1 + 0.25 * (j % 8): min -1, range / 7 = 0.25 exactly, codes j % 8
+    W3 = (-1.0 + 0.25 * (j % 8)).astype(np.float32)[None, :]
+    codes, s, b = oracle.quantize(W3, 3)
+    assert s[0, 0] == synth.f32_to_bf16_bits(np.float32(0.25)) and b[0, 0] == 0xBF80
+    want = streams[(3, tuple(list(range(8)) * 4))]
+    assert list(codes[0, :3]) == want and list(codes[0, 3:6]) == want
+    # 6-bit: -1 + 0.0625 * j: range / 63 = 0.0625 exactly, codes j
+    W6 = (-1.0 + 0.0625 * j).astype(np.float32)[None, :]
+    codes, s, b = oracle.quantize(W6, 6)
+    assert s[0, 0] == synth.f32_to_bf16_bits(np.float32(0.0625)) and b[0, 0] == 0xBF80
+    assert list(codes[0, :3]) == streams[(6, tuple(range(16)))]
