@@ -142,11 +142,20 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else None
 
 
-def _stream(stream):
+def _launch_on(device, stream):
+    """The device context and raw stream handle for a call on ``device``.
+
+    The library launches on the CUDA device that is current when it is
+    called, so every wrapper makes the tensors' device current for the call;
+    ``stream`` (default: that device's current stream) must belong to the
+    same device, else the launch would pair one device's pointers with
+    another device's stream."""
     torch = _torch()
     if stream is None:
-        stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+        stream = torch.cuda.current_stream(device)
+    elif stream.device != device:
+        raise ValueError("stream is on %s but the tensors are on %s" % (stream.device, device))
+    return torch.cuda.device(device), ctypes.c_void_p(stream.cuda_stream)
 
 
 def _require(t, name, dtypes, device=None):
@@ -202,8 +211,10 @@ def qmv(x, w, scales, biases, bits: int, out=None, dev_status=None, stream=None,
     _require(out, "out", (torch.bfloat16,), x.device)
     if dev_status is not None:
         _require(dev_status, "dev_status", (torch.int32,), x.device)
-    _check(lib().mxq_qmv(_ptr(x), _ptr(w), _ptr(scales), _ptr(biases), _ptr(out), K, N, bits,
-                         group_size, _ptr(dev_status), _stream(stream)), "mxq_qmv")
+    ctx, st = _launch_on(x.device, stream)
+    with ctx:
+        _check(lib().mxq_qmv(_ptr(x), _ptr(w), _ptr(scales), _ptr(biases), _ptr(out), K, N, bits,
+                             group_size, _ptr(dev_status), st), "mxq_qmv")
     return out
 
 
@@ -234,8 +245,10 @@ def qmv_kn(x, w, scales, biases, bits: int, out=None, dev_status=None, stream=No
     _require(out, "out", (torch.bfloat16,), x.device)
     if dev_status is not None:
         _require(dev_status, "dev_status", (torch.int32,), x.device)
-    _check(lib().mxq_qmv_kn(_ptr(x), _ptr(w), _ptr(scales), _ptr(biases), _ptr(out), K, N, bits,
-                            group_size, _ptr(dev_status), _stream(stream)), "mxq_qmv_kn")
+    ctx, st = _launch_on(x.device, stream)
+    with ctx:
+        _check(lib().mxq_qmv_kn(_ptr(x), _ptr(w), _ptr(scales), _ptr(biases), _ptr(out), K, N,
+                                bits, group_size, _ptr(dev_status), st), "mxq_qmv_kn")
     return out
 
 
@@ -258,8 +271,10 @@ def qmm(x, w, scales, biases, bits: int, out=None, dev_status=None, stream=None,
     _require(out, "out", (torch.bfloat16,), x.device)
     if dev_status is not None:
         _require(dev_status, "dev_status", (torch.int32,), x.device)
-    _check(lib().mxq_qmm(_ptr(x), _ptr(w), _ptr(scales), _ptr(biases), _ptr(out), M, K, N, bits,
-                         group_size, _ptr(dev_status), _stream(stream)), "mxq_qmm")
+    ctx, st = _launch_on(x.device, stream)
+    with ctx:
+        _check(lib().mxq_qmm(_ptr(x), _ptr(w), _ptr(scales), _ptr(biases), _ptr(out), M, K, N,
+                             bits, group_size, _ptr(dev_status), st), "mxq_qmm")
     return out
 
 
@@ -283,8 +298,10 @@ def quantize(w, bits: int, codes=None, scales=None, biases=None, stream=None,
     if biases is None:
         biases = torch.empty((N, K // group_size), dtype=torch.bfloat16, device=dev)
     _check_weights(codes, scales, biases, N, K, bits, dev, group_size=group_size)
-    _check(lib().mxq_quantize(_ptr(w), _ptr(codes), _ptr(scales), _ptr(biases), N, K, bits,
-                              group_size, _stream(stream)), "mxq_quantize")
+    ctx, st = _launch_on(dev, stream)
+    with ctx:
+        _check(lib().mxq_quantize(_ptr(w), _ptr(codes), _ptr(scales), _ptr(biases), N, K, bits,
+                                  group_size, st), "mxq_quantize")
     return codes, scales, biases
 
 
@@ -318,10 +335,12 @@ def gather_qmm_noalloc(x, w, scales, biases, expert_ids, row_src, bits: int, out
         raise ValueError("out has shape %s, expected %s" % (tuple(out.shape), (B, N)))
     if dev_status is not None:
         _require(dev_status, "dev_status", (torch.int32,), x.device)
-    _check(lib().mxq_gather_qmm_noalloc(_ptr(x), _ptr(w), _ptr(scales), _ptr(biases),
-                                        _ptr(expert_ids), _ptr(row_src), _ptr(out), T, B, E, K,
-                                        N, bits, group_size, _ptr(dev_status), _stream(stream)),
-           "mxq_gather_qmm_noalloc")
+    ctx, st = _launch_on(x.device, stream)
+    with ctx:
+        _check(lib().mxq_gather_qmm_noalloc(_ptr(x), _ptr(w), _ptr(scales), _ptr(biases),
+                                            _ptr(expert_ids), _ptr(row_src), _ptr(out), T, B, E, K,
+                                            N, bits, group_size, _ptr(dev_status),
+                                            st), "mxq_gather_qmm_noalloc")
     return out
 
 
@@ -358,8 +377,10 @@ def gather_qmm(x, w, scales, biases, expert_ids, row_src, bits: int, out=None, w
     _require(workspace, "workspace", (torch.uint8,), x.device)
     if dev_status is not None:
         _require(dev_status, "dev_status", (torch.int32,), x.device)
-    _check(lib().mxq_gather_qmm(_ptr(x), _ptr(w), _ptr(scales), _ptr(biases), _ptr(expert_ids),
-                                _ptr(row_src), _ptr(out), T, B, E, K, N, bits, group_size,
-                                _ptr(workspace), workspace.numel(), _ptr(dev_status),
-                                _stream(stream)), "mxq_gather_qmm")
+    ctx, st = _launch_on(x.device, stream)
+    with ctx:
+        _check(lib().mxq_gather_qmm(_ptr(x), _ptr(w), _ptr(scales), _ptr(biases),
+                                    _ptr(expert_ids), _ptr(row_src), _ptr(out), T, B, E, K, N,
+                                    bits, group_size, _ptr(workspace), workspace.numel(),
+                                    _ptr(dev_status), st), "mxq_gather_qmm")
     return out

@@ -22,6 +22,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/mxq.h"
+#include "mxq_internal.h"
 
 namespace {
 
@@ -61,8 +62,12 @@ extern "C" mxq_status mxq_gather_qmm_noalloc(const void* x, const uint32_t* w,
     // anything touches a device
     const size_t need = mxq_gather_workspace_bytes(B, E, row_src ? K : 0, N);
     if (need > (size_t)MXQ_NOALLOC_SCRATCH_BYTES) return MXQ_ERR_SCRATCH_LIMIT;
+    // a device of another architecture is reported as such before the
+    // scratch lookup (which would fail there with a plain CUDA error)
+    mxq_status st = mxq::check_current_device(nullptr);
+    if (st != MXQ_OK) return st;
     void* scratch = nullptr;
-    const mxq_status st = scratch_on_current_device(&scratch);
+    st = scratch_on_current_device(&scratch);
     if (st != MXQ_OK) return st;
     return mxq_gather_qmm(x, w, scales, biases, expert_ids, row_src, y, T, B, E, K, N, bits,
                           group_size, scratch, (size_t)MXQ_NOALLOC_SCRATCH_BYTES, dev_status,

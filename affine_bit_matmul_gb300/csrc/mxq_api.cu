@@ -103,6 +103,8 @@ size_t gather_table_bytes(int B, int E) {
 
 }  // namespace
 
+mxq_status mxq::check_current_device(int* sms) { return check_device(sms); }
+
 extern "C" {
 
 const char* mxq_status_string(mxq_status s) {

@@ -5,7 +5,14 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "../../include/mxq.h"
+
 namespace mxq {
+
+// The current device is compute capability 10.3 (MXQ_OK, *sms = its SM
+// count; sms may be null), else MXQ_ERR_ARCH, or MXQ_ERR_CUDA if the runtime
+// cannot say.  Cached per device.
+mxq_status check_current_device(int* sms);
 
 // One tile of output rows of the grouped (sorted mixture-of-experts) GEMM:
 // rows [row_start, row_start + rows) of the sorted order, all of expert e.

@@ -18,7 +18,8 @@
 // The chunks are equal in size (within one row) and as many as a multiple
 // of the grid, so every CTA streams the same share.  The kernel is a
 // programmatic dependent launch: its CTAs start as the previous kernel's
-// finish and wait for that kernel to complete before reading anything.
+// finish and wait for that kernel to complete before reading anything into
+// shared memory; meanwhile each asks L2 to prefetch its first chunk.
 //
 // qmv_generic_kernel (any other shape): direct 16-byte loads, one CTA per 16
 // rows.
@@ -402,6 +403,14 @@ __device__ __forceinline__ void expect_tx(uint64_t* bar, uint32_t bytes) {
         : "memory");
 }
 
+// Ask L2 to fetch `bytes` (a multiple of 16) from global memory at `src`
+// (16-byte aligned).  Only a hint: it returns nothing and orders nothing, so
+// it may be issued before the previous kernel on the stream has finished --
+// L2 is where every write lands, so a line fetched early cannot be stale.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Programmatic dependent launch: the kernel launched after this one on the
 // stream may start its CTAs as ours finish; it waits in grid_dep_wait()
 // until this grid has completed and its writes are visible.
@@ -612,6 +621,16 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 2) * 32, 1)
             const char* sbp = reinterpret_cast<const char*>(scales);
             const char* bbp = reinterpret_cast<const char*>(biases);
             const ChunkRows cr{N / sh.nchunks, N % sh.nchunks};
+            // while the previous kernel finishes, have L2 fetch this CTA's
+            // first chunk, so that the first copy after the wait does not
+            // start from DRAM latency
+            if ((int)blockIdx.x < sh.nchunks) {
+                const int r0 = cr.begin(blockIdx.x);
+                const int rows = cr.begin(blockIdx.x + 1) - r0;
+                bulk_prefetch_l2(wb + (long long)r0 * sh.row_bytes, (uint32_t)(rows * sh.row_bytes));
+                bulk_prefetch_l2(sbp + (long long)r0 * sh.sb_bytes, (uint32_t)(rows * sh.sb_bytes));
+                bulk_prefetch_l2(bbp + (long long)r0 * sh.sb_bytes, (uint32_t)(rows * sh.sb_bytes));
+            }
             // every read into shared memory, and every read of x or write
             // of y, comes after the previous kernel on the stream completed
             grid_dep_wait();

@@ -43,6 +43,12 @@ METRIC = "qmv HBM GB/s and qmm/gather_qmm TFLOPS on 1 GB300, % of roofline"
 DECODE_CASES = [(5120, 17408, 4), (5120, 17408, 8), (17408, 5120, 4), (17408, 5120, 8)]
 WORKLOAD = ("qmv decode M=1: K=5120 N=17408 and K=17408 N=5120, 4-bit and 8-bit, group 64, "
             "bf16 scales/biases")
+# the same config dict on both arms
+CONFIG = {"workload": WORKLOAD, "M": 1, "group_size": 64,
+          "l2": "inputs larger than L2: each case alternates two input copies "
+                "(580 MB working set vs 129 MB L2)",
+          "parallelism": "replicas (one per GPU, no collective)"}
+PREHEAT_S = 0.3
 
 
 def qmv_bytes(K, N, bits, group=64):
@@ -101,53 +107,74 @@ def traffic_per_launch():
 
 
 class Clocks:
-    """nvidia-smi sampling of SM clocks and throttle reasons."""
+    """nvidia-smi sampling of SM clocks and throttle reasons every 20 ms.
+
+    ``mark()`` returns the current sample count, so that ``summary(a, b)``
+    can describe the samples taken between two marks (one window per
+    measured entry)."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, index):
         self.index = index
         self.proc = None
         self.file = tempfile.NamedTemporaryFile(mode="w+", suffix=".csv", delete=False)
+        self.rows = None
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=self.file, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
 
+    def _read(self):
+        self.file.flush()
+        with open(self.file.name) as f:
+            text = f.read()
+        out = []
+        for line in text.splitlines():
+            r = line.strip().split(",")
+            try:
+                reasons = {n for n, v in zip(self.NAMES, r[5:9]) if v.strip().lower() == "active"}
+                out.append((float(r[1]), float(r[2]), float(r[3]), reasons))
+            except (ValueError, IndexError):
+                continue
+        return out
+
+    def mark(self):
+        if self.proc is None:
+            return 0
+        time.sleep(0.05)  # let the sampler write what it has seen so far
+        return len(self._read())
+
     def stop(self):
         if self.proc is None:
-            return None
+            return
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        self.file.flush()
-        self.file.seek(0)
-        rows = [l.strip().split(",") for l in self.file.read().splitlines() if l.strip()]
+        self.rows = self._read()
         os.unlink(self.file.name)
-        sms, maxes, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
-            try:
-                sms.append(float(r[1]))
-                maxes.append(float(r[2]))
-                for name, v in zip(names, r[5:9]):
-                    if v.strip().lower() == "active":
-                        reasons.add(name)
-            except (ValueError, IndexError):
-                continue
-        if not sms:
+
+    def summary(self, a=0, b=None):
+        rows = (self.rows if self.rows is not None else self._read())[a:b]
+        if not rows:
             return None
-        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes),
-                "reasons": sorted(reasons), "samples": len(sms)}
+        lo, hi = min(r[2] for r in rows), max(r[2] for r in rows)
+        loaded = [r for r in rows if r[2] >= (lo + hi) / 2] or rows  # samples drawing power
+        reasons = sorted(set().union(*[r[3] for r in rows]))
+        return {"sm_mhz": statistics.median(r[0] for r in loaded),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows), "samples_under_load": len(loaded),
+                "power_w_max": hi}
 
 
 def dist_setup(n_gpus):
@@ -254,14 +281,20 @@ def capture(fn, count):
     return g
 
 
-def time_launches(fn, iters, stream, reps=5):
+def time_launches(fn, iters, stream, reps=5, preheat_s=0.05):
     """Median per-launch device time of fn over graphs of ``iters`` launches
-    (CUDA events on the launching stream around each graph replay)."""
+    (CUDA events on the launching stream around each graph replay), after
+    replaying the graph for ``preheat_s`` seconds (untimed: the GPU reaches
+    its loaded clocks, and the clock sampler sees the entry)."""
     import torch
 
     g = capture(fn, iters)
     g.replay()
     torch.cuda.synchronize()
+    t_end = time.perf_counter() + preheat_s
+    while time.perf_counter() < t_end:
+        g.replay()
+        torch.cuda.synchronize()
     ts = []
     for _ in range(reps):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -290,6 +323,8 @@ def run_mxq(args):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
     hbm, bf16_peak, bf16_sus, peak_src = load_peaks()
+    clocks = Clocks(local)
+    clocks.start()
 
     # ---- decode workload: 4 cases, two input copies each
     Ws = {}
@@ -310,12 +345,30 @@ def run_mxq(args):
     # in the timed region
     big = capture(lambda j: step(j), STEPS_PER_GRAPH)
     graphs = [capture(lambda j, par=par: step(par), 1) for par in (0, 1)]
+
+    # per-case device time, each case alone (graphs of 20 launches): the
+    # breakdown of the step; it also brings the GPU to its loaded clocks
+    per_case = []
+    for c in cases:
+        m0 = clocks.mark()
+        t, _ = time_launches(
+            lambda i, c=c: mxq.qmv(c.x[0], *c.copies[i % 2], c.bits, out=c.y[0]), 20, stream,
+            reps=25)
+        nb = qmv_bytes(c.K, c.N, c.bits)
+        per_case.append({"n": "qmv K=%d N=%d b%d g64" % (c.K, c.N, c.bits), "us": r3(t * 1e6),
+                         "GBs": r1(nb / t / 1e9), "bound": "hbm", "frac": r4(nb / t / 1e9 / hbm),
+                         "mhz": _mhz(clocks.summary(m0))})
+
+    # preheat: the decode step back to back for about PREHEAT_S seconds, so
+    # that the timed region starts at the loaded clocks (untimed)
+    t_end = time.perf_counter() + PREHEAT_S
+    while time.perf_counter() < t_end:
+        big.replay()
+        torch.cuda.synchronize()
     for i in range(args.warmup):
         graphs[i % 2].replay()
     torch.cuda.synchronize()
-    clocks = Clocks(local)
-    clocks.start()
-    time.sleep(0.3)  # let the sampler start before the timed region
+    m_timed = clocks.mark()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
@@ -328,7 +381,6 @@ def run_mxq(args):
     t1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
-    clk = clocks.stop()
     local_elapsed = t0.elapsed_time(t1) * 1e-3
     elapsed = max_over_ranks(local_elapsed, world)
     value = step_bytes * args.steps * world / elapsed / 1e9
@@ -336,16 +388,7 @@ def run_mxq(args):
     # kernel's algorithmic bytes per launch over its mean launch duration
     # there is this rank's step bytes over its time per step
     achieved = step_bytes * args.steps / local_elapsed / 1e9
-
-    # per-case device time, each case alone (graphs of 20 launches): the
-    # breakdown of the step, not the roofline figure
-    per_case = []
-    for c in cases:
-        t, _ = time_launches(
-            lambda i, c=c: mxq.qmv(c.x[0], *c.copies[i % 2], c.bits, out=c.y[0]), 20, stream)
-        nb = qmv_bytes(c.K, c.N, c.bits)
-        per_case.append({"K": c.K, "N": c.N, "bits": c.bits, "us": t * 1e6, "GB_s": nb / t / 1e9,
-                         "frac_hbm": nb / t / 1e9 / hbm})
+    m_timed_end = clocks.mark()
 
     # ---- end to end through the public API with host buffers
     pinned = []
@@ -388,7 +431,17 @@ def run_mxq(args):
 
     secondary = []
     if not args.no_secondary:
-        secondary = secondary_measurements(mxq, dev, stream, hbm, bf16_peak, Ws)
+        secondary = secondary_measurements(mxq, dev, stream, hbm, bf16_peak, Ws, clocks)
+    clocks.stop()
+    clk = clocks.summary(m_timed, m_timed_end)
+    # the 20 ms sampler may see no sample inside a short timed region: then
+    # the window is widened to the preheat before it, the same launches
+    if clk is None or clk["samples"] < 3:
+        clk = clocks.summary(0, m_timed_end)
+        if clk is not None:
+            clk["window"] = "per-case timing, preheat and timed region"
+    elif clk is not None:
+        clk["window"] = "timed region"
 
     line = {
         "metric": METRIC,
@@ -403,86 +456,103 @@ def run_mxq(args):
         "vs_baseline": None,
         "dtype": "u4/u8 codes, bf16 x, fp32 accumulate",
         "data": "synthetic (seeded W~N(0,0.02) quantized per the workload recipe, x~N(0,1))",
-        "config": {"workload": WORKLOAD, "M": 1, "group_size": 64,
-                   "l2": "inputs larger than L2: each case alternates two input copies "
-                         "(580 MB working set vs 129 MB L2)",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "config": CONFIG,
         "roofline": {"bound": "hbm", "kernel": "qmv_stream_kernel (4- and 8-bit)",
                      "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4), "traffic": traffic_per_launch(),
                      "algorithmic_bytes_per_launch": step_bytes // len(cases),
                      "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs copy bandwidth)"},
-        "per_case": per_case,
         "gpu_launches": len(cases) * args.steps,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "note": "public API qmv with inputs copied from pinned host memory every step"},
         "clocks": clk,
-        "secondary": secondary,
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    # last, so that the end of the line carries the workload's own configs:
+    # every other measured entry, then the spec configs (M sweep, 4/8-bit
+    # pair, sorted-MoE gather, prefill), then the decode cases of `value`
+    line["secondary"] = secondary + per_case
     if rank == 0:
-        print(json.dumps(line), flush=True)
+        print(json.dumps(line, separators=(",", ":")), flush=True)
     if world > 1:
         import torch.distributed as dist
 
         dist.destroy_process_group()
 
 
-def secondary_measurements(mxq, dev, stream, hbm, bf16_peak, Ws):
-    """Prefill GEMM, M sweep, the 4/8-bit pair, other bit widths and group sizes,
-    the [K, N] layout GEMV, the encoder and the sorted-MoE gather."""
+def r1(v):
+    return round(float(v), 1)
+
+
+def r3(v):
+    return round(float(v), 3)
+
+
+def r4(v):
+    return round(float(v), 4)
+
+
+def _mhz(summary):
+    return None if summary is None else int(summary["sm_mhz"])
+
+
+def secondary_measurements(mxq, dev, stream, hbm, bf16_peak, Ws, clocks):
+    """Every other measured configuration, as compact entries: name ``n``,
+    time ``us``, TFLOP/s ``TF`` and/or GB/s ``GBs``, the binding roofline
+    ``bound`` and the fraction of it reached ``frac``, and the median SM
+    clock ``mhz`` while it ran.  The list ends with the workload's north-star
+    configurations, so that they close the JSON line."""
     import torch
 
     out = []
     iters = 40
+
+    def entry(name, t, nbytes, flops, m0, extra=None):
+        t_mem = nbytes / (hbm * 1e9)
+        t_fl = flops / (bf16_peak * 1e12) if flops else 0.0
+        bound = "hbm" if t_mem >= t_fl else "tensor"
+        e = {"n": name, "us": r3(t * 1e6), "GBs": r1(nbytes / t / 1e9)}
+        if flops:
+            e["TF"] = r1(flops / t / 1e12)
+        e["bound"] = bound
+        e["frac"] = r4(max(t_mem, t_fl) / t)
+        e["mhz"] = _mhz(clocks.summary(m0))
+        if extra:
+            e.update(extra)
+        return e
 
     def dense_entry(name, M, K, N, bits, W, copies, group=64):
         d = DenseInputs(W, M, K, N, bits, dev, copies=copies, group=group)
         if M == 1:
             fn = lambda i: mxq.qmv(d.x[0], *d.copies[i % copies], bits, out=d.y[0],  # noqa: E731
                                    group_size=group)
-            kern = "qmv_stream_kernel"
         else:
             fn = lambda i: mxq.qmm(d.x, *d.copies[i % copies], bits, out=d.y,  # noqa: E731
                                    group_size=group)
-            kern = "qmm_tc_kernel or qmm_persistent_kernel"
         for i in range(5):
             fn(i)
+        m0 = clocks.mark()
         t, _ = time_launches(fn, iters, stream)
-        flops = 2.0 * M * K * N
-        nbytes = qmm_bytes(M, K, N, bits, group)
-        t_star = max(nbytes / (hbm * 1e9), flops / (bf16_peak * 1e12))
-        bound = "hbm" if nbytes / (hbm * 1e9) >= flops / (bf16_peak * 1e12) else "tensor"
         del d
-        return {"name": name, "kernel": kern, "M": M, "K": K, "N": N, "bits": bits,
-                "group": group, "us": t * 1e6, "TFLOPS": flops / t / 1e12, "GB_s": nbytes / t / 1e9,
-                "frac_tensor": flops / t / 1e12 / bf16_peak, "frac_hbm": nbytes / t / 1e9 / hbm,
-                "bound": bound, "frac_roofline": t_star / t, "tokens_per_s": M / t}
+        return entry("%s M=%d K=%d N=%d b%d g%d" % (name, M, K, N, bits, group), t,
+                     qmm_bytes(M, K, N, bits, group), 2.0 * M * K * N if M > 1 else 0.0, m0)
 
-    W_big = Ws.get((5120, 17408)) if Ws.get((5120, 17408)) is not None else synth.dense_weights(
-        17408, 5120, seed=0)
-    out.append(dense_entry("qmm prefill", 600, 5120, 17408, 4, W_big, copies=3))
+    W_big = Ws.get((5120, 17408))
+    if W_big is None:
+        W_big = synth.dense_weights(17408, 5120, seed=0)
     W_sq = synth.dense_weights(5120, 5120, seed=0)
-    for M in (1, 8, 32, 128, 600):
-        out.append(dense_entry("qmm sweep", M, 5120, 5120, 4, W_sq, copies=6))
-    # controlled pair: same W, 8-bit (4-bit rows are in the sweep above)
-    out.append(dense_entry("pair qmv 8-bit", 1, 5120, 5120, 8, W_sq, copies=6))
-    out.append(dense_entry("pair qmv 4-bit", 1, 5120, 5120, 4, W_sq, copies=6))
-    out.append(dense_entry("pair qmm 8-bit", 128, 5120, 5120, 8, W_sq, copies=6))
-    # 2-, 3- and 6-bit codes and group sizes 32 and 128 on the decode and
-    # prefill shapes (same weights)
-    for bits in (2, 3, 6):
-        out.append(dense_entry("%d-bit qmv" % bits, 1, 5120, 17408, bits, W_big, copies=6))
-        out.append(dense_entry("%d-bit qmm prefill" % bits, 600, 5120, 17408, bits, W_big,
-                               copies=3))
-    for group in (32, 128):
-        out.append(dense_entry("group qmv", 1, 5120, 17408, 4, W_big, copies=6, group=group))
-        out.append(dense_entry("group qmm prefill", 600, 5120, 17408, 4, W_big, copies=3,
-                               group=group))
 
-    # the decode GEMV for the [K, N] operand layout (codes and groups along n)
+    # ---- other widths and group sizes on the decode and prefill shapes
+    for bits in (2, 3, 6):
+        out.append(dense_entry("qmv", 1, 5120, 17408, bits, W_big, copies=6))
+        out.append(dense_entry("qmm", 600, 5120, 17408, bits, W_big, copies=3))
+    for group in (32, 128):
+        out.append(dense_entry("qmv", 1, 5120, 17408, 4, W_big, copies=6, group=group))
+        out.append(dense_entry("qmm", 600, 5120, 17408, 4, W_big, copies=3, group=group))
+
+    # ---- the decode GEMV for the [K, N] operand layout (codes and groups along n)
     for (K, N) in ((5120, 17408), (17408, 5120)):
         Wkn = synth.dense_weights(K, N, seed=0)
         qkn = synth.quantize(Wkn, 4)
@@ -493,17 +563,13 @@ def secondary_measurements(mxq, dev, stream, hbm, bf16_peak, Ws):
         fnk = lambda i: mxq.qmv_kn(xkn, *kn_copies[i % 6], 4, out=ykn)  # noqa: E731
         for i in range(5):
             fnk(i)
+        m0 = clocks.mark()
         tk, _ = time_launches(fnk, iters, stream)
-        nbk = qmv_bytes(K, N, 4)
-        out.append({"name": "qmv [K, N] layout", "kernel": "qmv_kn_kernel", "M": 1, "K": K,
-                    "N": N, "bits": 4, "group": 64, "us": tk * 1e6,
-                    "TFLOPS": 2.0 * K * N / tk / 1e12, "GB_s": nbk / tk / 1e9,
-                    "frac_hbm": nbk / tk / 1e9 / hbm, "bound": "hbm",
-                    "frac_roofline": nbk / tk / 1e9 / hbm, "tokens_per_s": 1 / tk})
+        out.append(entry("qmv_kn K=%d N=%d b4 g64" % (K, N), tk, qmv_bytes(K, N, 4), 0.0, m0))
         del kn_copies, Wkn, qkn
     torch.cuda.empty_cache()
 
-    # the encoder on the prefill weight shape (float32 in, 4-bit codes out)
+    # ---- the encoder on the prefill weight shape (float32 in, 4-bit codes out)
     N_q, K_q = 17408, 5120
     Wq = [torch.randn((N_q, K_q), device=dev) * 0.02 for _ in range(2)]
     cq = torch.empty((N_q, K_q // 8), dtype=torch.int32, device=dev)
@@ -512,16 +578,15 @@ def secondary_measurements(mxq, dev, stream, hbm, bf16_peak, Ws):
     fnq = lambda i: mxq.quantize(Wq[i % 2], 4, codes=cq, scales=sq, biases=bq)  # noqa: E731
     for i in range(3):
         fnq(i)
+    m0 = clocks.mark()
     tq, _ = time_launches(fnq, iters, stream)
     nbq = N_q * K_q * 4 + N_q * K_q // 2 + N_q * (K_q // 64) * 4
-    out.append({"name": "quantize", "kernel": "quantize_kernel", "K": K_q, "N": N_q, "bits": 4,
-                "us": tq * 1e6, "TFLOPS": 0.0, "GB_s": nbq / tq / 1e9,
-                "frac_hbm": nbq / tq / 1e9 / hbm, "bound": "hbm",
-                "frac_roofline": nbq / tq / 1e9 / hbm, "tokens_per_s": 0.0})
+    out.append(entry("quantize f32 [17408,5120] -> b4 g64", tq, nbq, 0.0, m0))
     del Wq, cq, sq, bq
     torch.cuda.empty_cache()
 
-    # sorted MoE gather, both expert shapes
+    # ---- sorted MoE: experts of both shapes, the decode-sized calls first
+    north = []
     for K, N, ident in ((2816, 704, False), (704, 2816, True)):
         E, T, top_k, bits = 128, 573, 8, 4
         ids, src = synth.routing(T, E, top_k, seed=2)
@@ -536,47 +601,53 @@ def secondary_measurements(mxq, dev, stream, hbm, bf16_peak, Ws):
         s = dev_bf16(np.stack(sl), dev)
         b = dev_bf16(np.stack(bl), dev)
         copies = [(w, s, b), (w.clone(), s.clone(), b.clone())]
+        expert_bytes = N * K * bits // 8 + N * (K // 64) * 4
+        wsz = torch.empty((mxq.gather_workspace_bytes(B, E, K if not ident else 0, N),),
+                          dtype=torch.uint8, device=dev)
+        # decode-sized calls on the same experts: a few tokens x top 8
+        for tokens in (4,):
+            idsd, srcd = synth.routing(tokens, E, top_k, seed=3)
+            Bd = idsd.shape[0]
+            xd = dev_bf16(synth.activations(Bd if ident else tokens, K, seed=1), dev)
+            idsd_d = torch.from_numpy(idsd).to(dev)
+            srcd_d = None if ident else torch.from_numpy(srcd).to(dev)
+            yd = torch.empty((Bd, N), dtype=torch.bfloat16, device=dev)
+            fnd = lambda i: mxq.gather_qmm(xd, *copies[i % 2], idsd_d, srcd_d, bits,  # noqa: E731
+                                           out=yd, workspace=wsz)
+            for i in range(5):
+                fnd(i)
+            m0 = clocks.mark()
+            td, _ = time_launches(fnd, iters, stream)
+            used = len(set(idsd.tolist()))
+            nbd = used * expert_bytes + xd.numel() * 2 + Bd * N * 2
+            out.append(entry("gather decode T=%d B=%d K=%d N=%d b4" % (tokens, Bd, K, N), td, nbd,
+                             0.0, m0, {"experts": used}))
         Tx = B if ident else T
         x = dev_bf16(synth.activations(Tx, K, seed=1), dev)
         ids_d = torch.from_numpy(ids).to(dev)
         src_d = None if ident else torch.from_numpy(src).to(dev)
         y = torch.empty((B, N), dtype=torch.bfloat16, device=dev)
-        wsz = torch.empty((mxq.gather_workspace_bytes(B, E, K if src_d is not None else 0, N),), dtype=torch.uint8, device=dev)
         fn = lambda i: mxq.gather_qmm(x, *copies[i % 2], ids_d, src_d, bits, out=y,  # noqa: E731
                                       workspace=wsz)
         for i in range(5):
             fn(i)
+        m0 = clocks.mark()
         t, _ = time_launches(fn, iters, stream)
-        flops = 2.0 * B * K * N
-        nbytes = E * (N * K * bits // 8 + N * (K // 64) * 4) + Tx * K * 2 + B * N * 2
-        t_star = max(nbytes / (hbm * 1e9), flops / (bf16_peak * 1e12))
-        out.append({"name": "gather_qmm", "kernel": "gather_prepass + gather_rows + qmm_persistent_kernel",
-                    "E": E, "top_k": top_k, "tokens": T, "B": B, "K": K, "N": N, "bits": bits,
-                    "us": t * 1e6, "TFLOPS": flops / t / 1e12, "GB_s": nbytes / t / 1e9,
-                    "frac_tensor": flops / t / 1e12 / bf16_peak, "frac_hbm": nbytes / t / 1e9 / hbm,
-                    "bound": "hbm", "frac_roofline": t_star / t, "tokens_per_s": T / t})
-        # decode-sized call on the same experts: 4 tokens x top 8 = 32 rows
-        ids4, src4 = synth.routing(4, E, top_k, seed=3)
-        B4 = ids4.shape[0]
-        x4 = dev_bf16(synth.activations(B4 if ident else 4, K, seed=1), dev)
-        ids4_d = torch.from_numpy(ids4).to(dev)
-        src4_d = None if ident else torch.from_numpy(src4).to(dev)
-        y4 = torch.empty((B4, N), dtype=torch.bfloat16, device=dev)
-        fn4 = lambda i: mxq.gather_qmm(x4, *copies[i % 2], ids4_d, src4_d, bits, out=y4,  # noqa: E731
-                                       workspace=wsz)
-        for i in range(5):
-            fn4(i)
-        t4, _ = time_launches(fn4, iters, stream)
-        used = len(set(ids4.tolist()))
-        nb4 = used * (N * K * bits // 8 + N * (K // 64) * 4) + x4.numel() * 2 + B4 * N * 2
-        out.append({"name": "gather_qmm decode", "kernel": "gather_qmv_kernel",
-                    "E": E, "top_k": top_k, "tokens": 4, "B": B4, "experts_used": used, "K": K,
-                    "N": N, "bits": bits, "us": t4 * 1e6, "TFLOPS": 2.0 * B4 * K * N / t4 / 1e12,
-                    "GB_s": nb4 / t4 / 1e9, "frac_hbm": nb4 / t4 / 1e9 / hbm, "bound": "hbm",
-                    "frac_roofline": nb4 / t4 / 1e9 / hbm, "tokens_per_s": 4 / t4})
+        nbytes = E * expert_bytes + Tx * K * 2 + B * N * 2
+        north.append(entry("gather_qmm E=128 top8 T=573 B=%d K=%d N=%d b4 g64" % (B, K, N), t,
+                           nbytes, 2.0 * B * K * N, m0, {"tok_s": int(T / t)}))
         del w, s, b, copies, x, y
         torch.cuda.empty_cache()
-    return out
+
+    # ---- spec configurations: M sweep at K=N=5120, the 4/8-bit pair,
+    # then the prefill GEMM
+    sweep = [dense_entry("qmm", M, 5120, 5120, 4, W_sq, copies=6) for M in (1, 8, 32, 128, 600)]
+    pair = [dense_entry("pair qmv", 1, 5120, 5120, 8, W_sq, copies=6),
+            dense_entry("pair qmm", 128, 5120, 5120, 8, W_sq, copies=6)]
+    prefill = dense_entry("qmm prefill", 600, 5120, 17408, 4, W_big, copies=3)
+    prefill["tok_s"] = int(600 / (prefill["us"] * 1e-6))
+    return out + north + sweep + pair + [prefill]
+
 
 
 # ------------------------------------------------------------------ CPU side
@@ -657,7 +728,7 @@ def run_reference(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "M": 1, "group_size": 64},
+        "config": CONFIG,
         "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": oracle.threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,

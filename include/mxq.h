@@ -80,10 +80,10 @@ typedef enum {
  * Requirements: bits in {2, 3, 4, 6, 8}; group_size in {32, 64, 128}; K > 0,
  * K % 64 == 0 and K % group_size == 0 (K % 128 == 0 at 3 bits); N > 0;
  * x, w, y 16-byte aligned; scales, biases 2-byte aligned.  The streaming
- * kernel is used when bits is 2, 4 or 8, K % 512 == 0, K <= 20480,
- * K / group_size % 8 == 0 and scales/biases are 16-byte aligned; other
- * shapes take a direct-load kernel (same result
- * rule, different summation order).  The streaming kernel is launched as a
+ * kernel is used when K % 512 == 0, K <= 20480, K / group_size % 8 == 0 and
+ * scales/biases are 16-byte aligned; other shapes take a direct-load kernel
+ * (same result rule, different summation order).  The streaming kernel is
+ * launched as a
  * programmatic dependent launch: its CTAs may be placed on SMs while the
  * kernel before it on the stream finishes, but they read and write nothing
  * until that kernel has completed, so stream order is kept.                 */
@@ -184,7 +184,10 @@ size_t mxq_gather_workspace_bytes(int B, int E, int K, int N);
  *
  * Set-up: the first call on each device looks up the scratch's device
  * address with that device current (this may load the library's device
- * code); make that first call before capturing a stream into a graph.
+ * code); make that first call before capturing a stream into a graph.  The
+ * address is kept for the life of the process: do not use this entry point
+ * on a device after cudaDeviceReset (or any other teardown of its primary
+ * context), since the scratch may then live at another address.
  * Nothing in the scratch has to start at zero: every call writes all the
  * scratch it reads.
  *

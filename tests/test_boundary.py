@@ -169,3 +169,33 @@ def quantize(L, w=FAKE, codes=FAKE, s=FAKE, b=FAKE, N=16, K=128, bits=4, group=6
 ])
 def test_quantize_argument_checks(L, kw, code):
     assert quantize(L, **kw) == code
+
+
+def test_wrapper_refuses_a_stream_of_another_device():
+    # every Python wrapper makes the tensors' device current for the call and
+    # refuses a stream that belongs to another device (that pairing would
+    # launch one device's kernels on another device's pointers); the check
+    # runs before anything touches a GPU
+    import torch
+
+    import affine_bit_matmul_gb300 as mxq
+
+    class FakeStream:
+        device = torch.device("cuda", 1)
+        cuda_stream = 0
+
+    with pytest.raises(ValueError, match="stream is on cuda:1"):
+        mxq._launch_on(torch.device("cuda", 0), FakeStream())
+
+
+def test_bench_reference_arm_uses_the_same_config():
+    # both arms of bench.py print the identical config dict
+    import sys
+
+    sys.path.insert(0, ROOT)
+    import bench
+
+    src = open(os.path.join(ROOT, "bench.py")).read()
+    ref = src[src.index("def run_reference"):src.index("def run_profile")]
+    assert '"config": CONFIG' in ref
+    assert bench.CONFIG["workload"] == bench.WORKLOAD

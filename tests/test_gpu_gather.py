@@ -69,14 +69,20 @@ def _sample_check(c, y, count=3000):
             assert_close(yh[r], yr, bnd, "gather row %d (expert %d)" % (r, e))
 
 
-@pytest.mark.parametrize("K,N,ident", [(2816, 704, False), (704, 2816, True)])
-def test_gather_workload_shapes(K, N, ident):
+@pytest.mark.parametrize("K,N,ident,bits", [(2816, 704, False, 4), (704, 2816, True, 4),
+                                             (2816, 704, False, 8)])
+def test_gather_workload_shapes(K, N, ident, bits):
+    # the sorted-MoE workload (573 tokens, top 8 of 128 experts), every
+    # element of the [4584, N] output against the f64 checker, plus bitwise
+    # run-to-run determinism
     import torch
 
-    c = MoECase(573, 128, 8, K, N, 4, seed=0, identity_src=ident)
+    c = MoECase(573, 128, 8, K, N, bits, seed=0, identity_src=ident)
     assert c.B == 4584
     y = _run(c)
-    _sample_check(c, y)
+    yr, bnd = _ref(c)
+    assert_close(to_f64(y), yr, bnd, "gather workload K=%d N=%d bits=%d" % (K, N, bits))
+    _sample_check(c, y, count=500)
     y2 = _run(c)
     assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
 

@@ -56,6 +56,36 @@ def test_noalloc_workload_shape():
     assert _same(ref2, out2) and _same(out, out2)
 
 
+def test_noalloc_against_oracle_twice():
+    # the fixed-scratch form checked directly against the f64 checker, on two
+    # calls in a row (the second finds the first call's scratch contents)
+    import oracle
+    from tests.gpu_util import assert_close, to_f64
+
+    case = MoECase(T=70, E=9, top_k=3, K=448, N=160, bits=4, seed=34)
+    yr, bnd = oracle.gather_qmm(case.x, case.w, case.s, case.b, case.ids, case.src, case.T,
+                                case.B, case.E, case.K, case.N, case.bits)
+    for _ in range(2):
+        _, out = _both(case)
+        assert_close(to_f64(out), yr, bnd, "gather_qmm_noalloc vs oracle")
+
+
+def test_noalloc_decode_sized_call():
+    # a decode step: 3 tokens x top 8 of 128 experts (24 sorted rows), against
+    # the workspace form bit for bit and against the f64 checker
+    import oracle
+    from tests.gpu_util import assert_close, to_f64
+
+    case = MoECase(T=3, E=128, top_k=8, K=2816, N=704, bits=4, seed=35, routing_seed=6)
+    assert case.B <= 32
+    yr, bnd = oracle.gather_qmm(case.x, case.w, case.s, case.b, case.ids, case.src, case.T,
+                                case.B, case.E, case.K, case.N, case.bits)
+    for _ in range(2):
+        ref, out = _both(case)
+        assert _same(ref, out)
+        assert_close(to_f64(out), yr, bnd, "decode-sized gather_qmm_noalloc vs oracle")
+
+
 def test_noalloc_refuses_oversized_request():
     import torch
 
