@@ -32,6 +32,7 @@ __all__ = [
     "qmm",
     "qmv_kn",
     "gather_qmm",
+    "gather_qmm_gateup",
     "gather_workspace_bytes",
     "gather_qmm_noalloc",
     "quantize",
@@ -69,6 +70,7 @@ EXPORTED_SYMBOLS = (
     "mxq_qmm",
     "mxq_qmv_kn",
     "mxq_gather_qmm",
+    "mxq_gather_qmm_gateup",
     "mxq_gather_workspace_bytes",
     "mxq_gather_qmm_noalloc",
     "mxq_quantize",
@@ -105,6 +107,9 @@ def lib():
         L.mxq_qmv_kn.restype = I
         L.mxq_gather_qmm.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, Z, P, P]
         L.mxq_gather_qmm.restype = I
+        L.mxq_gather_qmm_gateup.argtypes = [P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I,
+                                             I, P, Z, P, P]
+        L.mxq_gather_qmm_gateup.restype = I
         L.mxq_gather_qmm_noalloc.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P]
         L.mxq_gather_qmm_noalloc.restype = I
         L.mxq_quantize.argtypes = [P, P, P, P, I, I, I, I, P]
@@ -306,7 +311,9 @@ def quantize(w, bits: int, codes=None, scales=None, biases=None, stream=None,
 
 
 def gather_workspace_bytes(B: int, E: int, K: int, N: int) -> int:
-    """Workspace bytes for gather_qmm; pass K = 0 when row_src is None."""
+    """Workspace bytes that always suffice for gather_qmm and
+    gather_qmm_gateup (K = 0: the tile table alone, enough for calls with
+    more than 8 * E rows and no row_src)."""
     return int(lib().mxq_gather_workspace_bytes(B, E, K, N))
 
 
@@ -372,8 +379,8 @@ def gather_qmm(x, w, scales, biases, expert_ids, row_src, bits: int, out=None, w
         out = torch.empty((B, N), dtype=torch.bfloat16, device=x.device)
     _require(out, "out", (torch.bfloat16,), x.device)
     if workspace is None:
-        workspace = torch.empty((gather_workspace_bytes(B, E, K if row_src is not None else 0, N),),
-                                dtype=torch.uint8, device=x.device)
+        workspace = torch.empty((gather_workspace_bytes(B, E, K, N),), dtype=torch.uint8,
+                                device=x.device)
     _require(workspace, "workspace", (torch.uint8,), x.device)
     if dev_status is not None:
         _require(dev_status, "dev_status", (torch.int32,), x.device)
@@ -384,3 +391,51 @@ def gather_qmm(x, w, scales, biases, expert_ids, row_src, bits: int, out=None, w
                                     bits, group_size, _ptr(workspace), workspace.numel(),
                                     _ptr(dev_status), st), "mxq_gather_qmm")
     return out
+
+
+def gather_qmm_gateup(x, w_gate, s_gate, b_gate, w_up, s_up, b_up, expert_ids, row_src,
+                      bits: int, out_gate=None, out_up=None, workspace=None, dev_status=None,
+                      stream=None, group_size: int = 64):
+    """The gate and up projections of a mixture-of-experts layer: the same
+    routed rows against two expert weight sets of one shape.  Returns
+    (y_gate, y_up), each bf16 [B, N] in sorted row order; no activation
+    function is applied."""
+    torch = _torch()
+    _require(x, "x", (torch.bfloat16,))
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D [T, K]")
+    T, K = x.shape
+    if w_gate.dim() != 3 or tuple(w_up.shape) != tuple(w_gate.shape):
+        raise ValueError("w_gate and w_up must both be [E, N, K*bits/32]")
+    E, N = w_gate.shape[0], w_gate.shape[1]
+    _check_weights(w_gate, s_gate, b_gate, N, K, bits, x.device, lead=(E,),
+                   group_size=group_size)
+    _check_weights(w_up, s_up, b_up, N, K, bits, x.device, lead=(E,), group_size=group_size)
+    _require(expert_ids, "expert_ids", (torch.int32,), x.device)
+    B = expert_ids.numel()
+    if row_src is not None:
+        _require(row_src, "row_src", (torch.int32,), x.device)
+        if row_src.numel() != B:
+            raise ValueError("row_src must have B entries")
+    outs = []
+    for o, name in ((out_gate, "out_gate"), (out_up, "out_up")):
+        if o is None:
+            o = torch.empty((B, N), dtype=torch.bfloat16, device=x.device)
+        _require(o, name, (torch.bfloat16,), x.device)
+        if tuple(o.shape) != (B, N):
+            raise ValueError("%s has shape %s, expected %s" % (name, tuple(o.shape), (B, N)))
+        outs.append(o)
+    if workspace is None:
+        workspace = torch.empty((gather_workspace_bytes(B, E, K, N),), dtype=torch.uint8,
+                                device=x.device)
+    _require(workspace, "workspace", (torch.uint8,), x.device)
+    if dev_status is not None:
+        _require(dev_status, "dev_status", (torch.int32,), x.device)
+    ctx, st = _launch_on(x.device, stream)
+    with ctx:
+        _check(lib().mxq_gather_qmm_gateup(
+            _ptr(x), _ptr(w_gate), _ptr(s_gate), _ptr(b_gate), _ptr(w_up), _ptr(s_up), _ptr(b_up),
+            _ptr(expert_ids), _ptr(row_src), _ptr(outs[0]), _ptr(outs[1]), T, B, E, K, N, bits,
+            group_size, _ptr(workspace), workspace.numel(), _ptr(dev_status), st),
+            "mxq_gather_qmm_gateup")
+    return outs[0], outs[1]

@@ -10,7 +10,8 @@
 //   3. cuts each segment into tiles of at most rows_per_tile rows of equal
 //      size, and writes the tile list with a block-wide exclusive scan
 //      (warp shuffles);
-//   4. zeroes the y rows no tile covers (ids outside [0, E)).
+//   4. zeroes the y rows no tile covers (ids outside [0, E)), in both
+//      outputs of the gate/up pair.
 // Unsorted ids make the call produce an all-zero y and no tiles.
 //
 // When the activation rows are routed through row_src, a second kernel
@@ -67,7 +68,8 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
 __global__ void __launch_bounds__(kPrepThreads) gather_prepass_kernel(
     const int32_t* __restrict__ ids, const int32_t* __restrict__ row_src, int T, int B, int E,
     int N, int rows_per_tile, MTile* __restrict__ tiles, int* __restrict__ tile_count,
-    int* __restrict__ seg_start, __nv_bfloat16* __restrict__ y, int32_t* __restrict__ status) {
+    int* __restrict__ seg_start, __nv_bfloat16* __restrict__ y, __nv_bfloat16* __restrict__ y2,
+    int32_t* __restrict__ status) {
     __shared__ int flags;
     __shared__ int warp_sums[33];
     // the sorted copy of the activation rows (the next launch) does not read
@@ -109,6 +111,7 @@ __global__ void __launch_bounds__(kPrepThreads) gather_prepass_kernel(
     if (all & MXQ_DEV_UNSORTED_IDS) {
         if (threadIdx.x == 0) *tile_count = 0;
         zero_rows(y, 0, B, N);
+        if (y2) zero_rows(y2, 0, B, N);
         return;
     }
 
@@ -166,6 +169,10 @@ __global__ void __launch_bounds__(kPrepThreads) gather_prepass_kernel(
     // 4. rows before expert 0 (negative ids) and from expert E on (ids >= E)
     zero_rows(y, 0, seg_start[0], N);
     zero_rows(y, seg_start[E], B, N);
+    if (y2) {
+        zero_rows(y2, 0, seg_start[0], N);
+        zero_rows(y2, seg_start[E], B, N);
+    }
 }
 
 // One warp per sorted row, 16-byte copies.  It runs alongside the prepass
@@ -226,11 +233,11 @@ cudaError_t launch_gather_rows(const void* x, const int32_t* row_src, int T, int
 
 cudaError_t launch_gather_prepass(const int32_t* expert_ids, const int32_t* row_src, int T,
                                   int B, int E, int N, int rows_per_tile, MTile* tiles,
-                                  int* tile_count, int* seg_start, void* y, int32_t* status,
-                                  cudaStream_t stream) {
+                                  int* tile_count, int* seg_start, void* y, void* y2,
+                                  int32_t* status, cudaStream_t stream) {
     gather_prepass_kernel<<<1, kPrepThreads, 0, stream>>>(
         expert_ids, row_src, T, B, E, N, rows_per_tile, tiles, tile_count, seg_start,
-        static_cast<__nv_bfloat16*>(y), status);
+        static_cast<__nv_bfloat16*>(y), static_cast<__nv_bfloat16*>(y2), status);
     return cudaGetLastError();
 }
 

@@ -60,7 +60,7 @@ extern "C" mxq_status mxq_gather_qmm_noalloc(const void* x, const uint32_t* w,
                                              int group_size, int32_t* dev_status, void* stream) {
     // the size check comes first, so an oversized request is refused before
     // anything touches a device
-    const size_t need = mxq_gather_workspace_bytes(B, E, row_src ? K : 0, N);
+    const size_t need = mxq::gather_scratch_bytes(B, E, K, N, bits, group_size, row_src != nullptr);
     if (need > (size_t)MXQ_NOALLOC_SCRATCH_BYTES) return MXQ_ERR_SCRATCH_LIMIT;
     // a device of another architecture is reported as such before the
     // scratch lookup (which would fail there with a plain CUDA error)

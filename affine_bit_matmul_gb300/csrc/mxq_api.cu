@@ -93,17 +93,55 @@ DensePlan plan_dense(int M, int K, int N, int bits, int sms) {
     return pl;
 }
 
+// Activation rows per item of the skinny kernel (decode-sized grouped calls).
+constexpr int kSkinnyRows = 8;
+
+// Tiles of the grouped tensor-core GEMM (at most 64 rows each), an upper bound.
 size_t gather_max_tiles(int B, int E) { return (size_t)B / kGatherRowsPerTile + (size_t)E + 1; }
+// Items of the skinny kernel (at most 8 rows each), an upper bound; the
+// table is sized for the larger of the two.
+size_t gather_max_items(int B, int E) { return (size_t)B / kSkinnyRows + (size_t)E + 1; }
 
 // Tile records, the tile count, each expert's first row; 256-byte aligned.
 size_t gather_table_bytes(int B, int E) {
-    return align_up(gather_max_tiles(B, E) * sizeof(mxq::MTile), 256) + 256 +
+    return align_up(gather_max_items(B, E) * sizeof(mxq::MTile), 256) + 256 +
            align_up(((size_t)E + 1) * sizeof(int), 256);
+}
+
+// Floats per row of the skinny kernel's group sums (groups of 32: the most).
+size_t skinny_xs_ld(int K, int group) { return ((size_t)(K / group) + 3) & ~(size_t)3; }
+
+// Skinny plan for a grouped call (no K split); false if it does not apply.
+bool skinny_gather_plan(int B, int E, int K, int N, int bits, int group, int sets, int sms,
+                        mxq::SkinnyParams& sp) {
+    if (bits != 4 || B > kSkinnyRows * E) return false;
+    if (check_common(K, N, bits, group) != MXQ_OK) return false;
+    std::memset(&sp, 0, sizeof sp);
+    sp.sets = sets;
+    sp.K = K;
+    sp.N = N;
+    sp.group = group;
+    sp.kc = K;
+    sp.S = 1;
+    sp.slabs = (N + 15) / 16;
+    sp.xslots = 2;
+    sp.slot_rows = kSkinnyRows;
+    (void)sms;
+    return mxq::plan_skinny(sp, 0);
 }
 
 }  // namespace
 
 mxq_status mxq::check_current_device(int* sms) { return check_device(sms); }
+
+size_t mxq::gather_scratch_bytes(int B, int E, int K, int N, int bits, int group_size,
+                                 bool has_row_src) {
+    mxq::SkinnyParams sp;
+    if (skinny_gather_plan(B, E, K, N, bits, group_size, 1, 0, sp))
+        return mxq_gather_workspace_bytes(B, E, K, N);  // sorted rows and their group sums
+    if (has_row_src) return gather_table_bytes(B, E) + align_up((size_t)B * K * 2, 256);
+    return gather_table_bytes(B, E);
+}
 
 extern "C" {
 
@@ -156,6 +194,64 @@ mxq_status mxq_qmm(const void* x, const uint32_t* w, const void* scales, const v
     int sms = 0;
     st = check_device(&sms);
     if (st != MXQ_OK) return st;
+    if (M == 1) {
+        // one activation row: the streaming GEMV (same operation)
+        cudaStream_t s1 = static_cast<cudaStream_t>(stream);
+        if (dev_status && cudaMemsetAsync(dev_status, 0, sizeof(int32_t), s1) != cudaSuccess)
+            return MXQ_ERR_CUDA;
+        cudaError_t err =
+            mxq::launch_qmv(x, w, scales, biases, y, K, N, bits, group_size, sms, dev_status, s1);
+        return err == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA;
+    }
+    if (bits == 4 && M <= kSkinnyRows) {
+        // a few rows: the skinny kernel streams the codes once for all of
+        // them; K is split over a cluster of S CTAs so that the 16-row slabs
+        // spread evenly over the SMs (the cheapest S by slabs per CTA times
+        // k per CTA, plus a per-slab overhead)
+        mxq::SkinnyParams sp;
+        const int slabs = (N + 15) / 16;
+        int best_s = 0, best_rounds = 0;
+        long long best_cost = 0;
+        mxq::SkinnyParams best;
+        for (int S = 1; S <= 8; ++S) {
+            if (K % (S * 256) != 0) continue;
+            const int C = sms / S;
+            if (C < 1) continue;
+            const int rounds = (slabs + C - 1) / C;
+            const long long cost = (long long)rounds * (K / S + 512);
+            std::memset(&sp, 0, sizeof sp);
+            sp.sets = 1;
+            sp.M = M;
+            sp.K = K;
+            sp.N = N;
+            sp.group = group_size;
+            sp.kc = K / S;
+            sp.S = S;
+            sp.slabs = slabs;
+            sp.xslots = 1;
+            sp.slot_rows = M;
+            if (!mxq::plan_skinny(sp, rounds)) continue;
+            if (best_s == 0 || cost < best_cost) {
+                best_s = S;
+                best_cost = cost;
+                best_rounds = rounds;
+                best = sp;
+            }
+        }
+        if (best_s > 0) {
+            cudaStream_t s1 = static_cast<cudaStream_t>(stream);
+            if (dev_status && cudaMemsetAsync(dev_status, 0, sizeof(int32_t), s1) != cudaSuccess)
+                return MXQ_ERR_CUDA;
+            best.x = x;
+            best.s[0] = static_cast<const uint16_t*>(scales);
+            best.b[0] = static_cast<const uint16_t*>(biases);
+            best.y[0] = static_cast<__nv_bfloat16*>(y);
+            best.status = dev_status;
+            (void)best_rounds;
+            cudaError_t err = mxq::launch_skinny(best, w, nullptr, 1, (sms / best_s) * best_s, s1);
+            return err == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA;
+        }
+    }
     // enough tiles of at most 256 rows to fill every SM: the persistent
     // kernel (no K split; the next tile's loads overlap this tile's MMAs and
     // epilogue); otherwise the K split over thread-block clusters
@@ -243,31 +339,96 @@ size_t mxq_gather_workspace_bytes(int B, int E, int K, int N) {
     (void)N;
     if (B <= 0 || E <= 0 || K < 0) return 0;
     // tile table + count, then room for the activation rows in sorted order
-    return gather_table_bytes(B, E) + align_up((size_t)B * K * 2, 256);
+    // and (decode-sized calls) their per-group sums
+    size_t bytes = gather_table_bytes(B, E);
+    if (K > 0)
+        bytes += align_up((size_t)B * K * 2, 256) + align_up((size_t)B * skinny_xs_ld(K, 32) * 4, 256);
+    return bytes;
 }
 
-mxq_status mxq_gather_qmm(const void* x, const uint32_t* w, const void* scales,
-                          const void* biases, const int32_t* expert_ids, const int32_t* row_src,
-                          void* y, int T, int B, int E, int K, int N, int bits, int group_size,
-                          void* workspace, size_t workspace_bytes, int32_t* dev_status,
-                          void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The grouped call for one weight set, or for the gate/up pair (w1 != null:
+// a second set of the same shape, written to y1).
+mxq_status gather_call(const void* x, const uint32_t* w, const void* scales, const void* biases,
+                       const uint32_t* w1, const void* scales1, const void* biases1,
+                       const int32_t* expert_ids, const int32_t* row_src, void* y, void* y1, int T,
+                       int B, int E, int K, int N, int bits, int group_size, void* workspace,
+                       size_t workspace_bytes, int32_t* dev_status, void* stream) {
     mxq_status st = check_common(K, N, bits, group_size);
     if (st != MXQ_OK) return st;
     if (T <= 0 || B <= 0 || E <= 0) return MXQ_ERR_INVALID_ARG;
     if (!row_src && T != B) return MXQ_ERR_INVALID_ARG;
     if (!x || !w || !scales || !biases || !expert_ids || !y) return MXQ_ERR_INVALID_ARG;
+    const bool pair = w1 != nullptr;
+    if (pair && (!scales1 || !biases1 || !y1)) return MXQ_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 16) || !aligned(scales, 2) ||
         !aligned(biases, 2) || !aligned(expert_ids, 4) || !aligned(row_src, 4) ||
         !aligned(dev_status, 4) || !aligned(workspace, 256))
         return MXQ_ERR_MISALIGNED;
-    const size_t need = row_src ? mxq_gather_workspace_bytes(B, E, K, N) : gather_table_bytes(B, E);
+    if (pair && (!aligned(w1, 16) || !aligned(y1, 16) || !aligned(scales1, 2) ||
+                 !aligned(biases1, 2)))
+        return MXQ_ERR_MISALIGNED;
+    mxq::SkinnyParams sp;
+    const bool skinny = skinny_gather_plan(B, E, K, N, bits, group_size, pair ? 2 : 1, 0, sp);
+    const size_t need = mxq::gather_scratch_bytes(B, E, K, N, bits, group_size, row_src != nullptr);
     if (!workspace || workspace_bytes < need) return MXQ_ERR_WORKSPACE;
-    const size_t max_tiles = gather_max_tiles(B, E);
-    if (max_tiles > 65535) return MXQ_ERR_UNSUPPORTED;  // grid.y limit
+    if (gather_max_tiles(B, E) > 65535) return MXQ_ERR_UNSUPPORTED;  // grid.y limit
     int sms = 0;
     st = check_device(&sms);
     if (st != MXQ_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    auto* tiles = static_cast<mxq::MTile*>(workspace);
+    int* tile_count = reinterpret_cast<int*>(static_cast<char*>(workspace) +
+                                             align_up(gather_max_items(B, E) * sizeof(mxq::MTile), 256));
+    int* seg_start = tile_count + 256 / sizeof(int);
+    char* rows_area = static_cast<char*>(workspace) + gather_table_bytes(B, E);
+
+    if (skinny) {
+        // decode-sized: items of at most 8 rows of one expert, the routed rows
+        // reordered for the tensor-core fragments, then one launch streams
+        // every used expert's codes once per item (both sets of a pair
+        // against one copy of the rows)
+        cudaError_t err = mxq::launch_gather_prepass(expert_ids, row_src, T, B, E, N, kSkinnyRows,
+                                                     tiles, tile_count, seg_start, y,
+                                                     pair ? y1 : nullptr, dev_status, s);
+        if (err != cudaSuccess) return MXQ_ERR_CUDA;
+        void* xp = rows_area;
+        float* xsum = reinterpret_cast<float*>(rows_area + align_up((size_t)B * K * 2, 256));
+        const int xs_ld = (int)skinny_xs_ld(K, group_size);
+        err = mxq::launch_skinny_xprep(x, row_src, T, B, K, group_size, xs_ld, xp, xsum, s);
+        if (err != cudaSuccess) return MXQ_ERR_CUDA;
+        sp.x = xp;
+        sp.xsum = xsum;
+        sp.xs_ld = xs_ld;
+        sp.items = tiles;
+        sp.item_count = tile_count;
+        sp.s[0] = static_cast<const uint16_t*>(scales);
+        sp.b[0] = static_cast<const uint16_t*>(biases);
+        sp.y[0] = static_cast<__nv_bfloat16*>(y);
+        if (pair) {
+            sp.s[1] = static_cast<const uint16_t*>(scales1);
+            sp.b[1] = static_cast<const uint16_t*>(biases1);
+            sp.y[1] = static_cast<__nv_bfloat16*>(y1);
+        }
+        sp.status = dev_status;
+        sp.sb_estride = (long long)N * (K / group_size);
+        err = mxq::launch_skinny(sp, w, w1, E, sms, s);
+        return err == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA;
+    }
+    if (pair) {
+        // larger calls: the two projections as two grouped GEMMs (the tile
+        // table is rebuilt for the second; the status word collects both)
+        st = gather_call(x, w, scales, biases, nullptr, nullptr, nullptr, expert_ids, row_src, y,
+                         nullptr, T, B, E, K, N, bits, group_size, workspace, workspace_bytes,
+                         dev_status, stream);
+        if (st != MXQ_OK) return st;
+        return gather_call(x, w1, scales1, biases1, nullptr, nullptr, nullptr, expert_ids,
+                           row_src, y1, nullptr, T, B, E, K, N, bits, group_size, workspace,
+                           workspace_bytes, nullptr, stream);
+    }
     if (B <= kGatherDecodeRows) {
         if (dev_status && cudaMemsetAsync(dev_status, 0, sizeof(int32_t), s) != cudaSuccess)
             return MXQ_ERR_CUDA;
@@ -275,17 +436,14 @@ mxq_status mxq_gather_qmm(const void* x, const uint32_t* w, const void* scales,
                                                  B, E, K, N, bits, group_size, dev_status, s);
         return err == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA;
     }
-    auto* tiles = static_cast<mxq::MTile*>(workspace);
-    int* tile_count = reinterpret_cast<int*>(static_cast<char*>(workspace) +
-                                             align_up(max_tiles * sizeof(mxq::MTile), 256));
-    int* seg_start = tile_count + 256 / sizeof(int);
+    const size_t max_tiles = gather_max_tiles(B, E);
     cudaError_t err = mxq::launch_gather_prepass(expert_ids, row_src, T, B, E, N,
                                                  kGatherRowsPerTile, tiles, tile_count, seg_start,
-                                                 y, dev_status, s);
+                                                 y, nullptr, dev_status, s);
     if (err != cudaSuccess) return MXQ_ERR_CUDA;
     const void* xa = x;
     if (row_src) {
-        void* x_sorted = static_cast<char*>(workspace) + gather_table_bytes(B, E);
+        void* x_sorted = rows_area;
         err = mxq::launch_gather_rows(x, row_src, T, B, K, x_sorted, s);
         if (err != cudaSuccess) return MXQ_ERR_CUDA;
         xa = x_sorted;
@@ -326,6 +484,33 @@ mxq_status mxq_gather_qmm(const void* x, const uint32_t* w, const void* scales,
     }
     err = mxq::launch_qmm_tc(p, bits, (int)max_tiles, kGatherRowsPerTile, s);
     return err == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+mxq_status mxq_gather_qmm(const void* x, const uint32_t* w, const void* scales,
+                          const void* biases, const int32_t* expert_ids, const int32_t* row_src,
+                          void* y, int T, int B, int E, int K, int N, int bits, int group_size,
+                          void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                          void* stream) {
+    return gather_call(x, w, scales, biases, nullptr, nullptr, nullptr, expert_ids, row_src, y,
+                       nullptr, T, B, E, K, N, bits, group_size, workspace, workspace_bytes,
+                       dev_status, stream);
+}
+
+mxq_status mxq_gather_qmm_gateup(const void* x, const uint32_t* w_gate, const void* scales_gate,
+                                 const void* biases_gate, const uint32_t* w_up,
+                                 const void* scales_up, const void* biases_up,
+                                 const int32_t* expert_ids, const int32_t* row_src, void* y_gate,
+                                 void* y_up, int T, int B, int E, int K, int N, int bits,
+                                 int group_size, void* workspace, size_t workspace_bytes,
+                                 int32_t* dev_status, void* stream) {
+    if (!w_up) return MXQ_ERR_INVALID_ARG;
+    return gather_call(x, w_gate, scales_gate, biases_gate, w_up, scales_up, biases_up,
+                       expert_ids, row_src, y_gate, y_up, T, B, E, K, N, bits, group_size,
+                       workspace, workspace_bytes, dev_status, stream);
 }
 
 }  // extern "C"

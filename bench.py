@@ -601,11 +601,14 @@ def secondary_measurements(mxq, dev, stream, hbm, bf16_peak, Ws, clocks):
         s = dev_bf16(np.stack(sl), dev)
         b = dev_bf16(np.stack(bl), dev)
         copies = [(w, s, b), (w.clone(), s.clone(), b.clone())]
+        # the up projection's weights for the gate/up pair: two more copies,
+        # so that no launch finds either set in L2
+        ucopies = [(w.clone(), s.clone(), b.clone()) for _ in range(2)] if not ident else None
         expert_bytes = N * K * bits // 8 + N * (K // 64) * 4
-        wsz = torch.empty((mxq.gather_workspace_bytes(B, E, K if not ident else 0, N),),
-                          dtype=torch.uint8, device=dev)
+        wsz = torch.empty((mxq.gather_workspace_bytes(B, E, K, N),), dtype=torch.uint8,
+                          device=dev)
         # decode-sized calls on the same experts: a few tokens x top 8
-        for tokens in (4,):
+        for tokens in (4, 16, 64, 128):
             idsd, srcd = synth.routing(tokens, E, top_k, seed=3)
             Bd = idsd.shape[0]
             xd = dev_bf16(synth.activations(Bd if ident else tokens, K, seed=1), dev)
@@ -622,6 +625,19 @@ def secondary_measurements(mxq, dev, stream, hbm, bf16_peak, Ws, clocks):
             nbd = used * expert_bytes + xd.numel() * 2 + Bd * N * 2
             out.append(entry("gather decode T=%d B=%d K=%d N=%d b4" % (tokens, Bd, K, N), td, nbd,
                              0.0, m0, {"experts": used}))
+            if not ident:
+                # the gate/up pair on the same routing: a second expert set
+                yu = torch.empty((Bd, N), dtype=torch.bfloat16, device=dev)
+                fng = lambda i: mxq.gather_qmm_gateup(  # noqa: E731
+                    xd, *copies[i % 2], *ucopies[i % 2], idsd_d, srcd_d, bits, out_gate=yd,
+                    out_up=yu, workspace=wsz)
+                for i in range(5):
+                    fng(i)
+                m0 = clocks.mark()
+                tg, _ = time_launches(fng, iters, stream)
+                nbg = 2 * used * expert_bytes + xd.numel() * 2 + 2 * Bd * N * 2
+                out.append(entry("gateup decode T=%d B=%d K=%d N=%d b4" % (tokens, Bd, K, N), tg,
+                                 nbg, 0.0, m0, {"experts": used}))
         Tx = B if ident else T
         x = dev_bf16(synth.activations(Tx, K, seed=1), dev)
         ids_d = torch.from_numpy(ids).to(dev)
@@ -636,7 +652,7 @@ def secondary_measurements(mxq, dev, stream, hbm, bf16_peak, Ws, clocks):
         nbytes = E * expert_bytes + Tx * K * 2 + B * N * 2
         north.append(entry("gather_qmm E=128 top8 T=573 B=%d K=%d N=%d b4 g64" % (B, K, N), t,
                            nbytes, 2.0 * B * K * N, m0, {"tok_s": int(T / t)}))
-        del w, s, b, copies, x, y
+        del w, s, b, copies, ucopies, x, y
         torch.cuda.empty_cache()
 
     # ---- spec configurations: M sweep at K=N=5120, the 4/8-bit pair,
