@@ -311,9 +311,8 @@ def quantize(w, bits: int, codes=None, scales=None, biases=None, stream=None,
 
 
 def gather_workspace_bytes(B: int, E: int, K: int, N: int) -> int:
-    """Workspace bytes that always suffice for gather_qmm and
-    gather_qmm_gateup (K = 0: the tile table alone, enough for calls with
-    more than 8 * E rows and no row_src)."""
+    """Workspace bytes for gather_qmm and gather_qmm_gateup; pass K = 0 when
+    row_src is None."""
     return int(lib().mxq_gather_workspace_bytes(B, E, K, N))
 
 
@@ -379,8 +378,8 @@ def gather_qmm(x, w, scales, biases, expert_ids, row_src, bits: int, out=None, w
         out = torch.empty((B, N), dtype=torch.bfloat16, device=x.device)
     _require(out, "out", (torch.bfloat16,), x.device)
     if workspace is None:
-        workspace = torch.empty((gather_workspace_bytes(B, E, K, N),), dtype=torch.uint8,
-                                device=x.device)
+        workspace = torch.empty((gather_workspace_bytes(B, E, K if row_src is not None else 0, N),),
+                                dtype=torch.uint8, device=x.device)
     _require(workspace, "workspace", (torch.uint8,), x.device)
     if dev_status is not None:
         _require(dev_status, "dev_status", (torch.int32,), x.device)
@@ -426,8 +425,8 @@ def gather_qmm_gateup(x, w_gate, s_gate, b_gate, w_up, s_up, b_up, expert_ids, r
             raise ValueError("%s has shape %s, expected %s" % (name, tuple(o.shape), (B, N)))
         outs.append(o)
     if workspace is None:
-        workspace = torch.empty((gather_workspace_bytes(B, E, K, N),), dtype=torch.uint8,
-                                device=x.device)
+        workspace = torch.empty((gather_workspace_bytes(B, E, K if row_src is not None else 0, N),),
+                                dtype=torch.uint8, device=x.device)
     _require(workspace, "workspace", (torch.uint8,), x.device)
     if dev_status is not None:
         _require(dev_status, "dev_status", (torch.int32,), x.device)

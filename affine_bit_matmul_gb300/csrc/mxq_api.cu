@@ -93,41 +93,13 @@ DensePlan plan_dense(int M, int K, int N, int bits, int sms) {
     return pl;
 }
 
-// Activation rows per item of the skinny kernel (decode-sized grouped calls).
-constexpr int kSkinnyRows = 8;
-
 // Tiles of the grouped tensor-core GEMM (at most 64 rows each), an upper bound.
 size_t gather_max_tiles(int B, int E) { return (size_t)B / kGatherRowsPerTile + (size_t)E + 1; }
-// Items of the skinny kernel (at most 8 rows each), an upper bound; the
-// table is sized for the larger of the two.
-size_t gather_max_items(int B, int E) { return (size_t)B / kSkinnyRows + (size_t)E + 1; }
 
 // Tile records, the tile count, each expert's first row; 256-byte aligned.
 size_t gather_table_bytes(int B, int E) {
-    return align_up(gather_max_items(B, E) * sizeof(mxq::MTile), 256) + 256 +
+    return align_up(gather_max_tiles(B, E) * sizeof(mxq::MTile), 256) + 256 +
            align_up(((size_t)E + 1) * sizeof(int), 256);
-}
-
-// Floats per row of the skinny kernel's group sums (groups of 32: the most).
-size_t skinny_xs_ld(int K, int group) { return ((size_t)(K / group) + 3) & ~(size_t)3; }
-
-// Skinny plan for a grouped call (no K split); false if it does not apply.
-bool skinny_gather_plan(int B, int E, int K, int N, int bits, int group, int sets, int sms,
-                        mxq::SkinnyParams& sp) {
-    if (bits != 4 || B > kSkinnyRows * E) return false;
-    if (check_common(K, N, bits, group) != MXQ_OK) return false;
-    std::memset(&sp, 0, sizeof sp);
-    sp.sets = sets;
-    sp.K = K;
-    sp.N = N;
-    sp.group = group;
-    sp.kc = K;
-    sp.S = 1;
-    sp.slabs = (N + 15) / 16;
-    sp.xslots = 2;
-    sp.slot_rows = kSkinnyRows;
-    (void)sms;
-    return mxq::plan_skinny(sp, 0);
 }
 
 }  // namespace
@@ -136,9 +108,9 @@ mxq_status mxq::check_current_device(int* sms) { return check_device(sms); }
 
 size_t mxq::gather_scratch_bytes(int B, int E, int K, int N, int bits, int group_size,
                                  bool has_row_src) {
-    mxq::SkinnyParams sp;
-    if (skinny_gather_plan(B, E, K, N, bits, group_size, 1, 0, sp))
-        return mxq_gather_workspace_bytes(B, E, K, N);  // sorted rows and their group sums
+    (void)N;
+    (void)bits;
+    (void)group_size;
     if (has_row_src) return gather_table_bytes(B, E) + align_up((size_t)B * K * 2, 256);
     return gather_table_bytes(B, E);
 }
@@ -203,55 +175,6 @@ mxq_status mxq_qmm(const void* x, const uint32_t* w, const void* scales, const v
             mxq::launch_qmv(x, w, scales, biases, y, K, N, bits, group_size, sms, dev_status, s1);
         return err == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA;
     }
-    if (bits == 4 && M <= kSkinnyRows) {
-        // a few rows: the skinny kernel streams the codes once for all of
-        // them; K is split over a cluster of S CTAs so that the 16-row slabs
-        // spread evenly over the SMs (the cheapest S by slabs per CTA times
-        // k per CTA, plus a per-slab overhead)
-        mxq::SkinnyParams sp;
-        const int slabs = (N + 15) / 16;
-        int best_s = 0, best_rounds = 0;
-        long long best_cost = 0;
-        mxq::SkinnyParams best;
-        for (int S = 1; S <= 8; ++S) {
-            if (K % (S * 256) != 0) continue;
-            const int C = sms / S;
-            if (C < 1) continue;
-            const int rounds = (slabs + C - 1) / C;
-            const long long cost = (long long)rounds * (K / S + 512);
-            std::memset(&sp, 0, sizeof sp);
-            sp.sets = 1;
-            sp.M = M;
-            sp.K = K;
-            sp.N = N;
-            sp.group = group_size;
-            sp.kc = K / S;
-            sp.S = S;
-            sp.slabs = slabs;
-            sp.xslots = 1;
-            sp.slot_rows = M;
-            if (!mxq::plan_skinny(sp, rounds)) continue;
-            if (best_s == 0 || cost < best_cost) {
-                best_s = S;
-                best_cost = cost;
-                best_rounds = rounds;
-                best = sp;
-            }
-        }
-        if (best_s > 0) {
-            cudaStream_t s1 = static_cast<cudaStream_t>(stream);
-            if (dev_status && cudaMemsetAsync(dev_status, 0, sizeof(int32_t), s1) != cudaSuccess)
-                return MXQ_ERR_CUDA;
-            best.x = x;
-            best.s[0] = static_cast<const uint16_t*>(scales);
-            best.b[0] = static_cast<const uint16_t*>(biases);
-            best.y[0] = static_cast<__nv_bfloat16*>(y);
-            best.status = dev_status;
-            (void)best_rounds;
-            cudaError_t err = mxq::launch_skinny(best, w, nullptr, 1, (sms / best_s) * best_s, s1);
-            return err == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA;
-        }
-    }
     // enough tiles of at most 256 rows to fill every SM: the persistent
     // kernel (no K split; the next tile's loads overlap this tile's MMAs and
     // epilogue); otherwise the K split over thread-block clusters
@@ -278,6 +201,7 @@ mxq_status mxq_qmm(const void* x, const uint32_t* w, const void* scales, const v
     p.K = K;
     p.N = N;
     p.group = group_size;
+    p.sets = 1;
     p.x_rows = M;
     p.x_box_rows = pl.m_tile;
     p.m_tile = pl.m_tile;
@@ -339,11 +263,7 @@ size_t mxq_gather_workspace_bytes(int B, int E, int K, int N) {
     (void)N;
     if (B <= 0 || E <= 0 || K < 0) return 0;
     // tile table + count, then room for the activation rows in sorted order
-    // and (decode-sized calls) their per-group sums
-    size_t bytes = gather_table_bytes(B, E);
-    if (K > 0)
-        bytes += align_up((size_t)B * K * 2, 256) + align_up((size_t)B * skinny_xs_ld(K, 32) * 4, 256);
-    return bytes;
+    return gather_table_bytes(B, E) + align_up((size_t)B * K * 2, 256);
 }
 
 }  // extern "C"
@@ -371,8 +291,6 @@ mxq_status gather_call(const void* x, const uint32_t* w, const void* scales, con
     if (pair && (!aligned(w1, 16) || !aligned(y1, 16) || !aligned(scales1, 2) ||
                  !aligned(biases1, 2)))
         return MXQ_ERR_MISALIGNED;
-    mxq::SkinnyParams sp;
-    const bool skinny = skinny_gather_plan(B, E, K, N, bits, group_size, pair ? 2 : 1, 0, sp);
     const size_t need = mxq::gather_scratch_bytes(B, E, K, N, bits, group_size, row_src != nullptr);
     if (!workspace || workspace_bytes < need) return MXQ_ERR_WORKSPACE;
     if (gather_max_tiles(B, E) > 65535) return MXQ_ERR_UNSUPPORTED;  // grid.y limit
@@ -380,66 +298,26 @@ mxq_status gather_call(const void* x, const uint32_t* w, const void* scales, con
     st = check_device(&sms);
     if (st != MXQ_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    auto* tiles = static_cast<mxq::MTile*>(workspace);
-    int* tile_count = reinterpret_cast<int*>(static_cast<char*>(workspace) +
-                                             align_up(gather_max_items(B, E) * sizeof(mxq::MTile), 256));
-    int* seg_start = tile_count + 256 / sizeof(int);
-    char* rows_area = static_cast<char*>(workspace) + gather_table_bytes(B, E);
-
-    if (skinny) {
-        // decode-sized: items of at most 8 rows of one expert, the routed rows
-        // reordered for the tensor-core fragments, then one launch streams
-        // every used expert's codes once per item (both sets of a pair
-        // against one copy of the rows)
-        cudaError_t err = mxq::launch_gather_prepass(expert_ids, row_src, T, B, E, N, kSkinnyRows,
-                                                     tiles, tile_count, seg_start, y,
-                                                     pair ? y1 : nullptr, dev_status, s);
-        if (err != cudaSuccess) return MXQ_ERR_CUDA;
-        void* xp = rows_area;
-        float* xsum = reinterpret_cast<float*>(rows_area + align_up((size_t)B * K * 2, 256));
-        const int xs_ld = (int)skinny_xs_ld(K, group_size);
-        err = mxq::launch_skinny_xprep(x, row_src, T, B, K, group_size, xs_ld, xp, xsum, s);
-        if (err != cudaSuccess) return MXQ_ERR_CUDA;
-        sp.x = xp;
-        sp.xsum = xsum;
-        sp.xs_ld = xs_ld;
-        sp.items = tiles;
-        sp.item_count = tile_count;
-        sp.s[0] = static_cast<const uint16_t*>(scales);
-        sp.b[0] = static_cast<const uint16_t*>(biases);
-        sp.y[0] = static_cast<__nv_bfloat16*>(y);
-        if (pair) {
-            sp.s[1] = static_cast<const uint16_t*>(scales1);
-            sp.b[1] = static_cast<const uint16_t*>(biases1);
-            sp.y[1] = static_cast<__nv_bfloat16*>(y1);
-        }
-        sp.status = dev_status;
-        sp.sb_estride = (long long)N * (K / group_size);
-        err = mxq::launch_skinny(sp, w, w1, E, sms, s);
-        return err == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA;
-    }
-    if (pair) {
-        // larger calls: the two projections as two grouped GEMMs (the tile
-        // table is rebuilt for the second; the status word collects both)
-        st = gather_call(x, w, scales, biases, nullptr, nullptr, nullptr, expert_ids, row_src, y,
-                         nullptr, T, B, E, K, N, bits, group_size, workspace, workspace_bytes,
-                         dev_status, stream);
-        if (st != MXQ_OK) return st;
-        return gather_call(x, w1, scales1, biases1, nullptr, nullptr, nullptr, expert_ids,
-                           row_src, y1, nullptr, T, B, E, K, N, bits, group_size, workspace,
-                           workspace_bytes, nullptr, stream);
-    }
+    const int sets = pair ? 2 : 1;
     if (B <= kGatherDecodeRows) {
+        // a decode step: one GEMV per sorted row (and weight set) against its
+        // expert's matrix, no tile table
         if (dev_status && cudaMemsetAsync(dev_status, 0, sizeof(int32_t), s) != cudaSuccess)
             return MXQ_ERR_CUDA;
-        cudaError_t err = mxq::launch_gather_qmv(x, w, scales, biases, expert_ids, row_src, y, T,
-                                                 B, E, K, N, bits, group_size, dev_status, s);
+        cudaError_t err = mxq::launch_gather_qmv(x, w, scales, biases, w1, scales1, biases1,
+                                                 expert_ids, row_src, y, y1, sets, T, B, E, K, N,
+                                                 bits, group_size, dev_status, s);
         return err == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA;
     }
+    auto* tiles = static_cast<mxq::MTile*>(workspace);
+    int* tile_count = reinterpret_cast<int*>(static_cast<char*>(workspace) +
+                                             align_up(gather_max_tiles(B, E) * sizeof(mxq::MTile), 256));
+    int* seg_start = tile_count + 256 / sizeof(int);
+    char* rows_area = static_cast<char*>(workspace) + gather_table_bytes(B, E);
     const size_t max_tiles = gather_max_tiles(B, E);
     cudaError_t err = mxq::launch_gather_prepass(expert_ids, row_src, T, B, E, N,
                                                  kGatherRowsPerTile, tiles, tile_count, seg_start,
-                                                 y, nullptr, dev_status, s);
+                                                 y, pair ? y1 : nullptr, dev_status, s);
     if (err != cudaSuccess) return MXQ_ERR_CUDA;
     const void* xa = x;
     if (row_src) {
@@ -472,12 +350,19 @@ mxq_status gather_call(const void* x, const uint32_t* w, const void* scales, con
     p.kb_per_split = K / 64;
     p.w_expert_stride = (long long)N * K * bits / 32;
     p.sb_expert_stride = (long long)N * (K / group_size);
-    // 2- and 4-bit: two persistent CTAs per SM take tiles of (tile list) x
-    // (n tiles) from a counter as they finish the previous one, so the
-    // pipeline fills once per CTA and long and short tiles balance; 3-, 6-
-    // and 8-bit (code slots too large for two CTAs per SM): one CTA per tile
+    // the gate/up pair: a second weight set and output, same tiles
+    p.sets = sets;
+    p.w1 = w1;
+    p.scales1 = static_cast<const uint16_t*>(scales1);
+    p.biases1 = static_cast<const uint16_t*>(biases1);
+    p.y1 = y1;
+    // 2- and 4-bit: two persistent CTAs per SM take tiles of (weight set) x
+    // (tile list) x (n tiles) from a counter as they finish the previous one,
+    // so the pipeline fills once per CTA and long and short tiles balance;
+    // 3-, 6- and 8-bit (code slots too large for two CTAs per SM): one CTA
+    // per tile and weight set
     if (bits == 2 || bits == 4) {
-        const long long bound = (long long)max_tiles * ((N + 127) / 128);
+        const long long bound = (long long)max_tiles * ((N + 127) / 128) * sets;
         p.persistent = 1;
         p.grid_ctas = (int)(bound < 2LL * sms ? bound : 2LL * sms);
         p.tile_counter = tile_count + 1;  // tiles handed out as CTAs free up

@@ -16,10 +16,8 @@ namespace mxq {
 // cannot say.  Cached per device.
 mxq_status check_current_device(int* sms);
 
-// Scratch bytes a grouped call with these arguments uses (at most
-// mxq_gather_workspace_bytes(B, E, K, N)): the tile table, plus the routed
-// rows in sorted order when row_src is given, plus (decode-sized calls,
-// which run the skinny kernel) the reordered rows and their group sums.
+// Scratch bytes a grouped call with these arguments needs: the tile table,
+// plus the routed rows in sorted order when row_src is given.
 size_t gather_scratch_bytes(int B, int E, int K, int N, int bits, int group_size,
                             bool has_row_src);
 
@@ -60,6 +58,13 @@ struct QmmParams {
     int grid_ctas;           // persistent form: CTAs launched
     int* tile_counter;       // persistent form: next unclaimed tile (zeroed before the
                              // launch), or null for a fixed gridDim.x stride
+    // grouped form, gate/up pair: a second weight set of the same shape and
+    // its output (sets = 2); the tiles of both sets share the activation rows
+    int sets;                // 1 or 2
+    const uint32_t* w1;
+    const uint16_t* scales1;
+    const uint16_t* biases1;
+    void* y1;
 };
 
 // cuTensorMapEncodeTiled, looked up once through the runtime (null if the
@@ -91,12 +96,15 @@ cudaError_t launch_gather_prepass(const int32_t* expert_ids, const int32_t* row_
                                   int* tile_count, int* seg_start, void* y, void* y2,
                                   int32_t* status, cudaStream_t stream);
 
-// Grouped form with few rows (decode): one GEMV per sorted row against its
-// expert's matrix, validating the ids itself (no tile table, no row copy).
+// Grouped form with few rows (decode): one GEMV per sorted row (and weight
+// set: sets = 2 adds w1, scales1, biases1 -> y1) against its expert's
+// matrix, validating the ids itself (no tile table, no row copy).
 cudaError_t launch_gather_qmv(const void* x, const uint32_t* w, const void* scales,
-                              const void* biases, const int32_t* expert_ids,
-                              const int32_t* row_src, void* y, int T, int B, int E, int K, int N,
-                              int bits, int group, int32_t* status, cudaStream_t stream);
+                              const void* biases, const uint32_t* w1, const void* scales1,
+                              const void* biases1, const int32_t* expert_ids,
+                              const int32_t* row_src, void* y, void* y1, int sets, int T, int B,
+                              int E, int K, int N, int bits, int group, int32_t* status,
+                              cudaStream_t stream);
 
 // Affine group-wise encoder (groups of 32, 64 or 128): float [N, K] ->
 // codes, bf16 scales and biases.
@@ -107,44 +115,6 @@ cudaError_t launch_quantize(const float* W, uint32_t* codes, void* scales, void*
 cudaError_t launch_qmv_kn(const void* x, const uint32_t* w, const void* scales, const void* biases,
                           void* y, int K, int N, int bits, int group, int sms,
                           cudaStream_t stream);
-
-// Arguments of the skinny kernel (host-filled, passed by value).
-struct SkinnyParams {
-    const void* x;           // dense: bf16 [M, K]; grouped: prepared rows bf16 [B, K]
-                             // (every 8 values reordered 0,4,1,5,2,6,3,7)
-    const float* xsum;       // grouped: per-group sums [B, xs_ld]; dense: null
-    int xs_ld;               // floats per row of xsum
-    const MTile* items;      // grouped: items of <= 8 rows of one expert; dense: null
-    const int* item_count;   // grouped: number of items (device)
-    const uint16_t* s[2];    // scales of the (one or two) weight sets
-    const uint16_t* b[2];    // biases
-    __nv_bfloat16* y[2];     // outputs
-    int32_t* status;
-    int sets;                // 1, or 2 (gate and up projections)
-    int M;                   // dense: activation rows (<= 8)
-    int K, N, group;
-    int kc;                  // K per CTA of a cluster
-    int S;                   // cluster size (K split)
-    int slabs;               // 16-row slabs of W = ceil(N / 16)
-    long long sb_estride;    // scale/bias entries between experts
-    // shared-memory layout
-    int slot_rows;           // activation rows per slot: M (dense) or 8 (grouped)
-    int stages, nbox, stage_bytes, xslots, xstride, xs_row, gpw;
-    int x_off, xs_off, sb_off, red_off, part_off, bar_off, part_tasks;
-};
-
-// Skinny-kernel plan: fills the stage count and shared-memory offsets of p
-// (K split p.S, p.kc, p.sets, p.xslots set by the caller); false if the
-// shape does not fit.  part_tasks: tasks per CTA when p.S > 1.
-bool plan_skinny(SkinnyParams& p, int part_tasks);
-size_t skinny_smem_bytes(const SkinnyParams& p);
-// 4-bit codes; w0 (and w1 when p.sets == 2) [E, N, K/8] (E = 1: dense).
-cudaError_t launch_skinny(const SkinnyParams& p, const uint32_t* w0, const uint32_t* w1, int E,
-                          int grid, cudaStream_t stream);
-// Grouped form: routed rows in sorted order, reordered for the skinny
-// kernel, and their per-group sums (xs_ld floats per row).
-cudaError_t launch_skinny_xprep(const void* x, const int32_t* row_src, int T, int B, int K,
-                                int group, int xs_ld, void* xp, float* xsum, cudaStream_t stream);
 
 cudaError_t launch_gather_rows(const void* x, const int32_t* row_src, int T, int B, int K,
                                void* x_sorted, cudaStream_t stream);

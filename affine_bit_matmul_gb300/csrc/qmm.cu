@@ -409,8 +409,9 @@ __device__ __forceinline__ void flag_status(int32_t* status, int bits) {
 
 template <int BITS, bool GATHER, int GROUP>
 __global__ void __launch_bounds__(kThreads, 1)
-    qmm_tc_kernel(const QmmParams p, int max_rows, const __grid_constant__ CUtensorMap code_map,
-                  const __grid_constant__ CUtensorMap x_map) {
+    qmm_tc_kernel(const QmmParams p, int max_rows, const __grid_constant__ CUtensorMap code_map0,
+                  const __grid_constant__ CUtensorMap x_map,
+                  const __grid_constant__ CUtensorMap code_map1) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const SmemLayout L = make_layout(max_rows, false, slot_row_bytes(BITS));
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -445,7 +446,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_mma = (rows + 15) & ~15;
     const int n0 = blockIdx.x * kTileN;
     const int KB = p.K / kHalfK;                       // 64-wide blocks
-    const int kb_begin = blockIdx.z * p.kb_per_split;  // in 64-wide blocks
+    // grid z: the K split (dense form) or the weight set (grouped form: the
+    // gate/up pair's second set in z = 1)
+    const int set = GATHER ? (int)blockIdx.z : 0;
+    const CUtensorMap& code_map = set ? code_map1 : code_map0;
+    const uint16_t* const set_scales = set ? p.scales1 : p.scales;
+    const uint16_t* const set_biases = set ? p.biases1 : p.biases;
+    void* const set_y = set ? p.y1 : p.y;
+    const int kb_begin = (GATHER ? 0 : (int)blockIdx.z) * p.kb_per_split;  // in 64-wide blocks
     const int nkb = min(KB, kb_begin + p.kb_per_split) - kb_begin;
     const int nst = (nkb + 1) / 2;                     // 128-wide stages
     const int groups = p.K / GROUP;
@@ -585,8 +593,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int grp = warp >> 2;
         const int n = n0 + r;
         const bool row_ok = n < p.N;
-        const uint16_t* srow = p.scales + (long long)e * p.sb_expert_stride + (long long)n * groups;
-        const uint16_t* brow = p.biases + (long long)e * p.sb_expert_stride + (long long)n * groups;
+        const uint16_t* srow = set_scales + (long long)e * p.sb_expert_stride + (long long)n * groups;
+        const uint16_t* brow = set_biases + (long long)e * p.sb_expert_stride + (long long)n * groups;
         constexpr int kRowBytes = kBK * BITS / 8;  // codes of one row per stage
         // this warp's 32 TMEM lanes
         const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
@@ -729,7 +737,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ny = n0 + lane_row;
         const bool y_ok = ny < p.N;
         const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
-        __nv_bfloat16* y = static_cast<__nv_bfloat16*>(p.y);
+        __nv_bfloat16* y = static_cast<__nv_bfloat16*>(set_y);
         if (p.splits == 1) {
             for (int c0 = colhalf * 16; c0 < n_mma; c0 += 32) {
                 uint32_t v[16];
@@ -775,7 +783,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int c4 = (threadIdx.x & 31) * 4;
             const int ph = threadIdx.x >> 5;
             const int n_out = n0 + c4;
-            __nv_bfloat16* y = static_cast<__nv_bfloat16*>(p.y);
+            __nv_bfloat16* y = static_cast<__nv_bfloat16*>(set_y);
             const bool vec_ok = (p.N % 4 == 0) && (n_out + 3 < p.N);
             for (int m0 = rank + S * ph; m0 < rows; m0 += S * kDequantWarps * 4) {
                 float4 acc[4];
@@ -860,13 +868,22 @@ constexpr int kPBarBytes = 64 + kTQ * 20;  // accfull[2], accempty[2], done, tme
                                            // tile queue (ids, full and empty barriers)
 
 struct PTile {
-    int e, row_start, rows, n0, n_mma;
+    int e, row_start, rows, n0, n_mma, set;
 };
 
+// Tile t of the sequence.  Grouped form: tiles of set 0 (all row tiles x n
+// tiles), then those of set 1 (the gate/up pair's second weight set);
+// per_set = row tiles x n tiles.
 template <bool GATHER>
-__device__ __forceinline__ PTile ptile(const QmmParams& p, int t, int m_tiles, int n_tiles) {
+__device__ __forceinline__ PTile ptile(const QmmParams& p, int t, int m_tiles, int n_tiles,
+                                       int per_set = 0) {
     PTile r;
     int nt;
+    r.set = 0;
+    if (GATHER && per_set > 0 && t >= per_set) {
+        r.set = 1;
+        t -= per_set;
+    }
     if (GATHER) {
         const int lt = t / n_tiles;  // tile of rows (one expert); its n tiles run side by side
         nt = t - lt * n_tiles;
@@ -955,7 +972,8 @@ template <int BITS, bool GATHER, bool COMPACT, int GROUP>
 __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 1)
     qmm_persistent_kernel(const QmmParams p, int max_rows, int m_tiles, int n_tiles,
                           const __grid_constant__ CUtensorMap code_map,
-                          const __grid_constant__ CUtensorMap x_map) {
+                          const __grid_constant__ CUtensorMap x_map,
+                          const __grid_constant__ CUtensorMap code_map1) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const SmemLayout L = make_layout(max_rows, COMPACT, slot_row_bytes(BITS));
     constexpr int kCols = COMPACT ? kCompactTmemCols : kTmemCols;
@@ -981,7 +999,9 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
 
     const int warp = threadIdx.x >> 5;
     const int lane = lane_id();
-    const int total = GATHER ? (*p.tile_count) * n_tiles : m_tiles * n_tiles;
+    // grouped form: tiles of each weight set (the gate/up pair has two)
+    const int per_set = GATHER ? (*p.tile_count) * n_tiles : 0;
+    const int total = GATHER ? per_set * p.sets : m_tiles * n_tiles;
     const int KB = p.K / kHalfK;              // 64-wide blocks
     const int nst = (KB + 1) / 2;             // 128-wide stages per tile
     constexpr int kSPS = slot_row_bytes(BITS) / (kBK * BITS / 8);  // stages per code slot
@@ -1086,7 +1106,7 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
                 break;
             }
             if (t >= total) break;
-            const PTile ti = ptile<GATHER>(p, t, m_tiles, n_tiles);
+            const PTile ti = ptile<GATHER>(p, t, m_tiles, n_tiles, per_set);
             for (int j = 0; j < nslots; ++j, ring.next(), ++issued) {
                 if (issued >= SC && !warp_wait_ab(&cempty[ring.slot], ring.parity ^ 1, abort_flag)) {
                     ok = false;
@@ -1099,8 +1119,8 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
                     const uint32_t dst = c_base0 + ring.slot * L.c_bytes;
                     for (int b = 0; b < nbox; ++b) {
                         if (GATHER)
-                            tma_load_3d(dst + b * kCodeBoxBytes, &code_map, c0 + b * kWordsPerBox,
-                                        ti.n0, ti.e, &cfull[ring.slot]);
+                            tma_load_3d(dst + b * kCodeBoxBytes, ti.set ? &code_map1 : &code_map,
+                                        c0 + b * kWordsPerBox, ti.n0, ti.e, &cfull[ring.slot]);
                         else
                             tma_load_2d(dst + b * kCodeBoxBytes, &code_map, c0 + b * kWordsPerBox,
                                         ti.n0, &cfull[ring.slot]);
@@ -1121,7 +1141,7 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
                 break;
             }
             if (t >= total) break;
-            const PTile ti = ptile<GATHER>(p, t, m_tiles, n_tiles);
+            const PTile ti = ptile<GATHER>(p, t, m_tiles, n_tiles, per_set);
             const int boxes = (ti.n_mma + p.x_box_rows - 1) / p.x_box_rows;
             const uint32_t x_bytes_in = (uint32_t)(boxes * p.x_box_rows * 128);
             for (int q = 0; q < KB; ++q, ring.next(), ++issued) {
@@ -1149,7 +1169,7 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
                 break;
             }
             if (t >= total) break;
-            const PTile ti = ptile<GATHER>(p, t, m_tiles, n_tiles);
+            const PTile ti = ptile<GATHER>(p, t, m_tiles, n_tiles, per_set);
             const int buf = acc_bufs == 2 ? (i & 1) : 0;
             const int use = acc_bufs == 2 ? (i >> 1) : i;  // earlier tiles on this buffer
             if (use > 0 && !warp_wait_ab(&accempty[buf], (uint32_t)((use - 1) & 1), abort_flag)) {
@@ -1213,7 +1233,7 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
                 break;
             }
             if (t >= total) break;
-            const PTile ti = ptile<GATHER>(p, t, m_tiles, n_tiles);
+            const PTile ti = ptile<GATHER>(p, t, m_tiles, n_tiles, per_set);
             const int buf = acc_bufs == 2 ? (i & 1) : 0;
             const int use = acc_bufs == 2 ? (i >> 1) : i;
             if (!warp_wait_ab(&accfull[buf], (uint32_t)(use & 1), abort_flag)) {
@@ -1266,11 +1286,13 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
                 break;
             }
             if (t >= total) break;
-            const PTile ti = ptile<GATHER>(p, t, m_tiles, n_tiles);
+            const PTile ti = ptile<GATHER>(p, t, m_tiles, n_tiles, per_set);
             const int n = ti.n0 + r;
             const bool row_ok = n < p.N;
-            const uint16_t* srow = p.scales + (long long)ti.e * p.sb_expert_stride + (long long)n * groups;
-            const uint16_t* brow = p.biases + (long long)ti.e * p.sb_expert_stride + (long long)n * groups;
+            const uint16_t* srow = (ti.set ? p.scales1 : p.scales) + (long long)ti.e * p.sb_expert_stride +
+                                   (long long)n * groups;
+            const uint16_t* brow = (ti.set ? p.biases1 : p.biases) + (long long)ti.e * p.sb_expert_stride +
+                                   (long long)n * groups;
             const int s0 = (int)((grp + g0) & 1);
             int csub = s0;  // stage within the code slot (kSPS >= 2, so s0 < kSPS)
             // scales then biases of a stage's pairs: {s_0 .. s_kP-1, b_0 .. b_kP-1}
@@ -1417,7 +1439,7 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
                 const int ny = ti.n0 + quarter * 32 + lane;
                 const bool y_ok = ny < p.N;
                 const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
-                __nv_bfloat16* y = static_cast<__nv_bfloat16*>(p.y);
+                __nv_bfloat16* y = static_cast<__nv_bfloat16*>(ti.set ? p.y1 : p.y);
                 for (int c0 = colhalf * 16; c0 < ti.n_mma; c0 += 32) {
                     uint32_t v[16];
                     tmem_ld16(taddr + c0, v);
@@ -1452,7 +1474,7 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
 template <int BITS, bool GATHER, bool COMPACT, int GROUP>
 cudaError_t launch_persistent(const QmmParams& p, int max_rows, int m_tiles, int n_tiles,
                               int grid, const CUtensorMap& cm, const CUtensorMap& xm,
-                              cudaStream_t stream) {
+                              const CUtensorMap& cm1, cudaStream_t stream) {
     const SmemLayout L = make_layout(max_rows, COMPACT, slot_row_bytes(BITS));
     const int smem = L.total + kPBarBytes;
     static bool attr_set[64] = {};
@@ -1469,7 +1491,7 @@ cudaError_t launch_persistent(const QmmParams& p, int max_rows, int m_tiles, int
     if (smem > 232448) return cudaErrorInvalidConfiguration;
     qmm_persistent_kernel<BITS, GATHER, COMPACT, GROUP>
         <<<grid, COMPACT ? kThreads : kPThreads, smem, stream>>>(p, max_rows, m_tiles, n_tiles, cm,
-                                                                 xm);
+                                                                 xm, cm1);
     return cudaGetLastError();
 }
 
@@ -1479,7 +1501,7 @@ EncodeTiledFn encode_fn() { return tensor_map_encoder(); }
 
 template <int BITS, bool GATHER, int GROUP>
 cudaError_t launch_variant(const QmmParams& p, int grid_m, int max_rows, const CUtensorMap& cm,
-                           const CUtensorMap& xm, cudaStream_t stream) {
+                           const CUtensorMap& xm, const CUtensorMap& cm1, cudaStream_t stream) {
     const SmemLayout L = make_layout(max_rows, false, slot_row_bytes(BITS));
     // the shared-memory opt-in is per device; do it once each
     static bool attr_set[64] = {};
@@ -1494,7 +1516,8 @@ cudaError_t launch_variant(const QmmParams& p, int grid_m, int max_rows, const C
         attr_set[dev] = true;
     }
     if (L.total > 232448) return cudaErrorInvalidConfiguration;  // cannot happen for rows <= 256
-    const dim3 grid((p.N + kTileN - 1) / kTileN, grid_m, p.splits);
+    // z: the K splits (dense form, a cluster) or the weight sets (grouped form)
+    const dim3 grid((p.N + kTileN - 1) / kTileN, grid_m, GATHER ? (p.sets > 1 ? p.sets : 1) : p.splits);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads);
@@ -1507,7 +1530,8 @@ cudaError_t launch_variant(const QmmParams& p, int grid_m, int max_rows, const C
     attr[0].val.clusterDim.z = p.splits;  // the K splits of one tile form a cluster
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t err = cudaLaunchKernelEx(&cfg, qmm_tc_kernel<BITS, GATHER, GROUP>, p, max_rows, cm, xm);
+    cudaError_t err = cudaLaunchKernelEx(&cfg, qmm_tc_kernel<BITS, GATHER, GROUP>, p, max_rows, cm, xm,
+                                         cm1);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
@@ -1518,49 +1542,49 @@ cudaError_t launch_variant(const QmmParams& p, int grid_m, int max_rows, const C
 template <int GROUP>
 cudaError_t launch_group(const QmmParams& p, int bits, bool gather, int grid_m,
                          int max_rows_per_tile, const CUtensorMap& cm, const CUtensorMap& xm,
-                         cudaStream_t stream) {
+                         const CUtensorMap& cm1, cudaStream_t stream) {
     if (p.persistent) {
         const int n_tiles = (p.N + kTileN - 1) / kTileN;
         if (gather) {
             // grouped, 2- or 4-bit, short tiles: two persistent CTAs per SM
             if (!compact_mode(bits, max_rows_per_tile, true)) return cudaErrorNotSupported;
             return bits == 2 ? launch_persistent<2, true, true, GROUP>(p, max_rows_per_tile, 0,
-                                                                       n_tiles, p.grid_ctas, cm, xm,
+                                                                       n_tiles, p.grid_ctas, cm, xm, cm1,
                                                                        stream)
                              : launch_persistent<4, true, true, GROUP>(p, max_rows_per_tile, 0,
-                                                                       n_tiles, p.grid_ctas, cm, xm,
+                                                                       n_tiles, p.grid_ctas, cm, xm, cm1,
                                                                        stream);
         }
         if (bits == 2)
             return launch_persistent<2, false, false, GROUP>(p, max_rows_per_tile, p.m_tiles,
-                                                             n_tiles, p.grid_ctas, cm, xm, stream);
+                                                             n_tiles, p.grid_ctas, cm, xm, cm1, stream);
         if (bits == 3)
             return launch_persistent<3, false, false, GROUP>(p, max_rows_per_tile, p.m_tiles,
-                                                             n_tiles, p.grid_ctas, cm, xm, stream);
+                                                             n_tiles, p.grid_ctas, cm, xm, cm1, stream);
         if (bits == 6)
             return launch_persistent<6, false, false, GROUP>(p, max_rows_per_tile, p.m_tiles,
-                                                             n_tiles, p.grid_ctas, cm, xm, stream);
+                                                             n_tiles, p.grid_ctas, cm, xm, cm1, stream);
         return bits == 4 ? launch_persistent<4, false, false, GROUP>(
-                               p, max_rows_per_tile, p.m_tiles, n_tiles, p.grid_ctas, cm, xm, stream)
+                               p, max_rows_per_tile, p.m_tiles, n_tiles, p.grid_ctas, cm, xm, cm1, stream)
                          : launch_persistent<8, false, false, GROUP>(
-                               p, max_rows_per_tile, p.m_tiles, n_tiles, p.grid_ctas, cm, xm, stream);
+                               p, max_rows_per_tile, p.m_tiles, n_tiles, p.grid_ctas, cm, xm, cm1, stream);
     }
     if (bits == 2) {
         if (gather) return cudaErrorNotSupported;  // 2-bit grouped calls are persistent (above)
-        return launch_variant<2, false, GROUP>(p, grid_m, max_rows_per_tile, cm, xm, stream);
+        return launch_variant<2, false, GROUP>(p, grid_m, max_rows_per_tile, cm, xm, cm1, stream);
     }
     if (bits == 3)
-        return gather ? launch_variant<3, true, GROUP>(p, grid_m, max_rows_per_tile, cm, xm, stream)
-                      : launch_variant<3, false, GROUP>(p, grid_m, max_rows_per_tile, cm, xm, stream);
+        return gather ? launch_variant<3, true, GROUP>(p, grid_m, max_rows_per_tile, cm, xm, cm1, stream)
+                      : launch_variant<3, false, GROUP>(p, grid_m, max_rows_per_tile, cm, xm, cm1, stream);
     if (bits == 6)
-        return gather ? launch_variant<6, true, GROUP>(p, grid_m, max_rows_per_tile, cm, xm, stream)
-                      : launch_variant<6, false, GROUP>(p, grid_m, max_rows_per_tile, cm, xm, stream);
+        return gather ? launch_variant<6, true, GROUP>(p, grid_m, max_rows_per_tile, cm, xm, cm1, stream)
+                      : launch_variant<6, false, GROUP>(p, grid_m, max_rows_per_tile, cm, xm, cm1, stream);
     if (bits == 4) {
         if (gather) return cudaErrorNotSupported;  // 4-bit grouped calls are persistent (above)
-        return launch_variant<4, false, GROUP>(p, grid_m, max_rows_per_tile, cm, xm, stream);
+        return launch_variant<4, false, GROUP>(p, grid_m, max_rows_per_tile, cm, xm, cm1, stream);
     }
-    return gather ? launch_variant<8, true, GROUP>(p, grid_m, max_rows_per_tile, cm, xm, stream)
-                  : launch_variant<8, false, GROUP>(p, grid_m, max_rows_per_tile, cm, xm, stream);
+    return gather ? launch_variant<8, true, GROUP>(p, grid_m, max_rows_per_tile, cm, xm, cm1, stream)
+                  : launch_variant<8, false, GROUP>(p, grid_m, max_rows_per_tile, cm, xm, cm1, stream);
 }
 
 }  // namespace
@@ -1584,7 +1608,7 @@ cudaError_t launch_qmm_tc(const QmmParams& p, int bits, int grid_m, int max_rows
     if (!enc) return cudaErrorNotSupported;
     const bool gather = p.tiles != nullptr;
     // packed codes: words along K, rows n, experts
-    CUtensorMap cm, xm;
+    CUtensorMap cm, xm, cm1;
     const cuuint64_t words = (cuuint64_t)p.K * bits / 32;
     const cuuint32_t box_words = kCodeBoxRowBytes / 4;    // 128 bytes of each row
     const cuuint32_t estr[3] = {1, 1, 1};
@@ -1593,6 +1617,12 @@ cudaError_t launch_qmm_tc(const QmmParams& p, int bits, int grid_m, int max_rows
         const cuuint64_t strides[2] = {words * 4, words * 4 * (cuuint64_t)p.N};
         const cuuint32_t box[3] = {box_words, (cuuint32_t)kTileN, 1};
         if (enc(&cm, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint32_t*>(p.w), dims, strides,
+                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        // the gate/up pair's second weight set: same shape, its own map
+        if (p.sets > 1 &&
+            enc(&cm1, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint32_t*>(p.w1), dims, strides,
                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
@@ -1613,10 +1643,11 @@ cudaError_t launch_qmm_tc(const QmmParams& p, int bits, int grid_m, int max_rows
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
+    if (!(gather && p.sets > 1)) cm1 = cm;  // one weight set: the second map is never read
     switch (p.group) {
-        case 32: return launch_group<32>(p, bits, gather, grid_m, max_rows_per_tile, cm, xm, stream);
-        case 64: return launch_group<64>(p, bits, gather, grid_m, max_rows_per_tile, cm, xm, stream);
-        case 128: return launch_group<128>(p, bits, gather, grid_m, max_rows_per_tile, cm, xm, stream);
+        case 32: return launch_group<32>(p, bits, gather, grid_m, max_rows_per_tile, cm, xm, cm1, stream);
+        case 64: return launch_group<64>(p, bits, gather, grid_m, max_rows_per_tile, cm, xm, cm1, stream);
+        case 128: return launch_group<128>(p, bits, gather, grid_m, max_rows_per_tile, cm, xm, cm1, stream);
         default: return cudaErrorInvalidValue;
     }
 }

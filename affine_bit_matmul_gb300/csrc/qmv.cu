@@ -335,13 +335,22 @@ __global__ void __launch_bounds__(direct_max_warps(BITS) * 32) qmv_generic_kerne
 // all the (few) ids itself, so no separate pass is needed: an id outside
 // [0, E) or a source row outside [0, T) makes the row zero; ids that
 // decrease anywhere make every row zero; the first CTA reports the bits.
+// blockIdx.z selects the weight set of the gate/up pair (set 1: w1,
+// scales1, biases1 -> y1).
 template <int BITS>
 __global__ void __launch_bounds__(direct_max_warps(BITS) * 32) gather_qmv_kernel(
-    const __nv_bfloat16* __restrict__ x, const uint32_t* __restrict__ w,
-    const uint16_t* __restrict__ scales, const uint16_t* __restrict__ biases,
-    const int32_t* __restrict__ ids, const int32_t* __restrict__ row_src,
-    __nv_bfloat16* __restrict__ y, int T, int B, int E, int K, int N, int group,
+    const __nv_bfloat16* __restrict__ x, const uint32_t* __restrict__ w0,
+    const uint16_t* __restrict__ scales0, const uint16_t* __restrict__ biases0,
+    const uint32_t* __restrict__ w1, const uint16_t* __restrict__ scales1,
+    const uint16_t* __restrict__ biases1, const int32_t* __restrict__ ids,
+    const int32_t* __restrict__ row_src, __nv_bfloat16* __restrict__ y0,
+    __nv_bfloat16* __restrict__ y1, int T, int B, int E, int K, int N, int group,
     long long w_expert_stride, long long sb_expert_stride, int32_t* status) {
+    const bool second = blockIdx.z != 0;
+    const uint32_t* __restrict__ w = second ? w1 : w0;
+    const uint16_t* __restrict__ scales = second ? scales1 : scales0;
+    const uint16_t* __restrict__ biases = second ? biases1 : biases0;
+    __nv_bfloat16* __restrict__ y = second ? y1 : y0;
     __shared__ int flags;
     if (threadIdx.x == 0) flags = 0;
     __syncthreads();
@@ -358,7 +367,7 @@ __global__ void __launch_bounds__(direct_max_warps(BITS) * 32) gather_qmv_kernel
     if (f) atomicOr(&flags, f);
     __syncthreads();
     const int all = flags;
-    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && all && status)
+    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0 && all && status)
         atomicOr(status, all);
     const int r = blockIdx.y;
     const int row0 = blockIdx.x * kRows;
@@ -848,37 +857,42 @@ cudaError_t launch_stream(const __nv_bfloat16* x, const uint32_t* w, const uint1
 }  // namespace
 
 cudaError_t launch_gather_qmv(const void* x, const uint32_t* w, const void* scales,
-                              const void* biases, const int32_t* expert_ids,
-                              const int32_t* row_src, void* y, int T, int B, int E, int K, int N,
-                              int bits, int group, int32_t* status, cudaStream_t stream) {
+                              const void* biases, const uint32_t* w1, const void* scales1,
+                              const void* biases1, const int32_t* expert_ids,
+                              const int32_t* row_src, void* y, void* y1, int sets, int T, int B,
+                              int E, int K, int N, int bits, int group, int32_t* status,
+                              cudaStream_t stream) {
     const int seg_k = bits == 8 ? 512 : 1024;
     const int nseg_g = (K + seg_k - 1) / seg_k;
     const int max_warps = direct_max_warps(bits);
     const int passes = (nseg_g + max_warps - 1) / max_warps;
     const int warps = (nseg_g + passes - 1) / passes;
-    const dim3 grid((N + kRows - 1) / kRows, B);
+    const dim3 grid((N + kRows - 1) / kRows, B, sets);
     const dim3 block(32 * warps);
     const auto* xb = static_cast<const __nv_bfloat16*>(x);
     const auto* sb = static_cast<const uint16_t*>(scales);
     const auto* bb = static_cast<const uint16_t*>(biases);
+    const auto* sb1 = static_cast<const uint16_t*>(scales1);
+    const auto* bb1 = static_cast<const uint16_t*>(biases1);
     auto* yb = static_cast<__nv_bfloat16*>(y);
+    auto* yb1 = static_cast<__nv_bfloat16*>(y1);
     const long long wst = (long long)N * K * bits / 32;
     const long long sbst = (long long)N * (K / group);
+#define MXQ_GATHER_QMV(BB)                                                                        \
+    gather_qmv_kernel<BB><<<grid, block, 0, stream>>>(xb, w, sb, bb, w1, sb1, bb1, expert_ids,     \
+                                                      row_src, yb, yb1, T, B, E, K, N, group, wst, \
+                                                      sbst, status)
     if (bits == 2)
-        gather_qmv_kernel<2><<<grid, block, 0, stream>>>(xb, w, sb, bb, expert_ids, row_src, yb, T,
-                                                        B, E, K, N, group, wst, sbst, status);
+        MXQ_GATHER_QMV(2);
     else if (bits == 3)
-        gather_qmv_kernel<3><<<grid, block, 0, stream>>>(xb, w, sb, bb, expert_ids, row_src, yb, T,
-                                                        B, E, K, N, group, wst, sbst, status);
+        MXQ_GATHER_QMV(3);
     else if (bits == 6)
-        gather_qmv_kernel<6><<<grid, block, 0, stream>>>(xb, w, sb, bb, expert_ids, row_src, yb, T,
-                                                        B, E, K, N, group, wst, sbst, status);
+        MXQ_GATHER_QMV(6);
     else if (bits == 4)
-        gather_qmv_kernel<4><<<grid, block, 0, stream>>>(xb, w, sb, bb, expert_ids, row_src, yb, T,
-                                                        B, E, K, N, group, wst, sbst, status);
+        MXQ_GATHER_QMV(4);
     else
-        gather_qmv_kernel<8><<<grid, block, 0, stream>>>(xb, w, sb, bb, expert_ids, row_src, yb, T,
-                                                        B, E, K, N, group, wst, sbst, status);
+        MXQ_GATHER_QMV(8);
+#undef MXQ_GATHER_QMV
     return cudaGetLastError();
 }
 

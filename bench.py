@@ -781,13 +781,17 @@ def run_profile(args):
     elif name.startswith("qmm"):
         M, K, N, bits = {"qmm": (600, 5120, 17408, 4), "qmm600": (600, 5120, 5120, 4),
                          "qmm128": (128, 5120, 5120, 4), "qmm8": (8, 5120, 5120, 4),
-                         "qmm32": (32, 5120, 5120, 4)}[name]
+                         "qmm2": (2, 5120, 5120, 4), "qmm32": (32, 5120, 5120, 4)}[name]
         d = DenseInputs(synth.dense_weights(N, K, seed=0), M, K, N, bits, dev, copies=2)
         for i in range(launches):
             mxq.qmm(d.x, *d.copies[i % 2], bits, out=d.y)
     else:
-        K, N, ident = {"gather_up": (2816, 704, False), "gather_down": (704, 2816, True)}[name]
+        K, N, ident = {"gather_up": (2816, 704, False), "gather_down": (704, 2816, True),
+                       "gather_up_t4": (2816, 704, False),
+                       "gather_down_t4": (704, 2816, True)}[name]
         E, T, top_k, bits = 128, 573, 8, 4
+        if name.endswith("_t4"):
+            T = 4  # a decode step of 4 tokens: 32 routed rows
         ids, src = synth.routing(T, E, top_k, seed=2)
         B = ids.shape[0]
         rng = np.random.default_rng(0)
@@ -809,7 +813,8 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--profile", default=None,
                     help="plain launches of one workload for ncu: decode qmv4 qmv8 qmv4t qmv8t qmm "
-                         "qmm600 qmm128 qmm8 qmm32 gather_up gather_down")
+                         "qmm600 qmm128 qmm8 qmm2 qmm32 gather_up gather_down gather_up_t4 "
+                         "gather_down_t4")
     ap.add_argument("--profile-launches", type=int, default=4)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20000)

@@ -110,20 +110,15 @@ mxq_status mxq_qmv_kn(const void* x, const uint32_t* w, const void* scales, cons
                       void* stream);
 
 /* Prefill GEMM, y[M, N] = x[M, K] . w^[N, K]^T (mlxcel issue #1536, Baseline
- * profile table and Diagnosis item 4: the qmm_naive kernel).  Kernels, by M
- * (each deterministic for a given shape; same result rule):
- *  - M = 1: the streaming GEMV of mxq_qmv;
- *  - 4-bit codes and M <= 8: a streaming kernel that reads each code once
- *    for all M rows and contracts on the tensor cores (mma.sync, fp32
- *    accumulation; the affine terms applied per group in fp32), K split
- *    over a thread-block cluster when N gives too few 16-row slabs for the
- *    SMs, partials added through distributed shared memory in rank order;
- *  - otherwise the tcgen05 tensor cores: codes are dequantised to bf16 into
- *    tensor memory (the MMA's A operand) and the products accumulate in fp32
- *    in tensor memory.  When M and N give fewer 128 x 256 tiles than the GPU
- *    has SMs, K is split over up to 8 CTAs of a cluster and the fp32
- *    partials are added through distributed shared memory in a fixed order;
- *    with enough tiles, one persistent CTA per SM walks them.
+ * profile table and Diagnosis item 4: the qmm_naive kernel).  M = 1 runs the
+ * streaming GEMV of mxq_qmv (the same operation).  Otherwise the tcgen05
+ * tensor cores: codes are dequantised to bf16 into tensor memory (the MMA's
+ * A operand) and the products accumulate in fp32 in tensor memory.  When M
+ * and N give fewer 128 x 256 tiles than the GPU has SMs, K is split over up
+ * to 8 CTAs of a thread-block cluster and the fp32 partials are added
+ * through distributed shared memory in a fixed order; with enough tiles, one
+ * persistent CTA per SM walks them.  Either way the result is deterministic
+ * for a given shape.
  * Requirements as for mxq_qmv plus M > 0.  `dev_status` (device int32, may
  * be NULL) receives 0 or MXQ_DEV_TIMEOUT.                                   */
 mxq_status mxq_qmm(const void* x, const uint32_t* w, const void* scales, const void* biases,
@@ -140,30 +135,22 @@ mxq_status mxq_qmm(const void* x, const uint32_t* w, const void* scales, const v
  *               (then T must equal B)
  *   y:          bf16 [B, N], in sorted row order
  *   workspace:  device scratch, 256-byte aligned, overwritten by the call:
- *               mxq_gather_workspace_bytes(B, E, K, N) bytes always
- *               suffice (tile table, the activation rows in sorted order,
- *               their per-group sums).  Calls with more than 8 * E rows
- *               and no row_src need only mxq_gather_workspace_bytes(B, E,
- *               0, N) (the tile table); a smaller workspace than a call
- *               needs returns MXQ_ERR_WORKSPACE.
+ *               mxq_gather_workspace_bytes(B, E, K, N) bytes when row_src
+ *               is given (it also holds the activation rows in sorted
+ *               order), otherwise the smaller mxq_gather_workspace_bytes(B,
+ *               E, 0, N) suffices.
  *   dev_status: device int32 or NULL; receives the MXQ_DEV_* bits.
  * Rows whose expert id lies outside [0, E), or whose row_src lies outside
  * [0, T), are skipped and their y rows set to zero.  If the ids are not
  * non-decreasing, nothing is computed, all of y is set to zero and
  * MXQ_DEV_UNSORTED_IDS is reported.  No invalid input makes the kernels
  * read or write out of bounds.
- * Kernels, by size (same result rule, different summation orders):
- *  - 4-bit codes and at most 8 rows per expert on average (B <= 8 * E: a
- *    decode step of up to a few hundred tokens): a tile table of items of
- *    at most 8 rows of one expert is built on the GPU, the routed rows are
- *    prepared in the workspace, and one launch streams every used expert's
- *    codes once per item through the tensor cores (mma.sync, fp32
- *    accumulation; the affine terms are applied per group in fp32);
- *  - other widths with at most 32 rows: one GEMV per row against its
- *    expert's matrix;
- *  - larger calls: a tile table of at most 64 rows per tile and the tcgen05
- *    GEMM (at 2 and 4 bits two persistent CTAs per SM take tiles from a
- *    counter; at 3, 6 and 8 bits one CTA computes each tile).
+ * Calls with at most 32 rows (a decode step) run one GEMV per row against
+ * its expert's matrix (the same result rule, another summation order) and
+ * use no workspace memory, though the size check still applies.
+ * Larger calls build a tile table on the GPU and run the tensor-core GEMM:
+ * at 2 and 4 bits two persistent CTAs per SM take tiles from a counter; at
+ * 3, 6 and 8 bits one CTA computes each tile.
  * Requirements: B, E, T, N > 0; K > 0, K % 64 == 0, K % group_size == 0;
  * bits in {2, 3, 4, 6, 8} (K % 128 == 0 at 3 bits); group_size in
  * {32, 64, 128}; x, w, y 16-byte aligned; the rest aligned to type.          */
@@ -173,10 +160,9 @@ mxq_status mxq_gather_qmm(const void* x, const uint32_t* w, const void* scales,
                           int bits, int group_size, void* workspace, size_t workspace_bytes,
                           int32_t* dev_status, void* stream);
 
-/* Workspace bytes that always suffice for mxq_gather_qmm and
- * mxq_gather_qmm_gateup over B rows, E experts and K-wide activation rows;
- * K = 0 gives the tile table alone (enough for calls with more than 8 * E
- * rows and no row_src). */
+/* Workspace bytes mxq_gather_qmm (and mxq_gather_qmm_gateup) needs for B
+ * rows over E experts with K-wide activation rows routed through row_src
+ * (K = 0: no row_src). */
 size_t mxq_gather_workspace_bytes(int B, int E, int K, int N);
 
 /* The gate and up projections of a mixture-of-experts layer in one call
@@ -186,13 +172,15 @@ size_t mxq_gather_workspace_bytes(int B, int E, int K, int N);
  *   y_gate[r, n] = sum_k x[src(r), k] * w^gate_{e(r)}[n, k]
  *   y_up[r, n]   = sum_k x[src(r), k] * w^up_{e(r)}[n, k]
  * with every argument as in mxq_gather_qmm (w_gate/w_up, scales_*,
- * biases_* each [E, N, ...]; y_gate, y_up [B, N]).  No activation function
- * is applied: the pages name none; a caller combines the two outputs.
- * Decode-sized calls (4-bit codes, B <= 8 * E) are one launch of the
- * skinny kernel that loads each item's activation rows once for both
- * projections; larger calls run the grouped GEMM once per projection.  The
- * status word reports the id and row_src checks (and timeouts of the first
- * projection at the larger sizes).                                         */
+ * biases_* each [E, N, ...] with the same shape; y_gate, y_up [B, N]; the
+ * same workspace size).  No activation function is applied: the pages name
+ * none; a caller combines the two outputs.  One launch computes both
+ * projections: with at most 32 rows the per-row GEMVs of both sets (grid z
+ * = the set); otherwise the routed rows are put in sorted order once and
+ * the grouped GEMM takes the tiles of both sets (persistent CTAs at 2 and 4
+ * bits, one CTA per tile and set otherwise).  Each output is bit for bit the
+ * output mxq_gather_qmm gives for its set.  The status word reports the id
+ * and row_src checks and timeouts of either set.                          */
 mxq_status mxq_gather_qmm_gateup(const void* x, const uint32_t* w_gate, const void* scales_gate,
                                  const void* biases_gate, const uint32_t* w_up,
                                  const void* scales_up, const void* biases_up,
@@ -214,11 +202,11 @@ mxq_status mxq_gather_qmm_gateup(const void* x, const uint32_t* w_gate, const vo
  * MXQ_NOALLOC_SCRATCH_BYTES of device memory reserved on each device when
  * the library's device code is loaded there.
  *
- * Limit: a request whose scratch (what mxq_gather_qmm would use of its
- * workspace for the same arguments) exceeds MXQ_NOALLOC_SCRATCH_BYTES
- * returns MXQ_ERR_SCRATCH_LIMIT before anything touches the device.  32 MiB
- * holds, for example, the tile table and the sorted rows of 4584 routed
- * rows of K = 2816.
+ * Limit: a request whose scratch, mxq_gather_workspace_bytes(B, E, K, N)
+ * with row_src (or mxq_gather_workspace_bytes(B, E, 0, N) without), exceeds
+ * MXQ_NOALLOC_SCRATCH_BYTES returns MXQ_ERR_SCRATCH_LIMIT before anything
+ * touches the device.  32 MiB holds, for example, the tile table and the
+ * sorted rows of 4584 routed rows of K = 2816.
  *
  * Set-up: the first call on each device looks up the scratch's device
  * address with that device current (this may load the library's device

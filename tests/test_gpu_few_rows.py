@@ -1,13 +1,15 @@
-"""GPU parity of the few-rows tensor-core path (the "skinny" kernel) against
-the f64 checker through the C ABI, element by element:
+"""GPU parity of the few-rows shapes against the f64 checker through the C
+ABI, element by element:
 
-* mxq_qmm with 2 <= M <= 8 and 4-bit codes (every group size; K splits over
-  clusters of 1 to 8 CTAs; N not a multiple of the 16-row slab);
-* mxq_gather_qmm at decode sizes (B <= 8 * E): one to 128 tokens routed to 8
-  of 128 experts, both expert shapes of the workload, routed and identity
-  sources, invalid ids and sources;
-* mxq_gather_qmm_gateup: both outputs against two separate checker calls, at
-  decode size (one launch) and at prefill size (two grouped GEMMs)."""
+* mxq_qmm with 1 <= M <= 8 (every group size; K split over clusters; N not
+  a multiple of the tile); M = 1 is bit for bit the GEMV;
+* mxq_gather_qmm at decode sizes: one to 128 tokens routed to 8 of 128
+  experts, both expert shapes of the workload, routed and identity sources,
+  a hot expert, invalid ids and sources, the constant-per-expert case;
+* mxq_gather_qmm_gateup (the gate and up projections of an MoE layer in one
+  launch): both outputs against two separate checker calls, at decode size
+  (per-row GEMVs) and at prefill size (the grouped GEMM), each bit for bit
+  equal to the single-set call."""
 
 import numpy as np
 import pytest
@@ -101,7 +103,7 @@ def test_gather_decode_group_sizes(group):
 
 
 def test_gather_decode_hot_expert():
-    # one expert takes 20 of 24 rows (three items of at most 8 rows)
+    # one expert takes 20 of 24 rows
     c = MoECase(24, 4, 1, 512, 130, 4, seed=63, identity_src=True)
     ids = np.array([0, 1] + [2] * 20 + [3, 3], np.int32)
     c.ids = ids
@@ -133,7 +135,7 @@ def test_gather_decode_invalid_rows():
     good[[0, 5, c.B - 1]] = False
     yr, bnd = oracle.gather_qmm(c.x, c.w, c.s, c.b, np.clip(ids, 0, E - 1),
                                 np.where(good, src, 0), c.T, c.B, c.E, c.K, c.N, 4)
-    assert_close(y[good], yr[good], bnd[good], "skinny gather with invalid rows")
+    assert_close(y[good], yr[good], bnd[good], "decode gather with invalid rows")
     # unsorted ids: all zero
     out.fill_(7.0)
     bad = np.array([1, 0] + [2] * (c.B - 2), np.int32)
@@ -173,22 +175,49 @@ def _second_set(c, seed):
     return np.stack(ws), np.stack(ss), np.stack(bs)
 
 
+@pytest.mark.parametrize("bits", [4, 8, 2])
 @pytest.mark.parametrize("T,K,N,ident", [(4, 2816, 704, False), (32, 704, 2816, True),
                                          (300, 256, 192, False)])
-def test_gateup_matches_two_checker_calls(T, K, N, ident):
+def test_gateup_matches_two_checker_calls(T, K, N, ident, bits):
     import torch
 
-    c = MoECase(T, 64 if T < 300 else 16, 4, K, N, 4, seed=81 + T, identity_src=ident,
+    c = MoECase(T, 64 if T < 300 else 16, 4, K, N, bits, seed=81 + T, identity_src=ident,
                 routing_seed=82 + T)
     wu, su, bu = _second_set(c, 83 + T)
     status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
     yg, yu = _mxq().gather_qmm_gateup(c.x_d, c.w_d, c.s_d, c.b_d, codes_dev(wu), bf16_dev(su),
-                                      bf16_dev(bu), c.ids_d, c.src_d, 4, dev_status=status)
-    rg, bg = oracle.gather_qmm(c.x, c.w, c.s, c.b, c.ids, c.src, c.T, c.B, c.E, c.K, c.N, 4)
-    ru, bu_ = oracle.gather_qmm(c.x, wu, su, bu, c.ids, c.src, c.T, c.B, c.E, c.K, c.N, 4)
-    assert_close(to_f64(yg), rg, bg, "gate T=%d" % T)
-    assert_close(to_f64(yu), ru, bu_, "up T=%d" % T)
+                                      bf16_dev(bu), c.ids_d, c.src_d, bits, dev_status=status)
+    rg, bg = oracle.gather_qmm(c.x, c.w, c.s, c.b, c.ids, c.src, c.T, c.B, c.E, c.K, c.N, bits)
+    ru, bu_ = oracle.gather_qmm(c.x, wu, su, bu, c.ids, c.src, c.T, c.B, c.E, c.K, c.N, bits)
+    assert_close(to_f64(yg), rg, bg, "gate T=%d bits=%d" % (T, bits))
+    assert_close(to_f64(yu), ru, bu_, "up T=%d bits=%d" % (T, bits))
     assert int(status.item()) == 0
     # each output equals the single-set call bit for bit
-    y1 = _mxq().gather_qmm(c.x_d, c.w_d, c.s_d, c.b_d, c.ids_d, c.src_d, 4)
+    y1 = _mxq().gather_qmm(c.x_d, c.w_d, c.s_d, c.b_d, c.ids_d, c.src_d, bits)
+    y2 = _mxq().gather_qmm(c.x_d, codes_dev(wu), bf16_dev(su), bf16_dev(bu), c.ids_d, c.src_d, bits)
     assert torch.equal(yg.view(torch.int16), y1.view(torch.int16))
+    assert torch.equal(yu.view(torch.int16), y2.view(torch.int16))
+
+
+def test_gateup_invalid_ids_zero_both_outputs():
+    import torch
+
+    T, E, K, N = 40, 4, 128, 128
+    c = MoECase(T, E, 1, K, N, 4, seed=91, identity_src=True)
+    ids = np.array([-1] * 3 + [0] * 10 + [1] * 10 + [3] * 12 + [4] * 5, np.int32)
+    c.ids = ids
+    c.ids_d = i32_dev(ids)
+    wu, su, bu = _second_set(c, 92)
+    og = torch.full((c.B, N), 7.0, dtype=torch.bfloat16, device="cuda")
+    ou = torch.full((c.B, N), 7.0, dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    _mxq().gather_qmm_gateup(c.x_d, c.w_d, c.s_d, c.b_d, codes_dev(wu), bf16_dev(su),
+                             bf16_dev(bu), c.ids_d, None, 4, out_gate=og, out_up=ou,
+                             dev_status=status)
+    assert int(status.item()) & _mxq().DEV_BAD_EXPERT_ID
+    for y in (to_f64(og), to_f64(ou)):
+        assert np.all(y[:3] == 0) and np.all(y[-5:] == 0)
+    rg, bg = oracle.gather_qmm(c.x, c.w, c.s, c.b, ids, None, c.T, c.B, c.E, c.K, c.N, 4)
+    ru, bu_ = oracle.gather_qmm(c.x, wu, su, bu, ids, None, c.T, c.B, c.E, c.K, c.N, 4)
+    assert_close(to_f64(og), rg, bg, "gate with invalid ids")
+    assert_close(to_f64(ou), ru, bu_, "up with invalid ids")
