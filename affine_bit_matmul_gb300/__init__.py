@@ -36,6 +36,7 @@ __all__ = [
     "gather_workspace_bytes",
     "gather_qmm_noalloc",
     "quantize",
+    "set_wait_budget",
     "NOALLOC_SCRATCH_BYTES",
     "MxqError",
     "DEV_BAD_EXPERT_ID",
@@ -76,6 +77,7 @@ EXPORTED_SYMBOLS = (
     "mxq_quantize",
     "mxq_status_string",
     "mxq_version",
+    "mxq_debug_set_wait_budget",
 )
 
 
@@ -119,6 +121,8 @@ def lib():
         L.mxq_status_string.argtypes = [I]
         L.mxq_status_string.restype = ctypes.c_char_p
         L.mxq_version.restype = I
+        L.mxq_debug_set_wait_budget.argtypes = [ctypes.c_longlong]
+        L.mxq_debug_set_wait_budget.restype = ctypes.c_longlong
         _lib_handle = L
     return _lib_handle
 
@@ -438,3 +442,13 @@ def gather_qmm_gateup(x, w_gate, s_gate, b_gate, w_up, s_up, b_up, expert_ids, r
             group_size, _ptr(workspace), workspace.numel(), _ptr(dev_status), st),
             "mxq_gather_qmm_gateup")
     return outs[0], outs[1]
+
+
+def set_wait_budget(cycles: int) -> int:
+    """Testing aid: the budget, in SM clock cycles, after which an on-chip
+    pipeline wait of a kernel launched from now on gives up (the call's
+    ``dev_status`` then gets ``DEV_TIMEOUT`` and its output is incomplete).
+    ``cycles <= 0`` restores the default of 2e9 cycles.  Returns the budget in
+    force.  Waits for a CTA's own copies and MMAs keep the default, so the
+    next call after a timed-out one runs normally."""
+    return int(lib().mxq_debug_set_wait_budget(int(cycles)))

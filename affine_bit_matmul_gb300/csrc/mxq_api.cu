@@ -1,9 +1,12 @@
 // C ABI of the library: argument checks, tile and split planning, launches.
+#include <atomic>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <cuda_runtime.h>
 
 #include "../../include/mxq.h"
+#include "mxq_device.cuh"
 #include "mxq_internal.h"
 
 namespace {
@@ -102,9 +105,29 @@ size_t gather_table_bytes(int B, int E) {
            align_up(((size_t)E + 1) * sizeof(int), 256);
 }
 
+// Pipeline-wait budget for kernels launched from now on; 0 until the first
+// launch reads MXQ_DEBUG_WAIT_BUDGET.
+std::atomic<long long> g_wait_budget{0};
+
+long long clamp_budget(long long cycles) {
+    return (cycles <= 0 || cycles > mxq::kWaitBudgetCycles) ? mxq::kWaitBudgetCycles : cycles;
+}
+
 }  // namespace
 
 mxq_status mxq::check_current_device(int* sms) { return check_device(sms); }
+
+long long mxq::wait_budget_cycles() {
+    long long b = g_wait_budget.load(std::memory_order_relaxed);
+    if (b == 0) {
+        const char* env = std::getenv("MXQ_DEBUG_WAIT_BUDGET");
+        long long expected = 0;
+        g_wait_budget.compare_exchange_strong(expected,
+                                              clamp_budget(env ? std::strtoll(env, nullptr, 10) : 0));
+        b = g_wait_budget.load(std::memory_order_relaxed);
+    }
+    return b;
+}
 
 size_t mxq::gather_scratch_bytes(int B, int E, int K, int N, int bits, int group_size,
                                  bool has_row_src) {
@@ -132,6 +155,11 @@ const char* mxq_status_string(mxq_status s) {
 }
 
 int mxq_version(void) { return 100; }
+
+long long mxq_debug_set_wait_budget(long long cycles) {
+    g_wait_budget.store(clamp_budget(cycles), std::memory_order_relaxed);
+    return g_wait_budget.load(std::memory_order_relaxed);
+}
 
 mxq_status mxq_qmv(const void* x, const uint32_t* w, const void* scales, const void* biases,
                    void* y, int K, int N, int bits, int group_size, int32_t* dev_status,

@@ -16,8 +16,12 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 
-// A wait gives up after this many SM clock cycles (about one second at
-// 2 GHz); the kernel then records MXQ_DEV_TIMEOUT and winds down.
+// A pipeline wait gives up after a budget of SM clock cycles; the kernel
+// then records MXQ_DEV_TIMEOUT and winds down.  The budget is a kernel
+// argument: this default (about one second at 2 GHz), or a shorter one set
+// with mxq_debug_set_wait_budget to exercise the give-up path.  A CTA's waits
+// for the copies and MMAs it issued itself (before it exits or frees tensor
+// memory) always take the default, so no asynchronous write outlives it.
 constexpr long long kWaitBudgetCycles = 2000000000LL;
 
 // ----------------------------------------------------------------- mbarrier
@@ -50,15 +54,47 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of the same phase.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// One poll under a budget: try_wait may hold the thread for a while in
+// hardware, so a budget shorter than the default polls with test_wait and
+// is kept to the cycle.
+__device__ __forceinline__ bool mbar_poll(uint64_t* bar, uint32_t parity, long long budget) {
+    return budget < kWaitBudgetCycles ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity);
+}
+
 // Waits for the phase with the given parity to complete.  Returns false if
 // the budget ran out (the caller then stops its pipeline role).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
-    long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
-        if (clock64() - t0 > kWaitBudgetCycles) return false;
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          long long budget = kWaitBudgetCycles) {
+    if (mbar_poll(bar, parity, budget)) return true;
+    const long long t0 = clock64();
+    while (!mbar_poll(bar, parity, budget)) {
+        if (clock64() - t0 > budget) return false;
     }
     return true;
+}
+
+// Waits (default budget) until the copies issued into the last n slots of a
+// ring have landed: copy g of the ring (g < issued) completes phase g / slots
+// of barrier full[g % slots].  A producer calls this before it leaves, also
+// after giving up, so that no copy writes shared memory after the CTA exits.
+__device__ __forceinline__ bool drain_ring(uint64_t* full, int slots, long long issued, int n) {
+    bool all = true;
+    for (long long g = issued - 1; g >= 0 && g >= issued - n; --g)
+        all = mbar_wait(&full[g % slots], (uint32_t)((g / slots) & 1)) && all;
+    return all;
 }
 
 // ----------------------------------------------------------------- cp.async

@@ -16,6 +16,12 @@ namespace mxq {
 // cannot say.  Cached per device.
 mxq_status check_current_device(int* sms);
 
+// The pipeline-wait budget, in SM clock cycles, for kernels launched now:
+// the default (about one second) unless mxq_debug_set_wait_budget, or the
+// MXQ_DEBUG_WAIT_BUDGET environment variable read at the first call, set a
+// shorter one.
+long long wait_budget_cycles();
+
 // Scratch bytes a grouped call with these arguments needs: the tile table,
 // plus the routed rows in sorted order when row_src is given.
 size_t gather_scratch_bytes(int B, int E, int K, int N, int bits, int group_size,
@@ -65,6 +71,7 @@ struct QmmParams {
     const uint16_t* scales1;
     const uint16_t* biases1;
     void* y1;
+    long long wait_budget;   // pipeline-wait budget in SM cycles (set by launch_qmm_tc)
 };
 
 // cuTensorMapEncodeTiled, looked up once through the runtime (null if the

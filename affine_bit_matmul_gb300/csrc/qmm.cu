@@ -365,11 +365,13 @@ __device__ __forceinline__ bool mbar_try_wait3(uint64_t* a, uint32_t pa, uint64_
 }
 
 __device__ __forceinline__ bool mbar_wait3(uint64_t* a, uint32_t pa, uint64_t* b, uint32_t pb,
-                                           uint64_t* c, uint32_t pc) {
+                                           uint64_t* c, uint32_t pc, long long budget) {
+    if (budget < kWaitBudgetCycles)  // a short budget: exact, non-blocking polls
+        return mbar_wait(a, pa, budget) && mbar_wait(b, pb, budget) && mbar_wait(c, pc, budget);
     if (mbar_try_wait3(a, pa, b, pb, c, pc)) return true;
     const long long t0 = clock64();
     while (!mbar_try_wait3(a, pa, b, pb, c, pc)) {
-        if (clock64() - t0 > kWaitBudgetCycles) return false;
+        if (clock64() - t0 > budget) return false;
     }
     return true;
 }
@@ -391,14 +393,14 @@ struct Ring {
 // Whole-warp waits: every lane polls with its own bounded budget, then the
 // warp agrees on the outcome, so the warp stays converged for elect.sync even
 // when a wait gives up.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
-    const bool ok = mbar_wait(bar, parity);
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, long long budget) {
+    const bool ok = mbar_wait(bar, parity, budget);
     return __all_sync(0xffffffffu, ok);
 }
 
 __device__ __forceinline__ bool warp_wait3(uint64_t* a, uint32_t pa, uint64_t* b, uint32_t pb,
-                                           uint64_t* c, uint32_t pc) {
-    const bool ok = mbar_wait3(a, pa, b, pb, c, pc);
+                                           uint64_t* c, uint32_t pc, long long budget) {
+    const bool ok = mbar_wait3(a, pa, b, pb, c, pc, budget);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -507,8 +509,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int words = p.K * BITS / 32;
         const int nslots = (nst + kStagesPerSlot - 1) / kStagesPerSlot;
         Ring ring(SC);
-        for (int i = 0; i < nslots; ++i, ring.next()) {
-            if (i >= SC && !warp_wait(&cempty[ring.slot], ring.parity ^ 1)) { ok = false; break; }
+        int i = 0;
+        for (; i < nslots; ++i, ring.next()) {
+            if (i >= SC && !warp_wait(&cempty[ring.slot], ring.parity ^ 1, p.wait_budget)) {
+                ok = false;
+                break;
+            }
             if (elect_one()) {
                 const int c0 = kb_begin * (kHalfK * BITS / 32) + i * kWordsPerSlot;
                 // a box that starts past the end of the row is not loaded
@@ -527,6 +533,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
         }
+        // the slots issued last may still be loading if a consumer gave up
+        if (lane == 0 && !drain_ring(cfull, SC, i, SC)) ok = false;
+        __syncwarp();
     } else if (warp == kXWarp0) {
         // ---------------------------------------------------------------- activation TMA
         // per 64-wide block, boxes of [x_box_rows x 64] bf16 (128-byte
@@ -535,8 +544,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int boxes = (n_mma + p.x_box_rows - 1) / p.x_box_rows;
         const uint32_t x_bytes_in = (uint32_t)(boxes * p.x_box_rows * 128);
         Ring ring(SX);
-        for (int q = 0; q < nkb; ++q, ring.next()) {
-            if (q >= SX && !warp_wait(&xempty[ring.slot], ring.parity ^ 1)) { ok = false; break; }
+        int q = 0;
+        for (; q < nkb; ++q, ring.next()) {
+            if (q >= SX && !warp_wait(&xempty[ring.slot], ring.parity ^ 1, p.wait_budget)) {
+                ok = false;
+                break;
+            }
             if (elect_one()) {
                 mbar_expect_tx(&xfull[ring.slot], x_bytes_in);
                 for (int b = 0; b < boxes; ++b)
@@ -546,6 +559,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
         }
+        if (lane == 0 && !drain_ring(xfull, SX, q, SX)) ok = false;
+        __syncwarp();
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issue
         // the whole warp waits (three barriers per stage in one round trip);
@@ -560,7 +575,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int x1 = two ? xr.slot : x0;
             const uint32_t p1 = two ? xr.parity : p0;
             if (two) xr.next();
-            if (!warp_wait3(&afull[ar.slot], ar.parity, &xfull[x0], p0, &xfull[x1], p1)) {
+            if (!warp_wait3(&afull[ar.slot], ar.parity, &xfull[x0], p0, &xfull[x1], p1,
+                            p.wait_budget)) {
                 ok = false;
                 break;
             }
@@ -605,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (grp) ar.next();
         auto stage = [&](int s, const uint32_t (&sb)[2 * kP]) -> bool {
             const int cs = cr.slot;
-            if (!warp_wait(&cfull[cs], cr.parity)) return false;
+            if (!warp_wait(&cfull[cs], cr.parity, p.wait_budget)) return false;
             // this stage's kRowBytes of row r: box (off / 128), chunks from
             // (off % 128) / 16 on, each at its swizzled place in the line
             const int off = csub * kRowBytes;
@@ -630,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     cw[j] = ld_shared_v4(c_line + (uint32_t)(((chunk0 + j) ^ (r & 7)) << 4));
             }
             const int as = ar.slot;
-            if (s >= SA && !warp_wait(&aempty[as], ar.parity ^ 1)) return false;
+            if (s >= SA && !warp_wait(&aempty[as], ar.parity ^ 1, p.wait_budget)) return false;
             tc_fence_after();
             const uint32_t a_col = t_lane + (uint32_t)(a0 + as * kAStageCols);
 #pragma unroll
@@ -729,7 +745,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 
         // ---------------------------------------------------------------- epilogue
-        if (ok && !mbar_wait(accf, 0)) ok = false;
+        if (ok && !mbar_wait(accf, 0, p.wait_budget)) ok = false;
         tc_fence_after();
         const int quarter = warp & 3;     // tensor-memory lanes 32*quarter ...
         const int colhalf = warp >> 2;    // 16-column chunks of this parity
@@ -838,8 +854,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (warp == kMmaWarp) {
         tc_fence_after();
-        // make sure no MMA is still writing tensor memory (bounded wait)
-        if (lane == 0 && !ok) (void)mbar_wait(accf, 0);
+        // no MMA may still be writing tensor memory when it is freed: accf
+        // fires once every MMA issued has finished (the epilogue may have
+        // given up on it under a short budget; this wait takes the default)
+        if (lane == 0 && !mbar_wait(accf, 0)) flag_status(p.status, MXQ_DEV_TIMEOUT);
         __syncwarp();
         tmem_dealloc(tmem, (uint32_t)kCols);
     }
@@ -908,40 +926,47 @@ __device__ __forceinline__ PTile ptile(const QmmParams& p, int t, int m_tiles, i
 // the warps doing the work.
 constexpr uint32_t kSuspendNs = 20000;
 
-__device__ __forceinline__ bool mbar_try_wait_s(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_try_wait_s(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
         : "memory");
     return ok != 0;
 }
 
-// Bounded wait that also gives up as soon as another role has given up.
-__device__ __forceinline__ bool wait_ab(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-    if (mbar_try_wait(bar, parity)) return true;
+// Bounded wait that also gives up as soon as another role has given up.  The
+// first poll does not suspend, and the abort flag and the budget are checked
+// before every suspending one, so a budget shorter than one poll gives up at
+// the first wait that is not already satisfied.
+__device__ __forceinline__ bool wait_ab(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                        long long budget) {
+    if (mbar_test_wait(bar, parity)) return true;
     const long long t0 = clock64();
-    while (!mbar_try_wait_s(bar, parity)) {
+    do {
         if (*abort_flag) return false;
-        if (clock64() - t0 > kWaitBudgetCycles) {
+        if (clock64() - t0 > budget) {
             *abort_flag = 1;
             return false;
         }
-    }
+    } while (!mbar_try_wait_s(bar, parity, kSuspendNs));
     return true;
 }
 
-__device__ __forceinline__ bool warp_wait_ab(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-    const bool ok = wait_ab(bar, parity, abort_flag);
+__device__ __forceinline__ bool warp_wait_ab(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                             long long budget) {
+    const bool ok = wait_ab(bar, parity, abort_flag, budget);
     return __all_sync(0xffffffffu, ok);
 }
 
 __device__ __forceinline__ bool warp_wait3_ab(uint64_t* a, uint32_t pa, uint64_t* b, uint32_t pb,
-                                              uint64_t* c, uint32_t pc, volatile int* abort_flag) {
-    const bool ok = wait_ab(a, pa, abort_flag) && wait_ab(b, pb, abort_flag) && wait_ab(c, pc, abort_flag);
+                                              uint64_t* c, uint32_t pc, volatile int* abort_flag,
+                                              long long budget) {
+    const bool ok = wait_ab(a, pa, abort_flag, budget) && wait_ab(b, pb, abort_flag, budget) &&
+                    wait_ab(c, pc, abort_flag, budget);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -954,18 +979,6 @@ __device__ __forceinline__ void mbar_arrive_n(uint64_t* bar, uint32_t count) {
         "mbarrier.arrive.release.cta.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
         "r"(count)
         : "memory");
-}
-
-// After giving up: wait a short, bounded while for the copies a producer
-// issued into the last `n` slots of its ring, so none lands after exit.
-__device__ __forceinline__ void drain_copies(uint64_t* full, int slots, long long issued, int n) {
-    for (long long g = issued - 1; g >= 0 && g >= issued - n; --g) {
-        const int slot = (int)(g % slots);
-        const uint32_t parity = (uint32_t)((g / slots) & 1);
-        const long long t0 = clock64();
-        while (!mbar_try_wait(&full[slot], parity))
-            if (clock64() - t0 > kWaitBudgetCycles / 16) break;
-    }
 }
 
 template <int BITS, bool GATHER, bool COMPACT, int GROUP>
@@ -1067,7 +1080,8 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
     // id >= total tells every role to stop.
     auto tq_push = [&](int i, int t) -> bool {
         const int slot = i % kTQ;
-        if (i >= kTQ && !warp_wait_ab(&tqempty[slot], (uint32_t)(((i / kTQ) - 1) & 1), abort_flag))
+        if (i >= kTQ && !warp_wait_ab(&tqempty[slot], (uint32_t)(((i / kTQ) - 1) & 1), abort_flag,
+                                      p.wait_budget))
             return false;
         if (lane == 0) {
             tq[slot] = t;
@@ -1078,7 +1092,8 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
     };
     auto tq_pop = [&](int i, int* t) -> bool {
         const int slot = i % kTQ;
-        if (!warp_wait_ab(&tqfull[slot], (uint32_t)((i / kTQ) & 1), abort_flag)) return false;
+        if (!warp_wait_ab(&tqfull[slot], (uint32_t)((i / kTQ) & 1), abort_flag, p.wait_budget))
+            return false;
         *t = tq[slot];
         __syncwarp();
         if (lane == 0) mbar_arrive(&tqempty[slot]);
@@ -1092,7 +1107,7 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
         constexpr int kBoxes = slot_row_bytes(BITS) / kCodeBoxRowBytes;
         const int words = p.K * BITS / 32;
         Ring ring(SC);
-        long long issued = 0;
+        int issued = 0;
         for (int i = 0; ok; ++i) {
             int t = blockIdx.x + i * gridDim.x;
             if (i > 0 && p.tile_counter) {
@@ -1108,7 +1123,8 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
             if (t >= total) break;
             const PTile ti = ptile<GATHER>(p, t, m_tiles, n_tiles, per_set);
             for (int j = 0; j < nslots; ++j, ring.next(), ++issued) {
-                if (issued >= SC && !warp_wait_ab(&cempty[ring.slot], ring.parity ^ 1, abort_flag)) {
+                if (issued >= SC && !warp_wait_ab(&cempty[ring.slot], ring.parity ^ 1, abort_flag,
+                                                  p.wait_budget)) {
                     ok = false;
                     break;
                 }
@@ -1129,11 +1145,13 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
                 __syncwarp();
             }
         }
-        if (!ok && lane == 0) drain_copies(cfull, SC, issued, SC);
+        // the slots issued last may still be loading if a consumer gave up
+        if (lane == 0 && !drain_ring(cfull, SC, issued, SC)) ok = false;
+        __syncwarp();
     } else if (warp == kXWarp0) {
         // ---------------------------------------------------------------- activation TMA
         Ring ring(SX);
-        long long issued = 0;
+        int issued = 0;
         for (int i = 0; ok; ++i) {
             int t;
             if (!tq_pop(i, &t)) {
@@ -1145,7 +1163,8 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
             const int boxes = (ti.n_mma + p.x_box_rows - 1) / p.x_box_rows;
             const uint32_t x_bytes_in = (uint32_t)(boxes * p.x_box_rows * 128);
             for (int q = 0; q < KB; ++q, ring.next(), ++issued) {
-                if (issued >= SX && !warp_wait_ab(&xempty[ring.slot], ring.parity ^ 1, abort_flag)) {
+                if (issued >= SX && !warp_wait_ab(&xempty[ring.slot], ring.parity ^ 1, abort_flag,
+                                                  p.wait_budget)) {
                     ok = false;
                     break;
                 }
@@ -1158,7 +1177,8 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
                 __syncwarp();
             }
         }
-        if (!ok && lane == 0) drain_copies(xfull, SX, issued, SX);
+        if (lane == 0 && !drain_ring(xfull, SX, issued, SX)) ok = false;
+        __syncwarp();
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issue
         Ring ar(SA), xr(SX);
@@ -1172,7 +1192,8 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
             const PTile ti = ptile<GATHER>(p, t, m_tiles, n_tiles, per_set);
             const int buf = acc_bufs == 2 ? (i & 1) : 0;
             const int use = acc_bufs == 2 ? (i >> 1) : i;  // earlier tiles on this buffer
-            if (use > 0 && !warp_wait_ab(&accempty[buf], (uint32_t)((use - 1) & 1), abort_flag)) {
+            if (use > 0 && !warp_wait_ab(&accempty[buf], (uint32_t)((use - 1) & 1), abort_flag,
+                                         p.wait_budget)) {
                 ok = false;
                 break;
             }
@@ -1188,7 +1209,7 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
                 const uint32_t p1 = two ? xr.parity : p0;
                 if (two) xr.next();
                 if (!warp_wait3_ab(&afull[ar.slot], ar.parity, &xfull[x0], p0, &xfull[x1], p1,
-                                   abort_flag)) {
+                                   abort_flag, p.wait_budget)) {
                     ok = false;
                     break;
                 }
@@ -1215,9 +1236,7 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
         // every MMA issued so far has finished before tensor memory is freed
         if (elect_one()) {
             umma_commit(done);
-            const long long t0 = clock64();
-            while (!mbar_try_wait(done, 0))
-                if (clock64() - t0 > kWaitBudgetCycles) break;
+            if (!mbar_wait(done, 0)) ok = false;  // default budget: these MMAs were issued
         }
         __syncwarp();
     } else if (!COMPACT && warp >= kPEpiWarp0) {
@@ -1236,7 +1255,7 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
             const PTile ti = ptile<GATHER>(p, t, m_tiles, n_tiles, per_set);
             const int buf = acc_bufs == 2 ? (i & 1) : 0;
             const int use = acc_bufs == 2 ? (i >> 1) : i;
-            if (!warp_wait_ab(&accfull[buf], (uint32_t)(use & 1), abort_flag)) {
+            if (!warp_wait_ab(&accfull[buf], (uint32_t)(use & 1), abort_flag, p.wait_budget)) {
                 ok = false;
                 break;
             }
@@ -1311,7 +1330,7 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
             };
             auto stage = [&](int s, const uint32_t (&sb)[2 * kP]) -> bool {
                 const int cs = cr.slot;
-                if (!warp_wait_ab(&cfull[cs], cr.parity, abort_flag)) return false;
+                if (!warp_wait_ab(&cfull[cs], cr.parity, abort_flag, p.wait_budget)) return false;
                 const int off = csub * kRowBytes;
                 uint4 cw[BITS];
                 if (BITS == 3 || BITS == 6) {
@@ -1333,7 +1352,9 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
                         cw[j] = ld_shared_v4(c_line + (uint32_t)(((chunk0 + j) ^ (r & 7)) << 4));
                 }
                 const int as = ar.slot;
-                if (g0 + s >= SA && !warp_wait_ab(&aempty[as], ar.parity ^ 1, abort_flag)) return false;
+                if (g0 + s >= SA &&
+                    !warp_wait_ab(&aempty[as], ar.parity ^ 1, abort_flag, p.wait_budget))
+                    return false;
                 tc_fence_after();
                 const uint32_t a_col = t_lane + (uint32_t)(a0 + as * kAStageCols);
 #pragma unroll
@@ -1429,7 +1450,7 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
             if (COMPACT && ok) {
                 // epilogue of this tile: warp w reads tensor-memory lanes
                 // 32 * (w % 4) ... and every other 16-column chunk
-                if (!warp_wait_ab(&accfull[0], (uint32_t)(tile_i & 1), abort_flag)) {
+                if (!warp_wait_ab(&accfull[0], (uint32_t)(tile_i & 1), abort_flag, p.wait_budget)) {
                     ok = false;
                     break;
                 }
@@ -1460,9 +1481,8 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
         }
     }
 
-    if (!ok || *abort_flag) {
-        if (threadIdx.x == 0) flag_status(p.status, MXQ_DEV_TIMEOUT);
-    }
+    // a role that gave up, or a drain that ran out of its budget
+    if (!ok || (threadIdx.x == 0 && *abort_flag)) flag_status(p.status, MXQ_DEV_TIMEOUT);
     tc_fence_before();
     __syncthreads();
     if (warp == kMmaWarp) {
@@ -1644,10 +1664,12 @@ cudaError_t launch_qmm_tc(const QmmParams& p, int bits, int grid_m, int max_rows
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     if (!(gather && p.sets > 1)) cm1 = cm;  // one weight set: the second map is never read
-    switch (p.group) {
-        case 32: return launch_group<32>(p, bits, gather, grid_m, max_rows_per_tile, cm, xm, cm1, stream);
-        case 64: return launch_group<64>(p, bits, gather, grid_m, max_rows_per_tile, cm, xm, cm1, stream);
-        case 128: return launch_group<128>(p, bits, gather, grid_m, max_rows_per_tile, cm, xm, cm1, stream);
+    QmmParams q = p;
+    q.wait_budget = wait_budget_cycles();
+    switch (q.group) {
+        case 32: return launch_group<32>(q, bits, gather, grid_m, max_rows_per_tile, cm, xm, cm1, stream);
+        case 64: return launch_group<64>(q, bits, gather, grid_m, max_rows_per_tile, cm, xm, cm1, stream);
+        case 128: return launch_group<128>(q, bits, gather, grid_m, max_rows_per_tile, cm, xm, cm1, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -430,12 +430,13 @@ __device__ __forceinline__ void grid_dep_launch_dependents() {
 
 // Waits unless another role already gave up; on its own timeout it raises
 // the shared abort flag so that every role winds down without waiting.
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-    if (mbar_try_wait(bar, parity)) return true;
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              long long budget) {
+    if (mbar_poll(bar, parity, budget)) return true;
     const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!mbar_poll(bar, parity, budget)) {
         if (*abort_flag) return false;
-        if (clock64() - t0 > kWaitBudgetCycles) {
+        if (clock64() - t0 > budget) {
             *abort_flag = 1;
             return false;
         }
@@ -453,6 +454,7 @@ struct StreamShape {
     int stage_bytes; // codes + scales + biases, 16-byte aligned pieces
     int x_offset;    // shared-memory offset of the activation copy (after the ring)
     int nchunks;     // chunks over all of N: at most `rows` rows each, a multiple of the grid
+    long long wait_budget;  // pipeline-wait budget in SM cycles
 };
 
 // The first `rem` chunks of the launch have q + 1 rows, the others q rows
@@ -648,12 +650,18 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 2) * 32, 1)
             // queueing behind tens of megabytes of it
             expect_tx(&xfull, (uint32_t)(K * 2));
             bulk_g2s(base + sh.x_offset, x, (uint32_t)(K * 2), &xfull);
-            for (int j = 0;; ++j) {
+            int j = 0;  // chunks issued
+            for (;; ++j) {
                 const int chunk = blockIdx.x + j * gridDim.x;
                 if (chunk >= sh.nchunks) break;
                 const int st = j % kStreamStages;
+                // a compute warp that gave up still hands its stage back:
+                // after an abort the stage's last copy may not have landed,
+                // so nothing more is issued into the ring
                 if (j >= kStreamStages &&
-                    !wait_or_abort(&empty[st], ((j / kStreamStages) + 1) & 1, &abort_flag))
+                    (!wait_or_abort(&empty[st], ((j / kStreamStages) + 1) & 1, &abort_flag,
+                                    sh.wait_budget) ||
+                     *static_cast<volatile int*>(&abort_flag)))
                     break;
                 const int r0 = cr.begin(chunk);
                 const int rows = cr.begin(chunk + 1) - r0;
@@ -667,6 +675,11 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 2) * 32, 1)
                 bulk_g2s(dst + sh.rows * (sh.row_bytes + sh.sb_bytes),
                          bbp + (long long)r0 * sh.sb_bytes, sbb, &full[st]);
             }
+            // every copy issued has landed before this CTA can exit (the
+            // compute warps wait for them too, unless they gave up)
+            const bool landed =
+                mbar_wait(&xfull, 0) && drain_ring(full, kStreamStages, j, kStreamStages);
+            if (!landed && status) atomicOr(status, 0x8 /* MXQ_DEV_TIMEOUT */);
         }
         return;
     }
@@ -680,7 +693,7 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 2) * 32, 1)
             const int chunk = blockIdx.x + j * gridDim.x;
             if (chunk >= sh.nchunks) break;
             const int buf = j % kRedBufs;
-            if (!wait_or_abort(&redfull[buf], (j / kRedBufs) & 1, &abort_flag)) break;
+            if (!wait_or_abort(&redfull[buf], (j / kRedBufs) & 1, &abort_flag, sh.wait_budget)) break;
             const int r0 = cr.begin(chunk);
             const int rows = cr.begin(chunk + 1) - r0;
             for (int r = lane; r < rows; r += 32) {
@@ -712,7 +725,7 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 2) * 32, 1)
         uint32_t u[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) u[j] = 0;
-        if (wait_or_abort(&xfull, 0, &abort_flag) && active) {
+        if (wait_or_abort(&xfull, 0, &abort_flag, sh.wait_budget) && active) {
             const uint32_t xs = base + sh.x_offset + (uint32_t)k0 * 2;
 #pragma unroll
             for (int c = 0; c < 4; ++c)
@@ -745,7 +758,8 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 2) * 32, 1)
         const int chunk = blockIdx.x + j * gridDim.x;
         if (chunk >= sh.nchunks) break;
         const int st = j % kStreamStages;
-        const bool have = wait_or_abort(&full[st], (j / kStreamStages) & 1, &abort_flag);
+        const bool have =
+            wait_or_abort(&full[st], (j / kStreamStages) & 1, &abort_flag, sh.wait_budget);
         const uint32_t sbase = base + st * sh.stage_bytes;
         const uint32_t s_off = sbase + sh.rows * sh.row_bytes;
         const uint32_t b_off = s_off + sh.rows * sh.sb_bytes;
@@ -806,7 +820,8 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 2) * 32, 1)
         const int buf = j % kRedBufs;
         // the reducer must be done with this buffer's previous chunk
         const bool free_buf =
-            j < kRedBufs || wait_or_abort(&redempty[buf], ((j / kRedBufs) + 1) & 1, &abort_flag);
+            j < kRedBufs ||
+            wait_or_abort(&redempty[buf], ((j / kRedBufs) + 1) & 1, &abort_flag, sh.wait_budget);
         if (free_buf && (lane & (span - 1)) == 0) {
             const int q = lane / span;
             const int r = phase + q * sh.phases;
@@ -928,6 +943,7 @@ cudaError_t launch_qmv(const void* x, const uint32_t* w, const void* scales, con
         sh.rows = sh.phases * rpw;
         sh.stage_bytes = sh.rows * (sh.row_bytes + 2 * sh.sb_bytes);  // pieces are 16-byte multiples
         sh.x_offset = kStreamStages * sh.stage_bytes;
+        sh.wait_budget = wait_budget_cycles();
         // chunks of at most sh.rows rows, as many as a multiple of the grid
         sh.nchunks = (N + sh.rows - 1) / sh.rows;
         const int grid = sh.nchunks < sms ? sh.nchunks : sms;

@@ -251,6 +251,21 @@ const char* mxq_status_string(mxq_status status);
 /* Library version, major * 10000 + minor * 100 + patch. */
 int mxq_version(void);
 
+/* Testing aid; the pages have no counterpart.  Every on-chip pipeline wait
+ * (a warp waiting for a copy, a stage or an accumulator) gives up after a
+ * budget of SM clock cycles, after which the kernel winds down, the call's
+ * dev_status receives MXQ_DEV_TIMEOUT and the output is incomplete.  This
+ * sets that budget for kernels launched from now on by any thread of the
+ * process (kernels already launched keep theirs) and returns the budget now
+ * in force.  cycles <= 0 restores the default, 2e9 cycles (about one second
+ * at 2 GHz); larger values are clamped to it.  The environment variable
+ * MXQ_DEBUG_WAIT_BUDGET, read at the first launch, gives the initial value.
+ * A CTA's waits for the copies and MMAs it issued itself, before it exits or
+ * frees tensor memory, always take the default budget, so a short budget
+ * leaves no asynchronous write behind a finished kernel, and a call after it
+ * runs normally.                                                             */
+long long mxq_debug_set_wait_budget(long long cycles);
+
 #ifdef __cplusplus
 }
 #endif

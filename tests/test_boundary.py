@@ -199,3 +199,17 @@ def test_bench_reference_arm_uses_the_same_config():
     ref = src[src.index("def run_reference"):src.index("def run_profile")]
     assert '"config": CONFIG' in ref
     assert bench.CONFIG["workload"] == bench.WORKLOAD
+
+
+def test_wait_budget_setter_clamps(L):
+    # the pipeline-wait budget is host state (no device needed): values in
+    # (0, default] are taken, anything else restores the default
+    default = 2_000_000_000
+    try:
+        assert L.mxq_debug_set_wait_budget(1000) == 1000
+        assert L.mxq_debug_set_wait_budget(default) == default
+        assert L.mxq_debug_set_wait_budget(10 ** 12) == default
+        assert L.mxq_debug_set_wait_budget(1) == 1
+        assert L.mxq_debug_set_wait_budget(-5) == default
+    finally:
+        assert L.mxq_debug_set_wait_budget(0) == default
