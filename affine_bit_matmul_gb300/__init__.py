@@ -31,7 +31,9 @@ __all__ = [
     "qmv",
     "qmm",
     "qmv_kn",
+    "qmm_kn",
     "gather_qmm",
+    "gather_qmm_kn",
     "gather_qmm_gateup",
     "gather_workspace_bytes",
     "gather_qmm_noalloc",
@@ -70,7 +72,9 @@ EXPORTED_SYMBOLS = (
     "mxq_qmv",
     "mxq_qmm",
     "mxq_qmv_kn",
+    "mxq_qmm_kn",
     "mxq_gather_qmm",
+    "mxq_gather_qmm_kn",
     "mxq_gather_qmm_gateup",
     "mxq_gather_workspace_bytes",
     "mxq_gather_qmm_noalloc",
@@ -107,8 +111,12 @@ def lib():
         L.mxq_qmm.restype = I
         L.mxq_qmv_kn.argtypes = [P, P, P, P, P, I, I, I, I, P, P]
         L.mxq_qmv_kn.restype = I
+        L.mxq_qmm_kn.argtypes = [P, P, P, P, P, I, I, I, I, I, P, P]
+        L.mxq_qmm_kn.restype = I
         L.mxq_gather_qmm.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, Z, P, P]
         L.mxq_gather_qmm.restype = I
+        L.mxq_gather_qmm_kn.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, Z, P, P]
+        L.mxq_gather_qmm_kn.restype = I
         L.mxq_gather_qmm_gateup.argtypes = [P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I,
                                              I, P, Z, P, P]
         L.mxq_gather_qmm_gateup.restype = I
@@ -284,6 +292,93 @@ def qmm(x, w, scales, biases, bits: int, out=None, dev_status=None, stream=None,
     with ctx:
         _check(lib().mxq_qmm(_ptr(x), _ptr(w), _ptr(scales), _ptr(biases), _ptr(out), M, K, N,
                              bits, group_size, _ptr(dev_status), st), "mxq_qmm")
+    return out
+
+
+def _check_weights_kn(w, scales, biases, K, N, bits, device, lead=(), group_size=64):
+    """[K, N]-layout weights: ``w`` int32 [..., K, N*bits/32], ``scales`` and
+    ``biases`` bf16 [..., K, N/G]."""
+    torch = _torch()
+    _require(w, "w", _code_dtypes(), device)
+    _require(scales, "scales", (torch.bfloat16,), device)
+    _require(biases, "biases", (torch.bfloat16,), device)
+    if group_size <= 0:
+        raise ValueError("group_size must be positive")
+    if tuple(w.shape) != tuple(lead) + (K, N * bits // 32):
+        raise ValueError("w has shape %s, expected %s" % (tuple(w.shape),
+                                                          tuple(lead) + (K, N * bits // 32)))
+    for t, name in ((scales, "scales"), (biases, "biases")):
+        if tuple(t.shape) != tuple(lead) + (K, N // group_size):
+            raise ValueError("%s has shape %s, expected %s" % (
+                name, tuple(t.shape), tuple(lead) + (K, N // group_size)))
+
+
+def qmm_kn(x, w, scales, biases, bits: int, out=None, dev_status=None, stream=None,
+           group_size: int = 64):
+    """Prefill GEMM with w stored [K, N] (codes and groups along n):
+    ``y[m, n] = sum_k x[m, k] (s[k, n/G] q[k, n] + b[k, n/G])``; ``x`` bf16
+    [M, K], ``w`` int32 [K, N*bits/32], ``scales``/``biases`` bf16 [K, N/G]."""
+    torch = _torch()
+    _require(x, "x", (torch.bfloat16,))
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D [M, K]")
+    M, K = x.shape
+    if w.dim() != 2:
+        raise ValueError("w must be [K, N*bits/32]")
+    N = w.shape[1] * 32 // bits
+    _check_weights_kn(w, scales, biases, K, N, bits, x.device, group_size=group_size)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _require(out, "out", (torch.bfloat16,), x.device)
+    if tuple(out.shape) != (M, N):
+        raise ValueError("out has shape %s, expected %s" % (tuple(out.shape), (M, N)))
+    if dev_status is not None:
+        _require(dev_status, "dev_status", (torch.int32,), x.device)
+    ctx, st = _launch_on(x.device, stream)
+    with ctx:
+        _check(lib().mxq_qmm_kn(_ptr(x), _ptr(w), _ptr(scales), _ptr(biases), _ptr(out), M, K, N,
+                                bits, group_size, _ptr(dev_status), st), "mxq_qmm_kn")
+    return out
+
+
+def gather_qmm_kn(x, w, scales, biases, expert_ids, row_src, bits: int, out=None, workspace=None,
+                  dev_status=None, stream=None, group_size: int = 64):
+    """Sorted mixture-of-experts GEMM with each expert's w stored [K, N]:
+    ``w`` int32 [E, K, N*bits/32], ``scales``/``biases`` bf16 [E, K, N/G];
+    sorted row r multiplies ``x[row_src[r]]`` by expert ``expert_ids[r]``."""
+    torch = _torch()
+    _require(x, "x", (torch.bfloat16,))
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D [T, K]")
+    T, K = x.shape
+    if w.dim() != 3:
+        raise ValueError("w must be [E, K, N*bits/32]")
+    E = w.shape[0]
+    N = w.shape[2] * 32 // bits
+    _check_weights_kn(w, scales, biases, K, N, bits, x.device, lead=(E,), group_size=group_size)
+    _require(expert_ids, "expert_ids", (torch.int32,), x.device)
+    B = expert_ids.numel()
+    if row_src is not None:
+        _require(row_src, "row_src", (torch.int32,), x.device)
+        if row_src.numel() != B:
+            raise ValueError("row_src must have B entries")
+    if out is None:
+        out = torch.empty((B, N), dtype=torch.bfloat16, device=x.device)
+    _require(out, "out", (torch.bfloat16,), x.device)
+    if tuple(out.shape) != (B, N):
+        raise ValueError("out has shape %s, expected %s" % (tuple(out.shape), (B, N)))
+    if workspace is None:
+        workspace = torch.empty((gather_workspace_bytes(B, E, K if row_src is not None else 0, N),),
+                                dtype=torch.uint8, device=x.device)
+    _require(workspace, "workspace", (torch.uint8,), x.device)
+    if dev_status is not None:
+        _require(dev_status, "dev_status", (torch.int32,), x.device)
+    ctx, st = _launch_on(x.device, stream)
+    with ctx:
+        _check(lib().mxq_gather_qmm_kn(
+            _ptr(x), _ptr(w), _ptr(scales), _ptr(biases), _ptr(expert_ids), _ptr(row_src),
+            _ptr(out), T, B, E, K, N, bits, group_size, _ptr(workspace), workspace.numel(),
+            _ptr(dev_status), st), "mxq_gather_qmm_kn")
     return out
 
 

@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
                                                           uint4* __restrict__ x_sorted) {
     const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (r < B) {
-        const int chunks = K / 8;  // 16-byte chunks per row (K % 64 == 0)
+        const int chunks = K / 8;  // 16-byte chunks per row (K % 8 == 0)
         const int src = row_src[r];
         uint4* dst = x_sorted + (long long)r * chunks;
         if (src < 0 || src >= T) {

@@ -273,6 +273,54 @@ mxq_status mxq_qmv_kn(const void* x, const uint32_t* w, const void* scales, cons
     return err == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA;
 }
 
+mxq_status mxq_qmm_kn(const void* x, const uint32_t* w, const void* scales, const void* biases,
+                      void* y, int M, int K, int N, int bits, int group_size, int32_t* dev_status,
+                      void* stream) {
+    if (bits == 3 || bits == 6) return MXQ_ERR_UNSUPPORTED;
+    if (bits != 2 && bits != 4 && bits != 8) return MXQ_ERR_INVALID_ARG;
+    if (group_size != 32 && group_size != 64 && group_size != 128) return MXQ_ERR_INVALID_ARG;
+    if (M <= 0 || K <= 0 || N <= 0 || N % 64 != 0 || N % group_size != 0) return MXQ_ERR_INVALID_ARG;
+    if (M > 1 && K % 8 != 0) return MXQ_ERR_INVALID_ARG;  // 16-byte activation rows for TMA
+    if (!x || !w || !scales || !biases || !y) return MXQ_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 16) || !aligned(scales, 2) ||
+        !aligned(biases, 2) || !aligned(dev_status, 4))
+        return MXQ_ERR_MISALIGNED;
+    if (M == 1)  // one activation row: the [K, N] GEMV (same operation)
+        return mxq_qmv_kn(x, w, scales, biases, y, K, N, bits, group_size, dev_status, stream);
+    int sms = 0;
+    mxq_status st = check_device(&sms);
+    if (st != MXQ_OK) return st;
+    const int K64 = (K + 63) / 64 * 64;
+    const DensePlan pl = plan_dense(M, K64, N, bits, sms);
+    if (pl.m_tiles > 65535) return MXQ_ERR_UNSUPPORTED;  // grid.y limit
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dev_status && cudaMemsetAsync(dev_status, 0, sizeof(int32_t), s) != cudaSuccess)
+        return MXQ_ERR_CUDA;
+    mxq::QmmParams p;
+    std::memset(&p, 0, sizeof p);
+    p.x = x;
+    p.w = w;
+    p.scales = static_cast<const uint16_t*>(scales);
+    p.biases = static_cast<const uint16_t*>(biases);
+    p.y = y;
+    p.status = dev_status;
+    p.M = M;
+    p.T = M;
+    p.E = 1;
+    p.K = K;
+    p.N = N;
+    p.group = group_size;
+    p.sets = 1;
+    p.x_rows = M;
+    p.x_box_rows = pl.m_tile;
+    p.m_tile = pl.m_tile;
+    p.tmem_cols = pl.tmem_cols;
+    p.splits = pl.splits;
+    p.kb_per_split = pl.kb_per_split;
+    cudaError_t err = mxq::launch_qmm_kn(p, bits, pl.m_tiles, pl.m_tile, s);
+    return err == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA;
+}
+
 mxq_status mxq_quantize(const float* w, uint32_t* codes, void* scales, void* biases, int N,
                         int K, int bits, int group_size, void* stream) {
     mxq_status st = check_common(K, N, bits, group_size);
@@ -402,6 +450,76 @@ mxq_status gather_call(const void* x, const uint32_t* w, const void* scales, con
 }  // namespace
 
 extern "C" {
+
+mxq_status mxq_gather_qmm_kn(const void* x, const uint32_t* w, const void* scales,
+                             const void* biases, const int32_t* expert_ids, const int32_t* row_src,
+                             void* y, int T, int B, int E, int K, int N, int bits, int group_size,
+                             void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                             void* stream) {
+    if (bits == 3 || bits == 6) return MXQ_ERR_UNSUPPORTED;
+    if (bits != 2 && bits != 4 && bits != 8) return MXQ_ERR_INVALID_ARG;
+    if (group_size != 32 && group_size != 64 && group_size != 128) return MXQ_ERR_INVALID_ARG;
+    if (K <= 0 || K % 8 != 0 || N <= 0 || N % 64 != 0 || N % group_size != 0)
+        return MXQ_ERR_INVALID_ARG;
+    if (T <= 0 || B <= 0 || E <= 0) return MXQ_ERR_INVALID_ARG;
+    if (!row_src && T != B) return MXQ_ERR_INVALID_ARG;
+    if (!x || !w || !scales || !biases || !expert_ids || !y) return MXQ_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 16) || !aligned(scales, 2) ||
+        !aligned(biases, 2) || !aligned(expert_ids, 4) || !aligned(row_src, 4) ||
+        !aligned(dev_status, 4) || !aligned(workspace, 256))
+        return MXQ_ERR_MISALIGNED;
+    const size_t need = mxq::gather_scratch_bytes(B, E, K, N, bits, group_size, row_src != nullptr);
+    if (!workspace || workspace_bytes < need) return MXQ_ERR_WORKSPACE;
+    if (gather_max_tiles(B, E) > 65535) return MXQ_ERR_UNSUPPORTED;  // grid.y limit
+    mxq_status st = check_device(nullptr);
+    if (st != MXQ_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    auto* tiles = static_cast<mxq::MTile*>(workspace);
+    int* tile_count = reinterpret_cast<int*>(static_cast<char*>(workspace) +
+                                             align_up(gather_max_tiles(B, E) * sizeof(mxq::MTile), 256));
+    int* seg_start = tile_count + 256 / sizeof(int);
+    char* rows_area = static_cast<char*>(workspace) + gather_table_bytes(B, E);
+    const size_t max_tiles = gather_max_tiles(B, E);
+    // the tile table (and zeroed rows for invalid ids), then the routed rows
+    // in sorted order, then one CTA per (tile, 128 columns)
+    cudaError_t err = mxq::launch_gather_prepass(expert_ids, row_src, T, B, E, N,
+                                                 kGatherRowsPerTile, tiles, tile_count, seg_start,
+                                                 y, nullptr, dev_status, s);
+    if (err != cudaSuccess) return MXQ_ERR_CUDA;
+    const void* xa = x;
+    if (row_src) {
+        err = mxq::launch_gather_rows(x, row_src, T, B, K, rows_area, s);
+        if (err != cudaSuccess) return MXQ_ERR_CUDA;
+        xa = rows_area;
+    }
+    mxq::QmmParams p;
+    std::memset(&p, 0, sizeof p);
+    p.x = xa;
+    p.w = w;
+    p.scales = static_cast<const uint16_t*>(scales);
+    p.biases = static_cast<const uint16_t*>(biases);
+    p.y = y;
+    p.tiles = tiles;
+    p.tile_count = tile_count;
+    p.status = dev_status;
+    p.x_rows = B;
+    p.x_box_rows = 16;
+    p.M = B;
+    p.T = T;
+    p.E = E;
+    p.K = K;
+    p.N = N;
+    p.group = group_size;
+    p.m_tile = kGatherRowsPerTile;
+    p.tmem_cols = kGatherRowsPerTile;
+    p.splits = 1;
+    p.kb_per_split = (K + 63) / 64;
+    p.sets = 1;
+    p.w_expert_stride = (long long)K * N * bits / 32;
+    p.sb_expert_stride = (long long)K * (N / group_size);
+    err = mxq::launch_qmm_kn(p, bits, (int)max_tiles, kGatherRowsPerTile, s);
+    return err == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA;
+}
 
 mxq_status mxq_gather_qmm(const void* x, const uint32_t* w, const void* scales,
                           const void* biases, const int32_t* expert_ids, const int32_t* row_src,

@@ -92,6 +92,11 @@ cudaError_t launch_qmv(const void* x, const uint32_t* w, const void* scales, con
 cudaError_t launch_qmm_tc(const QmmParams& p, int bits, int grid_m, int max_rows_per_tile,
                           cudaStream_t stream);
 
+// The same GEMM with w stored [K, N] (codes and groups along n; 2-, 4- and
+// 8-bit): dense (M tiles, K split over a cluster) or grouped (tile list).
+cudaError_t launch_qmm_kn(const QmmParams& p, int bits, int grid_m, int max_rows_per_tile,
+                          cudaStream_t stream);
+
 // Grouped form, step 1: validate ids, find each expert's rows, build the
 // tile list (count in tile_count[0]), zero tile_count[1] (the GEMM's tile
 // counter) and the y rows that no tile covers.

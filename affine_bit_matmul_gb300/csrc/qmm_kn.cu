@@ -1,0 +1,548 @@
+// Quantized GEMM on the sm_103a tensor cores for weights stored [K, N]: row k
+// of w holds the codes of every output column n as one little-endian bit
+// stream, and each group is G consecutive n of one row, so
+//
+//     y[m, n] = sum_k x[m, k] * (s[k, n/G] * q[k, n] + b[k, n/G]),
+//
+// the second operand layout the grouped GEMM is checked in (mlxcel PR #1562,
+// What changed).  Dense and sorted-MoE forms.
+//
+// In this layout one code word holds consecutive n of one k, so a word
+// dequantises into 16 bytes (8 bf16) that are contiguous along n: the natural
+// tensor-core operand is MN-major.  Per 64-wide block of k:
+//  * a TMA copy brings the block's codes of the CTA's 128 columns ([64 rows
+//    of k] x [128 * bits / 8 bytes]) into a ring of code slots, and another
+//    the activation tile (128-byte swizzle, the MMA's B operand, K-major);
+//  * eight dequant warps turn the codes into bf16 w^ = s*q + b (one rounding,
+//    as in the [N, K] kernels) and store them into a shared-memory A stage
+//    in the MN-major 128-byte-swizzled layout: 64-column atoms of 8 k rows x
+//    128 bytes, 16-byte chunk c of row r at chunk c ^ r; the two atoms along
+//    n are 1024 bytes apart (the descriptor's leading byte offset) and the
+//    8-row atoms along k 2048 bytes apart (its stride byte offset);
+//  * one elected lane issues four 128 x N x 16 tcgen05.mma with A read from
+//    shared memory ("transpose A" set in the instruction descriptor) and the
+//    fp32 accumulator in tensor memory; the epilogue reads it back with
+//    tcgen05.ld and stores bf16.
+// With few tiles (small M), K is split over the CTAs of a cluster and the
+// fp32 partials are added through distributed shared memory in rank order.
+//
+// Every pipeline wait is bounded by the kernel's wait budget; the copy warps
+// wait for their issued copies and the MMA warp for its MMAs before the CTA
+// exits or frees tensor memory (default budget), whatever happened.
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/mxq.h"
+#include "mxq_device.cuh"
+#include "mxq_internal.h"
+#include "tc_common.cuh"
+
+namespace mxq {
+namespace {
+
+constexpr int kDequantWarps = 8;     // warps 0-7: dequant, then epilogue
+constexpr int kDequantThreads = kDequantWarps * 32;
+constexpr int kCodeWarp = 8;         // codes TMA
+constexpr int kMmaWarp = 9;          // TMEM owner, MMA issue
+constexpr int kXWarp = 10;           // activation TMA
+constexpr int kThreads = 11 * 32;
+constexpr int kTileN = 128;          // output columns per CTA (MMA M)
+constexpr int kBK = 64;              // k per stage (one activation swizzle atom)
+constexpr int kAStageBytes = kTileN * kBK * 2;  // 16 KB of bf16, MN-major
+constexpr int kAtomMN = 1024;        // bytes between the two 64-column atoms
+constexpr int kAtomK = 2048;         // bytes between 8-row atoms along k
+constexpr int kAStages = 4;
+constexpr int kMaxCodeStages = 8;
+constexpr int kMaxXStages = 8;
+constexpr int kSmemBudget = 224 * 1024;
+
+struct KnLayout {
+    int x_bytes, x_stages;   // activation ring at 0 (one 64-wide atom column per slot)
+    int a_offset;            // A stages after it
+    int c_bytes, c_stages;   // code ring after the A stages
+    int c_offset;
+    int bar_offset, total;
+};
+
+__host__ __device__ inline KnLayout make_kn_layout(int max_rows, int bits) {
+    KnLayout L;
+    const int rows16 = (max_rows + 15) & ~15;
+    L.x_bytes = (rows16 / 8) * 1024;          // 128 B per row, 8-row atoms
+    L.c_bytes = kBK * kTileN * bits / 8;      // 2, 4 or 8 KB
+    int room = kSmemBudget - kAStages * kAStageBytes;
+    L.c_stages = 4;
+    room -= L.c_stages * L.c_bytes;
+    L.x_stages = room / L.x_bytes;
+    if (L.x_stages > kMaxXStages) L.x_stages = kMaxXStages;
+    if (L.x_stages < 2) L.x_stages = 2;
+    room -= L.x_stages * L.x_bytes;
+    while (L.c_stages < kMaxCodeStages && room >= L.c_bytes) {
+        ++L.c_stages;
+        room -= L.c_bytes;
+    }
+    L.a_offset = L.x_stages * L.x_bytes;
+    L.c_offset = L.a_offset + kAStages * kAStageBytes;
+    L.bar_offset = L.c_offset + L.c_stages * L.c_bytes;
+    // cfull, cempty, afull, aempty, xfull, xempty, accf; tmem base
+    L.total = L.bar_offset + (2 * kMaxCodeStages + 2 * kAStages + 2 * kMaxXStages + 1) * 8 + 16;
+    // a K split adds fp32 partial tiles [rows16][128] through the rings
+    if (L.total < rows16 * kTileN * 4) L.total = rows16 * kTileN * 4;
+    L.total += 1024;  // alignment slack
+    return L;
+}
+
+// Shared-memory descriptor of an MN-major operand in the 128-byte-swizzled
+// layout: leading byte offset = bytes between 64-column atoms along M,
+// stride byte offset = bytes between 8-row atoms along K; version 1,
+// swizzle mode "128B" = 2.
+__device__ __forceinline__ uint64_t umma_desc_mn_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)(kAtomMN >> 4) << 16;
+    d |= (uint64_t)(kAtomK >> 4) << 32;
+    d |= (uint64_t)1u << 46;
+    d |= (uint64_t)2u << 61;
+    return d;
+}
+
+// Byte offset of the 16-byte chunk holding columns [8c, 8c + 8) of row k in
+// an A stage.
+__device__ __forceinline__ uint32_t a_chunk(int k, int c) {
+    return (uint32_t)((c >> 3) * kAtomMN + (k >> 3) * kAtomK + (k & 7) * 128 +
+                      (((c & 7) ^ (k & 7)) << 4));
+}
+
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_shared_v2(uint32_t addr, uint32_t a, uint32_t b) {
+    asm volatile("st.shared.v2.b32 [%0], {%1,%2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+
+template <int BITS, bool GATHER, int GROUP>
+__global__ void __launch_bounds__(kThreads, 1)
+    qmm_kn_kernel(const QmmParams p, int max_rows, const __grid_constant__ CUtensorMap code_map,
+                  const __grid_constant__ CUtensorMap x_map) {
+    static_assert(BITS == 2 || BITS == 4 || BITS == 8, "2-, 4- or 8-bit codes");
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const KnLayout L = make_kn_layout(max_rows, BITS);
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    uint64_t* cfull = reinterpret_cast<uint64_t*>(smem + L.bar_offset);
+    uint64_t* cempty = cfull + kMaxCodeStages;
+    uint64_t* afull = cempty + kMaxCodeStages;
+    uint64_t* aempty = afull + kAStages;
+    uint64_t* xfull = aempty + kAStages;
+    uint64_t* xempty = xfull + kMaxXStages;
+    uint64_t* accf = xempty + kMaxXStages;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
+    const uint32_t smem_base = smem_u32(smem);
+    const uint32_t x_base0 = smem_base;
+    const uint32_t a_base0 = smem_base + L.a_offset;
+    const uint32_t c_base0 = smem_base + L.c_offset;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = lane_id();
+
+    // ---- which tile this CTA computes
+    int e = 0, row_start, rows;
+    if (GATHER) {
+        if ((int)blockIdx.y >= *p.tile_count) return;  // whole CTA, before any sync
+        const MTile t = p.tiles[blockIdx.y];
+        e = t.e;
+        row_start = t.row_start;
+        rows = t.rows;
+    } else {
+        row_start = blockIdx.y * p.m_tile;
+        rows = min(p.m_tile, p.M - row_start);
+    }
+    const int n_mma = (rows + 15) & ~15;
+    const int n0 = blockIdx.x * kTileN;
+    const int KB = (p.K + kBK - 1) / kBK;  // a last partial block reads zeros past K
+    const int kb_begin = (GATHER ? 0 : (int)blockIdx.z) * p.kb_per_split;
+    const int nkb = min(KB, kb_begin + p.kb_per_split) - kb_begin;
+    const int SC = L.c_stages;
+    const int SX = L.x_stages;
+    const int kCols = p.tmem_cols;
+
+    if (warp == kCodeWarp && lane == 0) prefetch_tmap(&code_map);
+    if (warp == kXWarp && lane == 0) prefetch_tmap(&x_map);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < SC; ++i) {
+            mbar_init(&cfull[i], 1);
+            mbar_init(&cempty[i], kDequantWarps);
+        }
+        for (int i = 0; i < kAStages; ++i) {
+            mbar_init(&afull[i], kDequantWarps);
+            mbar_init(&aempty[i], 1);
+        }
+        for (int i = 0; i < SX; ++i) {
+            mbar_init(&xfull[i], 1);
+            mbar_init(&xempty[i], 1);
+        }
+        mbar_init(accf, 1);
+        mbar_init_fence();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(tmem_slot, (uint32_t)kCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    bool ok = true;
+
+    if (warp == kCodeWarp) {
+        // ---------------------------------------------------------------- codes TMA
+        // one box per stage: 64 rows of k x the tile's 128 columns of codes;
+        // columns past N read as zero
+        const int x0 = n0 * BITS / 8;  // bytes; a multiple of 32
+        Ring ring(SC);
+        int q = 0;
+        for (; q < nkb; ++q, ring.next()) {
+            if (q >= SC && !warp_wait(&cempty[ring.slot], ring.parity ^ 1, p.wait_budget)) {
+                ok = false;
+                break;
+            }
+            if (elect_one()) {
+                mbar_expect_tx(&cfull[ring.slot], (uint32_t)L.c_bytes);
+                const uint32_t dst = c_base0 + ring.slot * L.c_bytes;
+                const int k0 = (kb_begin + q) * kBK;
+                if (GATHER)
+                    tma_load_3d(dst, &code_map, x0, k0, e, &cfull[ring.slot]);
+                else
+                    tma_load_2d(dst, &code_map, x0, k0, &cfull[ring.slot]);
+            }
+            __syncwarp();
+        }
+        // the slots issued last may still be loading if a consumer gave up
+        if (lane == 0 && !drain_ring(cfull, SC, q, SC)) ok = false;
+        __syncwarp();
+    } else if (warp == kXWarp) {
+        // ---------------------------------------------------------------- activation TMA
+        const int boxes = (n_mma + p.x_box_rows - 1) / p.x_box_rows;
+        const uint32_t x_bytes_in = (uint32_t)(boxes * p.x_box_rows * 128);
+        Ring ring(SX);
+        int q = 0;
+        for (; q < nkb; ++q, ring.next()) {
+            if (q >= SX && !warp_wait(&xempty[ring.slot], ring.parity ^ 1, p.wait_budget)) {
+                ok = false;
+                break;
+            }
+            if (elect_one()) {
+                mbar_expect_tx(&xfull[ring.slot], x_bytes_in);
+                for (int b = 0; b < boxes; ++b)
+                    tma_load_2d(x_base0 + ring.slot * L.x_bytes + b * p.x_box_rows * 128, &x_map,
+                                (kb_begin + q) * kBK, row_start + b * p.x_box_rows,
+                                &xfull[ring.slot]);
+            }
+            __syncwarp();
+        }
+        if (lane == 0 && !drain_ring(xfull, SX, q, SX)) ok = false;
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        // ---------------------------------------------------------------- MMA issue
+        const uint32_t idesc = umma_idesc_bf16(kTileN, (uint32_t)n_mma) | (1u << 15);  // A MN-major
+        Ring ar(kAStages), xr(SX);
+        for (int q = 0; q < nkb; ++q, ar.next(), xr.next()) {
+            if (!warp_wait(&afull[ar.slot], ar.parity, p.wait_budget) ||
+                !warp_wait(&xfull[xr.slot], xr.parity, p.wait_budget)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (elect_one()) {
+                const uint32_t a_stage = a_base0 + ar.slot * kAStageBytes;
+                const uint64_t bd = umma_desc_sw128(x_base0 + xr.slot * L.x_bytes);
+#pragma unroll
+                for (int j = 0; j < kBK / 16; ++j)  // 16 k = two 8-row atoms of A, 32 B of B
+                    umma_bf16(tmem, umma_desc_mn_sw128(a_stage + j * 2 * kAtomK), bd + 2 * j,
+                              idesc, (q > 0 || j > 0) ? 1u : 0u);
+                umma_commit(&aempty[ar.slot]);
+                umma_commit(&xempty[xr.slot]);
+            }
+            __syncwarp();
+        }
+        if (elect_one()) umma_commit(accf);  // also after an abort: fires once issued MMAs finish
+        __syncwarp();
+    } else if (warp < kDequantWarps) {
+        // ---------------------------------------------------------------- dequant
+        // a stage's codes are 64 rows of W words; thread t takes words
+        // t, t + 256, ...: word i is row i / W, columns [(i % W) * 32 / BITS, ...)
+        constexpr int W = kTileN * BITS / 32;                // words per code row
+        constexpr int kWords = kBK * W / kDequantThreads;    // words per thread: 2, 4, 8
+        constexpr int kRowStep = kDequantThreads / W;        // rows between a thread's words
+        constexpr int kPerWord = 32 / BITS;                  // columns per word
+        const int t = threadIdx.x;
+        const int wc = t % W;                   // word column: the same for all of the thread's words
+        const int r0 = t / W;                   // first row
+        const int nl = wc * kPerWord;           // first column of the word, within the tile
+        const bool col_ok = n0 + nl < p.N;      // columns past N: zero codes, no scale read
+        const int groups = p.N / GROUP;         // scale/bias entries per row of k
+        const long long sb_e = (long long)e * p.sb_expert_stride;
+        const uint16_t* srow = p.scales + sb_e + (n0 + nl) / GROUP;
+        const uint16_t* brow = p.biases + sb_e + (n0 + nl) / GROUP;
+        // this stage's scale/bias pairs, loaded a stage ahead
+        uint32_t sv[kWords], bv[kWords], sn[kWords], bn[kWords];
+        auto sb_load = [&](int q, uint32_t (&s)[kWords], uint32_t (&b)[kWords]) {
+#pragma unroll
+            for (int j = 0; j < kWords; ++j) {
+                s[j] = 0u;
+                b[j] = 0u;
+                const long long kr = (long long)(kb_begin + q) * kBK + r0 + j * kRowStep;
+                if (col_ok && q < nkb && kr < p.K) {
+                    s[j] = __ldg(srow + kr * groups);
+                    b[j] = __ldg(brow + kr * groups);
+                }
+            }
+        };
+        sb_load(0, sv, bv);
+        Ring cr(SC), ar(kAStages);
+        for (int q = 0; q < nkb; ++q, cr.next(), ar.next()) {
+            sb_load(q + 1, sn, bn);
+            if (!warp_wait(&cfull[cr.slot], cr.parity, p.wait_budget)) {
+                ok = false;
+                break;
+            }
+            const uint32_t c_slot = c_base0 + cr.slot * L.c_bytes;
+            uint32_t wd[kWords];
+#pragma unroll
+            for (int j = 0; j < kWords; ++j)
+                wd[j] = ld_shared_u32(c_slot + (uint32_t)(((r0 + j * kRowStep) * W + wc) * 4));
+            if (q >= kAStages && !warp_wait(&aempty[ar.slot], ar.parity ^ 1, p.wait_budget)) {
+                ok = false;
+                break;
+            }
+            const uint32_t a_stage = a_base0 + ar.slot * kAStageBytes;
+#pragma unroll
+            for (int j = 0; j < kWords; ++j) {
+                const int k = r0 + j * kRowStep;
+                if (BITS == 8) {
+                    uint32_t o[2];
+                    dequant_word8(wd[j], bf16_bits_to_float(sv[j]), bf16_bits_to_float(bv[j]), o);
+                    // four columns: half of a 16-byte chunk
+                    st_shared_v2(a_stage + a_chunk(k, nl >> 3) + (uint32_t)((nl & 7) * 2), o[0],
+                                 o[1]);
+                } else if (BITS == 4) {
+                    uint32_t o[4];
+                    dequant_word4(wd[j], sv[j] | (sv[j] << 16), bv[j] | (bv[j] << 16), o);
+                    st_shared_v4(a_stage + a_chunk(k, nl >> 3), o[0], o[1], o[2], o[3]);
+                } else {
+                    uint32_t o[8];
+                    dequant_word2(wd[j], sv[j] | (sv[j] << 16), bv[j] | (bv[j] << 16), o);
+                    st_shared_v4(a_stage + a_chunk(k, nl >> 3), o[0], o[1], o[2], o[3]);
+                    st_shared_v4(a_stage + a_chunk(k, (nl >> 3) + 1), o[4], o[5], o[6], o[7]);
+                }
+            }
+            // the tensor cores read the stage through the async proxy; the
+            // code slot is released only now that its words have been used
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&cempty[cr.slot]);
+                mbar_arrive(&afull[ar.slot]);
+            }
+#pragma unroll
+            for (int j = 0; j < kWords; ++j) {
+                sv[j] = sn[j];
+                bv[j] = bn[j];
+            }
+        }
+
+        // ---------------------------------------------------------------- epilogue
+        if (ok && !mbar_wait(accf, 0, p.wait_budget)) ok = false;
+        tc_fence_after();
+        const int quarter = warp & 3;     // tensor-memory lanes 32*quarter ...
+        const int colhalf = warp >> 2;    // 16-column chunks of this parity
+        const int lane_row = quarter * 32 + lane;
+        const int ny = n0 + lane_row;
+        const bool y_ok = ny < p.N;
+        const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
+        __nv_bfloat16* y = static_cast<__nv_bfloat16*>(p.y);
+        if (p.splits == 1) {
+            for (int c0 = colhalf * 16; c0 < n_mma; c0 += 32) {
+                uint32_t v[16];
+                tmem_ld16(taddr + c0, v);
+                tmem_ld_wait();
+                if (ok && y_ok) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int m = c0 + j;
+                        if (m < rows)
+                            y[(long long)(row_start + m) * p.N + ny] =
+                                __float2bfloat16_rn(__uint_as_float(v[j]));
+                    }
+                }
+            }
+        } else {
+            // K split: each CTA writes its fp32 partial tile [m][128] into its
+            // own shared memory (every stage has been consumed by the MMAs)
+            const uint32_t part = smem_base;
+            for (int c0 = colhalf * 16; c0 < n_mma; c0 += 32) {
+                uint32_t v[16];
+                tmem_ld16(taddr + c0, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(part + ((c0 + j) * kTileN + lane_row) * 4),
+                                 "r"(v[j])
+                                 : "memory");
+            }
+        }
+    }
+
+    if (p.splits > 1) {
+        // every thread of every CTA of the cluster takes part in both barriers
+        cluster_sync();
+        if (warp < kDequantWarps) {
+            // rank z sums rows m = z, z + S, ... over all ranks in rank order
+            const int rank = (int)cluster_rank();
+            const int S = p.splits;
+            const int c4 = (threadIdx.x & 31) * 4;
+            const int ph = threadIdx.x >> 5;
+            const int n_out = n0 + c4;
+            __nv_bfloat16* y = static_cast<__nv_bfloat16*>(p.y);
+            const bool vec_ok = n_out + 3 < p.N;  // N % 64 == 0: four columns stay together
+            for (int m = rank + S * ph; m < rows; m += S * kDequantWarps) {
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int z = 0; z < S; ++z) {
+                    const float4 v =
+                        ld_cluster_f32x4(map_cluster(smem_base + (m * kTileN + c4) * 4, (uint32_t)z));
+                    acc.x += v.x;
+                    acc.y += v.y;
+                    acc.z += v.z;
+                    acc.w += v.w;
+                }
+                if (ok && vec_ok) {
+                    uint2 pk;
+                    pk.x = cvt_bf16x2(acc.x, acc.y);
+                    pk.y = cvt_bf16x2(acc.z, acc.w);
+                    *reinterpret_cast<uint2*>(y + (long long)(row_start + m) * p.N + n_out) = pk;
+                }
+            }
+        }
+        cluster_sync();  // partials stay readable until every rank is done
+    }
+
+    if (!ok) flag_status(p.status, MXQ_DEV_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        // accf fires once every MMA issued has finished; tensor memory is
+        // freed only after that (default budget)
+        if (lane == 0 && !mbar_wait(accf, 0)) flag_status(p.status, MXQ_DEV_TIMEOUT);
+        __syncwarp();
+        tmem_dealloc(tmem, (uint32_t)kCols);
+    }
+}
+
+template <int BITS, bool GATHER, int GROUP>
+cudaError_t launch_kn(const QmmParams& p, int grid_m, int max_rows, const CUtensorMap& cm,
+                      const CUtensorMap& xm, cudaStream_t stream) {
+    const KnLayout L = make_kn_layout(max_rows, BITS);
+    static bool attr_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        cudaError_t err = cudaFuncSetAttribute(qmm_kn_kernel<BITS, GATHER, GROUP>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+        if (err != cudaSuccess) return err;
+        attr_set[dev] = true;
+    }
+    if (L.total > 232448) return cudaErrorInvalidConfiguration;
+    // the partial tiles of a K split must stay below the barriers
+    if (((max_rows + 15) & ~15) * kTileN * 4 > L.bar_offset) return cudaErrorInvalidConfiguration;
+    const dim3 grid((p.N + kTileN - 1) / kTileN, grid_m, GATHER ? 1 : p.splits);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = L.total;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = GATHER ? 1 : p.splits;  // the K splits of one tile form a cluster
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t err = cudaLaunchKernelEx(&cfg, qmm_kn_kernel<BITS, GATHER, GROUP>, p, max_rows, cm, xm);
+    if (err != cudaSuccess) return err;
+    return cudaGetLastError();
+}
+
+template <int GROUP>
+cudaError_t launch_kn_group(const QmmParams& p, int bits, bool gather, int grid_m, int max_rows,
+                            const CUtensorMap& cm, const CUtensorMap& xm, cudaStream_t stream) {
+    if (gather) {
+        if (bits == 2) return launch_kn<2, true, GROUP>(p, grid_m, max_rows, cm, xm, stream);
+        if (bits == 4) return launch_kn<4, true, GROUP>(p, grid_m, max_rows, cm, xm, stream);
+        return launch_kn<8, true, GROUP>(p, grid_m, max_rows, cm, xm, stream);
+    }
+    if (bits == 2) return launch_kn<2, false, GROUP>(p, grid_m, max_rows, cm, xm, stream);
+    if (bits == 4) return launch_kn<4, false, GROUP>(p, grid_m, max_rows, cm, xm, stream);
+    return launch_kn<8, false, GROUP>(p, grid_m, max_rows, cm, xm, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_qmm_kn(const QmmParams& p, int bits, int grid_m, int max_rows_per_tile,
+                          cudaStream_t stream) {
+    if (bits != 2 && bits != 4 && bits != 8) return cudaErrorInvalidValue;
+    EncodeTiledFn enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const bool gather = p.tiles != nullptr;
+    // packed codes as bytes: [E][K][N * bits / 8]; box = the tile's 128
+    // columns x 64 rows of k
+    CUtensorMap cm, xm;
+    const cuuint64_t row_bytes = (cuuint64_t)p.N * bits / 8;
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const cuuint32_t box[3] = {(cuuint32_t)(kTileN * bits / 8), (cuuint32_t)kBK, 1};
+    if (gather) {
+        const cuuint64_t dims[3] = {row_bytes, (cuuint64_t)p.K, (cuuint64_t)p.E};
+        const cuuint64_t strides[2] = {row_bytes, row_bytes * (cuuint64_t)p.K};
+        if (enc(&cm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint32_t*>(p.w), dims, strides, box,
+                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    } else {
+        const cuuint64_t dims[2] = {row_bytes, (cuuint64_t)p.K};
+        const cuuint64_t strides[1] = {row_bytes};
+        if (enc(&cm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint32_t*>(p.w), dims, strides, box,
+                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    // activation rows: [x_rows, K] bf16, 64-wide boxes with 128-byte swizzle
+    const cuuint64_t xdims[2] = {(cuuint64_t)p.K, (cuuint64_t)p.x_rows};
+    const cuuint64_t xstrides[1] = {(cuuint64_t)p.K * 2};
+    const cuuint32_t xbox[2] = {(cuuint32_t)kBK, (cuuint32_t)p.x_box_rows};
+    if (enc(&xm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p.x), xdims, xstrides, xbox,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    QmmParams q = p;
+    q.wait_budget = wait_budget_cycles();
+    switch (q.group) {
+        case 32: return launch_kn_group<32>(q, bits, gather, grid_m, max_rows_per_tile, cm, xm, stream);
+        case 64: return launch_kn_group<64>(q, bits, gather, grid_m, max_rows_per_tile, cm, xm, stream);
+        case 128: return launch_kn_group<128>(q, bits, gather, grid_m, max_rows_per_tile, cm, xm, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace mxq

@@ -109,6 +109,25 @@ mxq_status mxq_qmv_kn(const void* x, const uint32_t* w, const void* scales, cons
                       void* y, int K, int N, int bits, int group_size, int32_t* dev_status,
                       void* stream);
 
+/* Prefill GEMM for the [K, N] operand layout (mlxcel PR #1562, What
+ * changed: both operand layouts), w, scales and biases as for mxq_qmv_kn:
+ *   y[m, n] = sum_k x[m, k] * (s[k, n/G] * q[k, n] + b[k, n/G])
+ *   x: bf16 [M, K]; y: bf16 [M, N].
+ * M = 1 runs mxq_qmv_kn (the same operation).  Otherwise the tcgen05 tensor
+ * cores: each code word dequantises (one bf16 rounding of s*q + b, as in
+ * mxq_qmm) into 8 bf16 contiguous along n, stored as the MMA's MN-major A
+ * operand in shared memory; fp32 accumulation in tensor memory.  With fewer
+ * tiles than SMs, K is split over up to 8 CTAs of a cluster and the fp32
+ * partials are added in a fixed order: deterministic.
+ * Requirements: bits in {2, 4, 8} (3 and 6: MXQ_ERR_UNSUPPORTED);
+ * group_size in {32, 64, 128}; M > 0; K > 0 (K % 8 == 0 when M > 1); N > 0,
+ * N % 64 == 0, N % group_size == 0; x, w, y 16-byte aligned; scales,
+ * biases 2-byte aligned.  `dev_status` (device int32, may be NULL) receives
+ * 0 or MXQ_DEV_TIMEOUT.                                                     */
+mxq_status mxq_qmm_kn(const void* x, const uint32_t* w, const void* scales, const void* biases,
+                      void* y, int M, int K, int N, int bits, int group_size,
+                      int32_t* dev_status, void* stream);
+
 /* Prefill GEMM, y[M, N] = x[M, K] . w^[N, K]^T (mlxcel issue #1536, Baseline
  * profile table and Diagnosis item 4: the qmm_naive kernel).  M = 1 runs the
  * streaming GEMV of mxq_qmv (the same operation).  Otherwise the tcgen05
@@ -159,6 +178,26 @@ mxq_status mxq_gather_qmm(const void* x, const uint32_t* w, const void* scales,
                           const int32_t* row_src, void* y, int T, int B, int E, int K, int N,
                           int bits, int group_size, void* workspace, size_t workspace_bytes,
                           int32_t* dev_status, void* stream);
+
+/* The sorted mixture-of-experts grouped GEMM for the [K, N] operand layout
+ * (mlxcel PR #1562, What changed: the grouped GEMM is checked against the
+ * dense per-expert reference in both operand layouts):
+ *   w:      uint32 [E, K, N*bits/32]; scales, biases: bf16 [E, K, N/G]
+ *   y[r, n] = sum_k x[src(r), k] * (s_e[k, n/G] * q_e[k, n] + b_e[k, n/G]),
+ *             e = expert_ids[r]
+ * Every other argument, the workspace (mxq_gather_workspace_bytes) and the
+ * handling of invalid ids and rows are as for mxq_gather_qmm.  The call
+ * builds the tile table on the GPU (tiles of at most 64 sorted rows of one
+ * expert), copies routed rows into sorted order, and runs one CTA per (tile,
+ * 128 columns) on the tensor cores, at every B.
+ * Requirements: B, E, T > 0; bits in {2, 4, 8} (3 and 6:
+ * MXQ_ERR_UNSUPPORTED); group_size in {32, 64, 128}; K > 0, K % 8 == 0;
+ * N > 0, N % 64 == 0, N % group_size == 0; alignment as for mxq_gather_qmm. */
+mxq_status mxq_gather_qmm_kn(const void* x, const uint32_t* w, const void* scales,
+                             const void* biases, const int32_t* expert_ids,
+                             const int32_t* row_src, void* y, int T, int B, int E, int K, int N,
+                             int bits, int group_size, void* workspace, size_t workspace_bytes,
+                             int32_t* dev_status, void* stream);
 
 /* Workspace bytes mxq_gather_qmm (and mxq_gather_qmm_gateup) needs for B
  * rows over E experts with K-wide activation rows routed through row_src

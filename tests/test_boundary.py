@@ -30,8 +30,10 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("mxq_qmv", "mxq_qmm", "mxq_qmv_kn", "mxq_gather_qmm", "mxq_gather_workspace_bytes",
-              "mxq_gather_qmm_noalloc", "mxq_quantize", "mxq_status_string", "mxq_version"):
+    for n in ("mxq_qmv", "mxq_qmm", "mxq_qmv_kn", "mxq_qmm_kn", "mxq_gather_qmm",
+              "mxq_gather_qmm_kn", "mxq_gather_qmm_gateup", "mxq_gather_workspace_bytes",
+              "mxq_gather_qmm_noalloc", "mxq_quantize", "mxq_status_string", "mxq_version",
+              "mxq_debug_set_wait_budget"):
         assert n in names
 
 
@@ -84,6 +86,47 @@ def qmv_kn(L, K=100, N=128, bits=4, group=64, x=FAKE, w=FAKE, y=FAKE, status=Non
 ])
 def test_qmv_kn_argument_checks(L, kw, code):
     assert qmv_kn(L, **kw) == code
+
+
+def qmm_kn(L, M=16, K=200, N=128, bits=4, group=64, x=FAKE, w=FAKE, y=FAKE, status=None):
+    return L.mxq_qmm_kn(x, w, FAKE, FAKE, y, M, K, N, bits, group, status, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(bits=3), 3), (dict(bits=6), 3), (dict(bits=5), 1), (dict(group=16), 1),
+    (dict(N=96), 1), (dict(N=0), 1), (dict(K=0), 1), (dict(M=0), 1), (dict(K=100), 1),
+    (dict(N=64, group=128), 1), (dict(x=None), 1), (dict(w=None), 1), (dict(y=FAKE_ODD), 2),
+    (dict(w=FAKE_ODD), 2), (dict(x=FAKE_ODD), 2), (dict(status=ctypes.c_void_p(0x10002)), 2),
+])
+def test_qmm_kn_argument_checks(L, kw, code):
+    assert qmm_kn(L, **kw) == code
+
+
+def test_qmm_kn_single_row_takes_any_k(L):
+    # M = 1 is the [K, N] GEMV, which takes any K > 0: the host checks pass
+    # and only the device check remains
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; covered by the GPU tests")
+    assert qmm_kn(L, M=1, K=100) in (4, 5)
+
+
+def gather_kn(L, T=8, B=8, E=2, K=128, N=64, bits=4, group=64, ids=FAKE, src=FAKE, ws=FAKE,
+              wsb=1 << 24):
+    return L.mxq_gather_qmm_kn(FAKE, FAKE, FAKE, FAKE, ids, src, FAKE, T, B, E, K, N, bits, group,
+                               ws, wsb, None, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(bits=3), 3), (dict(bits=6), 3), (dict(bits=7), 1), (dict(T=0), 1), (dict(B=0), 1),
+    (dict(E=0), 1), (dict(K=100), 1), (dict(N=96), 1), (dict(N=64, group=128), 1),
+    (dict(ids=None), 1), (dict(src=None, T=5, B=8), 1),
+    (dict(ids=ctypes.c_void_p(0x10002)), 2), (dict(ws=ctypes.c_void_p(0x10080)), 2),
+    (dict(ws=None), 6), (dict(wsb=16), 6),
+])
+def test_gather_kn_argument_checks(L, kw, code):
+    assert gather_kn(L, **kw) == code
 
 
 def qmm(L, M=16, K=128, N=64, bits=4, group=64, status=None, x=FAKE, y=FAKE):

@@ -137,3 +137,20 @@ def test_gateup_grouped_timeout_then_parity(short_budget):
         yr, bnd = oracle.gather_qmm(c.x, w, s, b, c.ids, c.src, c.T, c.B, c.E, c.K, c.N, 4)
         assert_close(to_f64(y1[:, part * c.N:(part + 1) * c.N]), yr, bnd,
                      "gate/up set %d after a timeout" % part)
+
+
+@pytest.mark.parametrize("M,K,N", [(16, 2048, 2048), (300, 512, 4096)])
+def test_qmm_kn_timeout_then_parity(short_budget, M, K, N):
+    # the [K, N]-layout GEMM: with a K split over a cluster, and without
+    import synth
+    from tests.gpu_util import bf16_dev, codes_dev
+
+    mxq = _mxq()
+    qw = synth.quantize(synth.dense_weights(K, N, seed=M), 4, 64)
+    x = synth.activations(M, K, seed=M + 1)
+    w_d, s_d, b_d, x_d = codes_dev(qw.w), bf16_dev(qw.scales), bf16_dev(qw.biases), bf16_dev(x)
+    _, y1, code = _timed_out_then_normal(
+        lambda st: mxq.qmm_kn(x_d, w_d, s_d, b_d, 4, dev_status=st), short_budget)
+    assert code == mxq.DEV_TIMEOUT
+    yr, bnd = oracle.qmm_kn(x, qw.w, qw.scales, qw.biases, M, K, N, 4)
+    assert_close(to_f64(y1), yr, bnd, "qmm_kn after a timeout")
