@@ -701,23 +701,6 @@ __device__ __forceinline__ PTile ptile(const QmmParams& p, int t, int m_tiles, i
     return r;
 }
 
-// try_wait that lets the thread sleep in hardware until the phase completes
-// (or the hint, in ns, runs out), so waiting warps take no issue slots from
-// the warps doing the work.
-constexpr uint32_t kSuspendNs = 20000;
-
-__device__ __forceinline__ bool mbar_try_wait_s(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
-        : "memory");
-    return ok != 0;
-}
-
 // Bounded wait that also gives up as soon as another role has given up.  The
 // first poll does not suspend, and the abort flag and the budget are checked
 // before every suspending one, so a budget shorter than one poll gives up at

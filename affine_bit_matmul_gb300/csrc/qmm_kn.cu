@@ -42,12 +42,15 @@
 namespace mxq {
 namespace {
 
-constexpr int kDequantWarps = 8;     // warps 0-7: dequant, then epilogue
+constexpr int kDequantWarps = 16;    // warps 0-15: dequant, then epilogue
 constexpr int kDequantThreads = kDequantWarps * 32;
-constexpr int kCodeWarp = 8;         // codes TMA
-constexpr int kMmaWarp = 9;          // TMEM owner, MMA issue
-constexpr int kXWarp = 10;           // activation TMA
-constexpr int kThreads = 11 * 32;
+constexpr int kGroups = 2;                       // dequant groups taking stages in turn
+constexpr int kGroupWarps = kDequantWarps / kGroups;
+constexpr int kGroupThreads = kGroupWarps * 32;
+constexpr int kCodeWarp = 16;        // codes TMA
+constexpr int kMmaWarp = 17;         // TMEM owner, MMA issue
+constexpr int kXWarp = 18;           // activation TMA
+constexpr int kThreads = 19 * 32;
 constexpr int kTileN = 128;          // output columns per CTA (MMA M)
 constexpr int kBK = 64;              // k per stage (one activation swizzle atom)
 constexpr int kAStageBytes = kTileN * kBK * 2;  // 16 KB of bf16, MN-major
@@ -182,10 +185,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < SC; ++i) {
             mbar_init(&cfull[i], 1);
-            mbar_init(&cempty[i], kDequantWarps);
+            mbar_init(&cempty[i], kGroupWarps);
         }
         for (int i = 0; i < kAStages; ++i) {
-            mbar_init(&afull[i], kDequantWarps);
+            mbar_init(&afull[i], kGroupWarps);
             mbar_init(&aempty[i], 1);
         }
         for (int i = 0; i < SX; ++i) {
@@ -213,7 +216,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         Ring ring(SC);
         int q = 0;
         for (; q < nkb; ++q, ring.next()) {
-            if (q >= SC && !warp_wait(&cempty[ring.slot], ring.parity ^ 1, p.wait_budget)) {
+            if (q >= SC &&
+                !warp_wait_sleep(&cempty[ring.slot], ring.parity ^ 1, p.wait_budget)) {
                 ok = false;
                 break;
             }
@@ -238,7 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         Ring ring(SX);
         int q = 0;
         for (; q < nkb; ++q, ring.next()) {
-            if (q >= SX && !warp_wait(&xempty[ring.slot], ring.parity ^ 1, p.wait_budget)) {
+            if (q >= SX &&
+                !warp_wait_sleep(&xempty[ring.slot], ring.parity ^ 1, p.wait_budget)) {
                 ok = false;
                 break;
             }
@@ -256,23 +261,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issue
         const uint32_t idesc = umma_idesc_bf16(kTileN, (uint32_t)n_mma) | (1u << 15);  // A MN-major
+        // two stages per round: the MMAs of one round keep the tensor pipe
+        // busy while the warp waits for the next round's operands
         Ring ar(kAStages), xr(SX);
-        for (int q = 0; q < nkb; ++q, ar.next(), xr.next()) {
-            if (!warp_wait(&afull[ar.slot], ar.parity, p.wait_budget) ||
-                !warp_wait(&xfull[xr.slot], xr.parity, p.wait_budget)) {
+        for (int q = 0; q < nkb; q += 2) {
+            const bool two = q + 1 < nkb;
+            const int a0 = ar.slot, x0 = xr.slot;
+            const uint32_t pa0 = ar.parity, px0 = xr.parity;
+            ar.next();
+            xr.next();
+            const int a1 = ar.slot, x1 = xr.slot;
+            const uint32_t pa1 = ar.parity, px1 = xr.parity;
+            if (two) {
+                ar.next();
+                xr.next();
+            }
+            if (!warp_wait_sleep(&afull[a0], pa0, p.wait_budget) ||
+                !warp_wait_sleep(&xfull[x0], px0, p.wait_budget) ||
+                (two && (!warp_wait_sleep(&afull[a1], pa1, p.wait_budget) ||
+                         !warp_wait_sleep(&xfull[x1], px1, p.wait_budget)))) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             if (elect_one()) {
-                const uint32_t a_stage = a_base0 + ar.slot * kAStageBytes;
-                const uint64_t bd = umma_desc_sw128(x_base0 + xr.slot * L.x_bytes);
 #pragma unroll
-                for (int j = 0; j < kBK / 16; ++j)  // 16 k = two 8-row atoms of A, 32 B of B
-                    umma_bf16(tmem, umma_desc_mn_sw128(a_stage + j * 2 * kAtomK), bd + 2 * j,
-                              idesc, (q > 0 || j > 0) ? 1u : 0u);
-                umma_commit(&aempty[ar.slot]);
-                umma_commit(&xempty[xr.slot]);
+                for (int h = 0; h < 2; ++h) {
+                    if (h == 1 && !two) break;
+                    const uint32_t a_stage = a_base0 + (h ? a1 : a0) * kAStageBytes;
+                    const uint64_t bd = umma_desc_sw128(x_base0 + (h ? x1 : x0) * L.x_bytes);
+#pragma unroll
+                    for (int j = 0; j < kBK / 16; ++j)  // 16 k = two 8-row atoms of A, 32 B of B
+                        umma_bf16(tmem, umma_desc_mn_sw128(a_stage + j * 2 * kAtomK), bd + 2 * j,
+                                  idesc, (q > 0 || h > 0 || j > 0) ? 1u : 0u);
+                }
+                umma_commit(&aempty[a0]);
+                umma_commit(&xempty[x0]);
+                if (two) {
+                    umma_commit(&aempty[a1]);
+                    umma_commit(&xempty[x1]);
+                }
             }
             __syncwarp();
         }
@@ -280,71 +308,97 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp < kDequantWarps) {
         // ---------------------------------------------------------------- dequant
-        // a stage's codes are 64 rows of W words; thread t takes words
-        // t, t + 256, ...: word i is row i / W, columns [(i % W) * 32 / BITS, ...)
+        // kGroups groups of warps take the stages in turn (group g: stages g,
+        // g + kGroups, ...), so several stages are dequantised at once and
+        // each warp has kGroups stage times for one stage.  A stage's codes are 64 rows of
+        // W words; thread t of a group takes words t, t + 256, ...: word i is
+        // row i / W, columns [(i % W) * 32 / BITS, ...).  A thread's words
+        // share their columns (so their group of n) and lie kRowStep rows
+        // apart.
         constexpr int W = kTileN * BITS / 32;                // words per code row
-        constexpr int kWords = kBK * W / kDequantThreads;    // words per thread: 2, 4, 8
-        constexpr int kRowStep = kDequantThreads / W;        // rows between a thread's words
+        constexpr int kWords = kBK * W / kGroupThreads;      // words per thread: 2, 4, 8
+        constexpr int kRowStep = kGroupThreads / W;          // rows between a thread's words
         constexpr int kPerWord = 32 / BITS;                  // columns per word
-        const int t = threadIdx.x;
-        const int wc = t % W;                   // word column: the same for all of the thread's words
+        const int grp = warp / kGroupWarps;
+        const int t = threadIdx.x % kGroupThreads;
+        const int wc = t % W;                   // word column
         const int r0 = t / W;                   // first row
         const int nl = wc * kPerWord;           // first column of the word, within the tile
         const bool col_ok = n0 + nl < p.N;      // columns past N: zero codes, no scale read
         const int groups = p.N / GROUP;         // scale/bias entries per row of k
-        const long long sb_e = (long long)e * p.sb_expert_stride;
-        const uint16_t* srow = p.scales + sb_e + (n0 + nl) / GROUP;
-        const uint16_t* brow = p.biases + sb_e + (n0 + nl) / GROUP;
-        // this stage's scale/bias pairs, loaded a stage ahead
-        uint32_t sv[kWords], bv[kWords], sn[kWords], bn[kWords];
-        auto sb_load = [&](int q, uint32_t (&s)[kWords], uint32_t (&b)[kWords]) {
+        // scale and bias of row r0 of the CTA's first block; a stage moves
+        // them kBK rows on, word j kRowStep rows further
+        const long long sb0 = (long long)e * p.sb_expert_stride +
+                              ((long long)kb_begin * kBK + r0) * groups + (n0 + nl) / GROUP;
+        const uint16_t* sp = p.scales + sb0;
+        const uint16_t* bp = p.biases + sb0;
+        const long long stage_step = (long long)kBK * groups;
+        const int k_left0 = p.K - kb_begin * kBK - r0;  // rows of k left from row r0 of block 0
+        const uint32_t c_off = (uint32_t)((r0 * W + wc) * 4);
+        const uint32_t a_off = a_chunk(r0, nl >> 3) + (BITS == 8 ? (uint32_t)((nl & 7) * 2) : 0u);
+        const long long j_step = (long long)kRowStep * groups;
+        // scale/bias pairs of stage q, loaded two of the group's stages
+        // (2 * kGroups stage times) before their use
+        auto sb_load = [&](int q, uint32_t (&sl)[kWords], uint32_t (&bl)[kWords]) {
+            const long long at = (long long)q * stage_step;
+            const int left = k_left0 - q * kBK;
 #pragma unroll
             for (int j = 0; j < kWords; ++j) {
-                s[j] = 0u;
-                b[j] = 0u;
-                const long long kr = (long long)(kb_begin + q) * kBK + r0 + j * kRowStep;
-                if (col_ok && q < nkb && kr < p.K) {
-                    s[j] = __ldg(srow + kr * groups);
-                    b[j] = __ldg(brow + kr * groups);
+                sl[j] = 0u;
+                bl[j] = 0u;
+                if (col_ok && q < nkb && j * kRowStep < left) {
+                    sl[j] = __ldg(sp + at + j * j_step);
+                    bl[j] = __ldg(bp + at + j * j_step);
                 }
             }
         };
-        sb_load(0, sv, bv);
         Ring cr(SC), ar(kAStages);
-        for (int q = 0; q < nkb; ++q, cr.next(), ar.next()) {
-            sb_load(q + 1, sn, bn);
-            if (!warp_wait(&cfull[cr.slot], cr.parity, p.wait_budget)) {
-                ok = false;
-                break;
-            }
-            const uint32_t c_slot = c_base0 + cr.slot * L.c_bytes;
+        for (int i = 0; i < grp; ++i) {
+            cr.next();
+            ar.next();
+        }
+        // stage q with its scale/bias pairs in (sc, bc); loads the pairs of
+        // stage q + 2 * kGroups into (sn, bn)
+        auto stage = [&](int q, const uint32_t (&sc)[kWords], const uint32_t (&bc)[kWords],
+                         uint32_t (&sn)[kWords], uint32_t (&bn)[kWords]) -> bool {
+            sb_load(q + 2 * kGroups, sn, bn);
+            if (!warp_wait_sleep(&cfull[cr.slot], cr.parity, p.wait_budget)) return false;
+            const uint32_t c_word = c_base0 + cr.slot * L.c_bytes + c_off;
             uint32_t wd[kWords];
 #pragma unroll
-            for (int j = 0; j < kWords; ++j)
-                wd[j] = ld_shared_u32(c_slot + (uint32_t)(((r0 + j * kRowStep) * W + wc) * 4));
-            if (q >= kAStages && !warp_wait(&aempty[ar.slot], ar.parity ^ 1, p.wait_budget)) {
-                ok = false;
-                break;
-            }
+            for (int j = 0; j < kWords; ++j) wd[j] = ld_shared_u32(c_word + j * kRowStep * W * 4);
+            if (q >= kAStages &&
+                !warp_wait_sleep(&aempty[ar.slot], ar.parity ^ 1, p.wait_budget))
+                return false;
             const uint32_t a_stage = a_base0 + ar.slot * kAStageBytes;
 #pragma unroll
             for (int j = 0; j < kWords; ++j) {
-                const int k = r0 + j * kRowStep;
+                // with kRowStep a multiple of 8 every word sits at the same row
+                // of its 8-row atom, one atom stride per kRowStep / 8
+                const uint32_t dst =
+                    kRowStep % 8 == 0
+                        ? a_stage + a_off + j * (kRowStep / 8) * kAtomK
+                        : a_stage + a_chunk(r0 + j * kRowStep, nl >> 3) +
+                              (BITS == 8 ? (uint32_t)((nl & 7) * 2) : 0u);
                 if (BITS == 8) {
                     uint32_t o[2];
-                    dequant_word8(wd[j], bf16_bits_to_float(sv[j]), bf16_bits_to_float(bv[j]), o);
-                    // four columns: half of a 16-byte chunk
-                    st_shared_v2(a_stage + a_chunk(k, nl >> 3) + (uint32_t)((nl & 7) * 2), o[0],
-                                 o[1]);
-                } else if (BITS == 4) {
-                    uint32_t o[4];
-                    dequant_word4(wd[j], sv[j] | (sv[j] << 16), bv[j] | (bv[j] << 16), o);
-                    st_shared_v4(a_stage + a_chunk(k, nl >> 3), o[0], o[1], o[2], o[3]);
+                    dequant_word8(wd[j], bf16_bits_to_float(sc[j]), bf16_bits_to_float(bc[j]), o);
+                    st_shared_v2(dst, o[0], o[1]);  // four columns: half of a 16-byte chunk
                 } else {
-                    uint32_t o[8];
-                    dequant_word2(wd[j], sv[j] | (sv[j] << 16), bv[j] | (bv[j] << 16), o);
-                    st_shared_v4(a_stage + a_chunk(k, nl >> 3), o[0], o[1], o[2], o[3]);
-                    st_shared_v4(a_stage + a_chunk(k, (nl >> 3) + 1), o[4], o[5], o[6], o[7]);
+                    // both halves of a bf16x2 take the word's scale and bias
+                    const uint32_t sw = prmt(sc[j], 0u, 0x1010u), bw = prmt(bc[j], 0u, 0x1010u);
+                    if (BITS == 4) {
+                        uint32_t o[4];
+                        dequant_word4(wd[j], sw, bw, o);
+                        st_shared_v4(dst, o[0], o[1], o[2], o[3]);
+                    } else {
+                        uint32_t o[8];
+                        dequant_word2(wd[j], sw, bw, o);
+                        st_shared_v4(dst, o[0], o[1], o[2], o[3]);
+                        // the word's next 8 columns
+                        st_shared_v4(a_stage + a_chunk(r0 + j * kRowStep, (nl >> 3) + 1), o[4],
+                                     o[5], o[6], o[7]);
+                    }
                 }
             }
             // the tensor cores read the stage through the async proxy; the
@@ -356,24 +410,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(&afull[ar.slot]);
             }
 #pragma unroll
-            for (int j = 0; j < kWords; ++j) {
-                sv[j] = sn[j];
-                bv[j] = bn[j];
+            for (int i = 0; i < kGroups; ++i) {
+                cr.next();
+                ar.next();
             }
+            return true;
+        };
+        // three register sets in turn (the loop is unrolled by three), so
+        // no pair is ever copied
+        uint32_t sA[kWords], bA[kWords], sB[kWords], bB[kWords], sC[kWords], bC[kWords];
+        sb_load(grp, sA, bA);
+        sb_load(grp + kGroups, sB, bB);
+        for (int q = grp; q < nkb && ok; q += 3 * kGroups) {
+            ok = stage(q, sA, bA, sC, bC);
+            if (!ok || q + kGroups >= nkb) break;
+            ok = stage(q + kGroups, sB, bB, sA, bA);
+            if (!ok || q + 2 * kGroups >= nkb) break;
+            ok = stage(q + 2 * kGroups, sC, bC, sB, bB);
         }
 
         // ---------------------------------------------------------------- epilogue
-        if (ok && !mbar_wait(accf, 0, p.wait_budget)) ok = false;
+        if (ok && !mbar_wait_sleep(accf, 0, p.wait_budget)) ok = false;
         tc_fence_after();
         const int quarter = warp & 3;     // tensor-memory lanes 32*quarter ...
-        const int colhalf = warp >> 2;    // 16-column chunks of this parity
+        const int colq = warp >> 2;       // every fourth 16-column chunk from colq
         const int lane_row = quarter * 32 + lane;
         const int ny = n0 + lane_row;
         const bool y_ok = ny < p.N;
         const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
         __nv_bfloat16* y = static_cast<__nv_bfloat16*>(p.y);
         if (p.splits == 1) {
-            for (int c0 = colhalf * 16; c0 < n_mma; c0 += 32) {
+            for (int c0 = colq * 16; c0 < n_mma; c0 += 16 * (kDequantWarps / 4)) {
                 uint32_t v[16];
                 tmem_ld16(taddr + c0, v);
                 tmem_ld_wait();
@@ -391,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // K split: each CTA writes its fp32 partial tile [m][128] into its
             // own shared memory (every stage has been consumed by the MMAs)
             const uint32_t part = smem_base;
-            for (int c0 = colhalf * 16; c0 < n_mma; c0 += 32) {
+            for (int c0 = colq * 16; c0 < n_mma; c0 += 16 * (kDequantWarps / 4)) {
                 uint32_t v[16];
                 tmem_ld16(taddr + c0, v);
                 tmem_ld_wait();

@@ -230,6 +230,40 @@ __device__ __forceinline__ bool warp_wait3(uint64_t* a, uint32_t pa, uint64_t* b
 }
 
 
+// try_wait that lets the thread sleep in hardware until the phase completes
+// (or the hint, in ns, runs out), so waiting warps take no issue slots from
+// the warps doing the work.
+constexpr uint32_t kSuspendNs = 20000;
+
+__device__ __forceinline__ bool mbar_try_wait_s(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait that sleeps: the first poll does not suspend, then the
+// budget is checked before every suspending poll, so a budget shorter than
+// one poll gives up at the first wait that is not already satisfied.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, long long budget) {
+    if (mbar_test_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    do {
+        if (clock64() - t0 > budget) return false;
+    } while (!mbar_try_wait_s(bar, parity, kSuspendNs));
+    return true;
+}
+
+__device__ __forceinline__ bool warp_wait_sleep(uint64_t* bar, uint32_t parity, long long budget) {
+    const bool ok = mbar_wait_sleep(bar, parity, budget);
+    return __all_sync(0xffffffffu, ok);
+}
+
 __device__ __forceinline__ void flag_status(int32_t* status, int bits) {
     if (status) atomicOr(status, bits);
 }
