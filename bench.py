@@ -569,6 +569,52 @@ def secondary_measurements(mxq, dev, stream, hbm, bf16_peak, Ws, clocks):
         del kn_copies, Wkn, qkn
     torch.cuda.empty_cache()
 
+    # ---- the [K, N]-layout tensor-core GEMMs: the prefill shape and both
+    # expert shapes of the sorted-MoE workload (weights quantised along n
+    # by the library's encoder: a [K, N] matrix quantised row by row)
+    for bits in (4, 8):
+        K, N, M = 5120, 17408, 600
+        Wd = torch.randn((K, N), device=dev) * 0.02
+        knc = [mxq.quantize(Wd, bits)]
+        knc += [tuple(t.clone() for t in knc[0]) for _ in range(2)]
+        del Wd
+        xk = dev_bf16(synth.activations(M, K, seed=1), dev)
+        yk = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        fnk = lambda i: mxq.qmm_kn(xk, *knc[i % 3], bits, out=yk)  # noqa: E731
+        for i in range(5):
+            fnk(i)
+        m0 = clocks.mark()
+        tk, _ = time_launches(fnk, iters, stream)
+        out.append(entry("qmm_kn M=%d K=%d N=%d b%d g64" % (M, K, N, bits), tk,
+                         qmm_bytes(M, K, N, bits), 2.0 * M * K * N, m0))
+        del knc, xk, yk
+    for K, N, ident in ((2816, 704, False), (704, 2816, True)):
+        E, T, top_k, bits = 128, 573, 8, 4
+        ids, src = synth.routing(T, E, top_k, seed=2)
+        B = ids.shape[0]
+        We = torch.randn((E * K, N), device=dev) * 0.02
+        c0, s0, b0 = mxq.quantize(We, bits)
+        del We
+        knc = [(c0.view(E, K, -1), s0.view(E, K, -1), b0.view(E, K, -1))]
+        knc.append(tuple(t.clone() for t in knc[0]))
+        Tx = B if ident else T
+        xg = dev_bf16(synth.activations(Tx, K, seed=1), dev)
+        ids_d = torch.from_numpy(ids).to(dev)
+        src_d = None if ident else torch.from_numpy(src).to(dev)
+        yg = torch.empty((B, N), dtype=torch.bfloat16, device=dev)
+        wsk = torch.empty((mxq.gather_workspace_bytes(B, E, K, N),), dtype=torch.uint8, device=dev)
+        fng = lambda i: mxq.gather_qmm_kn(xg, *knc[i % 2], ids_d, src_d, bits,  # noqa: E731
+                                          out=yg, workspace=wsk)
+        for i in range(5):
+            fng(i)
+        m0 = clocks.mark()
+        tg, _ = time_launches(fng, iters, stream)
+        nbg = E * (K * N * bits // 8 + K * (N // 64) * 4) + Tx * K * 2 + B * N * 2
+        out.append(entry("gather_qmm_kn E=128 top8 T=573 B=%d K=%d N=%d b4 g64" % (B, K, N), tg,
+                         nbg, 2.0 * B * K * N, m0))
+        del knc, c0, s0, b0, xg, yg, wsk
+    torch.cuda.empty_cache()
+
     # ---- the encoder on the prefill weight shape (float32 in, 4-bit codes out)
     N_q, K_q = 17408, 5120
     Wq = [torch.randn((N_q, K_q), device=dev) * 0.02 for _ in range(2)]
@@ -778,6 +824,14 @@ def run_profile(args):
         d = DenseInputs(synth.dense_weights(N, K, seed=0), 1, K, N, bits, dev, copies=2)
         for i in range(launches):
             mxq.qmv(d.x[0], *d.copies[i % 2], bits, out=d.y[0])
+    elif name == "qmm_kn":
+        # the [K, N]-layout prefill GEMM: weights quantised along n by the
+        # library's encoder
+        M, K, N, bits = 600, 5120, 17408, 4
+        c = mxq.quantize(torch.randn((K, N), device=dev) * 0.02, bits)
+        x = dev_bf16(synth.activations(M, K, seed=1), dev)
+        for i in range(launches):
+            mxq.qmm_kn(x, *c, bits)
     elif name.startswith("qmm"):
         M, K, N, bits = {"qmm": (600, 5120, 17408, 4), "qmm600": (600, 5120, 5120, 4),
                          "qmm128": (128, 5120, 5120, 4), "qmm8": (8, 5120, 5120, 4),
