@@ -15,9 +15,14 @@ constexpr int kTileN = 128;           // rows of w per CTA in the tensor-core ke
 constexpr int kMaxRowsPerTile = 256;  // MMA N limit
 constexpr int kGatherRowsPerTile = 64;  // expert segments average ~36 rows
 constexpr int kMinKBlocksPerSplit = 8;
-// Grouped calls with at most this many rows (a decode step: a few tokens x
-// top_k) run one HBM-bound GEMV per row instead of the tensor-core GEMM.
+// Grouped calls with at most one row per SM, and at most kGatherStreamWaves
+// rows x weight sets per SM (a decode step: a few tokens x top_k), stream
+// each row's expert matrix through the streaming GEMV; where the shape does
+// not fit that kernel, calls with at most kGatherDecodeRows rows run one
+// direct-load GEMV per row.  Larger calls run the tensor-core GEMM, which
+// reads each expert once for all of its rows.
 constexpr int kGatherDecodeRows = 32;
+constexpr int kGatherStreamWaves = 2;
 constexpr int kMaxSplits = 8;             // portable cluster size
 constexpr int kMaxDevices = 64;
 
@@ -375,15 +380,23 @@ mxq_status gather_call(const void* x, const uint32_t* w, const void* scales, con
     if (st != MXQ_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int sets = pair ? 2 : 1;
-    if (B <= kGatherDecodeRows) {
+    const bool stream_rows = B <= sms && (long long)B * sets <= (long long)kGatherStreamWaves * sms;
+    if (stream_rows || B <= kGatherDecodeRows) {
         // a decode step: one GEMV per sorted row (and weight set) against its
         // expert's matrix, no tile table
         if (dev_status && cudaMemsetAsync(dev_status, 0, sizeof(int32_t), s) != cudaSuccess)
             return MXQ_ERR_CUDA;
-        cudaError_t err = mxq::launch_gather_qmv(x, w, scales, biases, w1, scales1, biases1,
-                                                 expert_ids, row_src, y, y1, sets, T, B, E, K, N,
-                                                 bits, group_size, dev_status, s);
-        return err == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA;
+        cudaError_t err = cudaErrorNotSupported;
+        if (stream_rows)
+            err = mxq::launch_gather_qmv(x, w, scales, biases, w1, scales1, biases1, expert_ids,
+                                         row_src, y, y1, sets, T, B, E, K, N, bits, group_size,
+                                         sms, true, dev_status, s);
+        if (err == cudaErrorNotSupported && B <= kGatherDecodeRows)
+            err = mxq::launch_gather_qmv(x, w, scales, biases, w1, scales1, biases1, expert_ids,
+                                         row_src, y, y1, sets, T, B, E, K, N, bits, group_size,
+                                         sms, false, dev_status, s);
+        if (err != cudaErrorNotSupported) return err == cudaSuccess ? MXQ_OK : MXQ_ERR_CUDA;
+        // neither GEMV form fits: the tensor-core GEMM below
     }
     auto* tiles = static_cast<mxq::MTile*>(workspace);
     int* tile_count = reinterpret_cast<int*>(static_cast<char*>(workspace) +

@@ -111,12 +111,15 @@ cudaError_t launch_gather_prepass(const int32_t* expert_ids, const int32_t* row_
 // Grouped form with few rows (decode): one GEMV per sorted row (and weight
 // set: sets = 2 adds w1, scales1, biases1 -> y1) against its expert's
 // matrix, validating the ids itself (no tile table, no row copy).
+// stream_form: the streaming GEMV with one grid row per sorted row and set
+// (cudaErrorNotSupported when the shape does not fit it); otherwise the
+// direct-load GEMV, grid (N / 16, B, sets).
 cudaError_t launch_gather_qmv(const void* x, const uint32_t* w, const void* scales,
                               const void* biases, const uint32_t* w1, const void* scales1,
                               const void* biases1, const int32_t* expert_ids,
                               const int32_t* row_src, void* y, void* y1, int sets, int T, int B,
-                              int E, int K, int N, int bits, int group, int32_t* status,
-                              cudaStream_t stream);
+                              int E, int K, int N, int bits, int group, int sms,
+                              bool stream_form, int32_t* status, cudaStream_t stream);
 
 // Affine group-wise encoder (groups of 32, 64 or 128): float [N, K] ->
 // codes, bf16 scales and biases.

@@ -454,19 +454,45 @@ struct StreamShape {
     int stage_bytes; // codes + scales + biases, 16-byte aligned pieces
     int x_offset;    // shared-memory offset of the activation copy (after the ring)
     int nchunks;     // chunks over all of N: at most `rows` rows each, a multiple of the grid
+    int quantum;     // chunk boundaries fall on multiples of this many rows, so every
+                     // chunk's scales and biases are whole 16-byte units
     long long wait_budget;  // pipeline-wait budget in SM cycles
 };
 
-// The first `rem` chunks of the launch have q + 1 rows, the others q rows
-// (q = N / nchunks): nchunks is a multiple of the grid, so every CTA streams
-// the same number of chunks of (within one row) the same size.  CTA b takes
+// The grouped (segment) form: grid row y is sorted row r = blockIdx.y, the
+// GEMV of expert ids[r]'s matrix with activation row row_src[r]; grid z
+// selects the weight set of the gate/up pair (set 1: w1, s1, b1 -> y1).
+struct StreamSeg {
+    const int32_t* ids;
+    const int32_t* row_src;  // null: row r
+    const uint32_t* w1;
+    const uint16_t* s1;
+    const uint16_t* b1;
+    __nv_bfloat16* y1;
+    int T, B, E;
+    long long w_expert_stride;   // words between experts
+    long long sb_expert_stride;  // scale/bias entries between experts
+};
+
+// Rows go in units of `qu` rows (the shape's quantum); the first `rem` chunks
+// of the launch have q + 1 units, the others q units (q = units / nchunks):
+// nchunks is a multiple of the grid, so every CTA streams the same number of
+// chunks of (within one unit) the same size.  CTA b takes
 // chunks b, b + grid, ...:
 // at any time the CTAs stream one contiguous window of the weights, which
 // keeps all DRAM channels evenly loaded (a contiguous share per CTA instead
 // spreads 152 streams at a fixed stride and runs markedly slower).
+// QUANT = false: a quantum of one row (the arithmetic is then in rows).
+template <bool QUANT>
 struct ChunkRows {
-    int q, rem;
-    __device__ int begin(int chunk) const { return chunk * q + min(chunk, rem); }
+    int q, rem, qu;
+    __device__ ChunkRows(int N, const StreamShape& sh)
+        : q(QUANT ? N / sh.quantum / sh.nchunks : N / sh.nchunks),
+          rem(QUANT ? N / sh.quantum % sh.nchunks : N % sh.nchunks),
+          qu(QUANT ? sh.quantum : 1) {}
+    __device__ int begin(int chunk) const {
+        return QUANT ? (chunk * q + min(chunk, rem)) * qu : chunk * q + min(chunk, rem);
+    }
 };
 
 // ---- exact integer dot products (streaming form)
@@ -590,14 +616,55 @@ __device__ __forceinline__ float lane_dot_int(uint32_t codes_addr, const XPlanes
     return fmaf((float)AB, 256.f, (float)C);
 }
 
-template <int BITS, int RPW>
+template <int BITS, int RPW, bool SEG, bool QUANT>
 __global__ void __launch_bounds__((kMaxStreamWarps + 2) * 32, 1)
     qmv_stream_kernel(const __nv_bfloat16* __restrict__ x, const uint32_t* __restrict__ w,
                       const uint16_t* __restrict__ scales, const uint16_t* __restrict__ biases,
                       __nv_bfloat16* __restrict__ y, int K, int N, int group,
-                      const StreamShape sh, int32_t* status) {
+                      const StreamShape sh, const StreamSeg sg, int32_t* status) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ uint64_t full[kStreamStages], empty[kStreamStages], xfull;
+    if (SEG) {
+        // the ids and source rows may come from the previous kernel
+        grid_dep_wait();
+        // every CTA checks all ids (there are few): an id outside [0, E) or
+        // a source row outside [0, T) makes its row zero, ids that decrease
+        // anywhere make every row zero; the first CTA reports the bits
+        __shared__ int seg_flags;
+        if (threadIdx.x == 0) seg_flags = 0;
+        __syncthreads();
+        int f = 0;
+        for (int i = threadIdx.x; i < sg.B; i += blockDim.x) {
+            const int ei = sg.ids[i];
+            if (ei < 0 || ei >= sg.E) f |= MXQ_DEV_BAD_EXPERT_ID;
+            if (i > 0 && sg.ids[i - 1] > ei) f |= MXQ_DEV_UNSORTED_IDS;
+            if (sg.row_src) {
+                const int sr = sg.row_src[i];
+                if (sr < 0 || sr >= sg.T) f |= MXQ_DEV_BAD_ROW_SRC;
+            }
+        }
+        if (f) atomicOr(&seg_flags, f);
+        __syncthreads();
+        const int all = seg_flags;
+        if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0 && all &&
+            status)
+            atomicOr(status, all);
+        const int r = blockIdx.y;
+        const bool second = blockIdx.z != 0;
+        const int e = sg.ids[r];
+        const int src = sg.row_src ? sg.row_src[r] : r;
+        __nv_bfloat16* const yr = (second ? sg.y1 : y) + (long long)r * N;
+        if ((all & MXQ_DEV_UNSORTED_IDS) || e < 0 || e >= sg.E || src < 0 || src >= sg.T) {
+            if (blockIdx.x == 0)
+                for (int n = threadIdx.x; n < N; n += blockDim.x) yr[n] = __float2bfloat16_rn(0.f);
+            return;  // the whole CTA, before any barrier is initialised
+        }
+        x += (long long)src * K;
+        w = (second ? sg.w1 : w) + (long long)e * sg.w_expert_stride;
+        scales = (second ? sg.s1 : scales) + (long long)e * sg.sb_expert_stride;
+        biases = (second ? sg.b1 : biases) + (long long)e * sg.sb_expert_stride;
+        y = yr;
+    }
     // per-chunk partial sums of each (row, K segment), handed to the reducer
     // warp through a ring of kRedBufs buffers
     __shared__ float red[kRedBufs][kMaxStreamWarps * 8];
@@ -631,7 +698,7 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 2) * 32, 1)
             const char* wb = reinterpret_cast<const char*>(w);
             const char* sbp = reinterpret_cast<const char*>(scales);
             const char* bbp = reinterpret_cast<const char*>(biases);
-            const ChunkRows cr{N / sh.nchunks, N % sh.nchunks};
+            const ChunkRows<QUANT> cr(N, sh);
             // while the previous kernel finishes, have L2 fetch this CTA's
             // first chunk, so that the first copy after the wait does not
             // start from DRAM latency
@@ -688,7 +755,7 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 2) * 32, 1)
         // sums each row's K-segment partials in a fixed order and stores y,
         // so the compute warps go on to the next chunk without waiting for
         // one another
-        const ChunkRows cr{N / sh.nchunks, N % sh.nchunks};
+        const ChunkRows<QUANT> cr(N, sh);
         for (int j = 0;; ++j) {
             const int chunk = blockIdx.x + j * gridDim.x;
             if (chunk >= sh.nchunks) break;
@@ -753,7 +820,7 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 2) * 32, 1)
     const int g = k0 / group;
     const uint32_t lane_code_off = (uint32_t)(seg * 1024 + lane * 32) * BITS / 8;
 
-    const ChunkRows cr{N / sh.nchunks, N % sh.nchunks};
+    const ChunkRows<QUANT> cr(N, sh);
     for (int j = 0;; ++j) {
         const int chunk = blockIdx.x + j * gridDim.x;
         if (chunk >= sh.nchunks) break;
@@ -833,13 +900,14 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 2) * 32, 1)
     if (threadIdx.x == 0 && abort_flag && status) atomicOr(status, 0x8 /* MXQ_DEV_TIMEOUT */);
 }
 
-template <int BITS>
+template <int BITS, bool SEG>
 cudaError_t launch_stream(const __nv_bfloat16* x, const uint32_t* w, const uint16_t* s,
                           const uint16_t* b, __nv_bfloat16* y, int K, int N, int group, int rpw,
-                          const StreamShape& sh, int grid, int32_t* status, cudaStream_t stream) {
+                          const StreamShape& sh, const StreamSeg& seg, dim3 grid,
+                          int32_t* status, cudaStream_t stream) {
     const int smem = sh.x_offset + K * 2;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
+    cfg.gridDim = grid;
     cfg.blockDim = dim3((sh.warps + 2) * 32);  // compute warps, producer, reducer
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
@@ -848,13 +916,16 @@ cudaError_t launch_stream(const __nv_bfloat16* x, const uint32_t* w, const uint1
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    // the segment form always takes the general chunk arithmetic
+    constexpr bool kAnyQuant = SEG;
 #define MXQ_STREAM_CASE(R)                                                                      \
     case R: {                                                                                   \
-        cudaError_t e = cudaFuncSetAttribute(qmv_stream_kernel<BITS, R>,                        \
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem); \
+        const auto kern = (kAnyQuant || sh.quantum > 1) ? qmv_stream_kernel<BITS, R, SEG, true>  \
+                                                        : qmv_stream_kernel<BITS, R, SEG, SEG>;  \
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,  \
+                                             smem);                                             \
         if (e != cudaSuccess) return e;                                                         \
-        e = cudaLaunchKernelEx(&cfg, qmv_stream_kernel<BITS, R>, x, w, s, b, y, K, N, group, sh, \
-                               status);                                                         \
+        e = cudaLaunchKernelEx(&cfg, kern, x, w, s, b, y, K, N, group, sh, seg, status);        \
         if (e != cudaSuccess) return e;                                                         \
         break;                                                                                  \
     }
@@ -869,14 +940,107 @@ cudaError_t launch_stream(const __nv_bfloat16* x, const uint32_t* w, const uint1
     return cudaGetLastError();
 }
 
+// The streaming GEMV's shape for a [N, K] matrix, or false when the shape
+// does not fit it (the direct-load kernel then runs): K % 64 == 0 (whole
+// 16-byte code rows; the callers check K % 128 at 3 bits), K <= 20480,
+// scales/biases 16-byte aligned, and N a multiple of the row quantum that
+// makes a chunk's scales (and biases) whole 16-byte units.  `ctas` is the
+// number of CTAs that will stream this matrix (the chunk count is made a
+// multiple of it); a negative value -c means min(c, the chunks needed), and
+// the number used is returned in it.
+bool stream_shape(int K, int N, int bits, int group, const void* scales, const void* biases,
+                  int& ctas, StreamShape& sh, int& rpw) {
+    const bool sb_aligned = (reinterpret_cast<uintptr_t>(scales) % 16 == 0) &&
+                            (reinterpret_cast<uintptr_t>(biases) % 16 == 0);
+    const int nseg = (K + 1023) / 1024;
+    if (K % 64 != 0 || nseg > kMaxStreamWarps || !sb_aligned) return false;
+    sh.nseg = nseg;
+    sh.phases = kTargetWarps / nseg > 1 ? kTargetWarps / nseg : 1;
+    if (sh.phases * nseg > kMaxStreamWarps) sh.phases = kMaxStreamWarps / nseg;
+    sh.warps = sh.phases * nseg;
+    sh.row_bytes = K * bits / 8;
+    sh.sb_bytes = (K / group) * 2;
+    // rows per unit: 16 / gcd(sb_bytes, 16)
+    int g = sh.sb_bytes & 15;
+    sh.quantum = g == 0 ? 1 : (g % 8 == 0 ? 2 : (g % 4 == 0 ? 4 : 8));
+    if (N % sh.quantum != 0) return false;
+    rpw = kChunkBytes / (sh.row_bytes * sh.phases);
+    rpw = rpw >= 8 ? 8 : rpw >= 4 ? 4 : rpw >= 2 ? 2 : 1;
+    // the ring and the activation copy share the 227 KB of shared memory
+    while (rpw > 1 && kStreamStages * sh.phases * rpw * (sh.row_bytes + 2 * sh.sb_bytes) + K * 2 >
+                          kStreamSmemMax)
+        rpw /= 2;
+    // a stage holds at most sh.rows rows, a multiple of the quantum
+    sh.rows = sh.phases * rpw / sh.quantum * sh.quantum;
+    if (sh.rows < sh.quantum) return false;
+    sh.stage_bytes = sh.rows * (sh.row_bytes + 2 * sh.sb_bytes);  // pieces are 16-byte multiples
+    sh.x_offset = kStreamStages * sh.stage_bytes;
+    sh.wait_budget = wait_budget_cycles();
+    // chunks of at most sh.rows rows, as many as a multiple of the CTAs
+    const int units = N / sh.quantum;
+    const int per_chunk = sh.rows / sh.quantum;
+    sh.nchunks = (units + per_chunk - 1) / per_chunk;
+    if (ctas < 0) ctas = sh.nchunks < -ctas ? sh.nchunks : -ctas;
+    sh.nchunks = (sh.nchunks + ctas - 1) / ctas * ctas;
+    if (sh.nchunks > units) sh.nchunks = units;
+    return true;
+}
+
+template <bool SEG>
+cudaError_t launch_stream_bits(int bits, const __nv_bfloat16* x, const uint32_t* w,
+                               const uint16_t* s, const uint16_t* b, __nv_bfloat16* y, int K,
+                               int N, int group, int rpw, const StreamShape& sh,
+                               const StreamSeg& seg, dim3 grid, int32_t* status,
+                               cudaStream_t stream) {
+    switch (bits) {
+        case 2: return launch_stream<2, SEG>(x, w, s, b, y, K, N, group, rpw, sh, seg, grid, status, stream);
+        case 3: return launch_stream<3, SEG>(x, w, s, b, y, K, N, group, rpw, sh, seg, grid, status, stream);
+        case 4: return launch_stream<4, SEG>(x, w, s, b, y, K, N, group, rpw, sh, seg, grid, status, stream);
+        case 6: return launch_stream<6, SEG>(x, w, s, b, y, K, N, group, rpw, sh, seg, grid, status, stream);
+        case 8: return launch_stream<8, SEG>(x, w, s, b, y, K, N, group, rpw, sh, seg, grid, status, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_gather_qmv(const void* x, const uint32_t* w, const void* scales,
                               const void* biases, const uint32_t* w1, const void* scales1,
                               const void* biases1, const int32_t* expert_ids,
                               const int32_t* row_src, void* y, void* y1, int sets, int T, int B,
-                              int E, int K, int N, int bits, int group, int32_t* status,
-                              cudaStream_t stream) {
+                              int E, int K, int N, int bits, int group, int sms,
+                              bool stream_form, int32_t* status, cudaStream_t stream) {
+    const long long wst = (long long)N * K * bits / 32;
+    const long long sbst = (long long)N * (K / group);
+    if (stream_form) {
+        // the streaming GEMV, one grid row per sorted row (and weight set):
+        // each sorted row's expert matrix streams through `ctas` CTAs
+        StreamShape sh;
+        int rpw = 1;
+        int ctas = sms / (B * sets) > 1 ? sms / (B * sets) : 1;
+        const bool set1_aligned = sets < 2 || (reinterpret_cast<uintptr_t>(scales1) % 16 == 0 &&
+                                               reinterpret_cast<uintptr_t>(biases1) % 16 == 0);
+        if (set1_aligned && stream_shape(K, N, bits, group, scales, biases, ctas, sh, rpw)) {
+            StreamSeg seg;
+            seg.ids = expert_ids;
+            seg.row_src = row_src;
+            seg.w1 = w1;
+            seg.s1 = static_cast<const uint16_t*>(scales1);
+            seg.b1 = static_cast<const uint16_t*>(biases1);
+            seg.y1 = static_cast<__nv_bfloat16*>(y1);
+            seg.T = T;
+            seg.B = B;
+            seg.E = E;
+            seg.w_expert_stride = wst;
+            seg.sb_expert_stride = sbst;
+            return launch_stream_bits<true>(
+                bits, static_cast<const __nv_bfloat16*>(x), w, static_cast<const uint16_t*>(scales),
+                static_cast<const uint16_t*>(biases), static_cast<__nv_bfloat16*>(y), K, N, group,
+                rpw, sh, seg, dim3(ctas, B, sets), status, stream);
+        }
+        return cudaErrorNotSupported;  // the shape does not fit the streaming form
+    }
+    // the direct-load GEMV: grid (N / 16, sorted rows, weight sets)
     const int seg_k = bits == 8 ? 512 : 1024;
     const int nseg_g = (K + seg_k - 1) / seg_k;
     const int max_warps = direct_max_warps(bits);
@@ -891,8 +1055,6 @@ cudaError_t launch_gather_qmv(const void* x, const uint32_t* w, const void* scal
     const auto* bb1 = static_cast<const uint16_t*>(biases1);
     auto* yb = static_cast<__nv_bfloat16*>(y);
     auto* yb1 = static_cast<__nv_bfloat16*>(y1);
-    const long long wst = (long long)N * K * bits / 32;
-    const long long sbst = (long long)N * (K / group);
 #define MXQ_GATHER_QMV(BB)                                                                        \
     gather_qmv_kernel<BB><<<grid, block, 0, stream>>>(xb, w, sb, bb, w1, sb1, bb1, expert_ids,     \
                                                       row_src, yb, yb1, T, B, E, K, N, group, wst, \
@@ -918,46 +1080,12 @@ cudaError_t launch_qmv(const void* x, const uint32_t* w, const void* scales, con
     const auto* sb = static_cast<const uint16_t*>(scales);
     const auto* bb = static_cast<const uint16_t*>(biases);
     auto* yb = static_cast<__nv_bfloat16*>(y);
-    const bool sb_aligned = (reinterpret_cast<uintptr_t>(scales) % 16 == 0) &&
-                            (reinterpret_cast<uintptr_t>(biases) % 16 == 0);
-    const int nseg = (K + 1023) / 1024;
-    // a chunk's scales (and biases) are one bulk copy: a row's pairs must
-    // fill whole 16-byte units
-    const bool sb_rows16 = (K / group) % 8 == 0;
-    const bool stream_bits = true;  // every width (3 and 6 bits: float code path)
-    if (stream_bits && K % 512 == 0 && nseg <= kMaxStreamWarps && sb_aligned && sb_rows16) {
-        StreamShape sh;
-        sh.nseg = nseg;
-        sh.phases = kTargetWarps / nseg > 1 ? kTargetWarps / nseg : 1;
-        if (sh.phases * nseg > kMaxStreamWarps) sh.phases = kMaxStreamWarps / nseg;
-        sh.warps = sh.phases * nseg;
-        sh.row_bytes = K * bits / 8;
-        sh.sb_bytes = (K / group) * 2;
-        int rpw = kChunkBytes / (sh.row_bytes * sh.phases);
-        rpw = rpw >= 8 ? 8 : rpw >= 4 ? 4 : rpw >= 2 ? 2 : 1;
-        sh.rows = sh.phases * rpw;
-        // the ring and the activation copy share the 227 KB of shared memory
-        while (rpw > 1 && kStreamStages * sh.phases * rpw * (sh.row_bytes + 2 * sh.sb_bytes) +
-                                  K * 2 > kStreamSmemMax)
-            rpw /= 2;
-        sh.rows = sh.phases * rpw;
-        sh.stage_bytes = sh.rows * (sh.row_bytes + 2 * sh.sb_bytes);  // pieces are 16-byte multiples
-        sh.x_offset = kStreamStages * sh.stage_bytes;
-        sh.wait_budget = wait_budget_cycles();
-        // chunks of at most sh.rows rows, as many as a multiple of the grid
-        sh.nchunks = (N + sh.rows - 1) / sh.rows;
-        const int grid = sh.nchunks < sms ? sh.nchunks : sms;
-        sh.nchunks = (sh.nchunks + grid - 1) / grid * grid;
-        if (sh.nchunks > N) sh.nchunks = N;
-        if (bits == 2)
-            return launch_stream<2>(xb, w, sb, bb, yb, K, N, group, rpw, sh, grid, status, stream);
-        if (bits == 3)
-            return launch_stream<3>(xb, w, sb, bb, yb, K, N, group, rpw, sh, grid, status, stream);
-        if (bits == 6)
-            return launch_stream<6>(xb, w, sb, bb, yb, K, N, group, rpw, sh, grid, status, stream);
-        return bits == 4
-                   ? launch_stream<4>(xb, w, sb, bb, yb, K, N, group, rpw, sh, grid, status, stream)
-                   : launch_stream<8>(xb, w, sb, bb, yb, K, N, group, rpw, sh, grid, status, stream);
+    StreamShape sh;
+    int rpw = 1, ctas = -sms;
+    if (stream_shape(K, N, bits, group, scales, biases, ctas, sh, rpw)) {
+        const StreamSeg none = {};
+        return launch_stream_bits<false>(bits, xb, w, sb, bb, yb, K, N, group, rpw, sh, none,
+                                         dim3(ctas), status, stream);
     }
     const int seg_k = bits == 8 ? 512 : 1024;
     const int nseg_g = (K + seg_k - 1) / seg_k;

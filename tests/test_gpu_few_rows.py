@@ -5,7 +5,9 @@ ABI, element by element:
   a multiple of the tile); M = 1 is bit for bit the GEMV;
 * mxq_gather_qmm at decode sizes: one to 128 tokens routed to 8 of 128
   experts, both expert shapes of the workload, routed and identity sources,
-  a hot expert, invalid ids and sources, the constant-per-expert case;
+  a hot expert, invalid ids and sources, the constant-per-expert case, and
+  both GEMV forms (streaming, and direct-load when the scales are not
+  16-byte aligned);
 * mxq_gather_qmm_gateup (the gate and up projections of an MoE layer in one
   launch): both outputs against two separate checker calls, at decode size
   (per-row GEMVs) and at prefill size (the grouped GEMM), each bit for bit
@@ -91,6 +93,26 @@ def test_gather_decode_sizes(T, K, N, ident):
     assert int(status.item()) == 0
     y2 = _mxq().gather_qmm(c.x_d, c.w_d, c.s_d, c.b_d, c.ids_d, c.src_d, 4)
     assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+
+
+@pytest.mark.parametrize("T,K,N,ident", [(2, 2816, 704, False), (4, 704, 2816, True)])
+def test_gather_decode_direct_form(T, K, N, ident):
+    # scales and biases that are not 16-byte aligned do not fit the streaming
+    # GEMV: the call takes the direct-load GEMV and must agree all the same
+    import torch
+
+    c = MoECase(T, 32, 8, K, N, 4, seed=70 + T, identity_src=ident, routing_seed=71 + T)
+    pad = []
+    for t in (c.s_d, c.b_d):
+        buf = torch.empty((t.numel() + 1,), dtype=torch.bfloat16, device="cuda")
+        v = buf[1:].view(t.shape)   # 2 bytes past a 16-byte boundary
+        v.copy_(t)
+        pad.append(v)
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    y = _mxq().gather_qmm(c.x_d, c.w_d, pad[0], pad[1], c.ids_d, c.src_d, 4, dev_status=status)
+    yr, bnd = oracle.gather_qmm(c.x, c.w, c.s, c.b, c.ids, c.src, c.T, c.B, c.E, c.K, c.N, 4)
+    assert_close(to_f64(y), yr, bnd, "gather decode, direct form")
+    assert int(status.item()) == 0
 
 
 @pytest.mark.parametrize("group", [32, 128])

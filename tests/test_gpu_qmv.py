@@ -25,7 +25,12 @@ def _ref(case):
 @pytest.mark.parametrize("bits", [4, 8])
 @pytest.mark.parametrize("K,N", [(512, 256), (64, 1), (64, 7), (128, 17), (704, 33), (1088, 100),
                                  (1024, 16), (2048, 31), (5120, 513), (6144, 129),
-                                 (1536, 77), (18432, 40), (19456, 40)])
+                                 (1536, 77), (18432, 40), (19456, 40),
+                                 # rows whose scales are not whole 16-byte units:
+                                 # chunks of the streaming kernel start on 2, 4
+                                 # or 8 rows
+                                 (2816, 704), (704, 2816), (1088, 104), (1472, 96),
+                                 (2880, 66), (320, 136)])
 def test_qmv_small(bits, K, N):
     case = DenseCase(1, K, N, bits, seed=K + N, x_seed=K)
     y = _run(case)
