@@ -87,6 +87,13 @@ cudaError_t launch_qmv(const void* x, const uint32_t* w, const void* scales, con
                        void* y, int K, int N, int bits, int group, int sms, int32_t* status,
                        cudaStream_t stream);
 
+// A few activation rows (M >= 2): one streaming GEMV per row, each row in
+// its own grid row (cudaErrorNotSupported when the shape does not fit the
+// streaming kernel).
+cudaError_t launch_qmv_rows(const void* x, const uint32_t* w, const void* scales,
+                            const void* biases, void* y, int M, int K, int N, int bits, int group,
+                            int sms, int32_t* status, cudaStream_t stream);
+
 // Dense or grouped tcgen05 GEMM; grid.y = number of M tiles (dense) or an
 // upper bound on the number of tiles (grouped).
 cudaError_t launch_qmm_tc(const QmmParams& p, int bits, int grid_m, int max_rows_per_tile,

@@ -463,7 +463,8 @@ struct StreamShape {
 // GEMV of expert ids[r]'s matrix with activation row row_src[r]; grid z
 // selects the weight set of the gate/up pair (set 1: w1, s1, b1 -> y1).
 struct StreamSeg {
-    const int32_t* ids;
+    const int32_t* ids;      // null: every row multiplies matrix 0 (a dense call with
+                             // a few activation rows, one row per grid row)
     const int32_t* row_src;  // null: row r
     const uint32_t* w1;
     const uint16_t* s1;
@@ -634,7 +635,7 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 2) * 32, 1)
         if (threadIdx.x == 0) seg_flags = 0;
         __syncthreads();
         int f = 0;
-        for (int i = threadIdx.x; i < sg.B; i += blockDim.x) {
+        for (int i = threadIdx.x; sg.ids && i < sg.B; i += blockDim.x) {
             const int ei = sg.ids[i];
             if (ei < 0 || ei >= sg.E) f |= MXQ_DEV_BAD_EXPERT_ID;
             if (i > 0 && sg.ids[i - 1] > ei) f |= MXQ_DEV_UNSORTED_IDS;
@@ -651,7 +652,7 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 2) * 32, 1)
             atomicOr(status, all);
         const int r = blockIdx.y;
         const bool second = blockIdx.z != 0;
-        const int e = sg.ids[r];
+        const int e = sg.ids ? sg.ids[r] : 0;
         const int src = sg.row_src ? sg.row_src[r] : r;
         __nv_bfloat16* const yr = (second ? sg.y1 : y) + (long long)r * N;
         if ((all & MXQ_DEV_UNSORTED_IDS) || e < 0 || e >= sg.E || src < 0 || src >= sg.T) {
@@ -1071,6 +1072,25 @@ cudaError_t launch_gather_qmv(const void* x, const uint32_t* w, const void* scal
         MXQ_GATHER_QMV(8);
 #undef MXQ_GATHER_QMV
     return cudaGetLastError();
+}
+
+cudaError_t launch_qmv_rows(const void* x, const uint32_t* w, const void* scales,
+                            const void* biases, void* y, int M, int K, int N, int bits, int group,
+                            int sms, int32_t* status, cudaStream_t stream) {
+    StreamShape sh;
+    int rpw = 1;
+    int ctas = sms / M > 1 ? sms / M : 1;
+    if (!stream_shape(K, N, bits, group, scales, biases, ctas, sh, rpw))
+        return cudaErrorNotSupported;
+    StreamSeg seg = {};
+    seg.T = M;
+    seg.B = M;
+    seg.E = 1;
+    return launch_stream_bits<true>(bits, static_cast<const __nv_bfloat16*>(x), w,
+                                    static_cast<const uint16_t*>(scales),
+                                    static_cast<const uint16_t*>(biases),
+                                    static_cast<__nv_bfloat16*>(y), K, N, group, rpw, sh, seg,
+                                    dim3(ctas, M, 1), status, stream);
 }
 
 cudaError_t launch_qmv(const void* x, const uint32_t* w, const void* scales, const void* biases,

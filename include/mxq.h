@@ -130,7 +130,9 @@ mxq_status mxq_qmm_kn(const void* x, const uint32_t* w, const void* scales, cons
 
 /* Prefill GEMM, y[M, N] = x[M, K] . w^[N, K]^T (mlxcel issue #1536, Baseline
  * profile table and Diagnosis item 4: the qmm_naive kernel).  M = 1 runs the
- * streaming GEMV of mxq_qmv (the same operation).  Otherwise the tcgen05
+ * streaming GEMV of mxq_qmv (the same operation); M = 2 or 3 runs one such
+ * GEMV per activation row where the shape allows (fewer rows than a tensor
+ * tile's fill is worth).  Otherwise the tcgen05
  * tensor cores: codes are dequantised to bf16 into tensor memory (the MMA's
  * A operand) and the products accumulate in fp32 in tensor memory.  When M
  * and N give fewer 128 x 256 tiles than the GPU has SMs, K is split over up
