@@ -250,7 +250,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kCols = kTmemCols;
     const int SA = min(kMaxAStages, (kCols - a0) / kAStageCols);
 
-    if (warp == kCodeWarp && lane == 0) prefetch_tmap(&code_map);
+    if (warp == kCodeWarp && lane == 0) {
+        prefetch_tmap(&code_map);
+        if (!GATHER) {
+            // the dense form starts while the previous kernel finishes (see
+            // the wait below): have L2 fetch this CTA's first code slot now
+            constexpr int kWordsPerBox = kCodeBoxRowBytes / 4;
+            const int c0 = kb_begin * (kHalfK * BITS / 32);
+            const int words = p.K * BITS / 32;
+            for (int b = 0; b < slot_row_bytes(BITS) / kCodeBoxRowBytes; ++b)
+                if (c0 + b * kWordsPerBox < words)
+                    tma_prefetch_l2_2d(&code_map, c0 + b * kWordsPerBox, n0);
+        }
+    }
     if (warp == kXWarp0 && lane == 0) prefetch_tmap(&x_map);
     if (threadIdx.x == 0) {
         for (int i = 0; i < SC; ++i) {
@@ -267,6 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(accf, 1);
         mbar_init_fence();
+        if (!GATHER) pdl_launch_dependents();
     }
     if (warp == kMmaWarp) {
         tmem_alloc(tmem_slot, (uint32_t)kCols);
@@ -277,6 +290,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     bool ok = true;
+    // the dense form is a programmatic dependent launch: everything above
+    // touched only this CTA's own resources; from here on it reads x, w,
+    // scales and biases and writes y, after the previous kernel completed
+    if (!GATHER) pdl_wait();
 
     if (warp == kCodeWarp) {
         // ---------------------------------------------------------------- codes TMA
@@ -1306,13 +1323,18 @@ cudaError_t launch_variant(const QmmParams& p, int grid_m, int max_rows, const C
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = L.total;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = p.splits;  // the K splits of one tile form a cluster
+    // the dense form may start while the previous kernel finishes (it waits
+    // before touching global memory); the grouped form reads the tile table
+    // the previous kernel writes, so it starts after it
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = GATHER ? 1 : 2;
     cudaError_t err = cudaLaunchKernelEx(&cfg, qmm_tc_kernel<BITS, GATHER, GROUP>, p, max_rows, cm, xm,
                                          cm1);
     if (err != cudaSuccess) return err;
