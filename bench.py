@@ -471,7 +471,7 @@ def run_mxq(args):
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     # last, so that the end of the line carries the workload's own configs:
-    # every other measured entry, then the spec configs (M sweep, 4/8-bit
+    # every other measured entry, then the workload configs (M sweep, 4/8-bit
     # pair, sorted-MoE gather, prefill), then the decode cases of `value`
     line["secondary"] = secondary + per_case
     if rank == 0:
@@ -502,7 +502,7 @@ def secondary_measurements(mxq, dev, stream, hbm, bf16_peak, Ws, clocks):
     """Every other measured configuration, as compact entries: name ``n``,
     time ``us``, TFLOP/s ``TF`` and/or GB/s ``GBs``, the binding roofline
     ``bound`` and the fraction of it reached ``frac``, and the median SM
-    clock ``mhz`` while it ran.  The list ends with the workload's north-star
+    clock ``mhz`` while it ran.  The list ends with the workload
     configurations, so that they close the JSON line."""
     import torch
 
@@ -632,7 +632,7 @@ def secondary_measurements(mxq, dev, stream, hbm, bf16_peak, Ws, clocks):
     torch.cuda.empty_cache()
 
     # ---- sorted MoE: experts of both shapes, the decode-sized calls first
-    north = []
+    workload = []
     for K, N, ident in ((2816, 704, False), (704, 2816, True)):
         E, T, top_k, bits = 128, 573, 8, 4
         ids, src = synth.routing(T, E, top_k, seed=2)
@@ -696,19 +696,19 @@ def secondary_measurements(mxq, dev, stream, hbm, bf16_peak, Ws, clocks):
         m0 = clocks.mark()
         t, _ = time_launches(fn, iters, stream)
         nbytes = E * expert_bytes + Tx * K * 2 + B * N * 2
-        north.append(entry("gather_qmm E=128 top8 T=573 B=%d K=%d N=%d b4 g64" % (B, K, N), t,
+        workload.append(entry("gather_qmm E=128 top8 T=573 B=%d K=%d N=%d b4 g64" % (B, K, N), t,
                            nbytes, 2.0 * B * K * N, m0, {"tok_s": int(T / t)}))
         del w, s, b, copies, ucopies, x, y
         torch.cuda.empty_cache()
 
-    # ---- spec configurations: M sweep at K=N=5120, the 4/8-bit pair,
+    # ---- the workload configurations: M sweep at K=N=5120, the 4/8-bit pair,
     # then the prefill GEMM
     sweep = [dense_entry("qmm", M, 5120, 5120, 4, W_sq, copies=6) for M in (1, 8, 32, 128, 600)]
     pair = [dense_entry("pair qmv", 1, 5120, 5120, 8, W_sq, copies=6),
             dense_entry("pair qmm", 128, 5120, 5120, 8, W_sq, copies=6)]
     prefill = dense_entry("qmm prefill", 600, 5120, 17408, 4, W_big, copies=3)
     prefill["tok_s"] = int(600 / (prefill["us"] * 1e-6))
-    return out + north + sweep + pair + [prefill]
+    return out + workload + sweep + pair + [prefill]
 
 
 
