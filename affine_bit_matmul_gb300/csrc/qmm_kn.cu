@@ -13,8 +13,9 @@
 //  * a TMA copy brings the block's codes of the CTA's 128 columns ([64 rows
 //    of k] x [128 * bits / 8 bytes]) into a ring of code slots, and another
 //    the activation tile (128-byte swizzle, the MMA's B operand, K-major);
-//  * eight dequant warps turn the codes into bf16 w^ = s*q + b (one rounding,
-//    as in the [N, K] kernels) and store them into a shared-memory A stage
+//  * a group of eight dequant warps (two groups, on alternate blocks) turns
+//    the codes into bf16 w^ = s*q + b (one rounding, as in the [N, K]
+//    kernels) and stores them into a shared-memory A stage
 //    in the MN-major 128-byte-swizzled layout: 64-column atoms of 8 k rows x
 //    128 bytes, 16-byte chunk c of row r at chunk c ^ r; the two atoms along
 //    n are 1024 bytes apart (the descriptor's leading byte offset) and the
@@ -117,21 +118,11 @@ __device__ __forceinline__ uint32_t a_chunk(int k, int c) {
                       (((c & 7) ^ (k & 7)) << 4));
 }
 
-__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
-    uint32_t v;
-    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-    return v;
-}
-
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
                  "r"(d)
                  : "memory");
-}
-
-__device__ __forceinline__ void st_shared_v2(uint32_t addr, uint32_t a, uint32_t b) {
-    asm volatile("st.shared.v2.b32 [%0], {%1,%2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
 }
 
 template <int BITS, bool GATHER, int GROUP>
@@ -310,46 +301,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------------- dequant
         // kGroups groups of warps take the stages in turn (group g: stages g,
         // g + kGroups, ...), so several stages are dequantised at once and
-        // each warp has kGroups stage times for one stage.  A stage's codes are 64 rows of
-        // W words; thread t of a group takes words t, t + 256, ...: word i is
-        // row i / W, columns [(i % W) * 32 / BITS, ...).  A thread's words
-        // share their columns (so their group of n) and lie kRowStep rows
-        // apart.
+        // each warp has kGroups stage times for one stage.  Thread t of a
+        // group takes row t / 4 of the stage's 64 rows of k and the 32
+        // columns [32 (t % 4), + 32) of the tile: BITS consecutive code words
+        // (one 8-, 16- or two 16-byte loads), one scale and one bias (32
+        // columns aligned to 32 lie in one group, G being 32, 64 or 128), and
+        // four 16-byte chunks of A.  A warp covers one 8-row atom along k, so
+        // each of its four stores puts the chunks' swizzled positions
+        // (c & 7) ^ (k & 7) on every bank quad equally often.
         constexpr int W = kTileN * BITS / 32;                // words per code row
-        constexpr int kWords = kBK * W / kGroupThreads;      // words per thread: 2, 4, 8
-        constexpr int kRowStep = kGroupThreads / W;          // rows between a thread's words
-        constexpr int kPerWord = 32 / BITS;                  // columns per word
+        constexpr int kColBlocks = kTileN / 32;              // threads per row of k
+        static_assert(kBK * kColBlocks == kGroupThreads, "one row block per thread");
         const int grp = warp / kGroupWarps;
         const int t = threadIdx.x % kGroupThreads;
-        const int wc = t % W;                   // word column
-        const int r0 = t / W;                   // first row
-        const int nl = wc * kPerWord;           // first column of the word, within the tile
-        const bool col_ok = n0 + nl < p.N;      // columns past N: zero codes, no scale read
+        const int r = t / kColBlocks;           // row of k within a stage
+        const int cb = t % kColBlocks;          // column block
+        const bool col_ok = n0 + cb * 32 < p.N; // columns past N: zero codes, no scale read
         const int groups = p.N / GROUP;         // scale/bias entries per row of k
-        // scale and bias of row r0 of the CTA's first block; a stage moves
-        // them kBK rows on, word j kRowStep rows further
+        // scale and bias of row r of the CTA's first block; a stage moves
+        // them kBK rows on
         const long long sb0 = (long long)e * p.sb_expert_stride +
-                              ((long long)kb_begin * kBK + r0) * groups + (n0 + nl) / GROUP;
+                              ((long long)kb_begin * kBK + r) * groups + (n0 + cb * 32) / GROUP;
         const uint16_t* sp = p.scales + sb0;
         const uint16_t* bp = p.biases + sb0;
         const long long stage_step = (long long)kBK * groups;
-        const int k_left0 = p.K - kb_begin * kBK - r0;  // rows of k left from row r0 of block 0
-        const uint32_t c_off = (uint32_t)((r0 * W + wc) * 4);
-        const uint32_t a_off = a_chunk(r0, nl >> 3) + (BITS == 8 ? (uint32_t)((nl & 7) * 2) : 0u);
-        const long long j_step = (long long)kRowStep * groups;
-        // scale/bias pairs of stage q, loaded two of the group's stages
-        // (2 * kGroups stage times) before their use
-        auto sb_load = [&](int q, uint32_t (&sl)[kWords], uint32_t (&bl)[kWords]) {
-            const long long at = (long long)q * stage_step;
-            const int left = k_left0 - q * kBK;
+        const int k_left0 = p.K - kb_begin * kBK - r;  // rows of k left from row r of block 0
+        // 8-bit: the thread's 32 code bytes are two 16-byte halves, read
+        // half hx first (hx = r & 1), so that the two rows of a quarter warp
+        // fall on different bank quads; its chunk order follows
+        const int hx = BITS == 8 ? (r & 1) : 0;
+        const uint32_t c_off = (uint32_t)(r * W * 4 + cb * BITS * 4);
+        uint32_t a_off[4];  // the A chunk that the thread's i-th store fills
 #pragma unroll
-            for (int j = 0; j < kWords; ++j) {
-                sl[j] = 0u;
-                bl[j] = 0u;
-                if (col_ok && q < nkb && j * kRowStep < left) {
-                    sl[j] = __ldg(sp + at + j * j_step);
-                    bl[j] = __ldg(bp + at + j * j_step);
-                }
+        for (int i = 0; i < 4; ++i) a_off[i] = a_chunk(r, cb * 4 + (i ^ (2 * hx)));
+        // scale/bias pair of stage q, loaded two of the group's stages
+        // (2 * kGroups stage times) before its use
+        auto sb_load = [&](int q, uint32_t& sl, uint32_t& bl) {
+            sl = 0u;
+            bl = 0u;
+            if (col_ok && q < nkb && q * kBK < k_left0) {
+                sl = __ldg(sp + (long long)q * stage_step);
+                bl = __ldg(bp + (long long)q * stage_step);
             }
         };
         Ring cr(SC), ar(kAStages);
@@ -357,47 +349,58 @@ __global__ void __launch_bounds__(kThreads, 1)
             cr.next();
             ar.next();
         }
-        // stage q with its scale/bias pairs in (sc, bc); loads the pairs of
-        // stage q + 2 * kGroups into (sn, bn)
-        auto stage = [&](int q, const uint32_t (&sc)[kWords], const uint32_t (&bc)[kWords],
-                         uint32_t (&sn)[kWords], uint32_t (&bn)[kWords]) -> bool {
+        // stage q with its scale/bias pair (sc, bc); loads the pair of stage
+        // q + 2 * kGroups into (sn, bn)
+        auto stage = [&](int q, uint32_t sc, uint32_t bc, uint32_t& sn, uint32_t& bn) -> bool {
             sb_load(q + 2 * kGroups, sn, bn);
             if (!warp_wait_sleep(&cfull[cr.slot], cr.parity, p.wait_budget)) return false;
-            const uint32_t c_word = c_base0 + cr.slot * L.c_bytes + c_off;
-            uint32_t wd[kWords];
+            const uint32_t c_at = c_base0 + cr.slot * L.c_bytes + c_off;
+            uint32_t wd[BITS];
+            if (BITS == 2) {
+                asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];"
+                             : "=r"(wd[0]), "=r"(wd[1])
+                             : "r"(c_at)
+                             : "memory");
+            } else {
 #pragma unroll
-            for (int j = 0; j < kWords; ++j) wd[j] = ld_shared_u32(c_word + j * kRowStep * W * 4);
+                for (int h = 0; h < BITS / 4; ++h) {
+                    const uint4 v = ld_shared_v4(c_at + (uint32_t)((h ^ hx) * 16));
+                    wd[4 * h] = v.x;
+                    wd[4 * h + 1] = v.y;
+                    wd[4 * h + 2] = v.z;
+                    wd[4 * h + 3] = v.w;
+                }
+            }
             if (q >= kAStages &&
                 !warp_wait_sleep(&aempty[ar.slot], ar.parity ^ 1, p.wait_budget))
                 return false;
             const uint32_t a_stage = a_base0 + ar.slot * kAStageBytes;
+            if (BITS == 8) {
+                const float s = bf16_bits_to_float(sc), b = bf16_bits_to_float(bc);
 #pragma unroll
-            for (int j = 0; j < kWords; ++j) {
-                // with kRowStep a multiple of 8 every word sits at the same row
-                // of its 8-row atom, one atom stride per kRowStep / 8
-                const uint32_t dst =
-                    kRowStep % 8 == 0
-                        ? a_stage + a_off + j * (kRowStep / 8) * kAtomK
-                        : a_stage + a_chunk(r0 + j * kRowStep, nl >> 3) +
-                              (BITS == 8 ? (uint32_t)((nl & 7) * 2) : 0u);
-                if (BITS == 8) {
-                    uint32_t o[2];
-                    dequant_word8(wd[j], bf16_bits_to_float(sc[j]), bf16_bits_to_float(bc[j]), o);
-                    st_shared_v2(dst, o[0], o[1]);  // four columns: half of a 16-byte chunk
-                } else {
-                    // both halves of a bf16x2 take the word's scale and bias
-                    const uint32_t sw = prmt(sc[j], 0u, 0x1010u), bw = prmt(bc[j], 0u, 0x1010u);
-                    if (BITS == 4) {
+                for (int i = 0; i < 4; ++i) {
+                    uint32_t o0[2], o1[2];
+                    dequant_word8(wd[2 * i], s, b, o0);
+                    dequant_word8(wd[2 * i + 1], s, b, o1);
+                    st_shared_v4(a_stage + a_off[i], o0[0], o0[1], o1[0], o1[1]);
+                }
+            } else {
+                // both halves of a bf16x2 take the scale and bias
+                const uint32_t sw = prmt(sc, 0u, 0x1010u), bw = prmt(bc, 0u, 0x1010u);
+                if (BITS == 4) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
                         uint32_t o[4];
-                        dequant_word4(wd[j], sw, bw, o);
-                        st_shared_v4(dst, o[0], o[1], o[2], o[3]);
-                    } else {
+                        dequant_word4(wd[i], sw, bw, o);
+                        st_shared_v4(a_stage + a_off[i], o[0], o[1], o[2], o[3]);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
                         uint32_t o[8];
                         dequant_word2(wd[j], sw, bw, o);
-                        st_shared_v4(dst, o[0], o[1], o[2], o[3]);
-                        // the word's next 8 columns
-                        st_shared_v4(a_stage + a_chunk(r0 + j * kRowStep, (nl >> 3) + 1), o[4],
-                                     o[5], o[6], o[7]);
+                        st_shared_v4(a_stage + a_off[2 * j], o[0], o[1], o[2], o[3]);
+                        st_shared_v4(a_stage + a_off[2 * j + 1], o[4], o[5], o[6], o[7]);
                     }
                 }
             }
@@ -416,9 +419,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             return true;
         };
-        // three register sets in turn (the loop is unrolled by three), so
+        // three register pairs in turn (the loop is unrolled by three), so
         // no pair is ever copied
-        uint32_t sA[kWords], bA[kWords], sB[kWords], bB[kWords], sC[kWords], bC[kWords];
+        uint32_t sA, bA, sB, bB, sC, bC;
         sb_load(grp, sA, bA);
         sb_load(grp + kGroups, sB, bB);
         for (int q = grp; q < nkb && ok; q += 3 * kGroups) {
