@@ -69,8 +69,11 @@ constexpr int kCodeSlotRowBytes = 256;
 constexpr int kCodeBoxRowBytes = 128;
 // 3- and 6-bit stages are 48 and 96 bytes per row: their slots hold 384
 // bytes (three boxes, 8 or 4 stages), so a stage may cross a box boundary.
-__host__ __device__ constexpr int slot_row_bytes(int bits) {
-    return (bits == 3 || bits == 6) ? 384 : kCodeSlotRowBytes;
+// The compact form (two CTAs per SM, 108 KB each) uses one-box slots: a
+// slot is held until its last stage is dequantised, so with 16 KB slots
+// three of four can be loading where two 32 KB slots left one.
+__host__ __device__ constexpr int slot_row_bytes(int bits, bool compact = false) {
+    return compact ? kCodeBoxRowBytes : (bits == 3 || bits == 6) ? 384 : kCodeSlotRowBytes;
 }
 constexpr int kCodeBoxBytes = kTileN * kCodeBoxRowBytes;
 constexpr int kMaxAStages = 6;       // dequantised stages held in tensor memory
@@ -768,7 +771,7 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
                           const __grid_constant__ CUtensorMap x_map,
                           const __grid_constant__ CUtensorMap code_map1) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    const SmemLayout L = make_layout(max_rows, COMPACT, slot_row_bytes(BITS));
+    const SmemLayout L = make_layout(max_rows, COMPACT, slot_row_bytes(BITS, COMPACT));
     constexpr int kCols = COMPACT ? kCompactTmemCols : kTmemCols;
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -797,7 +800,7 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
     const int total = GATHER ? per_set * p.sets : m_tiles * n_tiles;
     const int KB = p.K / kHalfK;              // 64-wide blocks
     const int nst = (KB + 1) / 2;             // 128-wide stages per tile
-    constexpr int kSPS = slot_row_bytes(BITS) / (kBK * BITS / 8);  // stages per code slot
+    constexpr int kSPS = slot_row_bytes(BITS, COMPACT) / (kBK * BITS / 8);  // stages per code slot
     const int nslots = (nst + kSPS - 1) / kSPS;
     const int groups = p.K / GROUP;
     using SG = StageGroups<GROUP>;
@@ -882,10 +885,13 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
 
     if (warp == kCodeWarp) {
         // ---------------------------------------------------------------- codes TMA
-        constexpr int kWordsPerSlot = slot_row_bytes(BITS) / 4;
+        constexpr int kWordsPerSlot = slot_row_bytes(BITS, COMPACT) / 4;
         constexpr int kWordsPerBox = kCodeBoxRowBytes / 4;
-        constexpr int kBoxes = slot_row_bytes(BITS) / kCodeBoxRowBytes;
+        constexpr int kBoxes = slot_row_bytes(BITS, COMPACT) / kCodeBoxRowBytes;
         const int words = p.K * BITS / 32;
+        // grouped form: each expert's codes are read once, so they may leave
+        // L2 first (the activation rows, read once per n tile, stay)
+        const uint64_t code_policy = l2_policy_evict_first();
         Ring ring(SC);
         int issued = 0;
         for (int i = 0; ok; ++i) {
@@ -915,8 +921,9 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
                     const uint32_t dst = c_base0 + ring.slot * L.c_bytes;
                     for (int b = 0; b < nbox; ++b) {
                         if (GATHER)
-                            tma_load_3d(dst + b * kCodeBoxBytes, ti.set ? &code_map1 : &code_map,
-                                        c0 + b * kWordsPerBox, ti.n0, ti.e, &cfull[ring.slot]);
+                            tma_load_3d_hint(dst + b * kCodeBoxBytes, ti.set ? &code_map1 : &code_map,
+                                             c0 + b * kWordsPerBox, ti.n0, ti.e, &cfull[ring.slot],
+                                             code_policy);
                         else
                             tma_load_2d(dst + b * kCodeBoxBytes, &code_map, c0 + b * kWordsPerBox,
                                         ti.n0, &cfull[ring.slot]);
@@ -930,6 +937,7 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
         __syncwarp();
     } else if (warp == kXWarp0) {
         // ---------------------------------------------------------------- activation TMA
+        const uint64_t x_policy = l2_policy_evict_last();
         Ring ring(SX);
         int issued = 0;
         for (int i = 0; ok; ++i) {
@@ -950,9 +958,15 @@ __global__ void __launch_bounds__(COMPACT ? kThreads : kPThreads, COMPACT ? 2 : 
                 }
                 if (elect_one()) {
                     mbar_expect_tx(&xfull[ring.slot], x_bytes_in);
-                    for (int b = 0; b < boxes; ++b)
-                        tma_load_2d(x_base0 + ring.slot * L.x_bytes + b * p.x_box_rows * 128, &x_map,
-                                    q * kHalfK, ti.row_start + b * p.x_box_rows, &xfull[ring.slot]);
+                    for (int b = 0; b < boxes; ++b) {
+                        const uint32_t dst = x_base0 + ring.slot * L.x_bytes + b * p.x_box_rows * 128;
+                        if (GATHER)
+                            tma_load_2d_hint(dst, &x_map, q * kHalfK, ti.row_start + b * p.x_box_rows,
+                                             &xfull[ring.slot], x_policy);
+                        else
+                            tma_load_2d(dst, &x_map, q * kHalfK, ti.row_start + b * p.x_box_rows,
+                                        &xfull[ring.slot]);
+                    }
                 }
                 __syncwarp();
             }
@@ -1275,7 +1289,7 @@ template <int BITS, bool GATHER, bool COMPACT, int GROUP>
 cudaError_t launch_persistent(const QmmParams& p, int max_rows, int m_tiles, int n_tiles,
                               int grid, const CUtensorMap& cm, const CUtensorMap& xm,
                               const CUtensorMap& cm1, cudaStream_t stream) {
-    const SmemLayout L = make_layout(max_rows, COMPACT, slot_row_bytes(BITS));
+    const SmemLayout L = make_layout(max_rows, COMPACT, slot_row_bytes(BITS, COMPACT));
     const int smem = L.total + kPBarBytes;
     static bool attr_set[64] = {};
     int dev = 0;
