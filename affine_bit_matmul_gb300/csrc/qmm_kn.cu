@@ -301,21 +301,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------------- dequant
         // kGroups groups of warps take the stages in turn (group g: stages g,
         // g + kGroups, ...), so several stages are dequantised at once and
-        // each warp has kGroups stage times for one stage.  Thread t of a
-        // group takes row t / 4 of the stage's 64 rows of k and the 32
-        // columns [32 (t % 4), + 32) of the tile: BITS consecutive code words
-        // (one 8-, 16- or two 16-byte loads), one scale and one bias (32
-        // columns aligned to 32 lie in one group, G being 32, 64 or 128), and
-        // four 16-byte chunks of A.  A warp covers one 8-row atom along k, so
-        // each of its four stores puts the chunks' swizzled positions
-        // (c & 7) ^ (k & 7) on every bank quad equally often.
+        // each warp has kGroups stage times for one stage.  Each thread takes
+        // one row r of the stage's 64 rows of k and 32 columns [32 cb, + 32)
+        // of the tile: BITS consecutive code words (one 8-, 16- or two
+        // 16-byte loads), one scale and one bias (32 columns aligned to 32 lie
+        // in one group, G being 32, 64 or 128), and four 16-byte chunks of A.
+        // Warp w of a group covers the 8-row atom 8w .. 8w + 7, all four
+        // column blocks; within it, quarter warp q (lanes 8q .. 8q + 7) takes
+        // rows {0,1} (or {4,5} for q >= 2) with one pair of column blocks and
+        // rows {2,3} (or {6,7}) with the other pair, so that its eight
+        // threads' code loads fall on eight different 16-byte bank quads and
+        // so do each of their four stores (chunk c of row k sits at quad
+        // (c & 7) ^ (k & 7)): no shared-memory bank conflicts.
         constexpr int W = kTileN * BITS / 32;                // words per code row
         constexpr int kColBlocks = kTileN / 32;              // threads per row of k
         static_assert(kBK * kColBlocks == kGroupThreads, "one row block per thread");
         const int grp = warp / kGroupWarps;
         const int t = threadIdx.x % kGroupThreads;
-        const int r = t / kColBlocks;           // row of k within a stage
-        const int cb = t % kColBlocks;          // column block
+        const int ql = (t >> 3) & 3, l8 = t & 7;       // quarter warp, lane within it
+        const int rowpair = l8 >> 2;
+        const int r = 8 * (t >> 5) + (ql >> 1) * 4 + rowpair * 2 + ((l8 >> 1) & 1);
+        const int cb = (l8 & 1) + 2 * (rowpair ^ (ql & 1));
         const bool col_ok = n0 + cb * 32 < p.N; // columns past N: zero codes, no scale read
         const int groups = p.N / GROUP;         // scale/bias entries per row of k
         // scale and bias of row r of the CTA's first block; a stage moves
@@ -327,8 +333,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const long long stage_step = (long long)kBK * groups;
         const int k_left0 = p.K - kb_begin * kBK - r;  // rows of k left from row r of block 0
         // 8-bit: the thread's 32 code bytes are two 16-byte halves, read
-        // half hx first (hx = r & 1), so that the two rows of a quarter warp
-        // fall on different bank quads; its chunk order follows
+        // half hx first (hx = r & 1), so that odd and even rows of a quarter
+        // warp fall on different bank quads; its store order follows
         const int hx = BITS == 8 ? (r & 1) : 0;
         const uint32_t c_off = (uint32_t)(r * W * 4 + cb * BITS * 4);
         uint32_t a_off[4];  // the A chunk that the thread's i-th store fills
