@@ -74,7 +74,7 @@ def test_qmm_kn_wide_other_widths(bits):
 @pytest.mark.parametrize("bits", [2, 4, 8])
 @pytest.mark.parametrize("M,K,N", [
     (2, 64, 128), (16, 4096, 256), (33, 200, 640), (130, 1000, 384), (257, 5120, 1280),
-    (64, 8, 64), (600, 704, 2816),
+    (64, 8, 64), (600, 704, 2816), (320, 1024, 512),
 ])
 def test_qmm_kn_shapes(bits, group, M, K, N):
     if N % group:
