@@ -439,7 +439,9 @@ mxq_status gather_call(const void* x, const uint32_t* w, const void* scales, con
     p.tile_count = tile_count;
     p.status = dev_status;
     p.x_rows = B;
-    p.x_box_rows = 16;
+    // one TMA box of a slot's 64 rows per 64-wide block (rows past the tile
+    // are loaded and never used): fewer copies than 16-row boxes
+    p.x_box_rows = kGatherRowsPerTile;
     p.M = B;
     p.T = T;
     p.E = E;
