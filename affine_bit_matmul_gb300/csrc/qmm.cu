@@ -121,13 +121,14 @@ struct SmemLayout {
 // memory).  The activation tile comes from L2 with about a microsecond of
 // latency and the packed codes stream from HBM with up to two: two code
 // slots, up to six activation slots, then more code slots (up to 8), then
-// more activation slots (up to 16).  A code slot is the same 32 KB for both
-// widths (4 stages of 4-bit codes or 2 of 8-bit).
+// more activation slots (up to 16).  A code slot is 32 KB at every width
+// (4 stages of 4-bit codes or 2 of 8-bit), 48 KB for 3- and 6-bit codes,
+// and 16 KB in the compact form.
 __host__ __device__ inline SmemLayout make_layout(int max_rows, bool compact, int slot_bytes) {
     SmemLayout L;
     const int budget = compact ? kCompactSmemBudget : kSmemBudget;
     const int rows16 = (max_rows + 15) & ~15;
-    L.c_bytes = kTileN * slot_bytes;  // 32 KB: 8, 4 or 2 stages of 2-, 4-, 8-bit; 48 KB: 8 or 4 of 3-, 6-bit
+    L.c_bytes = kTileN * slot_bytes;  // 32 KB: 8, 4 or 2 stages of 2-, 4-, 8-bit; 48 KB: 8 or 4 of 3-, 6-bit; compact 16 KB
     L.x_bytes = (rows16 / 8) * 1024;                  // 128 B per row, 8-row atoms
     // two code slots, up to six activation slots, then more code slots (up
     // to kMaxCodeStages), then more activation slots (up to kMaxXStages)
