@@ -77,6 +77,7 @@ __host__ __device__ constexpr int slot_row_bytes(int bits, bool compact = false)
 }
 constexpr int kCodeBoxBytes = kTileN * kCodeBoxRowBytes;
 constexpr int kMaxAStages = 6;       // dequantised stages held in tensor memory
+constexpr int kMaxClusterSplits = 8; // K splits per tile: the portable cluster size
 constexpr int kMaxXStages = 16;
 constexpr int kSmemBudget = 224 * 1024;
 constexpr int kTmemCols = 512;       // accumulator + dequantised A stages
@@ -593,57 +594,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         cluster_sync();
         if (warp < kDequantWarps) {
             // rank z sums rows m = z, z + S, ... over all ranks in rank order;
-            // a thread takes 4 consecutive columns of 4 rows at a time and
-            // issues all of their remote loads before adding
+            // a thread takes 4 consecutive columns of one row at a time and
+            // issues the remote loads of all S ranks before adding, so each
+            // row costs one distributed-shared-memory round trip
             const int rank = (int)cluster_rank();
-            const int S = p.splits;
+            const int S = p.splits;  // at most kMaxClusterSplits
             const int c4 = (threadIdx.x & 31) * 4;
             const int ph = threadIdx.x >> 5;
             const int n_out = n0 + c4;
             __nv_bfloat16* y = static_cast<__nv_bfloat16*>(set_y);
             const bool vec_ok = (p.N % 4 == 0) && (n_out + 3 < p.N);
-            for (int m0 = rank + S * ph; m0 < rows; m0 += S * kDequantWarps * 4) {
-                float4 acc[4];
+            for (int m = rank + S * ph; m < rows; m += S * kDequantWarps) {
+                float4 v[kMaxClusterSplits];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int z0 = 0; z0 < S; z0 += 2) {
-                    float4 v[4][2];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int m = m0 + u * S * kDequantWarps;
-#pragma unroll
-                        for (int dz = 0; dz < 2; ++dz) {
-                            v[u][dz] = make_float4(0.f, 0.f, 0.f, 0.f);
-                            if (z0 + dz < S && m < rows)
-                                v[u][dz] = ld_cluster_f32x4(
-                                    map_cluster(smem_base + (m * kTileN + c4) * 4, (uint32_t)(z0 + dz)));
-                        }
-                    }
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-#pragma unroll
-                        for (int dz = 0; dz < 2; ++dz) {  // rank order: z0, then z0 + 1
-                            acc[u].x += v[u][dz].x;
-                            acc[u].y += v[u][dz].y;
-                            acc[u].z += v[u][dz].z;
-                            acc[u].w += v[u][dz].w;
-                        }
+                for (int z = 0; z < kMaxClusterSplits; ++z) {
+                    v[z] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (z < S)
+                        v[z] = ld_cluster_f32x4(map_cluster(smem_base + (m * kTileN + c4) * 4, (uint32_t)z));
                 }
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int m = m0 + u * S * kDequantWarps;
-                    if (!ok || m >= rows) continue;
-                    __nv_bfloat16* yr = y + (long long)(row_start + m) * p.N;
-                    if (vec_ok) {
-                        uint2 pk;
-                        pk.x = cvt_bf16x2(acc[u].x, acc[u].y);
-                        pk.y = cvt_bf16x2(acc[u].z, acc[u].w);
-                        *reinterpret_cast<uint2*>(yr + n_out) = pk;
-                    } else {
-                        const float a4[4] = {acc[u].x, acc[u].y, acc[u].z, acc[u].w};
-                        for (int j = 0; j < 4; ++j)
-                            if (n_out + j < p.N) yr[n_out + j] = __float2bfloat16_rn(a4[j]);
+                for (int z = 0; z < kMaxClusterSplits; ++z) {  // rank order
+                    if (z < S) {
+                        acc.x += v[z].x;
+                        acc.y += v[z].y;
+                        acc.z += v[z].z;
+                        acc.w += v[z].w;
                     }
+                }
+                if (!ok) continue;
+                __nv_bfloat16* yr = y + (long long)(row_start + m) * p.N;
+                if (vec_ok) {
+                    uint2 pk;
+                    pk.x = cvt_bf16x2(acc.x, acc.y);
+                    pk.y = cvt_bf16x2(acc.z, acc.w);
+                    *reinterpret_cast<uint2*>(yr + n_out) = pk;
+                } else {
+                    const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+                    for (int j = 0; j < 4; ++j)
+                        if (n_out + j < p.N) yr[n_out + j] = __float2bfloat16_rn(a4[j]);
                 }
             }
         }
