@@ -61,6 +61,7 @@ constexpr int kAStages = 4;
 constexpr int kMaxCodeStages = 8;
 constexpr int kMaxXStages = 8;
 constexpr int kSmemBudget = 224 * 1024;
+constexpr int kMaxClusterSplits = 8; // K splits per tile: the portable cluster size
 
 struct KnLayout {
     int x_bytes, x_stages;   // activation ring at 0 (one 64-wide atom column per slot)
@@ -484,23 +485,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         // every thread of every CTA of the cluster takes part in both barriers
         cluster_sync();
         if (warp < kDequantWarps) {
-            // rank z sums rows m = z, z + S, ... over all ranks in rank order
+            // rank z sums rows m = z, z + S, ... over all ranks in rank order;
+            // a thread loads all S ranks' partials of its 4 columns before
+            // adding them, one remote round trip per row
             const int rank = (int)cluster_rank();
-            const int S = p.splits;
+            const int S = p.splits;  // at most kMaxClusterSplits
             const int c4 = (threadIdx.x & 31) * 4;
             const int ph = threadIdx.x >> 5;
             const int n_out = n0 + c4;
             __nv_bfloat16* y = static_cast<__nv_bfloat16*>(p.y);
             const bool vec_ok = n_out + 3 < p.N;  // N % 64 == 0: four columns stay together
             for (int m = rank + S * ph; m < rows; m += S * kDequantWarps) {
+                float4 v[kMaxClusterSplits];
+#pragma unroll
+                for (int z = 0; z < kMaxClusterSplits; ++z) {
+                    v[z] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (z < S)
+                        v[z] = ld_cluster_f32x4(map_cluster(smem_base + (m * kTileN + c4) * 4, (uint32_t)z));
+                }
                 float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int z = 0; z < S; ++z) {
-                    const float4 v =
-                        ld_cluster_f32x4(map_cluster(smem_base + (m * kTileN + c4) * 4, (uint32_t)z));
-                    acc.x += v.x;
-                    acc.y += v.y;
-                    acc.z += v.z;
-                    acc.w += v.w;
+#pragma unroll
+                for (int z = 0; z < kMaxClusterSplits; ++z) {  // rank order
+                    if (z < S) {
+                        acc.x += v[z].x;
+                        acc.y += v[z].y;
+                        acc.z += v[z].z;
+                        acc.w += v[z].w;
+                    }
                 }
                 if (ok && vec_ok) {
                     uint2 pk;
